@@ -1,0 +1,326 @@
+/*
+ * moe.h — C ABI of libmoe: the routed-expert MoE FFN layer at decode and
+ * small-batch time (and its prefill grouped-GEMM path) on one GB300 (sm_103a).
+ *
+ * The layer: a router GEMV, top-k expert selection with a softmax over the
+ * selected experts, block-quantised gate/up/down matvecs over the selected
+ * experts only, SwiGLU, and a router-weighted combine.  Expert weights are
+ * served from slot pools in device memory, one pool per type/shape group of
+ * layers, managed least-recently-used, with misses uploaded from pinned host
+ * memory on a side stream.
+ *
+ * Sources for the operations (web pages on llama.cpp MoE expert handling):
+ *  - page 1, "llama.cpp MoE 模型卸载" blog, section 3.1 (gating: logits,
+ *    softmax, partial_sort top-k), 3.2 (load on demand, LRU of non-active
+ *    experts), 3.3 (device-side expert pointers for the FFN kernel);
+ *  - page 2, "llama.cpp MoE GGUF 张量加载" notes (ffn_{gate,up,down}_exps
+ *    expert-major tensors);
+ *  - page 3, tiered MoE scheduling note (routed vs always-resident shared
+ *    experts, pinned memory and async H2D copies);
+ *  - page 4, "llama.cpp MoE缓存实测" (slot pools grouped by tensor type and
+ *    shape, LRU shared across a group's layers, PCIe upload on miss, the
+ *    <=32-token batch limit, the slot budget and its floor, hit statistics);
+ *  - page 5, "GPU 卸载研究笔记" section 1.2 (quantised blocks kept as-is and
+ *    multiplied by an on-GPU quantised GEMV).
+ *
+ * Conventions for every entry point:
+ *  - Return value: a moe_status code (0 = MOE_OK).  Nothing aborts the process.
+ *  - Pointers named d_* / "device" are device addresses; "host" pointers are
+ *    host addresses.  Every buffer is owned by the caller; the library never
+ *    frees caller memory and never allocates device memory the caller sees
+ *    (library-owned objects — moe_cache, moe_stack — hold only host memory and
+ *    CUDA events).
+ *  - Calls taking a stream are asynchronous on that stream unless noted;
+ *    argument errors are detected on the host before anything is enqueued.
+ *  - Device-side faults that can only be seen on the GPU (an expert id or a
+ *    slot out of range, a bounded wait that ran out) are recorded in a
+ *    per-device status word read by moe_device_status(); the offending work is
+ *    skipped, never trapped.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *moe_stream_t; /* the same type as cudaStream_t */
+
+/* ------------------------------------------------------------------ status */
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID = -1,     /* bad argument (null, shape, range, alignment, not pinned) */
+    MOE_ERR_CUDA = -2,        /* a CUDA runtime call failed */
+    MOE_ERR_CAPACITY = -3,    /* more distinct experts requested than the pool has slots */
+    MOE_ERR_BUDGET = -4,      /* a pool too small for one request (page 4's budget floor) */
+    MOE_ERR_TIMEOUT = -5,     /* a bounded device-side wait ran out */
+    MOE_ERR_UNSUPPORTED = -6  /* a shape/type combination this build has no kernel for */
+};
+
+/* Static message for a status code; never NULL. */
+const char *moe_status_string(int status);
+
+/* Library limits. */
+#define MOE_MAX_K 8          /* top-k limit (k <= 8 covers every workload) */
+#define MOE_MAX_E 256        /* experts per layer */
+#define MOE_DECODE_MAX_T 32  /* page 4: the slot cache serves batches of <= 32 tokens */
+
+/* Quantisation formats of expert weights (canonical block layouts). */
+enum moe_qtype {
+    MOE_Q8_0 = 0,  /* 34 B per 32 weights: fp16 d (little-endian), int8 q[32]; w = d*q */
+    MOE_Q4_SM = 1  /* 20 B per 32 weights: fp16 d, fp16 m, 16 B codes (byte i: q[2i] low
+                      nibble, q[2i+1] high nibble); w = d*q + m */
+};
+/* Activation element types. */
+enum moe_xtype { MOE_F32 = 0, MOE_BF16 = 1 };
+
+/* --------------------------------------------------------------- router (a1, a2) */
+
+/*
+ * moe_router_topk — gating for T tokens (page 1, section 3.1).
+ *   logits[t][e] = sum_h x[t][h] * w_router[h][e] + bias[e]   (fp32 accumulation)
+ *   ids[t][:]     = the k experts with the largest logits, in descending logit order,
+ *                   equal logits ordered by ascending expert id
+ *   weights[t][j] = exp(l_j - l_max) / sum_{i in top-k} exp(l_i - l_max)
+ * x        device [T][H], fp32 (xtype MOE_F32) or bf16 (MOE_BF16), row-major.
+ * w_router device [H][E] fp16 bit patterns, row-major (E contiguous).
+ * bias     device [E] fp32 or NULL.
+ * ids      device [T][k] int32 out;  weights device [T][k] fp32 out.
+ * logits   device [T][E] fp32 out, or NULL.
+ * Limits: 1 <= k <= min(E, MOE_MAX_K), E <= MOE_MAX_E, H % 32 == 0, T >= 0 (T == 0: no-op).
+ */
+int moe_router_topk(const void *x, int xtype, int T, int H, const uint16_t *w_router,
+                    const float *bias, int E, int k, int32_t *ids, float *weights,
+                    float *logits, moe_stream_t s);
+
+/* ------------------------------------------------------------------ slot images */
+
+/*
+ * moe_slot_image_bytes — size of one expert's slot image (gate + up + down).
+ * It equals the canonical size: 2*F*H/32*B + H*F/32*B with B = 34 (q8_0) or 20 (4-bit).
+ * H and F must be multiples of 32.
+ */
+int moe_slot_image_bytes(int qtype, int H, int F, size_t *bytes_out);
+
+/*
+ * moe_pack_expert — host: canonical expert tensors -> one slot image.
+ * gate_aos, up_aos: host [F rows][H/32 blocks] canonical blocks; down_aos: [H][F/32].
+ * slot_image_dst: host buffer of moe_slot_image_bytes() bytes (16-byte aligned);
+ * pass NULL to query the size only.  The image regroups each matrix into tiles of
+ * 32 rows so that one warp's 16-byte loads are contiguous, and keeps the block
+ * scales in a separate region; no value is changed (the bytes are a permutation).
+ */
+int moe_pack_expert(int qtype, int H, int F, const void *gate_aos, const void *up_aos,
+                    const void *down_aos, void *slot_image_dst, size_t *slot_bytes_out);
+
+/* moe_unpack_expert — host: slot image -> canonical tensors (the inverse of pack). */
+int moe_unpack_expert(int qtype, int H, int F, const void *slot_image, void *gate_aos,
+                      void *up_aos, void *down_aos);
+
+/* ------------------------------------------------------------ slot pool (a3) */
+
+/*
+ * One expert slot pool for a type/shape group of layers (page 4: groups by tensor
+ * type and shape; one VRAM pool per group; LRU shared across the group's layers).
+ */
+typedef struct {
+    int qtype, H, F;
+    int n_layers;                     /* layers of this group */
+    int n_experts;                    /* routed experts per layer (E) */
+    int first_layer;                  /* global index of the group's first layer */
+    int n_slots;                      /* slots in the pool */
+    size_t slot_bytes;                /* per-slot stride in the pool, >= image bytes, %256 == 0 */
+    void *device_pool;                /* device, n_slots * slot_bytes, caller-owned */
+    const void *const *host_images;   /* host array [n_layers * n_experts] of pinned slot
+                                         images (moe_pack_expert output), layer-major */
+    moe_stream_t copy_stream;         /* stream for miss uploads (caller-owned) */
+} moe_cache_desc;
+
+typedef struct moe_cache moe_cache; /* opaque, library-owned host object */
+
+typedef struct {
+    uint64_t queries[2];      /* distinct (layer, expert) lookups; [0]: ubatch <= 8 tokens, [1]: 9..32 */
+    uint64_t hits[2];
+    uint64_t misses[2];
+    uint64_t evictions;
+    uint64_t h2d_bytes;       /* bytes uploaded for misses */
+    uint64_t route_queries;   /* per-route (token, expert) lookups */
+    uint64_t route_hits;
+    uint64_t ensure_calls;
+} moe_cache_stats;
+
+/*
+ * moe_cache_create — validates the descriptor (every host image must be pinned:
+ * MOE_ERR_INVALID otherwise; n_slots must be >= 1) and creates an empty pool.
+ */
+int moe_cache_create(const moe_cache_desc *desc, moe_cache **out);
+
+/*
+ * moe_cache_ensure — make the experts of one request resident (host call).
+ * ids_host [n_tokens][k] are one layer's routed expert ids.  For the distinct ids,
+ * taken in ascending order: hits first (stamped most-recent), then misses, each
+ * taking the lowest free slot, else evicting the least-recently-used slot whose
+ * expert is not in this request (page 1 section 3.2; page 4).  Each miss is an
+ * async cudaMemcpyAsync of the pinned image into its slot on desc.copy_stream,
+ * issued after the slot's last reader (see moe_cache_release) has finished.
+ * Outputs: slots_host_out [n_tokens*k] (the slot of each input id), *n_miss_out,
+ * miss_mask_host_out (optional, [n_experts] bytes: 1 for experts uploaded by this
+ * call, 0 otherwise), and the layer's device expert->slot table d_slot_table
+ * [n_experts] (-1 for non-resident experts), written on stream s.
+ * Errors: MOE_ERR_CAPACITY when distinct ids > n_slots (nothing changes);
+ * MOE_ERR_INVALID for a layer outside the group or an id outside [0, E);
+ * MOE_ERR_CUDA if an upload could not be issued (the slot being filled is left
+ * empty and the pool stays consistent).
+ */
+int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host, int n_tokens, int k,
+                     int32_t *slots_host_out, int *n_miss_out, uint8_t *miss_mask_host_out,
+                     int32_t *d_slot_table, moe_stream_t s);
+
+/* moe_cache_wait_uploads — stream s waits for the uploads issued by the last ensure. */
+int moe_cache_wait_uploads(moe_cache *c, moe_stream_t s);
+
+/*
+ * moe_cache_release — records, on stream s, the point after which the slots of the
+ * last ensure are no longer read; later uploads into those slots wait for it.
+ * Call it after enqueueing the kernels that read the slots.
+ */
+int moe_cache_release(moe_cache *c, moe_stream_t s);
+
+int moe_cache_stats_get(const moe_cache *c, moe_cache_stats *out);
+/* Clears the pool (all slots empty), the clock and the statistics. Host only. */
+int moe_cache_reset(moe_cache *c);
+void moe_cache_destroy(moe_cache *c);
+/* Slot of (layer, expert) or -1 (host query; for tests). */
+int moe_cache_lookup(const moe_cache *c, int layer, int expert);
+
+/*
+ * moe_slots_for_budget — slot count per group from a byte budget (page 4, section
+ * "配置之前，先算清楚你的专家有多大": budget / per-expert bytes, shared by the groups'
+ * layers).  Every group gets n = floor(budget / sum_g per_expert_bytes[g]) slots.
+ * A group with fewer than k+1 slots is under budget; if every group is, returns
+ * MOE_ERR_BUDGET (page 4: the server refuses to start).
+ */
+int moe_slots_for_budget(size_t budget_bytes, const size_t *per_expert_bytes, int n_groups,
+                         int k, int *slots_out);
+
+/* ------------------------------------------------------ expert FFN (a4..a7, a9) */
+
+/*
+ * moe_expert_ffn — the routed experts' SwiGLU FFNs for T tokens, weighted.
+ *   for each route (t, j) with e = ids[t][j] (restricted to expert_subset if given):
+ *     h = silu(Wg_e x_t) * (Wu_e x_t),   partial[t][j][:] = weights[t][j] * (Wd_e h)
+ * Routes of experts outside the subset leave partial[t][j] untouched.
+ * x            device [T][H] fp32 or bf16.
+ * ids, weights device [T][k] (as produced by moe_router_topk).
+ * d_slot_table device [E] int32: expert -> slot in pool (or NULL: slot = expert).
+ * pool         device slot images (moe_pack_expert layout), slot s at pool + s*slot_bytes;
+ *              pool and slot_bytes must be 16-byte aligned.
+ * expert_subset device int32 list of experts to process, or NULL for all.
+ * partial      device [T][k][H] fp32 out.
+ * workspace    device scratch of moe_expert_ffn_workspace() bytes (256-byte aligned).
+ * Path: T <= MOE_DECODE_MAX_T uses the dequantising GEMV kernels; larger T uses the
+ * prefill grouped GEMM (tcgen05) when available for the format, else the GEMV kernels.
+ */
+int moe_expert_ffn(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
+                   const int32_t *ids, const float *weights, const int32_t *d_slot_table,
+                   int n_slots, const void *pool, size_t slot_bytes,
+                   const int32_t *expert_subset, int n_subset, float *partial,
+                   void *workspace, size_t ws_bytes, moe_stream_t s);
+
+int moe_expert_ffn_workspace(int T, int H, int F, int qtype, int E, int k, size_t *bytes);
+
+/* ---------------------------------------------------------------- combine (a8) */
+
+/*
+ * moe_combine — y[t][:] = extra[t][:] + sum_{j=0..k-1} partial[t][j][:], summed in the
+ * fixed order j = 0..k-1 after extra.  extra (device [T][H] fp32) may be NULL; it
+ * carries the residual stream and/or the shared experts' output.  y may alias extra.
+ */
+int moe_combine(const float *partial, int T, int k, int H, const float *extra, float *y,
+                moe_stream_t s);
+
+/* ------------------------------------------------------------ device status */
+
+/*
+ * moe_device_status — synchronous: reads (and if clear != 0 resets) the current
+ * device's status word: MOE_OK, MOE_ERR_INVALID (an id/slot out of range met on
+ * the device) or MOE_ERR_TIMEOUT (a bounded wait ran out).  Waits for the device.
+ */
+int moe_device_status(int *status_out, int clear);
+
+/* ------------------------------------------------------- decode-step runtime */
+
+/*
+ * A stack of MoE layers with the residual h_{l+1} = h_l + MoE_l(h_l), driven
+ * layer by layer on the host: router -> ids to host -> slot-pool ensure ->
+ * FFN over hit experts while misses upload -> FFN over missed experts -> combine.
+ */
+typedef struct {
+    int qtype, H, F, E, k, n_layers, n_shared;
+    const uint16_t *const *w_router;  /* host array [n_layers] of device [H][E] fp16 */
+    const float *const *bias;         /* host array [n_layers] of device [E] fp32, or NULL */
+    int n_groups;                     /* slot pools; 0 = every expert resident */
+    moe_cache *const *caches;         /* [n_groups]; group g covers its desc's layers */
+    const void *resident_pool;        /* n_groups == 0: slot (layer*E + e) images */
+    const void *shared_pool;          /* n_shared > 0: slot (layer*n_shared + s) images */
+    size_t slot_bytes;                /* slot stride of resident_pool / shared_pool */
+    int max_T;                        /* largest ubatch (<= MOE_DECODE_MAX_T) */
+    void *workspace;                  /* device, moe_stack_workspace() bytes */
+    size_t ws_bytes;
+    int overlap;                      /* 1: hit experts run while misses upload */
+    int profile;                      /* 0: off; 1: events around the gate/up GEMV only;
+                                         2: events around every kernel (moe_stack_profile) */
+} moe_stack_desc;
+
+typedef struct moe_stack moe_stack;
+
+typedef struct {
+    uint64_t steps, layers;
+    double router_ms, permute_ms, gateup_ms, down_ms, combine_ms; /* summed event times */
+    uint64_t gateup_launches, down_launches;
+    double gateup_bytes, down_bytes;    /* algorithmic expert bytes streamed */
+    double host_wait_ms;                /* host time blocked on the ids readback */
+    uint64_t kernel_launches;           /* libmoe kernels launched (counted with or without profile) */
+    uint64_t h2d_copies;                /* miss uploads issued */
+} moe_stack_profile;
+
+int moe_stack_workspace(int H, int F, int qtype, int E, int k, int max_T, int n_shared,
+                        size_t *bytes);
+int moe_stack_create(const moe_stack_desc *desc, moe_stack **out);
+/*
+ * moe_stack_decode — one decode step of T tokens through every layer.
+ * x_in, y_out: device [T][H] fp32 (may alias).  Host-synchronising once per layer
+ * (the routed ids are needed on the host by the slot pools); all kernels run on s.
+ * ids_host_out / weights_host_out (optional, host [n_layers][T][k]) receive the routing.
+ */
+int moe_stack_decode(moe_stack *st, const float *x_in, float *y_out, int T,
+                     int32_t *ids_host_out, float *weights_host_out, moe_stream_t s);
+/* moe_stack_layer — one layer only: y = x + MoE_layer(x) (same semantics as decode). */
+int moe_stack_layer(moe_stack *st, int layer, const float *x_in, float *y_out, int T,
+                    int32_t *ids_host_out, float *weights_host_out, moe_stream_t s);
+/* Synchronises the stream of the last call and returns the accumulated profile. */
+int moe_stack_profile_get(moe_stack *st, moe_stack_profile *out);
+int moe_stack_profile_reset(moe_stack *st);
+/* Sets the profiling level (0, 1, 2 as in moe_stack_desc.profile) for later calls. */
+int moe_stack_set_profile(moe_stack *st, int level);
+void moe_stack_destroy(moe_stack *st);
+
+/* ------------------------------------------------------------------ test hooks */
+
+/*
+ * moe_debug_inject_fault — host-side fault injection for tests: kind 1 makes the
+ * n-th following miss upload (n = countdown, 0 = the next) fail as if the copy
+ * could not be issued; kind 0 disarms.  Never touches the GPU.
+ */
+int moe_debug_inject_fault(int kind, int countdown);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,108 @@
+// Internal helpers shared by libmoe's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+#define MOE_TRY_CUDA(expr)                                   \
+    do {                                                     \
+        cudaError_t moe_err__ = (expr);                      \
+        if (moe_err__ != cudaSuccess) return MOE_ERR_CUDA;   \
+    } while (0)
+
+#define MOE_CHECK(cond)                                      \
+    do {                                                     \
+        if (!(cond)) return MOE_ERR_INVALID;                 \
+    } while (0)
+
+static inline cudaStream_t moe_cuda_stream(moe_stream_t s) { return (cudaStream_t)s; }
+
+// ------------------------------------------------------------------ slot image layout
+//
+// A matrix of R rows (output features) by K columns (reduction) is stored as
+//   [quant region][scale region]
+// Rows are grouped in tiles of 32 (one row per lane of a warp).  The quant region
+// holds, for row tile g and column piece p, 32 consecutive 16-byte pieces (lane 0..31),
+// so a warp's 16-byte loads of one piece are one contiguous 512-byte run and a whole
+// row tile is contiguous along K.  A piece is 16 int8 codes (q8_0) or one 32-code
+// block (4-bit; the block's 16 code bytes in canonical order).  The scale region holds
+// per (row tile g, block b) 32 consecutive per-lane entries: fp16 d (q8_0) or
+// fp16 d, fp16 m (4-bit).  An expert image is gate [F][H], up [F][H], down [H][F].
+
+#define MOE_TILE_ROWS 32
+
+__host__ __device__ static inline int moe_piece_cols(int qtype) { return qtype == MOE_Q8_0 ? 16 : 32; }
+__host__ __device__ static inline int moe_scale_entry_bytes(int qtype) { return qtype == MOE_Q8_0 ? 2 : 4; }
+__host__ __device__ static inline int moe_block_bytes(int qtype) { return qtype == MOE_Q8_0 ? 34 : 20; }
+
+__host__ __device__ static inline size_t moe_quant_bytes(int qtype, int R, int K) {
+    return qtype == MOE_Q8_0 ? (size_t)R * K : (size_t)R * K / 2;
+}
+__host__ __device__ static inline size_t moe_scale_bytes(int qtype, int R, int K) {
+    return (size_t)R * (K / 32) * moe_scale_entry_bytes(qtype);
+}
+__host__ __device__ static inline size_t moe_matrix_bytes(int qtype, int R, int K) {
+    return moe_quant_bytes(qtype, R, K) + moe_scale_bytes(qtype, R, K);
+}
+// byte offset of (row tile g, piece p) in the quant region (lane 0's piece)
+__host__ __device__ static inline size_t moe_piece_offset(int qtype, int K, int g, int p) {
+    int P = K / moe_piece_cols(qtype);
+    return ((size_t)g * P + p) * (MOE_TILE_ROWS * 16);
+}
+// byte offset of (row tile g, block b) in the scale region (lane 0's entry)
+__host__ __device__ static inline size_t moe_scale_offset(int qtype, int K, int g, int b) {
+    int NB = K / 32;
+    return ((size_t)g * NB + b) * (MOE_TILE_ROWS * moe_scale_entry_bytes(qtype));
+}
+__host__ __device__ static inline size_t moe_expert_image_bytes(int qtype, int H, int F) {
+    return 2 * moe_matrix_bytes(qtype, F, H) + moe_matrix_bytes(qtype, H, F);
+}
+// matrix m of an expert image: 0 gate, 1 up, 2 down
+__host__ __device__ static inline size_t moe_expert_matrix_offset(int qtype, int H, int F, int m) {
+    return (size_t)m * moe_matrix_bytes(qtype, F, H);
+}
+
+// ------------------------------------------------------------------ device status word
+
+// Address of the current device's status word (see moe_device_status).
+int *moe_status_word_device_ptr();
+
+#define MOE_DEV_STATUS_OK 0
+
+#ifdef __CUDACC__
+__device__ static inline void moe_set_status(int *status_word, int code) {
+    if (status_word) atomicCAS(status_word, 0, code);
+}
+#endif
+
+// Host-side fault injection (tests): returns true if this miss upload must fail.
+bool moe_fault_take_upload();
+
+// ------------------------------------------------------------------ decode FFN internals
+
+struct moe_ffn_timing {
+    // optional event pairs recorded around the kernels of one moe_expert_ffn call
+    // (a null event is not recorded)
+    cudaEvent_t permute0, permute1, gateup0, gateup1, down0, down1;
+};
+
+int moe_expert_ffn_impl(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
+                        const int32_t *ids, const float *weights, const int32_t *d_slot_table,
+                        int n_slots, const void *pool, size_t slot_bytes,
+                        const int32_t *expert_subset, int n_subset, float *partial,
+                        void *workspace, size_t ws_bytes, cudaStream_t s,
+                        const moe_ffn_timing *timing);
+
+// Writes up to three small int32 arrays (<= 256 values each) on stream s with one launch
+// (values travel as kernel parameters, so no host staging buffer outlives the call).
+int moe_write_ints(int32_t *const dst[3], const int n[3], const int32_t *const src[3], cudaStream_t s);
+
+// Pool base and slot count of a cache; the layer range of its group.
+const void *moe_cache_pool(const moe_cache *c, int *n_slots);
+int moe_cache_layer_range(const moe_cache *c, int *first_layer, int *n_layers);
+
+size_t moe_decode_workspace_bytes(int T, int H, int F, int qtype, int E, int k);
+int moe_gateup_ksplit(int qtype, int H);

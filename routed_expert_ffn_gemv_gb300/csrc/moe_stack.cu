@@ -1,0 +1,413 @@
+// Decode-step runtime: a stack of MoE layers with a residual, h_{l+1} = h_l + MoE_l(h_l).
+//
+// Per layer (page 4's cache flow, page 1 section 3): router -> routed ids to the host ->
+// slot-pool ensure (misses start uploading on the copy stream) -> FFN over the experts
+// that were already resident while the misses upload -> wait for the uploads -> FFN over
+// the missed experts -> release the slots -> combine with the residual (and the shared
+// experts, page 3: always-resident experts outside the pool).
+#include <chrono>
+#include <vector>
+
+#include "moe_common.cuh"
+
+namespace {
+
+inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct StackWs {
+    size_t ids, w, partial, table, hit, miss, hA, hB, ids_s, w_s, partial_s, tmp, ffn, total;
+    size_t ffn_bytes;
+};
+
+StackWs stack_ws(int H, int F, int qtype, int E, int k, int T, int n_shared) {
+    StackWs L;
+    size_t off = 0;
+    L.ids = off;       off = align256(off + (size_t)T * k * 4);
+    L.w = off;         off = align256(off + (size_t)T * k * 4);
+    L.partial = off;   off = align256(off + (size_t)T * k * H * 4);
+    L.table = off;     off = align256(off + (size_t)E * 4);
+    L.hit = off;       off = align256(off + (size_t)E * 4);
+    L.miss = off;      off = align256(off + (size_t)E * 4);
+    L.hA = off;        off = align256(off + (size_t)T * H * 4);
+    L.hB = off;        off = align256(off + (size_t)T * H * 4);
+    const int ns = n_shared > 0 ? n_shared : 0;
+    L.ids_s = off;     off = align256(off + (size_t)T * ns * 4);
+    L.w_s = off;       off = align256(off + (size_t)T * ns * 4);
+    L.partial_s = off; off = align256(off + (size_t)T * ns * H * 4);
+    L.tmp = off;       off = align256(off + (size_t)T * H * 4);
+    size_t f = moe_decode_workspace_bytes(T, H, F, qtype, E, k);
+    if (ns > 0) {
+        const size_t f2 = moe_decode_workspace_bytes(T, H, F, qtype, ns, ns);
+        if (f2 > f) f = f2;
+    }
+    L.ffn = off;       off = align256(off + f);
+    L.ffn_bytes = f;
+    L.total = off;
+    return L;
+}
+
+struct EventPair {
+    cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct moe_stack {
+    moe_stack_desc d{};
+    StackWs L{};
+    std::vector<const uint16_t *> w_router;
+    std::vector<const float *> bias;
+    std::vector<moe_cache *> caches;
+    std::vector<int> group_of_layer;   // -1: resident
+    std::vector<int> group_first, group_n;
+    int32_t *ids_h = nullptr;          // pinned [max_T * k]
+    int32_t *slots_h = nullptr;
+    cudaEvent_t ids_ready = nullptr;
+    cudaStream_t last_stream = nullptr;
+    // profiling
+    std::vector<cudaEvent_t> ev_pool;
+    size_t ev_used = 0;
+    std::vector<std::pair<int, EventPair>> timed;  // (kind, events)
+    moe_stack_profile prof{};
+    char *ws = nullptr;
+};
+
+namespace {
+
+enum { K_ROUTER = 0, K_PERMUTE, K_GATEUP, K_DOWN, K_COMBINE };
+
+int get_event(moe_stack *st, cudaEvent_t *out) {
+    if (st->ev_used == st->ev_pool.size()) {
+        cudaEvent_t e;
+        MOE_TRY_CUDA(cudaEventCreate(&e));
+        st->ev_pool.push_back(e);
+    }
+    *out = st->ev_pool[st->ev_used++];
+    return MOE_OK;
+}
+
+// Accumulates the elapsed times of recorded event pairs (all complete) and recycles them.
+int harvest(moe_stack *st) {
+    for (auto &te : st->timed) {
+        float ms = 0.f;
+        MOE_TRY_CUDA(cudaEventElapsedTime(&ms, te.second.a, te.second.b));
+        switch (te.first) {
+            case K_ROUTER: st->prof.router_ms += ms; break;
+            case K_PERMUTE: st->prof.permute_ms += ms; break;
+            case K_GATEUP: st->prof.gateup_ms += ms; break;
+            case K_DOWN: st->prof.down_ms += ms; break;
+            default: st->prof.combine_ms += ms; break;
+        }
+    }
+    st->timed.clear();
+    st->ev_used = 0;
+    return MOE_OK;
+}
+
+int begin_timed(moe_stack *st, cudaStream_t s, EventPair *ep) {
+    if (st->d.profile < 2) return MOE_OK;
+    int rc = get_event(st, &ep->a);
+    if (rc) return rc;
+    rc = get_event(st, &ep->b);
+    if (rc) return rc;
+    MOE_TRY_CUDA(cudaEventRecord(ep->a, s));
+    return MOE_OK;
+}
+
+int end_timed(moe_stack *st, cudaStream_t s, int kind, EventPair ep) {
+    if (st->d.profile < 2) return MOE_OK;
+    MOE_TRY_CUDA(cudaEventRecord(ep.b, s));
+    st->timed.push_back({kind, ep});
+    return MOE_OK;
+}
+
+// One FFN call with per-kernel timing when profiling.
+int ffn_call(moe_stack *st, const float *x, int T, int E, int k, const int32_t *ids, const float *w,
+             const int32_t *table, int n_slots, const void *pool, const int32_t *subset, int n_subset,
+             float *partial, int n_active, cudaStream_t s) {
+    const moe_stack_desc &d = st->d;
+    moe_ffn_timing tm{};
+    const moe_ffn_timing *tp = nullptr;
+    if (d.profile >= 1) {
+        int rc;
+        if ((rc = get_event(st, &tm.gateup0)) || (rc = get_event(st, &tm.gateup1))) return rc;
+        if (d.profile >= 2)
+            if ((rc = get_event(st, &tm.permute0)) || (rc = get_event(st, &tm.permute1)) ||
+                (rc = get_event(st, &tm.down0)) || (rc = get_event(st, &tm.down1)))
+                return rc;
+        tp = &tm;
+    }
+    const int rc = moe_expert_ffn_impl(x, MOE_F32, T, d.H, d.F, d.qtype, E, k, ids, w, table, n_slots,
+                                       pool, d.slot_bytes, subset, n_subset, partial,
+                                       st->ws + st->L.ffn, st->L.ffn_bytes, s, tp);
+    if (rc) return rc;
+    st->prof.kernel_launches += 3;
+    if (d.profile >= 1) {
+        st->timed.push_back({K_GATEUP, {tm.gateup0, tm.gateup1}});
+        if (d.profile >= 2) {
+            st->timed.push_back({K_PERMUTE, {tm.permute0, tm.permute1}});
+            st->timed.push_back({K_DOWN, {tm.down0, tm.down1}});
+        }
+        st->prof.gateup_launches++;
+        st->prof.down_launches++;
+        st->prof.gateup_bytes += (double)n_active * 2 * moe_matrix_bytes(d.qtype, d.F, d.H);
+        st->prof.down_bytes += (double)n_active * moe_matrix_bytes(d.qtype, d.H, d.F);
+    }
+    return MOE_OK;
+}
+
+int layer_step(moe_stack *st, int layer, const float *x, float *y, int T, int32_t *ids_out,
+               float *w_out, cudaStream_t s) {
+    const moe_stack_desc &d = st->d;
+    const StackWs &L = st->L;
+    int32_t *ids_d = (int32_t *)(st->ws + L.ids);
+    float *w_d = (float *)(st->ws + L.w);
+    float *partial = (float *)(st->ws + L.partial);
+    int32_t *table = (int32_t *)(st->ws + L.table);
+    int32_t *hit_d = (int32_t *)(st->ws + L.hit);
+    int32_t *miss_d = (int32_t *)(st->ws + L.miss);
+    int rc;
+    EventPair ep{};
+
+    if ((rc = begin_timed(st, s, &ep))) return rc;
+    if ((rc = moe_router_topk(x, MOE_F32, T, d.H, st->w_router[layer], st->bias[layer], d.E, d.k,
+                              ids_d, w_d, nullptr, (moe_stream_t)s)))
+        return rc;
+    st->prof.kernel_launches += 1;
+    if ((rc = end_timed(st, s, K_ROUTER, ep))) return rc;
+
+    const int g = st->group_of_layer[layer];
+    if (g >= 0) {
+        moe_cache *c = st->caches[g];
+        MOE_TRY_CUDA(cudaMemcpyAsync(st->ids_h, ids_d, (size_t)T * d.k * 4, cudaMemcpyDeviceToHost, s));
+        MOE_TRY_CUDA(cudaEventRecord(st->ids_ready, s));
+        const auto w0 = std::chrono::steady_clock::now();
+        MOE_TRY_CUDA(cudaEventSynchronize(st->ids_ready));
+        st->prof.host_wait_ms +=
+            std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - w0).count();
+        if (d.profile && (rc = harvest(st))) return rc;  // everything recorded so far has completed
+        int n_miss = 0;
+        uint8_t miss_mask[MOE_MAX_E];
+        if ((rc = moe_cache_ensure(c, layer, st->ids_h, T, d.k, st->slots_h, &n_miss, miss_mask,
+                                   nullptr, (moe_stream_t)s)))
+            return rc;
+        bool want[MOE_MAX_E] = {false};
+        for (int i = 0; i < T * d.k; ++i) want[st->ids_h[i]] = true;
+        int32_t hits[MOE_MAX_E], misses[MOE_MAX_E], tbl[MOE_MAX_E];
+        int nh = 0, nm = 0;
+        for (int e = 0; e < d.E; ++e) {
+            tbl[e] = moe_cache_lookup(c, layer, e);
+            if (!want[e]) continue;
+            if (miss_mask[e]) misses[nm++] = e;
+            else hits[nh++] = e;
+        }
+        const bool two_phase = d.overlap && nh > 0 && nm > 0;
+        {
+            int32_t *dst[3] = {table, hit_d, miss_d};
+            const int n[3] = {d.E, two_phase ? nh : 0, two_phase ? nm : 0};
+            const int32_t *src[3] = {tbl, hits, misses};
+            if ((rc = moe_write_ints(dst, n, src, s))) return rc;
+            st->prof.kernel_launches += 1;
+            st->prof.h2d_copies += n_miss;
+        }
+        {
+            int ns = 0;
+            const void *pool = moe_cache_pool(c, &ns);
+            if (two_phase) {
+                if ((rc = ffn_call(st, x, T, d.E, d.k, ids_d, w_d, table, ns, pool, hit_d, nh, partial, nh, s)))
+                    return rc;
+                if ((rc = moe_cache_wait_uploads(c, (moe_stream_t)s))) return rc;
+                if ((rc = ffn_call(st, x, T, d.E, d.k, ids_d, w_d, table, ns, pool, miss_d, nm, partial, nm, s)))
+                    return rc;
+            } else {
+                if ((rc = moe_cache_wait_uploads(c, (moe_stream_t)s))) return rc;
+                if ((rc = ffn_call(st, x, T, d.E, d.k, ids_d, w_d, table, ns, pool, nullptr, 0, partial,
+                                   nh + nm, s)))
+                    return rc;
+            }
+        }
+        if ((rc = moe_cache_release(c, (moe_stream_t)s))) return rc;
+    } else {
+        const void *pool = (const char *)d.resident_pool + (size_t)layer * d.E * d.slot_bytes;
+        int n_active = d.E < T * d.k ? d.E : T * d.k;
+        if (d.profile) {
+            // count the distinct experts for the byte accounting (profiling only)
+            MOE_TRY_CUDA(cudaMemcpyAsync(st->ids_h, ids_d, (size_t)T * d.k * 4, cudaMemcpyDeviceToHost, s));
+            MOE_TRY_CUDA(cudaStreamSynchronize(s));
+            bool want[MOE_MAX_E] = {false};
+            n_active = 0;
+            for (int i = 0; i < T * d.k; ++i)
+                if (!want[st->ids_h[i]]) { want[st->ids_h[i]] = true; ++n_active; }
+        }
+        if ((rc = ffn_call(st, x, T, d.E, d.k, ids_d, w_d, nullptr, d.E, pool, nullptr, 0, partial,
+                           n_active, s)))
+            return rc;
+    }
+
+    const float *extra = x;
+    if (d.n_shared > 0) {
+        const void *spool = (const char *)d.shared_pool + (size_t)layer * d.n_shared * d.slot_bytes;
+        int32_t *ids_s = (int32_t *)(st->ws + L.ids_s);
+        float *w_s = (float *)(st->ws + L.w_s);
+        float *partial_s = (float *)(st->ws + L.partial_s);
+        float *tmp = (float *)(st->ws + L.tmp);
+        if ((rc = ffn_call(st, x, T, d.n_shared, d.n_shared, ids_s, w_s, nullptr, d.n_shared, spool,
+                           nullptr, 0, partial_s, d.n_shared, s)))
+            return rc;
+        if ((rc = begin_timed(st, s, &ep))) return rc;
+        if ((rc = moe_combine(partial_s, T, d.n_shared, d.H, x, tmp, (moe_stream_t)s))) return rc;
+        st->prof.kernel_launches += 1;
+        if ((rc = end_timed(st, s, K_COMBINE, ep))) return rc;
+        extra = tmp;
+    }
+    if ((rc = begin_timed(st, s, &ep))) return rc;
+    if ((rc = moe_combine(partial, T, d.k, d.H, extra, y, (moe_stream_t)s))) return rc;
+    st->prof.kernel_launches += 1;
+    if ((rc = end_timed(st, s, K_COMBINE, ep))) return rc;
+
+    if (ids_out) MOE_TRY_CUDA(cudaMemcpyAsync(ids_out, ids_d, (size_t)T * d.k * 4, cudaMemcpyDeviceToHost, s));
+    if (w_out) MOE_TRY_CUDA(cudaMemcpyAsync(w_out, w_d, (size_t)T * d.k * 4, cudaMemcpyDeviceToHost, s));
+    st->prof.layers++;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_stack_workspace(int H, int F, int qtype, int E, int k, int max_T, int n_shared,
+                                   size_t *bytes) {
+    MOE_CHECK(bytes && H > 0 && F > 0 && H % 32 == 0 && F % 32 == 0);
+    MOE_CHECK(qtype == MOE_Q8_0 || qtype == MOE_Q4_SM);
+    MOE_CHECK(E >= 1 && E <= MOE_MAX_E && k >= 1 && k <= MOE_MAX_K && k <= E);
+    MOE_CHECK(max_T >= 1 && max_T <= MOE_DECODE_MAX_T && n_shared >= 0 && n_shared <= MOE_MAX_K);
+    *bytes = stack_ws(H, F, qtype, E, k, max_T, n_shared).total;
+    return MOE_OK;
+}
+
+extern "C" int moe_stack_create(const moe_stack_desc *desc, moe_stack **out) {
+    MOE_CHECK(desc && out);
+    *out = nullptr;
+    const moe_stack_desc &d = *desc;
+    size_t need = 0;
+    int rc = moe_stack_workspace(d.H, d.F, d.qtype, d.E, d.k, d.max_T, d.n_shared, &need);
+    if (rc) return rc;
+    MOE_CHECK(d.n_layers >= 1 && d.w_router);
+    MOE_CHECK(d.workspace && ((uintptr_t)d.workspace % 256) == 0 && d.ws_bytes >= need);
+    MOE_CHECK(d.slot_bytes >= moe_expert_image_bytes(d.qtype, d.H, d.F) && d.slot_bytes % 256 == 0);
+    MOE_CHECK(d.n_groups >= 0);
+    if (d.n_groups == 0) MOE_CHECK(d.resident_pool != nullptr);
+    else MOE_CHECK(d.caches != nullptr);
+    if (d.n_shared > 0) MOE_CHECK(d.shared_pool != nullptr);
+
+    moe_stack *st = new moe_stack();
+    st->d = d;
+    st->L = stack_ws(d.H, d.F, d.qtype, d.E, d.k, d.max_T, d.n_shared);
+    st->ws = (char *)d.workspace;
+    st->w_router.assign(d.w_router, d.w_router + d.n_layers);
+    st->bias.assign(d.n_layers, nullptr);
+    if (d.bias) st->bias.assign(d.bias, d.bias + d.n_layers);
+    st->group_of_layer.assign(d.n_layers, -1);
+    for (int g = 0; g < d.n_groups; ++g) {
+        moe_cache *c = d.caches[g];
+        int first = 0, n = 0;
+        if (!c || moe_cache_layer_range(c, &first, &n) != MOE_OK || first + n > d.n_layers) {
+            delete st;
+            return MOE_ERR_INVALID;
+        }
+        st->caches.push_back(c);
+        for (int l = first; l < first + n; ++l) st->group_of_layer[l] = g;
+    }
+    if (d.n_groups > 0)
+        for (int l = 0; l < d.n_layers; ++l)
+            if (st->group_of_layer[l] < 0) {
+                delete st;
+                return MOE_ERR_INVALID;  // every layer must belong to a group
+            }
+    if (cudaHostAlloc(&st->ids_h, (size_t)d.max_T * d.k * 4, cudaHostAllocDefault) != cudaSuccess ||
+        cudaHostAlloc(&st->slots_h, (size_t)d.max_T * d.k * 4, cudaHostAllocDefault) != cudaSuccess ||
+        cudaEventCreateWithFlags(&st->ids_ready, cudaEventDisableTiming) != cudaSuccess) {
+        moe_stack_destroy(st);
+        return MOE_ERR_CUDA;
+    }
+    if (d.n_shared > 0) {
+        // constant routing of the shared experts: every token, every shared expert, weight 1
+        std::vector<int32_t> ids((size_t)d.max_T * d.n_shared);
+        std::vector<float> w((size_t)d.max_T * d.n_shared, 1.0f);
+        for (int t = 0; t < d.max_T; ++t)
+            for (int j = 0; j < d.n_shared; ++j) ids[(size_t)t * d.n_shared + j] = j;
+        if (cudaMemcpy(st->ws + st->L.ids_s, ids.data(), ids.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(st->ws + st->L.w_s, w.data(), w.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess) {
+            moe_stack_destroy(st);
+            return MOE_ERR_CUDA;
+        }
+    }
+    *out = st;
+    return MOE_OK;
+}
+
+extern "C" int moe_stack_layer(moe_stack *st, int layer, const float *x_in, float *y_out, int T,
+                               int32_t *ids_host_out, float *weights_host_out, moe_stream_t s) {
+    MOE_CHECK(st && x_in && y_out);
+    MOE_CHECK(layer >= 0 && layer < st->d.n_layers);
+    MOE_CHECK(T >= 1 && T <= st->d.max_T);
+    cudaStream_t cs = moe_cuda_stream(s);
+    st->last_stream = cs;
+    return layer_step(st, layer, x_in, y_out, T, ids_host_out, weights_host_out, cs);
+}
+
+extern "C" int moe_stack_decode(moe_stack *st, const float *x_in, float *y_out, int T,
+                                int32_t *ids_host_out, float *weights_host_out, moe_stream_t s) {
+    MOE_CHECK(st && x_in && y_out);
+    MOE_CHECK(T >= 1 && T <= st->d.max_T);
+    cudaStream_t cs = moe_cuda_stream(s);
+    st->last_stream = cs;
+    const int L = st->d.n_layers;
+    float *hA = (float *)(st->ws + st->L.hA), *hB = (float *)(st->ws + st->L.hB);
+    const float *cur = x_in;
+    const size_t per = (size_t)T * st->d.k;
+    for (int l = 0; l < L; ++l) {
+        float *out = (l == L - 1) ? y_out : ((l & 1) ? hB : hA);
+        const int rc = layer_step(st, l, cur, out, T, ids_host_out ? ids_host_out + l * per : nullptr,
+                                  weights_host_out ? weights_host_out + l * per : nullptr, cs);
+        if (rc) return rc;
+        cur = out;
+    }
+    st->prof.steps++;
+    return MOE_OK;
+}
+
+extern "C" int moe_stack_profile_get(moe_stack *st, moe_stack_profile *out) {
+    MOE_CHECK(st && out);
+    if (st->last_stream) MOE_TRY_CUDA(cudaStreamSynchronize(st->last_stream));
+    const int rc = harvest(st);
+    if (rc) return rc;
+    *out = st->prof;
+    return MOE_OK;
+}
+
+extern "C" int moe_stack_profile_reset(moe_stack *st) {
+    MOE_CHECK(st);
+    if (st->last_stream) MOE_TRY_CUDA(cudaStreamSynchronize(st->last_stream));
+    st->timed.clear();
+    st->ev_used = 0;
+    st->prof = moe_stack_profile{};
+    return MOE_OK;
+}
+
+extern "C" int moe_stack_set_profile(moe_stack *st, int level) {
+    MOE_CHECK(st && level >= 0 && level <= 2);
+    if (st->last_stream) MOE_TRY_CUDA(cudaStreamSynchronize(st->last_stream));
+    const int rc = harvest(st);
+    if (rc) return rc;
+    st->d.profile = level;
+    return MOE_OK;
+}
+
+extern "C" void moe_stack_destroy(moe_stack *st) {
+    if (!st) return;
+    if (st->last_stream) cudaStreamSynchronize(st->last_stream);
+    for (cudaEvent_t e : st->ev_pool) cudaEventDestroy(e);
+    if (st->ids_ready) cudaEventDestroy(st->ids_ready);
+    if (st->ids_h) cudaFreeHost(st->ids_h);
+    if (st->slots_h) cudaFreeHost(st->slots_h);
+    delete st;
+}

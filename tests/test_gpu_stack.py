@@ -77,6 +77,7 @@ class Checker:
 
 
 def run_steps(stack, cfg, T, steps, step0=0):
+    stack.reset_caches()  # the simulator starts from an empty pool too
     ck = Checker(stack, cfg)
     for step in range(step0, step0 + steps):
         h = synth.tokens_x(cfg, step, T).astype(np.float64)
@@ -95,8 +96,8 @@ def test_tiny_layer():
 
 
 def test_small_stack_two_groups_shared_experts():
-    cfg0 = synth.small_config(0, H=256, F=128, E=16, k=2, L=4, n_shared=2, bias_a=1.0, seed_cfg=830,
-                              groups=(synth.PoolGroup(0, 2, 6), synth.PoolGroup(2, 2, 5)))
+    cfg0 = synth.small_config(0, H=256, F=128, E=24, k=2, L=4, n_shared=2, bias_a=1.0, seed_cfg=830,
+                              groups=(synth.PoolGroup(0, 2, 18), synth.PoolGroup(2, 2, 16)))
     import dataclasses
     cfg = dataclasses.replace(cfg0, tokens=(1, 3, 8))
     st = _stack(cfg, max_T=8)
@@ -105,7 +106,7 @@ def test_small_stack_two_groups_shared_experts():
     st.close()
 
 
-def test_small_stack_q4_resident_bf16_free():
+def test_small_stack_q4_resident():
     cfg = synth.small_config(1, H=512, F=256, E=32, k=4, L=3, bias_a=1.1, seed_cfg=831)
     st = _stack(cfg, max_T=5)
     run_steps(st, cfg, 5, 2)

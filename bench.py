@@ -226,7 +226,7 @@ def run_gpu(args, world, rank, local):
     peaks = load_peaks()
     stack = Stack(cfg, max_T=max(max(cfg.tokens), args.batch), profile=1)
     stream = torch.cuda.Stream()
-    batches = sorted(set(list(cfg.tokens) + [args.batch]))
+    batches = [args.batch] if args.lite else sorted(set(list(cfg.tokens) + [args.batch]))
     n_inputs = 64
     inputs = {T: [torch.from_numpy(synth.tokens_x(cfg, 3 + s, T)).cuda() for s in range(n_inputs)]
               for T in batches}
@@ -271,6 +271,15 @@ def run_gpu(args, world, rank, local):
         }
         if T == args.batch:
             main = (ms, prof, st, steps)
+
+    if args.lite:
+        r = results[args.batch]
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": r["tokens_per_s"], "unit": "tokens/s",
+                              "lite": True, "batch": args.batch, "result": r}), flush=True)
+        clocks.stop()
+        stack.close()
+        return 0
 
     # per-kernel breakdown (events around every kernel; a separate, shorter loop)
     stack.set_profile(2)
@@ -355,6 +364,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--batch", type=int, default=8)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--lite", action="store_true",
+                    help="only the timed loop at --batch (no other batches, breakdown, e2e or CPU "
+                         "baseline); used as the ncu target")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

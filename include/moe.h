@@ -234,6 +234,31 @@ int moe_expert_ffn(const void *x, int xtype, int T, int H, int F, int qtype, int
 
 int moe_expert_ffn_workspace(int T, int H, int F, int qtype, int E, int k, size_t *bytes);
 
+/*
+ * moe_expert_ffn_noalloc — moe_expert_ffn for callers that cannot allocate device
+ * memory (the pages have no counterpart; this is a library convenience).  Examples: a
+ * plugin whose host framework owns every device allocation and passes it only its
+ * input and output buffers, or a decode loop where a cudaMalloc/cudaFree, which can
+ * synchronise the whole device, is not allowed.  Same arguments and results as
+ * moe_expert_ffn, without workspace/ws_bytes; it allocates nothing.
+ * Scratch: one array of MOE_NOALLOC_SCRATCH_MAX bytes in device memory, defined in
+ * the library, present on every device that loads the library until the process
+ * exits.  A request whose moe_expert_ffn_workspace() size exceeds it is rejected with
+ * MOE_ERR_UNSUPPORTED before anything is enqueued.
+ * Set-up: the first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream capture.
+ * Sharing: every call on a device uses the same array, which keeps the last call's
+ * contents (nothing in it needs to start at zero).  Calls whose kernels can overlap on
+ * the GPU — different streams, or different host threads — race on the array;
+ * serialise them on one stream.
+ */
+#define MOE_NOALLOC_SCRATCH_MAX (8u << 20)
+int moe_expert_ffn_noalloc(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
+                           const int32_t *ids, const float *weights, const int32_t *d_slot_table,
+                           int n_slots, const void *pool, size_t slot_bytes,
+                           const int32_t *expert_subset, int n_subset, float *partial,
+                           moe_stream_t s);
+
 /* ---------------------------------------------------------------- combine (a8) */
 
 /*

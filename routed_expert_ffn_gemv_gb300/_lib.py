@@ -37,7 +37,9 @@ EXPORTED = [
     "moe_combine", "moe_device_status", "moe_stack_workspace", "moe_stack_create",
     "moe_stack_decode", "moe_stack_layer", "moe_stack_profile_get", "moe_stack_profile_reset",
     "moe_stack_destroy", "moe_debug_inject_fault", "moe_stack_set_profile",
+    "moe_expert_ffn_noalloc",
 ]
+MOE_NOALLOC_SCRATCH_MAX = 8 << 20
 
 
 class MoeError(RuntimeError):
@@ -124,6 +126,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_expert_ffn": ([_vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _sz, _vp, _i,
                             _vp, _vp, _sz, _vp], _i),
         "moe_expert_ffn_workspace": ([_i, _i, _i, _i, _i, _i, P(_sz)], _i),
+        "moe_expert_ffn_noalloc": ([_vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _sz, _vp,
+                                    _i, _vp, _vp], _i),
         "moe_combine": ([_vp, _i, _i, _i, _vp, _vp, _vp], _i),
         "moe_device_status": ([P(_i), _i], _i),
         "moe_stack_workspace": ([_i, _i, _i, _i, _i, _i, _i, P(_sz)], _i),
@@ -268,6 +272,15 @@ def moe_expert_ffn_workspace(T: int, H: int, F: int, qtype: int, E: int, k: int)
     out = _sz()
     _ck("moe_expert_ffn_workspace", load().moe_expert_ffn_workspace(T, H, F, qtype, E, k, ctypes.byref(out)))
     return out.value
+
+
+def moe_expert_ffn_noalloc(x, xtype: int, T: int, H: int, F: int, qtype: int, E: int, k: int, ids,
+                           weights, d_slot_table, n_slots: int, pool, slot_bytes: int, expert_subset,
+                           n_subset: int, partial, stream=None) -> None:
+    _ck("moe_expert_ffn_noalloc",
+        load().moe_expert_ffn_noalloc(_ptr(x), xtype, T, H, F, qtype, E, k, _ptr(ids), _ptr(weights),
+                                      _ptr(d_slot_table), n_slots, _ptr(pool), slot_bytes,
+                                      _ptr(expert_subset), n_subset, _ptr(partial), _stream(stream)))
 
 
 def moe_combine(partial, T: int, k: int, H: int, extra, y, stream=None) -> None:

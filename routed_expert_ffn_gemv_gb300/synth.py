@@ -153,8 +153,12 @@ def q8_0_blocks(rng: np.random.Generator, rows: int, cols: int, d_value: float,
     Codes are round(N(0,1)*40) clipped to [-127, 127] (round half away from zero).
     """
     nb = cols // QK
-    z = rng.standard_normal((rows, nb, QK), dtype=np.float32) * np.float32(40.0)
-    q = np.clip(_round_half_away(z), -127, 127).astype(np.int8)
+    z = rng.standard_normal((rows, nb, QK), dtype=np.float32)
+    z *= np.float32(40.0)
+    z += np.copysign(np.float32(0.5), z)   # round half away from zero: trunc(z + sign(z)/2)
+    np.trunc(z, out=z)
+    np.clip(z, -127, 127, out=z)
+    q = z.astype(np.int8)
     out = np.empty((rows, nb, Q8_0_BLOCK_BYTES), dtype=np.uint8)
     if random_scales:
         d = (rng.uniform(0.25, 4.0, size=(rows, nb)) * d_value).astype(np.float16)

@@ -518,6 +518,11 @@ size_t moe_decode_workspace_bytes(int T, int H, int F, int qtype, int E, int k) 
     return ws_layout(T, H, F, qtype, E, k).total;
 }
 
+size_t moe_ffn_workspace_bytes(int T, int H, int F, int qtype, int E, int k) {
+    if (moe_prefill_eligible(T, H, F, qtype)) return moe_prefill_workspace_bytes(T, H, F, E, k);
+    return moe_decode_workspace_bytes(T, H, F, qtype, E, k);
+}
+
 int moe_expert_ffn_impl(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
                         const int32_t *ids, const float *weights, const int32_t *d_slot_table,
                         int n_slots, const void *pool, size_t slot_bytes,
@@ -536,6 +541,11 @@ int moe_expert_ffn_impl(const void *x, int xtype, int T, int H, int F, int qtype
     MOE_CHECK(((uintptr_t)pool & 15) == 0 && (slot_bytes & 15) == 0);
     MOE_CHECK(slot_bytes >= moe_expert_image_bytes(qtype, H, F));
     MOE_CHECK(((uintptr_t)workspace & 255) == 0);
+    if (moe_prefill_eligible(T, H, F, qtype)) {
+        MOE_CHECK(ws_bytes >= moe_prefill_workspace_bytes(T, H, F, E, k));
+        return moe_prefill_ffn(x, xtype, T, H, F, qtype, E, k, ids, weights, d_slot_table, n_slots, pool,
+                               slot_bytes, expert_subset, n_subset, partial, workspace, ws_bytes, s, timing);
+    }
     const WsLayout W = ws_layout(T, H, F, qtype, E, k);
     MOE_CHECK(ws_bytes >= W.total);
     if ((size_t)T * k > (1u << 20)) return MOE_ERR_UNSUPPORTED;
@@ -603,7 +613,7 @@ extern "C" int moe_expert_ffn_workspace(int T, int H, int F, int qtype, int E, i
     MOE_CHECK(T >= 0 && H > 0 && F > 0 && H % 32 == 0 && F % 32 == 0);
     MOE_CHECK(qtype == MOE_Q8_0 || qtype == MOE_Q4_SM);
     MOE_CHECK(E >= 1 && E <= MOE_MAX_E && k >= 1 && k <= MOE_MAX_K);
-    *bytes = moe_decode_workspace_bytes(T, H, F, qtype, E, k);
+    *bytes = moe_ffn_workspace_bytes(T, H, F, qtype, E, k);
     return MOE_OK;
 }
 

@@ -1,0 +1,124 @@
+"""Parity of the prefill path (T > 32: tcgen05 grouped GEMM) against the fp64 oracle.
+
+Shapes span several 128-row weight tiles, several token tiles per expert with ragged
+tails, both token-tile widths (64 and 128 rows), q8_0 and 4-bit weights, fp32 and bf16
+activations, expert subsets and a slot table.  fp16 operands with fp32 accumulation keep
+outputs well inside the 2e-3 tolerance (simulated 5e-4 on the Qwen-shaped layer).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from tests.gpu_helpers import TOL, random_routes, rel_err
+from routed_expert_ffn_gemv_gb300 import _lib as L, synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _pool(cfg, experts, random_scales):
+    stride = (L.moe_slot_image_bytes(cfg.qtype, cfg.H, cfg.F) + 255) // 256 * 256
+    host = torch.empty(len(experts) * stride, dtype=torch.uint8, pin_memory=True)
+    for i, e in enumerate(experts):
+        g, u, d = synth.expert_weights(cfg, 0, e, random_scales)
+        L.moe_pack_expert(cfg.qtype, cfg.H, cfg.F, g.ctypes.data, u.ctypes.data, d.ctypes.data,
+                          host.data_ptr() + i * stride)
+    return host.cuda(), stride
+
+
+def _run(cfg, T, xtype, rs, subset=None, reverse_slots=False, seed=0):
+    H, F, E, k = cfg.H, cfg.F, cfg.E, cfg.k
+    order = list(range(E))[::-1] if reverse_slots else list(range(E))
+    pool, stride = _pool(cfg, order, rs)
+    table = None
+    if reverse_slots:
+        table = torch.tensor([E - 1 - e for e in range(E)], dtype=torch.int32, device="cuda")
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, H), dtype=np.float32)
+    if xtype == 1:
+        xb = synth.f32_to_bf16_bits(x)
+        x_d, x64 = torch.from_numpy(xb.view(np.int16)).cuda(), oracle.x_to_double(xb, 1)
+    else:
+        x_d, x64 = torch.from_numpy(x).cuda(), oracle.x_to_double(x, 0)
+    ids, w = random_routes(rng, T, E, k)
+    ws_bytes = L.moe_expert_ffn_workspace(T, H, F, cfg.qtype, E, k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    partial = torch.full((T, k, H), float("nan"), dtype=torch.float32, device="cuda")
+    sub = None if subset is None else torch.tensor(subset, dtype=torch.int32, device="cuda")
+    L.moe_expert_ffn(x_d, xtype, T, H, F, cfg.qtype, E, k, torch.from_numpy(ids).cuda(),
+                     torch.from_numpy(w).cuda(), table, E, pool, stride, sub,
+                     0 if subset is None else len(subset), partial, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert L.moe_device_status(clear=True) == 0
+    return ids, w, x64, partial.cpu().numpy()
+
+
+def _check(cfg, ids, w, x64, partial, rs, subset=None, sample=None):
+    worst = 0.0
+    T, k = ids.shape
+    cache = {}
+    toks = range(T) if sample is None else sample
+    for t in toks:
+        for j in range(k):
+            e = int(ids[t, j])
+            if subset is not None and e not in subset:
+                assert np.all(np.isnan(partial[t, j]))
+                continue
+            if e not in cache:
+                cache[e] = synth.expert_weights(cfg, 0, e, rs)
+            g, u, d = cache[e]
+            ref = float(w[t, j]) * oracle.expert_ffn(cfg.qtype, cfg.H, cfg.F, g, u, d, x64[t])
+            worst = max(worst, rel_err(partial[t, j][None], ref[None])[0])
+    assert worst <= TOL, worst
+    return worst
+
+
+PREFILL_CASES = [
+    # qtype, H, F, E, k, T, xtype, random_scales
+    (1, 256, 128, 8, 2, 48, 0, True),       # one token tile per expert (64-row tiles)
+    (0, 256, 128, 8, 2, 48, 0, True),
+    (1, 512, 256, 4, 2, 400, 1, True),      # 128-row token tiles, ragged tails, bf16 x
+    (0, 512, 256, 4, 2, 400, 0, False),
+    (1, 1024, 384, 16, 4, 200, 1, False),   # 3 weight tiles, 64-row token tiles
+]
+
+
+@pytest.mark.parametrize("qtype,H,F,E,k,T,xtype,rs", PREFILL_CASES)
+def test_prefill_parity(qtype, H, F, E, k, T, xtype, rs):
+    cfg = synth.small_config(qtype, H=H, F=F, E=E, k=k, seed_cfg=850 + qtype)
+    ids, w, x64, partial = _run(cfg, T, xtype, rs, seed=T)
+    worst = _check(cfg, ids, w, x64, partial, rs, sample=range(0, T, max(1, T // 40)))
+    print(f"prefill q{qtype} H{H} F{F} E{E} k{k} T{T}: worst rel err {worst:.2e}")
+
+
+def test_prefill_subset_and_slot_table():
+    cfg = synth.small_config(1, H=256, F=128, E=6, k=2, seed_cfg=860)
+    subset = [1, 2, 5]
+    ids, w, x64, partial = _run(cfg, 70, 0, True, subset=subset, reverse_slots=True, seed=3)
+    _check(cfg, ids, w, x64, partial, True, subset=subset)
+
+
+def test_prefill_qwen_layer_4096_tokens_sampled():
+    cfg = synth.config(4)
+    T = 4096
+    from routed_expert_ffn_gemv_gb300.workload import PinnedImages, slot_stride
+    imgs = PinnedImages(cfg, [0], range(cfg.E))
+    pool, stride = imgs.buf.cuda(), slot_stride(cfg)
+    xb = synth.tokens_x(cfg, 0, T)
+    x_d = torch.from_numpy(xb.view(np.int16)).cuda()
+    wr, b = synth.router_weights(cfg, 0), synth.router_bias(cfg, 0)
+    ids = torch.empty((T, cfg.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, cfg.k), dtype=torch.float32, device="cuda")
+    L.moe_router_topk(x_d, 1, T, cfg.H, torch.from_numpy(wr.view(np.int16)).cuda(),
+                      torch.from_numpy(b).cuda(), cfg.E, cfg.k, ids, w)
+    ws_bytes = L.moe_expert_ffn_workspace(T, cfg.H, cfg.F, cfg.qtype, cfg.E, cfg.k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    partial = torch.empty((T, cfg.k, cfg.H), dtype=torch.float32, device="cuda")
+    L.moe_expert_ffn(x_d, 1, T, cfg.H, cfg.F, cfg.qtype, cfg.E, cfg.k, ids, w, None, cfg.E, pool, stride,
+                     None, 0, partial, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert L.moe_device_status(clear=True) == 0
+    rng = np.random.default_rng(9)
+    sample = np.sort(rng.choice(T, size=12, replace=False))
+    x64 = oracle.x_to_double(xb, 1)
+    _check(cfg, ids.cpu().numpy(), w.cpu().numpy(), x64, partial.cpu().numpy(), False, sample=sample)

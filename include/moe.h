@@ -223,8 +223,10 @@ int moe_slots_for_budget(size_t budget_bytes, const size_t *per_expert_bytes, in
  * expert_subset device int32 list of experts to process, or NULL for all.
  * partial      device [T][k][H] fp32 out.
  * workspace    device scratch of moe_expert_ffn_workspace() bytes (256-byte aligned).
- * Path: T <= MOE_DECODE_MAX_T uses the dequantising GEMV kernels; larger T uses the
- * prefill grouped GEMM (tcgen05) when available for the format, else the GEMV kernels.
+ * Path: T <= MOE_DECODE_MAX_T uses the dequantising GEMV kernels (fp32 arithmetic).  Larger
+ * T with bf16 activations and H, F multiples of 128 uses the prefill grouped GEMM on tcgen05
+ * tensor cores with fp16 operands (activations, dequantised weights d*q[+m] and SwiGLU
+ * output each rounded once to fp16) and fp32 accumulation; otherwise the GEMV kernels.
  */
 int moe_expert_ffn(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
                    const int32_t *ids, const float *weights, const int32_t *d_slot_table,
@@ -232,7 +234,8 @@ int moe_expert_ffn(const void *x, int xtype, int T, int H, int F, int qtype, int
                    const int32_t *expert_subset, int n_subset, float *partial,
                    void *workspace, size_t ws_bytes, moe_stream_t s);
 
-int moe_expert_ffn_workspace(int T, int H, int F, int qtype, int E, int k, size_t *bytes);
+/* Workspace bytes of moe_expert_ffn for these sizes (it depends on the path taken). */
+int moe_expert_ffn_workspace(int T, int H, int F, int qtype, int xtype, int E, int k, size_t *bytes);
 
 /*
  * moe_expert_ffn_noalloc — moe_expert_ffn for callers that cannot allocate device

@@ -125,7 +125,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_slots_for_budget": ([_sz, P(_sz), _i, _i, P(_i)], _i),
         "moe_expert_ffn": ([_vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _sz, _vp, _i,
                             _vp, _vp, _sz, _vp], _i),
-        "moe_expert_ffn_workspace": ([_i, _i, _i, _i, _i, _i, P(_sz)], _i),
+        "moe_expert_ffn_workspace": ([_i, _i, _i, _i, _i, _i, _i, P(_sz)], _i),
         "moe_expert_ffn_noalloc": ([_vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _sz, _vp,
                                     _i, _vp, _vp], _i),
         "moe_combine": ([_vp, _i, _i, _i, _vp, _vp, _vp], _i),
@@ -268,9 +268,10 @@ def moe_expert_ffn(x, xtype: int, T: int, H: int, F: int, qtype: int, E: int, k:
                                                 _ptr(workspace), ws_bytes, _stream(stream)))
 
 
-def moe_expert_ffn_workspace(T: int, H: int, F: int, qtype: int, E: int, k: int) -> int:
+def moe_expert_ffn_workspace(T: int, H: int, F: int, qtype: int, xtype: int, E: int, k: int) -> int:
     out = _sz()
-    _ck("moe_expert_ffn_workspace", load().moe_expert_ffn_workspace(T, H, F, qtype, E, k, ctypes.byref(out)))
+    _ck("moe_expert_ffn_workspace", load().moe_expert_ffn_workspace(T, H, F, qtype, xtype, E, k,
+                                                                    ctypes.byref(out)))
     return out.value
 
 

@@ -106,10 +106,10 @@ int moe_cache_layer_range(const moe_cache *c, int *first_layer, int *n_layers);
 
 size_t moe_decode_workspace_bytes(int T, int H, int F, int qtype, int E, int k);
 // Workspace of moe_expert_ffn for these sizes (decode GEMV or prefill grouped GEMM path).
-size_t moe_ffn_workspace_bytes(int T, int H, int F, int qtype, int E, int k);
+size_t moe_ffn_workspace_bytes(int T, int H, int F, int qtype, int xtype, int E, int k);
 
 // Prefill path (moe_prefill.cu): grouped GEMM on tcgen05 for T > MOE_DECODE_MAX_T.
-bool moe_prefill_eligible(int T, int H, int F, int qtype);
+bool moe_prefill_eligible(int T, int H, int F, int qtype, int xtype);
 size_t moe_prefill_workspace_bytes(int T, int H, int F, int E, int k);
 int moe_prefill_ffn(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k, const int32_t *ids,
                     const float *weights, const int32_t *d_slot_table, int n_slots, const void *pool,

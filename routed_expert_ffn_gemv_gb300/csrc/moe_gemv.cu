@@ -518,8 +518,8 @@ size_t moe_decode_workspace_bytes(int T, int H, int F, int qtype, int E, int k) 
     return ws_layout(T, H, F, qtype, E, k).total;
 }
 
-size_t moe_ffn_workspace_bytes(int T, int H, int F, int qtype, int E, int k) {
-    if (moe_prefill_eligible(T, H, F, qtype)) return moe_prefill_workspace_bytes(T, H, F, E, k);
+size_t moe_ffn_workspace_bytes(int T, int H, int F, int qtype, int xtype, int E, int k) {
+    if (moe_prefill_eligible(T, H, F, qtype, xtype)) return moe_prefill_workspace_bytes(T, H, F, E, k);
     return moe_decode_workspace_bytes(T, H, F, qtype, E, k);
 }
 
@@ -541,7 +541,7 @@ int moe_expert_ffn_impl(const void *x, int xtype, int T, int H, int F, int qtype
     MOE_CHECK(((uintptr_t)pool & 15) == 0 && (slot_bytes & 15) == 0);
     MOE_CHECK(slot_bytes >= moe_expert_image_bytes(qtype, H, F));
     MOE_CHECK(((uintptr_t)workspace & 255) == 0);
-    if (moe_prefill_eligible(T, H, F, qtype)) {
+    if (moe_prefill_eligible(T, H, F, qtype, xtype)) {
         MOE_CHECK(ws_bytes >= moe_prefill_workspace_bytes(T, H, F, E, k));
         return moe_prefill_ffn(x, xtype, T, H, F, qtype, E, k, ids, weights, d_slot_table, n_slots, pool,
                                slot_bytes, expert_subset, n_subset, partial, workspace, ws_bytes, s, timing);
@@ -608,12 +608,14 @@ extern "C" int moe_expert_ffn(const void *x, int xtype, int T, int H, int F, int
                                ws_bytes, moe_cuda_stream(s), nullptr);
 }
 
-extern "C" int moe_expert_ffn_workspace(int T, int H, int F, int qtype, int E, int k, size_t *bytes) {
+extern "C" int moe_expert_ffn_workspace(int T, int H, int F, int qtype, int xtype, int E, int k,
+                                        size_t *bytes) {
     MOE_CHECK(bytes);
     MOE_CHECK(T >= 0 && H > 0 && F > 0 && H % 32 == 0 && F % 32 == 0);
     MOE_CHECK(qtype == MOE_Q8_0 || qtype == MOE_Q4_SM);
+    MOE_CHECK(xtype == MOE_F32 || xtype == MOE_BF16);
     MOE_CHECK(E >= 1 && E <= MOE_MAX_E && k >= 1 && k <= MOE_MAX_K);
-    *bytes = moe_ffn_workspace_bytes(T, H, F, qtype, E, k);
+    *bytes = moe_ffn_workspace_bytes(T, H, F, qtype, xtype, E, k);
     return MOE_OK;
 }
 

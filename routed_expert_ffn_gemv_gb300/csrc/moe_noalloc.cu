@@ -48,7 +48,8 @@ extern "C" int moe_expert_ffn_noalloc(const void *x, int xtype, int T, int H, in
     MOE_CHECK(T >= 0 && H > 0 && F > 0 && H % 32 == 0 && F % 32 == 0);
     MOE_CHECK(qtype == MOE_Q8_0 || qtype == MOE_Q4_SM);
     MOE_CHECK(E >= 1 && E <= MOE_MAX_E && k >= 1 && k <= MOE_MAX_K && k <= E);
-    if (moe_ffn_workspace_bytes(T, H, F, qtype, E, k) > MOE_NOALLOC_SCRATCH_BYTES)
+    MOE_CHECK(xtype == MOE_F32 || xtype == MOE_BF16);
+    if (moe_ffn_workspace_bytes(T, H, F, qtype, xtype, E, k) > MOE_NOALLOC_SCRATCH_BYTES)
         return MOE_ERR_UNSUPPORTED;  // the request needs more scratch than the static array holds
     void *scratch = nullptr;
     const int rc = noalloc_scratch(&scratch);

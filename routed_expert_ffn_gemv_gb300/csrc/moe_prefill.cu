@@ -552,8 +552,9 @@ int launch_gemms(const PfParams &p, int max_tiles, cudaStream_t s, const moe_ffn
 
 }  // namespace
 
-bool moe_prefill_eligible(int T, int H, int F, int qtype) {
-    return T > MOE_DECODE_MAX_T && H % PF_BM == 0 && F % PF_BM == 0 && (qtype == MOE_Q8_0 || qtype == MOE_Q4_SM);
+bool moe_prefill_eligible(int T, int H, int F, int qtype, int xtype) {
+    return T > MOE_DECODE_MAX_T && xtype == MOE_BF16 && H % PF_BM == 0 && F % PF_BM == 0 &&
+           (qtype == MOE_Q8_0 || qtype == MOE_Q4_SM);
 }
 
 size_t moe_prefill_workspace_bytes(int T, int H, int F, int E, int k) { return pf_layout(T, H, F, E, k).total; }

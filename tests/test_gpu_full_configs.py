@@ -36,13 +36,19 @@ def test_qwen_stack_full_size_batch1():
     st.close()
 
 
-@pytest.mark.parametrize("T", [1, 32])
-def test_deepseek_stack_full_size(T):
+@pytest.fixture(scope="module")
+def deepseek_stack():
     cfg = synth.config(3)
     st = _stack(cfg, max_T=32)
+    yield cfg, st
+    st.close()
+
+
+@pytest.mark.parametrize("T", [1, 32])
+def test_deepseek_stack_full_size(deepseek_stack, T):
+    cfg, st = deepseek_stack
     ck = run_steps(st, cfg, T, 2, step0=50 + T)
     print(f"config3 T={T}: worst rel err {ck.worst:.3e}, excluded {ck.excluded}")
-    st.close()
 
 
 def test_qwen_prefill_layer_512_tokens_sampled():
@@ -59,7 +65,7 @@ def test_qwen_prefill_layer_512_tokens_sampled():
     w = torch.empty((T, k), dtype=torch.float32, device="cuda")
     L.moe_router_topk(x_d, 1, T, H, torch.from_numpy(wr.view(np.int16)).cuda(), torch.from_numpy(b).cuda(),
                       E, k, ids, w)
-    ws_bytes = L.moe_expert_ffn_workspace(T, H, F, cfg.qtype, E, k)
+    ws_bytes = L.moe_expert_ffn_workspace(T, H, F, cfg.qtype, 1, E, k)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     partial = torch.empty((T, k, H), dtype=torch.float32, device="cuda")
     L.moe_expert_ffn(x_d, 1, T, H, F, cfg.qtype, E, k, ids, w, None, E, pool, stride, None, 0, partial, ws,

@@ -86,7 +86,7 @@ def make_pool(cfg, layer, experts, random_scales=False):
 
 def run_ffn(cfg, pool, stride, x_d, xtype, ids, w, subset=None, partial=None, table=None, n_slots=None):
     T, k = ids.shape
-    ws_bytes = L.moe_expert_ffn_workspace(T, cfg.H, cfg.F, cfg.qtype, cfg.E, k)
+    ws_bytes = L.moe_expert_ffn_workspace(T, cfg.H, cfg.F, cfg.qtype, xtype, cfg.E, k)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev())
     if partial is None:
         partial = torch.full((T, k, cfg.H), float("nan"), dtype=torch.float32, device=dev())

@@ -1,9 +1,15 @@
-"""Parity of the prefill path (T > 32: tcgen05 grouped GEMM) against the fp64 oracle.
+"""Parity of the prefill path (T > 32 with bf16 activations: tcgen05 grouped GEMM with fp16
+operands) against the fp64 oracle.
 
 Shapes span several 128-row weight tiles, several token tiles per expert with ragged
-tails, both token-tile widths (64 and 128 rows), q8_0 and 4-bit weights, fp32 and bf16
-activations, expert subsets and a slot table.  fp16 operands with fp32 accumulation keep
-outputs well inside the 2e-3 tolerance (simulated 5e-4 on the Qwen-shaped layer).
+tails, both token-tile widths (64 and 128 rows), q8_0 and 4-bit weights, expert subsets
+and a slot table.  The spec check is on the MoE output per token (the routes
+combined): max relative error <= 2e-3.  Each route's partial output is also checked, against
+a bound derived from fp16 arithmetic: weights and the SwiGLU output are each rounded once
+to fp16 (unit roundoff 2^-11); with 4-bit blocks whose per-block minimum is drawn at random,
+the block mean makes the dot products partly cancel, and simulation against fp64 gives up
+to 1.7e-3 per route, so the per-route bound is 3e-3.  fp32 activations above the decode
+limit keep the fp32 GEMV kernels (checked here too).
 """
 import numpy as np
 import pytest
@@ -14,6 +20,8 @@ from routed_expert_ffn_gemv_gb300 import _lib as L, synth
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
+
+ROUTE_TOL = 3e-3
 
 
 def _pool(cfg, experts, random_scales):
@@ -41,7 +49,7 @@ def _run(cfg, T, xtype, rs, subset=None, reverse_slots=False, seed=0):
     else:
         x_d, x64 = torch.from_numpy(x).cuda(), oracle.x_to_double(x, 0)
     ids, w = random_routes(rng, T, E, k)
-    ws_bytes = L.moe_expert_ffn_workspace(T, H, F, cfg.qtype, E, k)
+    ws_bytes = L.moe_expert_ffn_workspace(T, H, F, cfg.qtype, xtype, E, k)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     partial = torch.full((T, k, H), float("nan"), dtype=torch.float32, device="cuda")
     sub = None if subset is None else torch.tensor(subset, dtype=torch.int32, device="cuda")
@@ -54,11 +62,13 @@ def _run(cfg, T, xtype, rs, subset=None, reverse_slots=False, seed=0):
 
 
 def _check(cfg, ids, w, x64, partial, rs, subset=None, sample=None):
-    worst = 0.0
+    """Returns (worst per-token error of the combined output, worst per-route error)."""
     T, k = ids.shape
     cache = {}
-    toks = range(T) if sample is None else sample
-    for t in toks:
+    worst_tok, worst_route = 0.0, 0.0
+    for t in (range(T) if sample is None else sample):
+        y_gpu = np.zeros(cfg.H)
+        y_ref = np.zeros(cfg.H)
         for j in range(k):
             e = int(ids[t, j])
             if subset is not None and e not in subset:
@@ -68,18 +78,23 @@ def _check(cfg, ids, w, x64, partial, rs, subset=None, sample=None):
                 cache[e] = synth.expert_weights(cfg, 0, e, rs)
             g, u, d = cache[e]
             ref = float(w[t, j]) * oracle.expert_ffn(cfg.qtype, cfg.H, cfg.F, g, u, d, x64[t])
-            worst = max(worst, rel_err(partial[t, j][None], ref[None])[0])
-    assert worst <= TOL, worst
-    return worst
+            worst_route = max(worst_route, rel_err(partial[t, j][None], ref[None])[0])
+            y_gpu += partial[t, j]
+            y_ref += ref
+        worst_tok = max(worst_tok, rel_err(y_gpu[None], y_ref[None])[0])
+    assert worst_tok <= TOL, worst_tok
+    assert worst_route <= ROUTE_TOL, worst_route
+    return worst_tok, worst_route
 
 
 PREFILL_CASES = [
     # qtype, H, F, E, k, T, xtype, random_scales
-    (1, 256, 128, 8, 2, 48, 0, True),       # one token tile per expert (64-row tiles)
-    (0, 256, 128, 8, 2, 48, 0, True),
-    (1, 512, 256, 4, 2, 400, 1, True),      # 128-row token tiles, ragged tails, bf16 x
-    (0, 512, 256, 4, 2, 400, 0, False),
+    (1, 256, 128, 8, 2, 48, 1, True),       # one token tile per expert (64-row tiles)
+    (0, 256, 128, 8, 2, 48, 1, True),
+    (1, 512, 256, 4, 2, 400, 1, True),      # 128-row token tiles with ragged tails
+    (0, 512, 256, 4, 2, 400, 1, False),
     (1, 1024, 384, 16, 4, 200, 1, False),   # 3 weight tiles, 64-row token tiles
+    (1, 512, 256, 4, 2, 100, 0, True),      # fp32 activations: the fp32 GEMV kernels
 ]
 
 
@@ -87,14 +102,14 @@ PREFILL_CASES = [
 def test_prefill_parity(qtype, H, F, E, k, T, xtype, rs):
     cfg = synth.small_config(qtype, H=H, F=F, E=E, k=k, seed_cfg=850 + qtype)
     ids, w, x64, partial = _run(cfg, T, xtype, rs, seed=T)
-    worst = _check(cfg, ids, w, x64, partial, rs, sample=range(0, T, max(1, T // 40)))
-    print(f"prefill q{qtype} H{H} F{F} E{E} k{k} T{T}: worst rel err {worst:.2e}")
+    wt, wr = _check(cfg, ids, w, x64, partial, rs, sample=range(0, T, max(1, T // 40)))
+    print(f"prefill q{qtype} H{H} F{F} E{E} k{k} T{T} x{xtype}: token {wt:.2e}, route {wr:.2e}")
 
 
 def test_prefill_subset_and_slot_table():
     cfg = synth.small_config(1, H=256, F=128, E=6, k=2, seed_cfg=860)
     subset = [1, 2, 5]
-    ids, w, x64, partial = _run(cfg, 70, 0, True, subset=subset, reverse_slots=True, seed=3)
+    ids, w, x64, partial = _run(cfg, 70, 1, True, subset=subset, reverse_slots=True, seed=3)
     _check(cfg, ids, w, x64, partial, True, subset=subset)
 
 
@@ -111,7 +126,7 @@ def test_prefill_qwen_layer_4096_tokens_sampled():
     w = torch.empty((T, cfg.k), dtype=torch.float32, device="cuda")
     L.moe_router_topk(x_d, 1, T, cfg.H, torch.from_numpy(wr.view(np.int16)).cuda(),
                       torch.from_numpy(b).cuda(), cfg.E, cfg.k, ids, w)
-    ws_bytes = L.moe_expert_ffn_workspace(T, cfg.H, cfg.F, cfg.qtype, cfg.E, cfg.k)
+    ws_bytes = L.moe_expert_ffn_workspace(T, cfg.H, cfg.F, cfg.qtype, 1, cfg.E, cfg.k)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     partial = torch.empty((T, cfg.k, cfg.H), dtype=torch.float32, device="cuda")
     L.moe_expert_ffn(x_d, 1, T, cfg.H, cfg.F, cfg.qtype, cfg.E, cfg.k, ids, w, None, cfg.E, pool, stride,

@@ -115,7 +115,10 @@ def test_argument_validation_happens_before_device_work(lib):
 
 def test_workspace_sizes(lib):
     # the decode workspace holds the route lists and the K-split gate/up partial sums
-    n1 = L.moe_expert_ffn_workspace(1, 2048, 768, 1, 128, 8)
-    n8 = L.moe_expert_ffn_workspace(8, 2048, 768, 1, 128, 8)
+    n1 = L.moe_expert_ffn_workspace(1, 2048, 768, 1, 0, 128, 8)
+    n8 = L.moe_expert_ffn_workspace(8, 2048, 768, 1, 0, 128, 8)
+    # above the decode limit: bf16 activations take the grouped-GEMM path (its own sizing)
+    assert L.moe_expert_ffn_workspace(512, 2048, 768, 1, 1, 128, 8) != \
+        L.moe_expert_ffn_workspace(512, 2048, 768, 1, 0, 128, 8)
     assert n8 > n1 > 0 and n8 % 256 == 0
     assert L.moe_stack_workspace(1024, 512, 0, 32, 8, 8, 0) > n8 // 100

@@ -41,7 +41,7 @@ def _rel(a, b):
 def test_noalloc_matches_workspace_entry_point_twice(qtype, H, F, E, k, T):
     cfg = synth.small_config(qtype, H=H, F=F, E=E, k=k, seed_cfg=990 + qtype)
     pool, stride = _pool(cfg)
-    ws_bytes = L.moe_expert_ffn_workspace(T, H, F, qtype, E, k)
+    ws_bytes = L.moe_expert_ffn_workspace(T, H, F, qtype, 0, E, k)
     assert ws_bytes <= L.MOE_NOALLOC_SCRATCH_MAX
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     rng = np.random.default_rng(qtype + 7)
@@ -65,7 +65,7 @@ def test_noalloc_matches_workspace_entry_point_twice(qtype, H, F, E, k, T):
 
 def test_noalloc_rejects_requests_beyond_its_array():
     # batch 32, top-8 of the DeepSeek-shaped layer needs ~11.5 MB of scratch > 8 MiB
-    need = L.moe_expert_ffn_workspace(32, 2048, 1408, 0, 64, 8)
+    need = L.moe_expert_ffn_workspace(32, 2048, 1408, 0, 0, 64, 8)
     assert need > L.MOE_NOALLOC_SCRATCH_MAX
     dummy = torch.zeros(16, dtype=torch.float32, device="cuda")
     with pytest.raises(L.MoeError) as ei:

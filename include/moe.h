@@ -272,6 +272,19 @@ int moe_expert_ffn_noalloc(const void *x, int xtype, int T, int H, int F, int qt
 int moe_combine(const float *partial, int T, int k, int H, const float *extra, float *y,
                 moe_stream_t s);
 
+/*
+ * moe_combine_rmsnorm — the combine of a stack layer plus the next layer's input:
+ *   y[t]  = extra[t] + sum_{j=0..k-1} partial[t][j]      (as moe_combine; k may be 0)
+ *   xn[t] = y[t] / sqrt(mean_h y[t][h]^2 + eps)          (RMS normalisation, unit weight)
+ * The pages put the expert FFN inside each transformer block (page 1, section 3.1) but
+ * fix no normalisation; the stacks here normalise each layer's input (pre-norm) so that
+ * every layer sees inputs of the unit scale the workloads draw.  y or xn may be NULL (not
+ * both); xn may not alias y or extra; y may alias extra.  One CTA per token, reductions in
+ * a fixed order (deterministic).
+ */
+int moe_combine_rmsnorm(const float *partial, int T, int k, int H, const float *extra, float *y,
+                        float *xn, float eps, moe_stream_t s);
+
 /* ------------------------------------------------------------ device status */
 
 /*

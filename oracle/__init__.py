@@ -204,6 +204,19 @@ def moe_layer(qtype: int, H: int, F: int, k: int, x: np.ndarray, w_router_bits: 
     return LayerResult(logits, ids, w, gap, y_exp, y)
 
 
+STACK_EPS = 1e-6
+
+
+def rmsnorm(h: np.ndarray, eps: float = STACK_EPS) -> np.ndarray:
+    """Per-row RMS normalisation with unit weight: h / sqrt(mean(h^2) + eps), fp64.
+
+    The stacks feed each layer's MoE FFN the normalised residual stream (pre-norm), so
+    that every layer sees inputs of unit scale; the pages fix no normalisation.
+    """
+    h = np.asarray(h, dtype=np.float64)
+    return h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps)
+
+
 def relative_error(y: np.ndarray, y_ref: np.ndarray) -> np.ndarray:
     """Per-token normwise error max_i |y_i - ref_i| / max_i |ref_i| (rows of [T][H])."""
     y = np.asarray(y, dtype=np.float64).reshape(y_ref.shape)

@@ -37,7 +37,7 @@ EXPORTED = [
     "moe_combine", "moe_device_status", "moe_stack_workspace", "moe_stack_create",
     "moe_stack_decode", "moe_stack_layer", "moe_stack_profile_get", "moe_stack_profile_reset",
     "moe_stack_destroy", "moe_debug_inject_fault", "moe_stack_set_profile",
-    "moe_expert_ffn_noalloc",
+    "moe_expert_ffn_noalloc", "moe_combine_rmsnorm",
 ]
 MOE_NOALLOC_SCRATCH_MAX = 8 << 20
 
@@ -129,6 +129,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_expert_ffn_noalloc": ([_vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _sz, _vp,
                                     _i, _vp, _vp], _i),
         "moe_combine": ([_vp, _i, _i, _i, _vp, _vp, _vp], _i),
+        "moe_combine_rmsnorm": ([_vp, _i, _i, _i, _vp, _vp, _vp, ctypes.c_float, _vp], _i),
         "moe_device_status": ([P(_i), _i], _i),
         "moe_stack_workspace": ([_i, _i, _i, _i, _i, _i, _i, P(_sz)], _i),
         "moe_stack_create": ([P(StackDesc), P(_vp)], _i),
@@ -286,6 +287,12 @@ def moe_expert_ffn_noalloc(x, xtype: int, T: int, H: int, F: int, qtype: int, E:
 
 def moe_combine(partial, T: int, k: int, H: int, extra, y, stream=None) -> None:
     _ck("moe_combine", load().moe_combine(_ptr(partial), T, k, H, _ptr(extra), _ptr(y), _stream(stream)))
+
+
+def moe_combine_rmsnorm(partial, T: int, k: int, H: int, extra, y, xn, eps: float = 1e-6,
+                        stream=None) -> None:
+    _ck("moe_combine_rmsnorm", load().moe_combine_rmsnorm(_ptr(partial), T, k, H, _ptr(extra), _ptr(y), _ptr(xn),
+                                                          eps, _stream(stream)))
 
 
 def moe_device_status(clear: bool = True) -> int:

@@ -496,6 +496,39 @@ __global__ void combine_kernel(const float4 *__restrict__ partial, int T, int k,
     }
 }
 
+// Combine + RMSNorm for the stack: one CTA per token.  y = extra + sum_j partial[j] (fixed
+// order), then xn = y / sqrt(mean(y^2) + eps) with a fixed-order block reduction.
+__global__ void __launch_bounds__(256) combine_norm_kernel(const float4 *__restrict__ partial, int k, int H4,
+                                                           const float4 *extra, float4 *y, float4 *xn,
+                                                           float eps) {
+    __shared__ float red[8];
+    const int t = blockIdx.x;
+    float ss = 0.f;
+    for (int h = threadIdx.x; h < H4; h += blockDim.x) {
+        float4 s = extra ? extra[(size_t)t * H4 + h] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const float4 v = partial[((size_t)t * k + j) * H4 + h];
+            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+        }
+        if (y) y[(size_t)t * H4 + h] = s;
+        ss += s.x * s.x + s.y * s.y + s.z * s.z + s.w * s.w;
+        if (xn) xn[(size_t)t * H4 + h] = s;  // scaled below
+    }
+    if (!xn) return;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
+    const float inv = 1.0f / sqrtf(tot / (float)(4 * H4) + eps);
+    for (int h = threadIdx.x; h < H4; h += blockDim.x) {
+        float4 v = xn[(size_t)t * H4 + h];
+        v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
+        xn[(size_t)t * H4 + h] = v;
+    }
+}
+
 template <typename Kern>
 int launch_unit_kernel(Kern kern, int grid, size_t smem, const FfnParams &p, cudaStream_t s) {
     if (grid <= 0) return MOE_OK;
@@ -616,6 +649,21 @@ extern "C" int moe_expert_ffn_workspace(int T, int H, int F, int qtype, int xtyp
     MOE_CHECK(xtype == MOE_F32 || xtype == MOE_BF16);
     MOE_CHECK(E >= 1 && E <= MOE_MAX_E && k >= 1 && k <= MOE_MAX_K);
     *bytes = moe_ffn_workspace_bytes(T, H, F, qtype, xtype, E, k);
+    return MOE_OK;
+}
+
+extern "C" int moe_combine_rmsnorm(const float *partial, int T, int k, int H, const float *extra, float *y,
+                                   float *xn, float eps, moe_stream_t s) {
+    MOE_CHECK(T >= 0 && k >= 0 && k <= 64 && H > 0 && H % 4 == 0 && eps >= 0.f);
+    if (T == 0) return MOE_OK;
+    MOE_CHECK(k == 0 || partial);
+    MOE_CHECK(y || xn);
+    MOE_CHECK(((uintptr_t)partial & 15) == 0 && ((uintptr_t)y & 15) == 0 && ((uintptr_t)extra & 15) == 0 &&
+              ((uintptr_t)xn & 15) == 0);
+    MOE_CHECK(!(xn && (xn == extra || xn == y)));
+    combine_norm_kernel<<<T, 256, 0, moe_cuda_stream(s)>>>((const float4 *)partial, k, H / 4,
+                                                           (const float4 *)extra, (float4 *)y, (float4 *)xn, eps);
+    MOE_TRY_CUDA(cudaGetLastError());
     return MOE_OK;
 }
 

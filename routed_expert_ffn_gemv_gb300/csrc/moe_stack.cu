@@ -15,7 +15,7 @@ namespace {
 inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct StackWs {
-    size_t ids, w, partial, table, hit, miss, hA, hB, ids_s, w_s, partial_s, tmp, ffn, total;
+    size_t ids, w, partial, table, hit, miss, hA, hB, xn, ids_s, w_s, partial_s, tmp, ffn, total;
     size_t ffn_bytes;
 };
 
@@ -30,6 +30,7 @@ StackWs stack_ws(int H, int F, int qtype, int E, int k, int T, int n_shared) {
     L.miss = off;      off = align256(off + (size_t)E * 4);
     L.hA = off;        off = align256(off + (size_t)T * H * 4);
     L.hB = off;        off = align256(off + (size_t)T * H * 4);
+    L.xn = off;        off = align256(off + (size_t)T * H * 4);
     const int ns = n_shared > 0 ? n_shared : 0;
     L.ids_s = off;     off = align256(off + (size_t)T * ns * 4);
     L.w_s = off;       off = align256(off + (size_t)T * ns * 4);
@@ -156,8 +157,13 @@ int ffn_call(moe_stack *st, const float *x, int T, int E, int k, const int32_t *
     return MOE_OK;
 }
 
-int layer_step(moe_stack *st, int layer, const float *x, float *y, int T, int32_t *ids_out,
-               float *w_out, cudaStream_t s) {
+// RMSNorm epsilon of the stack's pre-norm
+#define MOE_STACK_EPS 1e-6f
+
+// One layer: y = h + MoE(RMSNorm(h)).  norm_in: compute RMSNorm(h) here (else the previous
+// layer's combine left it in the xn buffer); norm_out: leave RMSNorm(y) in xn for the next.
+int layer_step(moe_stack *st, int layer, const float *h, float *y, int T, int32_t *ids_out,
+               float *w_out, cudaStream_t s, bool norm_in, bool norm_out) {
     const moe_stack_desc &d = st->d;
     const StackWs &L = st->L;
     int32_t *ids_d = (int32_t *)(st->ws + L.ids);
@@ -166,9 +172,15 @@ int layer_step(moe_stack *st, int layer, const float *x, float *y, int T, int32_
     int32_t *table = (int32_t *)(st->ws + L.table);
     int32_t *hit_d = (int32_t *)(st->ws + L.hit);
     int32_t *miss_d = (int32_t *)(st->ws + L.miss);
+    float *x = (float *)(st->ws + L.xn);
     int rc;
     EventPair ep{};
 
+    if (norm_in) {
+        if ((rc = moe_combine_rmsnorm(nullptr, T, 0, d.H, h, nullptr, x, MOE_STACK_EPS, (moe_stream_t)s)))
+            return rc;
+        st->prof.kernel_launches += 1;
+    }
     if ((rc = begin_timed(st, s, &ep))) return rc;
     if ((rc = moe_router_topk(x, MOE_F32, T, d.H, st->w_router[layer], st->bias[layer], d.E, d.k,
                               ids_d, w_d, nullptr, (moe_stream_t)s)))
@@ -244,7 +256,7 @@ int layer_step(moe_stack *st, int layer, const float *x, float *y, int T, int32_
             return rc;
     }
 
-    const float *extra = x;
+    const float *extra = h;
     if (d.n_shared > 0) {
         const void *spool = (const char *)d.shared_pool + (size_t)layer * d.n_shared * d.slot_bytes;
         int32_t *ids_s = (int32_t *)(st->ws + L.ids_s);
@@ -255,13 +267,15 @@ int layer_step(moe_stack *st, int layer, const float *x, float *y, int T, int32_
                            nullptr, 0, partial_s, d.n_shared, s)))
             return rc;
         if ((rc = begin_timed(st, s, &ep))) return rc;
-        if ((rc = moe_combine(partial_s, T, d.n_shared, d.H, x, tmp, (moe_stream_t)s))) return rc;
+        if ((rc = moe_combine(partial_s, T, d.n_shared, d.H, h, tmp, (moe_stream_t)s))) return rc;
         st->prof.kernel_launches += 1;
         if ((rc = end_timed(st, s, K_COMBINE, ep))) return rc;
         extra = tmp;
     }
     if ((rc = begin_timed(st, s, &ep))) return rc;
-    if ((rc = moe_combine(partial, T, d.k, d.H, extra, y, (moe_stream_t)s))) return rc;
+    if ((rc = moe_combine_rmsnorm(partial, T, d.k, d.H, extra, y, norm_out ? x : nullptr, MOE_STACK_EPS,
+                                  (moe_stream_t)s)))
+        return rc;
     st->prof.kernel_launches += 1;
     if ((rc = end_timed(st, s, K_COMBINE, ep))) return rc;
 
@@ -351,7 +365,7 @@ extern "C" int moe_stack_layer(moe_stack *st, int layer, const float *x_in, floa
     MOE_CHECK(T >= 1 && T <= st->d.max_T);
     cudaStream_t cs = moe_cuda_stream(s);
     st->last_stream = cs;
-    return layer_step(st, layer, x_in, y_out, T, ids_host_out, weights_host_out, cs);
+    return layer_step(st, layer, x_in, y_out, T, ids_host_out, weights_host_out, cs, true, false);
 }
 
 extern "C" int moe_stack_decode(moe_stack *st, const float *x_in, float *y_out, int T,
@@ -367,7 +381,8 @@ extern "C" int moe_stack_decode(moe_stack *st, const float *x_in, float *y_out, 
     for (int l = 0; l < L; ++l) {
         float *out = (l == L - 1) ? y_out : ((l & 1) ? hB : hA);
         const int rc = layer_step(st, l, cur, out, T, ids_host_out ? ids_host_out + l * per : nullptr,
-                                  weights_host_out ? weights_host_out + l * per : nullptr, cs);
+                                  weights_host_out ? weights_host_out + l * per : nullptr, cs, l == 0,
+                                  l + 1 < L);
         if (rc) return rc;
         cur = out;
     }

@@ -196,6 +196,24 @@ def test_combine_order_and_extra():
     assert np.array_equal(y.cpu().numpy(), ref)
 
 
+def test_combine_rmsnorm_matches_fp64():
+    rng = np.random.default_rng(15)
+    T, k, H = 5, 3, 1024
+    p = rng.standard_normal((T, k, H), dtype=np.float32)
+    e = (rng.standard_normal((T, H)) * 3).astype(np.float32)
+    y = torch.empty((T, H), dtype=torch.float32, device=dev())
+    xn = torch.empty((T, H), dtype=torch.float32, device=dev())
+    L.moe_combine_rmsnorm(to_dev(p), T, k, H, to_dev(e), y, xn)
+    ref_y = e.copy()
+    for j in range(k):
+        ref_y = ref_y + p[:, j]
+    assert np.array_equal(y.cpu().numpy(), ref_y)
+    np.testing.assert_allclose(xn.cpu().numpy(), oracle.rmsnorm(ref_y.astype(np.float64)), rtol=2e-6, atol=1e-6)
+    # k = 0 and no y: normalise the extra only
+    L.moe_combine_rmsnorm(None, T, 0, H, to_dev(e), None, xn)
+    np.testing.assert_allclose(xn.cpu().numpy(), oracle.rmsnorm(e.astype(np.float64)), rtol=2e-6, atol=1e-6)
+
+
 # ------------------------------------------------------------------------------------ slot pool
 
 class PoolFixture:

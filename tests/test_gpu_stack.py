@@ -1,6 +1,7 @@
 """Stack-level parity on the GPU: every layer's routing (bit-exact ids), MoE output
 (<= 2e-3 normwise against the fp64 oracle) and slot-pool assignment (bit-exact against
-the LRU simulator), with the oracle's hidden state fed to each layer (teacher forcing)."""
+the LRU simulator), with the oracle's hidden state fed to each layer (teacher forcing).
+A stack layer is h -> h + MoE(RMSNorm(h))."""
 import numpy as np
 import pytest
 
@@ -48,7 +49,8 @@ class Checker:
         self.stack.layer(layer, x_d, y_d, ids, w)
         torch.cuda.synchronize()
         delta = y_d.cpu().numpy().astype(np.float64) - x32.astype(np.float64)
-        x64 = x32.astype(np.float64)
+        h64 = x32.astype(np.float64)
+        x64 = oracle.rmsnorm(h64)          # the layer's MoE input (pre-norm)
         res = layer_oracle(cfg, layer, x64)
         m = ids_match(ids, res.logits, res.ids, cfg.k)
         assert all(v is not False for v in m), (layer, m, ids, res.ids)
@@ -73,7 +75,7 @@ class Checker:
             c = self.stack.caches[g]
             for e, s in res_sim.items():
                 assert L.moe_cache_lookup(c, layer, e) == s, (layer, e)
-        return x64 + res.y
+        return h64 + res.y
 
 
 def run_steps(stack, cfg, T, steps, step0=0):

@@ -333,3 +333,17 @@ def test_block_sizes():
     assert synth.config(1).expert_bytes == 1671168
     assert synth.config(2).expert_bytes == 2949120
     assert synth.config(3).expert_bytes == 9191424
+
+
+def test_rmsnorm_closed_forms():
+    # [3, 4, 0]: mean of squares 25/3
+    got = oracle.rmsnorm(np.array([[3.0, 4.0, 0.0]]), eps=0.0)
+    np.testing.assert_allclose(got, [[3 / np.sqrt(25 / 3), 4 / np.sqrt(25 / 3), 0.0]], rtol=1e-15)
+    rng = np.random.default_rng(14)
+    h = rng.standard_normal((4, 64)) * 7.0
+    xn = oracle.rmsnorm(h, eps=0.0)
+    np.testing.assert_allclose(np.mean(xn * xn, axis=1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(oracle.rmsnorm(h * 1e3, eps=0.0), xn, rtol=1e-13)   # scale invariant
+    # eps: a constant vector c gives c / sqrt(c^2 + eps)
+    c = 0.01
+    np.testing.assert_allclose(oracle.rmsnorm(np.full((1, 8), c), eps=1e-6), c / np.sqrt(c * c + 1e-6), rtol=1e-14)

@@ -139,6 +139,11 @@ typedef struct {
     const void *const *host_images;   /* host array [n_layers * n_experts] of pinned slot
                                          images (moe_pack_expert output), layer-major */
     moe_stream_t copy_stream;         /* stream for miss uploads (caller-owned) */
+    int device_managed;               /* 0: LRU on the host (moe_cache_ensure); 1: LRU state in
+                                         device memory, run on the GPU by moe_cache_plan */
+    void *device_state;               /* device_managed: moe_cache_state_bytes() bytes of device
+                                         memory, caller-owned, initialised by moe_cache_create */
+    size_t device_state_bytes;
 } moe_cache_desc;
 
 typedef struct moe_cache moe_cache; /* opaque, library-owned host object */
@@ -180,6 +185,31 @@ int moe_cache_create(const moe_cache_desc *desc, moe_cache **out);
 int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host, int n_tokens, int k,
                      int32_t *slots_host_out, int *n_miss_out, uint8_t *miss_mask_host_out,
                      int32_t *d_slot_table, moe_stream_t s);
+
+/*
+ * Device-managed pools (desc.device_managed = 1).  The same pool and the same rules as
+ * moe_cache_ensure (page 4's LRU slot pool; page 1 section 3.2's "least-recently-used,
+ * not active" victim), with the bookkeeping on the GPU so that a decode step needs no
+ * host round trip per layer: the ids never leave the device.
+ *
+ * moe_cache_state_bytes — device bytes of the state of a pool (slot table, recency list,
+ * owners, host image addresses, statistics); the caller allocates it.
+ *
+ * moe_cache_plan — stream-ordered on s, one CTA: reads the layer's routed ids d_ids
+ * [n_tokens][k] (device), applies the LRU rules to the device state and writes
+ *   d_table_out [n_experts]  slot of each expert of the layer (-1: not resident),
+ *   d_fill_src_out [n_experts] for each expert that missed, the address of its pinned
+ *                  host image (the slot it was given must be filled from there), else 0.
+ * It moves no weight bytes: moe_expert_ffn_fill reads the missed experts from host memory
+ * and writes them into their slots while computing.  Capacity overflow or an id out of
+ * range is recorded in the device status word (moe_device_status); the layer's table is
+ * then all -1 and nothing is read.  Host-side ensure/wait/release are invalid on a
+ * device-managed pool; moe_cache_stats_get, moe_cache_lookup and moe_cache_reset work on
+ * both kinds (synchronously for this one).
+ */
+int moe_cache_state_bytes(int n_layers, int n_experts, int n_slots, size_t *bytes);
+int moe_cache_plan(moe_cache *c, int layer, const int32_t *d_ids, int n_tokens, int k,
+                   int32_t *d_table_out, uint64_t *d_fill_src_out, moe_stream_t s);
 
 /* moe_cache_wait_uploads — stream s waits for the uploads issued by the last ensure. */
 int moe_cache_wait_uploads(moe_cache *c, moe_stream_t s);
@@ -233,6 +263,20 @@ int moe_expert_ffn(const void *x, int xtype, int T, int H, int F, int qtype, int
                    int n_slots, const void *pool, size_t slot_bytes,
                    const int32_t *expert_subset, int n_subset, float *partial,
                    void *workspace, size_t ws_bytes, moe_stream_t s);
+
+/*
+ * moe_expert_ffn_fill — moe_expert_ffn over every routed expert, for a device-managed pool:
+ * each expert e with d_fill_src[e] != 0 (set by moe_cache_plan for the experts that
+ * missed) has its weights read from that pinned host image over the CPU-GPU link and
+ * written into its slot (d_slot_table[e]) by the same kernels that compute with them,
+ * so the upload and the compute overlap and no copy engine is involved; other experts
+ * are read from their slots.  Decode path only (T <= MOE_DECODE_MAX_T or fp32 x);
+ * otherwise MOE_ERR_UNSUPPORTED.  The pool must be the one the plan was made for.
+ */
+int moe_expert_ffn_fill(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
+                        const int32_t *ids, const float *weights, const int32_t *d_slot_table,
+                        int n_slots, void *pool, size_t slot_bytes, const uint64_t *d_fill_src,
+                        float *partial, void *workspace, size_t ws_bytes, moe_stream_t s);
 
 /* Workspace bytes of moe_expert_ffn for these sizes (it depends on the path taken). */
 int moe_expert_ffn_workspace(int T, int H, int F, int qtype, int xtype, int E, int k, size_t *bytes);
@@ -316,6 +360,12 @@ typedef struct {
     int overlap;                      /* 1: hit experts run while misses upload */
     int profile;                      /* 0: off; 1: events around the gate/up GEMV only;
                                          2: events around every kernel (moe_stack_profile) */
+    int device_managed;               /* 1: the caches are device-managed; each layer runs
+                                         router -> moe_cache_plan -> moe_expert_ffn_fill ->
+                                         combine on the stream, with no host round trip */
+    int use_graph;                    /* device_managed only: moe_stack_decode captures the
+                                         whole step once per batch size into a CUDA graph and
+                                         replays it (inputs/outputs copied in and out) */
 } moe_stack_desc;
 
 typedef struct moe_stack moe_stack;

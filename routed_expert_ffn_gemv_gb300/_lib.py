@@ -37,7 +37,8 @@ EXPORTED = [
     "moe_combine", "moe_device_status", "moe_stack_workspace", "moe_stack_create",
     "moe_stack_decode", "moe_stack_layer", "moe_stack_profile_get", "moe_stack_profile_reset",
     "moe_stack_destroy", "moe_debug_inject_fault", "moe_stack_set_profile",
-    "moe_expert_ffn_noalloc", "moe_combine_rmsnorm",
+    "moe_expert_ffn_noalloc", "moe_combine_rmsnorm", "moe_cache_state_bytes", "moe_cache_plan",
+    "moe_expert_ffn_fill",
 ]
 MOE_NOALLOC_SCRATCH_MAX = 8 << 20
 
@@ -56,7 +57,8 @@ _i = ctypes.c_int
 class CacheDesc(ctypes.Structure):
     _fields_ = [("qtype", _i), ("H", _i), ("F", _i), ("n_layers", _i), ("n_experts", _i),
                 ("first_layer", _i), ("n_slots", _i), ("slot_bytes", _sz), ("device_pool", _vp),
-                ("host_images", ctypes.POINTER(_vp)), ("copy_stream", _vp)]
+                ("host_images", ctypes.POINTER(_vp)), ("copy_stream", _vp), ("device_managed", _i),
+                ("device_state", _vp), ("device_state_bytes", _sz)]
 
 
 class CacheStats(ctypes.Structure):
@@ -77,7 +79,8 @@ class StackDesc(ctypes.Structure):
                 ("n_shared", _i), ("w_router", ctypes.POINTER(_vp)), ("bias", ctypes.POINTER(_vp)),
                 ("n_groups", _i), ("caches", ctypes.POINTER(_vp)), ("resident_pool", _vp),
                 ("shared_pool", _vp), ("slot_bytes", _sz), ("max_T", _i), ("workspace", _vp),
-                ("ws_bytes", _sz), ("overlap", _i), ("profile", _i)]
+                ("ws_bytes", _sz), ("overlap", _i), ("profile", _i), ("device_managed", _i),
+                ("use_graph", _i)]
 
 
 class StackProfile(ctypes.Structure):
@@ -130,6 +133,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                     _i, _vp, _vp], _i),
         "moe_combine": ([_vp, _i, _i, _i, _vp, _vp, _vp], _i),
         "moe_combine_rmsnorm": ([_vp, _i, _i, _i, _vp, _vp, _vp, ctypes.c_float, _vp], _i),
+        "moe_cache_state_bytes": ([_i, _i, _i, P(_sz)], _i),
+        "moe_cache_plan": ([_vp, _i, _vp, _i, _i, _vp, _vp, _vp], _i),
+        "moe_expert_ffn_fill": ([_vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _sz, _vp, _vp, _vp,
+                                 _sz, _vp], _i),
         "moe_device_status": ([P(_i), _i], _i),
         "moe_stack_workspace": ([_i, _i, _i, _i, _i, _i, _i, P(_sz)], _i),
         "moe_stack_create": ([P(StackDesc), P(_vp)], _i),
@@ -224,6 +231,27 @@ def moe_cache_ensure_status(cache: int, layer: int, ids_host_ptr: int, n_tokens:
     n_miss = _i()
     return load().moe_cache_ensure(cache, layer, ids_host_ptr, n_tokens, k, slots_host_ptr,
                                    ctypes.byref(n_miss), None, _ptr(d_slot_table), _stream(stream))
+
+
+def moe_cache_state_bytes(n_layers: int, n_experts: int, n_slots: int) -> int:
+    out = _sz()
+    _ck("moe_cache_state_bytes", load().moe_cache_state_bytes(n_layers, n_experts, n_slots, ctypes.byref(out)))
+    return out.value
+
+
+def moe_cache_plan(cache: int, layer: int, d_ids, n_tokens: int, k: int, d_table, d_fill_src,
+                   stream=None) -> None:
+    _ck("moe_cache_plan", load().moe_cache_plan(cache, layer, _ptr(d_ids), n_tokens, k, _ptr(d_table),
+                                                _ptr(d_fill_src), _stream(stream)))
+
+
+def moe_expert_ffn_fill(x, xtype: int, T: int, H: int, F: int, qtype: int, E: int, k: int, ids, weights,
+                        d_slot_table, n_slots: int, pool, slot_bytes: int, d_fill_src, partial, workspace,
+                        ws_bytes: int, stream=None) -> None:
+    _ck("moe_expert_ffn_fill",
+        load().moe_expert_ffn_fill(_ptr(x), xtype, T, H, F, qtype, E, k, _ptr(ids), _ptr(weights),
+                                   _ptr(d_slot_table), n_slots, _ptr(pool), slot_bytes, _ptr(d_fill_src),
+                                   _ptr(partial), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def moe_cache_wait_uploads(cache: int, stream=None) -> None:

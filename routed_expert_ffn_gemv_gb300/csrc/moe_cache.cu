@@ -66,7 +66,204 @@ void reset_state(moe_cache *c) {
     c->st = moe_cache_stats{};
 }
 
+// ------------------------------------------------------------------ device-managed state
+//
+// The recency order is an intrusive doubly linked list over the occupied slots (head =
+// least recently used, tail = most recent).  Taking hits in ascending id order to the
+// tail, then filling misses (ascending id) from the lowest free slot or else from the
+// first list entry not owned by this request, is the same rule as the host pool's
+// stamps: list order is stamp order.  Slots are only freed by a reset, so the lowest
+// free slot is the fill count.
+
+struct DevHeader {
+    int32_t n_filled, head, tail, pad;
+    uint64_t queries[2], hits[2], misses[2], evictions, h2d_bytes, route_queries, route_hits, ensure_calls;
+};
+
+struct DevLayout {
+    size_t slot_of, owner, prev, next, img, total;
+};
+
+DevLayout dev_layout(int n_layers, int E, int n_slots) {
+    DevLayout L;
+    const size_t nk = (size_t)n_layers * E;
+    size_t o = 256;
+    L.slot_of = o; o += (nk * 4 + 15) / 16 * 16;
+    L.owner = o;   o += ((size_t)n_slots * 4 + 15) / 16 * 16;
+    L.prev = o;    o += ((size_t)n_slots * 4 + 15) / 16 * 16;
+    L.next = o;    o += ((size_t)n_slots * 4 + 15) / 16 * 16;
+    L.img = o;     o += nk * 8;
+    L.total = (o + 255) / 256 * 256;
+    return L;
+}
+
+#define MOE_PLAN_MAX_SLOTS 12288
+
+__global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, DevLayout L, int ll, int E,
+                                                   int n_slots, const int32_t *__restrict__ ids, int n_tokens,
+                                                   int k, uint64_t image_bytes, int32_t *__restrict__ table_out,
+                                                   uint64_t *__restrict__ src_out, int *status) {
+    extern __shared__ int32_t sm[];
+    int32_t *owner = sm, *prev = sm + n_slots, *next = sm + 2 * n_slots, *slot_l = sm + 3 * n_slots;
+    unsigned char *want = (unsigned char *)(slot_l + E), *miss = want + E;
+    __shared__ int abort_flag;
+    DevHeader *hd = (DevHeader *)state;
+    int32_t *g_slot_of = (int32_t *)(state + L.slot_of);
+    int32_t *g_owner = (int32_t *)(state + L.owner);
+    int32_t *g_prev = (int32_t *)(state + L.prev);
+    int32_t *g_next = (int32_t *)(state + L.next);
+    const uint64_t *g_img = (const uint64_t *)(state + L.img);
+    const int key0 = ll * E, n_ids = n_tokens * k;
+    for (int i = threadIdx.x; i < n_slots; i += blockDim.x) {
+        owner[i] = g_owner[i];
+        prev[i] = g_prev[i];
+        next[i] = g_next[i];
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        slot_l[e] = g_slot_of[key0 + e];
+        want[e] = 0;
+        miss[e] = 0;
+    }
+    if (threadIdx.x == 0) abort_flag = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_ids; i += blockDim.x) {
+        const int e = ids[i];
+        if (e < 0 || e >= E) {
+            moe_set_status(status, MOE_ERR_INVALID);
+            abort_flag = 1;
+        } else {
+            want[e] = 1;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !abort_flag) {
+        int nd = 0;
+        for (int e = 0; e < E; ++e) nd += want[e];
+        if (nd > n_slots) {
+            moe_set_status(status, MOE_ERR_CAPACITY);
+            abort_flag = 1;
+        } else {
+            int head = hd->head, tail = hd->tail, filled = hd->n_filled;
+            auto unlink = [&](int s) {
+                const int p = prev[s], n = next[s];
+                if (p >= 0) next[p] = n; else head = n;
+                if (n >= 0) prev[n] = p; else tail = p;
+            };
+            auto append = [&](int s) {
+                prev[s] = tail;
+                next[s] = -1;
+                if (tail >= 0) next[tail] = s; else head = s;
+                tail = s;
+            };
+            int n_hit = 0, n_miss = 0, n_evict = 0, route_hits = 0;
+            for (int e = 0; e < E; ++e) {           // hits, ascending id: most recent
+                if (!want[e] || slot_l[e] < 0) continue;
+                unlink(slot_l[e]);
+                append(slot_l[e]);
+                ++n_hit;
+            }
+            for (int e = 0; e < E; ++e) {           // misses, ascending id
+                if (!want[e] || slot_l[e] >= 0) continue;
+                int s;
+                if (filled < n_slots) {
+                    s = filled++;
+                } else {
+                    s = head;
+                    while (s >= 0) {
+                        const int o = owner[s];
+                        if (!(o >= key0 && o < key0 + E && want[o - key0])) break;
+                        s = next[s];
+                    }
+                    if (s < 0) { moe_set_status(status, MOE_ERR_CAPACITY); abort_flag = 1; break; }
+                    unlink(s);
+                    const int o = owner[s];
+                    if (o >= key0 && o < key0 + E) slot_l[o - key0] = -1;
+                    else if (o >= 0) g_slot_of[o] = -1;
+                    ++n_evict;
+                }
+                append(s);
+                owner[s] = key0 + e;
+                slot_l[e] = s;
+                miss[e] = 1;
+                ++n_miss;
+            }
+            for (int i = 0; i < n_ids; ++i) route_hits += !miss[ids[i]];
+            hd->head = head;
+            hd->tail = tail;
+            hd->n_filled = filled;
+            const int b = n_tokens <= 8 ? 0 : 1;
+            hd->queries[b] += n_hit + n_miss;
+            hd->hits[b] += n_hit;
+            hd->misses[b] += n_miss;
+            hd->evictions += n_evict;
+            hd->h2d_bytes += (uint64_t)n_miss * image_bytes;
+            hd->route_queries += n_ids;
+            hd->route_hits += route_hits;
+            hd->ensure_calls += 1;
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_slots; i += blockDim.x) {
+        g_owner[i] = owner[i];
+        g_prev[i] = prev[i];
+        g_next[i] = next[i];
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        g_slot_of[key0 + e] = slot_l[e];
+        table_out[e] = abort_flag ? -1 : slot_l[e];
+        src_out[e] = (!abort_flag && miss[e]) ? g_img[key0 + e] : 0ull;
+    }
+}
+
+int dev_state_init(moe_cache *c) {
+    const moe_cache_desc &d = c->d;
+    const DevLayout L = dev_layout(d.n_layers, d.n_experts, d.n_slots);
+    std::vector<uint8_t> h(L.total, 0);
+    DevHeader *hd = (DevHeader *)h.data();
+    hd->n_filled = 0;
+    hd->head = -1;
+    hd->tail = -1;
+    const size_t nk = (size_t)d.n_layers * d.n_experts;
+    int32_t *slot_of = (int32_t *)(h.data() + L.slot_of);
+    for (size_t i = 0; i < nk; ++i) slot_of[i] = -1;
+    int32_t *owner = (int32_t *)(h.data() + L.owner), *prev = (int32_t *)(h.data() + L.prev),
+            *next = (int32_t *)(h.data() + L.next);
+    for (int s = 0; s < d.n_slots; ++s) owner[s] = prev[s] = next[s] = -1;
+    uint64_t *img = (uint64_t *)(h.data() + L.img);
+    for (size_t i = 0; i < nk; ++i) img[i] = (uint64_t)(uintptr_t)c->images[i];
+    MOE_TRY_CUDA(cudaMemcpy(d.device_state, h.data(), L.total, cudaMemcpyHostToDevice));
+    return MOE_OK;
+}
+
 }  // namespace
+
+extern "C" int moe_cache_state_bytes(int n_layers, int n_experts, int n_slots, size_t *bytes) {
+    MOE_CHECK(bytes && n_layers >= 1 && n_experts >= 1 && n_experts <= MOE_MAX_E && n_slots >= 1);
+    *bytes = dev_layout(n_layers, n_experts, n_slots).total;
+    return MOE_OK;
+}
+
+extern "C" int moe_cache_plan(moe_cache *c, int layer, const int32_t *d_ids, int n_tokens, int k,
+                              int32_t *d_table_out, uint64_t *d_fill_src_out, moe_stream_t s) {
+    MOE_CHECK(c && c->d.device_managed && d_ids && d_table_out && d_fill_src_out);
+    MOE_CHECK(n_tokens >= 1 && n_tokens <= MOE_DECODE_MAX_T && k >= 1 && k <= MOE_MAX_K);
+    const moe_cache_desc &d = c->d;
+    const int ll = layer - d.first_layer;
+    MOE_CHECK(ll >= 0 && ll < d.n_layers);
+    const DevLayout L = dev_layout(d.n_layers, d.n_experts, d.n_slots);
+    const size_t smem = (size_t)3 * d.n_slots * 4 + (size_t)d.n_experts * 4 + 2 * (size_t)d.n_experts;
+    static bool attr_set = false;
+    if (!attr_set) {
+        MOE_TRY_CUDA(cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          3 * MOE_PLAN_MAX_SLOTS * 4 + MOE_MAX_E * 6));
+        attr_set = true;
+    }
+    plan_kernel<<<1, 256, smem, moe_cuda_stream(s)>>>((uint8_t *)d.device_state, L, ll, d.n_experts, d.n_slots,
+                                                      d_ids, n_tokens, k, c->image_bytes, d_table_out,
+                                                      d_fill_src_out, moe_status_word_device_ptr());
+    MOE_TRY_CUDA(cudaGetLastError());
+    return MOE_OK;
+}
 
 int moe_write_ints(int32_t *const dst[3], const int n[3], const int32_t *const src[3], cudaStream_t s) {
     IntPayload pay;
@@ -101,10 +298,24 @@ extern "C" int moe_cache_create(const moe_cache_desc *desc, moe_cache **out) {
         if (cudaPointerGetAttributes(&attr, p) != cudaSuccess || attr.type != cudaMemoryTypeHost)
             return MOE_ERR_INVALID;  // not pinned (page-locked) host memory
     }
+    if (d.device_managed) {
+        MOE_CHECK(d.n_slots <= MOE_PLAN_MAX_SLOTS);
+        MOE_CHECK(d.device_state && ((uintptr_t)d.device_state % 256) == 0);
+        MOE_CHECK(d.device_state_bytes >= dev_layout(d.n_layers, d.n_experts, d.n_slots).total);
+        if (cudaPointerGetAttributes(&attr, d.device_state) != cudaSuccess || attr.type != cudaMemoryTypeDevice)
+            return MOE_ERR_INVALID;
+    }
     moe_cache *c = new moe_cache();
     c->d = d;
     c->image_bytes = img;
     c->images.assign(d.host_images, d.host_images + n_img);
+    if (d.device_managed) {
+        const int rc = dev_state_init(c);
+        if (rc != MOE_OK) {
+            delete c;
+            return rc;
+        }
+    }
     c->slot_of.assign(n_img, -1);
     c->owner.assign(d.n_slots, -1);
     c->stamp.assign(d.n_slots, 0);
@@ -128,6 +339,7 @@ extern "C" int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host
                                 int32_t *slots_host_out, int *n_miss_out, uint8_t *miss_mask_host_out,
                                 int32_t *d_slot_table, moe_stream_t s) {
     MOE_CHECK(c && ids_host && slots_host_out && n_miss_out);
+    MOE_CHECK(!c->d.device_managed);
     MOE_CHECK(n_tokens >= 0 && n_tokens <= MOE_DECODE_MAX_T && k >= 1 && k <= MOE_MAX_K);
     const moe_cache_desc &d = c->d;
     const int E = d.n_experts;
@@ -254,13 +466,13 @@ extern "C" int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host
 }
 
 extern "C" int moe_cache_wait_uploads(moe_cache *c, moe_stream_t s) {
-    MOE_CHECK(c);
+    MOE_CHECK(c && !c->d.device_managed);
     if (c->upload_pending) MOE_TRY_CUDA(cudaStreamWaitEvent(moe_cuda_stream(s), c->upload_done, 0));
     return MOE_OK;
 }
 
 extern "C" int moe_cache_release(moe_cache *c, moe_stream_t s) {
-    MOE_CHECK(c);
+    MOE_CHECK(c && !c->d.device_managed);
     if (c->last_slots.empty()) return MOE_OK;
     const int ev = c->ring_next;
     MOE_TRY_CUDA(cudaEventRecord(c->ring[ev], moe_cuda_stream(s)));
@@ -272,12 +484,34 @@ extern "C" int moe_cache_release(moe_cache *c, moe_stream_t s) {
 
 extern "C" int moe_cache_stats_get(const moe_cache *c, moe_cache_stats *out) {
     MOE_CHECK(c && out);
+    if (c->d.device_managed) {
+        DevHeader h;
+        MOE_TRY_CUDA(cudaDeviceSynchronize());
+        MOE_TRY_CUDA(cudaMemcpy(&h, c->d.device_state, sizeof h, cudaMemcpyDeviceToHost));
+        moe_cache_stats st{};
+        for (int b = 0; b < 2; ++b) {
+            st.queries[b] = h.queries[b];
+            st.hits[b] = h.hits[b];
+            st.misses[b] = h.misses[b];
+        }
+        st.evictions = h.evictions;
+        st.h2d_bytes = h.h2d_bytes;
+        st.route_queries = h.route_queries;
+        st.route_hits = h.route_hits;
+        st.ensure_calls = h.ensure_calls;
+        *out = st;
+        return MOE_OK;
+    }
     *out = c->st;
     return MOE_OK;
 }
 
 extern "C" int moe_cache_reset(moe_cache *c) {
     MOE_CHECK(c);
+    if (c->d.device_managed) {
+        MOE_TRY_CUDA(cudaDeviceSynchronize());
+        return dev_state_init(c);
+    }
     // wait for in-flight uploads and readers so that no copy lands in a slot reused later
     MOE_TRY_CUDA(cudaStreamSynchronize(moe_cuda_stream(c->d.copy_stream)));
     for (int i = 0; i < MOE_EVENT_RING; ++i) MOE_TRY_CUDA(cudaEventSynchronize(c->ring[i]));
@@ -298,6 +532,16 @@ extern "C" int moe_cache_lookup(const moe_cache *c, int layer, int expert) {
     if (!c) return -1;
     const int ll = layer - c->d.first_layer;
     if (ll < 0 || ll >= c->d.n_layers || expert < 0 || expert >= c->d.n_experts) return -1;
+    if (c->d.device_managed) {
+        const DevLayout L = dev_layout(c->d.n_layers, c->d.n_experts, c->d.n_slots);
+        int32_t v = -1;
+        if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+        if (cudaMemcpy(&v, (const uint8_t *)c->d.device_state + L.slot_of +
+                               ((size_t)ll * c->d.n_experts + expert) * 4,
+                       4, cudaMemcpyDeviceToHost) != cudaSuccess)
+            return -1;
+        return v;
+    }
     return c->slot_of[(size_t)ll * c->d.n_experts + expert];
 }
 
@@ -322,6 +566,8 @@ const void *moe_cache_pool(const moe_cache *c, int *n_slots) {
     if (n_slots) *n_slots = c ? c->d.n_slots : 0;
     return c ? c->d.device_pool : nullptr;
 }
+
+bool moe_cache_is_device_managed(const moe_cache *c) { return c && c->d.device_managed; }
 
 int moe_cache_layer_range(const moe_cache *c, int *first_layer, int *n_layers) {
     MOE_CHECK(c && first_layer && n_layers);

@@ -96,6 +96,15 @@ int moe_expert_ffn_impl(const void *x, int xtype, int T, int H, int F, int qtype
                         void *workspace, size_t ws_bytes, cudaStream_t s,
                         const moe_ffn_timing *timing);
 
+// moe_expert_ffn_impl plus the fill sources (device [E] pinned-host image addresses of the
+// experts whose slots the kernels fill while computing; NULL: none).
+int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
+                        const int32_t *ids, const float *weights, const int32_t *d_slot_table,
+                        int n_slots, const void *pool, size_t slot_bytes,
+                        const int32_t *expert_subset, int n_subset, const uint64_t *d_fill_src,
+                        float *partial, void *workspace, size_t ws_bytes, cudaStream_t s,
+                        const moe_ffn_timing *timing);
+
 // Writes up to three small int32 arrays (<= 256 values each) on stream s with one launch
 // (values travel as kernel parameters, so no host staging buffer outlives the call).
 int moe_write_ints(int32_t *const dst[3], const int n[3], const int32_t *const src[3], cudaStream_t s);
@@ -103,6 +112,7 @@ int moe_write_ints(int32_t *const dst[3], const int n[3], const int32_t *const s
 // Pool base and slot count of a cache; the layer range of its group.
 const void *moe_cache_pool(const moe_cache *c, int *n_slots);
 int moe_cache_layer_range(const moe_cache *c, int *first_layer, int *n_layers);
+bool moe_cache_is_device_managed(const moe_cache *c);
 
 size_t moe_decode_workspace_bytes(int T, int H, int F, int qtype, int E, int k);
 // Workspace of moe_expert_ffn for these sizes (decode GEMV or prefill grouped GEMM path).

@@ -253,7 +253,30 @@ struct FfnParams {
     float *partial;
     int *status;
     int ntok;          // activation rows staged per pass (<= GV_TOK)
+    const unsigned long long *fill_src;  // [E]: pinned host image of an expert to fill, or 0
 };
+
+// Fill path of a unit whose expert missed: its bytes come from the expert's pinned host
+// image over the CPU-GPU link (16-byte loads by every thread) and are written both to the
+// unit's shared-memory stage and through to the expert's slot, so the slot is filled by
+// the kernels that use it.  Same byte ranges as issue_unit_copies.
+template <int QT>
+__device__ void fill_unit(const uint8_t *src_mat, uint8_t *dst_mat, int R, int K, int g, int kb0, int nbr,
+                          unsigned char *smem, const UnitSmem &L) {
+    const int QB = QT == MOE_Q8_0 ? 1024 : 512;
+    const int SB = 32 * moe_scale_entry_bytes(QT);
+    const int PPB = QT == MOE_Q8_0 ? 2 : 1;
+    const size_t qoff = moe_piece_offset(QT, K, g, kb0 * PPB);
+    const size_t soff = moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, g, kb0);
+    const int nq = nbr * QB / 16, ns = nbr * SB / 16;
+    for (int i = threadIdx.x; i < nq + ns; i += GV_THREADS) {
+        const bool q = i < nq;
+        const size_t off = q ? qoff + (size_t)i * 16 : soff + (size_t)(i - nq) * 16;
+        const uint4 v = __ldcs((const uint4 *)(src_mat + off));
+        *(uint4 *)(smem + (q ? L.quant + (size_t)i * 16 : L.scale + (size_t)(i - nq) * 16)) = v;
+        __stcs((uint4 *)(dst_mat + off), v);
+    }
+}
 
 template <int XT>
 __device__ __forceinline__ float load_x(const void *x, size_t i) {
@@ -283,7 +306,15 @@ __global__ void __launch_bounds__(GV_THREADS) gateup_kernel(FfnParams p) {
     const int K = p.H, nbr = (K / 32) / p.KS, kb0 = ks * nbr, Kr = nbr * 32;
     const UnitSmem L = unit_smem(QT, nbr, p.ntok);
     const uint8_t *mat = p.pool + (size_t)slot * p.slot_bytes + moe_expert_matrix_offset(QT, p.H, p.F, m);
-    if (threadIdx.x == 0) issue_unit_copies<QT>(mat, p.F, K, g, kb0, nbr, smem, L);
+    const uint8_t *fill = p.fill_src ? (const uint8_t *)p.fill_src[e] : nullptr;
+    bool ready = false, ok = true;
+    if (fill) {
+        // visible to every warp after the first __syncthreads of the token loop
+        fill_unit<QT>(fill + moe_expert_matrix_offset(QT, p.H, p.F, m), (uint8_t *)mat, p.F, K, g, kb0, nbr, smem, L);
+        ready = true;
+    } else if (threadIdx.x == 0) {
+        issue_unit_copies<QT>(mat, p.F, K, g, kb0, nbr, smem, L);
+    }
     __syncthreads();
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -295,7 +326,6 @@ __global__ void __launch_bounds__(GV_THREADS) gateup_kernel(FfnParams p) {
     const int pos0 = ints[ws_aoff_off(p.E) + a];
     const int n_e = ints[ws_aoff_off(p.E) + a + 1] - pos0;
     const int *routes = ints + ws_routes_off(p.E);
-    bool ready = false, ok = true;
 
     for (int tg = 0; tg < n_e; tg += GV_TOK) {
         const int nt = min(GV_TOK, n_e - tg), ntp = pow2_tokens(nt);
@@ -353,7 +383,14 @@ __global__ void __launch_bounds__(GV_THREADS) down_kernel(FfnParams p) {
     const int K = p.F, nbr = K / 32, Kr = K;
     const UnitSmem L = unit_smem(QT, nbr, p.ntok);
     const uint8_t *mat = p.pool + (size_t)slot * p.slot_bytes + moe_expert_matrix_offset(QT, p.H, p.F, 2);
-    if (threadIdx.x == 0) issue_unit_copies<QT>(mat, p.H, K, g, 0, nbr, smem, L);
+    const uint8_t *fill = p.fill_src ? (const uint8_t *)p.fill_src[e] : nullptr;
+    bool ready = false, ok = true;
+    if (fill) {
+        fill_unit<QT>(fill + moe_expert_matrix_offset(QT, p.H, p.F, 2), (uint8_t *)mat, p.H, K, g, 0, nbr, smem, L);
+        ready = true;
+    } else if (threadIdx.x == 0) {
+        issue_unit_copies<QT>(mat, p.H, K, g, 0, nbr, smem, L);
+    }
     __syncthreads();
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -365,7 +402,6 @@ __global__ void __launch_bounds__(GV_THREADS) down_kernel(FfnParams p) {
     const int pos0 = ints[ws_aoff_off(p.E) + a];
     const int n_e = ints[ws_aoff_off(p.E) + a + 1] - pos0;
     const int *routes = ints + ws_routes_off(p.E);
-    bool ready = false, ok = true;
 
     for (int tg = 0; tg < n_e; tg += GV_TOK) {
         const int nt = min(GV_TOK, n_e - tg), ntp = pow2_tokens(nt);
@@ -562,6 +598,17 @@ int moe_expert_ffn_impl(const void *x, int xtype, int T, int H, int F, int qtype
                         const int32_t *expert_subset, int n_subset, float *partial,
                         void *workspace, size_t ws_bytes, cudaStream_t s,
                         const moe_ffn_timing *timing) {
+    return moe_expert_ffn_core(x, xtype, T, H, F, qtype, E, k, ids, weights, d_slot_table, n_slots, pool,
+                               slot_bytes, expert_subset, n_subset, nullptr, partial, workspace, ws_bytes, s,
+                               timing);
+}
+
+int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
+                        const int32_t *ids, const float *weights, const int32_t *d_slot_table,
+                        int n_slots, const void *pool, size_t slot_bytes,
+                        const int32_t *expert_subset, int n_subset, const uint64_t *d_fill_src,
+                        float *partial, void *workspace, size_t ws_bytes, cudaStream_t s,
+                        const moe_ffn_timing *timing) {
     MOE_CHECK(T >= 0);
     MOE_CHECK(qtype == MOE_Q8_0 || qtype == MOE_Q4_SM);
     MOE_CHECK(xtype == MOE_F32 || xtype == MOE_BF16);
@@ -575,6 +622,7 @@ int moe_expert_ffn_impl(const void *x, int xtype, int T, int H, int F, int qtype
     MOE_CHECK(slot_bytes >= moe_expert_image_bytes(qtype, H, F));
     MOE_CHECK(((uintptr_t)workspace & 255) == 0);
     if (moe_prefill_eligible(T, H, F, qtype, xtype)) {
+        if (d_fill_src) return MOE_ERR_UNSUPPORTED;  // slot filling is a decode-path feature
         MOE_CHECK(ws_bytes >= moe_prefill_workspace_bytes(T, H, F, E, k));
         return moe_prefill_ffn(x, xtype, T, H, F, qtype, E, k, ids, weights, d_slot_table, n_slots, pool,
                                slot_bytes, expert_subset, n_subset, partial, workspace, ws_bytes, s, timing);
@@ -599,6 +647,7 @@ int moe_expert_ffn_impl(const void *x, int xtype, int T, int H, int F, int qtype
     p.partial = partial;
     p.status = moe_status_word_device_ptr();
     p.ntok = pow2_tokens(T < GV_TOK ? T : GV_TOK);
+    p.fill_src = (const unsigned long long *)d_fill_src;
 
     const int n_act_max = expert_subset ? n_subset : (T * k < E ? T * k : E);
     const int nb1 = (H / 32) / p.KS;
@@ -639,6 +688,16 @@ extern "C" int moe_expert_ffn(const void *x, int xtype, int T, int H, int F, int
     return moe_expert_ffn_impl(x, xtype, T, H, F, qtype, E, k, ids, weights, d_slot_table, n_slots,
                                pool, slot_bytes, expert_subset, n_subset, partial, workspace,
                                ws_bytes, moe_cuda_stream(s), nullptr);
+}
+
+extern "C" int moe_expert_ffn_fill(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
+                                   const int32_t *ids, const float *weights, const int32_t *d_slot_table,
+                                   int n_slots, void *pool, size_t slot_bytes, const uint64_t *d_fill_src,
+                                   float *partial, void *workspace, size_t ws_bytes, moe_stream_t s) {
+    MOE_CHECK(d_slot_table && d_fill_src);
+    return moe_expert_ffn_core(x, xtype, T, H, F, qtype, E, k, ids, weights, d_slot_table, n_slots, pool,
+                               slot_bytes, nullptr, 0, d_fill_src, partial, workspace, ws_bytes,
+                               moe_cuda_stream(s), nullptr);
 }
 
 extern "C" int moe_expert_ffn_workspace(int T, int H, int F, int qtype, int xtype, int E, int k,

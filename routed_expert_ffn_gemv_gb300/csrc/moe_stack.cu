@@ -15,7 +15,7 @@ namespace {
 inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct StackWs {
-    size_t ids, w, partial, table, hit, miss, hA, hB, xn, ids_s, w_s, partial_s, tmp, ffn, total;
+    size_t ids, w, partial, table, hit, miss, hA, hB, xn, ids_s, w_s, partial_s, tmp, fill, gin, gout, ffn, total;
     size_t ffn_bytes;
 };
 
@@ -36,6 +36,9 @@ StackWs stack_ws(int H, int F, int qtype, int E, int k, int T, int n_shared) {
     L.w_s = off;       off = align256(off + (size_t)T * ns * 4);
     L.partial_s = off; off = align256(off + (size_t)T * ns * H * 4);
     L.tmp = off;       off = align256(off + (size_t)T * H * 4);
+    L.fill = off;      off = align256(off + (size_t)E * 8);
+    L.gin = off;       off = align256(off + (size_t)T * H * 4);
+    L.gout = off;      off = align256(off + (size_t)T * H * 4);
     size_t f = moe_decode_workspace_bytes(T, H, F, qtype, E, k);
     if (ns > 0) {
         const size_t f2 = moe_decode_workspace_bytes(T, H, F, qtype, ns, ns);
@@ -71,6 +74,10 @@ struct moe_stack {
     std::vector<std::pair<int, EventPair>> timed;  // (kind, events)
     moe_stack_profile prof{};
     char *ws = nullptr;
+    // CUDA graphs of whole decode steps, per batch size (device-managed stacks)
+    cudaGraphExec_t graph[MOE_DECODE_MAX_T + 1] = {};
+    uint64_t graph_launches[MOE_DECODE_MAX_T + 1] = {};  // kernels per captured step
+    bool eager_done[MOE_DECODE_MAX_T + 1] = {};
 };
 
 namespace {
@@ -125,7 +132,7 @@ int end_timed(moe_stack *st, cudaStream_t s, int kind, EventPair ep) {
 // One FFN call with per-kernel timing when profiling.
 int ffn_call(moe_stack *st, const float *x, int T, int E, int k, const int32_t *ids, const float *w,
              const int32_t *table, int n_slots, const void *pool, const int32_t *subset, int n_subset,
-             float *partial, int n_active, cudaStream_t s) {
+             float *partial, int n_active, cudaStream_t s, const uint64_t *fill = nullptr) {
     const moe_stack_desc &d = st->d;
     moe_ffn_timing tm{};
     const moe_ffn_timing *tp = nullptr;
@@ -138,8 +145,8 @@ int ffn_call(moe_stack *st, const float *x, int T, int E, int k, const int32_t *
                 return rc;
         tp = &tm;
     }
-    const int rc = moe_expert_ffn_impl(x, MOE_F32, T, d.H, d.F, d.qtype, E, k, ids, w, table, n_slots,
-                                       pool, d.slot_bytes, subset, n_subset, partial,
+    const int rc = moe_expert_ffn_core(x, MOE_F32, T, d.H, d.F, d.qtype, E, k, ids, w, table, n_slots,
+                                       pool, d.slot_bytes, subset, n_subset, fill, partial,
                                        st->ws + st->L.ffn, st->L.ffn_bytes, s, tp);
     if (rc) return rc;
     st->prof.kernel_launches += 3;
@@ -151,6 +158,8 @@ int ffn_call(moe_stack *st, const float *x, int T, int E, int k, const int32_t *
         }
         st->prof.gateup_launches++;
         st->prof.down_launches++;
+    }
+    if (d.profile >= 1 && n_active >= 0) {  // n_active < 0: not known on the host
         st->prof.gateup_bytes += (double)n_active * 2 * moe_matrix_bytes(d.qtype, d.F, d.H);
         st->prof.down_bytes += (double)n_active * moe_matrix_bytes(d.qtype, d.H, d.F);
     }
@@ -189,7 +198,17 @@ int layer_step(moe_stack *st, int layer, const float *h, float *y, int T, int32_
     if ((rc = end_timed(st, s, K_ROUTER, ep))) return rc;
 
     const int g = st->group_of_layer[layer];
-    if (g >= 0) {
+    if (g >= 0 && d.device_managed) {
+        // the pool's bookkeeping on the GPU, then the FFN filling the missed experts' slots
+        moe_cache *c = st->caches[g];
+        uint64_t *fill = (uint64_t *)(st->ws + L.fill);
+        if ((rc = moe_cache_plan(c, layer, ids_d, T, d.k, table, fill, (moe_stream_t)s))) return rc;
+        st->prof.kernel_launches += 1;
+        int ns = 0;
+        const void *pool = moe_cache_pool(c, &ns);
+        if ((rc = ffn_call(st, x, T, d.E, d.k, ids_d, w_d, table, ns, pool, nullptr, 0, partial, -1, s, fill)))
+            return rc;
+    } else if (g >= 0) {
         moe_cache *c = st->caches[g];
         MOE_TRY_CUDA(cudaMemcpyAsync(st->ids_h, ids_d, (size_t)T * d.k * 4, cudaMemcpyDeviceToHost, s));
         MOE_TRY_CUDA(cudaEventRecord(st->ids_ready, s));
@@ -327,6 +346,10 @@ extern "C" int moe_stack_create(const moe_stack_desc *desc, moe_stack **out) {
             delete st;
             return MOE_ERR_INVALID;
         }
+        if (moe_cache_is_device_managed(c) != (d.device_managed != 0)) {
+            delete st;
+            return MOE_ERR_INVALID;  // the caches' kind must match the stack's
+        }
         st->caches.push_back(c);
         for (int l = first; l < first + n; ++l) st->group_of_layer[l] = g;
     }
@@ -368,12 +391,10 @@ extern "C" int moe_stack_layer(moe_stack *st, int layer, const float *x_in, floa
     return layer_step(st, layer, x_in, y_out, T, ids_host_out, weights_host_out, cs, true, false);
 }
 
-extern "C" int moe_stack_decode(moe_stack *st, const float *x_in, float *y_out, int T,
-                                int32_t *ids_host_out, float *weights_host_out, moe_stream_t s) {
-    MOE_CHECK(st && x_in && y_out);
-    MOE_CHECK(T >= 1 && T <= st->d.max_T);
-    cudaStream_t cs = moe_cuda_stream(s);
-    st->last_stream = cs;
+namespace {
+
+int run_step(moe_stack *st, const float *x_in, float *y_out, int T, int32_t *ids_host_out,
+             float *weights_host_out, cudaStream_t cs) {
     const int L = st->d.n_layers;
     float *hA = (float *)(st->ws + st->L.hA), *hB = (float *)(st->ws + st->L.hB);
     const float *cur = x_in;
@@ -386,6 +407,62 @@ extern "C" int moe_stack_decode(moe_stack *st, const float *x_in, float *y_out, 
         if (rc) return rc;
         cur = out;
     }
+    return MOE_OK;
+}
+
+// Captures one whole step (device-managed stacks) reading gin and writing gout.
+int capture_step(moe_stack *st, int T, cudaStream_t cs) {
+    float *gin = (float *)(st->ws + st->L.gin), *gout = (float *)(st->ws + st->L.gout);
+    const uint64_t launches0 = st->prof.kernel_launches;
+    MOE_TRY_CUDA(cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed));
+    const int rc = run_step(st, gin, gout, T, nullptr, nullptr, cs);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(cs, &graph);
+    st->graph_launches[T] = st->prof.kernel_launches - launches0;
+    st->prof.kernel_launches = launches0;
+    if (rc != MOE_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return rc;
+    }
+    if (ec != cudaSuccess) return MOE_ERR_CUDA;
+    const cudaError_t ei = cudaGraphInstantiate(&st->graph[T], graph, 0);
+    cudaGraphDestroy(graph);
+    if (ei != cudaSuccess) {
+        st->graph[T] = nullptr;
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_stack_decode(moe_stack *st, const float *x_in, float *y_out, int T,
+                                int32_t *ids_host_out, float *weights_host_out, moe_stream_t s) {
+    MOE_CHECK(st && x_in && y_out);
+    MOE_CHECK(T >= 1 && T <= st->d.max_T);
+    cudaStream_t cs = moe_cuda_stream(s);
+    st->last_stream = cs;
+    const moe_stack_desc &d = st->d;
+    const bool graphable = d.use_graph && d.device_managed && !d.profile && !ids_host_out && !weights_host_out;
+    if (graphable && st->eager_done[T]) {
+        if (!st->graph[T]) {
+            const int rc = capture_step(st, T, cs);
+            if (rc) return rc;
+        }
+        const size_t bytes = (size_t)T * d.H * 4;
+        MOE_TRY_CUDA(cudaMemcpyAsync(st->ws + st->L.gin, x_in, bytes, cudaMemcpyDeviceToDevice, cs));
+        MOE_TRY_CUDA(cudaGraphLaunch(st->graph[T], cs));
+        MOE_TRY_CUDA(cudaMemcpyAsync(y_out, st->ws + st->L.gout, bytes, cudaMemcpyDeviceToDevice, cs));
+        st->prof.kernel_launches += st->graph_launches[T];
+        st->prof.layers += d.n_layers;
+        st->prof.steps++;
+        return MOE_OK;
+    }
+    // eager: every launch issued now (the first call of a graph-captured stack runs eagerly so
+    // that one-time set-up never happens inside a capture)
+    const int rc = run_step(st, x_in, y_out, T, ids_host_out, weights_host_out, cs);
+    if (rc) return rc;
+    st->eager_done[T] = true;
     st->prof.steps++;
     return MOE_OK;
 }
@@ -421,6 +498,8 @@ extern "C" void moe_stack_destroy(moe_stack *st) {
     if (!st) return;
     if (st->last_stream) cudaStreamSynchronize(st->last_stream);
     for (cudaEvent_t e : st->ev_pool) cudaEventDestroy(e);
+    for (int t = 0; t <= MOE_DECODE_MAX_T; ++t)
+        if (st->graph[t]) cudaGraphExecDestroy(st->graph[t]);
     if (st->ids_ready) cudaEventDestroy(st->ids_ready);
     if (st->ids_h) cudaFreeHost(st->ids_h);
     if (st->slots_h) cudaFreeHost(st->slots_h);

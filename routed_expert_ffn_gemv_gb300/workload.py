@@ -68,7 +68,7 @@ class Stack:
     def __init__(self, cfg: synth.MoEConfig, max_T: Optional[int] = None, overlap: bool = True,
                  profile: int = 0, pool_slots: Optional[Sequence[int]] = None,
                  n_layers: Optional[int] = None, random_scales: bool = False,
-                 resident: bool = False):
+                 resident: bool = False, device_managed: bool = False, use_graph: bool = False):
         self.cfg = cfg
         self.L = n_layers or cfg.L
         self.max_T = max_T or max(cfg.tokens)
@@ -87,6 +87,8 @@ class Stack:
         self.images = PinnedImages(cfg, range(self.L), range(E), random_scales)
         self.caches: List[int] = []
         self.pools: List[torch.Tensor] = []
+        self.states: List[torch.Tensor] = []
+        self.device_managed = device_managed
         self.copy_stream = torch.cuda.Stream(device=self.dev)
         groups = [] if resident else list(cfg.groups)
         self.resident_pool = None
@@ -102,11 +104,19 @@ class Stack:
                 pool = torch.empty(n_slots * self.stride, dtype=torch.uint8, device=self.dev)
                 imgs = (ctypes.c_void_p * (n_layers_g * E))(
                     *[self.images.ptr(grp.first_layer + li, e) for li in range(n_layers_g) for e in range(E)])
+                state, state_bytes = None, 0
+                if device_managed:
+                    state_bytes = L.moe_cache_state_bytes(n_layers_g, E, n_slots)
+                    state = torch.empty(state_bytes, dtype=torch.uint8, device=self.dev)
+                    self.states.append(state)
                 desc = L.CacheDesc(qtype=cfg.qtype, H=H, F=F, n_layers=n_layers_g, n_experts=E,
                                    first_layer=grp.first_layer, n_slots=n_slots, slot_bytes=self.stride,
                                    device_pool=pool.data_ptr(),
                                    host_images=ctypes.cast(imgs, ctypes.POINTER(ctypes.c_void_p)),
-                                   copy_stream=self.copy_stream.cuda_stream)
+                                   copy_stream=self.copy_stream.cuda_stream,
+                                   device_managed=int(device_managed),
+                                   device_state=None if state is None else state.data_ptr(),
+                                   device_state_bytes=state_bytes)
                 self.caches.append(L.moe_cache_create(desc))
                 self.pools.append(pool)
         # shared experts (always resident)
@@ -129,7 +139,9 @@ class Stack:
                            resident_pool=None if self.resident_pool is None else self.resident_pool.data_ptr(),
                            shared_pool=None if self.shared_pool is None else self.shared_pool.data_ptr(),
                            slot_bytes=self.stride, max_T=self.max_T, workspace=self.workspace.data_ptr(),
-                           ws_bytes=ws, overlap=int(overlap), profile=int(profile))
+                           ws_bytes=ws, overlap=int(overlap), profile=int(profile),
+                           device_managed=int(device_managed and bool(self.caches)),
+                           use_graph=int(use_graph))
         torch.cuda.synchronize()
         self.handle = L.moe_stack_create(desc)
 

@@ -169,11 +169,13 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
                     s = filled++;
                 } else {
                     s = head;
-                    while (s >= 0) {
+                    int steps = 0;  // the list holds at most n_slots entries: a longer walk is corruption
+                    while (s >= 0 && s < n_slots && steps++ <= n_slots) {
                         const int o = owner[s];
                         if (!(o >= key0 && o < key0 + E && want[o - key0])) break;
                         s = next[s];
                     }
+                    if (steps > n_slots + 1 || s >= n_slots) s = -1;
                     if (s < 0) { moe_set_status(status, MOE_ERR_CAPACITY); abort_flag = 1; break; }
                     unlink(s);
                     const int o = owner[s];

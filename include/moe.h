@@ -65,6 +65,9 @@ enum moe_status {
 /* Static message for a status code; never NULL. */
 const char *moe_status_string(int status);
 
+/* Name of the CUDA error behind the calling thread's last MOE_ERR_CUDA ("none" if none). */
+const char *moe_last_cuda_error(void);
+
 /* Library limits. */
 #define MOE_MAX_K 8          /* top-k limit (k <= 8 covers every workload) */
 #define MOE_MAX_E 256        /* experts per layer */

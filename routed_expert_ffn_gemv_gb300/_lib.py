@@ -38,7 +38,7 @@ EXPORTED = [
     "moe_stack_decode", "moe_stack_layer", "moe_stack_profile_get", "moe_stack_profile_reset",
     "moe_stack_destroy", "moe_debug_inject_fault", "moe_stack_set_profile",
     "moe_expert_ffn_noalloc", "moe_combine_rmsnorm", "moe_cache_state_bytes", "moe_cache_plan",
-    "moe_expert_ffn_fill",
+    "moe_expert_ffn_fill", "moe_last_cuda_error",
 ]
 MOE_NOALLOC_SCRATCH_MAX = 8 << 20
 
@@ -46,7 +46,8 @@ MOE_NOALLOC_SCRATCH_MAX = 8 << 20
 class MoeError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn} failed: {status} ({status_string(status)})")
+        detail = f", {load().moe_last_cuda_error().decode()}" if status == MOE_ERR_CUDA else ""
+        super().__init__(f"{fn} failed: {status} ({status_string(status)}{detail})")
 
 
 _vp = ctypes.c_void_p
@@ -113,6 +114,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     P = ctypes.POINTER
     sig = {
         "moe_status_string": ([_i], ctypes.c_char_p),
+        "moe_last_cuda_error": ([], ctypes.c_char_p),
         "moe_router_topk": ([_vp, _i, _i, _i, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp], _i),
         "moe_slot_image_bytes": ([_i, _i, _i, P(_sz)], _i),
         "moe_pack_expert": ([_i, _i, _i, _vp, _vp, _vp, _vp, P(_sz)], _i),

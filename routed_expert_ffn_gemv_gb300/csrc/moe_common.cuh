@@ -7,10 +7,16 @@
 
 #include "moe.h"
 
+// Records the CUDA error behind an MOE_ERR_CUDA (see moe_last_cuda_error).
+void moe_note_cuda_error(cudaError_t e);
+
 #define MOE_TRY_CUDA(expr)                                   \
     do {                                                     \
         cudaError_t moe_err__ = (expr);                      \
-        if (moe_err__ != cudaSuccess) return MOE_ERR_CUDA;   \
+        if (moe_err__ != cudaSuccess) {                      \
+            moe_note_cuda_error(moe_err__);                  \
+            return MOE_ERR_CUDA;                             \
+        }                                                    \
     } while (0)
 
 #define MOE_CHECK(cond)                                      \

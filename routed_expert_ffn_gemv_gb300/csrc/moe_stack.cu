@@ -75,6 +75,8 @@ struct moe_stack {
     moe_stack_profile prof{};
     char *ws = nullptr;
     // CUDA graphs of whole decode steps, per batch size (device-managed stacks)
+    cudaStream_t cap_stream = nullptr;                  // graphs are captured here (never the
+                                                        // legacy default stream), launched on the caller's
     cudaGraphExec_t graph[MOE_DECODE_MAX_T + 1] = {};
     uint64_t graph_launches[MOE_DECODE_MAX_T + 1] = {};  // kernels per captured step
     bool eager_done[MOE_DECODE_MAX_T + 1] = {};
@@ -410,10 +412,13 @@ int run_step(moe_stack *st, const float *x_in, float *y_out, int T, int32_t *ids
     return MOE_OK;
 }
 
-// Captures one whole step (device-managed stacks) reading gin and writing gout.
-int capture_step(moe_stack *st, int T, cudaStream_t cs) {
+// Captures one whole step (device-managed stacks) reading gin and writing gout, on the
+// stack's own capture stream (nothing executes during a capture).
+int capture_step(moe_stack *st, int T) {
     float *gin = (float *)(st->ws + st->L.gin), *gout = (float *)(st->ws + st->L.gout);
     const uint64_t launches0 = st->prof.kernel_launches;
+    if (!st->cap_stream) MOE_TRY_CUDA(cudaStreamCreateWithFlags(&st->cap_stream, cudaStreamNonBlocking));
+    cudaStream_t cs = st->cap_stream;
     MOE_TRY_CUDA(cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed));
     const int rc = run_step(st, gin, gout, T, nullptr, nullptr, cs);
     cudaGraph_t graph = nullptr;
@@ -446,7 +451,7 @@ extern "C" int moe_stack_decode(moe_stack *st, const float *x_in, float *y_out, 
     const bool graphable = d.use_graph && d.device_managed && !d.profile && !ids_host_out && !weights_host_out;
     if (graphable && st->eager_done[T]) {
         if (!st->graph[T]) {
-            const int rc = capture_step(st, T, cs);
+            const int rc = capture_step(st, T);
             if (rc) return rc;
         }
         const size_t bytes = (size_t)T * d.H * 4;
@@ -500,6 +505,7 @@ extern "C" void moe_stack_destroy(moe_stack *st) {
     for (cudaEvent_t e : st->ev_pool) cudaEventDestroy(e);
     for (int t = 0; t <= MOE_DECODE_MAX_T; ++t)
         if (st->graph[t]) cudaGraphExecDestroy(st->graph[t]);
+    if (st->cap_stream) cudaStreamDestroy(st->cap_stream);
     if (st->ids_ready) cudaEventDestroy(st->ids_ready);
     if (st->ids_h) cudaFreeHost(st->ids_h);
     if (st->slots_h) cudaFreeHost(st->slots_h);

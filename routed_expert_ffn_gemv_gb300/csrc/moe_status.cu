@@ -20,6 +20,14 @@ extern "C" const char *moe_status_string(int status) {
     }
 }
 
+static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+void moe_note_cuda_error(cudaError_t e) { g_last_cuda_error = e; }
+
+extern "C" const char *moe_last_cuda_error(void) {
+    return g_last_cuda_error == cudaSuccess ? "none" : cudaGetErrorName(g_last_cuda_error);
+}
+
 int *moe_status_word_device_ptr() {
     static std::mutex mu;
     static int *ptrs[64] = {nullptr};

@@ -439,12 +439,44 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--lite", action="store_true",
                     help="only the device-managed timed loop at --batch (the ncu target)")
+    ap.add_argument("--only", choices=["host", "prefill"], default=None,
+                    help="profiling targets: 'host' = host-managed pool loop at --batch (every GEMV "
+                         "byte from HBM), 'prefill' = the prefill layer at 512 and 4096 tokens")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.only:
+        return run_only(args)
     return run_gpu(args, world, rank, local)
+
+
+def run_only(args):
+    """Short single-purpose runs used as ncu targets (one JSON line, no headline)."""
+    import torch
+    torch.cuda.set_device(0)
+    from routed_expert_ffn_gemv_gb300 import _lib as L, synth
+    from routed_expert_ffn_gemv_gb300.workload import Stack
+    L.load()
+    peaks = load_peaks()
+    if args.only == "prefill":
+        print(json.dumps({"only": "prefill", "prefill": run_prefill(torch, peaks, steps=args.steps,
+                                                                   warmup=args.warmup)}), flush=True)
+        return 0
+    cfg = synth.config(CONFIG_INDEX)
+    T = args.batch
+    stack = Stack(cfg, max_T=T, profile=1)
+    xs = [torch.from_numpy(synth.tokens_x(cfg, 3 + s, T)).cuda() for s in range(16)]
+    ms, prof, st = time_steps(stack, xs, T, args.steps, args.warmup, torch, torch.cuda.Stream())
+    gl = max(1, prof["gateup_launches"])
+    print(json.dumps({"only": "host", "batch": T, "ms_per_step": ms / args.steps,
+                      "gateup_ms_per_launch": prof["gateup_ms"] / gl,
+                      "gateup_bytes_per_launch": prof["gateup_bytes"] / gl,
+                      "gateup_gbs": prof["gateup_bytes"] / max(1e-9, prof["gateup_ms"] / 1e3) / 1e9}),
+          flush=True)
+    stack.close()
+    return 0
 
 
 if __name__ == "__main__":

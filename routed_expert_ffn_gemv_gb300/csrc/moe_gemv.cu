@@ -1,78 +1,117 @@
-// Decode-time expert FFN: permute (P1), gate/up dequantising GEMV (G1), down GEMV with
-// the router-weighted scatter (G2), combine (C1).
+// Decode-time expert FFN: permute (P1), gate/up dequantising GEMV + SwiGLU (G1), down GEMV
+// with the router-weighted scatter (G2), combine (C1).
 //
 // What is computed (pages 1-5, see moe.h): for every route (t, j) of a token t to its
 // j-th selected expert e, h = silu(Wg_e x_t) * (Wu_e x_t) and
 // partial[t][j] = w[t][j] * (Wd_e h); the combine sums partial over j.  Weights stay in
 // their quantised blocks (page 5, section 1.2) and are dequantised in registers.
 //
-// GB300 mapping (the decode GEMVs are HBM-bound):
-//  * a CTA owns one unit = (active expert, matrix, 32-row tile, K range); its 4 warps
-//    split the K range; lane l owns row l of the tile, so each lane keeps the whole
-//    dot product in registers and no cross-lane reduction is needed;
-//  * at CTA start one thread issues bulk copies (TMA engine, cp.async.bulk) of every
-//    warp's weight bytes into shared memory, so all of a unit's bytes are in flight at
-//    once; the slot image layout makes each warp's bytes one contiguous run;
-//  * activations of the expert's tokens are staged once in shared memory and read as
-//    warp-wide broadcasts; codes become fp32 with exponent tricks (no int->float
-//    conversion instructions) and accumulate with packed fp32x2 FMAs; block scales are
-//    applied once per 32-weight block;
-//  * tokens beyond 8 per expert are processed in further passes over the same
-//    shared-memory weights.
+// GB300 mapping (the decode GEMVs stream the selected experts' bytes from HBM once):
+//  * work unit = (active expert, [K range,] matrix, 32-row tile): one 32-row tile of one
+//    matrix over a K range, whose bytes are one contiguous run per region in the slot image;
+//  * persistent CTAs of 8 warps: each CTA streams a contiguous range of units through a
+//    ring of shared-memory stages; thread 0 keeps S-1 units' bulk copies (TMA engine,
+//    cp.async.bulk) in flight ahead of the unit being computed;
+//  * lane l of each warp owns row l of the tile and keeps its dot products in registers
+//    (no cross-lane reduction); the 8 warps split the unit's K range and are reduced in
+//    shared memory in a fixed order;
+//  * activations of the unit's tokens are staged once in shared memory (vector loads,
+//    issued before the unit's weights are waited for) and reused while consecutive units
+//    share the expert and K range; they are read as warp broadcasts;
+//  * codes become fp32 with exponent tricks (no int->float conversions), accumulate with
+//    packed fp32x2 FMAs, and block scales are applied once per 32 weights;
+//  * gate/up partial sums of the K ranges meet in the workspace; the warp whose write
+//    completes a (expert, row tile) sums them in a fixed order and writes h = silu(g) * u,
+//    so the down kernel's activations are a plain copy;
+//  * an expert that missed in a device-managed pool is read from its pinned host image and
+//    written through to its slot by the unit that uses the bytes ("fill" units).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "moe_ptx.cuh"
 
-#define GV_WARPS 4
+#define GV_WARPS 8
 #define GV_THREADS (GV_WARPS * 32)
-#define GV_TOK 8            // tokens per pass
+#define GV_TOK 8            // tokens per pass (one per warp in the reduction)
 #define GV_UNIT_QUANT 16384 // target code bytes per gate/up unit
+#define GV_S1 4             // ring stages, gate/up
+#define GV_S2 3             // ring stages, down
+#define GV_SMEM_MAX (220 * 1024)  // dynamic shared memory a ring kernel may take
+#define GV_FILL_BATCH 6     // 16-byte pieces per thread loaded together by a fill unit
+
+static_assert(GV_TOK == GV_WARPS, "the reduction gives each warp one token of a pass");
 
 namespace {
 
 // ------------------------------------------------------------------ workspace layout
 
+// Per active expert, written by the permute kernel.
+struct ActInfo {
+    unsigned long long src;  // image base the weights are read from (slot, or pinned host image)
+    unsigned long long dst;  // slot base (written through when fill != 0)
+    int e, pos0, n_e, fill;  // n_e == 0: skip (invalid slot)
+};
+
 struct WsLayout {
-    size_t ints_off;   // int32 region: [0] n_active, [16..16+E) active, a_off [E+1], routes [R]
-    size_t gu_off;     // float [KS][2][R][F]
+    size_t ints_off;   // int32: [0] n_active, [16..16+E) active, a_off [E+1], routes [R], tickets [E][F/32],
+                       //        cost prefix [E+1]
+    size_t info_off;   // ActInfo [E]
+    size_t gu_off;     // float [KS][2][R][F]: gate/up partial dot products per K range
+    size_t h_off;      // float [R][F]: silu(gate) * up
     size_t total;
 };
 
 __host__ __device__ inline int ws_active_off() { return 16; }
 __host__ __device__ inline int ws_aoff_off(int E) { return 16 + E; }
 __host__ __device__ inline int ws_routes_off(int E) { return 16 + 2 * E + 1; }
+__host__ __device__ inline int ws_ticket_off(int E, int R) { return 16 + 2 * E + 1 + R; }
+__host__ __device__ inline int ws_cost_off(int E, int R, int F) { return 16 + 2 * E + 1 + R + E * (F / 32); }
+
+// Work of one unit of an expert with n_e tokens, in units of a token's dot products: the
+// unit's bytes and dequantisation cost about as much as GV_COST_MEM tokens.
+#define GV_COST_MEM 4
+__host__ __device__ inline int unit_cost(int n_e) { return n_e > 0 ? GV_COST_MEM + n_e : 1; }
 
 inline WsLayout ws_layout(int T, int H, int F, int qtype, int E, int k) {
     WsLayout L;
     const size_t R = (size_t)T * k;
-    const size_t ints = 16 + 2 * (size_t)E + 1 + R;
+    const size_t ints = 16 + 2 * (size_t)E + 1 + R + (size_t)E * (F / 32) + (size_t)E + 1;
     L.ints_off = 0;
-    L.gu_off = (ints * 4 + 255) / 256 * 256;
+    L.info_off = (ints * 4 + 255) / 256 * 256;
+    L.gu_off = L.info_off + ((size_t)E * sizeof(ActInfo) + 255) / 256 * 256;
     const int KS = moe_gateup_ksplit(qtype, H);
-    L.total = L.gu_off + (size_t)KS * 2 * R * F * 4;
-    L.total = (L.total + 255) / 256 * 256;
+    L.h_off = L.gu_off + ((size_t)KS * 2 * R * F * 4 + 255) / 256 * 256;
+    L.total = L.h_off + ((size_t)R * F * 4 + 255) / 256 * 256;
     return L;
 }
 
 // ------------------------------------------------------------------ shared-memory layout
 
-struct UnitSmem {
-    size_t bars, quant, scale, act, asum, red, total;
+struct RingSmem {
+    size_t bars, stages, stage_bytes, scale_off, act, asum, red, info, rts, wts, total;
 };
 
-__host__ __device__ inline UnitSmem unit_smem(int qtype, int nbr, int ntok) {
-    UnitSmem L;
-    const int QB = qtype == MOE_Q8_0 ? 1024 : 512;           // code bytes per block of a 32-row tile
-    const int SB = 32 * moe_scale_entry_bytes(qtype);        // scale bytes per block of a tile
+#define GV_ICACHE 64    // active experts of a CTA's range kept in shared memory
+#define GV_RCACHE 512   // routes (and their router weights) of a CTA's range kept in shared memory
+
+__host__ __device__ inline RingSmem ring_smem(int qtype, int nbr, int ntok, int S) {
+    RingSmem L;
+    const int QB = qtype == MOE_Q8_0 ? 1024 : 512;       // code bytes per block of a 32-row tile
+    const int SB = 32 * moe_scale_entry_bytes(qtype);    // scale bytes per block of a tile
+    L.scale_off = (size_t)nbr * QB;
+    L.stage_bytes = L.scale_off + ((size_t)nbr * SB + 127) / 128 * 128;
     size_t off = 0;
-    L.bars = off;  off += 128;
-    L.quant = off; off += (size_t)nbr * QB;
-    L.scale = off; off += ((size_t)nbr * SB + 127) / 128 * 128;
-    L.act = off;   off += (size_t)ntok * nbr * 32 * 4;
-    L.asum = off;  off += ((size_t)ntok * nbr * 4 + 15) / 16 * 16;
-    L.red = off;   off += (size_t)GV_WARPS * GV_TOK * 32 * 4;
+    L.bars = off;   off += 128;
+    L.stages = off; off += (size_t)S * L.stage_bytes;
+    L.act = off;    off += (size_t)ntok * nbr * 32 * 4;
+    L.asum = off;   off += ((size_t)ntok * nbr * 4 + 15) / 16 * 16;
+    L.red = off;    off += (size_t)GV_WARPS * GV_TOK * 32 * 4;
+    L.info = off;   off += (size_t)GV_ICACHE * 32;
+    L.rts = off;    off += (size_t)GV_RCACHE * 4;
+    L.wts = off;    off += (size_t)GV_RCACHE * 4;
     L.total = off;
     return L;
 }
@@ -82,28 +121,56 @@ __device__ __forceinline__ void warp_blocks(int nbr, int w, int &b0, int &b1) {
     b1 = ((w + 1) * nbr) / GV_WARPS;
 }
 
-// Issue the bulk copies of one unit: rows [32g, 32g+32) of matrix `mat` [R][K], blocks
-// [kb0, kb0+nbr), warp w's share completing on bars[w].
+// Bulk copies of one unit into a stage: rows [32g, 32g+32) of matrix `mat` [R][K], blocks
+// [kb0, kb0+nbr) — the codes and the scales are one contiguous run each.
 template <int QT>
-__device__ void issue_unit_copies(const uint8_t *mat, int R, int K, int g, int kb0, int nbr,
-                                  unsigned char *smem, const UnitSmem &L) {
-    uint64_t *bars = (uint64_t *)(smem + L.bars);
+__device__ __forceinline__ void issue_unit(const uint8_t *mat, int R, int K, int g, int kb0, int nbr,
+                                           unsigned char *stage, size_t scale_off, uint64_t *bar) {
     const int QB = QT == MOE_Q8_0 ? 1024 : 512;
     const int SB = 32 * moe_scale_entry_bytes(QT);
-    const int PPB = QT == MOE_Q8_0 ? 2 : 1;  // pieces per block
-    for (int w = 0; w < GV_WARPS; ++w) mbar_init(&bars[w], 1);
-    fence_mbar_init();
-    const uint8_t *scales = mat + moe_quant_bytes(QT, R, K);
-    for (int w = 0; w < GV_WARPS; ++w) {
-        int b0, b1;
-        warp_blocks(nbr, w, b0, b1);
-        if (b1 <= b0) continue;
-        const uint32_t qbytes = (uint32_t)(b1 - b0) * QB, sbytes = (uint32_t)(b1 - b0) * SB;
-        mbar_arrive_expect_tx(&bars[w], qbytes + sbytes);
-        bulk_g2s(smem + L.quant + (size_t)b0 * QB,
-                 mat + moe_piece_offset(QT, K, g, (kb0 + b0) * PPB), qbytes, &bars[w]);
-        bulk_g2s(smem + L.scale + (size_t)b0 * SB,
-                 scales + moe_scale_offset(QT, K, g, kb0 + b0), sbytes, &bars[w]);
+    const int PPB = QT == MOE_Q8_0 ? 2 : 1;  // 16-byte pieces per block
+    const uint32_t qbytes = (uint32_t)nbr * QB, sbytes = (uint32_t)nbr * SB;
+    mbar_arrive_expect_tx(bar, qbytes + sbytes);
+    bulk_g2s(stage, mat + moe_piece_offset(QT, K, g, kb0 * PPB), qbytes, bar);
+    bulk_g2s(stage + scale_off, mat + moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, g, kb0), sbytes, bar);
+}
+
+// Fill path of a unit whose expert missed: its bytes come from the expert's pinned host
+// image over the CPU-GPU link (16-byte loads by every thread) and are written both to the
+// stage and through to the expert's slot, so the slot is filled by the kernels that use
+// it.  Same byte ranges as issue_unit.
+template <int QT>
+__device__ void fill_unit(const uint8_t *src_mat, uint8_t *dst_mat, int R, int K, int g, int kb0, int nbr,
+                          unsigned char *stage, size_t scale_off) {
+    const int QB = QT == MOE_Q8_0 ? 1024 : 512;
+    const int SB = 32 * moe_scale_entry_bytes(QT);
+    const int PPB = QT == MOE_Q8_0 ? 2 : 1;
+    const size_t qoff = moe_piece_offset(QT, K, g, kb0 * PPB);
+    const size_t soff = moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, g, kb0);
+    const int nq = nbr * QB / 16, ns = nbr * SB / 16;
+    // loads of up to GV_FILL_BATCH pieces per thread are in flight together: one link round
+    // trip per batch instead of one per piece
+    constexpr int NB = GV_FILL_BATCH;
+    for (int i0 = 0; i0 < nq + ns; i0 += NB * GV_THREADS) {
+        uint4 v[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int i = i0 + b * GV_THREADS + threadIdx.x;
+            if (i < nq + ns) {
+                const size_t off = i < nq ? qoff + (size_t)i * 16 : soff + (size_t)(i - nq) * 16;
+                v[b] = __ldcs((const uint4 *)(src_mat + off));
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const int i = i0 + b * GV_THREADS + threadIdx.x;
+            if (i < nq + ns) {
+                const bool q = i < nq;
+                const size_t off = q ? qoff + (size_t)i * 16 : soff + (size_t)(i - nq) * 16;
+                *(uint4 *)(stage + (q ? (size_t)i * 16 : scale_off + (size_t)(i - nq) * 16)) = v[b];
+                __stcs((uint4 *)(dst_mat + off), v[b]);
+            }
+        }
     }
 }
 
@@ -122,341 +189,459 @@ __device__ __forceinline__ float q4_act_unscale(int c) {
     return __int_as_float((127 + 4 * e) << 23);
 }
 
-// Dot products of one lane's row with NT staged activation rows over warp blocks [b0,b1).
-// act: [NT][Kr] (zero rows beyond the real token count), asum: [NT][nbr].
+// One block b of one lane's row against NT staged activation rows; acc[t] += d * sum
+// (+ m * asum for 4-bit).  act: [NT][Kr] fp32, asum: [NT][nbr].
 template <int QT, int NT>
-__device__ __forceinline__ void tile_dot(const unsigned char *quant_s, const unsigned char *scale_s,
-                                         const float *act, const float *asum, int Kr, int nbr,
-                                         int b0, int b1, int lane, float *acc) {
+__device__ __forceinline__ void block_dot(const unsigned char *quant_s, const unsigned char *scale_s,
+                                          const float *act, const float *asum, int Kr, int nbr, int b,
+                                          int lane, float *acc) {
     const unsigned long long MAG8 = f2_pack(-8388736.0f, -8388736.0f);  // 2^23 + 128
     const unsigned long long MAG4 = f2_pack(-8388608.0f, -8388608.0f);  // 2^23
-    for (int b = b0; b < b1; ++b) {
-        unsigned long long inner[NT];
+    unsigned long long inner[NT];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) inner[t] = 0ull;
-        if constexpr (QT == MOE_Q8_0) {
-            const uint4 qa = *(const uint4 *)(quant_s + ((size_t)(2 * b) * 32 + lane) * 16);
-            const uint4 qb = *(const uint4 *)(quant_s + ((size_t)(2 * b + 1) * 32 + lane) * 16);
-            const uint32_t wd[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    for (int t = 0; t < NT; ++t) inner[t] = 0ull;
+    if constexpr (QT == MOE_Q8_0) {
+        const uint4 qa = *(const uint4 *)(quant_s + ((size_t)(2 * b) * 32 + lane) * 16);
+        const uint4 qb = *(const uint4 *)(quant_s + ((size_t)(2 * b + 1) * 32 + lane) * 16);
+        const unsigned short dh = *(const unsigned short *)(scale_s + ((size_t)b * 32 + lane) * 2);
+        const uint32_t wd[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t wx = wd[i] ^ 0x80808080u;  // int8 -> offset-128 bytes
-                const float v0 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7440));
-                const float v1 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7441));
-                const float v2 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7442));
-                const float v3 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7443));
-                const unsigned long long p01 = f2_add(f2_pack(v0, v1), MAG8);
-                const unsigned long long p23 = f2_add(f2_pack(v2, v3), MAG8);
-#pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    const float4 xv = *(const float4 *)(act + (size_t)t * Kr + b * 32 + 4 * i);
-                    inner[t] = f2_fma(p01, f2_pack(xv.x, xv.y), inner[t]);
-                    inner[t] = f2_fma(p23, f2_pack(xv.z, xv.w), inner[t]);
-                }
-            }
-            const float d = __half2float(
-                __ushort_as_half(*(const unsigned short *)(scale_s + ((size_t)b * 32 + lane) * 2)));
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t wx = wd[i] ^ 0x80808080u;  // int8 -> offset-128 bytes
+            const float v0 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7440));
+            const float v1 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7441));
+            const float v2 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7442));
+            const float v3 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7443));
+            const unsigned long long p01 = f2_add(f2_pack(v0, v1), MAG8);
+            const unsigned long long p23 = f2_add(f2_pack(v2, v3), MAG8);
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                float lo, hi;
-                f2_unpack(inner[t], lo, hi);
-                acc[t] = fmaf(d, lo + hi, acc[t]);
+                const float4 xv = *(const float4 *)(act + (size_t)t * Kr + b * 32 + 4 * i);
+                inner[t] = f2_fma(p01, f2_pack(xv.x, xv.y), inner[t]);
+                inner[t] = f2_fma(p23, f2_pack(xv.z, xv.w), inner[t]);
             }
-        } else {
-            const uint4 q = *(const uint4 *)(quant_s + ((size_t)b * 32 + lane) * 16);
-            const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+        }
+        const float d = __half2float(__ushort_as_half(dh));
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t w = wd[i], w5 = wd[i] >> 20;
-                const float v0 = __int_as_float((w & 0xFu) | 0x4B000000u);
-                const float v1 = __int_as_float((w & 0xF0u) | 0x4B000000u);
-                const float v2 = __int_as_float((w & 0xF00u) | 0x4B000000u);
-                const float v3 = __int_as_float((w & 0xF000u) | 0x4B000000u);
-                const float v4 = __int_as_float((w & 0xF0000u) | 0x4B000000u);
-                const float v5 = __int_as_float((w5 & 0xFu) | 0x4B000000u);
-                const float v6 = __int_as_float((w5 & 0xF0u) | 0x4B000000u);
-                const float v7 = __int_as_float((w5 & 0xF00u) | 0x4B000000u);
-                const unsigned long long p01 = f2_add(f2_pack(v0, v1), MAG4);
-                const unsigned long long p23 = f2_add(f2_pack(v2, v3), MAG4);
-                const unsigned long long p45 = f2_add(f2_pack(v4, v5), MAG4);
-                const unsigned long long p67 = f2_add(f2_pack(v6, v7), MAG4);
+        for (int t = 0; t < NT; ++t) {
+            float lo, hi;
+            f2_unpack(inner[t], lo, hi);
+            acc[t] = fmaf(d, lo + hi, acc[t]);
+        }
+    } else {
+        const uint4 q = *(const uint4 *)(quant_s + ((size_t)b * 32 + lane) * 16);
+        const uint32_t dm = *(const uint32_t *)(scale_s + ((size_t)b * 32 + lane) * 4);
+        const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    const float4 xa = *(const float4 *)(act + (size_t)t * Kr + b * 32 + 8 * i);
-                    const float4 xb = *(const float4 *)(act + (size_t)t * Kr + b * 32 + 8 * i + 4);
-                    inner[t] = f2_fma(p01, f2_pack(xa.x, xa.y), inner[t]);
-                    inner[t] = f2_fma(p23, f2_pack(xa.z, xa.w), inner[t]);
-                    inner[t] = f2_fma(p45, f2_pack(xb.x, xb.y), inner[t]);
-                    inner[t] = f2_fma(p67, f2_pack(xb.z, xb.w), inner[t]);
-                }
-            }
-            const uint32_t dm = *(const uint32_t *)(scale_s + ((size_t)b * 32 + lane) * 4);
-            const float d = __half2float(__ushort_as_half((unsigned short)(dm & 0xFFFFu)));
-            const float m = __half2float(__ushort_as_half((unsigned short)(dm >> 16)));
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w = wd[i], w5 = wd[i] >> 20;
+            const float v0 = __int_as_float((w & 0xFu) | 0x4B000000u);
+            const float v1 = __int_as_float((w & 0xF0u) | 0x4B000000u);
+            const float v2 = __int_as_float((w & 0xF00u) | 0x4B000000u);
+            const float v3 = __int_as_float((w & 0xF000u) | 0x4B000000u);
+            const float v4 = __int_as_float((w & 0xF0000u) | 0x4B000000u);
+            const float v5 = __int_as_float((w5 & 0xFu) | 0x4B000000u);
+            const float v6 = __int_as_float((w5 & 0xF0u) | 0x4B000000u);
+            const float v7 = __int_as_float((w5 & 0xF00u) | 0x4B000000u);
+            const unsigned long long p01 = f2_add(f2_pack(v0, v1), MAG4);
+            const unsigned long long p23 = f2_add(f2_pack(v2, v3), MAG4);
+            const unsigned long long p45 = f2_add(f2_pack(v4, v5), MAG4);
+            const unsigned long long p67 = f2_add(f2_pack(v6, v7), MAG4);
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                float lo, hi;
-                f2_unpack(inner[t], lo, hi);
-                acc[t] = fmaf(d, lo + hi, fmaf(m, asum[(size_t)t * nbr + b], acc[t]));
+                const float4 xa = *(const float4 *)(act + (size_t)t * Kr + b * 32 + 8 * i);
+                const float4 xb = *(const float4 *)(act + (size_t)t * Kr + b * 32 + 8 * i + 4);
+                inner[t] = f2_fma(p01, f2_pack(xa.x, xa.y), inner[t]);
+                inner[t] = f2_fma(p23, f2_pack(xa.z, xa.w), inner[t]);
+                inner[t] = f2_fma(p45, f2_pack(xb.x, xb.y), inner[t]);
+                inner[t] = f2_fma(p67, f2_pack(xb.z, xb.w), inner[t]);
             }
+        }
+        const float d = __half2float(__ushort_as_half((unsigned short)(dm & 0xFFFFu)));
+        const float m = __half2float(__ushort_as_half((unsigned short)(dm >> 16)));
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float lo, hi;
+            f2_unpack(inner[t], lo, hi);
+            acc[t] = fmaf(d, lo + hi, fmaf(m, asum[(size_t)t * nbr + b], acc[t]));
         }
     }
 }
 
+// A warp's blocks [b0, b1) of one lane's row; with few tokens two blocks per step so that
+// their loads and FMA chains interleave.
+template <int QT, int NT>
+__device__ __forceinline__ void tile_dot(const unsigned char *quant_s, const unsigned char *scale_s,
+                                         const float *act, const float *asum, int Kr, int nbr, int b0, int b1,
+                                         int lane, float *acc) {
+    int b = b0;
+    if constexpr (NT <= 4)  // few tokens: two blocks' chains side by side (more tokens carry their own ILP)
+        for (; b + 1 < b1; b += 2) {
+            block_dot<QT, NT>(quant_s, scale_s, act, asum, Kr, nbr, b, lane, acc);
+            block_dot<QT, NT>(quant_s, scale_s, act, asum, Kr, nbr, b + 1, lane, acc);
+        }
+    for (; b < b1; ++b) block_dot<QT, NT>(quant_s, scale_s, act, asum, Kr, nbr, b, lane, acc);
+}
+
 template <int QT>
-__device__ __forceinline__ void tile_dot_dispatch(int ntp, const unsigned char *quant_s,
-                                                  const unsigned char *scale_s, const float *act,
-                                                  const float *asum, int Kr, int nbr, int b0, int b1,
-                                                  int lane, float *acc) {
-    switch (ntp) {
+__device__ __forceinline__ void tile_dot_dispatch(int nt, const unsigned char *quant_s, const unsigned char *scale_s,
+                                                  const float *act, const float *asum, int Kr, int nbr, int b0,
+                                                  int b1, int lane, float *acc) {
+    switch (nt) {
         case 1: tile_dot<QT, 1>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
         case 2: tile_dot<QT, 2>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
+        case 3: tile_dot<QT, 3>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
         case 4: tile_dot<QT, 4>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
+        case 5: tile_dot<QT, 5>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
+        case 6: tile_dot<QT, 6>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
+        case 7: tile_dot<QT, 7>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
         default: tile_dot<QT, 8>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
     }
 }
 
-__host__ __device__ __forceinline__ int pow2_tokens(int nt) { return nt <= 1 ? 1 : nt <= 2 ? 2 : nt <= 4 ? 4 : 8; }
-
 // Block sums of the (unscaled) activations for the 4-bit min term.
 template <int QT>
-__device__ __forceinline__ void compute_asum(const float *act, float *asum, int ntp, int nbr, int Kr) {
+__device__ __forceinline__ void compute_asum(const float *act, float *asum, int nt, int nbr, int Kr) {
     if constexpr (QT == MOE_Q4_SM) {
-    for (int i = threadIdx.x; i < ntp * nbr; i += GV_THREADS) {
-        const int t = i / nbr, b = i % nbr;
-        float s = 0.f;
-        for (int c = 0; c < 32; ++c) s += act[(size_t)t * Kr + b * 32 + c] * q4_act_unscale(c);
-        asum[i] = s;
+        for (int i = threadIdx.x; i < nt * nbr; i += GV_THREADS) {
+            const int t = i / nbr, b = i % nbr;
+            float s = 0.f;
+            for (int c = 0; c < 32; ++c) s += act[(size_t)t * Kr + b * 32 + c] * q4_act_unscale(c);
+            asum[i] = s;
+        }
     }
-    }
-}
-
-// Reduce the 4 warps' accumulators (fixed order) for token t of this pass.
-__device__ __forceinline__ float reduce_warps(const float *red, int t, int lane) {
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < GV_WARPS; ++w) s += red[((size_t)w * GV_TOK + t) * 32 + lane];
-    return s;
 }
 
 struct FfnParams {
     const void *x;
     int T, H, F, k, E, KS, RT;
-    const int32_t *ids;
     const float *weights;
     const int32_t *ws_ints;
+    int32_t *tickets;  // [E][F/32] gate/up arrivals per (active expert, row tile)
+    const ActInfo *info;
     float *gu;
-    const int32_t *slot_table;
-    int n_slots;
-    const uint8_t *pool;
-    size_t slot_bytes;
+    float *h;
     float *partial;
     int *status;
-    int ntok;          // activation rows staged per pass (<= GV_TOK)
-    const unsigned long long *fill_src;  // [E]: pinned host image of an expert to fill, or 0
+    int stages;        // ring stages of this launch
+    int x_vec;         // x is 16-byte aligned: vector loads
 };
 
-// Fill path of a unit whose expert missed: its bytes come from the expert's pinned host
-// image over the CPU-GPU link (16-byte loads by every thread) and are written both to the
-// unit's shared-memory stage and through to the expert's slot, so the slot is filled by
-// the kernels that use it.  Same byte ranges as issue_unit_copies.
-template <int QT>
-__device__ void fill_unit(const uint8_t *src_mat, uint8_t *dst_mat, int R, int K, int g, int kb0, int nbr,
-                          unsigned char *smem, const UnitSmem &L) {
-    const int QB = QT == MOE_Q8_0 ? 1024 : 512;
-    const int SB = 32 * moe_scale_entry_bytes(QT);
-    const int PPB = QT == MOE_Q8_0 ? 2 : 1;
-    const size_t qoff = moe_piece_offset(QT, K, g, kb0 * PPB);
-    const size_t soff = moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, g, kb0);
-    const int nq = nbr * QB / 16, ns = nbr * SB / 16;
-    for (int i = threadIdx.x; i < nq + ns; i += GV_THREADS) {
-        const bool q = i < nq;
-        const size_t off = q ? qoff + (size_t)i * 16 : soff + (size_t)(i - nq) * 16;
-        const uint4 v = __ldcs((const uint4 *)(src_mat + off));
-        *(uint4 *)(smem + (q ? L.quant + (size_t)i * 16 : L.scale + (size_t)(i - nq) * 16)) = v;
-        __stcs((uint4 *)(dst_mat + off), v);
-    }
+__device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-template <int XT>
-__device__ __forceinline__ float load_x(const void *x, size_t i) {
-    if (XT == MOE_BF16) return __bfloat162float(((const __nv_bfloat16 *)x)[i]);
-    return ((const float *)x)[i];
+// This CTA's contiguous share [u0, u1) of the units, balanced by work: unit u of active
+// expert a starts at cost per_a * P[a] + (u - a * per_a) * cost(a) (P: prefix of the
+// experts' unit costs), and CTA c takes the units starting in [c C / G, (c+1) C / G).
+__device__ __forceinline__ int unit_at_cost(long long x, int n_act, int per_a, const int *P, const ActInfo *info) {
+    const long long C = (long long)per_a * P[n_act];
+    if (x >= C) return n_act * per_a;
+    int lo = 0, hi = n_act - 1;  // largest a with per_a * P[a] <= x
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if ((long long)per_a * P[mid] <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    const long long rem = x - (long long)per_a * P[lo];
+    const int c = unit_cost(info[lo].n_e);
+    return lo * per_a + (int)((rem + c - 1) / c);
 }
 
-// ------------------------------------------------------------------ G1: gate / up
-
-template <int QT, int XT>
-__global__ void __launch_bounds__(GV_THREADS) gateup_kernel(FfnParams p) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int RTF = p.F / 32;
-    int u = blockIdx.x;
-    const int ks = u % p.KS; u /= p.KS;
-    const int g = u % RTF;   u /= RTF;
-    const int m = u & 1;
-    const int a = u >> 1;
-    const int *ints = p.ws_ints;
-    if (a >= ints[0]) return;                       // uniform: fewer active experts than the grid
-    const int e = ints[ws_active_off() + a];
-    const int slot = p.slot_table ? p.slot_table[e] : e;
-    if (slot < 0 || slot >= p.n_slots) {
-        if (threadIdx.x == 0) moe_set_status(p.status, MOE_ERR_INVALID);
-        return;
-    }
-    const int K = p.H, nbr = (K / 32) / p.KS, kb0 = ks * nbr, Kr = nbr * 32;
-    const UnitSmem L = unit_smem(QT, nbr, p.ntok);
-    const uint8_t *mat = p.pool + (size_t)slot * p.slot_bytes + moe_expert_matrix_offset(QT, p.H, p.F, m);
-    const uint8_t *fill = p.fill_src ? (const uint8_t *)p.fill_src[e] : nullptr;
-    bool ready = false, ok = true;
-    if (fill) {
-        // visible to every warp after the first __syncthreads of the token loop
-        fill_unit<QT>(fill + moe_expert_matrix_offset(QT, p.H, p.F, m), (uint8_t *)mat, p.F, K, g, kb0, nbr, smem, L);
-        ready = true;
-    } else if (threadIdx.x == 0) {
-        issue_unit_copies<QT>(mat, p.F, K, g, kb0, nbr, smem, L);
-    }
-    __syncthreads();
-
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    int b0, b1;
-    warp_blocks(nbr, warp, b0, b1);
-    float *act = (float *)(smem + L.act);
-    float *asum = (float *)(smem + L.asum);
-    float *red = (float *)(smem + L.red);
-    const int pos0 = ints[ws_aoff_off(p.E) + a];
-    const int n_e = ints[ws_aoff_off(p.E) + a + 1] - pos0;
-    const int *routes = ints + ws_routes_off(p.E);
-
-    for (int tg = 0; tg < n_e; tg += GV_TOK) {
-        const int nt = min(GV_TOK, n_e - tg), ntp = pow2_tokens(nt);
-        for (int i = threadIdx.x; i < ntp * Kr; i += GV_THREADS) {
-            const int t = i / Kr, c = i % Kr;
-            float v = 0.f;
-            if (t < nt) {
-                const int tok = routes[pos0 + tg + t] / p.k;
-                v = load_x<XT>(p.x, (size_t)tok * p.H + (size_t)kb0 * 32 + c);
-                if (QT == MOE_Q4_SM) v *= q4_act_scale(c);
-            }
-            act[i] = v;
-        }
-        __syncthreads();
-        compute_asum<QT>(act, asum, ntp, nbr, Kr);
-        __syncthreads();
-        if (!ready) {
-            if (b1 > b0) ok = mbar_wait_bounded((uint64_t *)(smem + L.bars) + warp, 0, p.status);
-            ready = true;
-        }
-        float acc[GV_TOK];
-#pragma unroll
-        for (int t = 0; t < GV_TOK; ++t) acc[t] = 0.f;
-        if (ok) tile_dot_dispatch<QT>(ntp, smem + L.quant, smem + L.scale, act, asum, Kr, nbr, b0, b1, lane, acc);
-#pragma unroll
-        for (int t = 0; t < GV_TOK; ++t)
-            if (t < ntp) red[((size_t)warp * GV_TOK + t) * 32 + lane] = acc[t];
-        __syncthreads();
-        for (int t = warp; t < nt; t += GV_WARPS) {
-            const float s = reduce_warps(red, t, lane);
-            p.gu[(((size_t)ks * 2 + m) * p.RT + pos0 + tg + t) * p.F + 32 * g + lane] = s;
-        }
-        __syncthreads();
-    }
-    // never leave with this warp's copies in flight (a timed-out wait gets a second bounded wait)
-    if ((!ready || !ok) && b1 > b0) mbar_wait_bounded((uint64_t *)(smem + L.bars) + warp, 0, p.status);
+__device__ __forceinline__ void cta_range(int n_act, int per_a, const int *P, const ActInfo *info, int &u0,
+                                          int &u1) {
+    const long long C = (long long)per_a * P[n_act];
+    u0 = unit_at_cost(C * blockIdx.x / gridDim.x, n_act, per_a, P, info);
+    u1 = unit_at_cost(C * (blockIdx.x + 1) / gridDim.x, n_act, per_a, P, info);
 }
 
-// ------------------------------------------------------------------ G2: down + weighted scatter
-
-template <int QT>
-__global__ void __launch_bounds__(GV_THREADS) down_kernel(FfnParams p) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int RTH = p.H / 32;
-    const int g = blockIdx.x % RTH;
-    const int a = blockIdx.x / RTH;
-    const int *ints = p.ws_ints;
-    if (a >= ints[0]) return;
-    const int e = ints[ws_active_off() + a];
-    const int slot = p.slot_table ? p.slot_table[e] : e;
-    if (slot < 0 || slot >= p.n_slots) {
-        if (threadIdx.x == 0) moe_set_status(p.status, MOE_ERR_INVALID);
-        return;
-    }
-    const int K = p.F, nbr = K / 32, Kr = K;
-    const UnitSmem L = unit_smem(QT, nbr, p.ntok);
-    const uint8_t *mat = p.pool + (size_t)slot * p.slot_bytes + moe_expert_matrix_offset(QT, p.H, p.F, 2);
-    const uint8_t *fill = p.fill_src ? (const uint8_t *)p.fill_src[e] : nullptr;
-    bool ready = false, ok = true;
-    if (fill) {
-        fill_unit<QT>(fill + moe_expert_matrix_offset(QT, p.H, p.F, 2), (uint8_t *)mat, p.H, K, g, 0, nbr, smem, L);
-        ready = true;
-    } else if (threadIdx.x == 0) {
-        issue_unit_copies<QT>(mat, p.H, K, g, 0, nbr, smem, L);
-    }
-    __syncthreads();
-
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    int b0, b1;
-    warp_blocks(nbr, warp, b0, b1);
-    float *act = (float *)(smem + L.act);
-    float *asum = (float *)(smem + L.asum);
-    float *red = (float *)(smem + L.red);
-    const int pos0 = ints[ws_aoff_off(p.E) + a];
-    const int n_e = ints[ws_aoff_off(p.E) + a + 1] - pos0;
-    const int *routes = ints + ws_routes_off(p.E);
-
-    for (int tg = 0; tg < n_e; tg += GV_TOK) {
-        const int nt = min(GV_TOK, n_e - tg), ntp = pow2_tokens(nt);
-        // h = silu(gate) * up from the K-split partial dot products (fixed ks order)
-        for (int i = threadIdx.x; i < ntp * Kr; i += GV_THREADS) {
-            const int t = i / Kr, c = i % Kr;
-            float v = 0.f;
-            if (t < nt) {
-                const size_t pos = (size_t)pos0 + tg + t;
-                float gs = 0.f, us = 0.f;
-                for (int ks = 0; ks < p.KS; ++ks) {
-                    gs += p.gu[(((size_t)ks * 2 + 0) * p.RT + pos) * p.F + c];
-                    us += p.gu[(((size_t)ks * 2 + 1) * p.RT + pos) * p.F + c];
+// Stage the activations of route positions [pos, pos+nt) for columns [c0, c0+Kr): gate/up
+// reads x (fp32 or bf16) of the routes' tokens (route of position pos+t at rbase[rpos+t]),
+// down reads h.  Zero rows are not
+// needed: the dot products run over exactly nt rows.
+template <int QT, int XT, bool DOWN>
+__device__ __forceinline__ void load_act(const FfnParams &p, const int *rbase, int rpos, int pos, int nt, int c0,
+                                         int Kr, float *act) {
+    const int nq = Kr / 4;
+    for (int idx = threadIdx.x; idx < nt * nq; idx += GV_THREADS) {
+        const int t = idx / nq, c = 4 * (idx - t * nq);
+        float4 v;
+        if (DOWN) {
+            v = *(const float4 *)(p.h + (size_t)(pos + t) * p.F + c);
+        } else {
+            const size_t off = (size_t)(rbase[rpos + t] / p.k) * p.H + c0 + c;
+            if (XT == MOE_BF16) {
+                const __nv_bfloat16 *xb = (const __nv_bfloat16 *)p.x + off;
+                if (p.x_vec) {
+                    const uint2 r = *(const uint2 *)xb;
+                    const float2 lo = __bfloat1622float2(*(const __nv_bfloat162 *)&r.x);
+                    const float2 hi = __bfloat1622float2(*(const __nv_bfloat162 *)&r.y);
+                    v = make_float4(lo.x, lo.y, hi.x, hi.y);
+                } else {
+                    v = make_float4(__bfloat162float(xb[0]), __bfloat162float(xb[1]), __bfloat162float(xb[2]),
+                                    __bfloat162float(xb[3]));
                 }
-                v = gs / (1.0f + expf(-gs)) * us;
-                if (QT == MOE_Q4_SM) v *= q4_act_scale(c);
+            } else {
+                const float *xf = (const float *)p.x + off;
+                v = p.x_vec ? *(const float4 *)xf : make_float4(xf[0], xf[1], xf[2], xf[3]);
             }
-            act[i] = v;
         }
-        __syncthreads();
-        compute_asum<QT>(act, asum, ntp, nbr, Kr);
-        __syncthreads();
-        if (!ready) {
-            if (b1 > b0) ok = mbar_wait_bounded((uint64_t *)(smem + L.bars) + warp, 0, p.status);
-            ready = true;
+        if (QT == MOE_Q4_SM) {
+            v.x *= q4_act_scale(c);
+            v.y *= q4_act_scale(c + 1);
+            v.z *= q4_act_scale(c + 2);
+            v.w *= q4_act_scale(c + 3);
         }
-        float acc[GV_TOK];
-#pragma unroll
-        for (int t = 0; t < GV_TOK; ++t) acc[t] = 0.f;
-        if (ok) tile_dot_dispatch<QT>(ntp, smem + L.quant, smem + L.scale, act, asum, Kr, nbr, b0, b1, lane, acc);
-#pragma unroll
-        for (int t = 0; t < GV_TOK; ++t)
-            if (t < ntp) red[((size_t)warp * GV_TOK + t) * 32 + lane] = acc[t];
-        __syncthreads();
-        for (int t = warp; t < nt; t += GV_WARPS) {
-            const float s = reduce_warps(red, t, lane);
-            const int r = routes[pos0 + tg + t];
-            p.partial[(size_t)r * p.H + 32 * g + lane] = p.weights[r] * s;
-        }
-        __syncthreads();
+        *(float4 *)(act + (size_t)t * Kr + c) = v;
     }
-    // never leave with this warp's copies in flight (a timed-out wait gets a second bounded wait)
-    if ((!ready || !ok) && b1 > b0) mbar_wait_bounded((uint64_t *)(smem + L.bars) + warp, 0, p.status);
+}
+
+// Count one row write of (active expert a, row tile g) — 2*KS*n_e in all, one per (K range,
+// matrix, token); n_e and pos0 are the expert's token count and first route position.  The warp whose write completes the count forms h = silu(gate) * up for
+// every token of the expert on those rows, summing the K ranges in order.  The fence
+// publishes this warp's writes before the count; the last writer's fence orders the reads.
+struct TicketArgs {
+    int32_t *tickets;
+    const float *gu;
+    float *h;
+    int F, RT, KS;
+};
+
+__device__ __noinline__ void gu_ticket(TicketArgs p, int a, int g, int n_e, int pos0, int lane) {
+    __threadfence();
+    int last = 0;
+    if (lane == 0) last = atomicAdd(&p.tickets[a * (p.F / 32) + g], 1) == 2 * p.KS * n_e - 1;
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __threadfence();
+    constexpr int TB = 4;  // tokens whose partial sums are loaded together
+    for (int t0 = 0; t0 < n_e; t0 += TB) {
+        float gv[TB][4], uv[TB][4];
+#pragma unroll
+        for (int t = 0; t < TB; ++t)
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+                gv[t][k2] = uv[t][k2] = 0.f;
+                if (t0 + t < n_e && k2 < p.KS) {
+                    const size_t q = (size_t)(pos0 + t0 + t) * p.F + 32 * g + lane;
+                    gv[t][k2] = __ldcg(p.gu + ((size_t)k2 * 2 + 0) * p.RT * p.F + q);
+                    uv[t][k2] = __ldcg(p.gu + ((size_t)k2 * 2 + 1) * p.RT * p.F + q);
+                }
+            }
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+            if (t0 + t >= n_e) break;
+            float gs = 0.f, us = 0.f;  // K ranges summed in ascending order
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2)
+                if (k2 < p.KS) {
+                    gs += gv[t][k2];
+                    us += uv[t][k2];
+                }
+            for (int k2 = 4; k2 < p.KS; ++k2) {
+                const size_t q = (size_t)(pos0 + t0 + t) * p.F + 32 * g + lane;
+                gs += __ldcg(p.gu + ((size_t)k2 * 2 + 0) * p.RT * p.F + q);
+                us += __ldcg(p.gu + ((size_t)k2 * 2 + 1) * p.RT * p.F + q);
+            }
+            p.h[(size_t)(pos0 + t0 + t) * p.F + 32 * g + lane] = gs / (1.0f + expf(-gs)) * us;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ G1 / G2: the ring kernel
+//
+// G1 (gate/up): units per active expert are KS K ranges x 2 matrices x F/32 row tiles,
+// ordered (ks, m, g) so that consecutive units of a CTA share the expert's activations
+// for one K range; each unit writes its K range's dot products to gu, and the warp whose
+// write completes an (expert, row tile) writes h = silu(sum gate) * (sum up) for it.
+// G2 (down): units per active expert are H/32 row tiles over the whole of F with h as
+// activations; each unit writes w[r] * (Wd h) for its routes r.
+//
+// Ring protocol: stage s = i % S holds the CTA's i-th unit.  Thread 0 issues unit i+S-1
+// at the top of iteration i, into the stage that unit i-1 used; every thread has finished
+// reading that stage before the barrier that ends unit i-1's dot products.  A fill unit or
+// a skipped expert arrives on its stage's mbarrier without bytes, so each stage completes
+// exactly one phase per use and the waits use parity (i / S) & 1.
+
+template <int QT, int XT, bool DOWN>
+__global__ void __launch_bounds__(GV_THREADS, 2) ffn_ring_kernel(FfnParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int S = p.stages;
+    const int RTF = p.F / 32, RTH = p.H / 32;
+    const int nbr = DOWN ? p.F / 32 : (p.H / 32) / p.KS, Kr = nbr * 32;
+    const int R = DOWN ? p.H : p.F, K = DOWN ? p.F : p.H;
+    const int per_a = DOWN ? RTH : p.KS * 2 * RTF;
+    int u0, u1;
+    cta_range(p.ws_ints[0], per_a, p.ws_ints + ws_cost_off(p.E, p.RT, p.F), p.info, u0, u1);
+    if (u0 >= u1) return;
+    const RingSmem L = ring_smem(QT, nbr, min(p.T, GV_TOK), S);
+    uint64_t *bars = (uint64_t *)(smem + L.bars);
+    unsigned char *stages = smem + L.stages;
+    float *act = (float *)(smem + L.act);
+    float *asum = (float *)(smem + L.asum);
+    float *red = (float *)(smem + L.red);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int *routes = p.ws_ints + ws_routes_off(p.E);
+
+    // the experts and routes of this CTA's range, in shared memory when they fit
+    const int a_lo = u0 / per_a, a_hi = (u1 - 1) / per_a;
+    const bool icache = a_hi - a_lo < GV_ICACHE;
+    ActInfo *info_s = (ActInfo *)(smem + L.info);
+    const int pos_lo = p.info[a_lo].pos0, pos_hi = p.info[a_hi].pos0 + p.info[a_hi].n_e;
+    const bool rcache = pos_hi - pos_lo <= GV_RCACHE;
+    int *rts_s = (int *)(smem + L.rts);
+    float *wts_s = (float *)(smem + L.wts);
+    if (icache)
+        for (int a = a_lo + threadIdx.x; a <= a_hi; a += GV_THREADS) info_s[a - a_lo] = p.info[a];
+    if (rcache)
+        for (int q = pos_lo + threadIdx.x; q < pos_hi; q += GV_THREADS) {
+            const int r = routes[q];
+            rts_s[q - pos_lo] = r;
+            if (DOWN) wts_s[q - pos_lo] = p.weights[r];
+        }
+    auto info_at = [&](int a) { return icache ? info_s[a - a_lo] : p.info[a]; };
+    const int *rbase = rcache ? rts_s : routes;
+    const int rpos0 = rcache ? pos_lo : 0;  // route position q is at rbase[q - rpos0]
+
+    // unit u -> active expert a, K range ks, matrix m, row tile g
+    auto decode = [&](int u, int &a, int &ks, int &m, int &g) {
+        a = u / per_a;
+        int r = u - a * per_a;
+        if (DOWN) {
+            ks = 0;
+            m = 2;
+            g = r;
+        } else {
+            ks = r / (2 * RTF);
+            r -= ks * 2 * RTF;
+            m = r / RTF;
+            g = r - m * RTF;
+        }
+    };
+    auto issue = [&](int u, int s, bool cached) {  // thread 0 only
+        int a, ks, m, g;
+        decode(u, a, ks, m, g);
+        const ActInfo in = cached ? info_at(a) : p.info[a];
+        if (in.n_e == 0 || in.fill) {
+            mbar_arrive_plain(&bars[s]);
+            return;
+        }
+        issue_unit<QT>((const uint8_t *)in.src + moe_expert_matrix_offset(QT, p.H, p.F, m), R, K, g, ks * nbr, nbr,
+                       stages + (size_t)s * L.stage_bytes, L.scale_off, &bars[s]);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+        for (int j = 0; j < S - 1 && u0 + j < u1; ++j) issue(u0 + j, j, false);
+    }
+    __syncthreads();
+
+    int b0, b1;
+    warp_blocks(nbr, warp, b0, b1);
+    int cur_a = -1, cur_ks = -1, cur_tg = -1;
+    int pend_a = -1, pend_g = 0, pend_ne = 0, pend_pos = 0;  // gate/up: last row write not yet counted
+    const TicketArgs targs{p.tickets, p.gu, p.h, p.F, p.RT, p.KS};
+    int i = 0;
+    bool failed = false;
+    for (; u0 + i < u1; ++i) {
+        const int u = u0 + i, s = i % S;
+        if (threadIdx.x == 0 && u + S - 1 < u1) issue(u + S - 1, (i + S - 1) % S, true);
+        int a, ks, m, g;
+        decode(u, a, ks, m, g);
+        const ActInfo in = info_at(a);
+        unsigned char *stage = stages + (size_t)s * L.stage_bytes;
+        // activations of the first token pass, loaded while the unit's bytes arrive
+        const bool fresh = in.n_e > 0 && (a != cur_a || ks != cur_ks || cur_tg != 0);
+        if (fresh) load_act<QT, XT, DOWN>(p, rbase, in.pos0 - rpos0, in.pos0, min(GV_TOK, in.n_e), ks * Kr, Kr, act);
+        const bool ok = mbar_wait_bounded(&bars[s], (i / S) & 1, p.status);
+        if (in.fill && in.n_e > 0) {
+            const size_t mo = moe_expert_matrix_offset(QT, p.H, p.F, m);
+            fill_unit<QT>((const uint8_t *)in.src + mo, (uint8_t *)in.dst + mo, R, K, g, ks * nbr, nbr, stage,
+                          L.scale_off);
+            fence_proxy_async_smem();  // a later bulk copy overwrites this stage
+        }
+        // uniform: every thread saw its stage complete; the activations and a filled stage
+        // are visible; this unit's writes of red follow the previous unit's reads
+        if (!__syncthreads_and(ok)) {
+            failed = true;
+            break;
+        }
+        if (fresh) {
+            cur_a = a;
+            cur_ks = ks;
+            cur_tg = 0;
+            if (QT == MOE_Q4_SM) {
+                compute_asum<QT>(act, asum, min(GV_TOK, in.n_e), nbr, Kr);
+                __syncthreads();
+            }
+        }
+        for (int tg = 0; tg < in.n_e; tg += GV_TOK) {
+            const int nt = min(GV_TOK, in.n_e - tg);
+            if (tg != cur_tg) {  // further passes of an expert with more than 8 tokens
+                load_act<QT, XT, DOWN>(p, rbase, in.pos0 + tg - rpos0, in.pos0 + tg, nt, ks * Kr, Kr, act);
+                __syncthreads();
+                if (QT == MOE_Q4_SM) {
+                    compute_asum<QT>(act, asum, nt, nbr, Kr);
+                    __syncthreads();
+                }
+                cur_tg = tg;
+            }
+            float acc[GV_TOK];
+#pragma unroll
+            for (int t = 0; t < GV_TOK; ++t) acc[t] = 0.f;
+            tile_dot_dispatch<QT>(nt, stage, stage + L.scale_off, act, asum, Kr, nbr, b0, b1, lane, acc);
+#pragma unroll
+            for (int t = 0; t < GV_TOK; ++t)
+                if (t < nt) red[((size_t)warp * GV_TOK + t) * 32 + lane] = acc[t];
+            __syncthreads();  // red complete; every thread is done reading this stage and act
+            if (warp < nt) {
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < GV_WARPS; ++w) sum += red[((size_t)w * GV_TOK + warp) * 32 + lane];
+                const int pos = in.pos0 + tg + warp;
+                if (DOWN) {
+                    const int r = rbase[pos - rpos0];
+                    const float wr = rcache ? wts_s[pos - rpos0] : p.weights[r];
+                    p.partial[(size_t)r * p.H + 32 * g + lane] = wr * sum;
+                } else {
+                    // this warp's previous row writes have drained while it computed: their
+                    // ticket costs no wait now
+                    if (pend_a >= 0) gu_ticket(targs, pend_a, pend_g, pend_ne, pend_pos, lane);
+                    p.gu[(((size_t)ks * 2 + m) * p.RT + pos) * p.F + 32 * g + lane] = sum;
+                    pend_a = a;
+                    pend_g = g;
+                    pend_ne = in.n_e;
+                    pend_pos = in.pos0;
+                }
+            }
+            if (tg + GV_TOK < in.n_e) __syncthreads();  // red and act are rewritten by the next pass
+        }
+    }
+    if (!DOWN && pend_a >= 0) gu_ticket(targs, pend_a, pend_g, pend_ne, pend_pos, lane);
+    // A wait ran out: never leave with copies in flight.  Units i .. last issued are
+    // unconsumed; give each a second bounded wait.
+    if (failed && threadIdx.x == 0) {
+        const int last = min(u1 - 1, u0 + i + S - 1);
+        for (int j = i; u0 + j <= last; ++j) mbar_wait_bounded(&bars[j % S], (j / S) & 1, p.status);
+    }
 }
 
 // ------------------------------------------------------------------ P1: permute
 
-// Stable counting sort of the routes r = t*k + j by expert (restricted to a subset),
-// plus the ascending list of active experts and their route ranges.
+// Stable counting sort of the routes r = t*k + j by expert (restricted to a subset), the
+// ascending list of active experts, their route ranges, and per active expert where its
+// weights are read from (slot in the pool, or its pinned host image for a fill).
 __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict__ ids, int R, int E,
                                                       const int32_t *__restrict__ subset, int n_subset,
-                                                      int32_t *__restrict__ ints, int *status) {
+                                                      int32_t *__restrict__ ints, ActInfo *__restrict__ info,
+                                                      const int32_t *__restrict__ slot_table, int n_slots,
+                                                      const uint8_t *pool, size_t slot_bytes,
+                                                      const unsigned long long *__restrict__ fill_src,
+                                                      int RTF, int *status) {
     __shared__ int cnt[MOE_MAX_E], off[MOE_MAX_E + 1], run[MOE_MAX_E];
     __shared__ unsigned char insub[MOE_MAX_E];
     __shared__ int chunk_e[256];
+    __shared__ int n_act;
     const int tid = threadIdx.x;
     for (int e = tid; e < E; e += 256) {
         cnt[e] = 0;
@@ -478,10 +663,10 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
         if (insub[e]) atomicAdd(&cnt[e], 1);
     }
     __syncthreads();
+    int *active = ints + ws_active_off();
+    int *aoff = ints + ws_aoff_off(E);
     if (tid == 0) {
         int s = 0, na = 0;
-        int *active = ints + ws_active_off();
-        int *aoff = ints + ws_aoff_off(E);
         for (int e = 0; e < E; ++e) {
             off[e] = s;
             if (cnt[e] > 0) {
@@ -493,8 +678,42 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
         }
         aoff[na] = s;
         ints[0] = na;
+        n_act = na;
+
     }
     __syncthreads();
+    int *tickets = ints + ws_ticket_off(E, R);
+    for (int i = tid; i < n_act * RTF; i += 256) tickets[i] = 0;
+    for (int a = tid; a < n_act; a += 256) {
+        const int e = active[a];
+        const int slot = slot_table ? slot_table[e] : e;
+        ActInfo in;
+        in.e = e;
+        in.pos0 = aoff[a];
+        in.n_e = aoff[a + 1] - aoff[a];
+        in.fill = 0;
+        in.src = in.dst = 0ull;
+        if (slot < 0 || slot >= n_slots) {
+            moe_set_status(status, MOE_ERR_INVALID);
+            in.n_e = 0;  // nothing of this expert is read
+        } else {
+            in.dst = (unsigned long long)(pool + (size_t)slot * slot_bytes);
+            const unsigned long long f = fill_src ? fill_src[e] : 0ull;
+            in.fill = f != 0ull;
+            in.src = f ? f : in.dst;
+        }
+        info[a] = in;
+    }
+    __syncthreads();
+    if (tid == 0) {  // work prefix over the active experts (skipped experts cost 1 per unit)
+        int *P = ints + ws_cost_off(E, R, RTF * 32);
+        int c = 0;
+        for (int a = 0; a < n_act; ++a) {
+            P[a] = c;
+            c += unit_cost(info[a].n_e);
+        }
+        P[n_act] = c;
+    }
     int *routes = ints + ws_routes_off(E);
     for (int c0 = 0; c0 < R; c0 += 256) {
         const int r = c0 + tid;
@@ -565,13 +784,64 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(const float4 *__restr
     }
 }
 
+// Resident CTAs per SM of a ring kernel at a dynamic shared-memory size, and the SM
+// count, cached per (device, kernel, size).  The kernel's shared-memory limit is only
+// ever raised, so every cached size stays launchable.
+struct OccEntry {
+    int dev;
+    const void *fn;
+    size_t smem;
+    int ctas;  // resident CTAs on the whole device
+};
+
+int ring_grid_capacity(const void *fn, size_t smem, int *ctas) {
+    static std::mutex mu;
+    static OccEntry tab[64];
+    static int n_tab = 0;
+    static struct { int dev; const void *fn; size_t max; } lim[32];
+    static int n_lim = 0;
+    int dev = 0;
+    MOE_TRY_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < n_tab; ++i)
+        if (tab[i].dev == dev && tab[i].fn == fn && tab[i].smem == smem) {
+            *ctas = tab[i].ctas;
+            return MOE_OK;
+        }
+    int li = -1;
+    for (int i = 0; i < n_lim; ++i)
+        if (lim[i].dev == dev && lim[i].fn == fn) li = i;
+    if (li < 0 || lim[li].max < smem) {
+        MOE_TRY_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        if (li < 0 && n_lim < 32) li = n_lim++;
+        if (li >= 0) lim[li] = {dev, fn, smem};
+    }
+    int occ = 0, sms = 0;
+    MOE_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, GV_THREADS, smem));
+    MOE_TRY_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    if (occ < 1 || sms < 1) return MOE_ERR_UNSUPPORTED;
+    *ctas = occ * sms;
+    if (n_tab < 64) tab[n_tab++] = {dev, fn, smem, *ctas};
+    return MOE_OK;
+}
+
+// Persistent launch: as many CTAs as are resident at once, but no more than units.
 template <typename Kern>
-int launch_unit_kernel(Kern kern, int grid, size_t smem, const FfnParams &p, cudaStream_t s) {
-    if (grid <= 0) return MOE_OK;
-    MOE_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    kern<<<grid, GV_THREADS, smem, s>>>(p);
+int launch_ring_kernel(Kern kern, int max_units, size_t smem, const FfnParams &p, cudaStream_t s) {
+    if (max_units <= 0) return MOE_OK;
+    int ctas = 0;
+    const int rc = ring_grid_capacity((const void *)kern, smem, &ctas);
+    if (rc != MOE_OK) return rc;
+    kern<<<std::min(max_units, ctas), GV_THREADS, smem, s>>>(p);
     MOE_TRY_CUDA(cudaGetLastError());
     return MOE_OK;
+}
+
+// Ring depth: the preferred number of stages, fewer when the shared memory would not fit.
+int ring_stages(int qtype, int nbr, int ntok, int preferred) {
+    for (int S = preferred; S >= 1; --S)
+        if (ring_smem(qtype, nbr, ntok, S).total <= GV_SMEM_MAX) return S;
+    return 0;
 }
 
 }  // namespace
@@ -636,45 +906,51 @@ int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype
     p.T = T; p.H = H; p.F = F; p.k = k; p.E = E;
     p.KS = moe_gateup_ksplit(qtype, H);
     p.RT = T * k;
-    p.ids = ids;
     p.weights = weights;
     p.ws_ints = (const int32_t *)((char *)workspace + W.ints_off);
+    p.info = (const ActInfo *)((char *)workspace + W.info_off);
+    p.tickets = (int32_t *)((char *)workspace + W.ints_off) + ws_ticket_off(E, T * k);
     p.gu = (float *)((char *)workspace + W.gu_off);
-    p.slot_table = d_slot_table;
-    p.n_slots = n_slots;
-    p.pool = (const uint8_t *)pool;
-    p.slot_bytes = slot_bytes;
+    p.h = (float *)((char *)workspace + W.h_off);
     p.partial = partial;
     p.status = moe_status_word_device_ptr();
-    p.ntok = pow2_tokens(T < GV_TOK ? T : GV_TOK);
-    p.fill_src = (const unsigned long long *)d_fill_src;
+    p.x_vec = ((uintptr_t)x % (xtype == MOE_F32 ? 16 : 8)) == 0;
+    const int ntok = T < GV_TOK ? T : GV_TOK;
 
+    const unsigned long long *fill_src = (const unsigned long long *)d_fill_src;
     const int n_act_max = expert_subset ? n_subset : (T * k < E ? T * k : E);
-    const int nb1 = (H / 32) / p.KS;
-    const size_t smem1 = unit_smem(qtype, nb1, p.ntok).total;
-    const size_t smem2 = unit_smem(qtype, F / 32, p.ntok).total;
-    if (smem1 > 220 * 1024 || smem2 > 220 * 1024) return MOE_ERR_UNSUPPORTED;
+    const int nb1 = (H / 32) / p.KS, nb2 = F / 32;
+    const int S1 = ring_stages(qtype, nb1, ntok, GV_S1), S2 = ring_stages(qtype, nb2, ntok, GV_S2);
+    if (S1 == 0 || S2 == 0) return MOE_ERR_UNSUPPORTED;
+    const size_t smem1 = ring_smem(qtype, nb1, ntok, S1).total;
+    const size_t smem2 = ring_smem(qtype, nb2, ntok, S2).total;
 
     if (timing && timing->permute0) MOE_TRY_CUDA(cudaEventRecord(timing->permute0, s));
     permute_kernel<<<1, 256, 0, s>>>(ids, T * k, E, expert_subset, n_subset,
-                                     (int32_t *)((char *)workspace + W.ints_off), p.status);
+                                     (int32_t *)((char *)workspace + W.ints_off),
+                                     (ActInfo *)((char *)workspace + W.info_off), d_slot_table, n_slots,
+                                     (const uint8_t *)pool, slot_bytes, fill_src, F / 32, p.status);
     MOE_TRY_CUDA(cudaGetLastError());
     if (timing && timing->permute1) MOE_TRY_CUDA(cudaEventRecord(timing->permute1, s));
     if (timing && timing->gateup0) MOE_TRY_CUDA(cudaEventRecord(timing->gateup0, s));
-    const int grid1 = n_act_max * 2 * (F / 32) * p.KS;
+    const int units1 = n_act_max * 2 * (F / 32) * p.KS;
     int rc;
+    p.stages = S1;
     if (qtype == MOE_Q8_0)
-        rc = xtype == MOE_F32 ? launch_unit_kernel(gateup_kernel<MOE_Q8_0, MOE_F32>, grid1, smem1, p, s)
-                              : launch_unit_kernel(gateup_kernel<MOE_Q8_0, MOE_BF16>, grid1, smem1, p, s);
+        rc = xtype == MOE_F32
+                 ? launch_ring_kernel(ffn_ring_kernel<MOE_Q8_0, MOE_F32, false>, units1, smem1, p, s)
+                 : launch_ring_kernel(ffn_ring_kernel<MOE_Q8_0, MOE_BF16, false>, units1, smem1, p, s);
     else
-        rc = xtype == MOE_F32 ? launch_unit_kernel(gateup_kernel<MOE_Q4_SM, MOE_F32>, grid1, smem1, p, s)
-                              : launch_unit_kernel(gateup_kernel<MOE_Q4_SM, MOE_BF16>, grid1, smem1, p, s);
+        rc = xtype == MOE_F32
+                 ? launch_ring_kernel(ffn_ring_kernel<MOE_Q4_SM, MOE_F32, false>, units1, smem1, p, s)
+                 : launch_ring_kernel(ffn_ring_kernel<MOE_Q4_SM, MOE_BF16, false>, units1, smem1, p, s);
     if (rc != MOE_OK) return rc;
     if (timing && timing->gateup1) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
     if (timing && timing->down0) MOE_TRY_CUDA(cudaEventRecord(timing->down0, s));
-    const int grid2 = n_act_max * (H / 32);
-    rc = qtype == MOE_Q8_0 ? launch_unit_kernel(down_kernel<MOE_Q8_0>, grid2, smem2, p, s)
-                           : launch_unit_kernel(down_kernel<MOE_Q4_SM>, grid2, smem2, p, s);
+    const int units2 = n_act_max * (H / 32);
+    p.stages = S2;
+    rc = qtype == MOE_Q8_0 ? launch_ring_kernel(ffn_ring_kernel<MOE_Q8_0, MOE_F32, true>, units2, smem2, p, s)
+                           : launch_ring_kernel(ffn_ring_kernel<MOE_Q4_SM, MOE_F32, true>, units2, smem2, p, s);
     if (rc != MOE_OK) return rc;
     if (timing && timing->down1) MOE_TRY_CUDA(cudaEventRecord(timing->down1, s));
     return MOE_OK;

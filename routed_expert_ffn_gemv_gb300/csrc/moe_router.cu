@@ -56,6 +56,55 @@ __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
     return v1 > v2 || (v1 == v2 && i1 < i2);
 }
 
+// Top-k of one token's logits held by a warp (lane l holds experts l, l+32, ...; -inf
+// beyond E), larger first and ties to the lower id, then the softmax over the k selected;
+// lanes 0..k-1 write ids/weights of row `row`.
+__device__ __forceinline__ void select_topk_softmax(const float (&v)[MOE_MAX_E / 32], int E, int k, int lane,
+                                                    size_t row, int32_t *__restrict__ ids,
+                                                    float *__restrict__ weights) {
+    constexpr int NPL = MOE_MAX_E / 32;
+    unsigned taken = 0;
+    float sel_v[MOE_MAX_K];
+    int sel_i[MOE_MAX_K];
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !(taken >> i & 1u) && better(v[i], e, bv, bi)) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (better(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        sel_v[j] = bv;
+        sel_i[j] = bi;
+    }
+    float denom = 0.f;
+    for (int j = 0; j < k; ++j) denom += expf(sel_v[j] - sel_v[0]);
+    if (lane < k) {
+        float myv = sel_v[0];
+        int myi = sel_i[0];
+        for (int j = 1; j < k; ++j)
+            if (j == lane) {
+                myv = sel_v[j];
+                myi = sel_i[j];
+            }
+        ids[row * k + lane] = myi;
+        weights[row * k + lane] = expf(myv - sel_v[0]) / denom;
+    }
+}
+
 template <int XT>
 __global__ void __launch_bounds__(MOE_ROUTER_THREADS)
 router_topk_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__restrict__ w_router,
@@ -162,49 +211,204 @@ router_topk_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__r
                     v[i] = (s != s) ? -INFINITY : s;  // NaN never wins
                 }
             }
-            unsigned taken = 0;
-            float sel_v[MOE_MAX_K];
-            int sel_i[MOE_MAX_K];
-            for (int j = 0; j < k; ++j) {
-                float bv = -INFINITY;
-                int bi = 0x7FFFFFFF;
-#pragma unroll
-                for (int i = 0; i < NPL; ++i) {
-                    const int e = lane + 32 * i;
-                    if (e < E && !(taken >> i & 1u) && better(v[i], e, bv, bi)) {
-                        bv = v[i];
-                        bi = e;
-                    }
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                    if (better(ov, oi, bv, bi)) {
-                        bv = ov;
-                        bi = oi;
-                    }
-                }
-                if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-                sel_v[j] = bv;
-                sel_i[j] = bi;
-            }
-            float denom = 0.f;
-            for (int j = 0; j < k; ++j) denom += expf(sel_v[j] - sel_v[0]);
-            if (lane < k) {
-                float myv = sel_v[0];
-                int myi = sel_i[0];
-                for (int j = 1; j < k; ++j)
-                    if (j == lane) {
-                        myv = sel_v[j];
-                        myi = sel_i[j];
-                    }
-                ids[(size_t)(t0 + t) * k + lane] = myi;
-                weights[(size_t)(t0 + t) * k + lane] = expf(myv - sel_v[0]) / denom;
-            }
+            select_topk_softmax(v, E, k, lane, (size_t)(t0 + t), ids, weights);
         }
     }
     cluster_sync_all();  // rank 0 has finished reading the other CTAs' shared memory
+}
+
+// ------------------------------------------------------------------ many tokens (prefill)
+//
+// Above the decode batch limit the router is a small fp32 GEMM [T x H] . [H x E]: a CTA
+// owns 32 tokens and every expert and walks H in chunks of 32 rows, double-buffered in
+// shared memory (x duplicated into (v, v) pairs, W_r converted to fp32).  Thread (ty, tx)
+// keeps 4 tokens x EPT experts in registers and accumulates expert pairs with packed
+// fp32x2 FMAs, in ascending h per logit
+// within each chunk.  The logits then go through the same warp
+// selection as the cluster kernel.
+
+#define RT_TT 32
+#define RT_KC 32
+#define RT_XS (RT_TT + 2)  // float2 row stride of the x chunk (16-byte aligned, fewer conflicts)
+
+__host__ __device__ inline size_t router_tiled_smem(int EP) {
+    const size_t xs = 2 * (size_t)RT_KC * RT_XS * 8;
+    const size_t ws = 2 * (size_t)RT_KC * EP * 4;
+    const size_t lg = (size_t)RT_TT * EP * 4;
+    return xs + (ws > lg ? ws : lg);
+}
+
+template <int XT, int EPT>
+__global__ void __launch_bounds__(MOE_ROUTER_THREADS)
+router_tiled_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__restrict__ w_router,
+                    const float *__restrict__ bias, int E, int k, int32_t *__restrict__ ids,
+                    float *__restrict__ weights, float *__restrict__ logits_out) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int EP = 32 * EPT;
+    float2 *xs = (float2 *)smem;                                       // [2][KC][RT_XS]
+    float *ws = (float *)(smem + 2 * (size_t)RT_KC * RT_XS * 8);       // [2][KC][EP]
+    float *lg = ws;                                                    // [TT][EP] after the loop
+    const int tid = threadIdx.x, tx = tid % 32, ty = tid / 32;
+    const int t0 = blockIdx.x * RT_TT;
+    const int NC = H / RT_KC;
+    const int wn = RT_KC * E;                   // halfs per W_r chunk (contiguous rows)
+    const int wv = wn / 8;                      // 16-byte vectors per chunk
+
+    // columns E..EP-1 stay zero in both buffers
+    for (int i = tid; i < 2 * RT_KC * EP; i += MOE_ROUTER_THREADS)
+        if (i % EP >= E) ws[i] = 0.f;
+
+    constexpr int WPT = (RT_KC * EP / 8 + MOE_ROUTER_THREADS - 1) / MOE_ROUTER_THREADS;
+    float4 xr;                                  // this thread's x piece of a chunk
+    uint4 wr[WPT];                              // this thread's W_r vectors of a chunk
+    const int xt = tid / 8, xc = (tid % 8) * 4;  // token and first column of the x piece
+
+    auto load = [&](int c) {
+        const int h0 = c * RT_KC;
+        xr = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t0 + xt < T) {
+            const size_t off = (size_t)(t0 + xt) * H + h0 + xc;
+            if (XT == MOE_BF16) {
+                const uint2 b = *(const uint2 *)((const __nv_bfloat16 *)x + off);
+                const float2 lo = __bfloat1622float2(*(const __nv_bfloat162 *)&b.x);
+                const float2 hi = __bfloat1622float2(*(const __nv_bfloat162 *)&b.y);
+                xr = make_float4(lo.x, lo.y, hi.x, hi.y);
+            } else {
+                xr = *(const float4 *)((const float *)x + off);
+            }
+        }
+        // rows h0.. of W_r are 32*E contiguous halfs, a multiple of 8 starting 64*E*c bytes in
+        const uint4 *src = (const uint4 *)(w_router + (size_t)h0 * E);
+#pragma unroll
+        for (int q = 0; q < WPT; ++q) {
+            const int v = tid + q * MOE_ROUTER_THREADS;
+            if (v < wv) wr[q] = src[v];
+        }
+    };
+    auto store = [&](int buf) {
+        float2 *xb = xs + (size_t)buf * RT_KC * RT_XS;
+        xb[(xc + 0) * RT_XS + xt] = make_float2(xr.x, xr.x);
+        xb[(xc + 1) * RT_XS + xt] = make_float2(xr.y, xr.y);
+        xb[(xc + 2) * RT_XS + xt] = make_float2(xr.z, xr.z);
+        xb[(xc + 3) * RT_XS + xt] = make_float2(xr.w, xr.w);
+        float *wb = ws + (size_t)buf * RT_KC * EP;
+#pragma unroll
+        for (int q = 0; q < WPT; ++q) {
+            const int v = tid + q * MOE_ROUTER_THREADS;
+            if (v < wv) {
+                const uint16_t *h = (const uint16_t *)&wr[q];
+                int row = (8 * v) / E, e = (8 * v) % E;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    wb[row * EP + e] = __half2float(__ushort_as_half(h[j]));
+                    if (++e == E) {
+                        e = 0;
+                        ++row;
+                    }
+                }
+            }
+        }
+    };
+
+    unsigned long long acc[4][EPT / 2];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int p = 0; p < EPT / 2; ++p) acc[t][p] = 0ull;
+
+    load(0);
+    __syncthreads();  // zero fill of the padding columns before the first store
+    store(0);
+    __syncthreads();
+    for (int c = 0; c < NC; ++c) {
+        if (c + 1 < NC) load(c + 1);
+        // each chunk's 32 products are summed on their own, then added to the total (keeps
+        // the rounding error of a 2048-term logit near 1e-6)
+        unsigned long long part[4][EPT / 2];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int p = 0; p < EPT / 2; ++p) part[t][p] = 0ull;
+        const float2 *xb = xs + (size_t)(c & 1) * RT_KC * RT_XS;
+        const float *wb = ws + (size_t)(c & 1) * RT_KC * EP;
+#pragma unroll 4
+        for (int kk = 0; kk < RT_KC; ++kk) {
+            const float4 xa = *(const float4 *)&xb[kk * RT_XS + 4 * ty];      // (x0,x0,x1,x1)
+            const float4 xc4 = *(const float4 *)&xb[kk * RT_XS + 4 * ty + 2]; // (x2,x2,x3,x3)
+            const unsigned long long xd[4] = {f2_pack(xa.x, xa.y), f2_pack(xa.z, xa.w), f2_pack(xc4.x, xc4.y),
+                                              f2_pack(xc4.z, xc4.w)};
+#pragma unroll
+            for (int q = 0; q < EPT / 4; ++q) {
+                const float4 w4 = *(const float4 *)&wb[kk * EP + 128 * q + 4 * tx];
+                const unsigned long long w01 = f2_pack(w4.x, w4.y), w23 = f2_pack(w4.z, w4.w);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    part[t][2 * q] = f2_fma(w01, xd[t], part[t][2 * q]);
+                    part[t][2 * q + 1] = f2_fma(w23, xd[t], part[t][2 * q + 1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int p = 0; p < EPT / 2; ++p) acc[t][p] = f2_add(acc[t][p], part[t][p]);
+        if (c + 1 < NC) store((c + 1) & 1);
+        __syncthreads();
+    }
+    // logits (+ bias) -> shared memory (the W_r buffers are free after the last barrier)
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int q = 0; q < EPT / 4; ++q)
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                float a, b;
+                f2_unpack(acc[t][2 * q + p], a, b);
+                const int e = 128 * q + 4 * tx + 2 * p;
+                lg[(size_t)(4 * ty + t) * EP + e] = a + (bias && e < E ? bias[e] : 0.f);
+                lg[(size_t)(4 * ty + t) * EP + e + 1] = b + (bias && e + 1 < E ? bias[e + 1] : 0.f);
+            }
+    __syncthreads();
+    const int warp = ty, lane = tx;
+    for (int t = warp; t < RT_TT && t0 + t < T; t += MOE_ROUTER_THREADS / 32) {
+        float v[MOE_MAX_E / 32];
+#pragma unroll
+        for (int i = 0; i < MOE_MAX_E / 32; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = -INFINITY;
+            if (e < E) {
+                const float s = lg[(size_t)t * EP + e];
+                if (logits_out) logits_out[(size_t)(t0 + t) * E + e] = s;
+                v[i] = (s != s) ? -INFINITY : s;  // NaN never wins
+            }
+        }
+        select_topk_softmax(v, E, k, lane, (size_t)(t0 + t), ids, weights);
+    }
+}
+
+}  // namespace
+
+namespace {
+
+template <int XT, int EPT>
+int router_tiled_launch_t(const void *x, int T, int H, const uint16_t *w_router, const float *bias, int E,
+                          int k, int32_t *ids, float *weights, float *logits, cudaStream_t st) {
+    const size_t smem = router_tiled_smem(32 * EPT);
+    MOE_TRY_CUDA(cudaFuncSetAttribute(router_tiled_kernel<XT, EPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem));
+    router_tiled_kernel<XT, EPT><<<(T + RT_TT - 1) / RT_TT, MOE_ROUTER_THREADS, smem, st>>>(
+        x, T, H, w_router, bias, E, k, ids, weights, logits);
+    MOE_TRY_CUDA(cudaGetLastError());
+    return MOE_OK;
+}
+
+int router_tiled_launch(const void *x, int xtype, int T, int H, const uint16_t *w_router, const float *bias,
+                        int E, int k, int32_t *ids, float *weights, float *logits, cudaStream_t st) {
+    if (E <= 128)
+        return xtype == MOE_F32 ? router_tiled_launch_t<MOE_F32, 4>(x, T, H, w_router, bias, E, k, ids, weights, logits, st)
+                                : router_tiled_launch_t<MOE_BF16, 4>(x, T, H, w_router, bias, E, k, ids, weights, logits, st);
+    return xtype == MOE_F32 ? router_tiled_launch_t<MOE_F32, 8>(x, T, H, w_router, bias, E, k, ids, weights, logits, st)
+                            : router_tiled_launch_t<MOE_BF16, 8>(x, T, H, w_router, bias, E, k, ids, weights, logits, st);
 }
 
 }  // namespace
@@ -218,6 +422,9 @@ extern "C" int moe_router_topk(const void *x, int xtype, int T, int H, const uin
     MOE_CHECK(E >= 1 && E <= MOE_MAX_E && k >= 1 && k <= MOE_MAX_K && k <= E);
     if (T == 0) return MOE_OK;
     MOE_CHECK(x && w_router && ids && weights);
+    if (T > MOE_DECODE_MAX_T && ((uintptr_t)x & 15) == 0 && ((uintptr_t)w_router & 15) == 0)
+        return router_tiled_launch(x, xtype, T, H, w_router, bias, E, k, ids, weights, logits,
+                                   moe_cuda_stream(s));
     const RouterSmem L = router_smem_layout(H, E);
     if (L.total > 200 * 1024) return MOE_ERR_UNSUPPORTED;
     const int HS = H / MOE_ROUTER_CLUSTER;

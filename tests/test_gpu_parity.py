@@ -35,6 +35,12 @@ ROUTER_CASES = [
     (2048, 64, 2, 32, 0, 1.2),     # DeepSeek-shaped, batch 32
     (2048, 128, 8, 100, 1, 1.1),   # bf16 prefill tokens: 4 clusters with a ragged tail
     (96, 5, 3, 7, 0, 0.7),         # odd E, H with 12 rows per cluster CTA
+    # above 32 tokens: the tiled router (32-token CTAs, 32-row chunks of W_r)
+    (1024, 32, 8, 33, 0, 1.0),     # one token past the decode limit: a 1-token second tile
+    (96, 5, 3, 70, 0, 0.7),        # odd E (padded expert columns), 3 chunks
+    (2048, 256, 8, 64, 1, 1.0),    # E = 256: 8 experts per thread
+    (64, 200, 6, 45, 0, 0.5),      # E = 200, 2 chunks
+    (2048, 128, 8, 300, 0, 1.1),   # Qwen-shaped, fp32 tokens, ragged last tile
 ]
 
 
@@ -68,7 +74,11 @@ def test_router_topk_parity(H, E, k, T, xtype, bias_a):
     assert all(v is not False for v in m), m
     cmp = [t for t, v in enumerate(m) if v]
     assert len(cmp) >= T - 1
-    np.testing.assert_allclose(w.cpu().numpy()[cmp], wo[cmp], rtol=0, atol=2e-6)
+    # softmax over the selected logits moves each weight by at most 2*w*max|dl| for logit
+    # errors dl (plus a few fp32 ulps of exp and the division)
+    dl = np.max(np.abs(lg_h - lo), axis=1, keepdims=True)
+    tol = 2.0 * dl * wo + 4e-7
+    assert np.all(np.abs(w.cpu().numpy()[cmp] - wo[cmp]) <= tol[cmp])
     assert np.allclose(w.cpu().numpy().sum(axis=1), 1.0, atol=1e-6)
 
 

@@ -95,6 +95,9 @@ PREFILL_CASES = [
     (0, 512, 256, 4, 2, 400, 1, False),
     (1, 1024, 384, 16, 4, 200, 1, False),   # 3 weight tiles, 64-row token tiles
     (1, 512, 256, 4, 2, 100, 0, True),      # fp32 activations: the fp32 GEMV kernels
+    # more work items than SMs: each persistent CTA walks several items, alternating TMEM buffers
+    (1, 2048, 768, 64, 8, 600, 1, True),
+    (0, 1024, 512, 32, 4, 1500, 1, False),
 ]
 
 
@@ -111,6 +114,41 @@ def test_prefill_subset_and_slot_table():
     subset = [1, 2, 5]
     ids, w, x64, partial = _run(cfg, 70, 1, True, subset=subset, reverse_slots=True, seed=3)
     _check(cfg, ids, w, x64, partial, True, subset=subset)
+
+
+def test_prefill_invalid_slot_reported_others_computed():
+    """An expert whose slot is out of range is reported (MOE_ERR_INVALID) and skipped; the
+    other experts' routes are still computed."""
+    cfg = synth.small_config(1, H=256, F=128, E=6, k=2, seed_cfg=861)
+    H, F, E, k, T = cfg.H, cfg.F, cfg.E, cfg.k, 80
+    pool, stride = _pool(cfg, list(range(E)), True)
+    table = torch.tensor([0, 1, 2, E + 3, 4, 5], dtype=torch.int32, device="cuda")
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((T, H), dtype=np.float32)
+    xb = synth.f32_to_bf16_bits(x)
+    ids, w = random_routes(rng, T, E, k)
+    ws_bytes = L.moe_expert_ffn_workspace(T, H, F, cfg.qtype, 1, E, k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    partial = torch.full((T, k, H), float("nan"), dtype=torch.float32, device="cuda")
+    L.moe_expert_ffn(torch.from_numpy(xb.view(np.int16)).cuda(), 1, T, H, F, cfg.qtype, E, k,
+                     torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), table, E, pool, stride,
+                     None, 0, partial, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert L.moe_device_status(clear=True) == L.MOE_ERR_INVALID
+    part = partial.cpu().numpy()
+    x64 = oracle.x_to_double(xb, 1)
+    cache = {}
+    for t in range(0, T, 7):
+        for j in range(k):
+            e = int(ids[t, j])
+            if e == 3:
+                assert np.all(np.isnan(part[t, j]))
+                continue
+            if e not in cache:
+                cache[e] = synth.expert_weights(cfg, 0, e, True)
+            g, u, d = cache[e]
+            ref = float(w[t, j]) * oracle.expert_ffn(cfg.qtype, H, F, g, u, d, x64[t])
+            assert rel_err(part[t, j][None], ref[None])[0] <= ROUTE_TOL
 
 
 def test_prefill_qwen_layer_4096_tokens_sampled():

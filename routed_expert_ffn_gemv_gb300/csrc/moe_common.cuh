@@ -131,4 +131,4 @@ int moe_prefill_ffn(const void *x, int xtype, int T, int H, int F, int qtype, in
                     const float *weights, const int32_t *d_slot_table, int n_slots, const void *pool,
                     size_t slot_bytes, const int32_t *expert_subset, int n_subset, float *partial,
                     void *workspace, size_t ws_bytes, cudaStream_t s, const moe_ffn_timing *timing);
-int moe_gateup_ksplit(int qtype, int H);
+

@@ -1,5 +1,5 @@
-// Decode-time expert FFN: permute (P1), gate/up dequantising GEMV + SwiGLU (G1), down GEMV
-// with the router-weighted scatter (G2), combine (C1).
+// Decode-time expert FFN: permute (P1), gate/up dequantising GEMV with SwiGLU (G1), down
+// GEMV with the router-weighted scatter (G2), combine (C1).
 //
 // What is computed (pages 1-5, see moe.h): for every route (t, j) of a token t to its
 // j-th selected expert e, h = silu(Wg_e x_t) * (Wu_e x_t) and
@@ -7,44 +7,112 @@
 // their quantised blocks (page 5, section 1.2) and are dequantised in registers.
 //
 // GB300 mapping (the decode GEMVs stream the selected experts' bytes from HBM once):
-//  * work unit = (active expert, [K range,] matrix, 32-row tile): one 32-row tile of one
-//    matrix over a K range, whose bytes are one contiguous run per region in the slot image;
-//  * persistent CTAs of 8 warps: each CTA streams a contiguous range of units through a
-//    ring of shared-memory stages; thread 0 keeps S-1 units' bulk copies (TMA engine,
-//    cp.async.bulk) in flight ahead of the unit being computed;
-//  * lane l of each warp owns row l of the tile and keeps its dot products in registers
-//    (no cross-lane reduction); the 8 warps split the unit's K range and are reduced in
-//    shared memory in a fixed order;
-//  * activations of the unit's tokens are staged once in shared memory (vector loads,
-//    issued before the unit's weights are waited for) and reused while consecutive units
-//    share the expert and K range; they are read as warp broadcasts;
+//  * work unit = two 32-row tiles over a K range whose bytes are one contiguous run per
+//    tile and region in the slot image: the gate and the up tile of the same rows (G1), or
+//    two neighbouring down tiles (G2);
+//  * persistent CTAs of 16 warps, one per SM: each walks a contiguous, work-balanced range
+//    of units (precomputed by the permute kernel) through a ring of shared-memory stages;
+//    thread 0 keeps the next units' bulk copies (TMA engine, cp.async.bulk) in flight
+//    while the current one is computed;
+//  * lane l of every warp owns row l of both tiles and keeps its dot products in registers
+//    (no cross-lane reduction); each activation value read from shared memory (a warp
+//    broadcast) feeds both rows; the 16 warps split the K range and are reduced in shared
+//    memory in a fixed order;
 //  * codes become fp32 with exponent tricks (no int->float conversions), accumulate with
 //    packed fp32x2 FMAs, and block scales are applied once per 32 weights;
-//  * gate/up partial sums of the K ranges meet in the workspace; the warp whose write
-//    completes a (expert, row tile) sums them in a fixed order and writes h = silu(g) * u,
-//    so the down kernel's activations are a plain copy;
+//  * the warp that reduces a token's gate and up rows applies SwiGLU and writes h; when the
+//    K range is split (large H), the partial sums go to the workspace and the down kernel
+//    sums them in a fixed order while it stages its activations;
 //  * an expert that missed in a device-managed pool is read from its pinned host image and
 //    written through to its slot by the unit that uses the bytes ("fill" units).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "moe_ptx.cuh"
 
-#define GV_WARPS 8
+#define GV_WARPS 16
 #define GV_THREADS (GV_WARPS * 32)
-#define GV_TOK 8            // tokens per pass (one per warp in the reduction)
-#define GV_UNIT_QUANT 16384 // target code bytes per gate/up unit
-#define GV_S1 4             // ring stages, gate/up
-#define GV_S2 3             // ring stages, down
+#define GV_TOK 8                  // tokens per pass (one per reducing warp)
 #define GV_SMEM_MAX (220 * 1024)  // dynamic shared memory a ring kernel may take
-#define GV_FILL_BATCH 6     // 16-byte pieces per thread loaded together by a fill unit
-
-static_assert(GV_TOK == GV_WARPS, "the reduction gives each warp one token of a pass");
+#define GV_FILL_BATCH 4           // 16-byte pieces per thread loaded together by a fill unit
+#define GV_ICACHE 64              // active experts of a CTA's range kept in shared memory
+#define GV_RCACHE 512             // routes (and router weights) of a CTA's range in shared memory
+#define GV_MAX_GRID 1024          // CTAs per launch (bounds the precomputed range tables)
 
 namespace {
+
+// Work of one unit of an expert with n_e tokens, in units of a token's dot products: the
+// unit's bytes and dequantisation cost about as much as GV_COST_MEM tokens.
+#define GV_COST_MEM 4
+__host__ __device__ inline int unit_cost(int n_e) { return n_e > 0 ? GV_COST_MEM + n_e : 1; }
+
+// ------------------------------------------------------------------ shared-memory layout
+
+struct RingSmem {
+    size_t bars, stages, stage_bytes, tile_bytes, scale_off, act, asum, red, info, rts, wts, total;
+};
+
+// nbr blocks of 32 columns per tile, `tiles` tiles per unit, ntok staged token rows, S stages.
+__host__ __device__ inline RingSmem ring_smem(int qtype, int nbr, int tiles, int ntok, int S) {
+    RingSmem L;
+    const int QB = qtype == MOE_Q8_0 ? 1024 : 512;       // code bytes per block of a 32-row tile
+    const int SB = 32 * moe_scale_entry_bytes(qtype);    // scale bytes per block of a tile
+    L.scale_off = (size_t)nbr * QB;
+    L.tile_bytes = L.scale_off + ((size_t)nbr * SB + 127) / 128 * 128;
+    L.stage_bytes = (size_t)tiles * L.tile_bytes;
+    size_t off = 0;
+    L.bars = off;   off += 128;
+    L.stages = off; off += (size_t)S * L.stage_bytes;
+    L.act = off;    off += (size_t)ntok * nbr * 32 * 4;
+    L.asum = off;   off += ((size_t)ntok * nbr * 4 + 15) / 16 * 16;
+    L.red = off;    off += (size_t)GV_WARPS * ntok * 2 * 32 * 4;
+    L.info = off;   off += (size_t)GV_ICACHE * 32;
+    L.rts = off;    off += (size_t)GV_RCACHE * 4;
+    L.wts = off;    off += (size_t)GV_RCACHE * 4;
+    L.total = off;
+    return L;
+}
+
+// Launch plan of one decode FFN: the gate/up K split and ring depth, the down tiles per unit
+// and ring depth, chosen so that each kernel's shared memory fits.
+struct GvPlan {
+    int KS, S1, TPU, S2;
+};
+
+inline bool gv_plan(int T, int H, int F, int qtype, GvPlan *pl) {
+    const int ntok = T < GV_TOK ? T : GV_TOK;
+    const int NB = H / 32;
+    pl->KS = 0;
+    for (int ks = 1; ks <= NB && !pl->KS; ks *= 2) {
+        if (NB % ks) break;
+        for (int S = 3; S >= 2 && !pl->KS; --S)
+            if (ring_smem(qtype, NB / ks, 2, ntok, S).total <= GV_SMEM_MAX) {
+                pl->KS = ks;
+                pl->S1 = S;
+            }
+    }
+    if (!pl->KS) {  // a single stage of the smallest split
+        int ks = 1;
+        while (NB % (2 * ks) == 0 && ring_smem(qtype, NB / ks, 2, ntok, 1).total > GV_SMEM_MAX) ks *= 2;
+        if (ring_smem(qtype, NB / ks, 2, ntok, 1).total > GV_SMEM_MAX) return false;
+        pl->KS = ks;
+        pl->S1 = 1;
+    }
+    pl->TPU = 0;
+    const int cand[7][2] = {{2, 4}, {2, 3}, {2, 2}, {1, 4}, {1, 3}, {1, 2}, {1, 1}};
+    for (int i = 0; i < 7 && !pl->TPU; ++i) {
+        if (cand[i][0] == 2 && (H / 32) % 2) continue;
+        if (ring_smem(qtype, F / 32, cand[i][0], ntok, cand[i][1]).total <= GV_SMEM_MAX) {
+            pl->TPU = cand[i][0];
+            pl->S2 = cand[i][1];
+        }
+    }
+    return pl->TPU != 0;
+}
 
 // ------------------------------------------------------------------ workspace layout
 
@@ -55,64 +123,34 @@ struct ActInfo {
     int e, pos0, n_e, fill;  // n_e == 0: skip (invalid slot)
 };
 
-struct WsLayout {
-    size_t ints_off;   // int32: [0] n_active, [16..16+E) active, a_off [E+1], routes [R], tickets [E][F/32],
-                       //        cost prefix [E+1]
-    size_t info_off;   // ActInfo [E]
-    size_t gu_off;     // float [KS][2][R][F]: gate/up partial dot products per K range
-    size_t h_off;      // float [R][F]: silu(gate) * up
-    size_t total;
-};
-
+// int32 region: [0] n_active | active [E] | a_off [E+1] | routes [R] | ranges1 | ranges2
 __host__ __device__ inline int ws_active_off() { return 16; }
 __host__ __device__ inline int ws_aoff_off(int E) { return 16 + E; }
 __host__ __device__ inline int ws_routes_off(int E) { return 16 + 2 * E + 1; }
-__host__ __device__ inline int ws_ticket_off(int E, int R) { return 16 + 2 * E + 1 + R; }
-__host__ __device__ inline int ws_cost_off(int E, int R, int F) { return 16 + 2 * E + 1 + R + E * (F / 32); }
+__host__ __device__ inline int ws_ranges_off(int E, int R, int which) {
+    return 16 + 2 * E + 1 + R + which * (GV_MAX_GRID + 1);
+}
 
-// Work of one unit of an expert with n_e tokens, in units of a token's dot products: the
-// unit's bytes and dequantisation cost about as much as GV_COST_MEM tokens.
-#define GV_COST_MEM 4
-__host__ __device__ inline int unit_cost(int n_e) { return n_e > 0 ? GV_COST_MEM + n_e : 1; }
+struct WsLayout {
+    size_t ints_off, info_off;
+    size_t gu_off;     // float [KS][2][R][F] gate/up partial sums (KS > 1)
+    size_t h_off;      // float [R][F] silu(gate) * up (KS == 1)
+    size_t total;
+};
 
 inline WsLayout ws_layout(int T, int H, int F, int qtype, int E, int k) {
     WsLayout L;
     const size_t R = (size_t)T * k;
-    const size_t ints = 16 + 2 * (size_t)E + 1 + R + (size_t)E * (F / 32) + (size_t)E + 1;
+    GvPlan pl;
+    if (!gv_plan(T, H, F, qtype, &pl)) pl.KS = 1;
+    const size_t ints = 16 + 2 * (size_t)E + 1 + R + 2 * (GV_MAX_GRID + 1);
     L.ints_off = 0;
     L.info_off = (ints * 4 + 255) / 256 * 256;
     L.gu_off = L.info_off + ((size_t)E * sizeof(ActInfo) + 255) / 256 * 256;
-    const int KS = moe_gateup_ksplit(qtype, H);
-    L.h_off = L.gu_off + ((size_t)KS * 2 * R * F * 4 + 255) / 256 * 256;
-    L.total = L.h_off + ((size_t)R * F * 4 + 255) / 256 * 256;
-    return L;
-}
-
-// ------------------------------------------------------------------ shared-memory layout
-
-struct RingSmem {
-    size_t bars, stages, stage_bytes, scale_off, act, asum, red, info, rts, wts, total;
-};
-
-#define GV_ICACHE 64    // active experts of a CTA's range kept in shared memory
-#define GV_RCACHE 512   // routes (and their router weights) of a CTA's range kept in shared memory
-
-__host__ __device__ inline RingSmem ring_smem(int qtype, int nbr, int ntok, int S) {
-    RingSmem L;
-    const int QB = qtype == MOE_Q8_0 ? 1024 : 512;       // code bytes per block of a 32-row tile
-    const int SB = 32 * moe_scale_entry_bytes(qtype);    // scale bytes per block of a tile
-    L.scale_off = (size_t)nbr * QB;
-    L.stage_bytes = L.scale_off + ((size_t)nbr * SB + 127) / 128 * 128;
-    size_t off = 0;
-    L.bars = off;   off += 128;
-    L.stages = off; off += (size_t)S * L.stage_bytes;
-    L.act = off;    off += (size_t)ntok * nbr * 32 * 4;
-    L.asum = off;   off += ((size_t)ntok * nbr * 4 + 15) / 16 * 16;
-    L.red = off;    off += (size_t)GV_WARPS * GV_TOK * 32 * 4;
-    L.info = off;   off += (size_t)GV_ICACHE * 32;
-    L.rts = off;    off += (size_t)GV_RCACHE * 4;
-    L.wts = off;    off += (size_t)GV_RCACHE * 4;
-    L.total = off;
+    const size_t gu = pl.KS > 1 ? (size_t)pl.KS * 2 * R * F * 4 : 0;
+    L.h_off = L.gu_off + (gu + 255) / 256 * 256;
+    const size_t hb = pl.KS > 1 ? 0 : R * F * 4;
+    L.total = L.h_off + (hb + 255) / 256 * 256;
     return L;
 }
 
@@ -121,35 +159,32 @@ __device__ __forceinline__ void warp_blocks(int nbr, int w, int &b0, int &b1) {
     b1 = ((w + 1) * nbr) / GV_WARPS;
 }
 
-// Bulk copies of one unit into a stage: rows [32g, 32g+32) of matrix `mat` [R][K], blocks
-// [kb0, kb0+nbr) — the codes and the scales are one contiguous run each.
+// Bulk copies of one 32-row tile into a stage: rows [32g, 32g+32) of matrix `mat` [R][K],
+// blocks [kb0, kb0+nbr) — the codes and the scales are one contiguous run each.
 template <int QT>
-__device__ __forceinline__ void issue_unit(const uint8_t *mat, int R, int K, int g, int kb0, int nbr,
-                                           unsigned char *stage, size_t scale_off, uint64_t *bar) {
+__device__ __forceinline__ void issue_tile(const uint8_t *mat, int R, int K, int g, int kb0, int nbr,
+                                           unsigned char *tile, size_t scale_off, uint64_t *bar) {
     const int QB = QT == MOE_Q8_0 ? 1024 : 512;
     const int SB = 32 * moe_scale_entry_bytes(QT);
     const int PPB = QT == MOE_Q8_0 ? 2 : 1;  // 16-byte pieces per block
-    const uint32_t qbytes = (uint32_t)nbr * QB, sbytes = (uint32_t)nbr * SB;
-    mbar_arrive_expect_tx(bar, qbytes + sbytes);
-    bulk_g2s(stage, mat + moe_piece_offset(QT, K, g, kb0 * PPB), qbytes, bar);
-    bulk_g2s(stage + scale_off, mat + moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, g, kb0), sbytes, bar);
+    bulk_g2s(tile, mat + moe_piece_offset(QT, K, g, kb0 * PPB), (uint32_t)nbr * QB, bar);
+    bulk_g2s(tile + scale_off, mat + moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, g, kb0),
+             (uint32_t)nbr * SB, bar);
 }
 
-// Fill path of a unit whose expert missed: its bytes come from the expert's pinned host
-// image over the CPU-GPU link (16-byte loads by every thread) and are written both to the
-// stage and through to the expert's slot, so the slot is filled by the kernels that use
-// it.  Same byte ranges as issue_unit.
+// Fill path of a tile whose expert missed: its bytes come from the expert's pinned host
+// image over the CPU-GPU link (16-byte loads by every thread, GV_FILL_BATCH in flight per
+// thread) and are written both to the stage and through to the expert's slot, so the slot
+// is filled by the kernels that use it.  Same byte ranges as issue_tile.
 template <int QT>
-__device__ void fill_unit(const uint8_t *src_mat, uint8_t *dst_mat, int R, int K, int g, int kb0, int nbr,
-                          unsigned char *stage, size_t scale_off) {
+__device__ void fill_tile(const uint8_t *src_mat, uint8_t *dst_mat, int R, int K, int g, int kb0, int nbr,
+                          unsigned char *tile, size_t scale_off) {
     const int QB = QT == MOE_Q8_0 ? 1024 : 512;
     const int SB = 32 * moe_scale_entry_bytes(QT);
     const int PPB = QT == MOE_Q8_0 ? 2 : 1;
     const size_t qoff = moe_piece_offset(QT, K, g, kb0 * PPB);
     const size_t soff = moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, g, kb0);
     const int nq = nbr * QB / 16, ns = nbr * SB / 16;
-    // loads of up to GV_FILL_BATCH pieces per thread are in flight together: one link round
-    // trip per batch instead of one per piece
     constexpr int NB = GV_FILL_BATCH;
     for (int i0 = 0; i0 < nq + ns; i0 += NB * GV_THREADS) {
         uint4 v[NB];
@@ -167,7 +202,7 @@ __device__ void fill_unit(const uint8_t *src_mat, uint8_t *dst_mat, int R, int K
             if (i < nq + ns) {
                 const bool q = i < nq;
                 const size_t off = q ? qoff + (size_t)i * 16 : soff + (size_t)(i - nq) * 16;
-                *(uint4 *)(stage + (q ? (size_t)i * 16 : scale_off + (size_t)(i - nq) * 16)) = v[b];
+                *(uint4 *)(tile + (q ? (size_t)i * 16 : scale_off + (size_t)(i - nq) * 16)) = v[b];
                 __stcs((uint4 *)(dst_mat + off), v[b]);
             }
         }
@@ -189,114 +224,131 @@ __device__ __forceinline__ float q4_act_unscale(int c) {
     return __int_as_float((127 + 4 * e) << 23);
 }
 
-// One block b of one lane's row against NT staged activation rows; acc[t] += d * sum
-// (+ m * asum for 4-bit).  act: [NT][Kr] fp32, asum: [NT][nbr].
-template <int QT, int NT>
-__device__ __forceinline__ void block_dot(const unsigned char *quant_s, const unsigned char *scale_s,
-                                          const float *act, const float *asum, int Kr, int nbr, int b,
-                                          int lane, float *acc) {
-    const unsigned long long MAG8 = f2_pack(-8388736.0f, -8388736.0f);  // 2^23 + 128
-    const unsigned long long MAG4 = f2_pack(-8388608.0f, -8388608.0f);  // 2^23
-    unsigned long long inner[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) inner[t] = 0ull;
-    if constexpr (QT == MOE_Q8_0) {
-        const uint4 qa = *(const uint4 *)(quant_s + ((size_t)(2 * b) * 32 + lane) * 16);
-        const uint4 qb = *(const uint4 *)(quant_s + ((size_t)(2 * b + 1) * 32 + lane) * 16);
-        const unsigned short dh = *(const unsigned short *)(scale_s + ((size_t)b * 32 + lane) * 2);
-        const uint32_t wd[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t wx = wd[i] ^ 0x80808080u;  // int8 -> offset-128 bytes
-            const float v0 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7440));
-            const float v1 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7441));
-            const float v2 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7442));
-            const float v3 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7443));
-            const unsigned long long p01 = f2_add(f2_pack(v0, v1), MAG8);
-            const unsigned long long p23 = f2_add(f2_pack(v2, v3), MAG8);
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                const float4 xv = *(const float4 *)(act + (size_t)t * Kr + b * 32 + 4 * i);
-                inner[t] = f2_fma(p01, f2_pack(xv.x, xv.y), inner[t]);
-                inner[t] = f2_fma(p23, f2_pack(xv.z, xv.w), inner[t]);
-            }
-        }
-        const float d = __half2float(__ushort_as_half(dh));
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            float lo, hi;
-            f2_unpack(inner[t], lo, hi);
-            acc[t] = fmaf(d, lo + hi, acc[t]);
-        }
-    } else {
-        const uint4 q = *(const uint4 *)(quant_s + ((size_t)b * 32 + lane) * 16);
-        const uint32_t dm = *(const uint32_t *)(scale_s + ((size_t)b * 32 + lane) * 4);
-        const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t w = wd[i], w5 = wd[i] >> 20;
-            const float v0 = __int_as_float((w & 0xFu) | 0x4B000000u);
-            const float v1 = __int_as_float((w & 0xF0u) | 0x4B000000u);
-            const float v2 = __int_as_float((w & 0xF00u) | 0x4B000000u);
-            const float v3 = __int_as_float((w & 0xF000u) | 0x4B000000u);
-            const float v4 = __int_as_float((w & 0xF0000u) | 0x4B000000u);
-            const float v5 = __int_as_float((w5 & 0xFu) | 0x4B000000u);
-            const float v6 = __int_as_float((w5 & 0xF0u) | 0x4B000000u);
-            const float v7 = __int_as_float((w5 & 0xF00u) | 0x4B000000u);
-            const unsigned long long p01 = f2_add(f2_pack(v0, v1), MAG4);
-            const unsigned long long p23 = f2_add(f2_pack(v2, v3), MAG4);
-            const unsigned long long p45 = f2_add(f2_pack(v4, v5), MAG4);
-            const unsigned long long p67 = f2_add(f2_pack(v6, v7), MAG4);
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                const float4 xa = *(const float4 *)(act + (size_t)t * Kr + b * 32 + 8 * i);
-                const float4 xb = *(const float4 *)(act + (size_t)t * Kr + b * 32 + 8 * i + 4);
-                inner[t] = f2_fma(p01, f2_pack(xa.x, xa.y), inner[t]);
-                inner[t] = f2_fma(p23, f2_pack(xa.z, xa.w), inner[t]);
-                inner[t] = f2_fma(p45, f2_pack(xb.x, xb.y), inner[t]);
-                inner[t] = f2_fma(p67, f2_pack(xb.z, xb.w), inner[t]);
-            }
-        }
-        const float d = __half2float(__ushort_as_half((unsigned short)(dm & 0xFFFFu)));
-        const float m = __half2float(__ushort_as_half((unsigned short)(dm >> 16)));
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            float lo, hi;
-            f2_unpack(inner[t], lo, hi);
-            acc[t] = fmaf(d, lo + hi, fmaf(m, asum[(size_t)t * nbr + b], acc[t]));
-        }
-    }
-}
-
-// A warp's blocks [b0, b1) of one lane's row; with few tokens two blocks per step so that
-// their loads and FMA chains interleave.
-template <int QT, int NT>
-__device__ __forceinline__ void tile_dot(const unsigned char *quant_s, const unsigned char *scale_s,
-                                         const float *act, const float *asum, int Kr, int nbr, int b0, int b1,
-                                         int lane, float *acc) {
-    int b = b0;
-    if constexpr (NT <= 4)  // few tokens: two blocks' chains side by side (more tokens carry their own ILP)
-        for (; b + 1 < b1; b += 2) {
-            block_dot<QT, NT>(quant_s, scale_s, act, asum, Kr, nbr, b, lane, acc);
-            block_dot<QT, NT>(quant_s, scale_s, act, asum, Kr, nbr, b + 1, lane, acc);
-        }
-    for (; b < b1; ++b) block_dot<QT, NT>(quant_s, scale_s, act, asum, Kr, nbr, b, lane, acc);
-}
-
+// Decoded fp32 pairs of one 32-bit word of codes (q8_0: 4 codes -> 2 pairs; 4-bit: 8 codes
+// -> 4 pairs, code j scaled by 16^j or 16^(j-5)).
 template <int QT>
-__device__ __forceinline__ void tile_dot_dispatch(int nt, const unsigned char *quant_s, const unsigned char *scale_s,
-                                                  const float *act, const float *asum, int Kr, int nbr, int b0,
-                                                  int b1, int lane, float *acc) {
-    switch (nt) {
-        case 1: tile_dot<QT, 1>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
-        case 2: tile_dot<QT, 2>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
-        case 3: tile_dot<QT, 3>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
-        case 4: tile_dot<QT, 4>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
-        case 5: tile_dot<QT, 5>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
-        case 6: tile_dot<QT, 6>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
-        case 7: tile_dot<QT, 7>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
-        default: tile_dot<QT, 8>(quant_s, scale_s, act, asum, Kr, nbr, b0, b1, lane, acc); break;
+__device__ __forceinline__ void decode_word(uint32_t w, unsigned long long (&p)[QT == MOE_Q8_0 ? 2 : 4]) {
+    if constexpr (QT == MOE_Q8_0) {
+        const unsigned long long MAG8 = f2_pack(-8388736.0f, -8388736.0f);  // 2^23 + 128
+        const uint32_t wx = w ^ 0x80808080u;  // int8 -> offset-128 bytes
+        const float v0 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7440));
+        const float v1 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7441));
+        const float v2 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7442));
+        const float v3 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7443));
+        p[0] = f2_add(f2_pack(v0, v1), MAG8);
+        p[1] = f2_add(f2_pack(v2, v3), MAG8);
+    } else {
+        const unsigned long long MAG4 = f2_pack(-8388608.0f, -8388608.0f);  // 2^23
+        const uint32_t w5 = w >> 20;
+        const float v0 = __int_as_float((w & 0xFu) | 0x4B000000u);
+        const float v1 = __int_as_float((w & 0xF0u) | 0x4B000000u);
+        const float v2 = __int_as_float((w & 0xF00u) | 0x4B000000u);
+        const float v3 = __int_as_float((w & 0xF000u) | 0x4B000000u);
+        const float v4 = __int_as_float((w & 0xF0000u) | 0x4B000000u);
+        const float v5 = __int_as_float((w5 & 0xFu) | 0x4B000000u);
+        const float v6 = __int_as_float((w5 & 0xF0u) | 0x4B000000u);
+        const float v7 = __int_as_float((w5 & 0xF00u) | 0x4B000000u);
+        p[0] = f2_add(f2_pack(v0, v1), MAG4);
+        p[1] = f2_add(f2_pack(v2, v3), MAG4);
+        p[2] = f2_add(f2_pack(v4, v5), MAG4);
+        p[3] = f2_add(f2_pack(v6, v7), MAG4);
     }
+}
+
+// One block b of the lane's row in NTL tiles against NT staged activation rows:
+// acc[i][t] += d_i * sum (+ m_i * asum for 4-bit).  Each activation vector read from
+// shared memory serves every tile.  act: [NT][Kr] fp32, asum: [NT][nbr].
+template <int QT, int NT, int NTL>
+__device__ __forceinline__ void block_dot(const unsigned char *tile0, const unsigned char *tile1, size_t scale_off,
+                                          const float *act, const float *asum, int Kr, int nbr, int b, int lane,
+                                          float (&acc)[2][GV_TOK]) {
+    constexpr int WPB = QT == MOE_Q8_0 ? 8 : 4;  // 32-bit code words per lane and block
+    constexpr int PPW = QT == MOE_Q8_0 ? 2 : 4;  // fp32 pairs per word
+    const unsigned char *tl[2] = {tile0, tile1};
+    uint32_t wd[NTL][WPB];
+    uint32_t sc[NTL];
+#pragma unroll
+    for (int i = 0; i < NTL; ++i) {
+        if constexpr (QT == MOE_Q8_0) {
+            const uint4 qa = *(const uint4 *)(tl[i] + ((size_t)(2 * b) * 32 + lane) * 16);
+            const uint4 qb = *(const uint4 *)(tl[i] + ((size_t)(2 * b + 1) * 32 + lane) * 16);
+            wd[i][0] = qa.x; wd[i][1] = qa.y; wd[i][2] = qa.z; wd[i][3] = qa.w;
+            wd[i][4] = qb.x; wd[i][5] = qb.y; wd[i][6] = qb.z; wd[i][7] = qb.w;
+            sc[i] = *(const unsigned short *)(tl[i] + scale_off + ((size_t)b * 32 + lane) * 2);
+        } else {
+            const uint4 q = *(const uint4 *)(tl[i] + ((size_t)b * 32 + lane) * 16);
+            wd[i][0] = q.x; wd[i][1] = q.y; wd[i][2] = q.z; wd[i][3] = q.w;
+            sc[i] = *(const uint32_t *)(tl[i] + scale_off + ((size_t)b * 32 + lane) * 4);
+        }
+    }
+    unsigned long long inner[NTL][NT];
+#pragma unroll
+    for (int i = 0; i < NTL; ++i)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) inner[i][t] = 0ull;
+#pragma unroll
+    for (int wi = 0; wi < WPB; ++wi) {
+        unsigned long long pr[NTL][PPW];
+#pragma unroll
+        for (int i = 0; i < NTL; ++i) decode_word<QT>(wd[i][wi], pr[i]);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const float *ap = act + (size_t)t * Kr + b * 32 + 2 * PPW * wi;
+            const float4 xa = *(const float4 *)ap;
+            const unsigned long long x01 = f2_pack(xa.x, xa.y), x23 = f2_pack(xa.z, xa.w);
+            unsigned long long x45 = 0ull, x67 = 0ull;
+            if constexpr (PPW == 4) {
+                const float4 xb = *(const float4 *)(ap + 4);
+                x45 = f2_pack(xb.x, xb.y);
+                x67 = f2_pack(xb.z, xb.w);
+            }
+#pragma unroll
+            for (int i = 0; i < NTL; ++i) {
+                inner[i][t] = f2_fma(pr[i][0], x01, inner[i][t]);
+                inner[i][t] = f2_fma(pr[i][1], x23, inner[i][t]);
+                if constexpr (PPW == 4) {
+                    inner[i][t] = f2_fma(pr[i][2], x45, inner[i][t]);
+                    inner[i][t] = f2_fma(pr[i][3], x67, inner[i][t]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NTL; ++i) {
+        const float d = __half2float(__ushort_as_half((unsigned short)(sc[i] & 0xFFFFu)));
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float lo, hi;
+            f2_unpack(inner[i][t], lo, hi);
+            if constexpr (QT == MOE_Q8_0) {
+                acc[i][t] = fmaf(d, lo + hi, acc[i][t]);
+            } else {
+                const float m = __half2float(__ushort_as_half((unsigned short)(sc[i] >> 16)));
+                acc[i][t] = fmaf(d, lo + hi, fmaf(m, asum[(size_t)t * nbr + b], acc[i][t]));
+            }
+        }
+    }
+}
+
+template <int QT, int NTL>
+__device__ __forceinline__ void tile_dot_dispatch(int nt, const unsigned char *tile0, const unsigned char *tile1,
+                                                  size_t scale_off, const float *act, const float *asum, int Kr,
+                                                  int nbr, int b0, int b1, int lane, float (&acc)[2][GV_TOK]) {
+#define GV_DOT(N)                                                                                    \
+    for (int b = b0; b < b1; ++b)                                                                    \
+        block_dot<QT, N, NTL>(tile0, tile1, scale_off, act, asum, Kr, nbr, b, lane, acc);           \
+    break;
+    switch (nt) {
+        case 1: GV_DOT(1)
+        case 2: GV_DOT(2)
+        case 3: GV_DOT(3)
+        case 4: GV_DOT(4)
+        case 5: GV_DOT(5)
+        case 6: GV_DOT(6)
+        case 7: GV_DOT(7)
+        default: GV_DOT(8)
+    }
+#undef GV_DOT
 }
 
 // Block sums of the (unscaled) activations for the 4-bit min term.
@@ -314,10 +366,10 @@ __device__ __forceinline__ void compute_asum(const float *act, float *asum, int 
 
 struct FfnParams {
     const void *x;
-    int T, H, F, k, E, KS, RT;
+    int T, H, F, k, E, KS, RT, TPU;
     const float *weights;
     const int32_t *ws_ints;
-    int32_t *tickets;  // [E][F/32] gate/up arrivals per (active expert, row tile)
+    const int32_t *ranges;  // this launch's CTA boundaries: CTA c takes units [ranges[c], ranges[c+1])
     const ActInfo *info;
     float *gu;
     float *h;
@@ -331,34 +383,11 @@ __device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// This CTA's contiguous share [u0, u1) of the units, balanced by work: unit u of active
-// expert a starts at cost per_a * P[a] + (u - a * per_a) * cost(a) (P: prefix of the
-// experts' unit costs), and CTA c takes the units starting in [c C / G, (c+1) C / G).
-__device__ __forceinline__ int unit_at_cost(long long x, int n_act, int per_a, const int *P, const ActInfo *info) {
-    const long long C = (long long)per_a * P[n_act];
-    if (x >= C) return n_act * per_a;
-    int lo = 0, hi = n_act - 1;  // largest a with per_a * P[a] <= x
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) / 2;
-        if ((long long)per_a * P[mid] <= x) lo = mid;
-        else hi = mid - 1;
-    }
-    const long long rem = x - (long long)per_a * P[lo];
-    const int c = unit_cost(info[lo].n_e);
-    return lo * per_a + (int)((rem + c - 1) / c);
-}
-
-__device__ __forceinline__ void cta_range(int n_act, int per_a, const int *P, const ActInfo *info, int &u0,
-                                          int &u1) {
-    const long long C = (long long)per_a * P[n_act];
-    u0 = unit_at_cost(C * blockIdx.x / gridDim.x, n_act, per_a, P, info);
-    u1 = unit_at_cost(C * (blockIdx.x + 1) / gridDim.x, n_act, per_a, P, info);
-}
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 // Stage the activations of route positions [pos, pos+nt) for columns [c0, c0+Kr): gate/up
-// reads x (fp32 or bf16) of the routes' tokens (route of position pos+t at rbase[rpos+t]),
-// down reads h.  Zero rows are not
-// needed: the dot products run over exactly nt rows.
+// reads x (fp32 or bf16) of the routes' tokens (route of position pos+t at rbase[rpos+t]);
+// down reads h, or forms silu(sum gate) * (sum up) from the K-split partial sums.
 template <int QT, int XT, bool DOWN>
 __device__ __forceinline__ void load_act(const FfnParams &p, const int *rbase, int rpos, int pos, int nt, int c0,
                                          int Kr, float *act) {
@@ -367,7 +396,20 @@ __device__ __forceinline__ void load_act(const FfnParams &p, const int *rbase, i
         const int t = idx / nq, c = 4 * (idx - t * nq);
         float4 v;
         if (DOWN) {
-            v = *(const float4 *)(p.h + (size_t)(pos + t) * p.F + c);
+            const size_t q = (size_t)(pos + t) * p.F + c;
+            if (p.KS == 1) {
+                v = *(const float4 *)(p.h + q);
+            } else {
+                float4 gs = make_float4(0.f, 0.f, 0.f, 0.f), us = gs;
+                for (int ks = 0; ks < p.KS; ++ks) {  // fixed order over the K ranges
+                    const float4 gv = *(const float4 *)(p.gu + ((size_t)ks * 2 + 0) * p.RT * p.F + q);
+                    const float4 uv = *(const float4 *)(p.gu + ((size_t)ks * 2 + 1) * p.RT * p.F + q);
+                    gs.x += gv.x; gs.y += gv.y; gs.z += gv.z; gs.w += gv.w;
+                    us.x += uv.x; us.y += uv.y; us.z += uv.z; us.w += uv.w;
+                }
+                v = make_float4(silu_mul(gs.x, us.x), silu_mul(gs.y, us.y), silu_mul(gs.z, us.z),
+                                silu_mul(gs.w, us.w));
+            }
         } else {
             const size_t off = (size_t)(rbase[rpos + t] / p.k) * p.H + c0 + c;
             if (XT == MOE_BF16) {
@@ -396,65 +438,14 @@ __device__ __forceinline__ void load_act(const FfnParams &p, const int *rbase, i
     }
 }
 
-// Count one row write of (active expert a, row tile g) — 2*KS*n_e in all, one per (K range,
-// matrix, token); n_e and pos0 are the expert's token count and first route position.  The warp whose write completes the count forms h = silu(gate) * up for
-// every token of the expert on those rows, summing the K ranges in order.  The fence
-// publishes this warp's writes before the count; the last writer's fence orders the reads.
-struct TicketArgs {
-    int32_t *tickets;
-    const float *gu;
-    float *h;
-    int F, RT, KS;
-};
-
-__device__ __noinline__ void gu_ticket(TicketArgs p, int a, int g, int n_e, int pos0, int lane) {
-    __threadfence();
-    int last = 0;
-    if (lane == 0) last = atomicAdd(&p.tickets[a * (p.F / 32) + g], 1) == 2 * p.KS * n_e - 1;
-    if (!__shfl_sync(0xffffffffu, last, 0)) return;
-    __threadfence();
-    constexpr int TB = 4;  // tokens whose partial sums are loaded together
-    for (int t0 = 0; t0 < n_e; t0 += TB) {
-        float gv[TB][4], uv[TB][4];
-#pragma unroll
-        for (int t = 0; t < TB; ++t)
-#pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) {
-                gv[t][k2] = uv[t][k2] = 0.f;
-                if (t0 + t < n_e && k2 < p.KS) {
-                    const size_t q = (size_t)(pos0 + t0 + t) * p.F + 32 * g + lane;
-                    gv[t][k2] = __ldcg(p.gu + ((size_t)k2 * 2 + 0) * p.RT * p.F + q);
-                    uv[t][k2] = __ldcg(p.gu + ((size_t)k2 * 2 + 1) * p.RT * p.F + q);
-                }
-            }
-#pragma unroll
-        for (int t = 0; t < TB; ++t) {
-            if (t0 + t >= n_e) break;
-            float gs = 0.f, us = 0.f;  // K ranges summed in ascending order
-#pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2)
-                if (k2 < p.KS) {
-                    gs += gv[t][k2];
-                    us += uv[t][k2];
-                }
-            for (int k2 = 4; k2 < p.KS; ++k2) {
-                const size_t q = (size_t)(pos0 + t0 + t) * p.F + 32 * g + lane;
-                gs += __ldcg(p.gu + ((size_t)k2 * 2 + 0) * p.RT * p.F + q);
-                us += __ldcg(p.gu + ((size_t)k2 * 2 + 1) * p.RT * p.F + q);
-            }
-            p.h[(size_t)(pos0 + t0 + t) * p.F + 32 * g + lane] = gs / (1.0f + expf(-gs)) * us;
-        }
-    }
-}
-
 // ------------------------------------------------------------------ G1 / G2: the ring kernel
 //
-// G1 (gate/up): units per active expert are KS K ranges x 2 matrices x F/32 row tiles,
-// ordered (ks, m, g) so that consecutive units of a CTA share the expert's activations
-// for one K range; each unit writes its K range's dot products to gu, and the warp whose
-// write completes an (expert, row tile) writes h = silu(sum gate) * (sum up) for it.
-// G2 (down): units per active expert are H/32 row tiles over the whole of F with h as
-// activations; each unit writes w[r] * (Wd h) for its routes r.
+// G1 (gate/up): units per active expert are KS K ranges x F/32 row tiles, ordered (ks, g);
+// unit (ks, g) holds the gate tile g and the up tile g over K range ks, so consecutive units
+// of a CTA share the expert's activations.  The reducing warp of token t forms
+// h = silu(gate) * up (KS = 1) or stores both partial sums (KS > 1).
+// G2 (down): units per active expert are H/(32 TPU) groups of TPU row tiles over the whole
+// of F with h as activations; each unit writes w[r] * (Wd h) for its routes r.
 //
 // Ring protocol: stage s = i % S holds the CTA's i-th unit.  Thread 0 issues unit i+S-1
 // at the top of iteration i, into the stage that unit i-1 used; every thread has finished
@@ -463,17 +454,18 @@ __device__ __noinline__ void gu_ticket(TicketArgs p, int a, int g, int n_e, int 
 // exactly one phase per use and the waits use parity (i / S) & 1.
 
 template <int QT, int XT, bool DOWN>
-__global__ void __launch_bounds__(GV_THREADS, 2) ffn_ring_kernel(FfnParams p) {
+__global__ void __launch_bounds__(GV_THREADS, 1) ffn_ring_kernel(FfnParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int S = p.stages;
     const int RTF = p.F / 32, RTH = p.H / 32;
+    const int NTL = DOWN ? p.TPU : 2;
     const int nbr = DOWN ? p.F / 32 : (p.H / 32) / p.KS, Kr = nbr * 32;
     const int R = DOWN ? p.H : p.F, K = DOWN ? p.F : p.H;
-    const int per_a = DOWN ? RTH : p.KS * 2 * RTF;
-    int u0, u1;
-    cta_range(p.ws_ints[0], per_a, p.ws_ints + ws_cost_off(p.E, p.RT, p.F), p.info, u0, u1);
+    const int per_a = DOWN ? RTH / p.TPU : p.KS * RTF;
+    const int u0 = p.ranges[blockIdx.x], u1 = p.ranges[blockIdx.x + 1];
     if (u0 >= u1) return;
-    const RingSmem L = ring_smem(QT, nbr, min(p.T, GV_TOK), S);
+    const int ntok = min(p.T, GV_TOK);
+    const RingSmem L = ring_smem(QT, nbr, NTL, ntok, S);
     uint64_t *bars = (uint64_t *)(smem + L.bars);
     unsigned char *stages = smem + L.stages;
     float *act = (float *)(smem + L.act);
@@ -502,31 +494,34 @@ __global__ void __launch_bounds__(GV_THREADS, 2) ffn_ring_kernel(FfnParams p) {
     const int *rbase = rcache ? rts_s : routes;
     const int rpos0 = rcache ? pos_lo : 0;  // route position q is at rbase[q - rpos0]
 
-    // unit u -> active expert a, K range ks, matrix m, row tile g
-    auto decode = [&](int u, int &a, int &ks, int &m, int &g) {
+    // unit u -> active expert a, K range ks, first row tile g (tile i: matrix mats[i], row tile g + i*DOWN)
+    auto decode = [&](int u, int &a, int &ks, int &g) {
         a = u / per_a;
-        int r = u - a * per_a;
+        const int r = u - a * per_a;
         if (DOWN) {
             ks = 0;
-            m = 2;
-            g = r;
+            g = r * p.TPU;
         } else {
-            ks = r / (2 * RTF);
-            r -= ks * 2 * RTF;
-            m = r / RTF;
-            g = r - m * RTF;
+            ks = r / RTF;
+            g = r - ks * RTF;
         }
     };
+    auto tile_mat = [&](int i) { return DOWN ? 2 : i; };
+    auto tile_row = [&](int g, int i) { return DOWN ? g + i : g; };
     auto issue = [&](int u, int s, bool cached) {  // thread 0 only
-        int a, ks, m, g;
-        decode(u, a, ks, m, g);
+        int a, ks, g;
+        decode(u, a, ks, g);
         const ActInfo in = cached ? info_at(a) : p.info[a];
         if (in.n_e == 0 || in.fill) {
             mbar_arrive_plain(&bars[s]);
             return;
         }
-        issue_unit<QT>((const uint8_t *)in.src + moe_expert_matrix_offset(QT, p.H, p.F, m), R, K, g, ks * nbr, nbr,
-                       stages + (size_t)s * L.stage_bytes, L.scale_off, &bars[s]);
+        const int QB = QT == MOE_Q8_0 ? 1024 : 512, SB = 32 * moe_scale_entry_bytes(QT);
+        mbar_arrive_expect_tx(&bars[s], (uint32_t)(NTL * nbr * (QB + SB)));
+        for (int i = 0; i < NTL; ++i)
+            issue_tile<QT>((const uint8_t *)in.src + moe_expert_matrix_offset(QT, p.H, p.F, tile_mat(i)), R, K,
+                           tile_row(g, i), ks * nbr, nbr, stages + (size_t)s * L.stage_bytes + i * L.tile_bytes,
+                           L.scale_off, &bars[s]);
     };
 
     if (threadIdx.x == 0) {
@@ -539,25 +534,26 @@ __global__ void __launch_bounds__(GV_THREADS, 2) ffn_ring_kernel(FfnParams p) {
     int b0, b1;
     warp_blocks(nbr, warp, b0, b1);
     int cur_a = -1, cur_ks = -1, cur_tg = -1;
-    int pend_a = -1, pend_g = 0, pend_ne = 0, pend_pos = 0;  // gate/up: last row write not yet counted
-    const TicketArgs targs{p.tickets, p.gu, p.h, p.F, p.RT, p.KS};
     int i = 0;
     bool failed = false;
     for (; u0 + i < u1; ++i) {
         const int u = u0 + i, s = i % S;
         if (threadIdx.x == 0 && u + S - 1 < u1) issue(u + S - 1, (i + S - 1) % S, true);
-        int a, ks, m, g;
-        decode(u, a, ks, m, g);
+        int a, ks, g;
+        decode(u, a, ks, g);
         const ActInfo in = info_at(a);
         unsigned char *stage = stages + (size_t)s * L.stage_bytes;
         // activations of the first token pass, loaded while the unit's bytes arrive
         const bool fresh = in.n_e > 0 && (a != cur_a || ks != cur_ks || cur_tg != 0);
-        if (fresh) load_act<QT, XT, DOWN>(p, rbase, in.pos0 - rpos0, in.pos0, min(GV_TOK, in.n_e), ks * Kr, Kr, act);
+        if (fresh)
+            load_act<QT, XT, DOWN>(p, rbase, in.pos0 - rpos0, in.pos0, min(GV_TOK, in.n_e), ks * Kr, Kr, act);
         const bool ok = mbar_wait_bounded(&bars[s], (i / S) & 1, p.status);
         if (in.fill && in.n_e > 0) {
-            const size_t mo = moe_expert_matrix_offset(QT, p.H, p.F, m);
-            fill_unit<QT>((const uint8_t *)in.src + mo, (uint8_t *)in.dst + mo, R, K, g, ks * nbr, nbr, stage,
-                          L.scale_off);
+            for (int t = 0; t < NTL; ++t) {
+                const size_t mo = moe_expert_matrix_offset(QT, p.H, p.F, tile_mat(t));
+                fill_tile<QT>((const uint8_t *)in.src + mo, (uint8_t *)in.dst + mo, R, K, tile_row(g, t), ks * nbr,
+                              nbr, stage + t * L.tile_bytes, L.scale_off);
+            }
             fence_proxy_async_smem();  // a later bulk copy overwrites this stage
         }
         // uniform: every thread saw its stage complete; the activations and a filled stage
@@ -586,38 +582,44 @@ __global__ void __launch_bounds__(GV_THREADS, 2) ffn_ring_kernel(FfnParams p) {
                 }
                 cur_tg = tg;
             }
-            float acc[GV_TOK];
+            float acc[2][GV_TOK];
 #pragma unroll
-            for (int t = 0; t < GV_TOK; ++t) acc[t] = 0.f;
-            tile_dot_dispatch<QT>(nt, stage, stage + L.scale_off, act, asum, Kr, nbr, b0, b1, lane, acc);
+            for (int t = 0; t < GV_TOK; ++t) acc[0][t] = acc[1][t] = 0.f;
+            if (NTL == 2)
+                tile_dot_dispatch<QT, 2>(nt, stage, stage + L.tile_bytes, L.scale_off, act, asum, Kr, nbr, b0, b1,
+                                         lane, acc);
+            else
+                tile_dot_dispatch<QT, 1>(nt, stage, stage, L.scale_off, act, asum, Kr, nbr, b0, b1, lane, acc);
 #pragma unroll
             for (int t = 0; t < GV_TOK; ++t)
-                if (t < nt) red[((size_t)warp * GV_TOK + t) * 32 + lane] = acc[t];
+                if (t < nt) {
+                    red[(((size_t)warp * ntok + t) * 2 + 0) * 32 + lane] = acc[0][t];
+                    red[(((size_t)warp * ntok + t) * 2 + 1) * 32 + lane] = acc[1][t];
+                }
             __syncthreads();  // red complete; every thread is done reading this stage and act
             if (warp < nt) {
-                float sum = 0.f;
+                float v0 = 0.f, v1 = 0.f;
 #pragma unroll
-                for (int w = 0; w < GV_WARPS; ++w) sum += red[((size_t)w * GV_TOK + warp) * 32 + lane];
+                for (int w = 0; w < GV_WARPS; ++w) {
+                    v0 += red[(((size_t)w * ntok + warp) * 2 + 0) * 32 + lane];
+                    v1 += red[(((size_t)w * ntok + warp) * 2 + 1) * 32 + lane];
+                }
                 const int pos = in.pos0 + tg + warp;
                 if (DOWN) {
                     const int r = rbase[pos - rpos0];
                     const float wr = rcache ? wts_s[pos - rpos0] : p.weights[r];
-                    p.partial[(size_t)r * p.H + 32 * g + lane] = wr * sum;
+                    p.partial[(size_t)r * p.H + 32 * g + lane] = wr * v0;
+                    if (NTL == 2) p.partial[(size_t)r * p.H + 32 * (g + 1) + lane] = wr * v1;
+                } else if (p.KS == 1) {
+                    p.h[(size_t)pos * p.F + 32 * g + lane] = silu_mul(v0, v1);
                 } else {
-                    // this warp's previous row writes have drained while it computed: their
-                    // ticket costs no wait now
-                    if (pend_a >= 0) gu_ticket(targs, pend_a, pend_g, pend_ne, pend_pos, lane);
-                    p.gu[(((size_t)ks * 2 + m) * p.RT + pos) * p.F + 32 * g + lane] = sum;
-                    pend_a = a;
-                    pend_g = g;
-                    pend_ne = in.n_e;
-                    pend_pos = in.pos0;
+                    p.gu[(((size_t)ks * 2 + 0) * p.RT + pos) * p.F + 32 * g + lane] = v0;
+                    p.gu[(((size_t)ks * 2 + 1) * p.RT + pos) * p.F + 32 * g + lane] = v1;
                 }
             }
             if (tg + GV_TOK < in.n_e) __syncthreads();  // red and act are rewritten by the next pass
         }
     }
-    if (!DOWN && pend_a >= 0) gu_ticket(targs, pend_a, pend_g, pend_ne, pend_pos, lane);
     // A wait ran out: never leave with copies in flight.  Units i .. last issued are
     // unconsumed; give each a second bounded wait.
     if (failed && threadIdx.x == 0) {
@@ -628,17 +630,34 @@ __global__ void __launch_bounds__(GV_THREADS, 2) ffn_ring_kernel(FfnParams p) {
 
 // ------------------------------------------------------------------ P1: permute
 
+// First unit whose start cost is >= x: unit u of active expert a starts at cost
+// per_a * P[a] + (u - a * per_a) * cost[a].
+__device__ __forceinline__ int unit_at_cost(long long x, int n_act, int per_a, const int *P, const int *cost) {
+    const long long C = (long long)per_a * P[n_act];
+    if (x >= C) return n_act * per_a;
+    int lo = 0, hi = n_act - 1;  // largest a with per_a * P[a] <= x
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if ((long long)per_a * P[mid] <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    const long long rem = x - (long long)per_a * P[lo];
+    return lo * per_a + (int)((rem + cost[lo] - 1) / cost[lo]);
+}
+
 // Stable counting sort of the routes r = t*k + j by expert (restricted to a subset), the
-// ascending list of active experts, their route ranges, and per active expert where its
-// weights are read from (slot in the pool, or its pinned host image for a fill).
+// ascending list of active experts, their route ranges, per active expert where its weights
+// are read from (slot in the pool, or its pinned host image for a fill), and the unit
+// ranges of the CTAs of both GEMV launches, balanced by work (unit_cost).
 __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict__ ids, int R, int E,
                                                       const int32_t *__restrict__ subset, int n_subset,
                                                       int32_t *__restrict__ ints, ActInfo *__restrict__ info,
                                                       const int32_t *__restrict__ slot_table, int n_slots,
                                                       const uint8_t *pool, size_t slot_bytes,
                                                       const unsigned long long *__restrict__ fill_src,
-                                                      int RTF, int *status) {
+                                                      int G1, int per_a1, int G2, int per_a2, int *status) {
     __shared__ int cnt[MOE_MAX_E], off[MOE_MAX_E + 1], run[MOE_MAX_E];
+    __shared__ int P[MOE_MAX_E + 1], cost[MOE_MAX_E];
     __shared__ unsigned char insub[MOE_MAX_E];
     __shared__ int chunk_e[256];
     __shared__ int n_act;
@@ -679,11 +698,8 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
         aoff[na] = s;
         ints[0] = na;
         n_act = na;
-
     }
     __syncthreads();
-    int *tickets = ints + ws_ticket_off(E, R);
-    for (int i = tid; i < n_act * RTF; i += 256) tickets[i] = 0;
     for (int a = tid; a < n_act; a += 256) {
         const int e = active[a];
         const int slot = slot_table ? slot_table[e] : e;
@@ -703,16 +719,23 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
             in.src = f ? f : in.dst;
         }
         info[a] = in;
+        cost[a] = unit_cost(in.n_e);
     }
     __syncthreads();
     if (tid == 0) {  // work prefix over the active experts (skipped experts cost 1 per unit)
-        int *P = ints + ws_cost_off(E, R, RTF * 32);
         int c = 0;
         for (int a = 0; a < n_act; ++a) {
             P[a] = c;
-            c += unit_cost(info[a].n_e);
+            c += cost[a];
         }
         P[n_act] = c;
+    }
+    __syncthreads();
+    {
+        int *r1 = ints + ws_ranges_off(E, R, 0), *r2 = ints + ws_ranges_off(E, R, 1);
+        const long long C1 = (long long)per_a1 * P[n_act], C2 = (long long)per_a2 * P[n_act];
+        for (int c = tid; c <= G1; c += 256) r1[c] = unit_at_cost(C1 * c / G1, n_act, per_a1, P, cost);
+        for (int c = tid; c <= G2; c += 256) r2[c] = unit_at_cost(C2 * c / G2, n_act, per_a2, P, cost);
     }
     int *routes = ints + ws_routes_off(E);
     for (int c0 = 0; c0 < R; c0 += 256) {
@@ -784,14 +807,14 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(const float4 *__restr
     }
 }
 
-// Resident CTAs per SM of a ring kernel at a dynamic shared-memory size, and the SM
-// count, cached per (device, kernel, size).  The kernel's shared-memory limit is only
-// ever raised, so every cached size stays launchable.
+// Resident CTAs of a ring kernel on the whole device at a dynamic shared-memory size,
+// cached per (device, kernel, size).  The kernel's shared-memory limit is only ever raised,
+// so every cached size stays launchable.
 struct OccEntry {
     int dev;
     const void *fn;
     size_t smem;
-    int ctas;  // resident CTAs on the whole device
+    int ctas;
 };
 
 int ring_grid_capacity(const void *fn, size_t smem, int *ctas) {
@@ -820,38 +843,26 @@ int ring_grid_capacity(const void *fn, size_t smem, int *ctas) {
     MOE_TRY_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, GV_THREADS, smem));
     MOE_TRY_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     if (occ < 1 || sms < 1) return MOE_ERR_UNSUPPORTED;
-    *ctas = occ * sms;
+    *ctas = std::min(occ * sms, GV_MAX_GRID);
     if (n_tab < 64) tab[n_tab++] = {dev, fn, smem, *ctas};
     return MOE_OK;
 }
 
-// Persistent launch: as many CTAs as are resident at once, but no more than units.
-template <typename Kern>
-int launch_ring_kernel(Kern kern, int max_units, size_t smem, const FfnParams &p, cudaStream_t s) {
-    if (max_units <= 0) return MOE_OK;
-    int ctas = 0;
-    const int rc = ring_grid_capacity((const void *)kern, smem, &ctas);
-    if (rc != MOE_OK) return rc;
-    kern<<<std::min(max_units, ctas), GV_THREADS, smem, s>>>(p);
-    MOE_TRY_CUDA(cudaGetLastError());
-    return MOE_OK;
+template <int QT, int XT, bool DOWN>
+const void *ring_fn() {
+    return (const void *)ffn_ring_kernel<QT, XT, DOWN>;
 }
 
-// Ring depth: the preferred number of stages, fewer when the shared memory would not fit.
-int ring_stages(int qtype, int nbr, int ntok, int preferred) {
-    for (int S = preferred; S >= 1; --S)
-        if (ring_smem(qtype, nbr, ntok, S).total <= GV_SMEM_MAX) return S;
-    return 0;
+const void *ring_kernel_for(int qtype, int xtype, bool down) {
+    if (qtype == MOE_Q8_0) {
+        if (down) return ring_fn<MOE_Q8_0, MOE_F32, true>();
+        return xtype == MOE_F32 ? ring_fn<MOE_Q8_0, MOE_F32, false>() : ring_fn<MOE_Q8_0, MOE_BF16, false>();
+    }
+    if (down) return ring_fn<MOE_Q4_SM, MOE_F32, true>();
+    return xtype == MOE_F32 ? ring_fn<MOE_Q4_SM, MOE_F32, false>() : ring_fn<MOE_Q4_SM, MOE_BF16, false>();
 }
 
 }  // namespace
-
-int moe_gateup_ksplit(int qtype, int H) {
-    const int nb = H / 32;
-    int ks = 1;
-    while (moe_quant_bytes(qtype, 32, H / ks) > GV_UNIT_QUANT && nb % (2 * ks) == 0) ks *= 2;
-    return ks;
-}
 
 size_t moe_decode_workspace_bytes(int T, int H, int F, int qtype, int E, int k) {
     return ws_layout(T, H, F, qtype, E, k).total;
@@ -900,58 +911,63 @@ int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype
     const WsLayout W = ws_layout(T, H, F, qtype, E, k);
     MOE_CHECK(ws_bytes >= W.total);
     if ((size_t)T * k > (1u << 20)) return MOE_ERR_UNSUPPORTED;
+    GvPlan pl;
+    if (!gv_plan(T, H, F, qtype, &pl)) return MOE_ERR_UNSUPPORTED;
+    const int ntok = T < GV_TOK ? T : GV_TOK;
+    const int RTF = F / 32, RTH = H / 32;
+    const int nb1 = (H / 32) / pl.KS, nb2 = F / 32;
+    const size_t smem1 = ring_smem(qtype, nb1, 2, ntok, pl.S1).total;
+    const size_t smem2 = ring_smem(qtype, nb2, pl.TPU, ntok, pl.S2).total;
+    const void *k1 = ring_kernel_for(qtype, xtype, false), *k2 = ring_kernel_for(qtype, xtype, true);
+    int cap1 = 0, cap2 = 0, rc;
+    if ((rc = ring_grid_capacity(k1, smem1, &cap1)) != MOE_OK) return rc;
+    if ((rc = ring_grid_capacity(k2, smem2, &cap2)) != MOE_OK) return rc;
+    const int n_act_max = expert_subset ? n_subset : (T * k < E ? T * k : E);
+    const int per_a1 = pl.KS * RTF, per_a2 = RTH / pl.TPU;
+    const int G1 = std::max(1, std::min(cap1, n_act_max * per_a1));
+    const int G2 = std::max(1, std::min(cap2, n_act_max * per_a2));
 
     FfnParams p;
     p.x = x;
     p.T = T; p.H = H; p.F = F; p.k = k; p.E = E;
-    p.KS = moe_gateup_ksplit(qtype, H);
+    p.KS = pl.KS;
+    p.TPU = pl.TPU;
     p.RT = T * k;
     p.weights = weights;
     p.ws_ints = (const int32_t *)((char *)workspace + W.ints_off);
     p.info = (const ActInfo *)((char *)workspace + W.info_off);
-    p.tickets = (int32_t *)((char *)workspace + W.ints_off) + ws_ticket_off(E, T * k);
     p.gu = (float *)((char *)workspace + W.gu_off);
     p.h = (float *)((char *)workspace + W.h_off);
     p.partial = partial;
     p.status = moe_status_word_device_ptr();
     p.x_vec = ((uintptr_t)x % (xtype == MOE_F32 ? 16 : 8)) == 0;
-    const int ntok = T < GV_TOK ? T : GV_TOK;
-
-    const unsigned long long *fill_src = (const unsigned long long *)d_fill_src;
-    const int n_act_max = expert_subset ? n_subset : (T * k < E ? T * k : E);
-    const int nb1 = (H / 32) / p.KS, nb2 = F / 32;
-    const int S1 = ring_stages(qtype, nb1, ntok, GV_S1), S2 = ring_stages(qtype, nb2, ntok, GV_S2);
-    if (S1 == 0 || S2 == 0) return MOE_ERR_UNSUPPORTED;
-    const size_t smem1 = ring_smem(qtype, nb1, ntok, S1).total;
-    const size_t smem2 = ring_smem(qtype, nb2, ntok, S2).total;
 
     if (timing && timing->permute0) MOE_TRY_CUDA(cudaEventRecord(timing->permute0, s));
     permute_kernel<<<1, 256, 0, s>>>(ids, T * k, E, expert_subset, n_subset,
                                      (int32_t *)((char *)workspace + W.ints_off),
                                      (ActInfo *)((char *)workspace + W.info_off), d_slot_table, n_slots,
-                                     (const uint8_t *)pool, slot_bytes, fill_src, F / 32, p.status);
+                                     (const uint8_t *)pool, slot_bytes, (const unsigned long long *)d_fill_src,
+                                     G1, per_a1, G2, per_a2, p.status);
     MOE_TRY_CUDA(cudaGetLastError());
     if (timing && timing->permute1) MOE_TRY_CUDA(cudaEventRecord(timing->permute1, s));
     if (timing && timing->gateup0) MOE_TRY_CUDA(cudaEventRecord(timing->gateup0, s));
-    const int units1 = n_act_max * 2 * (F / 32) * p.KS;
-    int rc;
-    p.stages = S1;
-    if (qtype == MOE_Q8_0)
-        rc = xtype == MOE_F32
-                 ? launch_ring_kernel(ffn_ring_kernel<MOE_Q8_0, MOE_F32, false>, units1, smem1, p, s)
-                 : launch_ring_kernel(ffn_ring_kernel<MOE_Q8_0, MOE_BF16, false>, units1, smem1, p, s);
-    else
-        rc = xtype == MOE_F32
-                 ? launch_ring_kernel(ffn_ring_kernel<MOE_Q4_SM, MOE_F32, false>, units1, smem1, p, s)
-                 : launch_ring_kernel(ffn_ring_kernel<MOE_Q4_SM, MOE_BF16, false>, units1, smem1, p, s);
-    if (rc != MOE_OK) return rc;
+    p.stages = pl.S1;
+    p.ranges = p.ws_ints + ws_ranges_off(E, T * k, 0);
+    if (qtype == MOE_Q8_0) {
+        if (xtype == MOE_F32) ffn_ring_kernel<MOE_Q8_0, MOE_F32, false><<<G1, GV_THREADS, smem1, s>>>(p);
+        else ffn_ring_kernel<MOE_Q8_0, MOE_BF16, false><<<G1, GV_THREADS, smem1, s>>>(p);
+    } else {
+        if (xtype == MOE_F32) ffn_ring_kernel<MOE_Q4_SM, MOE_F32, false><<<G1, GV_THREADS, smem1, s>>>(p);
+        else ffn_ring_kernel<MOE_Q4_SM, MOE_BF16, false><<<G1, GV_THREADS, smem1, s>>>(p);
+    }
+    MOE_TRY_CUDA(cudaGetLastError());
     if (timing && timing->gateup1) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
     if (timing && timing->down0) MOE_TRY_CUDA(cudaEventRecord(timing->down0, s));
-    const int units2 = n_act_max * (H / 32);
-    p.stages = S2;
-    rc = qtype == MOE_Q8_0 ? launch_ring_kernel(ffn_ring_kernel<MOE_Q8_0, MOE_F32, true>, units2, smem2, p, s)
-                           : launch_ring_kernel(ffn_ring_kernel<MOE_Q4_SM, MOE_F32, true>, units2, smem2, p, s);
-    if (rc != MOE_OK) return rc;
+    p.stages = pl.S2;
+    p.ranges = p.ws_ints + ws_ranges_off(E, T * k, 1);
+    if (qtype == MOE_Q8_0) ffn_ring_kernel<MOE_Q8_0, MOE_F32, true><<<G2, GV_THREADS, smem2, s>>>(p);
+    else ffn_ring_kernel<MOE_Q4_SM, MOE_F32, true><<<G2, GV_THREADS, smem2, s>>>(p);
+    MOE_TRY_CUDA(cudaGetLastError());
     if (timing && timing->down1) MOE_TRY_CUDA(cudaEventRecord(timing->down1, s));
     return MOE_OK;
 }

@@ -83,14 +83,21 @@ struct GvPlan {
     int KS, S1, TPU, S2;
 };
 
-inline bool gv_plan(int T, int H, int F, int qtype, GvPlan *pl) {
+// Units are made small enough that a launch has about GV_UNITS_TARGET of them (a CTA's share
+// is then several units and the work-balanced split is fine-grained), but no smaller than one
+// 32-column block per warp.
+#define GV_UNITS_TARGET 1024
+
+inline bool gv_plan(int T, int H, int F, int qtype, int n_act_max, GvPlan *pl) {
     const int ntok = T < GV_TOK ? T : GV_TOK;
-    const int NB = H / 32;
+    const int NB = H / 32, RTF = F / 32, RTH = H / 32;
     pl->KS = 0;
     for (int ks = 1; ks <= NB && !pl->KS; ks *= 2) {
         if (NB % ks) break;
+        const bool more = (long)n_act_max * ks * RTF < GV_UNITS_TARGET && NB % (2 * ks) == 0 &&
+                          NB / (2 * ks) >= GV_WARPS;
         for (int S = 3; S >= 2 && !pl->KS; --S)
-            if (ring_smem(qtype, NB / ks, 2, ntok, S).total <= GV_SMEM_MAX) {
+            if (!more && ring_smem(qtype, NB / ks, 2, ntok, S).total <= GV_SMEM_MAX) {
                 pl->KS = ks;
                 pl->S1 = S;
             }
@@ -103,9 +110,10 @@ inline bool gv_plan(int T, int H, int F, int qtype, GvPlan *pl) {
         pl->S1 = 1;
     }
     pl->TPU = 0;
+    const bool pairs = RTH % 2 == 0 && (long)n_act_max * (RTH / 2) >= GV_UNITS_TARGET;
     const int cand[7][2] = {{2, 4}, {2, 3}, {2, 2}, {1, 4}, {1, 3}, {1, 2}, {1, 1}};
     for (int i = 0; i < 7 && !pl->TPU; ++i) {
-        if (cand[i][0] == 2 && (H / 32) % 2) continue;
+        if (cand[i][0] == 2 && !pairs) continue;
         if (ring_smem(qtype, F / 32, cand[i][0], ntok, cand[i][1]).total <= GV_SMEM_MAX) {
             pl->TPU = cand[i][0];
             pl->S2 = cand[i][1];
@@ -113,6 +121,8 @@ inline bool gv_plan(int T, int H, int F, int qtype, GvPlan *pl) {
     }
     return pl->TPU != 0;
 }
+
+inline int gv_n_act_max(int T, int E, int k) { return T * k < E ? T * k : E; }
 
 // ------------------------------------------------------------------ workspace layout
 
@@ -142,7 +152,7 @@ inline WsLayout ws_layout(int T, int H, int F, int qtype, int E, int k) {
     WsLayout L;
     const size_t R = (size_t)T * k;
     GvPlan pl;
-    if (!gv_plan(T, H, F, qtype, &pl)) pl.KS = 1;
+    if (!gv_plan(T, H, F, qtype, gv_n_act_max(T, E, k), &pl)) pl.KS = 1;
     const size_t ints = 16 + 2 * (size_t)E + 1 + R + 2 * (GV_MAX_GRID + 1);
     L.ints_off = 0;
     L.info_off = (ints * 4 + 255) / 256 * 256;
@@ -547,7 +557,8 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_ring_kernel(FfnParams p) {
         const bool fresh = in.n_e > 0 && (a != cur_a || ks != cur_ks || cur_tg != 0);
         if (fresh)
             load_act<QT, XT, DOWN>(p, rbase, in.pos0 - rpos0, in.pos0, min(GV_TOK, in.n_e), ks * Kr, Kr, act);
-        const bool ok = mbar_wait_bounded(&bars[s], (i / S) & 1, p.status);
+        // warp 0 waits for the stage; the barrier below publishes it to the other warps
+        const bool ok = warp == 0 ? mbar_wait_bounded(&bars[s], (i / S) & 1, p.status) : true;
         if (in.fill && in.n_e > 0) {
             for (int t = 0; t < NTL; ++t) {
                 const size_t mo = moe_expert_matrix_offset(QT, p.H, p.F, tile_mat(t));
@@ -911,8 +922,8 @@ int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype
     const WsLayout W = ws_layout(T, H, F, qtype, E, k);
     MOE_CHECK(ws_bytes >= W.total);
     if ((size_t)T * k > (1u << 20)) return MOE_ERR_UNSUPPORTED;
-    GvPlan pl;
-    if (!gv_plan(T, H, F, qtype, &pl)) return MOE_ERR_UNSUPPORTED;
+    GvPlan pl;  // planned for every expert routable (the workspace does not depend on a subset)
+    if (!gv_plan(T, H, F, qtype, gv_n_act_max(T, E, k), &pl)) return MOE_ERR_UNSUPPORTED;
     const int ntok = T < GV_TOK ? T : GV_TOK;
     const int RTF = F / 32, RTH = H / 32;
     const int nb1 = (H / 32) / pl.KS, nb2 = F / 32;

@@ -35,6 +35,11 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "moe_tc.cuh"
 
 #define PF_TM 128          // token rows per tile (MMA M)
@@ -43,7 +48,7 @@
 #define PF_DQ_WARPS 16
 #define PF_EPI_WARPS 4
 #define PF_THREADS ((2 + PF_DQ_WARPS + PF_EPI_WARPS) * 32)
-#define PF_AS 2            // dequantised (B operand) ring stages
+#define PF_AS 3            // dequantised (B operand) ring stages
 
 namespace {
 
@@ -74,7 +79,15 @@ inline PfLayout pf_layout(int T, int H, int F, int E, int k) {
     return L;
 }
 
+// TMA tensor maps over the pool, one per (matrix, region): 64-bit words x 512-byte pieces
+// (or 32-lane scale groups) x 32-row tiles x slots, so one copy brings a stage's box of
+// several row tiles of one matrix.
+struct PfMaps {
+    CUtensorMap code[3], scale[3];  // gate, up, down
+};
+
 struct PfParams {
+    PfMaps maps;
     const void *x;
     int T, H, F, k, E;
     const float *weights;
@@ -91,6 +104,17 @@ struct PfParams {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// 4-D TMA tile load global -> shared completing on `bar`; coordinates (x, y, z, w) in elements
+// of the map (x is always 0 here, so the 16-byte alignment of the innermost coordinate holds).
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int x, int y, int z, int w,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
 }
 
 // ------------------------------------------------------------------ route + gather
@@ -289,7 +313,7 @@ __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int *sta
 
 template <int QT>
 struct PfGeom {
-    static constexpr int RS = QT == MOE_Q8_0 ? 4 : 6;         // raw + token tile ring stages
+    static constexpr int RS = QT == MOE_Q8_0 ? 3 : 4;         // raw + token tile ring stages
     static constexpr int RSTAGE = ((PF_TM * 128 + RawGeom<QT>::BYTES) + 1023) / 1024 * 1024;
     static constexpr int BSTAGE = PF_WN * 128;                // dequantised weights, fp16
     static constexpr uint32_t NCOLS = 2 * PF_WN;              // two fp32 accumulators of 256 columns
@@ -301,7 +325,7 @@ struct PfGeom {
 // tile's x; epilogue h = silu(g) * u -> fp16 rows of GEMM 2's A operand.  GEMM 2: slab m =
 // down rows 256m.. of H x F against h; epilogue w[r] * (.) -> partial[r][256m ..].
 template <int QT, bool DOWN>
-__global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(PfParams p) {
+__global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_constant__ PfParams p) {
     extern __shared__ uint8_t smem_raw[];
     using G = RawGeom<QT>;
     using PG = PfGeom<QT>;
@@ -358,54 +382,42 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(PfParams p) {
     auto item_expert = [&](int j) { return ints[p.o_texp + j / MT]; };
 
     if (warp == 0) {
-        // ---------------- producer: raw weight pieces + token tile per K stage.  Lane 0
-        // waits for the stage and sets the byte count; lanes 0-7 then copy one 32-row tile
-        // each (codes and scales) and lane 8 the token tile, side by side.
-        using Gq = RawGeom<QT>;
-        const int R = DOWN ? p.H : p.F, K = DOWN ? p.F : p.H;
-        const size_t code_step = (size_t)2 * Gq::PPB * 512;              // bytes per 64-column stage
-        const size_t scale_step = (size_t)2 * 32 * moe_scale_entry_bytes(QT);
-        int g = 0;
-        bool ok = true;
-        for (int j = blockIdx.x; j < n_items && ok; j += gridDim.x) {
-            const int e = item_expert(j);
-            if (e < 0) continue;
-            const int tile = j / MT, m = j % MT;
-            const int slot = p.slot_table ? p.slot_table[e] : e;
-            const uint8_t *sb = p.pool + (size_t)slot * p.slot_bytes;
-            const uint8_t *csrc = nullptr, *ssrc = nullptr;
-            if (lane < 8) {
-                const int mat = DOWN ? 2 : (lane >> 2);
-                const int gr = DOWN ? 8 * m + lane : 4 * m + (lane & 3);
-                const uint8_t *base = sb + moe_expert_matrix_offset(QT, p.H, p.F, mat);
-                csrc = base + moe_piece_offset(QT, K, gr, 0);
-                ssrc = base + moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, gr, 0);
-            } else if (lane == 8) {
-                csrc = (DOWN ? p.hp : p.xp) + (size_t)tile * NK * PF_TM * 128;
-            }
-            for (int kc = 0; kc < NK; ++kc, ++g) {
-                const int s = g % RS;
-                bool w = true;
-                if (lane == 0) {
-                    if (g >= RS) w = pf_wait(&r_empty[s], ((g / RS) - 1) & 1, p.status, abort_flag);
-                    if (w) mbar_arrive_expect_tx(&r_full[s], Gq::BYTES + PF_TM * 128);
-                }
-                if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
-                __syncwarp();  // the byte count is set before any copy can complete
-                if (lane < 8) {
-                    bulk_g2s(RAW(s) + lane * Gq::QPB, csrc + kc * code_step, Gq::QPB, &r_full[s]);
-                    bulk_g2s(RAW(s) + 8 * Gq::QPB + lane * Gq::SPB, ssrc + kc * scale_step, Gq::SPB, &r_full[s]);
-                } else if (lane == 8) {
-                    bulk_g2s(At(s), csrc + (size_t)kc * PF_TM * 128, PF_TM * 128, &r_full[s]);
+        // ---------------- producer (lane 0): per K stage the token tile (one bulk copy) and, per
+        // weight matrix of the item, one TMA box of codes and one of scales
+        if (lane == 0) {
+            using Gq = RawGeom<QT>;
+            int g = 0;
+            bool ok = true;
+            for (int j = blockIdx.x; j < n_items && ok; j += gridDim.x) {
+                const int e = item_expert(j);
+                if (e < 0) continue;
+                const int tile = j / MT, m = j % MT;
+                const int slot = p.slot_table ? p.slot_table[e] : e;
+                const uint8_t *asrc = (DOWN ? p.hp : p.xp) + (size_t)tile * NK * PF_TM * 128;
+                for (int kc = 0; kc < NK; ++kc, ++g) {
+                    const int s = g % RS;
+                    if (g >= RS && !(ok = pf_wait(&r_empty[s], ((g / RS) - 1) & 1, p.status, abort_flag))) break;
+                    mbar_arrive_expect_tx(&r_full[s], Gq::BYTES + PF_TM * 128);
+                    bulk_g2s(At(s), asrc + (size_t)kc * PF_TM * 128, PF_TM * 128, &r_full[s]);
+                    if (DOWN) {
+                        tma_load_4d(RAW(s), &p.maps.code[2], 0, 2 * kc * Gq::PPB, 8 * m, slot, &r_full[s]);
+                        tma_load_4d(RAW(s) + 8 * Gq::QPB, &p.maps.scale[2], 0, 2 * kc, 8 * m, slot, &r_full[s]);
+                    } else {
+                        for (int mt = 0; mt < 2; ++mt) {
+                            tma_load_4d(RAW(s) + 4 * mt * Gq::QPB, &p.maps.code[mt], 0, 2 * kc * Gq::PPB, 4 * m,
+                                        slot, &r_full[s]);
+                            tma_load_4d(RAW(s) + 8 * Gq::QPB + 4 * mt * Gq::SPB, &p.maps.scale[mt], 0, 2 * kc,
+                                        4 * m, slot, &r_full[s]);
+                        }
+                    }
                 }
             }
-        }
-        // never leave with copies in flight: wait for the last phase issued on each stage
-        if (lane == 0)
+            // never leave with copies in flight: wait for the last phase issued on each stage
             for (int s = 0; s < RS && s < g; ++s) {
                 const int last = s + ((g - 1 - s) / RS) * RS;
                 mbar_wait_bounded(&r_full[s], (last / RS) & 1, p.status);
             }
+        }
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
@@ -542,6 +554,58 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(PfParams p) {
     }
 }
 
+// cuTensorMapEncodeTiled from the driver (looked up once through the runtime).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    });
+    return fn;
+}
+
+// Maps of one matrix (mat: 0 gate, 1 up, 2 down) of every slot: codes as [slot][row tile]
+// [piece][64 x uint64], scales as [slot][row tile][block][32 lanes x entry / 8 x uint64];
+// boxes of 2 K blocks x `tiles` row tiles.
+template <int QT>
+int encode_matrix_maps(const uint8_t *pool, int n_slots, size_t slot_bytes, int H, int F, int mat, int tiles,
+                       CUtensorMap *code, CUtensorMap *scale) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return MOE_ERR_UNSUPPORTED;
+    using G = RawGeom<QT>;
+    const int R = mat == 2 ? H : F, K = mat == 2 ? F : H;
+    const int NB = K / 32, P = NB * G::PPB, SE = moe_scale_entry_bytes(QT);
+    const uint8_t *base = pool + moe_expert_matrix_offset(QT, H, F, mat);
+    {
+        const cuuint64_t dims[4] = {64, (cuuint64_t)P, (cuuint64_t)(R / 32), (cuuint64_t)n_slots};
+        const cuuint64_t strides[3] = {512, (cuuint64_t)P * 512, (cuuint64_t)slot_bytes};
+        const cuuint32_t box[4] = {64, (cuuint32_t)(2 * G::PPB), (cuuint32_t)tiles, 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(code, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, (void *)base, dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return MOE_ERR_CUDA;
+    }
+    {
+        const uint8_t *sbase = base + moe_quant_bytes(QT, R, K);
+        const cuuint64_t dims[4] = {(cuuint64_t)(32 * SE / 8), (cuuint64_t)NB, (cuuint64_t)(R / 32),
+                                    (cuuint64_t)n_slots};
+        const cuuint64_t strides[3] = {(cuuint64_t)(32 * SE), (cuuint64_t)NB * 32 * SE, (cuuint64_t)slot_bytes};
+        const cuuint32_t box[4] = {(cuuint32_t)(32 * SE / 8), 2, (cuuint32_t)tiles, 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(scale, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, (void *)sbase, dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
 int sm_count_cached() {
     static int n = 0;
     if (!n) {
@@ -554,9 +618,14 @@ int sm_count_cached() {
 }
 
 template <int QT>
-int launch_gemms(const PfParams &p, int max_tiles, cudaStream_t s, const moe_ffn_timing *timing) {
+int launch_gemms(PfParams &p, int max_tiles, cudaStream_t s, const moe_ffn_timing *timing) {
     using PG = PfGeom<QT>;
     if (PG::SMEM > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+    for (int mat = 0; mat < 3; ++mat) {
+        const int rc = encode_matrix_maps<QT>(p.pool, p.n_slots, p.slot_bytes, p.H, p.F, mat, mat == 2 ? 8 : 4,
+                                              &p.maps.code[mat], &p.maps.scale[mat]);
+        if (rc != MOE_OK) return rc;
+    }
     MOE_TRY_CUDA(cudaFuncSetAttribute(pf_gemm_kernel<QT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)PG::SMEM));
     MOE_TRY_CUDA(cudaFuncSetAttribute(pf_gemm_kernel<QT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -15,7 +15,8 @@ namespace {
 inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct StackWs {
-    size_t ids, w, partial, table, hit, miss, hA, hB, xn, ids_s, w_s, partial_s, tmp, fill, gin, gout, ffn, total;
+    size_t ids, w, partial, table, hit, miss, hA, hB, xn, ids_s, w_s, partial_s, tmp, fill, gin, gout, nact, ffn,
+        total;
     size_t ffn_bytes;
 };
 
@@ -39,6 +40,7 @@ StackWs stack_ws(int H, int F, int qtype, int E, int k, int T, int n_shared) {
     L.fill = off;      off = align256(off + (size_t)E * 8);
     L.gin = off;       off = align256(off + (size_t)T * H * 4);
     L.gout = off;      off = align256(off + (size_t)T * H * 4);
+    L.nact = off;      off = align256(off + 8);
     size_t f = moe_decode_workspace_bytes(T, H, F, qtype, E, k);
     if (ns > 0) {
         const size_t f2 = moe_decode_workspace_bytes(T, H, F, qtype, ns, ns);
@@ -80,6 +82,7 @@ struct moe_stack {
     cudaGraphExec_t graph[MOE_DECODE_MAX_T + 1] = {};
     uint64_t graph_launches[MOE_DECODE_MAX_T + 1] = {};  // kernels per captured step
     bool eager_done[MOE_DECODE_MAX_T + 1] = {};
+    uint64_t nact_pending = 0;  // routed FFN calls counted on the device since the last harvest
 };
 
 namespace {
@@ -96,8 +99,22 @@ int get_event(moe_stack *st, cudaEvent_t *out) {
     return MOE_OK;
 }
 
+// Profiling: adds the active-expert count the permute kernel left in the FFN workspace to a
+// device-side sum (for the byte accounting of layers whose routing the host never sees).
+__global__ void nact_add_kernel(const int32_t *n_active, unsigned long long *sum) {
+    if (threadIdx.x == 0) *sum += (unsigned long long)*n_active;
+}
+
 // Accumulates the elapsed times of recorded event pairs (all complete) and recycles them.
 int harvest(moe_stack *st) {
+    if (st->nact_pending) {  // routed FFN calls whose active experts were counted on the device
+        unsigned long long sum = 0;
+        MOE_TRY_CUDA(cudaMemcpy(&sum, st->ws + st->L.nact, 8, cudaMemcpyDeviceToHost));
+        MOE_TRY_CUDA(cudaMemset(st->ws + st->L.nact, 0, 8));
+        st->prof.gateup_bytes += (double)sum * 2 * moe_matrix_bytes(st->d.qtype, st->d.F, st->d.H);
+        st->prof.down_bytes += (double)sum * moe_matrix_bytes(st->d.qtype, st->d.H, st->d.F);
+        st->nact_pending = 0;
+    }
     for (auto &te : st->timed) {
         float ms = 0.f;
         MOE_TRY_CUDA(cudaEventElapsedTime(&ms, te.second.a, te.second.b));
@@ -161,9 +178,14 @@ int ffn_call(moe_stack *st, const float *x, int T, int E, int k, const int32_t *
         st->prof.gateup_launches++;
         st->prof.down_launches++;
     }
-    if (d.profile >= 1 && n_active >= 0) {  // n_active < 0: not known on the host
+    if (d.profile >= 1 && n_active >= 0) {
         st->prof.gateup_bytes += (double)n_active * 2 * moe_matrix_bytes(d.qtype, d.F, d.H);
         st->prof.down_bytes += (double)n_active * moe_matrix_bytes(d.qtype, d.H, d.F);
+    } else if (d.profile >= 1) {  // not known on the host: count on the device (after the GEMVs)
+        nact_add_kernel<<<1, 32, 0, s>>>((const int32_t *)(st->ws + st->L.ffn),
+                                         (unsigned long long *)(st->ws + st->L.nact));
+        MOE_TRY_CUDA(cudaGetLastError());
+        ++st->nact_pending;
     }
     return MOE_OK;
 }
@@ -262,18 +284,7 @@ int layer_step(moe_stack *st, int layer, const float *h, float *y, int T, int32_
         if ((rc = moe_cache_release(c, (moe_stream_t)s))) return rc;
     } else {
         const void *pool = (const char *)d.resident_pool + (size_t)layer * d.E * d.slot_bytes;
-        int n_active = d.E < T * d.k ? d.E : T * d.k;
-        if (d.profile) {
-            // count the distinct experts for the byte accounting (profiling only)
-            MOE_TRY_CUDA(cudaMemcpyAsync(st->ids_h, ids_d, (size_t)T * d.k * 4, cudaMemcpyDeviceToHost, s));
-            MOE_TRY_CUDA(cudaStreamSynchronize(s));
-            bool want[MOE_MAX_E] = {false};
-            n_active = 0;
-            for (int i = 0; i < T * d.k; ++i)
-                if (!want[st->ids_h[i]]) { want[st->ids_h[i]] = true; ++n_active; }
-        }
-        if ((rc = ffn_call(st, x, T, d.E, d.k, ids_d, w_d, nullptr, d.E, pool, nullptr, 0, partial,
-                           n_active, s)))
+        if ((rc = ffn_call(st, x, T, d.E, d.k, ids_d, w_d, nullptr, d.E, pool, nullptr, 0, partial, -1, s)))
             return rc;
     }
 
@@ -361,7 +372,8 @@ extern "C" int moe_stack_create(const moe_stack_desc *desc, moe_stack **out) {
                 delete st;
                 return MOE_ERR_INVALID;  // every layer must belong to a group
             }
-    if (cudaHostAlloc(&st->ids_h, (size_t)d.max_T * d.k * 4, cudaHostAllocDefault) != cudaSuccess ||
+    if (cudaMemset(st->ws + st->L.nact, 0, 8) != cudaSuccess ||
+        cudaHostAlloc(&st->ids_h, (size_t)d.max_T * d.k * 4, cudaHostAllocDefault) != cudaSuccess ||
         cudaHostAlloc(&st->slots_h, (size_t)d.max_T * d.k * 4, cudaHostAllocDefault) != cudaSuccess ||
         cudaEventCreateWithFlags(&st->ids_ready, cudaEventDisableTiming) != cudaSuccess) {
         moe_stack_destroy(st);
@@ -487,6 +499,8 @@ extern "C" int moe_stack_profile_reset(moe_stack *st) {
     st->timed.clear();
     st->ev_used = 0;
     st->prof = moe_stack_profile{};
+    st->nact_pending = 0;
+    MOE_TRY_CUDA(cudaMemset(st->ws + st->L.nact, 0, 8));
     return MOE_OK;
 }
 

@@ -203,6 +203,33 @@ def time_steps(stack, xs, T, steps, warmup, torch, stream):
     return ms, prof, d
 
 
+def gemv_roofline(cfg, T, torch, stream, steps=40, warmup=5):
+    """The decode GEMV kernels on HBM-resident weights: every layer's experts resident (24 x 32
+    images, 1.28 GB, far above L2), eager launches queued behind a GPU spacer so that no kernel
+    waits for its launch, events around each gate/up and down launch.  Bytes per launch are the
+    active experts' quantised blocks, counted on the device."""
+    from routed_expert_ffn_gemv_gb300 import synth
+    from routed_expert_ffn_gemv_gb300.workload import Stack
+    st = Stack(cfg, max_T=T, resident=True, profile=2)
+    xs = [torch.from_numpy(synth.tokens_x(cfg, 500 + s, T)).cuda() for s in range(16)]
+    y = torch.empty((T, cfg.H), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            st.decode(xs[i % len(xs)], y, stream=stream)
+        stream.synchronize()
+        st.profile_reset()
+        torch.cuda._sleep(4_000_000)  # ~2 ms of GPU time while the host queues the steps
+        for i in range(steps):
+            st.decode(xs[(warmup + i) % len(xs)], y, stream=stream)
+        stream.synchronize()
+    prof = st.profile()
+    st.close()
+    gl, dl = max(1, prof["gateup_launches"]), max(1, prof["down_launches"])
+    return {"gateup_ms_per_launch": prof["gateup_ms"] / gl, "gateup_bytes_per_launch": prof["gateup_bytes"] / gl,
+            "down_ms_per_launch": prof["down_ms"] / dl, "down_bytes_per_launch": prof["down_bytes"] / dl,
+            "launches": int(prof["gateup_launches"]), "steps": steps}
+
+
 def max_over_ranks(v, world, torch):
     if world <= 1:
         return v
@@ -393,18 +420,23 @@ def run_gpu(args, world, rank, local):
 
     ms, prof, st, steps = main
     r = results[args.batch]
-    gu_launches = max(1, hprof["gateup_launches"])
-    gu_ms_launch = hprof["gateup_ms"] / gu_launches
-    gu_bytes_launch = hprof["gateup_bytes"] / gu_launches
+    gv = gemv_roofline(cfg, T, torch, stream)
+    gu_ms_launch, gu_bytes_launch = gv["gateup_ms_per_launch"], gv["gateup_bytes_per_launch"]
     achieved = gu_bytes_launch / (gu_ms_launch / 1e3) / 1e9 if gu_ms_launch > 0 else 0.0
+    dn_gbs = gv["down_bytes_per_launch"] / (gv["down_ms_per_launch"] / 1e3) / 1e9 if gv["down_ms_per_launch"] else 0.0
     tr = traffic_record(f"gateup_q8_0_h{cfg.H}_t{T}")
-    roofline = {"kernel": "gateup_kernel<q8_0> (dequantising gate/up GEMV)", "bound": "hbm",
+    roofline = {"kernel": "ffn_ring_kernel<q8_0, gate/up> (dequantising gate/up GEMV + SwiGLU)", "bound": "hbm",
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
                 "traffic": None if tr is None else tr["bytes_per_launch"],
                 "algorithmic_bytes_per_launch": gu_bytes_launch, "ms_per_launch": gu_ms_launch,
-                "launches": hprof["gateup_launches"],
-                "measured_in": "host-managed pool loop, batch %d (every GEMV byte read from HBM)" % T}
+                "launches": gv["launches"],
+                "down_kernel": {"achieved_gbs": dn_gbs, "frac": dn_gbs / peaks["hbm_gbs"],
+                                "ms_per_launch": gv["down_ms_per_launch"],
+                                "algorithmic_bytes_per_launch": gv["down_bytes_per_launch"]},
+                "measured_in": ("HBM-resident stack (all %d x %d expert images in HBM, above L2), batch %d, "
+                                "launches queued behind a GPU spacer, CUDA events on the launching stream"
+                                % (cfg.L, cfg.E, T))}
     if rank == 0:
         cb = cpu_baseline(cfg, T) if world == 1 else None
         line = {"metric": METRIC, "value": r["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
@@ -439,9 +471,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--lite", action="store_true",
                     help="only the device-managed timed loop at --batch (the ncu target)")
-    ap.add_argument("--only", choices=["host", "prefill"], default=None,
-                    help="profiling targets: 'host' = host-managed pool loop at --batch (every GEMV "
-                         "byte from HBM), 'prefill' = the prefill layer at 512 and 4096 tokens")
+    ap.add_argument("--only", choices=["host", "gemv", "prefill"], default=None,
+                    help="profiling targets: 'host' = host-managed pool loop at --batch, 'gemv' = the "
+                         "decode GEMVs on an HBM-resident stack at --batch, 'prefill' = the prefill "
+                         "layer at 512 and 4096 tokens")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup()
@@ -466,6 +499,13 @@ def run_only(args):
         return 0
     cfg = synth.config(CONFIG_INDEX)
     T = args.batch
+    if args.only == "gemv":
+        gv = gemv_roofline(cfg, T, torch, torch.cuda.Stream(), steps=args.steps, warmup=args.warmup)
+        gv.update({"only": "gemv", "batch": T,
+                   "gateup_gbs": gv["gateup_bytes_per_launch"] / (gv["gateup_ms_per_launch"] / 1e3) / 1e9,
+                   "down_gbs": gv["down_bytes_per_launch"] / (gv["down_ms_per_launch"] / 1e3) / 1e9})
+        print(json.dumps(gv), flush=True)
+        return 0
     stack = Stack(cfg, max_T=T, profile=1)
     xs = [torch.from_numpy(synth.tokens_x(cfg, 3 + s, T)).cuda() for s in range(16)]
     ms, prof, st = time_steps(stack, xs, T, args.steps, args.warmup, torch, torch.cuda.Stream())

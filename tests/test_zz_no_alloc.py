@@ -64,11 +64,13 @@ def test_noalloc_matches_workspace_entry_point_twice(qtype, H, F, E, k, T):
 
 
 def test_noalloc_rejects_requests_beyond_its_array():
-    # batch 32, top-8 of the DeepSeek-shaped layer needs ~11.5 MB of scratch > 8 MiB
-    need = L.moe_expert_ffn_workspace(32, 2048, 1408, 0, 0, 64, 8)
+    # batch 32, top-8 of a layer with hidden 4096 and FFN 14336 (q8_0): its gate/up partial
+    # sums alone need far more scratch than 8 MiB
+    need = L.moe_expert_ffn_workspace(32, 4096, 14336, 0, 0, 64, 8)
     assert need > L.MOE_NOALLOC_SCRATCH_MAX
     dummy = torch.zeros(16, dtype=torch.float32, device="cuda")
+    slot = (L.moe_slot_image_bytes(0, 4096, 14336) + 255) // 256 * 256
     with pytest.raises(L.MoeError) as ei:
-        L.moe_expert_ffn_noalloc(dummy, 0, 32, 2048, 1408, 0, 64, 8, dummy, dummy, None, 64, dummy, 9191424,
+        L.moe_expert_ffn_noalloc(dummy, 0, 32, 4096, 14336, 0, 64, 8, dummy, dummy, None, 64, dummy, slot,
                                  None, 0, dummy)
     assert ei.value.status == L.MOE_ERR_UNSUPPORTED

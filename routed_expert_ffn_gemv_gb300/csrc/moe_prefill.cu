@@ -144,10 +144,22 @@ __global__ void __launch_bounds__(1024) pf_route_kernel(const int32_t *__restric
             else moe_set_status(status, MOE_ERR_INVALID);
         }
     __syncthreads();
-    for (int r = tid; r < R; r += blockDim.x) {
-        const int e = ids[r];
-        if (e < 0 || e >= E) { moe_set_status(status, MOE_ERR_INVALID); continue; }
-        if (insub[e]) atomicAdd(&cnt[e], 1);
+    // ids are read RB per thread at a time so that the loads overlap
+    constexpr int RB = 8;
+    for (int r0 = 0; r0 < R; r0 += RB * (int)blockDim.x) {
+        int e8[RB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+            const int r = r0 + i * blockDim.x + tid;
+            e8[i] = r < R ? ids[r] : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+            if (r0 + i * (int)blockDim.x + tid >= R) continue;
+            const int e = e8[i];
+            if (e < 0 || e >= E) { moe_set_status(status, MOE_ERR_INVALID); continue; }
+            if (insub[e]) atomicAdd(&cnt[e], 1);
+        }
     }
     __syncthreads();
     if (tid == 0) {
@@ -175,11 +187,20 @@ __global__ void __launch_bounds__(1024) pf_route_kernel(const int32_t *__restric
         ints[o_tbase + e] = tb[e];
     }
     __syncthreads();
-    for (int r = tid; r < R; r += blockDim.x) {
-        const int e = ids[r];
-        if (e < 0 || e >= E || !insub[e]) continue;
-        const int i = atomicAdd(&cur[e], 1);
-        ints[o_troute + (size_t)(tb[e] + i / PF_TM) * PF_TM + (i % PF_TM)] = r;
+    for (int r0 = 0; r0 < R; r0 += RB * (int)blockDim.x) {
+        int e8[RB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+            const int r = r0 + i * blockDim.x + tid;
+            e8[i] = r < R ? ids[r] : -1;
+        }
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+            const int e = e8[i];  // -1 beyond R
+            if (e < 0 || e >= E || !insub[e]) continue;
+            const int j = atomicAdd(&cur[e], 1);
+            ints[o_troute + (size_t)(tb[e] + j / PF_TM) * PF_TM + (j % PF_TM)] = r0 + i * blockDim.x + tid;
+        }
     }
 }
 
@@ -189,12 +210,16 @@ template <int XT, bool Q4>
 __global__ void __launch_bounds__(256) pf_gather_kernel(const void *__restrict__ x, int H, int k,
                                                         const int32_t *__restrict__ ints, size_t o_troute,
                                                         uint8_t *__restrict__ xp) {
+    __shared__ int rt[PF_TM];
     const int tile = blockIdx.x;
     if (tile >= ints[0]) return;
+    for (int i = threadIdx.x; i < PF_TM; i += blockDim.x) rt[i] = ints[o_troute + (size_t)tile * PF_TM + i];
+    __syncthreads();
     const int NKC = H / PF_BK, C8 = H / 8;
+#pragma unroll 4
     for (int idx = threadIdx.x; idx < PF_TM * C8; idx += blockDim.x) {
         const int row = idx / C8, c8 = idx % C8;
-        const int r = ints[o_troute + (size_t)tile * PF_TM + row];
+        const int r = rt[row];
         uint4 v = make_uint4(0, 0, 0, 0);
         if (r >= 0) {
             const size_t base = (size_t)(r / k) * H + (size_t)c8 * 8;

@@ -219,13 +219,14 @@ router_topk_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__r
 
 // ------------------------------------------------------------------ many tokens (prefill)
 //
-// Above the decode batch limit the router is a small fp32 GEMM [T x H] . [H x E]: a CTA
-// owns 32 tokens and every expert and walks H in chunks of 32 rows, double-buffered in
-// shared memory (x duplicated into (v, v) pairs, W_r converted to fp32).  Thread (ty, tx)
-// keeps 4 tokens x EPT experts in registers and accumulates expert pairs with packed
-// fp32x2 FMAs, in ascending h per logit
-// within each chunk.  The logits then go through the same warp
-// selection as the cluster kernel.
+// Above the decode batch limit the router is a small fp32 GEMM [T x H] . [H x E]: a cluster
+// of up to 8 CTAs owns 32 tokens and every expert, each CTA walking its share of H in
+// chunks of 32 rows, double-buffered in shared memory (x duplicated into (v, v) pairs, W_r
+// converted to fp32).  Thread (ty, tx) keeps 4 tokens x EPT experts in registers and
+// accumulates expert pairs with packed fp32x2 FMAs, in ascending h per logit within each
+// chunk; chunk sums are added in order, the CTAs' partial logits are summed in rank order
+// over distributed shared memory, and each rank runs the warp selection of the cluster
+// kernel for its share of the tokens.
 
 #define RT_TT 32
 #define RT_KC 32
@@ -249,8 +250,11 @@ router_tiled_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__
     float *ws = (float *)(smem + 2 * (size_t)RT_KC * RT_XS * 8);       // [2][KC][EP]
     float *lg = ws;                                                    // [TT][EP] after the loop
     const int tid = threadIdx.x, tx = tid % 32, ty = tid / 32;
-    const int t0 = blockIdx.x * RT_TT;
+    // a cluster of C CTAs shares a 32-token tile; rank r sums chunks [c_lo, c_hi) of W_r
+    const int C = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
+    const int t0 = (blockIdx.x / C) * RT_TT;
     const int NC = H / RT_KC;
+    const int c_lo = rank * NC / C, c_hi = (rank + 1) * NC / C;
     const int wn = RT_KC * E;                   // halfs per W_r chunk (contiguous rows)
     const int wv = wn / 8;                      // 16-byte vectors per chunk
 
@@ -316,12 +320,12 @@ router_tiled_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__
 #pragma unroll
         for (int p = 0; p < EPT / 2; ++p) acc[t][p] = 0ull;
 
-    load(0);
+    if (c_lo < c_hi) load(c_lo);
     __syncthreads();  // zero fill of the padding columns before the first store
-    store(0);
+    if (c_lo < c_hi) store(c_lo & 1);
     __syncthreads();
-    for (int c = 0; c < NC; ++c) {
-        if (c + 1 < NC) load(c + 1);
+    for (int c = c_lo; c < c_hi; ++c) {
+        if (c + 1 < c_hi) load(c + 1);
         // each chunk's 32 products are summed on their own, then added to the total (keeps
         // the rounding error of a 2048-term logit near 1e-6)
         unsigned long long part[4][EPT / 2];
@@ -352,10 +356,10 @@ router_tiled_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__
         for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int p = 0; p < EPT / 2; ++p) acc[t][p] = f2_add(acc[t][p], part[t][p]);
-        if (c + 1 < NC) store((c + 1) & 1);
+        if (c + 1 < c_hi) store((c + 1) & 1);
         __syncthreads();
     }
-    // logits (+ bias) -> shared memory (the W_r buffers are free after the last barrier)
+    // this rank's partial logits -> shared memory (the W_r buffers are free after the last barrier)
 #pragma unroll
     for (int t = 0; t < 4; ++t)
 #pragma unroll
@@ -365,25 +369,29 @@ router_tiled_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__
                 float a, b;
                 f2_unpack(acc[t][2 * q + p], a, b);
                 const int e = 128 * q + 4 * tx + 2 * p;
-                lg[(size_t)(4 * ty + t) * EP + e] = a + (bias && e < E ? bias[e] : 0.f);
-                lg[(size_t)(4 * ty + t) * EP + e + 1] = b + (bias && e + 1 < E ? bias[e + 1] : 0.f);
+                lg[(size_t)(4 * ty + t) * EP + e] = a;
+                lg[(size_t)(4 * ty + t) * EP + e + 1] = b;
             }
-    __syncthreads();
+    cluster_sync_all();  // every rank's partial logits are complete and visible
+    // rank r selects tokens r, r + C, ...: the partials summed in rank order, then the bias
     const int warp = ty, lane = tx;
-    for (int t = warp; t < RT_TT && t0 + t < T; t += MOE_ROUTER_THREADS / 32) {
+    for (int t = rank + C * warp; t < RT_TT && t0 + t < T; t += C * (MOE_ROUTER_THREADS / 32)) {
         float v[MOE_MAX_E / 32];
 #pragma unroll
         for (int i = 0; i < MOE_MAX_E / 32; ++i) {
             const int e = lane + 32 * i;
             v[i] = -INFINITY;
             if (e < E) {
-                const float s = lg[(size_t)t * EP + e];
+                float s = 0.f;
+                for (int r = 0; r < C; ++r) s += ld_cluster_f32(cluster_map(&lg[(size_t)t * EP + e], r));
+                if (bias) s += bias[e];
                 if (logits_out) logits_out[(size_t)(t0 + t) * E + e] = s;
                 v[i] = (s != s) ? -INFINITY : s;  // NaN never wins
             }
         }
         select_topk_softmax(v, E, k, lane, (size_t)(t0 + t), ids, weights);
     }
+    cluster_sync_all();  // the other ranks have finished reading this CTA's shared memory
 }
 
 }  // namespace
@@ -396,9 +404,23 @@ int router_tiled_launch_t(const void *x, int T, int H, const uint16_t *w_router,
     const size_t smem = router_tiled_smem(32 * EPT);
     MOE_TRY_CUDA(cudaFuncSetAttribute(router_tiled_kernel<XT, EPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem));
-    router_tiled_kernel<XT, EPT><<<(T + RT_TT - 1) / RT_TT, MOE_ROUTER_THREADS, smem, st>>>(
-        x, T, H, w_router, bias, E, k, ids, weights, logits);
-    MOE_TRY_CUDA(cudaGetLastError());
+    const int NC = H / RT_KC;
+    int C = 1;  // CTAs per cluster splitting H (each keeps at least one chunk)
+    while (2 * C <= MOE_ROUTER_CLUSTER && 2 * C <= NC) C *= 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C * ((T + RT_TT - 1) / RT_TT), 1, 1);
+    cfg.blockDim = dim3(MOE_ROUTER_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, router_tiled_kernel<XT, EPT>, x, T, H, w_router, bias, E, k, ids, weights,
+                                    logits));
     return MOE_OK;
 }
 

@@ -7,24 +7,27 @@
 // their quantised blocks (page 5, section 1.2) and are dequantised in registers.
 //
 // GB300 mapping (the decode GEMVs stream the selected experts' bytes from HBM once):
-//  * work unit = two 32-row tiles over a K range whose bytes are one contiguous run per
-//    tile and region in the slot image: the gate and the up tile of the same rows (G1), or
-//    two neighbouring down tiles (G2);
-//  * persistent CTAs of 16 warps, one per SM: each walks a contiguous, work-balanced range
-//    of units (precomputed by the permute kernel) through a ring of shared-memory stages;
-//    thread 0 keeps the next units' bulk copies (TMA engine, cp.async.bulk) in flight
-//    while the current one is computed;
-//  * lane l of every warp owns row l of both tiles and keeps its dot products in registers
-//    (no cross-lane reduction); each activation value read from shared memory (a warp
-//    broadcast) feeds both rows; the 16 warps split the K range and are reduced in shared
-//    memory in a fixed order;
-//  * codes become fp32 with exponent tricks (no int->float conversions), accumulate with
-//    packed fp32x2 FMAs, and block scales are applied once per 32 weights;
-//  * the warp that reduces a token's gate and up rows applies SwiGLU and writes h; when the
-//    K range is split (large H), the partial sums go to the workspace and the down kernel
-//    sums them in a fixed order while it stages its activations;
+//  * the routes of an expert are cut into groups of at most 8 tokens ("virtual experts");
+//    a work unit is NTL 32-row tiles of one virtual expert over a K range: the gate and the
+//    up tile of the same rows (G1), or one or two neighbouring down tiles (G2);
+//  * persistent CTAs of 16 warps, one per SM, each over a contiguous, work-balanced range of
+//    units (precomputed by the permute kernel).  The warps of a CTA take its units in turn
+//    and are independent: each has its own ring of shared-memory stages, fed by its lane 0
+//    with bulk copies (TMA engine, cp.async.bulk) a few chunks ahead, and waits on its own
+//    mbarriers.  There is no block-wide barrier while weights stream;
+//  * a warp owns whole rows of its unit and needs no reduction with other warps: the codes
+//    of a 32-column block are turned into fp16 (exact small integers) in registers, laid
+//    out directly as the A fragments of mma.sync m16n8k16 (rows = weight rows, columns =
+//    tokens, fp32 accumulation), and the block's fp32 scale is applied to the block's
+//    partial sums in fp32, so the per-block arithmetic is exact except for the activations;
+//  * activations enter the tensor core as fp16 hi + lo parts of a per-token power-of-two
+//    scaled copy (about 22 significant bits), staged once per (virtual expert, K range) in
+//    shared memory for all warps of the CTA;
+//  * the warp's epilogue forms h = silu(gate) * up (G1, whole K), stores the two partial
+//    sums (G1, K split; the down kernel sums them in a fixed order while staging), or writes
+//    w[r] * (Wd h) for each route r (G2);
 //  * an expert that missed in a device-managed pool is read from its pinned host image and
-//    written through to its slot by the unit that uses the bytes ("fill" units).
+//    written through to its slot by the warps that use the bytes ("fill" units).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
@@ -36,104 +39,102 @@
 
 #define GV_WARPS 16
 #define GV_THREADS (GV_WARPS * 32)
-#define GV_TOK 8                  // tokens per pass (one per reducing warp)
-#define GV_SMEM_MAX (220 * 1024)  // dynamic shared memory a ring kernel may take
-#define GV_FILL_BATCH 4           // 16-byte pieces per thread loaded together by a fill unit
-#define GV_ICACHE 64              // active experts of a CTA's range kept in shared memory
-#define GV_RCACHE 512             // routes (and router weights) of a CTA's range in shared memory
+#define GV_TOK 8                  // tokens of a virtual expert
+#define GV_SMEM_MAX (220 * 1024)  // dynamic shared memory a GEMV kernel may take
+#define GV_BARS 1024              // mbarrier area: GV_WARPS x GV_MAX_STAGES
+#define GV_MAX_STAGES 8           // ring stages of one warp
+#define GV_MIN_STAGES 2
+#define GV_CHUNK_TARGET 5120      // bytes of one ring stage (a chunk of a unit)
+#define GV_FILL_BATCH 8           // 16-byte pieces per lane loaded together by a fill chunk
 #define GV_MAX_GRID 1024          // CTAs per launch (bounds the precomputed range tables)
+#define GV_UNITS_TARGET 1824      // units per launch the K split aims for (~12 per CTA)
+#define GV_KS_MAX 8               // largest K split of the gate/up GEMV
+#define GV_ACT_SLOTS_MAX 3        // staged (virtual expert, K range) pairs per CTA phase
+#define GV_PHASE_PAIRS 64         // pairs (used or skipped) per CTA phase
 
 namespace {
 
-// Work of one unit of an expert with n_e tokens, in units of a token's dot products: the
-// unit's bytes and dequantisation cost about as much as GV_COST_MEM tokens.
+// Work of one unit of a virtual expert with n_e tokens, in units of a token's dot products:
+// the unit's bytes and dequantisation cost about as much as GV_COST_MEM tokens.
 #define GV_COST_MEM 4
-__host__ __device__ inline int unit_cost(int n_e) { return n_e > 0 ? GV_COST_MEM + n_e : 1; }
+__host__ __device__ inline int unit_cost(int n_e) { return GV_COST_MEM + n_e; }
 
-// ------------------------------------------------------------------ shared-memory layout
+// ------------------------------------------------------------------ launch plan
 
-struct RingSmem {
-    size_t bars, stages, stage_bytes, tile_bytes, scale_off, act, asum, red, info, rts, wts, total;
+// Virtual experts hold at most NT8 routes (4 when T <= 4, else GV_TOK), so that a staged
+// activation slot of NT8 token rows always suffices.
+// Per kernel: NTL tiles per unit, nbr 32-column blocks per unit (the K range), CB blocks per
+// chunk (one ring stage), the staged activation slot of one (virtual expert, K range) pair
+// and how many of those a CTA phase holds, and the ring bytes left for the warps.
+struct GvGeom {
+    int NTL, nbr, CB, chunk_bytes, slot_bytes, act_slots, ring_bytes;
 };
 
-// nbr blocks of 32 columns per tile, `tiles` tiles per unit, ntok staged token rows, S stages.
-__host__ __device__ inline RingSmem ring_smem(int qtype, int nbr, int tiles, int ntok, int S) {
-    RingSmem L;
-    const int QB = qtype == MOE_Q8_0 ? 1024 : 512;       // code bytes per block of a 32-row tile
-    const int SB = 32 * moe_scale_entry_bytes(qtype);    // scale bytes per block of a tile
-    L.scale_off = (size_t)nbr * QB;
-    L.tile_bytes = L.scale_off + ((size_t)nbr * SB + 127) / 128 * 128;
-    L.stage_bytes = (size_t)tiles * L.tile_bytes;
-    size_t off = 0;
-    L.bars = off;   off += 128;
-    L.stages = off; off += (size_t)S * L.stage_bytes;
-    L.act = off;    off += (size_t)ntok * nbr * 32 * 4;
-    L.asum = off;   off += ((size_t)ntok * nbr * 4 + 15) / 16 * 16;
-    L.red = off;    off += (size_t)GV_WARPS * ntok * 2 * 32 * 4;
-    L.info = off;   off += (size_t)GV_ICACHE * 32;
-    L.rts = off;    off += (size_t)GV_RCACHE * 4;
-    L.wts = off;    off += (size_t)GV_RCACHE * 4;
-    L.total = off;
-    return L;
+struct GvPlan {
+    int KS, TPU, NT8;
+    GvGeom g1, g2;
+};
+
+__host__ __device__ inline int gv_qb(int qtype) { return qtype == MOE_Q8_0 ? 1024 : 512; }  // codes / block / tile
+__host__ __device__ inline int gv_sb(int qtype) { return 32 * moe_scale_entry_bytes(qtype); }
+
+// Row stride of the staged fp16 activations (bytes): 2 Kr + 32 keeps 16-byte alignment
+// and spreads the 8 rows of a B-fragment load over the banks.
+__host__ __device__ inline int gv_row_stride(int Kr) { return 2 * Kr + 32; }
+
+// One pair's slot: 2*NT8 fp16 rows (hi, lo per token), 8 inverse token scales, and for the
+// 4-bit format the per-block activation sums [nbr][8].
+__host__ __device__ inline int gv_slot_bytes(int qtype, int nbr, int NT8) {
+    const int b = 2 * NT8 * gv_row_stride(nbr * 32) + 32 + (qtype == MOE_Q4_SM ? nbr * 32 : 0);
+    return (b + 127) / 128 * 128;
 }
 
-// Launch plan of one decode FFN: the gate/up K split and ring depth, the down tiles per unit
-// and ring depth, chosen so that each kernel's shared memory fits.
-struct GvPlan {
-    int KS, S1, TPU, S2;
-};
+inline bool gv_geom(int qtype, int NTL, int nbr, int NT8, GvGeom *g) {
+    g->NTL = NTL;
+    g->nbr = nbr;
+    const int per_block = NTL * (gv_qb(qtype) + gv_sb(qtype));
+    g->CB = std::max(1, std::min(nbr, GV_CHUNK_TARGET / per_block));
+    g->chunk_bytes = g->CB * per_block;
+    g->slot_bytes = gv_slot_bytes(qtype, nbr, NT8);
+    const int ring_min = GV_WARPS * GV_MIN_STAGES * g->chunk_bytes;
+    const int room = GV_SMEM_MAX - GV_BARS - ring_min;
+    if (room < g->slot_bytes) return false;
+    g->act_slots = std::min(GV_ACT_SLOTS_MAX, room / g->slot_bytes);
+    g->ring_bytes = GV_SMEM_MAX - GV_BARS - g->act_slots * g->slot_bytes;
+    return true;
+}
 
-// Units are made small enough that a launch has about GV_UNITS_TARGET of them (a CTA's share
-// is then several units and the work-balanced split is fine-grained), but no smaller than one
-// 32-column block per warp.
-#define GV_UNITS_TARGET 1024
+inline int gv_smem_bytes(const GvGeom &g) { return GV_BARS + g.ring_bytes + g.act_slots * g.slot_bytes; }
 
+// The gate/up K split is the smallest power of two giving about GV_UNITS_TARGET units (at
+// most GV_KS_MAX, each K range at least one block); the down kernel takes two row tiles per
+// unit when that still gives enough units.
 inline bool gv_plan(int T, int H, int F, int qtype, int n_act_max, GvPlan *pl) {
-    const int ntok = T < GV_TOK ? T : GV_TOK;
     const int NB = H / 32, RTF = F / 32, RTH = H / 32;
-    pl->KS = 0;
-    for (int ks = 1; ks <= NB && !pl->KS; ks *= 2) {
-        if (NB % ks) break;
-        const bool more = (long)n_act_max * ks * RTF < GV_UNITS_TARGET && NB % (2 * ks) == 0 &&
-                          NB / (2 * ks) >= GV_WARPS;
-        for (int S = 3; S >= 2 && !pl->KS; --S)
-            if (!more && ring_smem(qtype, NB / ks, 2, ntok, S).total <= GV_SMEM_MAX) {
-                pl->KS = ks;
-                pl->S1 = S;
-            }
-    }
-    if (!pl->KS) {  // a single stage of the smallest split
-        int ks = 1;
-        while (NB % (2 * ks) == 0 && ring_smem(qtype, NB / ks, 2, ntok, 1).total > GV_SMEM_MAX) ks *= 2;
-        if (ring_smem(qtype, NB / ks, 2, ntok, 1).total > GV_SMEM_MAX) return false;
-        pl->KS = ks;
-        pl->S1 = 1;
-    }
-    pl->TPU = 0;
-    const bool pairs = RTH % 2 == 0 && (long)n_act_max * (RTH / 2) >= GV_UNITS_TARGET;
-    const int cand[7][2] = {{2, 4}, {2, 3}, {2, 2}, {1, 4}, {1, 3}, {1, 2}, {1, 1}};
-    for (int i = 0; i < 7 && !pl->TPU; ++i) {
-        if (cand[i][0] == 2 && !pairs) continue;
-        if (ring_smem(qtype, F / 32, cand[i][0], ntok, cand[i][1]).total <= GV_SMEM_MAX) {
-            pl->TPU = cand[i][0];
-            pl->S2 = cand[i][1];
-        }
-    }
-    return pl->TPU != 0;
+    pl->NT8 = T <= 4 ? 4 : GV_TOK;
+    int ks = 1;
+    while (ks < GV_KS_MAX && (long)n_act_max * RTF * ks < GV_UNITS_TARGET && NB % (2 * ks) == 0) ks *= 2;
+    pl->KS = ks;
+    pl->TPU = RTH % 2 == 0 && (long)n_act_max * (RTH / 2) >= GV_UNITS_TARGET ? 2 : 1;
+    return gv_geom(qtype, 2, NB / ks, pl->NT8, &pl->g1) && gv_geom(qtype, pl->TPU, F / 32, pl->NT8, &pl->g2);
 }
 
 inline int gv_n_act_max(int T, int E, int k) { return T * k < E ? T * k : E; }
+inline int gv_vt(int T) { return T <= 4 ? 4 : GV_TOK; }
+// virtual experts: at most one per active expert plus one per further group of vt routes
+inline int gv_n_virt_max(int T, int E, int k) { return gv_n_act_max(T, E, k) + (T * k) / gv_vt(T) + 1; }
 
 // ------------------------------------------------------------------ workspace layout
 
-// Per active expert, written by the permute kernel.
+// Per virtual expert, written by the permute kernel.
 struct ActInfo {
     unsigned long long src;  // image base the weights are read from (slot, or pinned host image)
-    unsigned long long dst;  // slot base (written through when fill != 0)
-    int e, pos0, n_e, fill;  // n_e == 0: skip (invalid slot)
+    unsigned long long dst;  // slot base (written through when wt != 0)
+    int pos0, n_e;           // route positions [pos0, pos0 + n_e); n_e == 0: skip (invalid slot)
+    int fill, wt;            // fill: read src with loads (host image); wt: write the bytes to dst
 };
 
-// int32 region: [0] n_active | active [E] | a_off [E+1] | routes [R] | ranges1 | ranges2
+// int32 region: [0] n_active [1] n_virtual | active [E] | a_off [E+1] | routes [R] | ranges1 | ranges2
 __host__ __device__ inline int ws_active_off() { return 16; }
 __host__ __device__ inline int ws_aoff_off(int E) { return 16 + E; }
 __host__ __device__ inline int ws_routes_off(int E) { return 16 + 2 * E + 1; }
@@ -156,222 +157,12 @@ inline WsLayout ws_layout(int T, int H, int F, int qtype, int E, int k) {
     const size_t ints = 16 + 2 * (size_t)E + 1 + R + 2 * (GV_MAX_GRID + 1);
     L.ints_off = 0;
     L.info_off = (ints * 4 + 255) / 256 * 256;
-    L.gu_off = L.info_off + ((size_t)E * sizeof(ActInfo) + 255) / 256 * 256;
+    L.gu_off = L.info_off + ((size_t)gv_n_virt_max(T, E, k) * sizeof(ActInfo) + 255) / 256 * 256;
     const size_t gu = pl.KS > 1 ? (size_t)pl.KS * 2 * R * F * 4 : 0;
     L.h_off = L.gu_off + (gu + 255) / 256 * 256;
     const size_t hb = pl.KS > 1 ? 0 : R * F * 4;
     L.total = L.h_off + (hb + 255) / 256 * 256;
     return L;
-}
-
-__device__ __forceinline__ void warp_blocks(int nbr, int w, int &b0, int &b1) {
-    b0 = (w * nbr) / GV_WARPS;
-    b1 = ((w + 1) * nbr) / GV_WARPS;
-}
-
-// Bulk copies of one 32-row tile into a stage: rows [32g, 32g+32) of matrix `mat` [R][K],
-// blocks [kb0, kb0+nbr) — the codes and the scales are one contiguous run each.
-template <int QT>
-__device__ __forceinline__ void issue_tile(const uint8_t *mat, int R, int K, int g, int kb0, int nbr,
-                                           unsigned char *tile, size_t scale_off, uint64_t *bar) {
-    const int QB = QT == MOE_Q8_0 ? 1024 : 512;
-    const int SB = 32 * moe_scale_entry_bytes(QT);
-    const int PPB = QT == MOE_Q8_0 ? 2 : 1;  // 16-byte pieces per block
-    bulk_g2s(tile, mat + moe_piece_offset(QT, K, g, kb0 * PPB), (uint32_t)nbr * QB, bar);
-    bulk_g2s(tile + scale_off, mat + moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, g, kb0),
-             (uint32_t)nbr * SB, bar);
-}
-
-// Fill path of a tile whose expert missed: its bytes come from the expert's pinned host
-// image over the CPU-GPU link (16-byte loads by every thread, GV_FILL_BATCH in flight per
-// thread) and are written both to the stage and through to the expert's slot, so the slot
-// is filled by the kernels that use it.  Same byte ranges as issue_tile.
-template <int QT>
-__device__ void fill_tile(const uint8_t *src_mat, uint8_t *dst_mat, int R, int K, int g, int kb0, int nbr,
-                          unsigned char *tile, size_t scale_off) {
-    const int QB = QT == MOE_Q8_0 ? 1024 : 512;
-    const int SB = 32 * moe_scale_entry_bytes(QT);
-    const int PPB = QT == MOE_Q8_0 ? 2 : 1;
-    const size_t qoff = moe_piece_offset(QT, K, g, kb0 * PPB);
-    const size_t soff = moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, g, kb0);
-    const int nq = nbr * QB / 16, ns = nbr * SB / 16;
-    constexpr int NB = GV_FILL_BATCH;
-    for (int i0 = 0; i0 < nq + ns; i0 += NB * GV_THREADS) {
-        uint4 v[NB];
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const int i = i0 + b * GV_THREADS + threadIdx.x;
-            if (i < nq + ns) {
-                const size_t off = i < nq ? qoff + (size_t)i * 16 : soff + (size_t)(i - nq) * 16;
-                v[b] = __ldcs((const uint4 *)(src_mat + off));
-            }
-        }
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const int i = i0 + b * GV_THREADS + threadIdx.x;
-            if (i < nq + ns) {
-                const bool q = i < nq;
-                const size_t off = q ? qoff + (size_t)i * 16 : soff + (size_t)(i - nq) * 16;
-                *(uint4 *)(tile + (q ? (size_t)i * 16 : scale_off + (size_t)(i - nq) * 16)) = v[b];
-                __stcs((uint4 *)(dst_mat + off), v[b]);
-            }
-        }
-    }
-}
-
-// fp32 scale of column c of a 4-bit block in the activation copy: code j = c % 8 of a
-// word decodes to q * 16^j (j <= 4) or q * 16^(j-5) (j >= 5), so the activation is
-// pre-multiplied by the inverse power of two (exact).
-__device__ __forceinline__ float q4_act_scale(int c) {
-    const int j = c & 7;
-    const int e = j <= 4 ? j : j - 5;
-    return __int_as_float((127 - 4 * e) << 23);
-}
-
-__device__ __forceinline__ float q4_act_unscale(int c) {
-    const int j = c & 7;
-    const int e = j <= 4 ? j : j - 5;
-    return __int_as_float((127 + 4 * e) << 23);
-}
-
-// Decoded fp32 pairs of one 32-bit word of codes (q8_0: 4 codes -> 2 pairs; 4-bit: 8 codes
-// -> 4 pairs, code j scaled by 16^j or 16^(j-5)).
-template <int QT>
-__device__ __forceinline__ void decode_word(uint32_t w, unsigned long long (&p)[QT == MOE_Q8_0 ? 2 : 4]) {
-    if constexpr (QT == MOE_Q8_0) {
-        const unsigned long long MAG8 = f2_pack(-8388736.0f, -8388736.0f);  // 2^23 + 128
-        const uint32_t wx = w ^ 0x80808080u;  // int8 -> offset-128 bytes
-        const float v0 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7440));
-        const float v1 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7441));
-        const float v2 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7442));
-        const float v3 = __int_as_float(__byte_perm(wx, 0x4B000000u, 0x7443));
-        p[0] = f2_add(f2_pack(v0, v1), MAG8);
-        p[1] = f2_add(f2_pack(v2, v3), MAG8);
-    } else {
-        const unsigned long long MAG4 = f2_pack(-8388608.0f, -8388608.0f);  // 2^23
-        const uint32_t w5 = w >> 20;
-        const float v0 = __int_as_float((w & 0xFu) | 0x4B000000u);
-        const float v1 = __int_as_float((w & 0xF0u) | 0x4B000000u);
-        const float v2 = __int_as_float((w & 0xF00u) | 0x4B000000u);
-        const float v3 = __int_as_float((w & 0xF000u) | 0x4B000000u);
-        const float v4 = __int_as_float((w & 0xF0000u) | 0x4B000000u);
-        const float v5 = __int_as_float((w5 & 0xFu) | 0x4B000000u);
-        const float v6 = __int_as_float((w5 & 0xF0u) | 0x4B000000u);
-        const float v7 = __int_as_float((w5 & 0xF00u) | 0x4B000000u);
-        p[0] = f2_add(f2_pack(v0, v1), MAG4);
-        p[1] = f2_add(f2_pack(v2, v3), MAG4);
-        p[2] = f2_add(f2_pack(v4, v5), MAG4);
-        p[3] = f2_add(f2_pack(v6, v7), MAG4);
-    }
-}
-
-// One block b of the lane's row in NTL tiles against NT staged activation rows:
-// acc[i][t] += d_i * sum (+ m_i * asum for 4-bit).  Each activation vector read from
-// shared memory serves every tile.  act: [NT][Kr] fp32, asum: [NT][nbr].
-template <int QT, int NT, int NTL>
-__device__ __forceinline__ void block_dot(const unsigned char *tile0, const unsigned char *tile1, size_t scale_off,
-                                          const float *act, const float *asum, int Kr, int nbr, int b, int lane,
-                                          float (&acc)[2][GV_TOK]) {
-    constexpr int WPB = QT == MOE_Q8_0 ? 8 : 4;  // 32-bit code words per lane and block
-    constexpr int PPW = QT == MOE_Q8_0 ? 2 : 4;  // fp32 pairs per word
-    const unsigned char *tl[2] = {tile0, tile1};
-    uint32_t wd[NTL][WPB];
-    uint32_t sc[NTL];
-#pragma unroll
-    for (int i = 0; i < NTL; ++i) {
-        if constexpr (QT == MOE_Q8_0) {
-            const uint4 qa = *(const uint4 *)(tl[i] + ((size_t)(2 * b) * 32 + lane) * 16);
-            const uint4 qb = *(const uint4 *)(tl[i] + ((size_t)(2 * b + 1) * 32 + lane) * 16);
-            wd[i][0] = qa.x; wd[i][1] = qa.y; wd[i][2] = qa.z; wd[i][3] = qa.w;
-            wd[i][4] = qb.x; wd[i][5] = qb.y; wd[i][6] = qb.z; wd[i][7] = qb.w;
-            sc[i] = *(const unsigned short *)(tl[i] + scale_off + ((size_t)b * 32 + lane) * 2);
-        } else {
-            const uint4 q = *(const uint4 *)(tl[i] + ((size_t)b * 32 + lane) * 16);
-            wd[i][0] = q.x; wd[i][1] = q.y; wd[i][2] = q.z; wd[i][3] = q.w;
-            sc[i] = *(const uint32_t *)(tl[i] + scale_off + ((size_t)b * 32 + lane) * 4);
-        }
-    }
-    unsigned long long inner[NTL][NT];
-#pragma unroll
-    for (int i = 0; i < NTL; ++i)
-#pragma unroll
-        for (int t = 0; t < NT; ++t) inner[i][t] = 0ull;
-#pragma unroll
-    for (int wi = 0; wi < WPB; ++wi) {
-        unsigned long long pr[NTL][PPW];
-#pragma unroll
-        for (int i = 0; i < NTL; ++i) decode_word<QT>(wd[i][wi], pr[i]);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const float *ap = act + (size_t)t * Kr + b * 32 + 2 * PPW * wi;
-            const float4 xa = *(const float4 *)ap;
-            const unsigned long long x01 = f2_pack(xa.x, xa.y), x23 = f2_pack(xa.z, xa.w);
-            unsigned long long x45 = 0ull, x67 = 0ull;
-            if constexpr (PPW == 4) {
-                const float4 xb = *(const float4 *)(ap + 4);
-                x45 = f2_pack(xb.x, xb.y);
-                x67 = f2_pack(xb.z, xb.w);
-            }
-#pragma unroll
-            for (int i = 0; i < NTL; ++i) {
-                inner[i][t] = f2_fma(pr[i][0], x01, inner[i][t]);
-                inner[i][t] = f2_fma(pr[i][1], x23, inner[i][t]);
-                if constexpr (PPW == 4) {
-                    inner[i][t] = f2_fma(pr[i][2], x45, inner[i][t]);
-                    inner[i][t] = f2_fma(pr[i][3], x67, inner[i][t]);
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < NTL; ++i) {
-        const float d = __half2float(__ushort_as_half((unsigned short)(sc[i] & 0xFFFFu)));
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            float lo, hi;
-            f2_unpack(inner[i][t], lo, hi);
-            if constexpr (QT == MOE_Q8_0) {
-                acc[i][t] = fmaf(d, lo + hi, acc[i][t]);
-            } else {
-                const float m = __half2float(__ushort_as_half((unsigned short)(sc[i] >> 16)));
-                acc[i][t] = fmaf(d, lo + hi, fmaf(m, asum[(size_t)t * nbr + b], acc[i][t]));
-            }
-        }
-    }
-}
-
-template <int QT, int NTL>
-__device__ __forceinline__ void tile_dot_dispatch(int nt, const unsigned char *tile0, const unsigned char *tile1,
-                                                  size_t scale_off, const float *act, const float *asum, int Kr,
-                                                  int nbr, int b0, int b1, int lane, float (&acc)[2][GV_TOK]) {
-#define GV_DOT(N)                                                                                    \
-    for (int b = b0; b < b1; ++b)                                                                    \
-        block_dot<QT, N, NTL>(tile0, tile1, scale_off, act, asum, Kr, nbr, b, lane, acc);           \
-    break;
-    switch (nt) {
-        case 1: GV_DOT(1)
-        case 2: GV_DOT(2)
-        case 3: GV_DOT(3)
-        case 4: GV_DOT(4)
-        case 5: GV_DOT(5)
-        case 6: GV_DOT(6)
-        case 7: GV_DOT(7)
-        default: GV_DOT(8)
-    }
-#undef GV_DOT
-}
-
-// Block sums of the (unscaled) activations for the 4-bit min term.
-template <int QT>
-__device__ __forceinline__ void compute_asum(const float *act, float *asum, int nt, int nbr, int Kr) {
-    if constexpr (QT == MOE_Q4_SM) {
-        for (int i = threadIdx.x; i < nt * nbr; i += GV_THREADS) {
-            const int t = i / nbr, b = i % nbr;
-            float s = 0.f;
-            for (int c = 0; c < 32; ++c) s += act[(size_t)t * Kr + b * 32 + c] * q4_act_unscale(c);
-            asum[i] = s;
-        }
-    }
 }
 
 struct FfnParams {
@@ -385,8 +176,8 @@ struct FfnParams {
     float *h;
     float *partial;
     int *status;
-    int stages;        // ring stages of this launch
-    int x_vec;         // x is 16-byte aligned: vector loads
+    int x_vec;              // x is 16-byte aligned: vector loads
+    GvGeom geo;             // this launch's geometry
 };
 
 __device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
@@ -395,280 +186,579 @@ __device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
-// Stage the activations of route positions [pos, pos+nt) for columns [c0, c0+Kr): gate/up
-// reads x (fp32 or bf16) of the routes' tokens (route of position pos+t at rbase[rpos+t]);
-// down reads h, or forms silu(sum gate) * (sum up) from the K-split partial sums.
-template <int QT, int XT, bool DOWN>
-__device__ __forceinline__ void load_act(const FfnParams &p, const int *rbase, int rpos, int pos, int nt, int c0,
-                                         int Kr, float *act) {
-    const int nq = Kr / 4;
-    for (int idx = threadIdx.x; idx < nt * nq; idx += GV_THREADS) {
-        const int t = idx / nq, c = 4 * (idx - t * nq);
-        float4 v;
-        if (DOWN) {
-            const size_t q = (size_t)(pos + t) * p.F + c;
-            if (p.KS == 1) {
-                v = *(const float4 *)(p.h + q);
-            } else {
-                float4 gs = make_float4(0.f, 0.f, 0.f, 0.f), us = gs;
-                for (int ks = 0; ks < p.KS; ++ks) {  // fixed order over the K ranges
-                    const float4 gv = *(const float4 *)(p.gu + ((size_t)ks * 2 + 0) * p.RT * p.F + q);
-                    const float4 uv = *(const float4 *)(p.gu + ((size_t)ks * 2 + 1) * p.RT * p.F + q);
-                    gs.x += gv.x; gs.y += gv.y; gs.z += gv.z; gs.w += gv.w;
-                    us.x += uv.x; us.y += uv.y; us.z += uv.z; us.w += uv.w;
-                }
-                v = make_float4(silu_mul(gs.x, us.x), silu_mul(gs.y, us.y), silu_mul(gs.z, us.z),
-                                silu_mul(gs.w, us.w));
-            }
-        } else {
-            const size_t off = (size_t)(rbase[rpos + t] / p.k) * p.H + c0 + c;
-            if (XT == MOE_BF16) {
-                const __nv_bfloat16 *xb = (const __nv_bfloat16 *)p.x + off;
-                if (p.x_vec) {
-                    const uint2 r = *(const uint2 *)xb;
-                    const float2 lo = __bfloat1622float2(*(const __nv_bfloat162 *)&r.x);
-                    const float2 hi = __bfloat1622float2(*(const __nv_bfloat162 *)&r.y);
-                    v = make_float4(lo.x, lo.y, hi.x, hi.y);
+// ------------------------------------------------------------------ fp16 fragments
+
+// d = A B + c for one m16n8k16 tile: A 16x16 fp16 (row-major fragments), B 16x8 fp16, fp32
+// accumulation.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1, const float (&c)[4]) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Two int8 codes of the offset-128 word t (bytes chosen by sel) as an fp16 pair of exact
+// integers: the byte under an 0x64 high byte reads 1024 + (q + 128); subtracting 1152
+// leaves q.
+__device__ __forceinline__ uint32_t q8_pair(uint32_t t, uint32_t sel) {
+    return hsub2_u(__byte_perm(t, 0x64646464u, sel), 0x64806480u);
+}
+
+// 4-bit codes of a word (nibble j = column j of its 8): nibbles 0 and 4 as an fp16 pair
+// (1024 + q, minus 1024), and nibbles 1 and 5 ((1024 + 16 q) / 16 - 64).  The word shifted
+// right by 8 gives nibbles 2, 6 and 3, 7 the same way.
+__device__ __forceinline__ uint32_t q4_even(uint32_t w) {
+    return hsub2_u((w & 0x000F000Fu) | 0x64006400u, 0x64006400u);
+}
+__device__ __forceinline__ uint32_t q4_odd(uint32_t w) {
+    return hfma2_u((w & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD400D400u);
+}
+
+// ------------------------------------------------------------------ one chunk of a unit
+//
+// Fragment layout.  Lane (r = lane/4, c = lane%4) holds, for the 16-row group hr of a tile,
+// rows 16 hr + r and 16 hr + r + 8, and for a 32-column block the columns 8c .. 8c+7: the
+// first k16 step of the block takes columns 8c+{0,1} (as k = 2c+{0,1}) and 8c+{2,3} (as
+// k = 2c+8+{0,1}), the second step 8c+{4,5} and 8c+{6,7} (4-bit: the pairs (0,4), (1,5)
+// and (2,6), (3,7) of the 8, which is why the staged 4-bit activations are permuted the
+// same way within each group of 8).  The B fragment of a lane is then the 16 bytes of fp16
+// activations at columns 8c .. 8c+7 of its B row, one shared-memory load per block.
+// B rows: with one column set (NS = 1) column n is token n%4, hi (n < 4) or lo; with two
+// sets, set 0 is the hi and set 1 the lo part of tokens 0..7.
+
+// acc[i][hr][s][j]: tile i, row 16 hr + r (+ 8 for j >= 2), column 2c + (j & 1) of set s.
+template <int QT, int NTL, int NS>
+__device__ __forceinline__ void chunk_dot(const unsigned char *st, int tb, int CB, int cb, const unsigned char *act,
+                                          int RS, const float *asum, int lane, float (&acc)[NTL][2][2][4]) {
+    constexpr int QB = QT == MOE_Q8_0 ? 1024 : 512;
+    const int r = lane >> 2, c = lane & 3;
+    const unsigned char *brow[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+        const int row = NS == 1 ? 2 * (r & 3) + (r >> 2) : 2 * r + s;
+        brow[s] = act + (size_t)row * RS + 16 * c;
+    }
+    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int b = 0; b < cb; ++b) {
+        uint4 bf[NS];
+#pragma unroll
+        for (int s = 0; s < NS; ++s) bf[s] = *(const uint4 *)(brow[s] + 64 * b);
+        float2 as = make_float2(0.f, 0.f);
+        if constexpr (QT == MOE_Q4_SM) as = *(const float2 *)(asum + 8 * b + 2 * c);
+#pragma unroll
+        for (int i = 0; i < NTL; ++i) {
+            const unsigned char *tc = st + (size_t)i * tb;
+            const unsigned char *ts = tc + (size_t)CB * QB;
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int R0 = 16 * hr + r;
+                uint32_t A0[4], A1[4];
+                float d0, d1, m0 = 0.f, m1 = 0.f;
+                if constexpr (QT == MOE_Q8_0) {
+                    const unsigned char *cp = tc + (size_t)(2 * b + (c >> 1)) * 512 + (c & 1) * 8;
+                    const uint2 w0 = *(const uint2 *)(cp + R0 * 16);
+                    const uint2 w1 = *(const uint2 *)(cp + (R0 + 8) * 16);
+                    const uint32_t t0x = w0.x ^ 0x80808080u, t0y = w0.y ^ 0x80808080u;
+                    const uint32_t t1x = w1.x ^ 0x80808080u, t1y = w1.y ^ 0x80808080u;
+                    A0[0] = q8_pair(t0x, 0x4140); A0[1] = q8_pair(t1x, 0x4140);
+                    A0[2] = q8_pair(t0x, 0x4342); A0[3] = q8_pair(t1x, 0x4342);
+                    A1[0] = q8_pair(t0y, 0x4140); A1[1] = q8_pair(t1y, 0x4140);
+                    A1[2] = q8_pair(t0y, 0x4342); A1[3] = q8_pair(t1y, 0x4342);
+                    d0 = __half2float(*(const __half *)(ts + (size_t)(b * 32 + R0) * 2));
+                    d1 = __half2float(*(const __half *)(ts + (size_t)(b * 32 + R0 + 8) * 2));
                 } else {
-                    v = make_float4(__bfloat162float(xb[0]), __bfloat162float(xb[1]), __bfloat162float(xb[2]),
-                                    __bfloat162float(xb[3]));
+                    const unsigned char *cp = tc + (size_t)b * 512 + 4 * c;
+                    const uint32_t w0 = *(const uint32_t *)(cp + R0 * 16);
+                    const uint32_t w1 = *(const uint32_t *)(cp + (R0 + 8) * 16);
+                    const uint32_t v0 = w0 >> 8, v1 = w1 >> 8;
+                    A0[0] = q4_even(w0); A0[1] = q4_even(w1); A0[2] = q4_odd(w0); A0[3] = q4_odd(w1);
+                    A1[0] = q4_even(v0); A1[1] = q4_even(v1); A1[2] = q4_odd(v0); A1[3] = q4_odd(v1);
+                    const __half2 e0 = *(const __half2 *)(ts + (size_t)(b * 32 + R0) * 4);
+                    const __half2 e1 = *(const __half2 *)(ts + (size_t)(b * 32 + R0 + 8) * 4);
+                    d0 = __low2float(e0);
+                    m0 = __high2float(e0);
+                    d1 = __low2float(e1);
+                    m1 = __high2float(e1);
                 }
-            } else {
-                const float *xf = (const float *)p.x + off;
-                v = p.x_vec ? *(const float4 *)xf : make_float4(xf[0], xf[1], xf[2], xf[3]);
+#pragma unroll
+                for (int s = 0; s < NS; ++s) {
+                    float C[4];
+                    mma16816(C, A0[0], A0[1], A0[2], A0[3], bf[s].x, bf[s].y, zero);
+                    mma16816(C, A1[0], A1[1], A1[2], A1[3], bf[s].z, bf[s].w, C);
+                    float *a = acc[i][hr][s];
+                    a[0] = fmaf(d0, C[0], a[0]);
+                    a[1] = fmaf(d0, C[1], a[1]);
+                    a[2] = fmaf(d1, C[2], a[2]);
+                    a[3] = fmaf(d1, C[3], a[3]);
+                    if (QT == MOE_Q4_SM && s == 0) {  // the block minimum times the hi columns' sums
+                        a[0] = fmaf(m0, as.x, a[0]);
+                        a[1] = fmaf(m0, as.y, a[1]);
+                        a[2] = fmaf(m1, as.x, a[2]);
+                        a[3] = fmaf(m1, as.y, a[3]);
+                    }
+                }
             }
         }
-        if (QT == MOE_Q4_SM) {
-            v.x *= q4_act_scale(c);
-            v.y *= q4_act_scale(c + 1);
-            v.z *= q4_act_scale(c + 2);
-            v.w *= q4_act_scale(c + 3);
-        }
-        *(float4 *)(act + (size_t)t * Kr + c) = v;
     }
 }
 
-// ------------------------------------------------------------------ G1 / G2: the ring kernel
-//
-// G1 (gate/up): units per active expert are KS K ranges x F/32 row tiles, ordered (ks, g);
-// unit (ks, g) holds the gate tile g and the up tile g over K range ks, so consecutive units
-// of a CTA share the expert's activations.  The reducing warp of token t forms
-// h = silu(gate) * up (KS = 1) or stores both partial sums (KS > 1).
-// G2 (down): units per active expert are H/(32 TPU) groups of TPU row tiles over the whole
-// of F with h as activations; each unit writes w[r] * (Wd h) for its routes r.
-//
-// Ring protocol: stage s = i % S holds the CTA's i-th unit.  Thread 0 issues unit i+S-1
-// at the top of iteration i, into the stage that unit i-1 used; every thread has finished
-// reading that stage before the barrier that ends unit i-1's dot products.  A fill unit or
-// a skipped expert arrives on its stage's mbarrier without bytes, so each stage completes
-// exactly one phase per use and the waits use parity (i / S) & 1.
+// Hi and lo parts of this lane's columns added and the token scale removed, into
+// acc[i][hr][0][j] for token 2c + (j & 1) (lanes c < 2 only when NS == 1).
+template <int NTL, int NS>
+__device__ __forceinline__ void finish_acc(float (&acc)[NTL][2][2][4], const float *inv_sc, int lane) {
+    const int c = lane & 3;
+    const float i0 = inv_sc[(2 * c) & 7], i1 = inv_sc[(2 * c + 1) & 7];
+#pragma unroll
+    for (int i = 0; i < NTL; ++i)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float v = acc[i][hr][0][j];
+                if (NS == 1) v += __shfl_xor_sync(0xffffffffu, v, 2);
+                else v += acc[i][hr][1][j];
+                acc[i][hr][0][j] = v * ((j & 1) ? i1 : i0);
+            }
+}
 
+// ------------------------------------------------------------------ staging the activations
+
+// Eight consecutive activations of one source row at column col: G1 reads row `row` of x
+// (a token), G2 row `row` (a route position) of h, or silu(sum gate) * (sum up) of the
+// K-split partial sums in a fixed order.
+template <int XT, bool DOWN>
+__device__ __forceinline__ void act_load8(const FfnParams &p, int row, int col, float (&v)[8]) {
+    if (DOWN) {
+        const size_t q = (size_t)row * p.F + col;
+        if (p.KS == 1) {
+            const float4 a = *(const float4 *)(p.h + q), b = *(const float4 *)(p.h + q + 4);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+            float g[8], u[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) g[e] = u[e] = 0.f;
+            for (int ks = 0; ks < p.KS; ++ks) {
+                const float *gp = p.gu + ((size_t)ks * 2 + 0) * p.RT * p.F + q;
+                const float *up = p.gu + ((size_t)ks * 2 + 1) * p.RT * p.F + q;
+                const float4 g0 = *(const float4 *)gp, g1 = *(const float4 *)(gp + 4);
+                const float4 u0 = *(const float4 *)up, u1 = *(const float4 *)(up + 4);
+                g[0] += g0.x; g[1] += g0.y; g[2] += g0.z; g[3] += g0.w;
+                g[4] += g1.x; g[5] += g1.y; g[6] += g1.z; g[7] += g1.w;
+                u[0] += u0.x; u[1] += u0.y; u[2] += u0.z; u[3] += u0.w;
+                u[4] += u1.x; u[5] += u1.y; u[6] += u1.z; u[7] += u1.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = silu_mul(g[e], u[e]);
+        }
+    } else {
+        const size_t off = (size_t)row * p.H + col;
+        if (XT == MOE_BF16) {
+            const __nv_bfloat16 *xb = (const __nv_bfloat16 *)p.x + off;
+            if (p.x_vec) {
+                const uint4 r = *(const uint4 *)xb;
+                const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(*(const __nv_bfloat162 *)&w[e]);
+                    v[2 * e] = f.x;
+                    v[2 * e + 1] = f.y;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = __bfloat162float(xb[e]);
+            }
+        } else {
+            const float *xf = (const float *)p.x + off;
+            if (p.x_vec) {
+                const float4 a = *(const float4 *)xf, b = *(const float4 *)(xf + 4);
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = xf[e];
+            }
+        }
+    }
+}
+
+// One token row of a pair's slot, by one warp: the activations y = x * sc over the pair's
+// K range [c0, c0 + Kr) with sc a power of two putting max |y| in [2^14, 2^15), stored as
+// fp16 hi = rn(y) (row 2t) and lo = rn(y - hi) (row 2t + 1); 1/sc at inv[t]; for the 4-bit
+// format the fp32 block sums of y at asum[b][t] and the columns of each group of 8 in the
+// order 0 4 1 5 2 6 3 7.
 template <int QT, int XT, bool DOWN>
-__global__ void __launch_bounds__(GV_THREADS, 1) ffn_ring_kernel(FfnParams p) {
+__device__ void stage_row(const FfnParams &p, int row, int c0, int Kr, unsigned char *slot, int NT8, int t,
+                          int lane) {
+    const int RS = gv_row_stride(Kr);
+    float amax = 0.f;
+    for (int base = 0; base < Kr; base += 256) {
+        const int col = base + 8 * lane;
+        if (col < Kr) {
+            float v[8];
+            act_load8<XT, DOWN>(p, row, c0 + col, v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int ex = amax > 0.f ? ((__float_as_int(amax) >> 23) & 0xFF) - 127 : 0;
+    ex = max(ex, -100);  // subnormal maxima: any scale keeps them exact enough
+    const float sc = __int_as_float((127 + 14 - ex) << 23);
+    float *inv = (float *)(slot + (size_t)2 * NT8 * RS);
+    float *asum = inv + 8;
+    if (lane == 0) inv[t] = __int_as_float((127 - 14 + ex) << 23);
+    __half *hi = (__half *)(slot + (size_t)(2 * t) * RS);
+    __half *lo = (__half *)(slot + (size_t)(2 * t + 1) * RS);
+    for (int base = 0; base < Kr; base += 256) {
+        const int col = base + 8 * lane;
+        float bs = 0.f;
+        if (col < Kr) {
+            float v[8];
+            act_load8<XT, DOWN>(p, row, c0 + col, v);
+            __align__(16) __half h8[8];
+            __align__(16) __half l8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float y = v[e] * sc;
+                const __half hh = __float2half_rn(y);
+                const __half ll = __float2half_rn(y - __half2float(hh));
+                const int at = QT == MOE_Q4_SM ? ((e & 3) * 2 + (e >> 2)) : e;
+                h8[at] = hh;
+                l8[at] = ll;
+                bs += y;
+            }
+            *(uint4 *)(hi + col) = *(const uint4 *)h8;
+            *(uint4 *)(lo + col) = *(const uint4 *)l8;
+        }
+        if (QT == MOE_Q4_SM) {  // 4 lanes cover one 32-column block
+            bs += __shfl_xor_sync(0xffffffffu, bs, 1);
+            bs += __shfl_xor_sync(0xffffffffu, bs, 2);
+            if (col < Kr && (lane & 3) == 0) asum[(col / 32) * 8 + t] = bs;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ fill chunks
+
+// A chunk of a unit whose expert missed: its bytes are read from the expert's pinned host
+// image over the CPU-GPU link by the warp's lanes (GV_FILL_BATCH 16-byte loads in flight
+// per lane) and written both to the stage and, when wt, through to the expert's slot.  Same
+// byte ranges and stage layout as the bulk copies of a resident chunk.
+template <int QT>
+__device__ void fill_chunk(const ActInfo &in, int H, int F, bool down, int NTL, int g, int kb0, int cb,
+                           unsigned char *st, int tb, int CB, int lane) {
+    constexpr int QB = QT == MOE_Q8_0 ? 1024 : 512;
+    constexpr int SB = QT == MOE_Q8_0 ? 64 : 128;
+    constexpr int PPB = QT == MOE_Q8_0 ? 2 : 1;
+    const int R = down ? H : F, K = down ? F : H;
+    const int nq = cb * QB / 16, ns = cb * SB / 16, n = nq + ns;
+    for (int i = 0; i < NTL; ++i) {
+        const size_t mo = moe_expert_matrix_offset(QT, H, F, down ? 2 : i);
+        const int gi = down ? g + i : g;
+        const size_t qoff = mo + moe_piece_offset(QT, K, gi, kb0 * PPB);
+        const size_t soff = mo + moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, gi, kb0);
+        const uint8_t *src = (const uint8_t *)in.src;
+        uint8_t *dst = in.wt ? (uint8_t *)in.dst : nullptr;
+        unsigned char *tile = st + (size_t)i * tb;
+        for (int j0 = 0; j0 < n; j0 += 32 * GV_FILL_BATCH) {
+            uint4 v[GV_FILL_BATCH];
+#pragma unroll
+            for (int b = 0; b < GV_FILL_BATCH; ++b) {
+                const int j = j0 + b * 32 + lane;
+                if (j < n) v[b] = __ldcs((const uint4 *)(src + (j < nq ? qoff + (size_t)j * 16 : soff + (size_t)(j - nq) * 16)));
+            }
+#pragma unroll
+            for (int b = 0; b < GV_FILL_BATCH; ++b) {
+                const int j = j0 + b * 32 + lane;
+                if (j < n) {
+                    const bool q = j < nq;
+                    *(uint4 *)(tile + (q ? (size_t)j * 16 : (size_t)CB * QB + (size_t)(j - nq) * 16)) = v[b];
+                    if (dst) __stcs((uint4 *)(dst + (q ? qoff + (size_t)j * 16 : soff + (size_t)(j - nq) * 16)), v[b]);
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ G1 / G2: the warp-ring kernel
+//
+// Units of a virtual expert: G1 has KS K ranges x F/32 row tiles, ordered (ks, g); unit
+// (ks, g) holds the gate and the up tile g over K range ks.  G2 has H/(32 NTL) groups of
+// NTL down tiles over the whole of F.  A pair = (virtual expert, K range) shares one staged
+// activation slot; a CTA stages the pairs of its unit range in phases of at most
+// act_slots pairs (usually one phase), between CTA barriers.
+//
+// Warp ring: the warp's chunks (its units in turn within each phase, each unit cut into
+// chunks of CB blocks) go through S stages; chunk J lives in stage J % S and completes phase
+// (J / S) & 1 of that stage's mbarrier, on which every lane waits.  Lane 0 issues chunk J+S
+// into the stage once all lanes are done with chunk J (after a __syncwarp).  A fill chunk or
+// a skipped expert's chunk arrives on its mbarrier without bytes.
+
+template <int QT, int XT, bool DOWN, int NTL>
+__global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    const int S = p.stages;
-    const int RTF = p.F / 32, RTH = p.H / 32;
-    const int NTL = DOWN ? p.TPU : 2;
-    const int nbr = DOWN ? p.F / 32 : (p.H / 32) / p.KS, Kr = nbr * 32;
-    const int R = DOWN ? p.H : p.F, K = DOWN ? p.F : p.H;
-    const int per_a = DOWN ? RTH / p.TPU : p.KS * RTF;
+    __shared__ int slot_of[GV_PHASE_PAIRS];
     const int u0 = p.ranges[blockIdx.x], u1 = p.ranges[blockIdx.x + 1];
     if (u0 >= u1) return;
-    const int ntok = min(p.T, GV_TOK);
-    const RingSmem L = ring_smem(QT, nbr, NTL, ntok, S);
-    uint64_t *bars = (uint64_t *)(smem + L.bars);
-    unsigned char *stages = smem + L.stages;
-    float *act = (float *)(smem + L.act);
-    float *asum = (float *)(smem + L.asum);
-    float *red = (float *)(smem + L.red);
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int QB = QT == MOE_Q8_0 ? 1024 : 512;
+    constexpr int SB = QT == MOE_Q8_0 ? 64 : 128;
+    constexpr int PPB = QT == MOE_Q8_0 ? 2 : 1;
+    const GvGeom G = p.geo;
+    const int R = DOWN ? p.H : p.F, K = DOWN ? p.F : p.H;
+    const int nbr = G.nbr, Kr = nbr * 32, CB = G.CB;
+    const int upp = DOWN ? (p.H / 32) / NTL : p.F / 32;  // units per pair
+    const int kspp = DOWN ? 1 : p.KS;                     // pairs per virtual expert
+    const int tb = CB * (QB + SB);                        // tile stride in a stage
+    const int nch = (nbr + CB - 1) / CB;                  // chunks per unit
+    const int RS = gv_row_stride(Kr);
+    const int NT8 = p.T <= 4 ? 4 : 8;
+    const int n_w = min(GV_WARPS, u1 - u0);
+    const int S = min(GV_MAX_STAGES, G.ring_bytes / (n_w * G.chunk_bytes));
+    uint64_t *bars = (uint64_t *)smem + warp * GV_MAX_STAGES;
+    unsigned char *ring = smem + GV_BARS + (size_t)warp * S * G.chunk_bytes;
+    unsigned char *act_region = smem + GV_BARS + G.ring_bytes;
     const int *routes = p.ws_ints + ws_routes_off(p.E);
 
-    // the experts and routes of this CTA's range, in shared memory when they fit
-    const int a_lo = u0 / per_a, a_hi = (u1 - 1) / per_a;
-    const bool icache = a_hi - a_lo < GV_ICACHE;
-    ActInfo *info_s = (ActInfo *)(smem + L.info);
-    const int pos_lo = p.info[a_lo].pos0, pos_hi = p.info[a_hi].pos0 + p.info[a_hi].n_e;
-    const bool rcache = pos_hi - pos_lo <= GV_RCACHE;
-    int *rts_s = (int *)(smem + L.rts);
-    float *wts_s = (float *)(smem + L.wts);
-    if (icache)
-        for (int a = a_lo + threadIdx.x; a <= a_hi; a += GV_THREADS) info_s[a - a_lo] = p.info[a];
-    if (rcache)
-        for (int q = pos_lo + threadIdx.x; q < pos_hi; q += GV_THREADS) {
-            const int r = routes[q];
-            rts_s[q - pos_lo] = r;
-            if (DOWN) wts_s[q - pos_lo] = p.weights[r];
-        }
-    auto info_at = [&](int a) { return icache ? info_s[a - a_lo] : p.info[a]; };
-    const int *rbase = rcache ? rts_s : routes;
-    const int rpos0 = rcache ? pos_lo : 0;  // route position q is at rbase[q - rpos0]
-
-    // unit u -> active expert a, K range ks, first row tile g (tile i: matrix mats[i], row tile g + i*DOWN)
-    auto decode = [&](int u, int &a, int &ks, int &g) {
-        a = u / per_a;
-        const int r = u - a * per_a;
-        if (DOWN) {
-            ks = 0;
-            g = r * p.TPU;
-        } else {
-            ks = r / RTF;
-            g = r - ks * RTF;
+    auto decode = [&](int u, int &v, int &pair, int &ks, int &g) {
+        pair = u / upp;
+        v = pair / kspp;
+        ks = pair - v * kspp;
+        g = (u - pair * upp) * (DOWN ? NTL : 1);
+    };
+    // End of the phase starting at unit a: at most act_slots pairs that need activations
+    // and GV_PHASE_PAIRS pairs in all.
+    auto phase_end = [&](int a) {
+        int pr = a / upp, used = 0;
+        for (int n = 0;; ++n, ++pr) {
+            const int first = max(a, pr * upp);
+            if (first >= u1) return u1;
+            if (n == GV_PHASE_PAIRS) return first;
+            if (p.info[pr / kspp].n_e > 0) {
+                if (used == G.act_slots) return first;
+                ++used;
+            }
         }
     };
-    auto tile_mat = [&](int i) { return DOWN ? 2 : i; };
-    auto tile_row = [&](int g, int i) { return DOWN ? g + i : g; };
-    auto issue = [&](int u, int s, bool cached) {  // thread 0 only
-        int a, ks, g;
-        decode(u, a, ks, g);
-        const ActInfo in = cached ? info_at(a) : p.info[a];
-        if (in.n_e == 0 || in.fill) {
-            mbar_arrive_plain(&bars[s]);
+
+    // ---- producer state (lane 0): the next chunk to issue
+    int pc_ph1 = u0, pc_u = u1, pc_ch = 0;  // phase end, unit (u1: none left), chunk
+    int pc_cached_v = -1;
+    ActInfo pc_in;
+    auto pc_first = [&](int a) {  // this warp's first unit at or after phase start a
+        pc_u = u1;
+        while (a < u1) {
+            const int e = phase_end(a);
+            if (a + warp < e) {
+                pc_ph1 = e;
+                pc_u = a + warp;
+                pc_ch = 0;
+                return;
+            }
+            a = e;
+        }
+    };
+    auto pc_next = [&]() {
+        if (++pc_ch < nch) return;
+        pc_ch = 0;
+        pc_u += GV_WARPS;
+        if (pc_u >= pc_ph1) pc_first(pc_ph1);
+    };
+    auto issue = [&](int stage) {
+        uint64_t *bar = &bars[stage];
+        int v, pair, ks, g;
+        decode(pc_u, v, pair, ks, g);
+        if (v != pc_cached_v) {
+            pc_in = p.info[v];
+            pc_cached_v = v;
+        }
+        if (pc_in.n_e == 0 || pc_in.fill) {
+            mbar_arrive_plain(bar);
             return;
         }
-        const int QB = QT == MOE_Q8_0 ? 1024 : 512, SB = 32 * moe_scale_entry_bytes(QT);
-        mbar_arrive_expect_tx(&bars[s], (uint32_t)(NTL * nbr * (QB + SB)));
-        for (int i = 0; i < NTL; ++i)
-            issue_tile<QT>((const uint8_t *)in.src + moe_expert_matrix_offset(QT, p.H, p.F, tile_mat(i)), R, K,
-                           tile_row(g, i), ks * nbr, nbr, stages + (size_t)s * L.stage_bytes + i * L.tile_bytes,
-                           L.scale_off, &bars[s]);
+        const int kb0 = ks * nbr + pc_ch * CB, cb = min(CB, nbr - pc_ch * CB);
+        mbar_arrive_expect_tx(bar, (uint32_t)(NTL * cb * (QB + SB)));
+        unsigned char *dst = ring + (size_t)stage * G.chunk_bytes;
+        for (int i = 0; i < NTL; ++i) {
+            const uint8_t *mat = (const uint8_t *)pc_in.src + moe_expert_matrix_offset(QT, p.H, p.F, DOWN ? 2 : i);
+            const int gi = DOWN ? g + i : g;
+            bulk_g2s(dst + (size_t)i * tb, mat + moe_piece_offset(QT, K, gi, kb0 * PPB), (uint32_t)(cb * QB), bar);
+            bulk_g2s(dst + (size_t)i * tb + (size_t)CB * QB,
+                     mat + moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, gi, kb0), (uint32_t)(cb * SB), bar);
+        }
     };
 
-    if (threadIdx.x == 0) {
+    int J_issued = 0;  // chunks issued by this warp (lane 0's count; broadcast when needed)
+    if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
-        for (int j = 0; j < S - 1 && u0 + j < u1; ++j) issue(u0 + j, j, false);
+        pc_first(u0);
+        for (int s = 0; s < S && pc_u < u1; ++s) {
+            issue(s);
+            pc_next();
+            ++J_issued;
+        }
     }
-    __syncthreads();
+    __syncwarp();
 
-    int b0, b1;
-    warp_blocks(nbr, warp, b0, b1);
-    int cur_a = -1, cur_ks = -1, cur_tg = -1;
-    int i = 0;
-    bool failed = false;
-    for (; u0 + i < u1; ++i) {
-        const int u = u0 + i, s = i % S;
-        if (threadIdx.x == 0 && u + S - 1 < u1) issue(u + S - 1, (i + S - 1) % S, true);
-        int a, ks, g;
-        decode(u, a, ks, g);
-        const ActInfo in = info_at(a);
-        unsigned char *stage = stages + (size_t)s * L.stage_bytes;
-        // activations of the first token pass, loaded while the unit's bytes arrive
-        const bool fresh = in.n_e > 0 && (a != cur_a || ks != cur_ks || cur_tg != 0);
-        if (fresh)
-            load_act<QT, XT, DOWN>(p, rbase, in.pos0 - rpos0, in.pos0, min(GV_TOK, in.n_e), ks * Kr, Kr, act);
-        // warp 0 waits for the stage; the barrier below publishes it to the other warps
-        const bool ok = warp == 0 ? mbar_wait_bounded(&bars[s], (i / S) & 1, p.status) : true;
-        if (in.fill && in.n_e > 0) {
-            for (int t = 0; t < NTL; ++t) {
-                const size_t mo = moe_expert_matrix_offset(QT, p.H, p.F, tile_mat(t));
-                fill_tile<QT>((const uint8_t *)in.src + mo, (uint8_t *)in.dst + mo, R, K, tile_row(g, t), ks * nbr,
-                              nbr, stage + t * L.tile_bytes, L.scale_off);
-            }
-            fence_proxy_async_smem();  // a later bulk copy overwrites this stage
+    int J = 0;           // chunks this warp has reached
+    int J_done = 0;      // chunks whose stage completed (waited on)
+    bool dead = false;   // a wait ran out: no more waits, copies or outputs
+    for (int a = u0; a < u1;) {
+        const int e = phase_end(a);
+        const int pr0 = a / upp, npr = (e - 1) / upp - pr0 + 1;
+        __syncthreads();  // the previous phase's slots and slot table are no longer read
+        if (threadIdx.x == 0) {
+            int s = 0;
+            for (int i = 0; i < npr; ++i) slot_of[i] = p.info[(pr0 + i) / kspp].n_e > 0 ? s++ : -1;
         }
-        // uniform: every thread saw its stage complete; the activations and a filled stage
-        // are visible; this unit's writes of red follow the previous unit's reads
-        if (!__syncthreads_and(ok)) {
-            failed = true;
-            break;
-        }
-        if (fresh) {
-            cur_a = a;
-            cur_ks = ks;
-            cur_tg = 0;
-            if (QT == MOE_Q4_SM) {
-                compute_asum<QT>(act, asum, min(GV_TOK, in.n_e), nbr, Kr);
-                __syncthreads();
+        __syncthreads();
+        for (int it = warp; it < npr * 8; it += GV_WARPS) {
+            const int si = slot_of[it >> 3], t = it & 7;
+            if (si < 0) continue;
+            const int pr = pr0 + (it >> 3), v = pr / kspp, ks = pr - v * kspp;
+            const ActInfo in = p.info[v];
+            unsigned char *slot = act_region + (size_t)si * G.slot_bytes;
+            if (t < in.n_e) {
+                const int pos = in.pos0 + t;
+                const int row = DOWN ? pos : routes[pos] / p.k;
+                stage_row<QT, XT, DOWN>(p, row, ks * Kr, Kr, slot, NT8, t, lane);
+            } else if (QT == MOE_Q4_SM) {
+                float *asum = (float *)(slot + (size_t)2 * NT8 * RS) + 8;
+                for (int b = lane; b < nbr; b += 32) asum[b * 8 + t] = 0.f;
             }
         }
-        for (int tg = 0; tg < in.n_e; tg += GV_TOK) {
-            const int nt = min(GV_TOK, in.n_e - tg);
-            if (tg != cur_tg) {  // further passes of an expert with more than 8 tokens
-                load_act<QT, XT, DOWN>(p, rbase, in.pos0 + tg - rpos0, in.pos0 + tg, nt, ks * Kr, Kr, act);
-                __syncthreads();
-                if (QT == MOE_Q4_SM) {
-                    compute_asum<QT>(act, asum, nt, nbr, Kr);
-                    __syncthreads();
-                }
-                cur_tg = tg;
-            }
-            float acc[2][GV_TOK];
+        __syncthreads();
+
+        for (int u = a + warp; u < e; u += GV_WARPS) {
+            int v, pair, ks, g;
+            decode(u, v, pair, ks, g);
+            const ActInfo in = p.info[v];
+            const unsigned char *slot = act_region + (size_t)slot_of[pair - pr0] * G.slot_bytes;
+            float acc[NTL][2][2][4];
 #pragma unroll
-            for (int t = 0; t < GV_TOK; ++t) acc[0][t] = acc[1][t] = 0.f;
-            if (NTL == 2)
-                tile_dot_dispatch<QT, 2>(nt, stage, stage + L.tile_bytes, L.scale_off, act, asum, Kr, nbr, b0, b1,
-                                         lane, acc);
-            else
-                tile_dot_dispatch<QT, 1>(nt, stage, stage, L.scale_off, act, asum, Kr, nbr, b0, b1, lane, acc);
+            for (int i = 0; i < NTL; ++i)
 #pragma unroll
-            for (int t = 0; t < GV_TOK; ++t)
-                if (t < nt) {
-                    red[(((size_t)warp * ntok + t) * 2 + 0) * 32 + lane] = acc[0][t];
-                    red[(((size_t)warp * ntok + t) * 2 + 1) * 32 + lane] = acc[1][t];
-                }
-            __syncthreads();  // red complete; every thread is done reading this stage and act
-            if (warp < nt) {
-                float v0 = 0.f, v1 = 0.f;
+                for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
-                for (int w = 0; w < GV_WARPS; ++w) {
-                    v0 += red[(((size_t)w * ntok + warp) * 2 + 0) * 32 + lane];
-                    v1 += red[(((size_t)w * ntok + warp) * 2 + 1) * 32 + lane];
+                    for (int s = 0; s < 2; ++s)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) acc[i][hr][s][j] = 0.f;
+            for (int ch = 0; ch < nch; ++ch, ++J) {
+                const int stg = J % S;
+                unsigned char *st = ring + (size_t)stg * G.chunk_bytes;
+                if (!dead) {
+                    const bool ok = mbar_wait_bounded(&bars[stg], (J / S) & 1, p.status);
+                    if (__all_sync(0xffffffffu, ok)) J_done = J + 1;
+                    else dead = true;
                 }
-                const int pos = in.pos0 + tg + warp;
-                if (DOWN) {
-                    const int r = rbase[pos - rpos0];
-                    const float wr = rcache ? wts_s[pos - rpos0] : p.weights[r];
-                    p.partial[(size_t)r * p.H + 32 * g + lane] = wr * v0;
-                    if (NTL == 2) p.partial[(size_t)r * p.H + 32 * (g + 1) + lane] = wr * v1;
-                } else if (p.KS == 1) {
-                    p.h[(size_t)pos * p.F + 32 * g + lane] = silu_mul(v0, v1);
-                } else {
-                    p.gu[(((size_t)ks * 2 + 0) * p.RT + pos) * p.F + 32 * g + lane] = v0;
-                    p.gu[(((size_t)ks * 2 + 1) * p.RT + pos) * p.F + 32 * g + lane] = v1;
+                if (!dead && in.n_e > 0) {
+                    const int cb = min(CB, nbr - ch * CB);
+                    if (in.fill) {
+                        fill_chunk<QT>(in, p.H, p.F, DOWN, NTL, g, ks * nbr + ch * CB, cb, st, tb, CB, lane);
+                        fence_proxy_async_smem();  // a later bulk copy overwrites this stage
+                        __syncwarp();
+                    }
+                    const unsigned char *ac = slot + (size_t)64 * ch * CB;
+                    const float *as = (const float *)(slot + (size_t)2 * NT8 * RS) + 8 + 8 * ch * CB;
+                    if (in.n_e <= 4) chunk_dot<QT, NTL, 1>(st, tb, CB, cb, ac, RS, as, lane, acc);
+                    else chunk_dot<QT, NTL, 2>(st, tb, CB, cb, ac, RS, as, lane, acc);
+                }
+                __syncwarp();  // every lane is done with the stage
+                if (lane == 0 && !dead && pc_u < u1) {
+                    issue(J_issued % S);
+                    pc_next();
+                    ++J_issued;
                 }
             }
-            if (tg + GV_TOK < in.n_e) __syncthreads();  // red and act are rewritten by the next pass
+            if (dead || in.n_e == 0) continue;
+            const float *inv = (const float *)(slot + (size_t)2 * NT8 * RS);
+            if (in.n_e <= 4) finish_acc<NTL, 1>(acc, inv, lane);
+            else finish_acc<NTL, 2>(acc, inv, lane);
+            const int r = lane >> 2, c = lane & 3;
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int row = 16 * hr + r + 8 * (j >> 1), t = 2 * c + (j & 1);
+                    if (t >= in.n_e) continue;
+                    const int pos = in.pos0 + t;
+                    if (DOWN) {
+                        const int rt = routes[pos];
+                        const float w = p.weights[rt];
+#pragma unroll
+                        for (int i = 0; i < NTL; ++i)
+                            p.partial[(size_t)rt * p.H + 32 * (g + i) + row] = w * acc[i][hr][0][j];
+                    } else if (p.KS == 1) {
+                        p.h[(size_t)pos * p.F + 32 * g + row] = silu_mul(acc[0][hr][0][j], acc[NTL - 1][hr][0][j]);
+                    } else {
+                        p.gu[(((size_t)ks * 2 + 0) * p.RT + pos) * p.F + 32 * g + row] = acc[0][hr][0][j];
+                        p.gu[(((size_t)ks * 2 + 1) * p.RT + pos) * p.F + 32 * g + row] = acc[NTL - 1][hr][0][j];
+                    }
+                }
         }
+        a = e;
     }
-    // A wait ran out: never leave with copies in flight.  Units i .. last issued are
+    // Never leave with copies in flight: a wait that ran out left chunks J_done .. issued-1
     // unconsumed; give each a second bounded wait.
-    if (failed && threadIdx.x == 0) {
-        const int last = min(u1 - 1, u0 + i + S - 1);
-        for (int j = i; u0 + j <= last; ++j) mbar_wait_bounded(&bars[j % S], (j / S) & 1, p.status);
-    }
+    if (lane == 0)
+        for (int j = J_done; j < J_issued; ++j) mbar_wait_bounded(&bars[j % S], (j / S) & 1, p.status);
 }
 
 // ------------------------------------------------------------------ P1: permute
 
-// First unit whose start cost is >= x: unit u of active expert a starts at cost
-// per_a * P[a] + (u - a * per_a) * cost[a].
-__device__ __forceinline__ int unit_at_cost(long long x, int n_act, int per_a, const int *P, const int *cost) {
-    const long long C = (long long)per_a * P[n_act];
-    if (x >= C) return n_act * per_a;
-    int lo = 0, hi = n_act - 1;  // largest a with per_a * P[a] <= x
+// First unit whose start cost is >= x.  Active expert a has nv(a) = vb[a+1] - vb[a] virtual
+// experts, all of vt routes but the last; each of their per_v units costs
+// unit_cost(routes), so a's first unit starts at cost per_v * Q[a] with
+// Q[a] = GV_COST_MEM * vb[a] + aoff[a].
+__device__ __forceinline__ int unit_at_cost(long long x, int n_act, int per_v, int vt, const int *vb,
+                                            const int *aoff) {
+    auto Q = [&](int a) { return (long long)GV_COST_MEM * vb[a] + aoff[a]; };
+    if (x >= per_v * Q(n_act)) return vb[n_act] * per_v;
+    int lo = 0, hi = n_act - 1;  // largest a with per_v * Q[a] <= x
     while (lo < hi) {
         const int mid = (lo + hi + 1) / 2;
-        if ((long long)per_a * P[mid] <= x) lo = mid;
+        if (per_v * Q(mid) <= x) lo = mid;
         else hi = mid - 1;
     }
-    const long long rem = x - (long long)per_a * P[lo];
-    return lo * per_a + (int)((rem + cost[lo] - 1) / cost[lo]);
+    const long long rem = x - per_v * Q(lo);
+    const int nv = vb[lo + 1] - vb[lo];
+    const long long full = (long long)per_v * unit_cost(vt);
+    const int j = (int)min((long long)(nv - 1), rem / full);
+    const long long rem2 = rem - j * full;
+    const int cv = unit_cost(min(vt, aoff[lo + 1] - aoff[lo] - vt * j));
+    return (vb[lo] + j) * per_v + (int)((rem2 + cv - 1) / cv);
 }
 
 // Stable counting sort of the routes r = t*k + j by expert (restricted to a subset), the
-// ascending list of active experts, their route ranges, per active expert where its weights
-// are read from (slot in the pool, or its pinned host image for a fill), and the unit
-// ranges of the CTAs of both GEMV launches, balanced by work (unit_cost).
+// ascending list of active experts and their route ranges, the virtual experts (groups of
+// at most vt routes of one expert) with where their weights are read from (slot in the
+// pool, or the pinned host image for a fill, written through by the first group only), and
+// the unit ranges of the CTAs of both GEMV launches, balanced by work (unit_cost).
 __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict__ ids, int R, int E,
                                                       const int32_t *__restrict__ subset, int n_subset,
                                                       int32_t *__restrict__ ints, ActInfo *__restrict__ info,
                                                       const int32_t *__restrict__ slot_table, int n_slots,
                                                       const uint8_t *pool, size_t slot_bytes,
                                                       const unsigned long long *__restrict__ fill_src,
-                                                      int G1, int per_a1, int G2, int per_a2, int *status) {
+                                                      int vt, int G1, int per_v1, int G2, int per_v2,
+                                                      int *status) {
     __shared__ int cnt[MOE_MAX_E], off[MOE_MAX_E + 1], run[MOE_MAX_E];
-    __shared__ int P[MOE_MAX_E + 1], cost[MOE_MAX_E];
+    __shared__ int vb[MOE_MAX_E + 1];
     __shared__ unsigned char insub[MOE_MAX_E];
     __shared__ int chunk_e[256];
     __shared__ int n_act;
@@ -696,57 +786,55 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
     int *active = ints + ws_active_off();
     int *aoff = ints + ws_aoff_off(E);
     if (tid == 0) {
-        int s = 0, na = 0;
+        int s = 0, na = 0, nv = 0;
         for (int e = 0; e < E; ++e) {
             off[e] = s;
             if (cnt[e] > 0) {
                 active[na] = e;
                 aoff[na] = s;
+                vb[na] = nv;
+                nv += (cnt[e] + vt - 1) / vt;
                 ++na;
             }
             s += cnt[e];
         }
         aoff[na] = s;
+        vb[na] = nv;
         ints[0] = na;
+        ints[1] = nv;
         n_act = na;
     }
     __syncthreads();
     for (int a = tid; a < n_act; a += 256) {
         const int e = active[a];
         const int slot = slot_table ? slot_table[e] : e;
+        const int n_e = aoff[a + 1] - aoff[a];
         ActInfo in;
-        in.e = e;
-        in.pos0 = aoff[a];
-        in.n_e = aoff[a + 1] - aoff[a];
-        in.fill = 0;
+        in.fill = in.wt = 0;
         in.src = in.dst = 0ull;
-        if (slot < 0 || slot >= n_slots) {
-            moe_set_status(status, MOE_ERR_INVALID);
-            in.n_e = 0;  // nothing of this expert is read
+        const bool bad = slot < 0 || slot >= n_slots;
+        if (bad) {
+            moe_set_status(status, MOE_ERR_INVALID);  // nothing of this expert is read
         } else {
             in.dst = (unsigned long long)(pool + (size_t)slot * slot_bytes);
             const unsigned long long f = fill_src ? fill_src[e] : 0ull;
             in.fill = f != 0ull;
             in.src = f ? f : in.dst;
         }
-        info[a] = in;
-        cost[a] = unit_cost(in.n_e);
-    }
-    __syncthreads();
-    if (tid == 0) {  // work prefix over the active experts (skipped experts cost 1 per unit)
-        int c = 0;
-        for (int a = 0; a < n_act; ++a) {
-            P[a] = c;
-            c += cost[a];
+        for (int j = 0; j < vb[a + 1] - vb[a]; ++j) {
+            in.pos0 = aoff[a] + vt * j;
+            in.n_e = bad ? 0 : min(vt, n_e - vt * j);
+            in.wt = in.fill && j == 0;
+            info[vb[a] + j] = in;
         }
-        P[n_act] = c;
     }
     __syncthreads();
     {
         int *r1 = ints + ws_ranges_off(E, R, 0), *r2 = ints + ws_ranges_off(E, R, 1);
-        const long long C1 = (long long)per_a1 * P[n_act], C2 = (long long)per_a2 * P[n_act];
-        for (int c = tid; c <= G1; c += 256) r1[c] = unit_at_cost(C1 * c / G1, n_act, per_a1, P, cost);
-        for (int c = tid; c <= G2; c += 256) r2[c] = unit_at_cost(C2 * c / G2, n_act, per_a2, P, cost);
+        const long long C1 = (long long)per_v1 * (GV_COST_MEM * vb[n_act] + aoff[n_act]);
+        const long long C2 = (long long)per_v2 * (GV_COST_MEM * vb[n_act] + aoff[n_act]);
+        for (int c = tid; c <= G1; c += 256) r1[c] = unit_at_cost(C1 * c / G1, n_act, per_v1, vt, vb, aoff);
+        for (int c = tid; c <= G2; c += 256) r2[c] = unit_at_cost(C2 * c / G2, n_act, per_v2, vt, vb, aoff);
     }
     int *routes = ints + ws_routes_off(E);
     for (int c0 = 0; c0 < R; c0 += 256) {
@@ -859,18 +947,20 @@ int ring_grid_capacity(const void *fn, size_t smem, int *ctas) {
     return MOE_OK;
 }
 
-template <int QT, int XT, bool DOWN>
-const void *ring_fn() {
-    return (const void *)ffn_ring_kernel<QT, XT, DOWN>;
+template <int QT, int XT, bool DOWN, int NTL>
+const void *warp_fn() {
+    return (const void *)ffn_warp_kernel<QT, XT, DOWN, NTL>;
 }
 
-const void *ring_kernel_for(int qtype, int xtype, bool down) {
+// The GEMV kernel of a launch: G1 takes x as fp32 or bf16 and two tiles per unit; G2 takes
+// fp32 activations and one or two tiles per unit.
+const void *gemv_kernel_for(int qtype, int xtype, bool down, int ntl) {
     if (qtype == MOE_Q8_0) {
-        if (down) return ring_fn<MOE_Q8_0, MOE_F32, true>();
-        return xtype == MOE_F32 ? ring_fn<MOE_Q8_0, MOE_F32, false>() : ring_fn<MOE_Q8_0, MOE_BF16, false>();
+        if (down) return ntl == 2 ? warp_fn<MOE_Q8_0, MOE_F32, true, 2>() : warp_fn<MOE_Q8_0, MOE_F32, true, 1>();
+        return xtype == MOE_F32 ? warp_fn<MOE_Q8_0, MOE_F32, false, 2>() : warp_fn<MOE_Q8_0, MOE_BF16, false, 2>();
     }
-    if (down) return ring_fn<MOE_Q4_SM, MOE_F32, true>();
-    return xtype == MOE_F32 ? ring_fn<MOE_Q4_SM, MOE_F32, false>() : ring_fn<MOE_Q4_SM, MOE_BF16, false>();
+    if (down) return ntl == 2 ? warp_fn<MOE_Q4_SM, MOE_F32, true, 2>() : warp_fn<MOE_Q4_SM, MOE_F32, true, 1>();
+    return xtype == MOE_F32 ? warp_fn<MOE_Q4_SM, MOE_F32, false, 2>() : warp_fn<MOE_Q4_SM, MOE_BF16, false, 2>();
 }
 
 }  // namespace
@@ -924,19 +1014,17 @@ int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype
     if ((size_t)T * k > (1u << 20)) return MOE_ERR_UNSUPPORTED;
     GvPlan pl;  // planned for every expert routable (the workspace does not depend on a subset)
     if (!gv_plan(T, H, F, qtype, gv_n_act_max(T, E, k), &pl)) return MOE_ERR_UNSUPPORTED;
-    const int ntok = T < GV_TOK ? T : GV_TOK;
     const int RTF = F / 32, RTH = H / 32;
-    const int nb1 = (H / 32) / pl.KS, nb2 = F / 32;
-    const size_t smem1 = ring_smem(qtype, nb1, 2, ntok, pl.S1).total;
-    const size_t smem2 = ring_smem(qtype, nb2, pl.TPU, ntok, pl.S2).total;
-    const void *k1 = ring_kernel_for(qtype, xtype, false), *k2 = ring_kernel_for(qtype, xtype, true);
+    const size_t smem1 = gv_smem_bytes(pl.g1), smem2 = gv_smem_bytes(pl.g2);
+    const void *k1 = gemv_kernel_for(qtype, xtype, false, 2), *k2 = gemv_kernel_for(qtype, xtype, true, pl.TPU);
     int cap1 = 0, cap2 = 0, rc;
     if ((rc = ring_grid_capacity(k1, smem1, &cap1)) != MOE_OK) return rc;
     if ((rc = ring_grid_capacity(k2, smem2, &cap2)) != MOE_OK) return rc;
-    const int n_act_max = expert_subset ? n_subset : (T * k < E ? T * k : E);
-    const int per_a1 = pl.KS * RTF, per_a2 = RTH / pl.TPU;
-    const int G1 = std::max(1, std::min(cap1, n_act_max * per_a1));
-    const int G2 = std::max(1, std::min(cap2, n_act_max * per_a2));
+    const int n_act_max = expert_subset ? n_subset : gv_n_act_max(T, E, k);
+    const long n_virt_max = n_act_max + (long)T * k / gv_vt(T) + 1;
+    const int per_v1 = pl.KS * RTF, per_v2 = RTH / pl.TPU;
+    const int G1 = (int)std::max(1L, std::min((long)cap1, n_virt_max * per_v1));
+    const int G2 = (int)std::max(1L, std::min((long)cap2, n_virt_max * per_v2));
 
     FfnParams p;
     p.x = x;
@@ -951,34 +1039,26 @@ int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype
     p.h = (float *)((char *)workspace + W.h_off);
     p.partial = partial;
     p.status = moe_status_word_device_ptr();
-    p.x_vec = ((uintptr_t)x % (xtype == MOE_F32 ? 16 : 8)) == 0;
+    p.x_vec = ((uintptr_t)x & 15) == 0;
 
     if (timing && timing->permute0) MOE_TRY_CUDA(cudaEventRecord(timing->permute0, s));
     permute_kernel<<<1, 256, 0, s>>>(ids, T * k, E, expert_subset, n_subset,
                                      (int32_t *)((char *)workspace + W.ints_off),
                                      (ActInfo *)((char *)workspace + W.info_off), d_slot_table, n_slots,
                                      (const uint8_t *)pool, slot_bytes, (const unsigned long long *)d_fill_src,
-                                     G1, per_a1, G2, per_a2, p.status);
+                                     pl.NT8, G1, per_v1, G2, per_v2, p.status);
     MOE_TRY_CUDA(cudaGetLastError());
     if (timing && timing->permute1) MOE_TRY_CUDA(cudaEventRecord(timing->permute1, s));
     if (timing && timing->gateup0) MOE_TRY_CUDA(cudaEventRecord(timing->gateup0, s));
-    p.stages = pl.S1;
+    p.geo = pl.g1;
     p.ranges = p.ws_ints + ws_ranges_off(E, T * k, 0);
-    if (qtype == MOE_Q8_0) {
-        if (xtype == MOE_F32) ffn_ring_kernel<MOE_Q8_0, MOE_F32, false><<<G1, GV_THREADS, smem1, s>>>(p);
-        else ffn_ring_kernel<MOE_Q8_0, MOE_BF16, false><<<G1, GV_THREADS, smem1, s>>>(p);
-    } else {
-        if (xtype == MOE_F32) ffn_ring_kernel<MOE_Q4_SM, MOE_F32, false><<<G1, GV_THREADS, smem1, s>>>(p);
-        else ffn_ring_kernel<MOE_Q4_SM, MOE_BF16, false><<<G1, GV_THREADS, smem1, s>>>(p);
-    }
-    MOE_TRY_CUDA(cudaGetLastError());
+    void *args[] = {&p};
+    MOE_TRY_CUDA(cudaLaunchKernel(k1, dim3(G1), dim3(GV_THREADS), args, smem1, s));
     if (timing && timing->gateup1) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
     if (timing && timing->down0) MOE_TRY_CUDA(cudaEventRecord(timing->down0, s));
-    p.stages = pl.S2;
+    p.geo = pl.g2;
     p.ranges = p.ws_ints + ws_ranges_off(E, T * k, 1);
-    if (qtype == MOE_Q8_0) ffn_ring_kernel<MOE_Q8_0, MOE_F32, true><<<G2, GV_THREADS, smem2, s>>>(p);
-    else ffn_ring_kernel<MOE_Q4_SM, MOE_F32, true><<<G2, GV_THREADS, smem2, s>>>(p);
-    MOE_TRY_CUDA(cudaGetLastError());
+    MOE_TRY_CUDA(cudaLaunchKernel(k2, dim3(G2), dim3(GV_THREADS), args, smem2, s));
     if (timing && timing->down1) MOE_TRY_CUDA(cudaEventRecord(timing->down1, s));
     return MOE_OK;
 }

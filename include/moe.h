@@ -402,6 +402,27 @@ int moe_stack_profile_get(moe_stack *st, moe_stack_profile *out);
 int moe_stack_profile_reset(moe_stack *st);
 /* Sets the profiling level (0, 1, 2 as in moe_stack_desc.profile) for later calls. */
 int moe_stack_set_profile(moe_stack *st, int level);
+
+/*
+ * moe_stack_gemv_timing — the decode GEMV kernels of a resident stack (n_groups == 0)
+ * timed alone: the router and the token-to-expert permute of every layer run first for the
+ * batch x_in (device [T][H] fp32, the same FFN input for each layer, 1 <= T <=
+ * MOE_DECODE_MAX_T); then, on stream s, `reps` rounds of the gate/up GEMV of every layer are
+ * launched back to back between two CUDA events, then `reps` rounds of the down GEMV.
+ * Consecutive launches read different layers' experts, so no launch finds the previous
+ * one's weights in L2.  Results: the average time of one launch (microseconds, launch gaps
+ * included, no events between launches) and the quantised bytes of the selected experts
+ * one launch reads (the permute kernel's active-expert counts).  Allocates and frees its
+ * own device buffers and synchronises s.  Errors: MOE_ERR_UNSUPPORTED for a stack with
+ * pool groups.
+ */
+typedef struct moe_gemv_timing {
+    double gateup_us, down_us;        /* average per launch */
+    double gateup_bytes, down_bytes;  /* average per launch */
+    int launches;                     /* per kernel: reps * layers */
+} moe_gemv_timing;
+int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, int reps, moe_gemv_timing *out,
+                          moe_stream_t s);
 void moe_stack_destroy(moe_stack *st);
 
 /* ------------------------------------------------------------------ test hooks */

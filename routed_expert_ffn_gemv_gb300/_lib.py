@@ -36,7 +36,7 @@ EXPORTED = [
     "moe_cache_lookup", "moe_slots_for_budget", "moe_expert_ffn", "moe_expert_ffn_workspace",
     "moe_combine", "moe_device_status", "moe_stack_workspace", "moe_stack_create",
     "moe_stack_decode", "moe_stack_layer", "moe_stack_profile_get", "moe_stack_profile_reset",
-    "moe_stack_destroy", "moe_debug_inject_fault", "moe_stack_set_profile",
+    "moe_stack_destroy", "moe_debug_inject_fault", "moe_stack_set_profile", "moe_stack_gemv_timing",
     "moe_expert_ffn_noalloc", "moe_combine_rmsnorm", "moe_cache_state_bytes", "moe_cache_plan",
     "moe_expert_ffn_fill", "moe_last_cuda_error",
 ]
@@ -97,6 +97,14 @@ class StackProfile(ctypes.Structure):
         return {f[0]: getattr(self, f[0]) for f in self._fields_}
 
 
+class GemvTiming(ctypes.Structure):
+    _fields_ = [("gateup_us", ctypes.c_double), ("down_us", ctypes.c_double),
+                ("gateup_bytes", ctypes.c_double), ("down_bytes", ctypes.c_double), ("launches", _i)]
+
+    def as_dict(self):
+        return {f[0]: getattr(self, f[0]) for f in self._fields_}
+
+
 _lib: Optional[ctypes.CDLL] = None
 
 
@@ -148,6 +156,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_stack_profile_reset": ([_vp], _i),
         "moe_stack_destroy": ([_vp], None),
         "moe_stack_set_profile": ([_vp, _i], _i),
+        "moe_stack_gemv_timing": ([_vp, _vp, _i, _i, P(GemvTiming), _vp], _i),
         "moe_debug_inject_fault": ([_i, _i], _i),
     }
     for name, (args, res) in sig.items():
@@ -366,6 +375,13 @@ def moe_stack_profile_reset(stack: int) -> None:
 
 def moe_stack_set_profile(stack: int, level: int) -> None:
     _ck("moe_stack_set_profile", load().moe_stack_set_profile(stack, level))
+
+
+def moe_stack_gemv_timing(stack: int, x, T: int, reps: int, stream=None) -> dict:
+    t = GemvTiming()
+    _ck("moe_stack_gemv_timing", load().moe_stack_gemv_timing(stack, _ptr(x), T, reps, ctypes.byref(t),
+                                                              _stream(stream)))
+    return t.as_dict()
 
 
 def moe_stack_destroy(stack: int) -> None:

@@ -28,21 +28,28 @@ static inline cudaStream_t moe_cuda_stream(moe_stream_t s) { return (cudaStream_
 
 // ------------------------------------------------------------------ slot image layout
 //
-// A matrix of R rows (output features) by K columns (reduction) is stored as
-//   [quant region][scale region]
-// Rows are grouped in tiles of 32 (one row per lane of a warp).  The quant region
-// holds, for row tile g and column piece p, 32 consecutive 16-byte pieces (lane 0..31),
-// so a warp's 16-byte loads of one piece are one contiguous 512-byte run and a whole
-// row tile is contiguous along K.  A piece is 16 int8 codes (q8_0) or one 32-code
-// block (4-bit; the block's 16 code bytes in canonical order).  The scale region holds
-// per (row tile g, block b) 32 consecutive per-lane entries: fp16 d (q8_0) or
-// fp16 d, fp16 m (4-bit).  An expert image is gate [F][H], up [F][H], down [H][F].
+// A matrix of R rows (output features) by K columns (reduction) is stored in 32-row tiles
+// (one row per lane of a warp), each tile a run of "tile blocks", one per 32-column block
+// along K, so that any K range of a tile is one contiguous run of bytes.  A tile block is
+//   codes:  PPB pieces of 512 bytes (q8_0: 2, 4-bit: 1); piece p holds, for lane 0..31,
+//           16 bytes of codes: q8_0 columns 16p .. 16p+15 of the block, one byte each, stored
+//           as q + 128 (offset binary); 4-bit the block's 16 code bytes in canonical order;
+//   scales: 32 entries, fp16 d (q8_0) or fp16 d, fp16 m (4-bit), the entry of row (lane) l
+//           at position moe_scale_pos(l) = 4 (l % 8) + l / 8, so that rows l, l+8, l+16,
+//           l+24 are adjacent.
+// An expert image is gate [F][H], up [F][H], down [H][F].
 
 #define MOE_TILE_ROWS 32
 
 __host__ __device__ static inline int moe_piece_cols(int qtype) { return qtype == MOE_Q8_0 ? 16 : 32; }
+__host__ __device__ static inline int moe_pieces_per_block(int qtype) { return qtype == MOE_Q8_0 ? 2 : 1; }
 __host__ __device__ static inline int moe_scale_entry_bytes(int qtype) { return qtype == MOE_Q8_0 ? 2 : 4; }
 __host__ __device__ static inline int moe_block_bytes(int qtype) { return qtype == MOE_Q8_0 ? 34 : 20; }
+// bytes of one tile block: 32 rows of one 32-column block, codes then scales
+__host__ __device__ static inline int moe_tile_block_bytes(int qtype) {
+    return MOE_TILE_ROWS * (qtype == MOE_Q8_0 ? 32 : 16) + MOE_TILE_ROWS * moe_scale_entry_bytes(qtype);
+}
+__host__ __device__ static inline int moe_scale_pos(int lane) { return 4 * (lane & 7) + (lane >> 3); }
 
 __host__ __device__ static inline size_t moe_quant_bytes(int qtype, int R, int K) {
     return qtype == MOE_Q8_0 ? (size_t)R * K : (size_t)R * K / 2;
@@ -53,15 +60,14 @@ __host__ __device__ static inline size_t moe_scale_bytes(int qtype, int R, int K
 __host__ __device__ static inline size_t moe_matrix_bytes(int qtype, int R, int K) {
     return moe_quant_bytes(qtype, R, K) + moe_scale_bytes(qtype, R, K);
 }
-// byte offset of (row tile g, piece p) in the quant region (lane 0's piece)
-__host__ __device__ static inline size_t moe_piece_offset(int qtype, int K, int g, int p) {
-    int P = K / moe_piece_cols(qtype);
-    return ((size_t)g * P + p) * (MOE_TILE_ROWS * 16);
+// byte offset of tile block (row tile g, block b) in a matrix
+__host__ __device__ static inline size_t moe_tile_block_offset(int qtype, int K, int g, int b) {
+    return ((size_t)g * (K / 32) + b) * moe_tile_block_bytes(qtype);
 }
-// byte offset of (row tile g, block b) in the scale region (lane 0's entry)
-__host__ __device__ static inline size_t moe_scale_offset(int qtype, int K, int g, int b) {
-    int NB = K / 32;
-    return ((size_t)g * NB + b) * (MOE_TILE_ROWS * moe_scale_entry_bytes(qtype));
+// within a tile block: the code bytes of lane l in piece p, and the scale entry of lane l
+__host__ __device__ static inline int moe_piece_in_block(int p, int lane) { return p * 512 + lane * 16; }
+__host__ __device__ static inline int moe_scale_in_block(int qtype, int lane) {
+    return MOE_TILE_ROWS * (qtype == MOE_Q8_0 ? 32 : 16) + moe_scale_pos(lane) * moe_scale_entry_bytes(qtype);
 }
 __host__ __device__ static inline size_t moe_expert_image_bytes(int qtype, int H, int F) {
     return 2 * moe_matrix_bytes(qtype, F, H) + moe_matrix_bytes(qtype, H, F);
@@ -110,6 +116,19 @@ int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype
                         const int32_t *expert_subset, int n_subset, const uint64_t *d_fill_src,
                         float *partial, void *workspace, size_t ws_bytes, cudaStream_t s,
                         const moe_ffn_timing *timing);
+
+// The stages of one decode-path FFN call (T <= MOE_DECODE_MAX_T): a later stage reads what
+// the earlier stages of the same call left in the workspace.
+#define MOE_FFN_PERMUTE 1
+#define MOE_FFN_GATEUP 2
+#define MOE_FFN_DOWN 4
+#define MOE_FFN_ALL 7
+int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
+                          const int32_t *ids, const float *weights, const int32_t *d_slot_table,
+                          int n_slots, const void *pool, size_t slot_bytes,
+                          const int32_t *expert_subset, int n_subset, const uint64_t *d_fill_src,
+                          float *partial, void *workspace, size_t ws_bytes, cudaStream_t s,
+                          const moe_ffn_timing *timing, int stages);
 
 // Writes up to three small int32 arrays (<= 256 values each) on stream s with one launch
 // (values travel as kernel parameters, so no host staging buffer outlives the call).

@@ -7,7 +7,7 @@
 // their quantised blocks (page 5, section 1.2) and are dequantised in registers.
 //
 // GB300 mapping (the decode GEMVs stream the selected experts' bytes from HBM once):
-//  * the routes of an expert are cut into groups of at most 8 tokens ("virtual experts");
+//  * the routes of an expert are cut into groups of at most 4 ("virtual experts");
 //    a work unit is NTL 32-row tiles of one virtual expert over a K range: the gate and the
 //    up tile of the same rows (G1), or one or two neighbouring down tiles (G2);
 //  * persistent CTAs of 16 warps, one per SM, each over a contiguous, work-balanced range of
@@ -39,7 +39,7 @@
 
 #define GV_WARPS 16
 #define GV_THREADS (GV_WARPS * 32)
-#define GV_TOK 8                  // tokens of a virtual expert
+#define GV_TOK 4                  // routes of a virtual expert (one m16n8 column set: hi + lo)
 #define GV_SMEM_MAX (220 * 1024)  // dynamic shared memory a GEMV kernel may take
 #define GV_BARS 1024              // mbarrier area: GV_WARPS x GV_MAX_STAGES
 #define GV_MAX_STAGES 8           // ring stages of one warp
@@ -61,8 +61,6 @@ __host__ __device__ inline int unit_cost(int n_e) { return GV_COST_MEM + n_e; }
 
 // ------------------------------------------------------------------ launch plan
 
-// Virtual experts hold at most NT8 routes (4 when T <= 4, else GV_TOK), so that a staged
-// activation slot of NT8 token rows always suffices.
 // Per kernel: NTL tiles per unit, nbr 32-column blocks per unit (the K range), CB blocks per
 // chunk (one ring stage), the staged activation slot of one (virtual expert, K range) pair
 // and how many of those a CTA phase holds, and the ring bytes left for the warps.
@@ -71,7 +69,7 @@ struct GvGeom {
 };
 
 struct GvPlan {
-    int KS, TPU, NT8;
+    int KS, TPU;
     GvGeom g1, g2;
 };
 
@@ -82,20 +80,26 @@ __host__ __device__ inline int gv_sb(int qtype) { return 32 * moe_scale_entry_by
 // and spreads the 8 rows of a B-fragment load over the banks.
 __host__ __device__ inline int gv_row_stride(int Kr) { return 2 * Kr + 32; }
 
-// One pair's slot: 2*NT8 fp16 rows (hi, lo per token), 8 inverse token scales, and for the
-// 4-bit format the per-block activation sums [nbr][8].
-__host__ __device__ inline int gv_slot_bytes(int qtype, int nbr, int NT8) {
-    const int b = 2 * NT8 * gv_row_stride(nbr * 32) + 32 + (qtype == MOE_Q4_SM ? nbr * 32 : 0);
+// One pair's slot: 2*NTS fp16 rows (hi, lo per token row), up to 32 inverse token scales,
+// the header (SlotHdr, 128 bytes), and for the 4-bit format the per-block activation sums
+// [nbr][NTS].  The gate/up kernel stages every token of the call (NTS = T <= 32), the down
+// kernel the routes of one virtual expert (NTS = GV_TOK).
+#define GV_INV_OFF(NTS, RS) ((size_t)2 * (NTS) * (RS))
+#define GV_HDR_OFF(NTS, RS) ((size_t)2 * (NTS) * (RS) + 128)
+#define GV_ASUM_OFF(NTS, RS) ((size_t)2 * (NTS) * (RS) + 256)
+#define GV_SLOT_MAX (72 * 1024)  // the gate/up K split is raised until a slot fits
+__host__ __device__ inline int gv_slot_bytes(int qtype, int nbr, int NTS) {
+    const int b = (int)GV_ASUM_OFF(NTS, gv_row_stride(nbr * 32)) + (qtype == MOE_Q4_SM ? nbr * NTS * 4 : 0);
     return (b + 127) / 128 * 128;
 }
 
-inline bool gv_geom(int qtype, int NTL, int nbr, int NT8, GvGeom *g) {
+inline bool gv_geom(int qtype, int NTL, int nbr, int NTS, GvGeom *g) {
     g->NTL = NTL;
     g->nbr = nbr;
     const int per_block = NTL * (gv_qb(qtype) + gv_sb(qtype));
     g->CB = std::max(1, std::min(nbr, GV_CHUNK_TARGET / per_block));
     g->chunk_bytes = g->CB * per_block;
-    g->slot_bytes = gv_slot_bytes(qtype, nbr, NT8);
+    g->slot_bytes = gv_slot_bytes(qtype, nbr, NTS);
     const int ring_min = GV_WARPS * GV_MIN_STAGES * g->chunk_bytes;
     const int room = GV_SMEM_MAX - GV_BARS - ring_min;
     if (room < g->slot_bytes) return false;
@@ -110,19 +114,19 @@ inline int gv_smem_bytes(const GvGeom &g) { return GV_BARS + g.ring_bytes + g.ac
 // most GV_KS_MAX, each K range at least one block); the down kernel takes two row tiles per
 // unit when that still gives enough units.
 inline bool gv_plan(int T, int H, int F, int qtype, int n_act_max, GvPlan *pl) {
+    if (T < 1 || T > MOE_DECODE_MAX_T) return false;
     const int NB = H / 32, RTF = F / 32, RTH = H / 32;
-    pl->NT8 = T <= 4 ? 4 : GV_TOK;
     int ks = 1;
     while (ks < GV_KS_MAX && (long)n_act_max * RTF * ks < GV_UNITS_TARGET && NB % (2 * ks) == 0) ks *= 2;
+    while (gv_slot_bytes(qtype, NB / ks, T) > GV_SLOT_MAX && NB % (2 * ks) == 0) ks *= 2;
     pl->KS = ks;
     pl->TPU = RTH % 2 == 0 && (long)n_act_max * (RTH / 2) >= GV_UNITS_TARGET ? 2 : 1;
-    return gv_geom(qtype, 2, NB / ks, pl->NT8, &pl->g1) && gv_geom(qtype, pl->TPU, F / 32, pl->NT8, &pl->g2);
+    return gv_geom(qtype, 2, NB / ks, T, &pl->g1) && gv_geom(qtype, pl->TPU, F / 32, GV_TOK, &pl->g2);
 }
 
 inline int gv_n_act_max(int T, int E, int k) { return T * k < E ? T * k : E; }
-inline int gv_vt(int T) { return T <= 4 ? 4 : GV_TOK; }
-// virtual experts: at most one per active expert plus one per further group of vt routes
-inline int gv_n_virt_max(int T, int E, int k) { return gv_n_act_max(T, E, k) + (T * k) / gv_vt(T) + 1; }
+// virtual experts: at most one per active expert plus one per further group of GV_TOK routes
+inline int gv_n_virt_max(int T, int E, int k) { return gv_n_act_max(T, E, k) + (T * k) / GV_TOK + 1; }
 
 // ------------------------------------------------------------------ workspace layout
 
@@ -132,7 +136,16 @@ struct ActInfo {
     unsigned long long dst;  // slot base (written through when wt != 0)
     int pos0, n_e;           // route positions [pos0, pos0 + n_e); n_e == 0: skip (invalid slot)
     int fill, wt;            // fill: read src with loads (host image); wt: write the bytes to dst
+    int rt[GV_TOK];          // the routes t*k + j at those positions
 };
+
+// Header of a staged slot: the pair's virtual expert and, for the down kernel, its routes'
+// router weights.
+struct SlotHdr {
+    ActInfo in;
+    float w[GV_TOK];
+};
+static_assert(sizeof(SlotHdr) <= 128, "slot header");
 
 // int32 region: [0] n_active [1] n_virtual | active [E] | a_off [E+1] | routes [R] | ranges1 | ranges2
 __host__ __device__ inline int ws_active_off() { return 16; }
@@ -210,9 +223,10 @@ __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) 
     return d;
 }
 
-// Two int8 codes of the offset-128 word t (bytes chosen by sel) as an fp16 pair of exact
-// integers: the byte under an 0x64 high byte reads 1024 + (q + 128); subtracting 1152
-// leaves q.
+// Two codes of a word of offset-binary bytes q + 128 (chosen by sel) as an fp16 pair of
+// exact integers: the byte under an 0x64 high byte reads 1024 + (q + 128); subtracting
+// 1152 leaves q.
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<const __half2 *>(&u); }
 __device__ __forceinline__ uint32_t q8_pair(uint32_t t, uint32_t sel) {
     return hsub2_u(__byte_perm(t, 0x64646464u, sel), 0x64806480u);
 }
@@ -236,102 +250,99 @@ __device__ __forceinline__ uint32_t q4_odd(uint32_t w) {
 // and (2,6), (3,7) of the 8, which is why the staged 4-bit activations are permuted the
 // same way within each group of 8).  The B fragment of a lane is then the 16 bytes of fp16
 // activations at columns 8c .. 8c+7 of its B row, one shared-memory load per block.
-// B rows: with one column set (NS = 1) column n is token n%4, hi (n < 4) or lo; with two
-// sets, set 0 is the hi and set 1 the lo part of tokens 0..7.
+// B rows: column n is route n % 4 of the virtual expert, its hi part (n < 4) or lo part.
 
-// acc[i][hr][s][j]: tile i, row 16 hr + r (+ 8 for j >= 2), column 2c + (j & 1) of set s.
-template <int QT, int NTL, int NS>
-__device__ __forceinline__ void chunk_dot(const unsigned char *st, int tb, int CB, int cb, const unsigned char *act,
-                                          int RS, const float *asum, int lane, float (&acc)[NTL][2][2][4]) {
-    constexpr int QB = QT == MOE_Q8_0 ? 1024 : 512;
+// acc[i][hr][j]: tile i, row 16 hr + r (+ 8 for j >= 2), column 2c + (j & 1).
+// brow: this lane's B row at the chunk's first column (plus 16 c bytes); as0 / as1: the
+// 4-bit block sums of the lane's two columns at the chunk's first block (stride NTS per
+// block), or null for lo columns (no minimum term).
+template <int QT, int NTL>
+__device__ __forceinline__ void chunk_dot(const unsigned char *st, int tb, int cb, const unsigned char *brow,
+                                          const float *as0, const float *as1, int NTS, int lane,
+                                          float (&acc)[NTL][2][4]) {
+    constexpr int TBB = QT == MOE_Q8_0 ? 1088 : 640;  // tile block: codes, then 32 scale entries
+    constexpr int SC = QT == MOE_Q8_0 ? 1024 : 512;   // offset of the scales in a tile block
     const int r = lane >> 2, c = lane & 3;
-    const unsigned char *brow[NS];
-#pragma unroll
-    for (int s = 0; s < NS; ++s) {
-        const int row = NS == 1 ? 2 * (r & 3) + (r >> 2) : 2 * r + s;
-        brow[s] = act + (size_t)row * RS + 16 * c;
-    }
     const float zero[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
     for (int b = 0; b < cb; ++b) {
-        uint4 bf[NS];
-#pragma unroll
-        for (int s = 0; s < NS; ++s) bf[s] = *(const uint4 *)(brow[s] + 64 * b);
+        const uint4 bf = *(const uint4 *)(brow + 64 * b);
         float2 as = make_float2(0.f, 0.f);
-        if constexpr (QT == MOE_Q4_SM) as = *(const float2 *)(asum + 8 * b + 2 * c);
+        if constexpr (QT == MOE_Q4_SM) {
+            if (as0) as = make_float2(as0[b * NTS], as1[b * NTS]);
+        }
 #pragma unroll
         for (int i = 0; i < NTL; ++i) {
-            const unsigned char *tc = st + (size_t)i * tb;
-            const unsigned char *ts = tc + (size_t)CB * QB;
+            const unsigned char *blk = st + (size_t)i * tb + (size_t)b * TBB;
+            // the scale entries of rows r, r+8, r+16, r+24 are adjacent (moe_scale_pos)
+            float dd[4], mm[4];
+            if constexpr (QT == MOE_Q8_0) {
+                const uint2 e = *(const uint2 *)(blk + SC + 8 * r);
+                dd[0] = __low2float(u32_as_h2(e.x)); dd[1] = __high2float(u32_as_h2(e.x));
+                dd[2] = __low2float(u32_as_h2(e.y)); dd[3] = __high2float(u32_as_h2(e.y));
+                mm[0] = mm[1] = mm[2] = mm[3] = 0.f;
+            } else {
+                const uint4 e = *(const uint4 *)(blk + SC + 16 * r);
+                const uint32_t ew[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    dd[q] = __low2float(u32_as_h2(ew[q]));
+                    mm[q] = __high2float(u32_as_h2(ew[q]));
+                }
+            }
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int R0 = 16 * hr + r;
                 uint32_t A0[4], A1[4];
-                float d0, d1, m0 = 0.f, m1 = 0.f;
-                if constexpr (QT == MOE_Q8_0) {
-                    const unsigned char *cp = tc + (size_t)(2 * b + (c >> 1)) * 512 + (c & 1) * 8;
+                if constexpr (QT == MOE_Q8_0) {  // offset-binary codes: no sign flip needed
+                    const unsigned char *cp = blk + (c >> 1) * 512 + (c & 1) * 8;
                     const uint2 w0 = *(const uint2 *)(cp + R0 * 16);
                     const uint2 w1 = *(const uint2 *)(cp + (R0 + 8) * 16);
-                    const uint32_t t0x = w0.x ^ 0x80808080u, t0y = w0.y ^ 0x80808080u;
-                    const uint32_t t1x = w1.x ^ 0x80808080u, t1y = w1.y ^ 0x80808080u;
-                    A0[0] = q8_pair(t0x, 0x4140); A0[1] = q8_pair(t1x, 0x4140);
-                    A0[2] = q8_pair(t0x, 0x4342); A0[3] = q8_pair(t1x, 0x4342);
-                    A1[0] = q8_pair(t0y, 0x4140); A1[1] = q8_pair(t1y, 0x4140);
-                    A1[2] = q8_pair(t0y, 0x4342); A1[3] = q8_pair(t1y, 0x4342);
-                    d0 = __half2float(*(const __half *)(ts + (size_t)(b * 32 + R0) * 2));
-                    d1 = __half2float(*(const __half *)(ts + (size_t)(b * 32 + R0 + 8) * 2));
+                    A0[0] = q8_pair(w0.x, 0x4140); A0[1] = q8_pair(w1.x, 0x4140);
+                    A0[2] = q8_pair(w0.x, 0x4342); A0[3] = q8_pair(w1.x, 0x4342);
+                    A1[0] = q8_pair(w0.y, 0x4140); A1[1] = q8_pair(w1.y, 0x4140);
+                    A1[2] = q8_pair(w0.y, 0x4342); A1[3] = q8_pair(w1.y, 0x4342);
                 } else {
-                    const unsigned char *cp = tc + (size_t)b * 512 + 4 * c;
+                    const unsigned char *cp = blk + 4 * c;
                     const uint32_t w0 = *(const uint32_t *)(cp + R0 * 16);
                     const uint32_t w1 = *(const uint32_t *)(cp + (R0 + 8) * 16);
                     const uint32_t v0 = w0 >> 8, v1 = w1 >> 8;
                     A0[0] = q4_even(w0); A0[1] = q4_even(w1); A0[2] = q4_odd(w0); A0[3] = q4_odd(w1);
                     A1[0] = q4_even(v0); A1[1] = q4_even(v1); A1[2] = q4_odd(v0); A1[3] = q4_odd(v1);
-                    const __half2 e0 = *(const __half2 *)(ts + (size_t)(b * 32 + R0) * 4);
-                    const __half2 e1 = *(const __half2 *)(ts + (size_t)(b * 32 + R0 + 8) * 4);
-                    d0 = __low2float(e0);
-                    m0 = __high2float(e0);
-                    d1 = __low2float(e1);
-                    m1 = __high2float(e1);
                 }
-#pragma unroll
-                for (int s = 0; s < NS; ++s) {
-                    float C[4];
-                    mma16816(C, A0[0], A0[1], A0[2], A0[3], bf[s].x, bf[s].y, zero);
-                    mma16816(C, A1[0], A1[1], A1[2], A1[3], bf[s].z, bf[s].w, C);
-                    float *a = acc[i][hr][s];
-                    a[0] = fmaf(d0, C[0], a[0]);
-                    a[1] = fmaf(d0, C[1], a[1]);
-                    a[2] = fmaf(d1, C[2], a[2]);
-                    a[3] = fmaf(d1, C[3], a[3]);
-                    if (QT == MOE_Q4_SM && s == 0) {  // the block minimum times the hi columns' sums
-                        a[0] = fmaf(m0, as.x, a[0]);
-                        a[1] = fmaf(m0, as.y, a[1]);
-                        a[2] = fmaf(m1, as.x, a[2]);
-                        a[3] = fmaf(m1, as.y, a[3]);
-                    }
+                const float d0 = dd[2 * hr], d1 = dd[2 * hr + 1], m0 = mm[2 * hr], m1 = mm[2 * hr + 1];
+                float C[4];
+                mma16816(C, A0[0], A0[1], A0[2], A0[3], bf.x, bf.y, zero);
+                mma16816(C, A1[0], A1[1], A1[2], A1[3], bf.z, bf.w, C);
+                float *a = acc[i][hr];
+                a[0] = fmaf(d0, C[0], a[0]);
+                a[1] = fmaf(d0, C[1], a[1]);
+                a[2] = fmaf(d1, C[2], a[2]);
+                a[3] = fmaf(d1, C[3], a[3]);
+                if (QT == MOE_Q4_SM) {  // the block minimum times the hi columns' sums
+                    a[0] = fmaf(m0, as.x, a[0]);
+                    a[1] = fmaf(m0, as.y, a[1]);
+                    a[2] = fmaf(m1, as.x, a[2]);
+                    a[3] = fmaf(m1, as.y, a[3]);
                 }
             }
         }
     }
 }
 
-// Hi and lo parts of this lane's columns added and the token scale removed, into
-// acc[i][hr][0][j] for token 2c + (j & 1) (lanes c < 2 only when NS == 1).
-template <int NTL, int NS>
-__device__ __forceinline__ void finish_acc(float (&acc)[NTL][2][2][4], const float *inv_sc, int lane) {
-    const int c = lane & 3;
-    const float i0 = inv_sc[(2 * c) & 7], i1 = inv_sc[(2 * c + 1) & 7];
+// Hi and lo parts of this lane's columns added (lane c + 2 holds the lo part of lane c's
+// columns) and the route scales (i0, i1 for its two columns) removed, into acc[i][hr][j]
+// for column 2c + (j & 1) (valid on lanes c < 2).
+template <int NTL>
+__device__ __forceinline__ void finish_acc(float (&acc)[NTL][2][4], float i0, float i1) {
 #pragma unroll
     for (int i = 0; i < NTL; ++i)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float v = acc[i][hr][0][j];
-                if (NS == 1) v += __shfl_xor_sync(0xffffffffu, v, 2);
-                else v += acc[i][hr][1][j];
-                acc[i][hr][0][j] = v * ((j & 1) ? i1 : i0);
+                const float v = acc[i][hr][j] + __shfl_xor_sync(0xffffffffu, acc[i][hr][j], 2);
+                acc[i][hr][j] = v * ((j & 1) ? i1 : i0);
             }
 }
 
@@ -397,14 +408,24 @@ __device__ __forceinline__ void act_load8(const FfnParams &p, int row, int col, 
 // One token row of a pair's slot, by one warp: the activations y = x * sc over the pair's
 // K range [c0, c0 + Kr) with sc a power of two putting max |y| in [2^14, 2^15), stored as
 // fp16 hi = rn(y) (row 2t) and lo = rn(y - hi) (row 2t + 1); 1/sc at inv[t]; for the 4-bit
-// format the fp32 block sums of y at asum[b][t] and the columns of each group of 8 in the
-// order 0 4 1 5 2 6 3 7.
+// format the fp32 block sums of y at asum[b][t] (row stride NTS) and the columns of each
+// group of 8 in the order 0 4 1 5 2 6 3 7.
 template <int QT, int XT, bool DOWN>
-__device__ void stage_row(const FfnParams &p, int row, int c0, int Kr, unsigned char *slot, int NT8, int t,
+__device__ void stage_row(const FfnParams &p, int row, int c0, int Kr, unsigned char *slot, int NTS, int t,
                           int lane) {
     const int RS = gv_row_stride(Kr);
     float amax = 0.f;
-    for (int base = 0; base < Kr; base += 256) {
+    float keep[2][8];  // the first 512 columns stay in registers for the second pass
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int col = 256 * i + 8 * lane;
+        if (col < Kr) {
+            act_load8<XT, DOWN>(p, row, c0 + col, keep[i]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(keep[i][e]));
+        }
+    }
+    for (int base = 512; base < Kr; base += 256) {
         const int col = base + 8 * lane;
         if (col < Kr) {
             float v[8];
@@ -418,17 +439,15 @@ __device__ void stage_row(const FfnParams &p, int row, int c0, int Kr, unsigned 
     int ex = amax > 0.f ? ((__float_as_int(amax) >> 23) & 0xFF) - 127 : 0;
     ex = max(ex, -100);  // subnormal maxima: any scale keeps them exact enough
     const float sc = __int_as_float((127 + 14 - ex) << 23);
-    float *inv = (float *)(slot + (size_t)2 * NT8 * RS);
-    float *asum = inv + 8;
+    float *inv = (float *)(slot + GV_INV_OFF(NTS, RS));
+    float *asum = (float *)(slot + GV_ASUM_OFF(NTS, RS));
     if (lane == 0) inv[t] = __int_as_float((127 - 14 + ex) << 23);
     __half *hi = (__half *)(slot + (size_t)(2 * t) * RS);
     __half *lo = (__half *)(slot + (size_t)(2 * t + 1) * RS);
-    for (int base = 0; base < Kr; base += 256) {
-        const int col = base + 8 * lane;
+    // one step of 8 columns per lane; every lane calls it (the 4-bit block sums shuffle)
+    auto emit = [&](int col, const float (&v)[8]) {
         float bs = 0.f;
         if (col < Kr) {
-            float v[8];
-            act_load8<XT, DOWN>(p, row, c0 + col, v);
             __align__(16) __half h8[8];
             __align__(16) __half l8[8];
 #pragma unroll
@@ -447,47 +466,51 @@ __device__ void stage_row(const FfnParams &p, int row, int c0, int Kr, unsigned 
         if (QT == MOE_Q4_SM) {  // 4 lanes cover one 32-column block
             bs += __shfl_xor_sync(0xffffffffu, bs, 1);
             bs += __shfl_xor_sync(0xffffffffu, bs, 2);
-            if (col < Kr && (lane & 3) == 0) asum[(col / 32) * 8 + t] = bs;
+            if (col < Kr && (lane & 3) == 0) asum[(col / 32) * NTS + t] = bs;
         }
+    };
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        if (256 * i < Kr) emit(256 * i + 8 * lane, keep[i]);
+    for (int base = 512; base < Kr; base += 256) {
+        const int col = base + 8 * lane;
+        float v[8] = {};
+        if (col < Kr) act_load8<XT, DOWN>(p, row, c0 + col, v);
+        emit(col, v);
     }
 }
 
 // ------------------------------------------------------------------ fill chunks
 
-// A chunk of a unit whose expert missed: its bytes are read from the expert's pinned host
-// image over the CPU-GPU link by the warp's lanes (GV_FILL_BATCH 16-byte loads in flight
-// per lane) and written both to the stage and, when wt, through to the expert's slot.  Same
-// byte ranges and stage layout as the bulk copies of a resident chunk.
+// A chunk of a unit whose expert missed: its bytes (one run of tile blocks per tile) are
+// read from the expert's pinned host image over the CPU-GPU link by the warp's lanes
+// (GV_FILL_BATCH 16-byte loads in flight per lane) and written both to the stage and, when
+// wt, through to the expert's slot.  Same byte ranges and stage layout as the bulk copies
+// of a resident chunk.
 template <int QT>
 __device__ void fill_chunk(const ActInfo &in, int H, int F, bool down, int NTL, int g, int kb0, int cb,
-                           unsigned char *st, int tb, int CB, int lane) {
-    constexpr int QB = QT == MOE_Q8_0 ? 1024 : 512;
-    constexpr int SB = QT == MOE_Q8_0 ? 64 : 128;
-    constexpr int PPB = QT == MOE_Q8_0 ? 2 : 1;
-    const int R = down ? H : F, K = down ? F : H;
-    const int nq = cb * QB / 16, ns = cb * SB / 16, n = nq + ns;
+                           unsigned char *st, int tb, int lane) {
+    const int K = down ? F : H;
+    const int n = cb * moe_tile_block_bytes(QT) / 16;
     for (int i = 0; i < NTL; ++i) {
-        const size_t mo = moe_expert_matrix_offset(QT, H, F, down ? 2 : i);
-        const int gi = down ? g + i : g;
-        const size_t qoff = mo + moe_piece_offset(QT, K, gi, kb0 * PPB);
-        const size_t soff = mo + moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, gi, kb0);
-        const uint8_t *src = (const uint8_t *)in.src;
-        uint8_t *dst = in.wt ? (uint8_t *)in.dst : nullptr;
+        const size_t off = moe_expert_matrix_offset(QT, H, F, down ? 2 : i) +
+                           moe_tile_block_offset(QT, K, down ? g + i : g, kb0);
+        const uint8_t *src = (const uint8_t *)in.src + off;
+        uint8_t *dst = in.wt ? (uint8_t *)in.dst + off : nullptr;
         unsigned char *tile = st + (size_t)i * tb;
         for (int j0 = 0; j0 < n; j0 += 32 * GV_FILL_BATCH) {
             uint4 v[GV_FILL_BATCH];
 #pragma unroll
             for (int b = 0; b < GV_FILL_BATCH; ++b) {
                 const int j = j0 + b * 32 + lane;
-                if (j < n) v[b] = __ldcs((const uint4 *)(src + (j < nq ? qoff + (size_t)j * 16 : soff + (size_t)(j - nq) * 16)));
+                if (j < n) v[b] = __ldcs((const uint4 *)(src + (size_t)j * 16));
             }
 #pragma unroll
             for (int b = 0; b < GV_FILL_BATCH; ++b) {
                 const int j = j0 + b * 32 + lane;
                 if (j < n) {
-                    const bool q = j < nq;
-                    *(uint4 *)(tile + (q ? (size_t)j * 16 : (size_t)CB * QB + (size_t)(j - nq) * 16)) = v[b];
-                    if (dst) __stcs((uint4 *)(dst + (q ? qoff + (size_t)j * 16 : soff + (size_t)(j - nq) * 16)), v[b]);
+                    *(uint4 *)(tile + (size_t)j * 16) = v[b];
+                    if (dst) __stcs((uint4 *)(dst + (size_t)j * 16), v[b]);
                 }
             }
         }
@@ -511,28 +534,28 @@ __device__ void fill_chunk(const ActInfo &in, int H, int F, bool down, int NTL, 
 template <int QT, int XT, bool DOWN, int NTL>
 __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int slot_of[GV_PHASE_PAIRS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *bars = (uint64_t *)smem + warp * GV_MAX_STAGES;
+    if (lane == 0) {  // while the range is loaded: every stage barrier this warp may use
+        for (int s = 0; s < GV_MAX_STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
     const int u0 = p.ranges[blockIdx.x], u1 = p.ranges[blockIdx.x + 1];
     if (u0 >= u1) return;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int QB = QT == MOE_Q8_0 ? 1024 : 512;
-    constexpr int SB = QT == MOE_Q8_0 ? 64 : 128;
-    constexpr int PPB = QT == MOE_Q8_0 ? 2 : 1;
+    constexpr int TBB = QT == MOE_Q8_0 ? 1088 : 640;  // bytes of a tile block (codes + scales)
     const GvGeom G = p.geo;
-    const int R = DOWN ? p.H : p.F, K = DOWN ? p.F : p.H;
+    const int K = DOWN ? p.F : p.H;
     const int nbr = G.nbr, Kr = nbr * 32, CB = G.CB;
     const int upp = DOWN ? (p.H / 32) / NTL : p.F / 32;  // units per pair
     const int kspp = DOWN ? 1 : p.KS;                     // pairs per virtual expert
-    const int tb = CB * (QB + SB);                        // tile stride in a stage
+    const int tb = CB * TBB;                              // tile stride in a stage
     const int nch = (nbr + CB - 1) / CB;                  // chunks per unit
     const int RS = gv_row_stride(Kr);
-    const int NT8 = p.T <= 4 ? 4 : 8;
+    const int NTS = DOWN ? GV_TOK : p.T;  // token rows of a slot
     const int n_w = min(GV_WARPS, u1 - u0);
     const int S = min(GV_MAX_STAGES, G.ring_bytes / (n_w * G.chunk_bytes));
-    uint64_t *bars = (uint64_t *)smem + warp * GV_MAX_STAGES;
     unsigned char *ring = smem + GV_BARS + (size_t)warp * S * G.chunk_bytes;
     unsigned char *act_region = smem + GV_BARS + G.ring_bytes;
-    const int *routes = p.ws_ints + ws_routes_off(p.E);
 
     auto decode = [&](int u, int &v, int &pair, int &ks, int &g) {
         pair = u / upp;
@@ -540,25 +563,23 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
         ks = pair - v * kspp;
         g = (u - pair * upp) * (DOWN ? NTL : 1);
     };
-    // End of the phase starting at unit a: at most act_slots pairs that need activations
-    // and GV_PHASE_PAIRS pairs in all.
-    auto phase_end = [&](int a) {
-        int pr = a / upp, used = 0;
-        for (int n = 0;; ++n, ++pr) {
-            const int first = max(a, pr * upp);
-            if (first >= u1) return u1;
-            if (n == GV_PHASE_PAIRS) return first;
-            if (p.info[pr / kspp].n_e > 0) {
-                if (used == G.act_slots) return first;
-                ++used;
-            }
-        }
-    };
+    // a phase covers the units of act_slots consecutive pairs (slot = pair - first pair)
+    auto phase_end = [&](int a) { return min(u1, (a / upp + G.act_slots) * upp); };
 
     // ---- producer state (lane 0): the next chunk to issue
     int pc_ph1 = u0, pc_u = u1, pc_ch = 0;  // phase end, unit (u1: none left), chunk
     int pc_cached_v = -1;
-    ActInfo pc_in;
+    unsigned long long pc_src = 0ull;
+    bool pc_skip = true;
+    auto pc_info = [&]() {  // where the weights of the next chunk's virtual expert are read from
+        const int v = pc_u / (upp * kspp);
+        if (v != pc_cached_v) {
+            const ActInfo &in = p.info[v];
+            pc_src = in.src;
+            pc_skip = in.n_e == 0 || in.fill;
+            pc_cached_v = v;
+        }
+    };
     auto pc_first = [&](int a) {  // this warp's first unit at or after phase start a
         pc_u = u1;
         while (a < u1) {
@@ -582,36 +603,25 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
         uint64_t *bar = &bars[stage];
         int v, pair, ks, g;
         decode(pc_u, v, pair, ks, g);
-        if (v != pc_cached_v) {
-            pc_in = p.info[v];
-            pc_cached_v = v;
-        }
-        if (pc_in.n_e == 0 || pc_in.fill) {
+        pc_info();
+        if (pc_skip) {
             mbar_arrive_plain(bar);
             return;
         }
         const int kb0 = ks * nbr + pc_ch * CB, cb = min(CB, nbr - pc_ch * CB);
-        mbar_arrive_expect_tx(bar, (uint32_t)(NTL * cb * (QB + SB)));
+        mbar_arrive_expect_tx(bar, (uint32_t)(NTL * cb * TBB));
         unsigned char *dst = ring + (size_t)stage * G.chunk_bytes;
         for (int i = 0; i < NTL; ++i) {
-            const uint8_t *mat = (const uint8_t *)pc_in.src + moe_expert_matrix_offset(QT, p.H, p.F, DOWN ? 2 : i);
-            const int gi = DOWN ? g + i : g;
-            bulk_g2s(dst + (size_t)i * tb, mat + moe_piece_offset(QT, K, gi, kb0 * PPB), (uint32_t)(cb * QB), bar);
-            bulk_g2s(dst + (size_t)i * tb + (size_t)CB * QB,
-                     mat + moe_quant_bytes(QT, R, K) + moe_scale_offset(QT, K, gi, kb0), (uint32_t)(cb * SB), bar);
+            const uint8_t *mat = (const uint8_t *)pc_src + moe_expert_matrix_offset(QT, p.H, p.F, DOWN ? 2 : i);
+            bulk_g2s(dst + (size_t)i * tb, mat + moe_tile_block_offset(QT, K, DOWN ? g + i : g, kb0),
+                     (uint32_t)(cb * TBB), bar);
         }
     };
 
-    int J_issued = 0;  // chunks issued by this warp (lane 0's count; broadcast when needed)
+    int J_issued = 0;  // chunks issued by this warp (lane 0's count)
     if (lane == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
-        fence_mbar_init();
         pc_first(u0);
-        for (int s = 0; s < S && pc_u < u1; ++s) {
-            issue(s);
-            pc_next();
-            ++J_issued;
-        }
+        if (pc_u < u1) pc_info();
     }
     __syncwarp();
 
@@ -621,43 +631,63 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
     for (int a = u0; a < u1;) {
         const int e = phase_end(a);
         const int pr0 = a / upp, npr = (e - 1) / upp - pr0 + 1;
-        __syncthreads();  // the previous phase's slots and slot table are no longer read
-        if (threadIdx.x == 0) {
-            int s = 0;
-            for (int i = 0; i < npr; ++i) slot_of[i] = p.info[(pr0 + i) / kspp].n_e > 0 ? s++ : -1;
-        }
-        __syncthreads();
-        for (int it = warp; it < npr * 8; it += GV_WARPS) {
-            const int si = slot_of[it >> 3], t = it & 7;
-            if (si < 0) continue;
-            const int pr = pr0 + (it >> 3), v = pr / kspp, ks = pr - v * kspp;
-            const ActInfo in = p.info[v];
-            unsigned char *slot = act_region + (size_t)si * G.slot_bytes;
-            if (t < in.n_e) {
-                const int pos = in.pos0 + t;
-                const int row = DOWN ? pos : routes[pos] / p.k;
-                stage_row<QT, XT, DOWN>(p, row, ks * Kr, Kr, slot, NT8, t, lane);
-            } else if (QT == MOE_Q4_SM) {
-                float *asum = (float *)(slot + (size_t)2 * NT8 * RS) + 8;
-                for (int b = lane; b < nbr; b += 32) asum[b * 8 + t] = 0.f;
+        if (a != u0) __syncthreads();  // the previous phase's slots are no longer read
+        // Staging, item (pair i, token row t).  Gate/up: every token of the call over the
+        // pair's K range, read from x without the routing metadata.  Down: the routes of the
+        // pair's virtual expert, read from h (or the K-split sums).  Row 0's item also writes
+        // the slot header.
+        for (int it = warp; it < npr * NTS; it += GV_WARPS) {
+            const int i = it / NTS, t = it - i * NTS;
+            const int pr = pr0 + i, v = pr / kspp, ks = pr - v * kspp;
+            unsigned char *slot = act_region + (size_t)i * G.slot_bytes;
+            SlotHdr *hdr = (SlotHdr *)(slot + GV_HDR_OFF(NTS, RS));
+            if (DOWN) {
+                const ActInfo in = p.info[v];
+                if (t == 0 && lane == 0) hdr->in = in;
+                if (t < in.n_e) {
+                    if (lane == 0) hdr->w[t] = p.weights[in.rt[t]];
+                    stage_row<QT, XT, DOWN>(p, in.pos0 + t, 0, Kr, slot, NTS, t, lane);
+                } else if (QT == MOE_Q4_SM) {
+                    float *asum = (float *)(slot + GV_ASUM_OFF(NTS, RS));
+                    for (int b = lane; b < nbr; b += 32) asum[b * NTS + t] = 0.f;
+                }
+            } else {
+                if (t == 0 && lane == 0) hdr->in = p.info[v];
+                stage_row<QT, XT, DOWN>(p, t, ks * Kr, Kr, slot, NTS, t, lane);
             }
         }
+        if (a == u0 && lane == 0)
+            for (int s = 0; s < S && pc_u < u1; ++s) {
+                issue(s);
+                pc_next();
+                ++J_issued;
+            }
         __syncthreads();
 
         for (int u = a + warp; u < e; u += GV_WARPS) {
             int v, pair, ks, g;
             decode(u, v, pair, ks, g);
-            const ActInfo in = p.info[v];
-            const unsigned char *slot = act_region + (size_t)slot_of[pair - pr0] * G.slot_bytes;
-            float acc[NTL][2][2][4];
+            const unsigned char *slot = act_region + (size_t)(pair - pr0) * G.slot_bytes;
+            const SlotHdr *hdr = (const SlotHdr *)(slot + GV_HDR_OFF(NTS, RS));
+            const int n_e = hdr->in.n_e, fill = hdr->in.fill;
+            // Token row of route slot q of this virtual expert in the staged slot (gate/up: the
+            // route's token; down: q); slots past n_e read row 0 (their columns are not used).
+            auto trow = [&](int q) { return q >= n_e ? 0 : (DOWN ? q : hdr->in.rt[q] / p.k); };
+            const int r_ = lane >> 2, c_ = lane & 3;
+            // B row of column r_: route slot r_ % 4, hi (r_ < 4) or lo
+            const unsigned char *brow = slot + (size_t)(2 * trow(r_ & 3) + (r_ >> 2)) * RS + 16 * c_;
+            // the lane's two accumulator columns 2c, 2c+1: route slots, hi on lanes c < 2
+            const int q0 = (2 * c_) & 3, q1 = q0 + 1;
+            const bool hi_cols = c_ < 2;
+            const int tr0 = trow(q0), tr1 = trow(q1);
+            const float *asb = (const float *)(slot + GV_ASUM_OFF(NTS, RS));
+            float acc[NTL][2][4];
 #pragma unroll
             for (int i = 0; i < NTL; ++i)
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
-                    for (int s = 0; s < 2; ++s)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) acc[i][hr][s][j] = 0.f;
+                    for (int j = 0; j < 4; ++j) acc[i][hr][j] = 0.f;
             for (int ch = 0; ch < nch; ++ch, ++J) {
                 const int stg = J % S;
                 unsigned char *st = ring + (size_t)stg * G.chunk_bytes;
@@ -666,17 +696,16 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
                     if (__all_sync(0xffffffffu, ok)) J_done = J + 1;
                     else dead = true;
                 }
-                if (!dead && in.n_e > 0) {
+                if (!dead && n_e > 0) {
                     const int cb = min(CB, nbr - ch * CB);
-                    if (in.fill) {
-                        fill_chunk<QT>(in, p.H, p.F, DOWN, NTL, g, ks * nbr + ch * CB, cb, st, tb, CB, lane);
+                    if (fill) {
+                        fill_chunk<QT>(hdr->in, p.H, p.F, DOWN, NTL, g, ks * nbr + ch * CB, cb, st, tb, lane);
                         fence_proxy_async_smem();  // a later bulk copy overwrites this stage
                         __syncwarp();
                     }
-                    const unsigned char *ac = slot + (size_t)64 * ch * CB;
-                    const float *as = (const float *)(slot + (size_t)2 * NT8 * RS) + 8 + 8 * ch * CB;
-                    if (in.n_e <= 4) chunk_dot<QT, NTL, 1>(st, tb, CB, cb, ac, RS, as, lane, acc);
-                    else chunk_dot<QT, NTL, 2>(st, tb, CB, cb, ac, RS, as, lane, acc);
+                    const float *a0 = hi_cols ? asb + (size_t)ch * CB * NTS + tr0 : nullptr;
+                    const float *a1 = hi_cols ? asb + (size_t)ch * CB * NTS + tr1 : nullptr;
+                    chunk_dot<QT, NTL>(st, tb, cb, brow + (size_t)64 * ch * CB, a0, a1, NTS, lane, acc);
                 }
                 __syncwarp();  // every lane is done with the stage
                 if (lane == 0 && !dead && pc_u < u1) {
@@ -685,31 +714,32 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
                     ++J_issued;
                 }
             }
-            if (dead || in.n_e == 0) continue;
-            const float *inv = (const float *)(slot + (size_t)2 * NT8 * RS);
-            if (in.n_e <= 4) finish_acc<NTL, 1>(acc, inv, lane);
-            else finish_acc<NTL, 2>(acc, inv, lane);
-            const int r = lane >> 2, c = lane & 3;
+            if (dead || n_e == 0) continue;
+            const float *inv = (const float *)(slot + GV_INV_OFF(NTS, RS));
+            finish_acc<NTL>(acc, inv[tr0], inv[tr1]);
+            const int r = lane >> 2, c = lane & 3, pos0 = hdr->in.pos0;
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr)
+            for (int j = 0; j < 4; ++j) {
+                const int t = 2 * c + (j & 1);
+                if (t >= n_e) continue;
+                const int pos = pos0 + t;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int row = 16 * hr + r + 8 * (j >> 1), t = 2 * c + (j & 1);
-                    if (t >= in.n_e) continue;
-                    const int pos = in.pos0 + t;
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int row = 16 * hr + r + 8 * (j >> 1);
                     if (DOWN) {
-                        const int rt = routes[pos];
-                        const float w = p.weights[rt];
+                        const int rt = hdr->in.rt[t];
+                        const float w = hdr->w[t];
 #pragma unroll
                         for (int i = 0; i < NTL; ++i)
-                            p.partial[(size_t)rt * p.H + 32 * (g + i) + row] = w * acc[i][hr][0][j];
+                            p.partial[(size_t)rt * p.H + 32 * (g + i) + row] = w * acc[i][hr][j];
                     } else if (p.KS == 1) {
-                        p.h[(size_t)pos * p.F + 32 * g + row] = silu_mul(acc[0][hr][0][j], acc[NTL - 1][hr][0][j]);
+                        p.h[(size_t)pos * p.F + 32 * g + row] = silu_mul(acc[0][hr][j], acc[NTL - 1][hr][j]);
                     } else {
-                        p.gu[(((size_t)ks * 2 + 0) * p.RT + pos) * p.F + 32 * g + row] = acc[0][hr][0][j];
-                        p.gu[(((size_t)ks * 2 + 1) * p.RT + pos) * p.F + 32 * g + row] = acc[NTL - 1][hr][0][j];
+                        p.gu[(((size_t)ks * 2 + 0) * p.RT + pos) * p.F + 32 * g + row] = acc[0][hr][j];
+                        p.gu[(((size_t)ks * 2 + 1) * p.RT + pos) * p.F + 32 * g + row] = acc[NTL - 1][hr][j];
                     }
                 }
+            }
         }
         a = e;
     }
@@ -805,6 +835,25 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
         n_act = na;
     }
     __syncthreads();
+    int *routes = ints + ws_routes_off(E);
+    for (int c0 = 0; c0 < R; c0 += 256) {
+        const int r = c0 + tid;
+        int e = -1;
+        if (r < R) {
+            e = ids[r];
+            if (e < 0 || e >= E || !insub[e]) e = -1;
+        }
+        chunk_e[tid] = e;
+        __syncthreads();
+        if (e >= 0) {
+            int rank = 0;
+            for (int i = 0; i < tid; ++i) rank += (chunk_e[i] == e);
+            routes[off[e] + run[e] + rank] = r;
+        }
+        __syncthreads();
+        if (e >= 0) atomicAdd(&run[e], 1);
+        __syncthreads();
+    }
     for (int a = tid; a < n_act; a += 256) {
         const int e = active[a];
         const int slot = slot_table ? slot_table[e] : e;
@@ -825,6 +874,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
             in.pos0 = aoff[a] + vt * j;
             in.n_e = bad ? 0 : min(vt, n_e - vt * j);
             in.wt = in.fill && j == 0;
+            for (int t = 0; t < GV_TOK; ++t) in.rt[t] = t < in.n_e ? routes[in.pos0 + t] : 0;
             info[vb[a] + j] = in;
         }
     }
@@ -835,25 +885,6 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
         const long long C2 = (long long)per_v2 * (GV_COST_MEM * vb[n_act] + aoff[n_act]);
         for (int c = tid; c <= G1; c += 256) r1[c] = unit_at_cost(C1 * c / G1, n_act, per_v1, vt, vb, aoff);
         for (int c = tid; c <= G2; c += 256) r2[c] = unit_at_cost(C2 * c / G2, n_act, per_v2, vt, vb, aoff);
-    }
-    int *routes = ints + ws_routes_off(E);
-    for (int c0 = 0; c0 < R; c0 += 256) {
-        const int r = c0 + tid;
-        int e = -1;
-        if (r < R) {
-            e = ids[r];
-            if (e < 0 || e >= E || !insub[e]) e = -1;
-        }
-        chunk_e[tid] = e;
-        __syncthreads();
-        if (e >= 0) {
-            int rank = 0;
-            for (int i = 0; i < tid; ++i) rank += (chunk_e[i] == e);
-            routes[off[e] + run[e] + rank] = r;
-        }
-        __syncthreads();
-        if (e >= 0) atomicAdd(&run[e], 1);
-        __syncthreads();
     }
 }
 
@@ -966,7 +997,8 @@ const void *gemv_kernel_for(int qtype, int xtype, bool down, int ntl) {
 }  // namespace
 
 size_t moe_decode_workspace_bytes(int T, int H, int F, int qtype, int E, int k) {
-    return ws_layout(T, H, F, qtype, E, k).total;
+    // larger calls run in blocks of MOE_DECODE_MAX_T tokens that reuse one workspace
+    return ws_layout(std::min(T, MOE_DECODE_MAX_T), H, F, qtype, E, k).total;
 }
 
 size_t moe_ffn_workspace_bytes(int T, int H, int F, int qtype, int xtype, int E, int k) {
@@ -991,6 +1023,17 @@ int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype
                         const int32_t *expert_subset, int n_subset, const uint64_t *d_fill_src,
                         float *partial, void *workspace, size_t ws_bytes, cudaStream_t s,
                         const moe_ffn_timing *timing) {
+    return moe_expert_ffn_stages(x, xtype, T, H, F, qtype, E, k, ids, weights, d_slot_table, n_slots, pool,
+                                 slot_bytes, expert_subset, n_subset, d_fill_src, partial, workspace, ws_bytes, s,
+                                 timing, MOE_FFN_ALL);
+}
+
+int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
+                          const int32_t *ids, const float *weights, const int32_t *d_slot_table,
+                          int n_slots, const void *pool, size_t slot_bytes,
+                          const int32_t *expert_subset, int n_subset, const uint64_t *d_fill_src,
+                          float *partial, void *workspace, size_t ws_bytes, cudaStream_t s,
+                          const moe_ffn_timing *timing, int stages) {
     MOE_CHECK(T >= 0);
     MOE_CHECK(qtype == MOE_Q8_0 || qtype == MOE_Q4_SM);
     MOE_CHECK(xtype == MOE_F32 || xtype == MOE_BF16);
@@ -1004,14 +1047,28 @@ int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype
     MOE_CHECK(slot_bytes >= moe_expert_image_bytes(qtype, H, F));
     MOE_CHECK(((uintptr_t)workspace & 255) == 0);
     if (moe_prefill_eligible(T, H, F, qtype, xtype)) {
-        if (d_fill_src) return MOE_ERR_UNSUPPORTED;  // slot filling is a decode-path feature
+        if (d_fill_src || stages != MOE_FFN_ALL) return MOE_ERR_UNSUPPORTED;  // decode-path features
         MOE_CHECK(ws_bytes >= moe_prefill_workspace_bytes(T, H, F, E, k));
         return moe_prefill_ffn(x, xtype, T, H, F, qtype, E, k, ids, weights, d_slot_table, n_slots, pool,
                                slot_bytes, expert_subset, n_subset, partial, workspace, ws_bytes, s, timing);
     }
+    if ((size_t)T * k > (1u << 20)) return MOE_ERR_UNSUPPORTED;
+    if (T > MOE_DECODE_MAX_T) {  // token blocks of the decode size, one after another
+        if (stages != MOE_FFN_ALL) return MOE_ERR_UNSUPPORTED;
+        const size_t xb = xtype == MOE_F32 ? 4 : 2;
+        for (int t0 = 0; t0 < T; t0 += MOE_DECODE_MAX_T) {
+            const int Tb = std::min(MOE_DECODE_MAX_T, T - t0);
+            const int rc = moe_expert_ffn_core((const char *)x + (size_t)t0 * H * xb, xtype, Tb, H, F, qtype, E, k,
+                                               ids + (size_t)t0 * k, weights + (size_t)t0 * k, d_slot_table,
+                                               n_slots, pool, slot_bytes, expert_subset, n_subset, d_fill_src,
+                                               partial + (size_t)t0 * k * H, workspace, ws_bytes, s,
+                                               t0 == 0 ? timing : nullptr);
+            if (rc != MOE_OK) return rc;
+        }
+        return MOE_OK;
+    }
     const WsLayout W = ws_layout(T, H, F, qtype, E, k);
     MOE_CHECK(ws_bytes >= W.total);
-    if ((size_t)T * k > (1u << 20)) return MOE_ERR_UNSUPPORTED;
     GvPlan pl;  // planned for every expert routable (the workspace does not depend on a subset)
     if (!gv_plan(T, H, F, qtype, gv_n_act_max(T, E, k), &pl)) return MOE_ERR_UNSUPPORTED;
     const int RTF = F / 32, RTH = H / 32;
@@ -1021,7 +1078,7 @@ int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype
     if ((rc = ring_grid_capacity(k1, smem1, &cap1)) != MOE_OK) return rc;
     if ((rc = ring_grid_capacity(k2, smem2, &cap2)) != MOE_OK) return rc;
     const int n_act_max = expert_subset ? n_subset : gv_n_act_max(T, E, k);
-    const long n_virt_max = n_act_max + (long)T * k / gv_vt(T) + 1;
+    const long n_virt_max = n_act_max + (long)T * k / GV_TOK + 1;
     const int per_v1 = pl.KS * RTF, per_v2 = RTH / pl.TPU;
     const int G1 = (int)std::max(1L, std::min((long)cap1, n_virt_max * per_v1));
     const int G2 = (int)std::max(1L, std::min((long)cap2, n_virt_max * per_v2));
@@ -1041,25 +1098,31 @@ int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype
     p.status = moe_status_word_device_ptr();
     p.x_vec = ((uintptr_t)x & 15) == 0;
 
+    if (stages & MOE_FFN_PERMUTE) {
     if (timing && timing->permute0) MOE_TRY_CUDA(cudaEventRecord(timing->permute0, s));
     permute_kernel<<<1, 256, 0, s>>>(ids, T * k, E, expert_subset, n_subset,
                                      (int32_t *)((char *)workspace + W.ints_off),
                                      (ActInfo *)((char *)workspace + W.info_off), d_slot_table, n_slots,
                                      (const uint8_t *)pool, slot_bytes, (const unsigned long long *)d_fill_src,
-                                     pl.NT8, G1, per_v1, G2, per_v2, p.status);
+                                     GV_TOK, G1, per_v1, G2, per_v2, p.status);
     MOE_TRY_CUDA(cudaGetLastError());
     if (timing && timing->permute1) MOE_TRY_CUDA(cudaEventRecord(timing->permute1, s));
-    if (timing && timing->gateup0) MOE_TRY_CUDA(cudaEventRecord(timing->gateup0, s));
-    p.geo = pl.g1;
-    p.ranges = p.ws_ints + ws_ranges_off(E, T * k, 0);
+    }
     void *args[] = {&p};
-    MOE_TRY_CUDA(cudaLaunchKernel(k1, dim3(G1), dim3(GV_THREADS), args, smem1, s));
-    if (timing && timing->gateup1) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
-    if (timing && timing->down0) MOE_TRY_CUDA(cudaEventRecord(timing->down0, s));
-    p.geo = pl.g2;
-    p.ranges = p.ws_ints + ws_ranges_off(E, T * k, 1);
-    MOE_TRY_CUDA(cudaLaunchKernel(k2, dim3(G2), dim3(GV_THREADS), args, smem2, s));
-    if (timing && timing->down1) MOE_TRY_CUDA(cudaEventRecord(timing->down1, s));
+    if (stages & MOE_FFN_GATEUP) {
+        if (timing && timing->gateup0) MOE_TRY_CUDA(cudaEventRecord(timing->gateup0, s));
+        p.geo = pl.g1;
+        p.ranges = p.ws_ints + ws_ranges_off(E, T * k, 0);
+        MOE_TRY_CUDA(cudaLaunchKernel(k1, dim3(G1), dim3(GV_THREADS), args, smem1, s));
+        if (timing && timing->gateup1) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
+    }
+    if (stages & MOE_FFN_DOWN) {
+        if (timing && timing->down0) MOE_TRY_CUDA(cudaEventRecord(timing->down0, s));
+        p.geo = pl.g2;
+        p.ranges = p.ws_ints + ws_ranges_off(E, T * k, 1);
+        MOE_TRY_CUDA(cudaLaunchKernel(k2, dim3(G2), dim3(GV_THREADS), args, smem2, s));
+        if (timing && timing->down1) MOE_TRY_CUDA(cudaEventRecord(timing->down1, s));
+    }
     return MOE_OK;
 }
 

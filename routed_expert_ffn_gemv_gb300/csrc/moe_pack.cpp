@@ -2,10 +2,11 @@
 //
 // Canonical tensors are page 2's expert-major ffn_{gate,up,down}_exps layout: one
 // row per output feature, each row a run of quantised blocks along the reduction
-// dimension.  The slot image (layout in moe_common.cuh) is a byte permutation of
-// the same blocks: codes regrouped into 32-row tiles so that a warp's 16-byte loads
-// are contiguous, and block scales moved to their own region.  Page 5 (section 1.2)
-// keeps quantised blocks as they are on the GPU; so does this image.
+// dimension.  The slot image (layout in moe_common.cuh) holds the same blocks
+// regrouped: codes in 32-row tiles so that a warp's 16-byte loads are contiguous, each
+// 32-column block's scales right after its codes (any K range of a tile is one run of
+// bytes), and 8-bit codes in offset binary (q + 128).  Page 5 (section 1.2) keeps
+// quantised blocks as they are on the GPU; so does this image (no dequantisation).
 #include <string.h>
 
 #include "moe_common.cuh"
@@ -14,19 +15,19 @@ namespace {
 
 void pack_matrix(int qtype, int R, int K, const uint8_t *aos, uint8_t *dst) {
     const int NB = K / 32, BB = moe_block_bytes(qtype), SE = moe_scale_entry_bytes(qtype);
-    uint8_t *quant = dst;
-    uint8_t *scale = dst + moe_quant_bytes(qtype, R, K);
     for (int r = 0; r < R; ++r) {
         const int g = r / MOE_TILE_ROWS, lane = r % MOE_TILE_ROWS;
         for (int b = 0; b < NB; ++b) {
             const uint8_t *blk = aos + ((size_t)r * NB + b) * BB;
-            memcpy(scale + moe_scale_offset(qtype, K, g, b) + (size_t)lane * SE, blk, SE);
+            uint8_t *tb = dst + moe_tile_block_offset(qtype, K, g, b);
+            memcpy(tb + moe_scale_in_block(qtype, lane), blk, SE);
             if (qtype == MOE_Q8_0) {
-                for (int half = 0; half < 2; ++half)
-                    memcpy(quant + moe_piece_offset(qtype, K, g, 2 * b + half) + (size_t)lane * 16,
-                           blk + 2 + 16 * half, 16);
+                for (int half = 0; half < 2; ++half) {
+                    uint8_t *q = tb + moe_piece_in_block(half, lane);
+                    for (int i = 0; i < 16; ++i) q[i] = (uint8_t)(blk[2 + 16 * half + i] ^ 0x80);  // q + 128
+                }
             } else {
-                memcpy(quant + moe_piece_offset(qtype, K, g, b) + (size_t)lane * 16, blk + 4, 16);
+                memcpy(tb + moe_piece_in_block(0, lane), blk + 4, 16);
             }
         }
     }
@@ -34,19 +35,19 @@ void pack_matrix(int qtype, int R, int K, const uint8_t *aos, uint8_t *dst) {
 
 void unpack_matrix(int qtype, int R, int K, const uint8_t *src, uint8_t *aos) {
     const int NB = K / 32, BB = moe_block_bytes(qtype), SE = moe_scale_entry_bytes(qtype);
-    const uint8_t *quant = src;
-    const uint8_t *scale = src + moe_quant_bytes(qtype, R, K);
     for (int r = 0; r < R; ++r) {
         const int g = r / MOE_TILE_ROWS, lane = r % MOE_TILE_ROWS;
         for (int b = 0; b < NB; ++b) {
             uint8_t *blk = aos + ((size_t)r * NB + b) * BB;
-            memcpy(blk, scale + moe_scale_offset(qtype, K, g, b) + (size_t)lane * SE, SE);
+            const uint8_t *tb = src + moe_tile_block_offset(qtype, K, g, b);
+            memcpy(blk, tb + moe_scale_in_block(qtype, lane), SE);
             if (qtype == MOE_Q8_0) {
-                for (int half = 0; half < 2; ++half)
-                    memcpy(blk + 2 + 16 * half,
-                           quant + moe_piece_offset(qtype, K, g, 2 * b + half) + (size_t)lane * 16, 16);
+                for (int half = 0; half < 2; ++half) {
+                    const uint8_t *q = tb + moe_piece_in_block(half, lane);
+                    for (int i = 0; i < 16; ++i) blk[2 + 16 * half + i] = (uint8_t)(q[i] ^ 0x80);
+                }
             } else {
-                memcpy(blk + 4, quant + moe_piece_offset(qtype, K, g, b) + (size_t)lane * 16, 16);
+                memcpy(blk + 4, tb + moe_piece_in_block(0, lane), 16);
             }
         }
     }

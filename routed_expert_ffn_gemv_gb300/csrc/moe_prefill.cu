@@ -79,11 +79,11 @@ inline PfLayout pf_layout(int T, int H, int F, int E, int k) {
     return L;
 }
 
-// TMA tensor maps over the pool, one per (matrix, region): 64-bit words x 512-byte pieces
-// (or 32-lane scale groups) x 32-row tiles x slots, so one copy brings a stage's box of
-// several row tiles of one matrix.
+// TMA tensor maps over the pool, one per matrix: 64-bit words of a tile block (codes and
+// scales of 32 rows x 32 columns) x blocks x 32-row tiles x slots, so one copy brings a
+// stage's box of 2 blocks of several row tiles of one matrix.
 struct PfMaps {
-    CUtensorMap code[3], scale[3];  // gate, up, down
+    CUtensorMap blk[3];  // gate, up, down
 };
 
 struct PfParams {
@@ -252,21 +252,22 @@ __global__ void __launch_bounds__(256) pf_gather_kernel(const void *__restrict__
 
 // ------------------------------------------------------------------ dequant of one piece
 
-// Raw stage layout (both GEMMs): 8 row tiles of 32 weight rows x [codes of 2 blocks], then
-// 8 row tiles x [scales of 2 blocks].  GEMM 1: row tiles 0-3 gate, 4-7 up; GEMM 2: down.
+// Raw stage layout (both GEMMs): 8 row tiles of 32 weight rows x 2 tile blocks (each the
+// codes of 32 rows x 32 columns, then their 32 scale entries; slot image layout).  GEMM 1:
+// row tiles 0-3 gate, 4-7 up; GEMM 2: down.
 template <int QT> struct RawGeom {
-    static constexpr int QPB = QT == MOE_Q8_0 ? 2048 : 1024;  // code bytes per row tile (2 blocks)
-    static constexpr int SPB = 2 * 32 * (QT == MOE_Q8_0 ? 2 : 4);
-    static constexpr int BYTES = 8 * (QPB + SPB);
-    static constexpr int PPB = QT == MOE_Q8_0 ? 2 : 1;         // 16-byte pieces per block
+    static constexpr int TBB = QT == MOE_Q8_0 ? 1088 : 640;   // bytes of a tile block
+    static constexpr int SC = QT == MOE_Q8_0 ? 1024 : 512;    // its scale entries' offset
+    static constexpr int BYTES = 8 * 2 * TBB;
 };
 
 __device__ __forceinline__ __half2 u32_as_half2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 __device__ __forceinline__ uint32_t half2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
 // Dequantise (row, block) of the raw stage into the swizzled fp16 B tile (256 rows).
-//  q8_0: bytes x ^ 0x80 placed under the fp16 exponent of 1024 give 1152 + q exactly;
-//        subtracting 1152 leaves q, and one fp16 multiply by d rounds d*q once.
+//  q8_0: the offset-binary bytes q + 128 placed under the fp16 exponent of 1024 give
+//        1152 + q exactly; subtracting 1152 leaves q, and one fp16 multiply by d rounds d*q
+//        once.
 //  4-bit: nibble pairs (n, n+4) masked under the exponent of 1024 give 1024 + q; then
 //        q*d + m in one fp16 FMA (one rounding).
 template <int QT>
@@ -274,17 +275,16 @@ __device__ __forceinline__ void dequant_piece(const uint8_t *raw, int row, int b
     using G = RawGeom<QT>;
     const int rt = row >> 5, lr = row & 31;
     if constexpr (QT == MOE_Q8_0) {
-        const __half dh = __ushort_as_half(
-            *(const unsigned short *)(raw + 8 * G::QPB + rt * G::SPB + (blk * 32 + lr) * 2));
+        const uint8_t *tb = raw + (size_t)(rt * 2 + blk) * G::TBB;
+        const __half dh = __ushort_as_half(*(const unsigned short *)(tb + G::SC + moe_scale_pos(lr) * 2));
         const __half2 d2 = __halves2half2(dh, dh);
         const __half2 off = __float2half2_rn(1152.0f);
         uint4 q[2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) q[h] = *(const uint4 *)(raw + rt * G::QPB + ((2 * blk + h) * 32 + lr) * 16);
+        for (int h = 0; h < 2; ++h) q[h] = *(const uint4 *)(tb + moe_piece_in_block(h, lr));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const uint32_t wd[4] = {q[h].x ^ 0x80808080u, q[h].y ^ 0x80808080u, q[h].z ^ 0x80808080u,
-                                    q[h].w ^ 0x80808080u};
+            const uint32_t wd[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
             uint32_t o[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -297,8 +297,9 @@ __device__ __forceinline__ void dequant_piece(const uint8_t *raw, int row, int b
             *(uint4 *)(b_tile + sw128_offset(row, blk * 32 + 16 * h + 8)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
     } else {
-        const uint32_t dm = *(const uint32_t *)(raw + 8 * G::QPB + rt * G::SPB + (blk * 32 + lr) * 4);
-        const uint4 q = *(const uint4 *)(raw + rt * G::QPB + (blk * 32 + lr) * 16);
+        const uint8_t *tb = raw + (size_t)(rt * 2 + blk) * G::TBB;
+        const uint32_t dm = *(const uint32_t *)(tb + G::SC + moe_scale_pos(lr) * 4);
+        const uint4 q = *(const uint4 *)(tb + moe_piece_in_block(0, lr));
         const __half dh = __ushort_as_half((unsigned short)(dm & 0xFFFFu));
         const __half mh = __ushort_as_half((unsigned short)(dm >> 16));
         const __half2 d2 = __halves2half2(dh, dh), m2 = __halves2half2(mh, mh);
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
 
     if (warp == 0) {
         // ---------------- producer (lane 0): per K stage the token tile (one bulk copy) and, per
-        // weight matrix of the item, one TMA box of codes and one of scales
+        // weight matrix of the item, one TMA box of tile blocks
         if (lane == 0) {
             using Gq = RawGeom<QT>;
             int g = 0;
@@ -425,15 +426,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                     mbar_arrive_expect_tx(&r_full[s], Gq::BYTES + PF_TM * 128);
                     bulk_g2s(At(s), asrc + (size_t)kc * PF_TM * 128, PF_TM * 128, &r_full[s]);
                     if (DOWN) {
-                        tma_load_4d(RAW(s), &p.maps.code[2], 0, 2 * kc * Gq::PPB, 8 * m, slot, &r_full[s]);
-                        tma_load_4d(RAW(s) + 8 * Gq::QPB, &p.maps.scale[2], 0, 2 * kc, 8 * m, slot, &r_full[s]);
+                        tma_load_4d(RAW(s), &p.maps.blk[2], 0, 2 * kc, 8 * m, slot, &r_full[s]);
                     } else {
-                        for (int mt = 0; mt < 2; ++mt) {
-                            tma_load_4d(RAW(s) + 4 * mt * Gq::QPB, &p.maps.code[mt], 0, 2 * kc * Gq::PPB, 4 * m,
-                                        slot, &r_full[s]);
-                            tma_load_4d(RAW(s) + 8 * Gq::QPB + 4 * mt * Gq::SPB, &p.maps.scale[mt], 0, 2 * kc,
-                                        4 * m, slot, &r_full[s]);
-                        }
+                        for (int mt = 0; mt < 2; ++mt)
+                            tma_load_4d(RAW(s) + 4 * mt * 2 * Gq::TBB, &p.maps.blk[mt], 0, 2 * kc, 4 * m, slot,
+                                        &r_full[s]);
                     }
                 }
             }
@@ -594,40 +591,25 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// Maps of one matrix (mat: 0 gate, 1 up, 2 down) of every slot: codes as [slot][row tile]
-// [piece][64 x uint64], scales as [slot][row tile][block][32 lanes x entry / 8 x uint64];
-// boxes of 2 K blocks x `tiles` row tiles.
+// Map of one matrix (mat: 0 gate, 1 up, 2 down) of every slot: tile blocks as [slot][row
+// tile][block][TBB / 8 x uint64]; boxes of 2 K blocks x `tiles` row tiles.
 template <int QT>
-int encode_matrix_maps(const uint8_t *pool, int n_slots, size_t slot_bytes, int H, int F, int mat, int tiles,
-                       CUtensorMap *code, CUtensorMap *scale) {
+int encode_matrix_map(const uint8_t *pool, int n_slots, size_t slot_bytes, int H, int F, int mat, int tiles,
+                      CUtensorMap *map) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return MOE_ERR_UNSUPPORTED;
     using G = RawGeom<QT>;
     const int R = mat == 2 ? H : F, K = mat == 2 ? F : H;
-    const int NB = K / 32, P = NB * G::PPB, SE = moe_scale_entry_bytes(QT);
+    const int NB = K / 32;
     const uint8_t *base = pool + moe_expert_matrix_offset(QT, H, F, mat);
-    {
-        const cuuint64_t dims[4] = {64, (cuuint64_t)P, (cuuint64_t)(R / 32), (cuuint64_t)n_slots};
-        const cuuint64_t strides[3] = {512, (cuuint64_t)P * 512, (cuuint64_t)slot_bytes};
-        const cuuint32_t box[4] = {64, (cuuint32_t)(2 * G::PPB), (cuuint32_t)tiles, 1};
-        const cuuint32_t es[4] = {1, 1, 1, 1};
-        if (enc(code, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, (void *)base, dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return MOE_ERR_CUDA;
-    }
-    {
-        const uint8_t *sbase = base + moe_quant_bytes(QT, R, K);
-        const cuuint64_t dims[4] = {(cuuint64_t)(32 * SE / 8), (cuuint64_t)NB, (cuuint64_t)(R / 32),
-                                    (cuuint64_t)n_slots};
-        const cuuint64_t strides[3] = {(cuuint64_t)(32 * SE), (cuuint64_t)NB * 32 * SE, (cuuint64_t)slot_bytes};
-        const cuuint32_t box[4] = {(cuuint32_t)(32 * SE / 8), 2, (cuuint32_t)tiles, 1};
-        const cuuint32_t es[4] = {1, 1, 1, 1};
-        if (enc(scale, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, (void *)sbase, dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return MOE_ERR_CUDA;
-    }
+    const cuuint64_t dims[4] = {(cuuint64_t)(G::TBB / 8), (cuuint64_t)NB, (cuuint64_t)(R / 32), (cuuint64_t)n_slots};
+    const cuuint64_t strides[3] = {(cuuint64_t)G::TBB, (cuuint64_t)NB * G::TBB, (cuuint64_t)slot_bytes};
+    const cuuint32_t box[4] = {(cuuint32_t)(G::TBB / 8), 2, (cuuint32_t)tiles, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, (void *)base, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MOE_ERR_CUDA;
     return MOE_OK;
 }
 
@@ -647,8 +629,8 @@ int launch_gemms(PfParams &p, int max_tiles, cudaStream_t s, const moe_ffn_timin
     using PG = PfGeom<QT>;
     if (PG::SMEM > 227 * 1024) return MOE_ERR_UNSUPPORTED;
     for (int mat = 0; mat < 3; ++mat) {
-        const int rc = encode_matrix_maps<QT>(p.pool, p.n_slots, p.slot_bytes, p.H, p.F, mat, mat == 2 ? 8 : 4,
-                                              &p.maps.code[mat], &p.maps.scale[mat]);
+        const int rc = encode_matrix_map<QT>(p.pool, p.n_slots, p.slot_bytes, p.H, p.F, mat, mat == 2 ? 8 : 4,
+                                             &p.maps.blk[mat]);
         if (rc != MOE_OK) return rc;
     }
     MOE_TRY_CUDA(cudaFuncSetAttribute(pf_gemm_kernel<QT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,

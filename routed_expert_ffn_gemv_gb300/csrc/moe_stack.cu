@@ -513,6 +513,77 @@ extern "C" int moe_stack_set_profile(moe_stack *st, int level) {
     return MOE_OK;
 }
 
+extern "C" int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, int reps, moe_gemv_timing *out,
+                                     moe_stream_t sv) {
+    MOE_CHECK(st && x_in && out && reps >= 1);
+    MOE_CHECK(T >= 1 && T <= st->d.max_T && T <= MOE_DECODE_MAX_T);
+    const moe_stack_desc &d = st->d;
+    if (d.n_groups != 0 || !d.resident_pool) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = moe_cuda_stream(sv);
+    const int L = d.n_layers, R = T * d.k;
+    const size_t wsb = moe_decode_workspace_bytes(T, d.H, d.F, d.qtype, d.E, d.k);
+    const size_t per = align256((size_t)R * 4) * 2 + align256((size_t)R * d.H * 4) + align256(wsb);
+    char *buf = nullptr;
+    MOE_TRY_CUDA(cudaMalloc(&buf, per * L));
+    cudaEvent_t ev[3] = {};
+    int rc = MOE_OK;
+    auto lay = [&](int l, int32_t **ids, float **w, float **partial, void **ws) {
+        char *b = buf + per * l;
+        *ids = (int32_t *)b;
+        *w = (float *)(b + align256((size_t)R * 4));
+        *partial = (float *)(b + 2 * align256((size_t)R * 4));
+        *ws = b + 2 * align256((size_t)R * 4) + align256((size_t)R * d.H * 4);
+    };
+    auto stage = [&](int l, int what) {
+        int32_t *ids; float *w, *partial; void *ws;
+        lay(l, &ids, &w, &partial, &ws);
+        const void *pool = (const char *)d.resident_pool + (size_t)l * d.E * d.slot_bytes;
+        return moe_expert_ffn_stages(x_in, MOE_F32, T, d.H, d.F, d.qtype, d.E, d.k, ids, w, nullptr, d.E, pool,
+                                     d.slot_bytes, nullptr, 0, nullptr, partial, ws, wsb, s, nullptr, what);
+    };
+    for (int i = 0; i < 3 && rc == MOE_OK; ++i)
+        if (cudaEventCreate(&ev[i]) != cudaSuccess) rc = MOE_ERR_CUDA;
+    for (int l = 0; l < L && rc == MOE_OK; ++l) {  // routing of every layer, then its permute
+        int32_t *ids; float *w, *partial; void *ws;
+        lay(l, &ids, &w, &partial, &ws);
+        rc = moe_router_topk(x_in, MOE_F32, T, d.H, st->w_router[l], st->bias[l], d.E, d.k, ids, w, nullptr, sv);
+        if (rc == MOE_OK) rc = stage(l, MOE_FFN_PERMUTE);
+    }
+    for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_GATEUP);  // warm-up
+    for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_DOWN);
+    if (rc == MOE_OK && cudaEventRecord(ev[0], s) != cudaSuccess) rc = MOE_ERR_CUDA;
+    for (int r = 0; r < reps && rc == MOE_OK; ++r)
+        for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_GATEUP);
+    if (rc == MOE_OK && cudaEventRecord(ev[1], s) != cudaSuccess) rc = MOE_ERR_CUDA;
+    for (int r = 0; r < reps && rc == MOE_OK; ++r)
+        for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_DOWN);
+    if (rc == MOE_OK && cudaEventRecord(ev[2], s) != cudaSuccess) rc = MOE_ERR_CUDA;
+    if (rc == MOE_OK && cudaStreamSynchronize(s) != cudaSuccess) rc = MOE_ERR_CUDA;
+    if (rc == MOE_OK) {
+        float t1 = 0.f, t2 = 0.f;
+        cudaEventElapsedTime(&t1, ev[0], ev[1]);
+        cudaEventElapsedTime(&t2, ev[1], ev[2]);
+        double nact = 0.0;
+        for (int l = 0; l < L && rc == MOE_OK; ++l) {
+            int32_t n = 0;
+            if (cudaMemcpy(&n, buf + per * l + 2 * align256((size_t)R * 4) + align256((size_t)R * d.H * 4), 4,
+                           cudaMemcpyDeviceToHost) != cudaSuccess)
+                rc = MOE_ERR_CUDA;
+            nact += n;
+        }
+        const int n_l = reps * L;
+        out->gateup_us = 1e3 * t1 / n_l;
+        out->down_us = 1e3 * t2 / n_l;
+        out->gateup_bytes = nact / L * 2 * moe_matrix_bytes(d.qtype, d.F, d.H);
+        out->down_bytes = nact / L * moe_matrix_bytes(d.qtype, d.H, d.F);
+        out->launches = n_l;
+    }
+    for (int i = 0; i < 3; ++i)
+        if (ev[i]) cudaEventDestroy(ev[i]);
+    cudaFree(buf);
+    return rc;
+}
+
 extern "C" void moe_stack_destroy(moe_stack *st) {
     if (!st) return;
     if (st->last_stream) cudaStreamSynchronize(st->last_stream);

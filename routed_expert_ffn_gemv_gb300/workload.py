@@ -171,6 +171,12 @@ class Stack:
     def profile_reset(self) -> None:
         L.moe_stack_profile_reset(self.handle)
 
+    def gemv_timing(self, x: torch.Tensor, reps: int, stream=None) -> dict:
+        """The decode GEMV kernels timed alone (resident stacks): every layer's router and
+        permute for x, then reps rounds of back-to-back gate/up launches over all layers,
+        then of down launches; average microseconds and bytes per launch."""
+        return L.moe_stack_gemv_timing(self.handle, x, x.shape[0], reps, stream)
+
     def reset_caches(self) -> None:
         for c in self.caches:
             L.moe_cache_reset(c)

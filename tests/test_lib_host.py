@@ -48,28 +48,36 @@ def test_pack_unpack_round_trip_and_layout(lib, qtype):
     off = (-img.ctypes.data) % 16
     view = img[off:off + n]
     assert L.moe_pack_expert(qtype, 64, 96, g.ctypes.data, u.ctypes.data, d.ctypes.data, view.ctypes.data) == n
-    # a permutation of the same bytes
-    assert np.array_equal(np.sort(view), np.sort(np.concatenate([g, u, d])))
+    # the same blocks regrouped; 8-bit codes in offset binary (q + 128), scales unchanged
+    BB = 34 if qtype == 0 else 20
+    canon = np.concatenate([g, u, d])
+    if qtype == 0:
+        canon = canon.reshape(-1, BB).copy()
+        canon[:, 2:] ^= 0x80
+        canon = canon.reshape(-1)
+    assert np.array_equal(np.sort(view), np.sort(canon))
     g2, u2, d2 = np.zeros_like(g), np.zeros_like(u), np.zeros_like(d)
     L.moe_unpack_expert(qtype, 64, 96, view.ctypes.data, g2.ctypes.data, u2.ctypes.data, d2.ctypes.data)
     assert np.array_equal(g, g2) and np.array_equal(u, u2) and np.array_equal(d, d2)
-    # documented layout: gate row r, block b -> tile g = r // 32, lane = r % 32
-    BB = 34 if qtype == 0 else 20
-    K, nb = 64, 2
+    # documented layout: gate row r, block b -> tile g = r // 32, lane = r % 32, tile block
+    # (g, b) at (g * nb + b) * TBB: codes (piece p of lane l at 512 p + 16 l), then the scale
+    # entries with lane l at position 4 (l % 8) + l // 8
+    nb = 2
     r, b = 37, 1
     blk = g[(r * nb + b) * BB:(r * nb + b + 1) * BB]
     tile, lane = r // 32, r % 32
+    pos = 4 * (lane % 8) + lane // 8
     if qtype == 0:
-        P = K // 16
-        p = 2 * b + 1   # second half of the block: codes 16..31
-        q_off = ((tile * P + p) * 32 + lane) * 16
-        assert np.array_equal(view[q_off:q_off + 16], blk[2 + 16:2 + 32])
-        s_off = 96 * 64 + ((tile * nb + b) * 32 + lane) * 2
+        tb = (tile * nb + b) * 1088
+        q_off = tb + 512 + lane * 16  # second piece of the block: codes 16..31
+        assert np.array_equal(view[q_off:q_off + 16], blk[2 + 16:2 + 32] ^ 0x80)
+        s_off = tb + 1024 + pos * 2
         assert np.array_equal(view[s_off:s_off + 2], blk[0:2])
     else:
-        q_off = ((tile * nb + b) * 32 + lane) * 16
+        tb = (tile * nb + b) * 640
+        q_off = tb + lane * 16
         assert np.array_equal(view[q_off:q_off + 16], blk[4:20])
-        s_off = 96 * 64 // 2 + ((tile * nb + b) * 32 + lane) * 4
+        s_off = tb + 512 + pos * 4
         assert np.array_equal(view[s_off:s_off + 4], blk[0:4])
 
 

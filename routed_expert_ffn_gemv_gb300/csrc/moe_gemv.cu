@@ -23,9 +23,9 @@
 //  * activations enter the tensor core as fp16 hi + lo parts of a per-token power-of-two
 //    scaled copy (about 22 significant bits), staged once per (virtual expert, K range) in
 //    shared memory for all warps of the CTA;
-//  * the warp's epilogue forms h = silu(gate) * up (G1, whole K), stores the two partial
-//    sums (G1, K split; the down kernel sums them in a fixed order while staging), or writes
-//    w[r] * (Wd h) for each route r (G2);
+//  * the warp's epilogue forms h = silu(gate) * up (G1, whole K), or stores the two partial
+//    sums (G1, K split) and, if its unit is the last of the row tile's K ranges to finish,
+//    sums all of them in K order and forms h; or writes w[r] * (Wd h) for each route r (G2);
 //  * an expert that missed in a device-managed pool is read from its pinned host image and
 //    written through to its slot by the warps that use the bytes ("fill" units).
 #include <cuda_bf16.h>
@@ -158,7 +158,8 @@ __host__ __device__ inline int ws_ranges_off(int E, int R, int which) {
 struct WsLayout {
     size_t ints_off, info_off;
     size_t gu_off;     // float [KS][2][R][F] gate/up partial sums (KS > 1)
-    size_t h_off;      // float [R][F] silu(gate) * up (KS == 1)
+    size_t h_off;      // float [R][F] silu(gate) * up
+    size_t cnt_off;    // int [virtual experts][F/32] K ranges done per gate/up row tile (KS > 1)
     size_t total;
 };
 
@@ -173,8 +174,8 @@ inline WsLayout ws_layout(int T, int H, int F, int qtype, int E, int k) {
     L.gu_off = L.info_off + ((size_t)gv_n_virt_max(T, E, k) * sizeof(ActInfo) + 255) / 256 * 256;
     const size_t gu = pl.KS > 1 ? (size_t)pl.KS * 2 * R * F * 4 : 0;
     L.h_off = L.gu_off + (gu + 255) / 256 * 256;
-    const size_t hb = pl.KS > 1 ? 0 : R * F * 4;
-    L.total = L.h_off + (hb + 255) / 256 * 256;
+    L.cnt_off = L.h_off + (R * F * 4 + 255) / 256 * 256;
+    L.total = L.cnt_off + ((size_t)gv_n_virt_max(T, E, k) * (F / 32) * 4 + 255) / 256 * 256;
     return L;
 }
 
@@ -188,6 +189,7 @@ struct FfnParams {
     float *gu;
     float *h;
     float *partial;
+    int *cnt;               // K-range counters of the gate/up row tiles (KS > 1)
     int *status;
     int x_vec;              // x is 16-byte aligned: vector loads
     GvGeom geo;             // this launch's geometry
@@ -349,32 +351,13 @@ __device__ __forceinline__ void finish_acc(float (&acc)[NTL][2][4], float i0, fl
 // ------------------------------------------------------------------ staging the activations
 
 // Eight consecutive activations of one source row at column col: G1 reads row `row` of x
-// (a token), G2 row `row` (a route position) of h, or silu(sum gate) * (sum up) of the
-// K-split partial sums in a fixed order.
+// (a token), G2 row `row` (a route position) of h.
 template <int XT, bool DOWN>
 __device__ __forceinline__ void act_load8(const FfnParams &p, int row, int col, float (&v)[8]) {
     if (DOWN) {
         const size_t q = (size_t)row * p.F + col;
-        if (p.KS == 1) {
-            const float4 a = *(const float4 *)(p.h + q), b = *(const float4 *)(p.h + q + 4);
-            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-        } else {
-            float g[8], u[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) g[e] = u[e] = 0.f;
-            for (int ks = 0; ks < p.KS; ++ks) {
-                const float *gp = p.gu + ((size_t)ks * 2 + 0) * p.RT * p.F + q;
-                const float *up = p.gu + ((size_t)ks * 2 + 1) * p.RT * p.F + q;
-                const float4 g0 = *(const float4 *)gp, g1 = *(const float4 *)(gp + 4);
-                const float4 u0 = *(const float4 *)up, u1 = *(const float4 *)(up + 4);
-                g[0] += g0.x; g[1] += g0.y; g[2] += g0.z; g[3] += g0.w;
-                g[4] += g1.x; g[5] += g1.y; g[6] += g1.z; g[7] += g1.w;
-                u[0] += u0.x; u[1] += u0.y; u[2] += u0.z; u[3] += u0.w;
-                u[4] += u1.x; u[5] += u1.y; u[6] += u1.z; u[7] += u1.w;
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = silu_mul(g[e], u[e]);
-        }
+        const float4 a = *(const float4 *)(p.h + q), b = *(const float4 *)(p.h + q + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     } else {
         const size_t off = (size_t)row * p.H + col;
         if (XT == MOE_BF16) {
@@ -740,6 +723,42 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
                     }
                 }
             }
+            if (!DOWN && p.KS > 1) {
+                // The last of the KS units of row tile g to finish forms h = silu(sum gate) *
+                // (sum up) over the K ranges in order (a fixed order: the same h whichever unit
+                // comes last) and resets the counter for the next launch.
+                __threadfence();  // this unit's partial sums, before its arrival is counted
+                int old = 0;
+                if (lane == 0) old = atomicAdd(&p.cnt[v * (p.F / 32) + g], 1);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                if (old == p.KS - 1) {
+                    __threadfence();  // the other units' partial sums, after their counted arrivals
+                    const int row = 32 * g + lane;
+#pragma unroll
+                    for (int t = 0; t < GV_TOK; ++t) {
+                        if (t >= n_e) break;
+                        const size_t q = (size_t)(pos0 + t) * p.F + row;
+                        float gs = 0.f, us = 0.f;
+                        for (int k0 = 0; k0 < p.KS; k0 += 4) {  // four K ranges' loads in flight
+                            float gp[4], up[4];
+#pragma unroll
+                            for (int k2 = 0; k2 < 4; ++k2)
+                                if (k0 + k2 < p.KS) {
+                                    gp[k2] = __ldcg(p.gu + ((size_t)(k0 + k2) * 2 + 0) * p.RT * p.F + q);
+                                    up[k2] = __ldcg(p.gu + ((size_t)(k0 + k2) * 2 + 1) * p.RT * p.F + q);
+                                }
+#pragma unroll
+                            for (int k2 = 0; k2 < 4; ++k2)
+                                if (k0 + k2 < p.KS) {
+                                    gs += gp[k2];
+                                    us += up[k2];
+                                }
+                        }
+                        p.h[q] = silu_mul(gs, us);
+                    }
+                    if (lane == 0) p.cnt[v * (p.F / 32) + g] = 0;
+                }
+            }
         }
         a = e;
     }
@@ -786,7 +805,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
                                                       const uint8_t *pool, size_t slot_bytes,
                                                       const unsigned long long *__restrict__ fill_src,
                                                       int vt, int G1, int per_v1, int G2, int per_v2,
-                                                      int *status) {
+                                                      int *__restrict__ kcnt, int n_cnt_per_v, int *status) {
     __shared__ int cnt[MOE_MAX_E], off[MOE_MAX_E + 1], run[MOE_MAX_E];
     __shared__ int vb[MOE_MAX_E + 1];
     __shared__ unsigned char insub[MOE_MAX_E];
@@ -835,6 +854,8 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
         n_act = na;
     }
     __syncthreads();
+    if (kcnt)  // the gate/up kernel's K-range counters start at 0 (its last arrivals reset them)
+        for (int i = tid; i < vb[n_act] * n_cnt_per_v; i += 256) kcnt[i] = 0;
     int *routes = ints + ws_routes_off(E);
     for (int c0 = 0; c0 < R; c0 += 256) {
         const int r = c0 + tid;
@@ -1094,6 +1115,7 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
     p.info = (const ActInfo *)((char *)workspace + W.info_off);
     p.gu = (float *)((char *)workspace + W.gu_off);
     p.h = (float *)((char *)workspace + W.h_off);
+    p.cnt = (int *)((char *)workspace + W.cnt_off);
     p.partial = partial;
     p.status = moe_status_word_device_ptr();
     p.x_vec = ((uintptr_t)x & 15) == 0;
@@ -1104,7 +1126,8 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
                                      (int32_t *)((char *)workspace + W.ints_off),
                                      (ActInfo *)((char *)workspace + W.info_off), d_slot_table, n_slots,
                                      (const uint8_t *)pool, slot_bytes, (const unsigned long long *)d_fill_src,
-                                     GV_TOK, G1, per_v1, G2, per_v2, p.status);
+                                     GV_TOK, G1, per_v1, G2, per_v2, pl.KS > 1 ? p.cnt : nullptr, RTF,
+                                     p.status);
     MOE_TRY_CUDA(cudaGetLastError());
     if (timing && timing->permute1) MOE_TRY_CUDA(cudaEventRecord(timing->permute1, s));
     }

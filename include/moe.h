@@ -407,8 +407,10 @@ int moe_stack_set_profile(moe_stack *st, int level);
  * moe_stack_gemv_timing — the decode GEMV kernels of a resident stack (n_groups == 0)
  * timed alone: the router and the token-to-expert permute of every layer run first for the
  * batch x_in (device [T][H] fp32, the same FFN input for each layer, 1 <= T <=
- * MOE_DECODE_MAX_T); then, on stream s, `reps` rounds of the gate/up GEMV of every layer are
- * launched back to back between two CUDA events, then `reps` rounds of the down GEMV.
+ * MOE_DECODE_MAX_T); then, on stream s behind a GPU spacer (a bounded spin, so that every
+ * timed launch is queued before the first starts), `reps` rounds of the gate/up GEMV of
+ * every layer are launched back to back between two CUDA events, then `reps` rounds of the
+ * down GEMV.
  * Consecutive launches read different layers' experts, so no launch finds the previous
  * one's weights in L2.  Results: the average time of one launch (microseconds, launch gaps
  * included, no events between launches) and the quantised bytes of the selected experts

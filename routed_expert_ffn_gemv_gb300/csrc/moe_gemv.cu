@@ -393,21 +393,21 @@ __device__ __forceinline__ void act_load8(const FfnParams &p, int row, int col, 
 // fp16 hi = rn(y) (row 2t) and lo = rn(y - hi) (row 2t + 1); 1/sc at inv[t]; for the 4-bit
 // format the fp32 block sums of y at asum[b][t] (row stride NTS) and the columns of each
 // group of 8 in the order 0 4 1 5 2 6 3 7.
-template <int QT, int XT, bool DOWN>
+template <int QT, int XT, bool DOWN, typename Mid>
 __device__ void stage_row(const FfnParams &p, int row, int c0, int Kr, unsigned char *slot, int NTS, int t,
-                          int lane) {
+                          int lane, Mid &&mid) {
     const int RS = gv_row_stride(Kr);
     float amax = 0.f;
     float keep[2][8];  // the first 512 columns stay in registers for the second pass
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int col = 256 * i + 8 * lane;
-        if (col < Kr) {
-            act_load8<XT, DOWN>(p, row, c0 + col, keep[i]);
+    for (int i = 0; i < 2; ++i)
+        if (256 * i + 8 * lane < Kr) act_load8<XT, DOWN>(p, row, c0 + 256 * i + 8 * lane, keep[i]);
+    mid();  // the first loads are in flight
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        if (256 * i + 8 * lane < Kr)
 #pragma unroll
             for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(keep[i][e]));
-        }
-    }
     for (int base = 512; base < Kr; base += 256) {
         const int col = base + 8 * lane;
         if (col < Kr) {
@@ -602,6 +602,17 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
     };
 
     int J_issued = 0;  // chunks issued by this warp (lane 0's count)
+    bool dead = false;   // a wait ran out: no more waits, copies or outputs
+    // lane 0: issue chunks until `limit` have been issued (chunk X goes to stage X % S, which
+    // chunk X - S has left)
+    auto top_up = [&](int limit) {
+        if (lane != 0 || dead) return;
+        while (J_issued < limit && pc_u < u1) {
+            issue(J_issued % S);
+            pc_next();
+            ++J_issued;
+        }
+    };
     if (lane == 0) {
         pc_first(u0);
         if (pc_u < u1) pc_info();
@@ -610,7 +621,6 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
 
     int J = 0;           // chunks this warp has reached
     int J_done = 0;      // chunks whose stage completed (waited on)
-    bool dead = false;   // a wait ran out: no more waits, copies or outputs
     for (int a = u0; a < u1;) {
         const int e = phase_end(a);
         const int pr0 = a / upp, npr = (e - 1) / upp - pr0 + 1;
@@ -619,6 +629,13 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
         // pair's K range, read from x without the routing metadata.  Down: the routes of the
         // pair's virtual expert, read from h (or the K-split sums).  Row 0's item also writes
         // the slot header.
+        // the warp's first chunk goes out once its first staging loads are in flight (or at
+        // once for a warp without staging work), ahead of the conversion; the rest of its ring
+        // is filled at its first wait, so that every warp's first chunk is ahead of them in the
+        // copy engine's queue
+        auto first_issue = [&]() {
+            if (a == u0) top_up(1);
+        };
         for (int it = warp; it < npr * NTS; it += GV_WARPS) {
             const int i = it / NTS, t = it - i * NTS;
             const int pr = pr0 + i, v = pr / kspp, ks = pr - v * kspp;
@@ -629,22 +646,17 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
                 if (t == 0 && lane == 0) hdr->in = in;
                 if (t < in.n_e) {
                     if (lane == 0) hdr->w[t] = p.weights[in.rt[t]];
-                    stage_row<QT, XT, DOWN>(p, in.pos0 + t, 0, Kr, slot, NTS, t, lane);
+                    stage_row<QT, XT, DOWN>(p, in.pos0 + t, 0, Kr, slot, NTS, t, lane, first_issue);
                 } else if (QT == MOE_Q4_SM) {
                     float *asum = (float *)(slot + GV_ASUM_OFF(NTS, RS));
                     for (int b = lane; b < nbr; b += 32) asum[b * NTS + t] = 0.f;
                 }
             } else {
                 if (t == 0 && lane == 0) hdr->in = p.info[v];
-                stage_row<QT, XT, DOWN>(p, t, ks * Kr, Kr, slot, NTS, t, lane);
+                stage_row<QT, XT, DOWN>(p, t, ks * Kr, Kr, slot, NTS, t, lane, first_issue);
             }
         }
-        if (a == u0 && lane == 0)
-            for (int s = 0; s < S && pc_u < u1; ++s) {
-                issue(s);
-                pc_next();
-                ++J_issued;
-            }
+        first_issue();
         __syncthreads();
 
         for (int u = a + warp; u < e; u += GV_WARPS) {
@@ -674,6 +686,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
             for (int ch = 0; ch < nch; ++ch, ++J) {
                 const int stg = J % S;
                 unsigned char *st = ring + (size_t)stg * G.chunk_bytes;
+                top_up(J + S);
                 if (!dead) {
                     const bool ok = mbar_wait_bounded(&bars[stg], (J / S) & 1, p.status);
                     if (__all_sync(0xffffffffu, ok)) J_done = J + 1;
@@ -691,11 +704,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
                     chunk_dot<QT, NTL>(st, tb, cb, brow + (size_t)64 * ch * CB, a0, a1, NTS, lane, acc);
                 }
                 __syncwarp();  // every lane is done with the stage
-                if (lane == 0 && !dead && pc_u < u1) {
-                    issue(J_issued % S);
-                    pc_next();
-                    ++J_issued;
-                }
+                top_up(J + 1 + S);
             }
             if (dead || n_e == 0) continue;
             const float *inv = (const float *)(slot + GV_INV_OFF(NTS, RS));

@@ -5,6 +5,7 @@
 // that were already resident while the misses upload -> wait for the uploads -> FFN over
 // the missed experts -> release the slots -> combine with the residual (and the shared
 // experts, page 3: always-resident experts outside the pool).
+#include <algorithm>
 #include <chrono>
 #include <vector>
 
@@ -513,6 +514,18 @@ extern "C" int moe_stack_set_profile(moe_stack *st, int level) {
     return MOE_OK;
 }
 
+namespace {
+// A GPU spacer: one warp spinning for about `ns` nanoseconds of wall time (bounded), so that
+// the host has queued every timed launch before the first of them can start.
+__global__ void spacer_kernel(unsigned long long ns) {
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    do {
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    } while (t - t0 < ns);
+}
+}  // namespace
+
 extern "C" int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, int reps, moe_gemv_timing *out,
                                      moe_stream_t sv) {
     MOE_CHECK(st && x_in && out && reps >= 1);
@@ -551,6 +564,11 @@ extern "C" int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, in
     }
     for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_GATEUP);  // warm-up
     for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_DOWN);
+    if (rc == MOE_OK) {  // about 40 us of host time per launch to queue, at least 2 ms
+        const unsigned long long ns = std::max(2000000ull, 40000ull * 2 * (unsigned long long)reps * L);
+        spacer_kernel<<<1, 32, 0, s>>>(ns);
+        if (cudaGetLastError() != cudaSuccess) rc = MOE_ERR_CUDA;
+    }
     if (rc == MOE_OK && cudaEventRecord(ev[0], s) != cudaSuccess) rc = MOE_ERR_CUDA;
     for (int r = 0; r < reps && rc == MOE_OK; ++r)
         for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_GATEUP);

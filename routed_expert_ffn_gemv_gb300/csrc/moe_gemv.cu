@@ -54,10 +54,12 @@
 
 namespace {
 
-// Work of one unit of a virtual expert with n_e tokens, in units of a token's dot products:
-// the unit's bytes and dequantisation cost about as much as GV_COST_MEM tokens.
-#define GV_COST_MEM 4
-__host__ __device__ inline int unit_cost(int n_e) { return GV_COST_MEM + n_e; }
+// Work of one unit of a virtual expert with n_e routes, for balancing the CTAs' ranges: its
+// bytes, dequantisation and MMAs do not depend on n_e (the MMA computes all 8 columns of a
+// virtual expert), so every unit weighs GV_COST_MEM and routes GV_COST_TOK each.
+#define GV_COST_MEM 1
+#define GV_COST_TOK 0
+__host__ __device__ inline int unit_cost(int n_e) { return GV_COST_MEM + GV_COST_TOK * n_e; }
 
 // ------------------------------------------------------------------ launch plan
 
@@ -782,10 +784,10 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
 // First unit whose start cost is >= x.  Active expert a has nv(a) = vb[a+1] - vb[a] virtual
 // experts, all of vt routes but the last; each of their per_v units costs
 // unit_cost(routes), so a's first unit starts at cost per_v * Q[a] with
-// Q[a] = GV_COST_MEM * vb[a] + aoff[a].
+// Q[a] = GV_COST_MEM * vb[a] + GV_COST_TOK * aoff[a].
 __device__ __forceinline__ int unit_at_cost(long long x, int n_act, int per_v, int vt, const int *vb,
                                             const int *aoff) {
-    auto Q = [&](int a) { return (long long)GV_COST_MEM * vb[a] + aoff[a]; };
+    auto Q = [&](int a) { return (long long)GV_COST_MEM * vb[a] + (long long)GV_COST_TOK * aoff[a]; };
     if (x >= per_v * Q(n_act)) return vb[n_act] * per_v;
     int lo = 0, hi = n_act - 1;  // largest a with per_v * Q[a] <= x
     while (lo < hi) {
@@ -911,8 +913,8 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
     __syncthreads();
     {
         int *r1 = ints + ws_ranges_off(E, R, 0), *r2 = ints + ws_ranges_off(E, R, 1);
-        const long long C1 = (long long)per_v1 * (GV_COST_MEM * vb[n_act] + aoff[n_act]);
-        const long long C2 = (long long)per_v2 * (GV_COST_MEM * vb[n_act] + aoff[n_act]);
+        const long long Cv = (long long)GV_COST_MEM * vb[n_act] + (long long)GV_COST_TOK * aoff[n_act];
+        const long long C1 = (long long)per_v1 * Cv, C2 = (long long)per_v2 * Cv;
         for (int c = tid; c <= G1; c += 256) r1[c] = unit_at_cost(C1 * c / G1, n_act, per_v1, vt, vb, aoff);
         for (int c = tid; c <= G2; c += 256) r2[c] = unit_at_cost(C2 * c / G2, n_act, per_v2, vt, vb, aoff);
     }

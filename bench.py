@@ -220,6 +220,7 @@ def gemv_roofline(cfg, T, torch, stream, steps=40, warmup=5):
     st.close()
     return {"gateup_ms_per_launch": r["gateup_us"] / 1e3, "gateup_bytes_per_launch": r["gateup_bytes"],
             "down_ms_per_launch": r["down_us"] / 1e3, "down_bytes_per_launch": r["down_bytes"],
+            "reduce_ms_per_launch": r["reduce_us"] / 1e3,
             "launches": int(r["launches"]), "steps": steps}
 
 
@@ -427,6 +428,8 @@ def run_gpu(args, world, rank, local):
                 "down_kernel": {"achieved_gbs": dn_gbs, "frac": dn_gbs / peaks["hbm_gbs"],
                                 "ms_per_launch": gv["down_ms_per_launch"],
                                 "algorithmic_bytes_per_launch": gv["down_bytes_per_launch"]},
+                "ks_reduce_kernel_ms_per_launch": gv["reduce_ms_per_launch"],
+                "ffn_gemv_ms_per_layer": gu_ms_launch + gv["reduce_ms_per_launch"] + gv["down_ms_per_launch"],
                 "measured_in": ("HBM-resident stack (all %d x %d expert images in HBM, above L2), batch %d; "
                                 "each layer's gate/up GEMV launched back to back over all layers, CUDA events "
                                 "on the launching stream around the rounds (launch gaps included)"

@@ -410,7 +410,7 @@ int moe_stack_set_profile(moe_stack *st, int level);
  * MOE_DECODE_MAX_T); then, on stream s behind a GPU spacer (a bounded spin, so that every
  * timed launch is queued before the first starts), `reps` rounds of the gate/up GEMV of
  * every layer are launched back to back between two CUDA events, then `reps` rounds of the
- * down GEMV.
+ * K-split reduce (if any), then `reps` rounds of the down GEMV.
  * Consecutive launches read different layers' experts, so no launch finds the previous
  * one's weights in L2.  Results: the average time of one launch (microseconds, launch gaps
  * included, no events between launches) and the quantised bytes of the selected experts
@@ -422,6 +422,8 @@ typedef struct moe_gemv_timing {
     double gateup_us, down_us;        /* average per launch */
     double gateup_bytes, down_bytes;  /* average per launch */
     int launches;                     /* per kernel: reps * layers */
+    double reduce_us;                 /* the K-split reduce between them (0 launches when the
+                                         gate/up GEMV does not split K), timed the same way */
 } moe_gemv_timing;
 int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, int reps, moe_gemv_timing *out,
                           moe_stream_t s);

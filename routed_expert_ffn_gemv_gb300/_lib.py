@@ -99,7 +99,8 @@ class StackProfile(ctypes.Structure):
 
 class GemvTiming(ctypes.Structure):
     _fields_ = [("gateup_us", ctypes.c_double), ("down_us", ctypes.c_double),
-                ("gateup_bytes", ctypes.c_double), ("down_bytes", ctypes.c_double), ("launches", _i)]
+                ("gateup_bytes", ctypes.c_double), ("down_bytes", ctypes.c_double), ("launches", _i),
+                ("reduce_us", ctypes.c_double)]
 
     def as_dict(self):
         return {f[0]: getattr(self, f[0]) for f in self._fields_}

@@ -120,9 +120,12 @@ int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype
 // The stages of one decode-path FFN call (T <= MOE_DECODE_MAX_T): a later stage reads what
 // the earlier stages of the same call left in the workspace.
 #define MOE_FFN_PERMUTE 1
-#define MOE_FFN_GATEUP 2
+#define MOE_FFN_GATEUP 2   // the gate/up GEMV
 #define MOE_FFN_DOWN 4
-#define MOE_FFN_ALL 7
+#define MOE_FFN_REDUCE 8   // h from the gate/up kernel's K-split partial sums (no-op without a split)
+#define MOE_FFN_ALL 15
+// Kernels one decode-path FFN call (T <= MOE_DECODE_MAX_T, all stages) launches.
+int moe_decode_ffn_launches(int T, int H, int F, int qtype, int E, int k);
 int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
                           const int32_t *ids, const float *weights, const int32_t *d_slot_table,
                           int n_slots, const void *pool, size_t slot_bytes,

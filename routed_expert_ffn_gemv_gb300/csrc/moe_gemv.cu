@@ -23,9 +23,9 @@
 //  * activations enter the tensor core as fp16 hi + lo parts of a per-token power-of-two
 //    scaled copy (about 22 significant bits), staged once per (virtual expert, K range) in
 //    shared memory for all warps of the CTA;
-//  * the warp's epilogue forms h = silu(gate) * up (G1, whole K), or stores the two partial
-//    sums (G1, K split) and, if its unit is the last of the row tile's K ranges to finish,
-//    sums all of them in K order and forms h; or writes w[r] * (Wd h) for each route r (G2);
+//  * the warp's epilogue forms h = silu(gate) * up (G1, whole K) or stores the two partial
+//    sums (G1, K split; a small kernel between the GEMVs sums them in K order and forms h),
+//    or writes w[r] * (Wd h) for each route r (G2);
 //  * an expert that missed in a device-managed pool is read from its pinned host image and
 //    written through to its slot by the warps that use the bytes ("fill" units).
 #include <cuda_bf16.h>
@@ -120,7 +120,7 @@ inline bool gv_plan(int T, int H, int F, int qtype, int n_act_max, GvPlan *pl) {
     const int NB = H / 32, RTF = F / 32, RTH = H / 32;
     int ks = 1;
     while (ks < GV_KS_MAX && (long)n_act_max * RTF * ks < GV_UNITS_TARGET && NB % (2 * ks) == 0) ks *= 2;
-    while (gv_slot_bytes(qtype, NB / ks, T) > GV_SLOT_MAX && NB % (2 * ks) == 0) ks *= 2;
+    while (gv_slot_bytes(qtype, NB / ks, T) > GV_SLOT_MAX && NB % (2 * ks) == 0 && ks < 16) ks *= 2;
     pl->KS = ks;
     pl->TPU = RTH % 2 == 0 && (long)n_act_max * (RTH / 2) >= GV_UNITS_TARGET ? 2 : 1;
     return gv_geom(qtype, 2, NB / ks, T, &pl->g1) && gv_geom(qtype, pl->TPU, F / 32, GV_TOK, &pl->g2);
@@ -161,7 +161,7 @@ struct WsLayout {
     size_t ints_off, info_off;
     size_t gu_off;     // float [KS][2][R][F] gate/up partial sums (KS > 1)
     size_t h_off;      // float [R][F] silu(gate) * up
-    size_t cnt_off;    // int [virtual experts][F/32] K ranges done per gate/up row tile (KS > 1)
+    size_t first_off;  // u64 [2 launches][GV_MAX_GRID][GV_WARPS] source image of each warp's first unit
     size_t total;
 };
 
@@ -176,8 +176,8 @@ inline WsLayout ws_layout(int T, int H, int F, int qtype, int E, int k) {
     L.gu_off = L.info_off + ((size_t)gv_n_virt_max(T, E, k) * sizeof(ActInfo) + 255) / 256 * 256;
     const size_t gu = pl.KS > 1 ? (size_t)pl.KS * 2 * R * F * 4 : 0;
     L.h_off = L.gu_off + (gu + 255) / 256 * 256;
-    L.cnt_off = L.h_off + (R * F * 4 + 255) / 256 * 256;
-    L.total = L.cnt_off + ((size_t)gv_n_virt_max(T, E, k) * (F / 32) * 4 + 255) / 256 * 256;
+    L.first_off = L.h_off + (R * F * 4 + 255) / 256 * 256;
+    L.total = L.first_off + (size_t)2 * GV_MAX_GRID * GV_WARPS * 8;
     return L;
 }
 
@@ -191,7 +191,7 @@ struct FfnParams {
     float *gu;
     float *h;
     float *partial;
-    int *cnt;               // K-range counters of the gate/up row tiles (KS > 1)
+    const unsigned long long *first;  // [CTA][warp]: image of the warp's first unit, 0: none/skip/fill
     int *status;
     int x_vec;              // x is 16-byte aligned: vector loads
     GvGeom geo;             // this launch's geometry
@@ -502,6 +502,32 @@ __device__ void fill_chunk(const ActInfo &in, int H, int F, bool down, int NTL, 
     }
 }
 
+// ------------------------------------------------------------------ R1: K-split reduction
+
+// h[q] = silu(sum gate) * (sum up) over the K-split partial sums gu [KS][2][R][F], the K
+// ranges summed in order, for every route position q of the call (n = R * F elements, one per
+// thread, all partials of a thread in flight).  Runs between the gate/up and the down GEMV
+// when the gate/up kernel split K.
+template <int KS>
+__global__ void __launch_bounds__(256) ks_reduce_kernel(const float *__restrict__ gu, float *__restrict__ h,
+                                                        size_t n) {
+    for (size_t q = (size_t)blockIdx.x * 256 + threadIdx.x; q < n; q += (size_t)gridDim.x * 256) {
+        float gp[KS], up[KS];
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+            gp[k] = __ldcg(gu + (size_t)(2 * k) * n + q);
+            up[k] = __ldcg(gu + (size_t)(2 * k + 1) * n + q);
+        }
+        float gs = 0.f, us = 0.f;
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+            gs += gp[k];
+            us += up[k];
+        }
+        h[q] = silu_mul(gs, us);
+    }
+}
+
 // ------------------------------------------------------------------ G1 / G2: the warp-ring kernel
 //
 // Units of a virtual expert: G1 has KS K ranges x F/32 row tiles, ordered (ks, g); unit
@@ -526,6 +552,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
         fence_mbar_init();
     }
     const int u0 = p.ranges[blockIdx.x], u1 = p.ranges[blockIdx.x + 1];
+    const unsigned long long first_src = lane == 0 ? p.first[blockIdx.x * GV_WARPS + warp] : 0ull;
     if (u0 >= u1) return;
     constexpr int TBB = QT == MOE_Q8_0 ? 1088 : 640;  // bytes of a tile block (codes + scales)
     const GvGeom G = p.geo;
@@ -617,7 +644,14 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
     };
     if (lane == 0) {
         pc_first(u0);
-        if (pc_u < u1) pc_info();
+        if (pc_u == u0 + warp && first_src) {  // the permute kernel resolved it: issue at once
+            pc_src = first_src;
+            pc_skip = false;
+            pc_cached_v = pc_u / (upp * kspp);
+            top_up(1);
+        } else if (pc_u < u1) {
+            pc_info();
+        }
     }
     __syncwarp();
 
@@ -629,8 +663,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
         if (a != u0) __syncthreads();  // the previous phase's slots are no longer read
         // Staging, item (pair i, token row t).  Gate/up: every token of the call over the
         // pair's K range, read from x without the routing metadata.  Down: the routes of the
-        // pair's virtual expert, read from h (or the K-split sums).  Row 0's item also writes
-        // the slot header.
+        // pair's virtual expert, read from h.  Row 0's item also writes the slot header.
         // the warp's first chunk goes out once its first staging loads are in flight (or at
         // once for a warp without staging work), ahead of the conversion; the rest of its ring
         // is filled at its first wait, so that every warp's first chunk is ahead of them in the
@@ -734,42 +767,6 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
                     }
                 }
             }
-            if (!DOWN && p.KS > 1) {
-                // The last of the KS units of row tile g to finish forms h = silu(sum gate) *
-                // (sum up) over the K ranges in order (a fixed order: the same h whichever unit
-                // comes last) and resets the counter for the next launch.
-                __threadfence();  // this unit's partial sums, before its arrival is counted
-                int old = 0;
-                if (lane == 0) old = atomicAdd(&p.cnt[v * (p.F / 32) + g], 1);
-                old = __shfl_sync(0xffffffffu, old, 0);
-                if (old == p.KS - 1) {
-                    __threadfence();  // the other units' partial sums, after their counted arrivals
-                    const int row = 32 * g + lane;
-#pragma unroll
-                    for (int t = 0; t < GV_TOK; ++t) {
-                        if (t >= n_e) break;
-                        const size_t q = (size_t)(pos0 + t) * p.F + row;
-                        float gs = 0.f, us = 0.f;
-                        for (int k0 = 0; k0 < p.KS; k0 += 4) {  // four K ranges' loads in flight
-                            float gp[4], up[4];
-#pragma unroll
-                            for (int k2 = 0; k2 < 4; ++k2)
-                                if (k0 + k2 < p.KS) {
-                                    gp[k2] = __ldcg(p.gu + ((size_t)(k0 + k2) * 2 + 0) * p.RT * p.F + q);
-                                    up[k2] = __ldcg(p.gu + ((size_t)(k0 + k2) * 2 + 1) * p.RT * p.F + q);
-                                }
-#pragma unroll
-                            for (int k2 = 0; k2 < 4; ++k2)
-                                if (k0 + k2 < p.KS) {
-                                    gs += gp[k2];
-                                    us += up[k2];
-                                }
-                        }
-                        p.h[q] = silu_mul(gs, us);
-                    }
-                    if (lane == 0) p.cnt[v * (p.F / 32) + g] = 0;
-                }
-            }
         }
         a = e;
     }
@@ -816,7 +813,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
                                                       const uint8_t *pool, size_t slot_bytes,
                                                       const unsigned long long *__restrict__ fill_src,
                                                       int vt, int G1, int per_v1, int G2, int per_v2,
-                                                      int *__restrict__ kcnt, int n_cnt_per_v, int *status) {
+                                                      unsigned long long *__restrict__ first, int *status) {
     __shared__ int cnt[MOE_MAX_E], off[MOE_MAX_E + 1], run[MOE_MAX_E];
     __shared__ int vb[MOE_MAX_E + 1];
     __shared__ unsigned char insub[MOE_MAX_E];
@@ -865,8 +862,6 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
         n_act = na;
     }
     __syncthreads();
-    if (kcnt)  // the gate/up kernel's K-range counters start at 0 (its last arrivals reset them)
-        for (int i = tid; i < vb[n_act] * n_cnt_per_v; i += 256) kcnt[i] = 0;
     int *routes = ints + ws_routes_off(E);
     for (int c0 = 0; c0 < R; c0 += 256) {
         const int r = c0 + tid;
@@ -917,6 +912,23 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
         const long long C1 = (long long)per_v1 * Cv, C2 = (long long)per_v2 * Cv;
         for (int c = tid; c <= G1; c += 256) r1[c] = unit_at_cost(C1 * c / G1, n_act, per_v1, vt, vb, aoff);
         for (int c = tid; c <= G2; c += 256) r2[c] = unit_at_cost(C2 * c / G2, n_act, per_v2, vt, vb, aoff);
+        __syncthreads();
+        // where each warp's first unit (unit ranges[c] + warp) is read from, so that a GEMV warp
+        // can issue its first copy with the range load (0: no such unit, a skip or a fill)
+        for (int l = 0; l < 2; ++l) {
+            const int *rr = l ? r2 : r1;
+            const int G = l ? G2 : G1, per_v = l ? per_v2 : per_v1;
+            unsigned long long *fo = first + (size_t)l * GV_MAX_GRID * GV_WARPS;
+            for (int i = tid; i < G * GV_WARPS; i += 256) {
+                const int c = i / GV_WARPS, u = rr[c] + i % GV_WARPS;
+                unsigned long long d = 0ull;
+                if (u < rr[c + 1]) {
+                    const ActInfo &in = info[u / per_v];
+                    if (in.n_e > 0 && !in.fill) d = in.src;
+                }
+                fo[i] = d;
+            }
+        }
     }
 }
 
@@ -1028,6 +1040,12 @@ const void *gemv_kernel_for(int qtype, int xtype, bool down, int ntl) {
 
 }  // namespace
 
+int moe_decode_ffn_launches(int T, int H, int F, int qtype, int E, int k) {
+    GvPlan pl;
+    if (T <= 0 || !gv_plan(T, H, F, qtype, gv_n_act_max(T, E, k), &pl)) return 0;
+    return pl.KS > 1 ? 4 : 3;  // permute, gate/up, (K-split reduce,) down
+}
+
 size_t moe_decode_workspace_bytes(int T, int H, int F, int qtype, int E, int k) {
     // larger calls run in blocks of MOE_DECODE_MAX_T tokens that reuse one workspace
     return ws_layout(std::min(T, MOE_DECODE_MAX_T), H, F, qtype, E, k).total;
@@ -1126,7 +1144,6 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
     p.info = (const ActInfo *)((char *)workspace + W.info_off);
     p.gu = (float *)((char *)workspace + W.gu_off);
     p.h = (float *)((char *)workspace + W.h_off);
-    p.cnt = (int *)((char *)workspace + W.cnt_off);
     p.partial = partial;
     p.status = moe_status_word_device_ptr();
     p.x_vec = ((uintptr_t)x & 15) == 0;
@@ -1137,8 +1154,8 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
                                      (int32_t *)((char *)workspace + W.ints_off),
                                      (ActInfo *)((char *)workspace + W.info_off), d_slot_table, n_slots,
                                      (const uint8_t *)pool, slot_bytes, (const unsigned long long *)d_fill_src,
-                                     GV_TOK, G1, per_v1, G2, per_v2, pl.KS > 1 ? p.cnt : nullptr, RTF,
-                                     p.status);
+                                     GV_TOK, G1, per_v1, G2, per_v2,
+                                     (unsigned long long *)((char *)workspace + W.first_off), p.status);
     MOE_TRY_CUDA(cudaGetLastError());
     if (timing && timing->permute1) MOE_TRY_CUDA(cudaEventRecord(timing->permute1, s));
     }
@@ -1147,13 +1164,29 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
         if (timing && timing->gateup0) MOE_TRY_CUDA(cudaEventRecord(timing->gateup0, s));
         p.geo = pl.g1;
         p.ranges = p.ws_ints + ws_ranges_off(E, T * k, 0);
+        p.first = (const unsigned long long *)((char *)workspace + W.first_off);
         MOE_TRY_CUDA(cudaLaunchKernel(k1, dim3(G1), dim3(GV_THREADS), args, smem1, s));
-        if (timing && timing->gateup1) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
+        if (timing && timing->gateup1 && !(stages & MOE_FFN_REDUCE)) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
+    }
+    if ((stages & MOE_FFN_REDUCE) && pl.KS > 1) {  // h from the K-split partial sums
+        const size_t n = (size_t)T * k * F;
+        const int grid = (int)std::min<size_t>((n + 255) / 256, 4096);
+        switch (pl.KS) {
+            case 2: ks_reduce_kernel<2><<<grid, 256, 0, s>>>(p.gu, p.h, n); break;
+            case 4: ks_reduce_kernel<4><<<grid, 256, 0, s>>>(p.gu, p.h, n); break;
+            case 8: ks_reduce_kernel<8><<<grid, 256, 0, s>>>(p.gu, p.h, n); break;
+            default: ks_reduce_kernel<16><<<grid, 256, 0, s>>>(p.gu, p.h, n); break;
+        }
+        MOE_TRY_CUDA(cudaGetLastError());
+    }
+    if (stages & MOE_FFN_GATEUP) {
+        if (timing && timing->gateup1 && (stages & MOE_FFN_REDUCE)) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
     }
     if (stages & MOE_FFN_DOWN) {
         if (timing && timing->down0) MOE_TRY_CUDA(cudaEventRecord(timing->down0, s));
         p.geo = pl.g2;
         p.ranges = p.ws_ints + ws_ranges_off(E, T * k, 1);
+        p.first = (const unsigned long long *)((char *)workspace + W.first_off) + (size_t)GV_MAX_GRID * GV_WARPS;
         MOE_TRY_CUDA(cudaLaunchKernel(k2, dim3(G2), dim3(GV_THREADS), args, smem2, s));
         if (timing && timing->down1) MOE_TRY_CUDA(cudaEventRecord(timing->down1, s));
     }

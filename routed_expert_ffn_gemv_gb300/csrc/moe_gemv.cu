@@ -817,6 +817,10 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
     __shared__ int cnt[MOE_MAX_E], off[MOE_MAX_E + 1], run[MOE_MAX_E];
     __shared__ int vb[MOE_MAX_E + 1];
     __shared__ unsigned char insub[MOE_MAX_E];
+    // per virtual expert: where its weights are read from (0: skip or fill), for the first-unit
+    // table below; up to GV_VSRC entries, the rest read back from `info`
+    constexpr int GV_VSRC = 512;
+    __shared__ unsigned long long vsrc[GV_VSRC];
     __shared__ int chunk_e[256];
     __shared__ int n_act;
     const int tid = threadIdx.x;
@@ -903,6 +907,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
             in.wt = in.fill && j == 0;
             for (int t = 0; t < GV_TOK; ++t) in.rt[t] = t < in.n_e ? routes[in.pos0 + t] : 0;
             info[vb[a] + j] = in;
+            if (vb[a] + j < GV_VSRC) vsrc[vb[a] + j] = in.n_e > 0 && !in.fill ? in.src : 0ull;
         }
     }
     __syncthreads();
@@ -923,8 +928,13 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
                 const int c = i / GV_WARPS, u = rr[c] + i % GV_WARPS;
                 unsigned long long d = 0ull;
                 if (u < rr[c + 1]) {
-                    const ActInfo &in = info[u / per_v];
-                    if (in.n_e > 0 && !in.fill) d = in.src;
+                    const int v = u / per_v;
+                    if (v < GV_VSRC) {
+                        d = vsrc[v];
+                    } else {
+                        const ActInfo &in = info[v];
+                        if (in.n_e > 0 && !in.fill) d = in.src;
+                    }
                 }
                 fo[i] = d;
             }

@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "moe_common.cuh"
+#include "moe_ptx.cuh"
 
 #define MOE_EVENT_RING 64
 
@@ -114,6 +115,8 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     int32_t *g_next = (int32_t *)(state + L.next);
     const uint64_t *g_img = (const uint64_t *)(state + L.img);
     const int key0 = ll * E, n_ids = n_tokens * k;
+    pdl_wait();  // ids and the pool state come from earlier kernels
+    pdl_trigger();
     for (int i = threadIdx.x; i < n_slots; i += blockDim.x) {
         owner[i] = g_owner[i];
         prev[i] = g_prev[i];
@@ -260,9 +263,12 @@ extern "C" int moe_cache_plan(moe_cache *c, int layer, const int32_t *d_ids, int
                                           3 * MOE_PLAN_MAX_SLOTS * 4 + MOE_MAX_E * 6));
         attr_set = true;
     }
-    plan_kernel<<<1, 256, smem, moe_cuda_stream(s)>>>((uint8_t *)d.device_state, L, ll, d.n_experts, d.n_slots,
-                                                      d_ids, n_tokens, k, c->image_bytes, d_table_out,
-                                                      d_fill_src_out, moe_status_word_device_ptr());
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    moe_pdl_config(&cfg, attr, dim3(1), dim3(256), smem, moe_cuda_stream(s));
+    MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, plan_kernel, (uint8_t *)d.device_state, L, ll, d.n_experts, d.n_slots,
+                                    d_ids, n_tokens, k, c->image_bytes, d_table_out, d_fill_src_out,
+                                    moe_status_word_device_ptr()));
     MOE_TRY_CUDA(cudaGetLastError());
     return MOE_OK;
 }

@@ -133,6 +133,21 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
                           float *partial, void *workspace, size_t ws_bytes, cudaStream_t s,
                           const moe_ffn_timing *timing, int stages);
 
+// Launch attributes of the decode chain's kernels: the programmatic dependency on the previous
+// kernel of the stream (each kernel waits for it with griddepcontrol.wait before reading its
+// outputs, so the launch and the prologue overlap the previous kernel's tail).
+static inline void moe_pdl_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *attr, dim3 grid, dim3 block,
+                                  size_t smem, cudaStream_t s) {
+    cfg->gridDim = grid;
+    cfg->blockDim = block;
+    cfg->dynamicSmemBytes = smem;
+    cfg->stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+}
+
 // Writes up to three small int32 arrays (<= 256 values each) on stream s with one launch
 // (values travel as kernel parameters, so no host staging buffer outlives the call).
 int moe_write_ints(int32_t *const dst[3], const int n[3], const int32_t *const src[3], cudaStream_t s);

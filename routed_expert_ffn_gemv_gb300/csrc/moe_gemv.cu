@@ -511,6 +511,8 @@ __device__ void fill_chunk(const ActInfo &in, int H, int F, bool down, int NTL, 
 template <int KS>
 __global__ void __launch_bounds__(256) ks_reduce_kernel(const float *__restrict__ gu, float *__restrict__ h,
                                                         size_t n) {
+    pdl_wait();
+    pdl_trigger();
     for (size_t q = (size_t)blockIdx.x * 256 + threadIdx.x; q < n; q += (size_t)gridDim.x * 256) {
         float gp[KS], up[KS];
 #pragma unroll
@@ -547,10 +549,12 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *bars = (uint64_t *)smem + warp * GV_MAX_STAGES;
-    if (lane == 0) {  // while the range is loaded: every stage barrier this warp may use
+    if (lane == 0) {  // before the dependency wait: every stage barrier this warp may use
         for (int s = 0; s < GV_MAX_STAGES; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
+    pdl_wait();  // ranges, routing and activations come from earlier kernels
+    pdl_trigger();
     const int u0 = p.ranges[blockIdx.x], u1 = p.ranges[blockIdx.x + 1];
     const unsigned long long first_src = lane == 0 ? p.first[blockIdx.x * GV_WARPS + warp] : 0ull;
     if (u0 >= u1) return;
@@ -824,6 +828,8 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
     __shared__ int chunk_e[256];
     __shared__ int n_act;
     const int tid = threadIdx.x;
+    pdl_wait();  // ids and the slot table come from earlier kernels
+    pdl_trigger();
     for (int e = tid; e < E; e += 256) {
         cnt[e] = 0;
         run[e] = 0;
@@ -965,6 +971,8 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(const float4 *__restr
                                                            float eps) {
     __shared__ float red[8];
     const int t = blockIdx.x;
+    pdl_wait();  // the partial outputs come from the down GEMV
+    pdl_trigger();
     float ss = 0.f;
     for (int h = threadIdx.x; h < H4; h += blockDim.x) {
         float4 s = extra ? extra[(size_t)t * H4 + h] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1160,13 +1168,17 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
 
     if (stages & MOE_FFN_PERMUTE) {
     if (timing && timing->permute0) MOE_TRY_CUDA(cudaEventRecord(timing->permute0, s));
-    permute_kernel<<<1, 256, 0, s>>>(ids, T * k, E, expert_subset, n_subset,
-                                     (int32_t *)((char *)workspace + W.ints_off),
-                                     (ActInfo *)((char *)workspace + W.info_off), d_slot_table, n_slots,
-                                     (const uint8_t *)pool, slot_bytes, (const unsigned long long *)d_fill_src,
-                                     GV_TOK, G1, per_v1, G2, per_v2,
-                                     (unsigned long long *)((char *)workspace + W.first_off), p.status);
-    MOE_TRY_CUDA(cudaGetLastError());
+    {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        moe_pdl_config(&cfg, attr, dim3(1), dim3(256), 0, s);
+        MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, permute_kernel, ids, T * k, E, expert_subset, n_subset,
+                                        (int32_t *)((char *)workspace + W.ints_off),
+                                        (ActInfo *)((char *)workspace + W.info_off), d_slot_table, n_slots,
+                                        (const uint8_t *)pool, slot_bytes,
+                                        (const unsigned long long *)d_fill_src, (int)GV_TOK, G1, per_v1, G2, per_v2,
+                                        (unsigned long long *)((char *)workspace + W.first_off), p.status));
+    }
     if (timing && timing->permute1) MOE_TRY_CUDA(cudaEventRecord(timing->permute1, s));
     }
     void *args[] = {&p};
@@ -1175,19 +1187,26 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
         p.geo = pl.g1;
         p.ranges = p.ws_ints + ws_ranges_off(E, T * k, 0);
         p.first = (const unsigned long long *)((char *)workspace + W.first_off);
-        MOE_TRY_CUDA(cudaLaunchKernel(k1, dim3(G1), dim3(GV_THREADS), args, smem1, s));
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        moe_pdl_config(&cfg, attr, dim3(G1), dim3(GV_THREADS), smem1, s);
+        MOE_TRY_CUDA(cudaLaunchKernelExC(&cfg, k1, args));
         if (timing && timing->gateup1 && !(stages & MOE_FFN_REDUCE)) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
     }
     if ((stages & MOE_FFN_REDUCE) && pl.KS > 1) {  // h from the K-split partial sums
         const size_t n = (size_t)T * k * F;
         const int grid = (int)std::min<size_t>((n + 255) / 256, 4096);
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        moe_pdl_config(&cfg, attr, dim3(grid), dim3(256), 0, s);
+        const float *gu = p.gu;
+        float *h = p.h;
         switch (pl.KS) {
-            case 2: ks_reduce_kernel<2><<<grid, 256, 0, s>>>(p.gu, p.h, n); break;
-            case 4: ks_reduce_kernel<4><<<grid, 256, 0, s>>>(p.gu, p.h, n); break;
-            case 8: ks_reduce_kernel<8><<<grid, 256, 0, s>>>(p.gu, p.h, n); break;
-            default: ks_reduce_kernel<16><<<grid, 256, 0, s>>>(p.gu, p.h, n); break;
+            case 2: MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, ks_reduce_kernel<2>, gu, h, n)); break;
+            case 4: MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, ks_reduce_kernel<4>, gu, h, n)); break;
+            case 8: MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, ks_reduce_kernel<8>, gu, h, n)); break;
+            default: MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, ks_reduce_kernel<16>, gu, h, n)); break;
         }
-        MOE_TRY_CUDA(cudaGetLastError());
     }
     if (stages & MOE_FFN_GATEUP) {
         if (timing && timing->gateup1 && (stages & MOE_FFN_REDUCE)) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
@@ -1197,7 +1216,10 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
         p.geo = pl.g2;
         p.ranges = p.ws_ints + ws_ranges_off(E, T * k, 1);
         p.first = (const unsigned long long *)((char *)workspace + W.first_off) + (size_t)GV_MAX_GRID * GV_WARPS;
-        MOE_TRY_CUDA(cudaLaunchKernel(k2, dim3(G2), dim3(GV_THREADS), args, smem2, s));
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        moe_pdl_config(&cfg, attr, dim3(G2), dim3(GV_THREADS), smem2, s);
+        MOE_TRY_CUDA(cudaLaunchKernelExC(&cfg, k2, args));
         if (timing && timing->down1) MOE_TRY_CUDA(cudaEventRecord(timing->down1, s));
     }
     return MOE_OK;
@@ -1243,9 +1265,11 @@ extern "C" int moe_combine_rmsnorm(const float *partial, int T, int k, int H, co
     MOE_CHECK(((uintptr_t)partial & 15) == 0 && ((uintptr_t)y & 15) == 0 && ((uintptr_t)extra & 15) == 0 &&
               ((uintptr_t)xn & 15) == 0);
     MOE_CHECK(!(xn && (xn == extra || xn == y)));
-    combine_norm_kernel<<<T, 256, 0, moe_cuda_stream(s)>>>((const float4 *)partial, k, H / 4,
-                                                           (const float4 *)extra, (float4 *)y, (float4 *)xn, eps);
-    MOE_TRY_CUDA(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    moe_pdl_config(&cfg, attr, dim3(T), dim3(256), 0, moe_cuda_stream(s));
+    MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, combine_norm_kernel, (const float4 *)partial, k, H / 4,
+                                    (const float4 *)extra, (float4 *)y, (float4 *)xn, eps));
     return MOE_OK;
 }
 

@@ -141,6 +141,8 @@ router_topk_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__r
             ((uint16_t *)w_s)[i] = w_router[(size_t)h0 * E + i];
     }
     if (tid == 0) ((uint16_t *)w_s)[(size_t)HS * E] = 0;  // pad read by the odd-E pair
+    pdl_wait();  // x comes from the previous kernel (the weights do not)
+    pdl_trigger();
     // ---- x slice of this cluster's tokens
     for (int i = tid; i < TT * HS; i += MOE_ROUTER_THREADS) {
         const int t = i / HS, h = i % HS;
@@ -460,13 +462,15 @@ extern "C" int moe_router_topk(const void *x, int xtype, int T, int H, const uin
     cfg.blockDim = dim3(MOE_ROUTER_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L.total;
     cfg.stream = moe_cuda_stream(s);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = MOE_ROUTER_CLUSTER;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (xtype == MOE_F32) {
         MOE_TRY_CUDA(cudaFuncSetAttribute(router_topk_kernel<MOE_F32>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total));

@@ -51,6 +51,7 @@
 #define GV_KS_MAX 8               // largest K split of the gate/up GEMV
 #define GV_ACT_SLOTS_MAX 3        // staged (virtual expert, K range) pairs per CTA phase
 #define GV_PHASE_PAIRS 64         // pairs (used or skipped) per CTA phase
+#define GV_PERMUTE_MAX_R (MOE_DECODE_MAX_T * MOE_MAX_K)  // routes of one decode call
 
 namespace {
 
@@ -818,22 +819,26 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
                                                       const unsigned long long *__restrict__ fill_src,
                                                       int vt, int G1, int per_v1, int G2, int per_v2,
                                                       unsigned long long *__restrict__ first, int *status) {
-    __shared__ int cnt[MOE_MAX_E], off[MOE_MAX_E + 1], run[MOE_MAX_E];
-    __shared__ int vb[MOE_MAX_E + 1];
+    // everything the kernel reads is loaded once into shared memory (R <= GV_PERMUTE_MAX_R)
+    __shared__ int cnt[MOE_MAX_E], off[MOE_MAX_E + 1];
+    __shared__ int vb[MOE_MAX_E + 1], s_active[MOE_MAX_E], s_aoff[MOE_MAX_E + 1], s_slot[MOE_MAX_E];
+    __shared__ unsigned long long s_fill[MOE_MAX_E];
     __shared__ unsigned char insub[MOE_MAX_E];
+    __shared__ int s_ids[GV_PERMUTE_MAX_R], s_routes[GV_PERMUTE_MAX_R];
     // per virtual expert: where its weights are read from (0: skip or fill), for the first-unit
     // table below; up to GV_VSRC entries, the rest read back from `info`
     constexpr int GV_VSRC = 512;
     __shared__ unsigned long long vsrc[GV_VSRC];
-    __shared__ int chunk_e[256];
     __shared__ int n_act;
     const int tid = threadIdx.x;
     pdl_wait();  // ids and the slot table come from earlier kernels
     pdl_trigger();
+    for (int r = tid; r < R; r += 256) s_ids[r] = ids[r];
     for (int e = tid; e < E; e += 256) {
         cnt[e] = 0;
-        run[e] = 0;
         insub[e] = subset ? 0 : 1;
+        s_slot[e] = slot_table ? slot_table[e] : e;
+        s_fill[e] = fill_src ? fill_src[e] : 0ull;
     }
     __syncthreads();
     if (subset) {
@@ -842,10 +847,10 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
             if (e >= 0 && e < E) insub[e] = 1;
             else moe_set_status(status, MOE_ERR_INVALID);
         }
+        __syncthreads();
     }
-    __syncthreads();
     for (int r = tid; r < R; r += 256) {
-        const int e = ids[r];
+        const int e = s_ids[r];
         if (e < 0 || e >= E) { moe_set_status(status, MOE_ERR_INVALID); continue; }
         if (insub[e]) atomicAdd(&cnt[e], 1);
     }
@@ -857,44 +862,40 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
         for (int e = 0; e < E; ++e) {
             off[e] = s;
             if (cnt[e] > 0) {
-                active[na] = e;
-                aoff[na] = s;
+                s_active[na] = e;
+                s_aoff[na] = s;
                 vb[na] = nv;
                 nv += (cnt[e] + vt - 1) / vt;
                 ++na;
             }
             s += cnt[e];
         }
-        aoff[na] = s;
+        s_aoff[na] = s;
         vb[na] = nv;
         ints[0] = na;
         ints[1] = nv;
         n_act = na;
     }
     __syncthreads();
-    int *routes = ints + ws_routes_off(E);
-    for (int c0 = 0; c0 < R; c0 += 256) {
-        const int r = c0 + tid;
-        int e = -1;
-        if (r < R) {
-            e = ids[r];
-            if (e < 0 || e >= E || !insub[e]) e = -1;
-        }
-        chunk_e[tid] = e;
-        __syncthreads();
-        if (e >= 0) {
-            int rank = 0;
-            for (int i = 0; i < tid; ++i) rank += (chunk_e[i] == e);
-            routes[off[e] + run[e] + rank] = r;
-        }
-        __syncthreads();
-        if (e >= 0) atomicAdd(&run[e], 1);
-        __syncthreads();
+    for (int a = tid; a <= n_act; a += 256) {
+        aoff[a] = s_aoff[a];
+        if (a < n_act) active[a] = s_active[a];
     }
+    // stable order of the routes of each expert: rank among the earlier routes of the same expert
+    int *routes = ints + ws_routes_off(E);
+    for (int r = tid; r < R; r += 256) {
+        const int e = s_ids[r];
+        if (e < 0 || e >= E || !insub[e]) continue;
+        int rank = 0;
+        for (int i = 0; i < r; ++i) rank += (s_ids[i] == e);
+        s_routes[off[e] + rank] = r;
+        routes[off[e] + rank] = r;
+    }
+    __syncthreads();
     for (int a = tid; a < n_act; a += 256) {
-        const int e = active[a];
-        const int slot = slot_table ? slot_table[e] : e;
-        const int n_e = aoff[a + 1] - aoff[a];
+        const int e = s_active[a];
+        const int slot = s_slot[e];
+        const int n_e = s_aoff[a + 1] - s_aoff[a];
         ActInfo in;
         in.fill = in.wt = 0;
         in.src = in.dst = 0ull;
@@ -903,15 +904,15 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
             moe_set_status(status, MOE_ERR_INVALID);  // nothing of this expert is read
         } else {
             in.dst = (unsigned long long)(pool + (size_t)slot * slot_bytes);
-            const unsigned long long f = fill_src ? fill_src[e] : 0ull;
+            const unsigned long long f = s_fill[e];
             in.fill = f != 0ull;
             in.src = f ? f : in.dst;
         }
         for (int j = 0; j < vb[a + 1] - vb[a]; ++j) {
-            in.pos0 = aoff[a] + vt * j;
+            in.pos0 = s_aoff[a] + vt * j;
             in.n_e = bad ? 0 : min(vt, n_e - vt * j);
             in.wt = in.fill && j == 0;
-            for (int t = 0; t < GV_TOK; ++t) in.rt[t] = t < in.n_e ? routes[in.pos0 + t] : 0;
+            for (int t = 0; t < GV_TOK; ++t) in.rt[t] = t < in.n_e ? s_routes[in.pos0 + t] : 0;
             info[vb[a] + j] = in;
             if (vb[a] + j < GV_VSRC) vsrc[vb[a] + j] = in.n_e > 0 && !in.fill ? in.src : 0ull;
         }
@@ -919,10 +920,10 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
     __syncthreads();
     {
         int *r1 = ints + ws_ranges_off(E, R, 0), *r2 = ints + ws_ranges_off(E, R, 1);
-        const long long Cv = (long long)GV_COST_MEM * vb[n_act] + (long long)GV_COST_TOK * aoff[n_act];
+        const long long Cv = (long long)GV_COST_MEM * vb[n_act] + (long long)GV_COST_TOK * s_aoff[n_act];
         const long long C1 = (long long)per_v1 * Cv, C2 = (long long)per_v2 * Cv;
-        for (int c = tid; c <= G1; c += 256) r1[c] = unit_at_cost(C1 * c / G1, n_act, per_v1, vt, vb, aoff);
-        for (int c = tid; c <= G2; c += 256) r2[c] = unit_at_cost(C2 * c / G2, n_act, per_v2, vt, vb, aoff);
+        for (int c = tid; c <= G1; c += 256) r1[c] = unit_at_cost(C1 * c / G1, n_act, per_v1, vt, vb, s_aoff);
+        for (int c = tid; c <= G2; c += 256) r2[c] = unit_at_cost(C2 * c / G2, n_act, per_v2, vt, vb, s_aoff);
         __syncthreads();
         // where each warp's first unit (unit ranges[c] + warp) is read from, so that a GEMV warp
         // can issue its first copy with the range load (0: no such unit, a skip or a fill)
@@ -1135,6 +1136,7 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
         }
         return MOE_OK;
     }
+    if (T * k > GV_PERMUTE_MAX_R) return MOE_ERR_UNSUPPORTED;
     const WsLayout W = ws_layout(T, H, F, qtype, E, k);
     MOE_CHECK(ws_bytes >= W.total);
     GvPlan pl;  // planned for every expert routable (the workspace does not depend on a subset)

@@ -208,9 +208,10 @@ def gemv_roofline(cfg, T, torch, stream, steps=40, warmup=5):
     images, 1.28 GB, far above L2); every layer's router and permute run first, then rounds of
     the gate/up GEMV of all layers are launched back to back on `stream` between two CUDA
     events (so no launch finds its weights in L2 and no event sits between launches), then of
-    the down GEMV.  Bytes per launch are the active experts' quantised blocks, counted on the
-    device.  `steps` rounds are timed after `warmup` untimed ones (at least 3 each)."""
-    from routed_expert_ffn_gemv_gb300 import synth
+    the down GEMV, then of each layer's whole chain (permute, the GEMVs).
+    Bytes per launch are the active experts' quantised blocks, counted on the device.
+    `steps` rounds are timed after `warmup` untimed ones (at least 3 each)."""
+    from routed_expert_ffn_gemv_gb300 import _lib as L, synth
     from routed_expert_ffn_gemv_gb300.workload import Stack
     st = Stack(cfg, max_T=T, resident=True, profile=0)
     x = torch.from_numpy(synth.tokens_x(cfg, 500, T)).cuda()
@@ -221,7 +222,44 @@ def gemv_roofline(cfg, T, torch, stream, steps=40, warmup=5):
     return {"gateup_ms_per_launch": r["gateup_us"] / 1e3, "gateup_bytes_per_launch": r["gateup_bytes"],
             "down_ms_per_launch": r["down_us"] / 1e3, "down_bytes_per_launch": r["down_bytes"],
             "reduce_ms_per_launch": r["reduce_us"] / 1e3,
+            "gemv_ms_per_launch": r["gemv_us"] / 1e3, "fused": bool(r["fused"]),
             "launches": int(r["launches"]), "steps": steps}
+
+
+def gemv_roofline_block(gv, cfg, T, peaks):
+    """The roofline object of the JSON line.  The unit that moves the decode path's weight
+    bytes is one layer's FFN chain: the permute kernel (routing metadata and work ranges),
+    the gate/up GEMV, the K-split reduce and the down GEMV (or their fused launch); its
+    bytes are the selected experts' quantised blocks.  The separate kernels' own figures
+    (each timed in rounds of its own) stand beside it."""
+    def gbs(b, ms):
+        return b / (ms / 1e3) / 1e9 if ms > 0 else 0.0
+    hbm = peaks["hbm_gbs"]
+    gu_ms, gu_b = gv["gateup_ms_per_launch"], gv["gateup_bytes_per_launch"]
+    dn_ms, dn_b = gv["down_ms_per_launch"], gv["down_bytes_per_launch"]
+    separate = {"gateup_kernel": {"achieved_gbs": gbs(gu_b, gu_ms), "frac": gbs(gu_b, gu_ms) / hbm,
+                                  "ms_per_launch": gu_ms, "algorithmic_bytes_per_launch": gu_b},
+                "down_kernel": {"achieved_gbs": gbs(dn_b, dn_ms), "frac": gbs(dn_b, dn_ms) / hbm,
+                                "ms_per_launch": dn_ms, "algorithmic_bytes_per_launch": dn_b},
+                "ks_reduce_kernel_ms_per_launch": gv["reduce_ms_per_launch"],
+                "ms_per_layer": gu_ms + gv["reduce_ms_per_launch"] + dn_ms,
+                "measured_in": "each kernel alone in rounds of back-to-back launches over all layers"}
+    if gv["fused"]:
+        kernel = ("decode FFN chain per layer: permute_kernel -> ffn_fused_kernel<q8_0> "
+                  "(gate/up GEMV + SwiGLU, K-split reduce, down GEMV + weighting in one launch)")
+    else:
+        kernel = ("decode FFN chain per layer: permute_kernel -> ffn_warp_kernel<q8_0, gate/up> "
+                  "-> ks_reduce_kernel -> ffn_warp_kernel<q8_0, down>")
+    ms, b = gv["gemv_ms_per_launch"], gu_b + dn_b
+    tr = traffic_record(f"chain_q8_0_h{cfg.H}_t{T}")
+    return {"kernel": kernel, "bound": "hbm", "achieved": gbs(b, ms), "peak": hbm, "unit": "GB/s",
+            "frac": gbs(b, ms) / hbm, "peak_source": peaks["source"],
+            "traffic": None if tr is None else tr["bytes_per_launch"],
+            "algorithmic_bytes_per_launch": b, "ms_per_launch": ms, "launches": gv["launches"],
+            "separate_kernels": separate,
+            "measured_in": ("HBM-resident stack (all %d x %d expert images in HBM, above L2), batch %d; "
+                            "each layer's chain launched back to back over all layers, CUDA events on the "
+                            "launching stream around the rounds (launch gaps included)" % (cfg.L, cfg.E, T))}
 
 
 def max_over_ranks(v, world, torch):
@@ -371,7 +409,9 @@ def run_gpu(args, world, rank, local):
                  ("router_ms", "permute_ms", "gateup_ms", "down_ms", "combine_ms")}
     breakdown["steps"] = bsteps
     breakdown["note"] = ("device-managed pool, eager launches with events around every kernel; the "
-                         "gate/up and down kernels also read missed experts over the CPU-GPU link")
+                         "gate/up and down kernels also read missed experts over the CPU-GPU link"
+                         + ("; the GEMVs run as one fused launch, all counted under gateup_ms"
+                            if L.moe_get_decode_fused() else ""))
     dev_stack.set_profile(0)
 
     # host-managed pool (moe_cache_ensure + copy-engine uploads); its profiled loop times the
@@ -415,25 +455,7 @@ def run_gpu(args, world, rank, local):
     ms, prof, st, steps = main
     r = results[args.batch]
     gv = gemv_roofline(cfg, T, torch, stream, steps=20, warmup=3)
-    gu_ms_launch, gu_bytes_launch = gv["gateup_ms_per_launch"], gv["gateup_bytes_per_launch"]
-    achieved = gu_bytes_launch / (gu_ms_launch / 1e3) / 1e9 if gu_ms_launch > 0 else 0.0
-    dn_gbs = gv["down_bytes_per_launch"] / (gv["down_ms_per_launch"] / 1e3) / 1e9 if gv["down_ms_per_launch"] else 0.0
-    tr = traffic_record(f"gateup_q8_0_h{cfg.H}_t{T}")
-    roofline = {"kernel": "ffn_warp_kernel<q8_0, gate/up> (dequantising gate/up GEMV + SwiGLU)", "bound": "hbm",
-                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
-                "traffic": None if tr is None else tr["bytes_per_launch"],
-                "algorithmic_bytes_per_launch": gu_bytes_launch, "ms_per_launch": gu_ms_launch,
-                "launches": gv["launches"],
-                "down_kernel": {"achieved_gbs": dn_gbs, "frac": dn_gbs / peaks["hbm_gbs"],
-                                "ms_per_launch": gv["down_ms_per_launch"],
-                                "algorithmic_bytes_per_launch": gv["down_bytes_per_launch"]},
-                "ks_reduce_kernel_ms_per_launch": gv["reduce_ms_per_launch"],
-                "ffn_gemv_ms_per_layer": gu_ms_launch + gv["reduce_ms_per_launch"] + gv["down_ms_per_launch"],
-                "measured_in": ("HBM-resident stack (all %d x %d expert images in HBM, above L2), batch %d; "
-                                "each layer's gate/up GEMV launched back to back over all layers, CUDA events "
-                                "on the launching stream around the rounds (launch gaps included)"
-                                % (cfg.L, cfg.E, T))}
+    roofline = gemv_roofline_block(gv, cfg, T, peaks)
     if rank == 0:
         cb = cpu_baseline(cfg, T) if world == 1 else None
         line = {"metric": METRIC, "value": r["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
@@ -499,8 +521,7 @@ def run_only(args):
     if args.only == "gemv":
         gv = gemv_roofline(cfg, T, torch, torch.cuda.Stream(), steps=args.steps, warmup=args.warmup)
         gv.update({"only": "gemv", "batch": T,
-                   "gateup_gbs": gv["gateup_bytes_per_launch"] / (gv["gateup_ms_per_launch"] / 1e3) / 1e9,
-                   "down_gbs": gv["down_bytes_per_launch"] / (gv["down_ms_per_launch"] / 1e3) / 1e9})
+                   "roofline": gemv_roofline_block(gv, cfg, T, peaks)})
         print(json.dumps(gv), flush=True)
         return 0
     stack = Stack(cfg, max_T=T, profile=1)

@@ -410,7 +410,9 @@ int moe_stack_set_profile(moe_stack *st, int level);
  * MOE_DECODE_MAX_T); then, on stream s behind a GPU spacer (a bounded spin, so that every
  * timed launch is queued before the first starts), `reps` rounds of the gate/up GEMV of
  * every layer are launched back to back between two CUDA events, then `reps` rounds of the
- * K-split reduce (if any), then `reps` rounds of the down GEMV.
+ * K-split reduce (if any), then `reps` rounds of the down GEMV, then `reps` rounds of the
+ * whole decode FFN chain of every layer as the FFN entry points run it: the permute kernel,
+ * then the fused GEMV launch when moe_get_decode_fused() is 1, else the three GEMV kernels.
  * Consecutive launches read different layers' experts, so no launch finds the previous
  * one's weights in L2.  Results: the average time of one launch (microseconds, launch gaps
  * included, no events between launches) and the quantised bytes of the selected experts
@@ -424,10 +426,25 @@ typedef struct moe_gemv_timing {
     int launches;                     /* per kernel: reps * layers */
     double reduce_us;                 /* the K-split reduce between them (0 launches when the
                                          gate/up GEMV does not split K), timed the same way */
+    double gemv_us;                   /* one layer's whole chain: permute, gate/up, reduce, down */
+    int fused;                        /* 1: gemv_us timed the fused GEMV launch */
 } moe_gemv_timing;
 int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, int reps, moe_gemv_timing *out,
                           moe_stream_t s);
 void moe_stack_destroy(moe_stack *st);
+
+/*
+ * moe_set_decode_fused — process-wide choice of how the decode path runs its GEMVs.
+ * on == 0 (the default): the gate/up GEMV, the K-split reduce and the down GEMV run as
+ * three kernels one after another.  on != 0: as one cooperative launch whose CTAs meet at a
+ * grid barrier (bounded wait: MOE_ERR_TIMEOUT in the status word) after issuing their
+ * down-weight copies, so that the down GEMV's weight reads overlap the gate/up GEMV's tail
+ * (measured slower on GB300 at the decode sizes: each grid barrier costs about as much as a
+ * launch).  Both compute the same values in the same order.  Takes effect for calls (and
+ * graph captures) made after it; a captured graph keeps the choice it was captured with.
+ */
+int moe_set_decode_fused(int on);
+int moe_get_decode_fused(void);
 
 /* ------------------------------------------------------------------ test hooks */
 

@@ -37,6 +37,7 @@ EXPORTED = [
     "moe_combine", "moe_device_status", "moe_stack_workspace", "moe_stack_create",
     "moe_stack_decode", "moe_stack_layer", "moe_stack_profile_get", "moe_stack_profile_reset",
     "moe_stack_destroy", "moe_debug_inject_fault", "moe_stack_set_profile", "moe_stack_gemv_timing",
+    "moe_set_decode_fused", "moe_get_decode_fused",
     "moe_expert_ffn_noalloc", "moe_combine_rmsnorm", "moe_cache_state_bytes", "moe_cache_plan",
     "moe_expert_ffn_fill", "moe_last_cuda_error",
 ]
@@ -100,7 +101,7 @@ class StackProfile(ctypes.Structure):
 class GemvTiming(ctypes.Structure):
     _fields_ = [("gateup_us", ctypes.c_double), ("down_us", ctypes.c_double),
                 ("gateup_bytes", ctypes.c_double), ("down_bytes", ctypes.c_double), ("launches", _i),
-                ("reduce_us", ctypes.c_double)]
+                ("reduce_us", ctypes.c_double), ("gemv_us", ctypes.c_double), ("fused", _i)]
 
     def as_dict(self):
         return {f[0]: getattr(self, f[0]) for f in self._fields_}
@@ -158,6 +159,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_stack_destroy": ([_vp], None),
         "moe_stack_set_profile": ([_vp, _i], _i),
         "moe_stack_gemv_timing": ([_vp, _vp, _i, _i, P(GemvTiming), _vp], _i),
+        "moe_set_decode_fused": ([_i], _i),
+        "moe_get_decode_fused": ([], _i),
         "moe_debug_inject_fault": ([_i, _i], _i),
     }
     for name, (args, res) in sig.items():
@@ -383,6 +386,14 @@ def moe_stack_gemv_timing(stack: int, x, T: int, reps: int, stream=None) -> dict
     _ck("moe_stack_gemv_timing", load().moe_stack_gemv_timing(stack, _ptr(x), T, reps, ctypes.byref(t),
                                                               _stream(stream)))
     return t.as_dict()
+
+
+def moe_set_decode_fused(on: bool) -> None:
+    _ck("moe_set_decode_fused", load().moe_set_decode_fused(1 if on else 0))
+
+
+def moe_get_decode_fused() -> bool:
+    return bool(load().moe_get_decode_fused())
 
 
 def moe_stack_destroy(stack: int) -> None:

@@ -104,10 +104,15 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
                                                    int n_slots, const int32_t *__restrict__ ids, int n_tokens,
                                                    int k, uint64_t image_bytes, int32_t *__restrict__ table_out,
                                                    uint64_t *__restrict__ src_out, int *status) {
+    // Everything is read once into shared memory (one round of loads), the list is updated
+    // there by one thread, and the results are stored once.
     extern __shared__ int32_t sm[];
     int32_t *owner = sm, *prev = sm + n_slots, *next = sm + 2 * n_slots, *slot_l = sm + 3 * n_slots;
     unsigned char *want = (unsigned char *)(slot_l + E), *miss = want + E;
-    __shared__ int abort_flag;
+    __shared__ int abort_flag, route_hits, commit;
+    __shared__ int32_t s_ids[MOE_DECODE_MAX_T * MOE_MAX_K];
+    __shared__ DevHeader s_hd;
+    __shared__ uint64_t s_img[MOE_MAX_E];
     DevHeader *hd = (DevHeader *)state;
     int32_t *g_slot_of = (int32_t *)(state + L.slot_of);
     int32_t *g_owner = (int32_t *)(state + L.owner);
@@ -124,13 +129,22 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     }
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         slot_l[e] = g_slot_of[key0 + e];
+        s_img[e] = g_img[key0 + e];
         want[e] = 0;
         miss[e] = 0;
     }
-    if (threadIdx.x == 0) abort_flag = 0;
+    for (int i = threadIdx.x; i < n_ids; i += blockDim.x) s_ids[i] = ids[i];
+    static_assert(sizeof(DevHeader) % 4 == 0, "header words");
+    for (int i = threadIdx.x; i < (int)(sizeof(DevHeader) / 4); i += blockDim.x)
+        ((int32_t *)&s_hd)[i] = ((const int32_t *)hd)[i];
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        route_hits = 0;
+        commit = 0;
+    }
     __syncthreads();
     for (int i = threadIdx.x; i < n_ids; i += blockDim.x) {
-        const int e = ids[i];
+        const int e = s_ids[i];
         if (e < 0 || e >= E) {
             moe_set_status(status, MOE_ERR_INVALID);
             abort_flag = 1;
@@ -146,7 +160,8 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
             moe_set_status(status, MOE_ERR_CAPACITY);
             abort_flag = 1;
         } else {
-            int head = hd->head, tail = hd->tail, filled = hd->n_filled;
+            commit = 1;  // the list is updated (up to a capacity error) and its header stored
+            int head = s_hd.head, tail = s_hd.tail, filled = s_hd.n_filled;
             auto unlink = [&](int s) {
                 const int p = prev[s], n = next[s];
                 if (p >= 0) next[p] = n; else head = n;
@@ -158,7 +173,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
                 if (tail >= 0) next[tail] = s; else head = s;
                 tail = s;
             };
-            int n_hit = 0, n_miss = 0, n_evict = 0, route_hits = 0;
+            int n_hit = 0, n_miss = 0, n_evict = 0;
             for (int e = 0; e < E; ++e) {           // hits, ascending id: most recent
                 if (!want[e] || slot_l[e] < 0) continue;
                 unlink(slot_l[e]);
@@ -192,22 +207,30 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
                 miss[e] = 1;
                 ++n_miss;
             }
-            for (int i = 0; i < n_ids; ++i) route_hits += !miss[ids[i]];
-            hd->head = head;
-            hd->tail = tail;
-            hd->n_filled = filled;
+            s_hd.head = head;
+            s_hd.tail = tail;
+            s_hd.n_filled = filled;
             const int b = n_tokens <= 8 ? 0 : 1;
-            hd->queries[b] += n_hit + n_miss;
-            hd->hits[b] += n_hit;
-            hd->misses[b] += n_miss;
-            hd->evictions += n_evict;
-            hd->h2d_bytes += (uint64_t)n_miss * image_bytes;
-            hd->route_queries += n_ids;
-            hd->route_hits += route_hits;
-            hd->ensure_calls += 1;
+            s_hd.queries[b] += n_hit + n_miss;
+            s_hd.hits[b] += n_hit;
+            s_hd.misses[b] += n_miss;
+            s_hd.evictions += n_evict;
+            s_hd.h2d_bytes += (uint64_t)n_miss * image_bytes;
+            s_hd.route_queries += n_ids;
+            s_hd.ensure_calls += 1;
         }
     }
     __syncthreads();
+    if (commit) {  // routes whose expert was resident before this call (every id is valid here)
+        int h = 0;
+        for (int i = threadIdx.x; i < n_ids; i += blockDim.x) h += !miss[s_ids[i]];
+        if (h) atomicAdd(&route_hits, h);
+        __syncthreads();
+        if (threadIdx.x == 0) s_hd.route_hits += route_hits;
+        __syncthreads();
+        for (int i = threadIdx.x; i < (int)(sizeof(DevHeader) / 4); i += blockDim.x)
+            ((int32_t *)hd)[i] = ((const int32_t *)&s_hd)[i];
+    }
     for (int i = threadIdx.x; i < n_slots; i += blockDim.x) {
         g_owner[i] = owner[i];
         g_prev[i] = prev[i];
@@ -216,7 +239,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         g_slot_of[key0 + e] = slot_l[e];
         table_out[e] = abort_flag ? -1 : slot_l[e];
-        src_out[e] = (!abort_flag && miss[e]) ? g_img[key0 + e] : 0ull;
+        src_out[e] = (!abort_flag && miss[e]) ? s_img[e] : 0ull;
     }
 }
 

@@ -33,6 +33,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "moe_ptx.cuh"
@@ -41,7 +42,7 @@
 #define GV_THREADS (GV_WARPS * 32)
 #define GV_TOK 4                  // routes of a virtual expert (one m16n8 column set: hi + lo)
 #define GV_SMEM_MAX (220 * 1024)  // dynamic shared memory a GEMV kernel may take
-#define GV_BARS 1024              // mbarrier area: GV_WARPS x GV_MAX_STAGES
+#define GV_BARS 2048              // mbarriers: a gate/up and a down set of GV_WARPS x GV_MAX_STAGES
 #define GV_MAX_STAGES 8           // ring stages of one warp
 #define GV_MIN_STAGES 2
 #define GV_CHUNK_TARGET 5120      // bytes of one ring stage (a chunk of a unit)
@@ -54,13 +55,6 @@
 #define GV_PERMUTE_MAX_R (MOE_DECODE_MAX_T * MOE_MAX_K)  // routes of one decode call
 
 namespace {
-
-// Work of one unit of a virtual expert with n_e routes, for balancing the CTAs' ranges: its
-// bytes, dequantisation and MMAs do not depend on n_e (the MMA computes all 8 columns of a
-// virtual expert), so every unit weighs GV_COST_MEM and routes GV_COST_TOK each.
-#define GV_COST_MEM 1
-#define GV_COST_TOK 0
-__host__ __device__ inline int unit_cost(int n_e) { return GV_COST_MEM + GV_COST_TOK * n_e; }
 
 // ------------------------------------------------------------------ launch plan
 
@@ -150,6 +144,8 @@ struct SlotHdr {
 };
 static_assert(sizeof(SlotHdr) <= 128, "slot header");
 
+// ints[GV_SYNC_OFF], [GV_SYNC_OFF + 1]: the fused GEMV launch's grid barrier (count, generation)
+#define GV_SYNC_OFF 4
 // int32 region: [0] n_active [1] n_virtual | active [E] | a_off [E+1] | routes [R] | ranges1 | ranges2
 __host__ __device__ inline int ws_active_off() { return 16; }
 __host__ __device__ inline int ws_aoff_off(int E) { return 16 + E; }
@@ -359,7 +355,7 @@ template <int XT, bool DOWN>
 __device__ __forceinline__ void act_load8(const FfnParams &p, int row, int col, float (&v)[8]) {
     if (DOWN) {
         const size_t q = (size_t)row * p.F + col;
-        const float4 a = *(const float4 *)(p.h + q), b = *(const float4 *)(p.h + q + 4);
+        const float4 a = __ldcg((const float4 *)(p.h + q)), b = __ldcg((const float4 *)(p.h + q + 4));
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     } else {
         const size_t off = (size_t)row * p.H + col;
@@ -510,11 +506,9 @@ __device__ void fill_chunk(const ActInfo &in, int H, int F, bool down, int NTL, 
 // thread, all partials of a thread in flight).  Runs between the gate/up and the down GEMV
 // when the gate/up kernel split K.
 template <int KS>
-__global__ void __launch_bounds__(256) ks_reduce_kernel(const float *__restrict__ gu, float *__restrict__ h,
-                                                        size_t n) {
-    pdl_wait();
-    pdl_trigger();
-    for (size_t q = (size_t)blockIdx.x * 256 + threadIdx.x; q < n; q += (size_t)gridDim.x * 256) {
+__device__ __forceinline__ void ks_reduce_range(const float *__restrict__ gu, float *__restrict__ h, size_t n,
+                                                size_t q0, size_t step) {
+    for (size_t q = q0; q < n; q += step) {
         float gp[KS], up[KS];
 #pragma unroll
         for (int k = 0; k < KS; ++k) {
@@ -531,6 +525,14 @@ __global__ void __launch_bounds__(256) ks_reduce_kernel(const float *__restrict_
     }
 }
 
+template <int KS>
+__global__ void __launch_bounds__(256) ks_reduce_kernel(const float *__restrict__ gu, float *__restrict__ h,
+                                                        size_t n) {
+    pdl_wait();
+    pdl_trigger();
+    ks_reduce_range<KS>(gu, h, n, (size_t)blockIdx.x * 256 + threadIdx.x, (size_t)gridDim.x * 256);
+}
+
 // ------------------------------------------------------------------ G1 / G2: the warp-ring kernel
 //
 // Units of a virtual expert: G1 has KS K ranges x F/32 row tiles, ordered (ks, g); unit
@@ -545,20 +547,26 @@ __global__ void __launch_bounds__(256) ks_reduce_kernel(const float *__restrict_
 // into the stage once all lanes are done with chunk J (after a __syncwarp).  A fill chunk or
 // a skipped expert's chunk arrives on its mbarrier without bytes.
 
-template <int QT, int XT, bool DOWN, int NTL>
-__global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
-    extern __shared__ __align__(128) unsigned char smem[];
+// The stage barriers of warp `warp` for the gate/up (DOWN false) or the down GEMV.
+template <bool DOWN>
+__device__ __forceinline__ uint64_t *gv_bars(unsigned char *smem, int warp) {
+    return (uint64_t *)smem + (DOWN ? GV_WARPS * GV_MAX_STAGES : 0) + warp * GV_MAX_STAGES;
+}
+
+// One GEMV over this CTA's unit range.  `gate()` is called once by every thread of the CTA
+// before anything produced by the earlier stages of the call (activations, h) is read:
+// at once when PRIME is false; when PRIME is true, after each warp's lane 0 has issued the
+// weight copies of its whole ring (they depend only on the routing metadata).
+template <int QT, int XT, bool DOWN, int NTL, bool PRIME, typename Gate>
+__device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem, Gate &&gate) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint64_t *bars = (uint64_t *)smem + warp * GV_MAX_STAGES;
-    if (lane == 0) {  // before the dependency wait: every stage barrier this warp may use
-        for (int s = 0; s < GV_MAX_STAGES; ++s) mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
-    pdl_wait();  // ranges, routing and activations come from earlier kernels
-    pdl_trigger();
+    uint64_t *bars = gv_bars<DOWN>(smem, warp);
     const int u0 = p.ranges[blockIdx.x], u1 = p.ranges[blockIdx.x + 1];
-    const unsigned long long first_src = lane == 0 ? p.first[blockIdx.x * GV_WARPS + warp] : 0ull;
-    if (u0 >= u1) return;
+    const unsigned long long first_src = !PRIME && lane == 0 ? p.first[blockIdx.x * GV_WARPS + warp] : 0ull;
+    if (u0 >= u1) {
+        gate();
+        return;
+    }
     constexpr int TBB = QT == MOE_Q8_0 ? 1088 : 640;  // bytes of a tile block (codes + scales)
     const GvGeom G = p.geo;
     const int K = DOWN ? p.F : p.H;
@@ -649,7 +657,9 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
     };
     if (lane == 0) {
         pc_first(u0);
-        if (pc_u == u0 + warp && first_src) {  // the permute kernel resolved it: issue at once
+        if (PRIME) {
+            top_up(S);
+        } else if (pc_u == u0 + warp && first_src) {  // the permute kernel resolved it: issue at once
             pc_src = first_src;
             pc_skip = false;
             pc_cached_v = pc_u / (upp * kspp);
@@ -659,6 +669,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
         }
     }
     __syncwarp();
+    gate();
 
     int J = 0;           // chunks this warp has reached
     int J_done = 0;      // chunks whose stage completed (waited on)
@@ -781,64 +792,166 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
         for (int j = J_done; j < J_issued; ++j) mbar_wait_bounded(&bars[j % S], (j / S) & 1, p.status);
 }
 
+template <int QT, int XT, bool DOWN, int NTL>
+__global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    if ((threadIdx.x & 31) == 0) {  // before the dependency wait: every stage barrier this warp may use
+        uint64_t *bars = gv_bars<DOWN>(smem, threadIdx.x >> 5);
+        for (int s = 0; s < GV_MAX_STAGES; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    pdl_wait();  // ranges, routing and activations come from earlier kernels
+    pdl_trigger();
+    ffn_body<QT, XT, DOWN, NTL, false>(p, smem, [] {});
+}
+
+// ------------------------------------------------------------------ G1 + R1 + G2 in one launch
+//
+// All CTAs are resident at once (cooperative launch, grid within the occupancy).  Each CTA
+// runs its gate/up units, then issues the weight copies of its down units into its rings
+// (the down weights depend only on the routing), and only then waits at a grid barrier for
+// every CTA's gate/up results; with a K split the grid forms h between two barriers.  The
+// down kernel's ramp-up thus overlaps the gate/up kernel's tail instead of following it.
+
+// Grid barrier: sync[0] counts the CTAs that arrived, sync[1] is the barrier's generation.
+// The last CTA to arrive resets the count and advances the generation, so the barrier can be
+// passed any number of times (sync[0] starts at 0: the permute kernel clears it).  The wait
+// is bounded: past GV_GRID_WAIT_NS the CTA sets MOE_ERR_TIMEOUT and goes on.
+#define GV_GRID_WAIT_NS 500000000ull
+__device__ __forceinline__ unsigned long long gv_globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int *a) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ void grid_sync(int *sync, int *status) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int gen = ld_acquire_gpu(sync + 1);
+        __threadfence();  // this CTA's writes before its arrival
+        if (atomicAdd(sync, 1) == (int)gridDim.x - 1) {
+            atomicExch(sync, 0);
+            __threadfence();
+            atomicAdd(sync + 1, 1);
+        } else {
+            const unsigned long long t0 = gv_globaltimer();
+            while (ld_acquire_gpu(sync + 1) == gen) {
+                if (gv_globaltimer() - t0 > GV_GRID_WAIT_NS) {
+                    moe_set_status(status, MOE_ERR_TIMEOUT);
+                    break;
+                }
+                __nanosleep(32);
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+}
+
+template <int QT, int XT, int NTL2>
+__global__ void __launch_bounds__(GV_THREADS, 1) ffn_fused_kernel(FfnParams p1, FfnParams p2, int *sync) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    if ((threadIdx.x & 31) == 0) {
+        uint64_t *b1 = gv_bars<false>(smem, threadIdx.x >> 5), *b2 = gv_bars<true>(smem, threadIdx.x >> 5);
+        for (int s = 0; s < GV_MAX_STAGES; ++s) {
+            mbar_init(&b1[s], 1);
+            mbar_init(&b2[s], 1);
+        }
+        fence_mbar_init();
+    }
+    pdl_wait();
+    pdl_trigger();
+    ffn_body<QT, XT, false, 2, false>(p1, smem, [] {});
+    __syncthreads();  // the gate/up rings and slots are no longer read: the down rings reuse them
+    ffn_body<QT, MOE_F32, true, NTL2, true>(p2, smem, [&] {
+        grid_sync(sync, p1.status);
+        if (p1.KS > 1) {
+            const size_t n = (size_t)p1.RT * p1.F, i0 = (size_t)blockIdx.x * GV_THREADS + threadIdx.x,
+                         step = (size_t)gridDim.x * GV_THREADS;
+            switch (p1.KS) {
+                case 2: ks_reduce_range<2>(p1.gu, p2.h, n, i0, step); break;
+                case 4: ks_reduce_range<4>(p1.gu, p2.h, n, i0, step); break;
+                case 8: ks_reduce_range<8>(p1.gu, p2.h, n, i0, step); break;
+                default: ks_reduce_range<16>(p1.gu, p2.h, n, i0, step); break;
+            }
+            grid_sync(sync, p1.status);
+        }
+    });
+}
+
 // ------------------------------------------------------------------ P1: permute
 
-// First unit whose start cost is >= x.  Active expert a has nv(a) = vb[a+1] - vb[a] virtual
-// experts, all of vt routes but the last; each of their per_v units costs
-// unit_cost(routes), so a's first unit starts at cost per_v * Q[a] with
-// Q[a] = GV_COST_MEM * vb[a] + GV_COST_TOK * aoff[a].
-__device__ __forceinline__ int unit_at_cost(long long x, int n_act, int per_v, int vt, const int *vb,
-                                            const int *aoff) {
-    auto Q = [&](int a) { return (long long)GV_COST_MEM * vb[a] + (long long)GV_COST_TOK * aoff[a]; };
-    if (x >= per_v * Q(n_act)) return vb[n_act] * per_v;
-    int lo = 0, hi = n_act - 1;  // largest a with per_v * Q[a] <= x
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) / 2;
-        if (per_v * Q(mid) <= x) lo = mid;
-        else hi = mid - 1;
+// Exclusive prefix sum over the 256 threads of the block of a 64-bit value (warp shuffles,
+// then the 8 warp totals); *total receives the sum over the block.  Every thread calls it.
+__device__ __forceinline__ unsigned long long block_scan_excl(unsigned long long v, unsigned long long *wsum,
+                                                              unsigned long long *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
     }
-    const long long rem = x - per_v * Q(lo);
-    const int nv = vb[lo + 1] - vb[lo];
-    const long long full = (long long)per_v * unit_cost(vt);
-    const int j = (int)min((long long)(nv - 1), rem / full);
-    const long long rem2 = rem - j * full;
-    const int cv = unit_cost(min(vt, aoff[lo + 1] - aoff[lo] - vt * j));
-    return (vb[lo] + j) * per_v + (int)((rem2 + cv - 1) / cv);
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    unsigned long long before = 0ull, all = 0ull;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        before += w < warp ? wsum[w] : 0ull;
+        all += wsum[w];
+    }
+    *total = all;
+    return before + x - v;
 }
 
 // Stable counting sort of the routes r = t*k + j by expert (restricted to a subset), the
 // ascending list of active experts and their route ranges, the virtual experts (groups of
-// at most vt routes of one expert) with where their weights are read from (slot in the
+// at most GV_TOK routes of one expert) with where their weights are read from (slot in the
 // pool, or the pinned host image for a fill, written through by the first group only), and
-// the unit ranges of the CTAs of both GEMV launches, balanced by work (unit_cost).
+// the unit ranges of the CTAs of both GEMV launches.  Every unit weighs the same (its bytes,
+// dequantisation and MMAs do not depend on its routes: the MMA computes every column of a
+// virtual expert), so CTA c of G takes units [floor(c U / G), floor((c+1) U / G)).
+//
+// One CTA of 256 threads, everything in shared memory, no serial loop: a route's rank among
+// the earlier routes of its expert comes from a warp match (rank within the warp) plus the
+// counts of the earlier warps; offsets, active-expert indices and virtual-expert bases come
+// from one block-wide scan over the experts.
 __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict__ ids, int R, int E,
                                                       const int32_t *__restrict__ subset, int n_subset,
                                                       int32_t *__restrict__ ints, ActInfo *__restrict__ info,
                                                       const int32_t *__restrict__ slot_table, int n_slots,
                                                       const uint8_t *pool, size_t slot_bytes,
                                                       const unsigned long long *__restrict__ fill_src,
-                                                      int vt, int G1, int per_v1, int G2, int per_v2,
+                                                      int G1, int per_v1, int G2, int per_v2,
                                                       unsigned long long *__restrict__ first, int *status) {
-    // everything the kernel reads is loaded once into shared memory (R <= GV_PERMUTE_MAX_R)
-    __shared__ int cnt[MOE_MAX_E], off[MOE_MAX_E + 1];
-    __shared__ int vb[MOE_MAX_E + 1], s_active[MOE_MAX_E], s_aoff[MOE_MAX_E + 1], s_slot[MOE_MAX_E];
-    __shared__ unsigned long long s_fill[MOE_MAX_E];
+    static_assert(GV_PERMUTE_MAX_R <= 256 && MOE_MAX_E <= 256, "one route and one expert per thread");
+    constexpr int NW = 8;  // warps
+    __shared__ int cntw[NW][MOE_MAX_E];  // routes of expert e in warp w; then the earlier warps' count
+    __shared__ int s_off[MOE_MAX_E], s_slot[MOE_MAX_E];
+    __shared__ int s_active[MOE_MAX_E], s_aoff[MOE_MAX_E + 1], vb[MOE_MAX_E + 1];
+    __shared__ unsigned long long s_fill[MOE_MAX_E], wsum[NW];
     __shared__ unsigned char insub[MOE_MAX_E];
-    __shared__ int s_ids[GV_PERMUTE_MAX_R], s_routes[GV_PERMUTE_MAX_R];
+    __shared__ int s_routes[GV_PERMUTE_MAX_R];
+    __shared__ int s_rng[2][GV_MAX_GRID + 1];
     // per virtual expert: where its weights are read from (0: skip or fill), for the first-unit
-    // table below; up to GV_VSRC entries, the rest read back from `info`
+    // table; up to GV_VSRC entries (the most a decode call has), the rest read back from info
     constexpr int GV_VSRC = 512;
     __shared__ unsigned long long vsrc[GV_VSRC];
-    __shared__ int n_act;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();  // ids and the slot table come from earlier kernels
     pdl_trigger();
-    for (int r = tid; r < R; r += 256) s_ids[r] = ids[r];
-    for (int e = tid; e < E; e += 256) {
-        cnt[e] = 0;
-        insub[e] = subset ? 0 : 1;
-        s_slot[e] = slot_table ? slot_table[e] : e;
-        s_fill[e] = fill_src ? fill_src[e] : 0ull;
+    // ---- loads (one round trip) and clears
+    const int e_r = tid < R ? ids[tid] : -1;  // this thread's route
+    if (tid < E) {
+        s_slot[tid] = slot_table ? slot_table[tid] : tid;
+        s_fill[tid] = fill_src ? fill_src[tid] : 0ull;
+        insub[tid] = subset ? 0 : 1;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) cntw[w][tid] = 0;
     }
     __syncthreads();
     if (subset) {
@@ -849,52 +962,66 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
         }
         __syncthreads();
     }
-    for (int r = tid; r < R; r += 256) {
-        const int e = s_ids[r];
-        if (e < 0 || e >= E) { moe_set_status(status, MOE_ERR_INVALID); continue; }
-        if (insub[e]) atomicAdd(&cnt[e], 1);
+    // ---- per warp: rank of each route among the warp's routes of its expert, and counts
+    int e = -1;
+    if (tid < R) {
+        if (e_r < 0 || e_r >= E) moe_set_status(status, MOE_ERR_INVALID);
+        else if (insub[e_r]) e = e_r;
     }
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    const int wrank = __popc(grp & ((1u << lane) - 1u));
+    if (e >= 0 && wrank == 0) cntw[warp][e] = __popc(grp);
     __syncthreads();
-    int *active = ints + ws_active_off();
-    int *aoff = ints + ws_aoff_off(E);
-    if (tid == 0) {
-        int s = 0, na = 0, nv = 0;
-        for (int e = 0; e < E; ++e) {
-            off[e] = s;
-            if (cnt[e] > 0) {
-                s_active[na] = e;
-                s_aoff[na] = s;
-                vb[na] = nv;
-                nv += (cnt[e] + vt - 1) / vt;
-                ++na;
-            }
-            s += cnt[e];
+    // ---- per expert: count, earlier-warp counts, then the scan over experts
+    int cnt = 0;
+    if (tid < E) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const int c = cntw[w][tid];
+            cntw[w][tid] = cnt;
+            cnt += c;
         }
-        s_aoff[na] = s;
-        vb[na] = nv;
-        ints[0] = na;
-        ints[1] = nv;
-        n_act = na;
+    }
+    const int nvirt = (cnt + GV_TOK - 1) / GV_TOK;
+    // packed (route offset, active index, virtual base): each field < 2^20
+    const unsigned long long packed = (unsigned long long)cnt | ((unsigned long long)(cnt > 0) << 20) |
+                                      ((unsigned long long)nvirt << 40);
+    unsigned long long tot;
+    const unsigned long long ex = block_scan_excl(packed, wsum, &tot);
+    const int off_e = (int)(ex & 0xFFFFF), aidx = (int)((ex >> 20) & 0xFFFFF), vbase = (int)(ex >> 40);
+    const int n_act = (int)((tot >> 20) & 0xFFFFF), n_routes = (int)(tot & 0xFFFFF), n_virt = (int)(tot >> 40);
+    if (tid < E) {
+        s_off[tid] = off_e;
+        if (cnt > 0) {
+            s_active[aidx] = tid;
+            s_aoff[aidx] = off_e;
+            vb[aidx] = vbase;
+        }
+    }
+    if (tid == 0) {
+        s_aoff[n_act] = n_routes;
+        vb[n_act] = n_virt;
+        ints[0] = n_act;
+        ints[1] = n_virt;
+        ints[GV_SYNC_OFF] = 0;  // the fused GEMV's grid barrier count
     }
     __syncthreads();
-    for (int a = tid; a <= n_act; a += 256) {
-        aoff[a] = s_aoff[a];
-        if (a < n_act) active[a] = s_active[a];
-    }
-    // stable order of the routes of each expert: rank among the earlier routes of the same expert
+    // ---- routes in expert order (stable: warp order, then lane order)
     int *routes = ints + ws_routes_off(E);
-    for (int r = tid; r < R; r += 256) {
-        const int e = s_ids[r];
-        if (e < 0 || e >= E || !insub[e]) continue;
-        int rank = 0;
-        for (int i = 0; i < r; ++i) rank += (s_ids[i] == e);
-        s_routes[off[e] + rank] = r;
-        routes[off[e] + rank] = r;
+    if (e >= 0) {
+        const int pos = s_off[e] + cntw[warp][e] + wrank;
+        s_routes[pos] = tid;
+        routes[pos] = tid;
+    }
+    {
+        int *active = ints + ws_active_off(), *aoff = ints + ws_aoff_off(E);
+        if (tid < n_act) active[tid] = s_active[tid];
+        if (tid <= n_act) aoff[tid] = s_aoff[tid];
     }
     __syncthreads();
-    for (int a = tid; a < n_act; a += 256) {
-        const int e = s_active[a];
-        const int slot = s_slot[e];
+    // ---- virtual experts of each active expert
+    if (tid < n_act) {
+        const int a = tid, ex_id = s_active[a], slot = s_slot[ex_id];
         const int n_e = s_aoff[a + 1] - s_aoff[a];
         ActInfo in;
         in.fill = in.wt = 0;
@@ -904,46 +1031,61 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
             moe_set_status(status, MOE_ERR_INVALID);  // nothing of this expert is read
         } else {
             in.dst = (unsigned long long)(pool + (size_t)slot * slot_bytes);
-            const unsigned long long f = s_fill[e];
+            const unsigned long long f = s_fill[ex_id];
             in.fill = f != 0ull;
             in.src = f ? f : in.dst;
         }
         for (int j = 0; j < vb[a + 1] - vb[a]; ++j) {
-            in.pos0 = s_aoff[a] + vt * j;
-            in.n_e = bad ? 0 : min(vt, n_e - vt * j);
+            in.pos0 = s_aoff[a] + GV_TOK * j;
+            in.n_e = bad ? 0 : min(GV_TOK, n_e - GV_TOK * j);
             in.wt = in.fill && j == 0;
+#pragma unroll
             for (int t = 0; t < GV_TOK; ++t) in.rt[t] = t < in.n_e ? s_routes[in.pos0 + t] : 0;
             info[vb[a] + j] = in;
             if (vb[a] + j < GV_VSRC) vsrc[vb[a] + j] = in.n_e > 0 && !in.fill ? in.src : 0ull;
         }
     }
-    __syncthreads();
+    // ---- unit ranges of both launches
     {
-        int *r1 = ints + ws_ranges_off(E, R, 0), *r2 = ints + ws_ranges_off(E, R, 1);
-        const long long Cv = (long long)GV_COST_MEM * vb[n_act] + (long long)GV_COST_TOK * s_aoff[n_act];
-        const long long C1 = (long long)per_v1 * Cv, C2 = (long long)per_v2 * Cv;
-        for (int c = tid; c <= G1; c += 256) r1[c] = unit_at_cost(C1 * c / G1, n_act, per_v1, vt, vb, s_aoff);
-        for (int c = tid; c <= G2; c += 256) r2[c] = unit_at_cost(C2 * c / G2, n_act, per_v2, vt, vb, s_aoff);
-        __syncthreads();
-        // where each warp's first unit (unit ranges[c] + warp) is read from, so that a GEMV warp
-        // can issue its first copy with the range load (0: no such unit, a skip or a fill)
+        const int G[2] = {G1, G2}, per_v[2] = {per_v1, per_v2};
+#pragma unroll
         for (int l = 0; l < 2; ++l) {
-            const int *rr = l ? r2 : r1;
-            const int G = l ? G2 : G1, per_v = l ? per_v2 : per_v1;
-            unsigned long long *fo = first + (size_t)l * GV_MAX_GRID * GV_WARPS;
-            for (int i = tid; i < G * GV_WARPS; i += 256) {
-                const int c = i / GV_WARPS, u = rr[c] + i % GV_WARPS;
+            int *rg = ints + ws_ranges_off(E, R, l);
+            const unsigned long long U = (unsigned long long)n_virt * per_v[l];
+            for (int c = tid; c <= G[l]; c += 256) {
+                const int u = (int)(U * (unsigned long long)c / (unsigned long long)G[l]);
+                s_rng[l][c] = u;
+                rg[c] = u;
+            }
+        }
+    }
+    __syncthreads();
+    // ---- where each warp's first unit (unit ranges[c] + warp) is read from, so that a GEMV warp
+    // can issue its first copy with the range load (0: no such unit, a skip or a fill).  The 16
+    // units of a CTA row start at v0 = ranges[c] / per_v and cross into the next virtual
+    // expert at most per_v apart.
+#pragma unroll
+    for (int l = 0; l < 2; ++l) {
+        const int G = l ? G2 : G1, pv = l ? per_v2 : per_v1;
+        unsigned long long *fo = first + (size_t)l * GV_MAX_GRID * GV_WARPS;
+        for (int c = tid; c < G; c += 256) {
+            const int u0 = s_rng[l][c], u1 = s_rng[l][c + 1];
+            int v = u0 / pv, r = u0 - v * pv;
+            for (int w = 0; w < GV_WARPS; ++w) {
                 unsigned long long d = 0ull;
-                if (u < rr[c + 1]) {
-                    const int v = u / per_v;
+                if (u0 + w < u1) {
                     if (v < GV_VSRC) {
                         d = vsrc[v];
                     } else {
-                        const ActInfo &in = info[v];
+                        const ActInfo &in = info[v];  // written above by this CTA
                         if (in.n_e > 0 && !in.fill) d = in.src;
                     }
                 }
-                fo[i] = d;
+                fo[(size_t)c * GV_WARPS + w] = d;
+                if (++r == pv) {
+                    r = 0;
+                    ++v;
+                }
             }
         }
     }
@@ -971,11 +1113,14 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(const float4 *__restr
                                                            const float4 *extra, float4 *y, float4 *xn,
                                                            float eps) {
     __shared__ float red[8];
+    constexpr int KEEP = 4;  // sums kept in registers for the scaling pass (H <= 4096 at 256 threads)
     const int t = blockIdx.x;
     pdl_wait();  // the partial outputs come from the down GEMV
     pdl_trigger();
     float ss = 0.f;
-    for (int h = threadIdx.x; h < H4; h += blockDim.x) {
+    float4 keep[KEEP];
+    int n = 0;
+    for (int h = threadIdx.x; h < H4; h += blockDim.x, ++n) {
         float4 s = extra ? extra[(size_t)t * H4 + h] : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < k; ++j) {
             const float4 v = partial[((size_t)t * k + j) * H4 + h];
@@ -983,7 +1128,10 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(const float4 *__restr
         }
         if (y) y[(size_t)t * H4 + h] = s;
         ss += s.x * s.x + s.y * s.y + s.z * s.z + s.w * s.w;
-        if (xn) xn[(size_t)t * H4 + h] = s;  // scaled below
+#pragma unroll
+        for (int i = 0; i < KEEP; ++i)
+            if (i == n) keep[i] = s;
+        if (xn && n >= KEEP) xn[(size_t)t * H4 + h] = s;  // scaled below
     }
     if (!xn) return;
 #pragma unroll
@@ -993,8 +1141,16 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(const float4 *__restr
     float tot = 0.f;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
     const float inv = 1.0f / sqrtf(tot / (float)(4 * H4) + eps);
-    for (int h = threadIdx.x; h < H4; h += blockDim.x) {
-        float4 v = xn[(size_t)t * H4 + h];
+    n = 0;
+    for (int h = threadIdx.x; h < H4; h += blockDim.x, ++n) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (n < KEEP) {
+#pragma unroll
+            for (int i = 0; i < KEEP; ++i)
+                if (i == n) v = keep[i];
+        } else {
+            v = xn[(size_t)t * H4 + h];
+        }
         v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
         xn[(size_t)t * H4 + h] = v;
     }
@@ -1057,12 +1213,71 @@ const void *gemv_kernel_for(int qtype, int xtype, bool down, int ntl) {
     return xtype == MOE_F32 ? warp_fn<MOE_Q4_SM, MOE_F32, false, 2>() : warp_fn<MOE_Q4_SM, MOE_BF16, false, 2>();
 }
 
+template <int QT, int XT, int NTL2>
+const void *fused_fn() {
+    return (const void *)ffn_fused_kernel<QT, XT, NTL2>;
+}
+
+const void *fused_kernel_for(int qtype, int xtype, int ntl2) {
+    if (qtype == MOE_Q8_0) {
+        if (xtype == MOE_F32) return ntl2 == 2 ? fused_fn<MOE_Q8_0, MOE_F32, 2>() : fused_fn<MOE_Q8_0, MOE_F32, 1>();
+        return ntl2 == 2 ? fused_fn<MOE_Q8_0, MOE_BF16, 2>() : fused_fn<MOE_Q8_0, MOE_BF16, 1>();
+    }
+    if (xtype == MOE_F32) return ntl2 == 2 ? fused_fn<MOE_Q4_SM, MOE_F32, 2>() : fused_fn<MOE_Q4_SM, MOE_F32, 1>();
+    return ntl2 == 2 ? fused_fn<MOE_Q4_SM, MOE_BF16, 2>() : fused_fn<MOE_Q4_SM, MOE_BF16, 1>();
+}
+
+// Process-wide choice between the fused GEMV launch and the separate kernels.
+std::atomic<int> g_fused{0};
+// Whether a cooperative launch also takes the programmatic-dependency attribute (learnt at the
+// first fused launch: 1 yes, 0 no, -1 not tried).
+std::atomic<int> g_coop_pdl{-1};
+
 }  // namespace
+
+// A launch whose CTAs wait on one another: cooperative (the driver refuses a grid that cannot
+// be resident at once), with the programmatic dependency on the previous kernel when the
+// driver takes both attributes together.
+static int launch_cooperative(const void *fn, dim3 grid, size_t smem, cudaStream_t s, void **args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    moe_pdl_config(&cfg, attr, grid, dim3(GV_THREADS), smem, s);
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    const int mode = g_coop_pdl.load();
+    if (mode != 0) {
+        cfg.numAttrs = 2;
+        const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+        if (e == cudaSuccess) {
+            g_coop_pdl.store(1);
+            return MOE_OK;
+        }
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (mode == 1 || cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+            moe_note_cuda_error(e);
+            return MOE_ERR_CUDA;
+        }
+        (void)cudaGetLastError();  // the combination was refused: launch cooperative alone
+        g_coop_pdl.store(0);
+    }
+    cfg.attrs = attr + 1;
+    cfg.numAttrs = 1;
+    MOE_TRY_CUDA(cudaLaunchKernelExC(&cfg, fn, args));
+    return MOE_OK;
+}
+
+extern "C" int moe_set_decode_fused(int on) {
+    g_fused.store(on ? 1 : 0);
+    return MOE_OK;
+}
+
+extern "C" int moe_get_decode_fused(void) { return g_fused.load(); }
 
 int moe_decode_ffn_launches(int T, int H, int F, int qtype, int E, int k) {
     GvPlan pl;
     if (T <= 0 || !gv_plan(T, H, F, qtype, gv_n_act_max(T, E, k), &pl)) return 0;
-    return pl.KS > 1 ? 4 : 3;  // permute, gate/up, (K-split reduce,) down
+    if (g_fused.load()) return 2;  // permute, fused gate/up + down
+    return pl.KS > 1 ? 4 : 3;       // permute, gate/up, (K-split reduce,) down
 }
 
 size_t moe_decode_workspace_bytes(int T, int H, int F, int qtype, int E, int k) {
@@ -1150,8 +1365,15 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
     const int n_act_max = expert_subset ? n_subset : gv_n_act_max(T, E, k);
     const long n_virt_max = n_act_max + (long)T * k / GV_TOK + 1;
     const int per_v1 = pl.KS * RTF, per_v2 = RTH / pl.TPU;
-    const int G1 = (int)std::max(1L, std::min((long)cap1, n_virt_max * per_v1));
-    const int G2 = (int)std::max(1L, std::min((long)cap2, n_virt_max * per_v2));
+    // One grid for both GEMVs, so that the permute kernel's unit ranges serve the fused launch
+    // and the separate kernels alike.
+    const void *kf = fused_kernel_for(qtype, xtype, pl.TPU);
+    const size_t smemf = std::max(smem1, smem2);
+    int capf = 0;
+    if ((rc = ring_grid_capacity(kf, smemf, &capf)) != MOE_OK) return rc;
+    const int cap = std::min(std::min(cap1, cap2), capf);
+    const int G1 = (int)std::max(1L, std::min((long)cap, n_virt_max * std::max(per_v1, per_v2)));
+    const int G2 = G1;
 
     FfnParams p;
     p.x = x;
@@ -1178,12 +1400,30 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
                                         (int32_t *)((char *)workspace + W.ints_off),
                                         (ActInfo *)((char *)workspace + W.info_off), d_slot_table, n_slots,
                                         (const uint8_t *)pool, slot_bytes,
-                                        (const unsigned long long *)d_fill_src, (int)GV_TOK, G1, per_v1, G2, per_v2,
+                                        (const unsigned long long *)d_fill_src, G1, per_v1, G2, per_v2,
                                         (unsigned long long *)((char *)workspace + W.first_off), p.status));
     }
     if (timing && timing->permute1) MOE_TRY_CUDA(cudaEventRecord(timing->permute1, s));
     }
     void *args[] = {&p};
+    constexpr int kGemvStages = MOE_FFN_GATEUP | MOE_FFN_REDUCE | MOE_FFN_DOWN;
+    if (g_fused.load() && (stages & kGemvStages) == kGemvStages) {
+        if (timing && timing->gateup0) MOE_TRY_CUDA(cudaEventRecord(timing->gateup0, s));
+        FfnParams p1 = p, p2 = p;
+        p1.geo = pl.g1;
+        p1.ranges = p.ws_ints + ws_ranges_off(E, T * k, 0);
+        p1.first = (const unsigned long long *)((char *)workspace + W.first_off);
+        p2.geo = pl.g2;
+        p2.ranges = p.ws_ints + ws_ranges_off(E, T * k, 1);
+        p2.first = p1.first + (size_t)GV_MAX_GRID * GV_WARPS;
+        int *sync = (int *)((char *)workspace + W.ints_off) + GV_SYNC_OFF;
+        void *fargs[] = {&p1, &p2, &sync};
+        if ((rc = launch_cooperative(kf, dim3(G1), smemf, s, fargs)) != MOE_OK) return rc;
+        if (timing && timing->gateup1) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
+        if (timing && timing->down0) MOE_TRY_CUDA(cudaEventRecord(timing->down0, s));
+        if (timing && timing->down1) MOE_TRY_CUDA(cudaEventRecord(timing->down1, s));
+        return MOE_OK;
+    }
     if (stages & MOE_FFN_GATEUP) {
         if (timing && timing->gateup0) MOE_TRY_CUDA(cudaEventRecord(timing->gateup0, s));
         p.geo = pl.g1;

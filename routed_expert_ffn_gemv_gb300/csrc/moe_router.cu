@@ -141,7 +141,10 @@ router_topk_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__r
             ((uint16_t *)w_s)[i] = w_router[(size_t)h0 * E + i];
     }
     if (tid == 0) ((uint16_t *)w_s)[(size_t)HS * E] = 0;  // pad read by the odd-E pair
-    pdl_wait();  // x comes from the previous kernel (the weights do not)
+    __shared__ float bias_s[MOE_MAX_E];
+    if (rank == 0)
+        for (int e = tid; e < E; e += MOE_ROUTER_THREADS) bias_s[e] = bias ? bias[e] : 0.f;
+    pdl_wait();  // x comes from the previous kernel (the weights and the bias do not)
     pdl_trigger();
     // ---- x slice of this cluster's tokens
     for (int i = tid; i < TT * HS; i += MOE_ROUTER_THREADS) {
@@ -208,7 +211,7 @@ router_topk_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__r
                     float s = 0.f;
                     for (int r = 0; r < MOE_ROUTER_CLUSTER; ++r)
                         s += ld_cluster_f32(cluster_map(&part[(size_t)t * E + e], r));
-                    if (bias) s += bias[e];
+                    if (bias) s += bias_s[e];
                     if (logits_out) logits_out[(size_t)(t0 + t) * E + e] = s;
                     v[i] = (s != s) ? -INFINITY : s;  // NaN never wins
                 }

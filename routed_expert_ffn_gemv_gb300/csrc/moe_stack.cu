@@ -538,7 +538,7 @@ extern "C" int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, in
     const size_t per = align256((size_t)R * 4) * 2 + align256((size_t)R * d.H * 4) + align256(wsb);
     char *buf = nullptr;
     MOE_TRY_CUDA(cudaMalloc(&buf, per * L));
-    cudaEvent_t ev[4] = {};
+    cudaEvent_t ev[5] = {};
     int rc = MOE_OK;
     auto lay = [&](int l, int32_t **ids, float **w, float **partial, void **ws) {
         char *b = buf + per * l;
@@ -554,7 +554,7 @@ extern "C" int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, in
         return moe_expert_ffn_stages(x_in, MOE_F32, T, d.H, d.F, d.qtype, d.E, d.k, ids, w, nullptr, d.E, pool,
                                      d.slot_bytes, nullptr, 0, nullptr, partial, ws, wsb, s, nullptr, what);
     };
-    for (int i = 0; i < 4 && rc == MOE_OK; ++i)
+    for (int i = 0; i < 5 && rc == MOE_OK; ++i)
         if (cudaEventCreate(&ev[i]) != cudaSuccess) rc = MOE_ERR_CUDA;
     for (int l = 0; l < L && rc == MOE_OK; ++l) {  // routing of every layer, then its permute
         int32_t *ids; float *w, *partial; void *ws;
@@ -564,8 +564,9 @@ extern "C" int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, in
     }
     for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_GATEUP | MOE_FFN_REDUCE);  // warm-up
     for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_DOWN);
+    for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_ALL);
     if (rc == MOE_OK) {  // about 40 us of host time per launch to queue, at least 2 ms
-        const unsigned long long ns = std::max(2000000ull, 40000ull * 2 * (unsigned long long)reps * L);
+        const unsigned long long ns = std::max(2000000ull, 40000ull * 3 * (unsigned long long)reps * L);
         spacer_kernel<<<1, 32, 0, s>>>(ns);
         if (cudaGetLastError() != cudaSuccess) rc = MOE_ERR_CUDA;
     }
@@ -579,9 +580,13 @@ extern "C" int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, in
     for (int r = 0; r < reps && rc == MOE_OK; ++r)
         for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_DOWN);
     if (rc == MOE_OK && cudaEventRecord(ev[3], s) != cudaSuccess) rc = MOE_ERR_CUDA;
+    for (int r = 0; r < reps && rc == MOE_OK; ++r)
+        for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_ALL);
+    if (rc == MOE_OK && cudaEventRecord(ev[4], s) != cudaSuccess) rc = MOE_ERR_CUDA;
     if (rc == MOE_OK && cudaStreamSynchronize(s) != cudaSuccess) rc = MOE_ERR_CUDA;
     if (rc == MOE_OK) {
-        float t1 = 0.f, t2 = 0.f, t3 = 0.f;
+        float t1 = 0.f, t2 = 0.f, t3 = 0.f, t4 = 0.f;
+        cudaEventElapsedTime(&t4, ev[3], ev[4]);
         cudaEventElapsedTime(&t1, ev[0], ev[1]);
         cudaEventElapsedTime(&t3, ev[1], ev[2]);
         cudaEventElapsedTime(&t2, ev[2], ev[3]);
@@ -597,11 +602,13 @@ extern "C" int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, in
         out->gateup_us = 1e3 * t1 / n_l;
         out->down_us = 1e3 * t2 / n_l;
         out->reduce_us = 1e3 * t3 / n_l;
+        out->gemv_us = 1e3 * t4 / n_l;
+        out->fused = moe_get_decode_fused();
         out->gateup_bytes = nact / L * 2 * moe_matrix_bytes(d.qtype, d.F, d.H);
         out->down_bytes = nact / L * moe_matrix_bytes(d.qtype, d.H, d.F);
         out->launches = n_l;
     }
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 5; ++i)
         if (ev[i]) cudaEventDestroy(ev[i]);
     cudaFree(buf);
     return rc;

@@ -122,8 +122,17 @@ FFN_CASES = [
 ]
 
 
+@pytest.fixture(params=[True, False], ids=["fused", "separate"])
+def gemv_mode(request):
+    """Runs a test with the decode GEMVs as one fused launch, then as three kernels."""
+    before = L.moe_get_decode_fused()
+    L.moe_set_decode_fused(request.param)
+    yield request.param
+    L.moe_set_decode_fused(before)
+
+
 @pytest.mark.parametrize("qtype,H,F,E,k,T,rs,xtype", FFN_CASES)
-def test_expert_ffn_parity(qtype, H, F, E, k, T, rs, xtype):
+def test_expert_ffn_parity(qtype, H, F, E, k, T, rs, xtype, gemv_mode):
     cfg = synth.small_config(qtype, H=H, F=F, E=E, k=k, seed_cfg=800 + H + F)
     pool, stride = make_pool(cfg, 0, range(E), rs)
     rng = np.random.default_rng(T * 31 + E)
@@ -145,6 +154,28 @@ def test_expert_ffn_parity(qtype, H, F, E, k, T, rs, xtype):
             worst = max(worst, err)
     assert worst <= TOL, worst
     assert worst <= 1e-4, worst  # fp32 accumulation of exact products stays far below 2e-3
+
+
+@pytest.mark.parametrize("qtype,H,F,E,k,T,rs,xtype", FFN_CASES)
+def test_fused_and_separate_gemvs_agree_bit_for_bit(qtype, H, F, E, k, T, rs, xtype):
+    """The fused launch and the three separate kernels do the same arithmetic in the same order."""
+    cfg = synth.small_config(qtype, H=H, F=F, E=E, k=k, seed_cfg=900 + H + F)
+    pool, stride = make_pool(cfg, 0, range(E), rs)
+    rng = np.random.default_rng(T * 17 + E)
+    x = rng.standard_normal((T, H), dtype=np.float32)
+    x_d = to_dev(synth.f32_to_bf16_bits(x).view(np.int16)) if xtype == 1 else to_dev(x)
+    ids, w = random_routes(rng, T, E, k)
+    before = L.moe_get_decode_fused()
+    try:
+        out = {}
+        for mode in (True, False):
+            L.moe_set_decode_fused(mode)
+            out[mode] = run_ffn(cfg, pool, stride, x_d, xtype, ids, w).cpu().numpy()
+    finally:
+        L.moe_set_decode_fused(before)
+    status_clear()
+    assert np.all(np.isfinite(out[True]))
+    assert np.array_equal(out[True].view(np.uint32), out[False].view(np.uint32))
 
 
 def test_expert_ffn_subset_and_slot_table():

@@ -227,39 +227,33 @@ def gemv_roofline(cfg, T, torch, stream, steps=40, warmup=5):
 
 
 def gemv_roofline_block(gv, cfg, T, peaks):
-    """The roofline object of the JSON line.  The unit that moves the decode path's weight
-    bytes is one layer's FFN chain: the permute kernel (routing metadata and work ranges),
-    the gate/up GEMV, the K-split reduce and the down GEMV (or their fused launch); its
-    bytes are the selected experts' quantised blocks.  The separate kernels' own figures
-    (each timed in rounds of its own) stand beside it."""
+    """The roofline object of the JSON line: the decode path's dominant kernel, the gate/up
+    GEMV (ffn_warp_kernel, two thirds of the weight bytes), timed in rounds of its own launches
+    back to back; beside it the down GEMV and the K-split reduce timed the same way, and one
+    layer's whole chain (permute, gate/up, reduce, down; or the fused launch when the library
+    runs it) with the selected experts' bytes of all three matrices."""
     def gbs(b, ms):
         return b / (ms / 1e3) / 1e9 if ms > 0 else 0.0
     hbm = peaks["hbm_gbs"]
     gu_ms, gu_b = gv["gateup_ms_per_launch"], gv["gateup_bytes_per_launch"]
     dn_ms, dn_b = gv["down_ms_per_launch"], gv["down_bytes_per_launch"]
-    separate = {"gateup_kernel": {"achieved_gbs": gbs(gu_b, gu_ms), "frac": gbs(gu_b, gu_ms) / hbm,
-                                  "ms_per_launch": gu_ms, "algorithmic_bytes_per_launch": gu_b},
-                "down_kernel": {"achieved_gbs": gbs(dn_b, dn_ms), "frac": gbs(dn_b, dn_ms) / hbm,
-                                "ms_per_launch": dn_ms, "algorithmic_bytes_per_launch": dn_b},
-                "ks_reduce_kernel_ms_per_launch": gv["reduce_ms_per_launch"],
-                "ms_per_layer": gu_ms + gv["reduce_ms_per_launch"] + dn_ms,
-                "measured_in": "each kernel alone in rounds of back-to-back launches over all layers"}
-    if gv["fused"]:
-        kernel = ("decode FFN chain per layer: permute_kernel -> ffn_fused_kernel<q8_0> "
-                  "(gate/up GEMV + SwiGLU, K-split reduce, down GEMV + weighting in one launch)")
-    else:
-        kernel = ("decode FFN chain per layer: permute_kernel -> ffn_warp_kernel<q8_0, gate/up> "
-                  "-> ks_reduce_kernel -> ffn_warp_kernel<q8_0, down>")
-    ms, b = gv["gemv_ms_per_launch"], gu_b + dn_b
-    tr = traffic_record(f"chain_q8_0_h{cfg.H}_t{T}")
-    return {"kernel": kernel, "bound": "hbm", "achieved": gbs(b, ms), "peak": hbm, "unit": "GB/s",
-            "frac": gbs(b, ms) / hbm, "peak_source": peaks["source"],
-            "traffic": None if tr is None else tr["bytes_per_launch"],
-            "algorithmic_bytes_per_launch": b, "ms_per_launch": ms, "launches": gv["launches"],
-            "separate_kernels": separate,
+    ch_ms, ch_b = gv["gemv_ms_per_launch"], gu_b + dn_b
+    tr = traffic_record(f"gateup_q8_0_h{cfg.H}_t{T}")
+    chain = ("permute_kernel -> ffn_fused_kernel (gate/up + reduce + down in one launch)" if gv["fused"] else
+             "permute_kernel -> ffn_warp_kernel<gate/up> -> ks_reduce_kernel -> ffn_warp_kernel<down>")
+    return {"kernel": "ffn_warp_kernel<q8_0, gate/up> (dequantising gate/up GEMV + SwiGLU)", "bound": "hbm",
+            "achieved": gbs(gu_b, gu_ms), "peak": hbm, "unit": "GB/s", "frac": gbs(gu_b, gu_ms) / hbm,
+            "peak_source": peaks["source"], "traffic": None if tr is None else tr["bytes_per_launch"],
+            "algorithmic_bytes_per_launch": gu_b, "ms_per_launch": gu_ms, "launches": gv["launches"],
+            "down_kernel": {"achieved_gbs": gbs(dn_b, dn_ms), "frac": gbs(dn_b, dn_ms) / hbm,
+                            "ms_per_launch": dn_ms, "algorithmic_bytes_per_launch": dn_b},
+            "ks_reduce_kernel_ms_per_launch": gv["reduce_ms_per_launch"],
+            "layer_chain": {"kernels": chain, "achieved_gbs": gbs(ch_b, ch_ms), "frac": gbs(ch_b, ch_ms) / hbm,
+                            "ms_per_layer": ch_ms, "algorithmic_bytes_per_layer": ch_b},
             "measured_in": ("HBM-resident stack (all %d x %d expert images in HBM, above L2), batch %d; "
-                            "each layer's chain launched back to back over all layers, CUDA events on the "
-                            "launching stream around the rounds (launch gaps included)" % (cfg.L, cfg.E, T))}
+                            "each kernel (and each layer's chain) launched back to back over all layers in "
+                            "rounds, CUDA events on the launching stream around the rounds (launch gaps "
+                            "included)" % (cfg.L, cfg.E, T))}
 
 
 def max_over_ranks(v, world, torch):

@@ -46,7 +46,6 @@
 #define GV_MAX_STAGES 8           // ring stages of one warp
 #define GV_MIN_STAGES 2
 #define GV_CHUNK_TARGET 5120      // bytes of one ring stage (a chunk of a unit)
-#define GV_FILL_BATCH 8           // 16-byte pieces per lane loaded together by a fill chunk
 #define GV_MAX_GRID 1024          // CTAs per launch (bounds the precomputed range tables)
 #define GV_UNITS_TARGET 1824      // units per launch the K split aims for (~12 per CTA)
 #define GV_KS_MAX 8               // largest K split of the gate/up GEMV
@@ -177,6 +176,11 @@ inline WsLayout ws_layout(int T, int H, int F, int qtype, int E, int k) {
     L.total = L.first_off + (size_t)2 * GV_MAX_GRID * GV_WARPS * 8;
     return L;
 }
+
+// how a chunk reaches its ring stage
+#define GV_BULK 0  // bulk copy from the slot (HBM)
+#define GV_FILL 1  // cp.async pieces from the pinned host image (a miss of a device-managed pool)
+#define GV_SKIP 2  // nothing (invalid slot): the stage barrier completes without bytes
 
 struct FfnParams {
     const void *x;
@@ -462,40 +466,40 @@ __device__ void stage_row(const FfnParams &p, int row, int c0, int Kr, unsigned 
     }
 }
 
-// ------------------------------------------------------------------ fill chunks
+// ------------------------------------------------------------------ fills
 
-// A chunk of a unit whose expert missed: its bytes (one run of tile blocks per tile) are
-// read from the expert's pinned host image over the CPU-GPU link by the warp's lanes
-// (GV_FILL_BATCH 16-byte loads in flight per lane) and written both to the stage and, when
-// wt, through to the expert's slot.  Same byte ranges and stage layout as the bulk copies
-// of a resident chunk.
+// Issues one fill chunk into a ring stage (whole warp): the runs of n16 16-byte pieces of its
+// tiles (src0 for tile 0, src1 for tile NTL - 1; at most two tiles) as cp.async pieces tied to
+// the stage barrier, then lane 0's arrival.  Kept out of line: the resident path stays free of
+// its registers.
+__device__ __noinline__ void issue_fill(uint64_t *bar, unsigned char *dst, const uint8_t *src0,
+                                        const uint8_t *src1, int ntl, int tb, int n16, int lane) {
+    for (int i = 0; i < ntl; ++i) {
+        const uint8_t *src = (i ? src1 : src0) + 16 * lane;
+        unsigned char *d = dst + (size_t)i * tb + 16 * lane;
+        for (int j = lane; j < n16; j += 32, src += 512, d += 512) cp_async_16(d, src);
+    }
+    cp_async_mbar_arrive(bar);
+    __syncwarp();  // every lane's pieces are counted before lane 0's arrival
+    if (lane == 0) mbar_arrive_plain(bar);
+}
+
+// A chunk of a unit whose expert missed arrives in its ring stage from the expert's pinned
+// host image over the CPU-GPU link (cp.async pieces, issued S stages ahead like the bulk
+// copies of resident chunks).  The first virtual expert of the expert also writes the chunk's
+// bytes (one run of tile blocks per tile) from the stage to the same offsets of the expert's
+// slot, so the slot holds the image once every chunk has passed.
 template <int QT>
-__device__ void fill_chunk(const ActInfo &in, int H, int F, bool down, int NTL, int g, int kb0, int cb,
-                           unsigned char *st, int tb, int lane) {
+__device__ void write_through(const ActInfo &in, int H, int F, bool down, int NTL, int g, int kb0, int cb,
+                              const unsigned char *st, int tb, int lane) {
     const int K = down ? F : H;
-    const int n = cb * moe_tile_block_bytes(QT) / 16;
+    const int n16 = cb * moe_tile_block_bytes(QT) / 16;
     for (int i = 0; i < NTL; ++i) {
         const size_t off = moe_expert_matrix_offset(QT, H, F, down ? 2 : i) +
                            moe_tile_block_offset(QT, K, down ? g + i : g, kb0);
-        const uint8_t *src = (const uint8_t *)in.src + off;
-        uint8_t *dst = in.wt ? (uint8_t *)in.dst + off : nullptr;
-        unsigned char *tile = st + (size_t)i * tb;
-        for (int j0 = 0; j0 < n; j0 += 32 * GV_FILL_BATCH) {
-            uint4 v[GV_FILL_BATCH];
-#pragma unroll
-            for (int b = 0; b < GV_FILL_BATCH; ++b) {
-                const int j = j0 + b * 32 + lane;
-                if (j < n) v[b] = __ldcs((const uint4 *)(src + (size_t)j * 16));
-            }
-#pragma unroll
-            for (int b = 0; b < GV_FILL_BATCH; ++b) {
-                const int j = j0 + b * 32 + lane;
-                if (j < n) {
-                    *(uint4 *)(tile + (size_t)j * 16) = v[b];
-                    if (dst) __stcs((uint4 *)(dst + (size_t)j * 16), v[b]);
-                }
-            }
-        }
+        uint4 *dst = (uint4 *)((uint8_t *)in.dst + off);
+        const uint4 *tile = (const uint4 *)(st + (size_t)i * tb);
+        for (int j = lane; j < n16; j += 32) __stcs(dst + j, tile[j]);
     }
 }
 
@@ -591,17 +595,17 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
     // a phase covers the units of act_slots consecutive pairs (slot = pair - first pair)
     auto phase_end = [&](int a) { return min(u1, (a / upp + G.act_slots) * upp); };
 
-    // ---- producer state (lane 0): the next chunk to issue
+    // ---- producer state (the same in every lane): the next chunk to issue
     int pc_ph1 = u0, pc_u = u1, pc_ch = 0;  // phase end, unit (u1: none left), chunk
     int pc_cached_v = -1;
     unsigned long long pc_src = 0ull;
-    bool pc_skip = true;
+    int pc_kind = GV_SKIP;
     auto pc_info = [&]() {  // where the weights of the next chunk's virtual expert are read from
         const int v = pc_u / (upp * kspp);
         if (v != pc_cached_v) {
             const ActInfo &in = p.info[v];
             pc_src = in.src;
-            pc_skip = in.n_e == 0 || in.fill;
+            pc_kind = in.n_e == 0 ? GV_SKIP : in.fill ? GV_FILL : GV_BULK;
             pc_cached_v = v;
         }
     };
@@ -624,44 +628,63 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
         pc_u += GV_WARPS;
         if (pc_u >= pc_ph1) pc_first(pc_ph1);
     };
+    // Called by the whole warp.  A resident chunk: lane 0 issues one bulk copy per tile (TMA
+    // engine), counted in bytes on the stage barrier.  A fill chunk (the expert's pinned host
+    // image): every lane copies its 16-byte pieces with cp.async and ties them to the stage
+    // barrier, then lane 0 arrives, so the stage completes when the pieces have landed — fill
+    // chunks are in flight S stages ahead like resident ones.  A skipped expert's chunk: lane 0
+    // arrives without bytes.
     auto issue = [&](int stage) {
         uint64_t *bar = &bars[stage];
         int v, pair, ks, g;
         decode(pc_u, v, pair, ks, g);
         pc_info();
-        if (pc_skip) {
-            mbar_arrive_plain(bar);
+        if (pc_kind == GV_SKIP) {
+            if (lane == 0) mbar_arrive_plain(bar);
             return;
         }
         const int kb0 = ks * nbr + pc_ch * CB, cb = min(CB, nbr - pc_ch * CB);
-        mbar_arrive_expect_tx(bar, (uint32_t)(NTL * cb * TBB));
         unsigned char *dst = ring + (size_t)stage * G.chunk_bytes;
-        for (int i = 0; i < NTL; ++i) {
-            const uint8_t *mat = (const uint8_t *)pc_src + moe_expert_matrix_offset(QT, p.H, p.F, DOWN ? 2 : i);
-            bulk_g2s(dst + (size_t)i * tb, mat + moe_tile_block_offset(QT, K, DOWN ? g + i : g, kb0),
-                     (uint32_t)(cb * TBB), bar);
+        if (pc_kind == GV_BULK) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar, (uint32_t)(NTL * cb * TBB));
+                for (int i = 0; i < NTL; ++i) {
+                    const uint8_t *mat =
+                        (const uint8_t *)pc_src + moe_expert_matrix_offset(QT, p.H, p.F, DOWN ? 2 : i);
+                    bulk_g2s(dst + (size_t)i * tb, mat + moe_tile_block_offset(QT, K, DOWN ? g + i : g, kb0),
+                             (uint32_t)(cb * TBB), bar);
+                }
+            }
+            return;
         }
+        const uint8_t *img = (const uint8_t *)pc_src;
+        issue_fill(bar, dst, img + moe_expert_matrix_offset(QT, p.H, p.F, DOWN ? 2 : 0) +
+                                 moe_tile_block_offset(QT, K, g, kb0),
+                   img + moe_expert_matrix_offset(QT, p.H, p.F, DOWN ? 2 : NTL - 1) +
+                       moe_tile_block_offset(QT, K, DOWN ? g + NTL - 1 : g, kb0),
+                   NTL, tb, cb * TBB / 16, lane);
     };
 
-    int J_issued = 0;  // chunks issued by this warp (lane 0's count)
+    int J_issued = 0;    // chunks issued by this warp
     bool dead = false;   // a wait ran out: no more waits, copies or outputs
-    // lane 0: issue chunks until `limit` have been issued (chunk X goes to stage X % S, which
-    // chunk X - S has left)
+    // issue chunks until `limit` have been issued (chunk X goes to stage X % S, which chunk
+    // X - S has left); warp-uniform
     auto top_up = [&](int limit) {
-        if (lane != 0 || dead) return;
+        if (dead) return;
         while (J_issued < limit && pc_u < u1) {
             issue(J_issued % S);
             pc_next();
             ++J_issued;
         }
     };
-    if (lane == 0) {
-        pc_first(u0);
-        if (PRIME) {
-            top_up(S);
-        } else if (pc_u == u0 + warp && first_src) {  // the permute kernel resolved it: issue at once
-            pc_src = first_src;
-            pc_skip = false;
+    pc_first(u0);
+    if (PRIME) {
+        top_up(S);
+    } else {
+        const unsigned long long fs = __shfl_sync(0xffffffffu, first_src, 0);
+        if (pc_u == u0 + warp && fs) {  // the permute kernel resolved it: issue at once
+            pc_src = fs;
+            pc_kind = GV_BULK;
             pc_cached_v = pc_u / (upp * kspp);
             top_up(1);
         } else if (pc_u < u1) {
@@ -745,14 +768,14 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
                 }
                 if (!dead && n_e > 0) {
                     const int cb = min(CB, nbr - ch * CB);
-                    if (fill) {
-                        fill_chunk<QT>(hdr->in, p.H, p.F, DOWN, NTL, g, ks * nbr + ch * CB, cb, st, tb, lane);
-                        fence_proxy_async_smem();  // a later bulk copy overwrites this stage
-                        __syncwarp();
-                    }
+                    if (fill && hdr->in.wt)  // the first group of a missed expert fills its slot
+                        write_through<QT>(hdr->in, p.H, p.F, DOWN, NTL, g, ks * nbr + ch * CB, cb, st, tb, lane);
                     const float *a0 = hi_cols ? asb + (size_t)ch * CB * NTS + tr0 : nullptr;
                     const float *a1 = hi_cols ? asb + (size_t)ch * CB * NTS + tr1 : nullptr;
                     chunk_dot<QT, NTL>(st, tb, cb, brow + (size_t)64 * ch * CB, a0, a1, NTS, lane, acc);
+                    // the stage was written through the generic proxy (cp.async); a later bulk
+                    // copy (async proxy) overwrites it
+                    if (fill) fence_proxy_async_smem();
                 }
                 __syncwarp();  // every lane is done with the stage
                 top_up(J + 1 + S);

@@ -124,6 +124,10 @@ int moe_expert_ffn_core(const void *x, int xtype, int T, int H, int F, int qtype
 #define MOE_FFN_DOWN 4
 #define MOE_FFN_REDUCE 8   // h from the gate/up kernel's K-split partial sums (no-op without a split)
 #define MOE_FFN_ALL 15
+// The caller guarantees that x was complete before the launch preceding this call started (so
+// a gate/up launch without this call's permute kernel in front may still start early and read
+// x before its dependency wait).
+#define MOE_FFN_X_READY 16
 // Kernels one decode-path FFN call (T <= MOE_DECODE_MAX_T, all stages) launches.
 int moe_decode_ffn_launches(int T, int H, int F, int qtype, int E, int k);
 int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,

@@ -363,10 +363,11 @@ __device__ __forceinline__ void act_load8(const FfnParams &p, int row, int col, 
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     } else {
         const size_t off = (size_t)row * p.H + col;
+        // x is read through L2: the gate/up kernel stages it before its dependency wait
         if (XT == MOE_BF16) {
             const __nv_bfloat16 *xb = (const __nv_bfloat16 *)p.x + off;
             if (p.x_vec) {
-                const uint4 r = *(const uint4 *)xb;
+                const uint4 r = __ldcg((const uint4 *)xb);
                 const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -376,16 +377,17 @@ __device__ __forceinline__ void act_load8(const FfnParams &p, int row, int col, 
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = __bfloat162float(xb[e]);
+                for (int e = 0; e < 8; ++e)
+                    v[e] = __bfloat162float(__ushort_as_bfloat16(__ldcg((const unsigned short *)xb + e)));
             }
         } else {
             const float *xf = (const float *)p.x + off;
             if (p.x_vec) {
-                const float4 a = *(const float4 *)xf, b = *(const float4 *)(xf + 4);
+                const float4 a = __ldcg((const float4 *)xf), b = __ldcg((const float4 *)(xf + 4));
                 v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = xf[e];
+                for (int e = 0; e < 8; ++e) v[e] = __ldcg(xf + e);
             }
         }
     }
@@ -576,7 +578,6 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
     const int K = DOWN ? p.F : p.H;
     const int nbr = G.nbr, Kr = nbr * 32, CB = G.CB;
     const int upp = DOWN ? (p.H / 32) / NTL : p.F / 32;  // units per pair
-    const int kspp = DOWN ? 1 : p.KS;                     // pairs per virtual expert
     const int tb = CB * TBB;                              // tile stride in a stage
     const int nch = (nbr + CB - 1) / CB;                  // chunks per unit
     const int RS = gv_row_stride(Kr);
@@ -586,10 +587,15 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
     unsigned char *ring = smem + GV_BARS + (size_t)warp * S * G.chunk_bytes;
     unsigned char *act_region = smem + GV_BARS + G.ring_bytes;
 
+    // Pairs are ordered (K range, virtual expert) in the gate/up launch — CTA c works on K range
+    // c / (G / KS) only, so it stages x before its dependency wait — and by virtual expert in
+    // the down launch.
+    const int nv = DOWN ? 1 : __ldcg(p.ws_ints + 1);  // virtual experts of the call
+    auto pair_v = [&](int pair) { return DOWN ? pair : pair % nv; };
     auto decode = [&](int u, int &v, int &pair, int &ks, int &g) {
         pair = u / upp;
-        v = pair / kspp;
-        ks = pair - v * kspp;
+        ks = DOWN ? 0 : pair / nv;
+        v = DOWN ? pair : pair - ks * nv;
         g = (u - pair * upp) * (DOWN ? NTL : 1);
     };
     // a phase covers the units of act_slots consecutive pairs (slot = pair - first pair)
@@ -601,7 +607,7 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
     unsigned long long pc_src = 0ull;
     int pc_kind = GV_SKIP;
     auto pc_info = [&]() {  // where the weights of the next chunk's virtual expert are read from
-        const int v = pc_u / (upp * kspp);
+        const int v = pair_v(pc_u / upp);
         if (v != pc_cached_v) {
             const ActInfo &in = p.info[v];
             pc_src = in.src;
@@ -685,7 +691,7 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
         if (pc_u == u0 + warp && fs) {  // the permute kernel resolved it: issue at once
             pc_src = fs;
             pc_kind = GV_BULK;
-            pc_cached_v = pc_u / (upp * kspp);
+            pc_cached_v = pair_v(pc_u / upp);
             top_up(1);
         } else if (pc_u < u1) {
             pc_info();
@@ -710,12 +716,19 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
         auto first_issue = [&]() {
             if (a == u0) top_up(1);
         };
-        for (int it = warp; it < npr * NTS; it += GV_WARPS) {
+        if (!DOWN) {  // x is staged (slot 0's rows); each pair's slot holds its header
+            if (a == u0) top_up(S);
+            for (int i = warp; i < npr; i += GV_WARPS)
+                if (lane == 0)
+                    ((SlotHdr *)(act_region + (size_t)i * G.slot_bytes + GV_HDR_OFF(NTS, RS)))->in =
+                        p.info[pair_v(pr0 + i)];
+        }
+        for (int it = warp; DOWN && it < npr * NTS; it += GV_WARPS) {
             const int i = it / NTS, t = it - i * NTS;
-            const int pr = pr0 + i, v = pr / kspp, ks = pr - v * kspp;
+            const int v = pr0 + i;
             unsigned char *slot = act_region + (size_t)i * G.slot_bytes;
             SlotHdr *hdr = (SlotHdr *)(slot + GV_HDR_OFF(NTS, RS));
-            if (DOWN) {
+            {
                 const ActInfo in = p.info[v];
                 if (t == 0 && lane == 0) hdr->in = in;
                 if (t < in.n_e) {
@@ -725,9 +738,6 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
                     float *asum = (float *)(slot + GV_ASUM_OFF(NTS, RS));
                     for (int b = lane; b < nbr; b += 32) asum[b * NTS + t] = 0.f;
                 }
-            } else {
-                if (t == 0 && lane == 0) hdr->in = p.info[v];
-                stage_row<QT, XT, DOWN>(p, t, ks * Kr, Kr, slot, NTS, t, lane, first_issue);
             }
         }
         first_issue();
@@ -736,8 +746,9 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
         for (int u = a + warp; u < e; u += GV_WARPS) {
             int v, pair, ks, g;
             decode(u, v, pair, ks, g);
-            const unsigned char *slot = act_region + (size_t)(pair - pr0) * G.slot_bytes;
-            const SlotHdr *hdr = (const SlotHdr *)(slot + GV_HDR_OFF(NTS, RS));
+            const unsigned char *hslot = act_region + (size_t)(pair - pr0) * G.slot_bytes;
+            const SlotHdr *hdr = (const SlotHdr *)(hslot + GV_HDR_OFF(NTS, RS));
+            const unsigned char *slot = DOWN ? hslot : act_region;  // the staged activations
             const int n_e = hdr->in.n_e, fill = hdr->in.fill;
             // Token row of route slot q of this virtual expert in the staged slot (gate/up: the
             // route's token; down: q); slots past n_e read row 0 (their columns are not used).
@@ -815,6 +826,20 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
         for (int j = J_done; j < J_issued; ++j) mbar_wait_bounded(&bars[j % S], (j / S) & 1, p.status);
 }
 
+// Gate/up launch: CTA c works on K range c / (G / KS) only, so it stages x (every token row
+// over that range, into slot 0) before its dependency wait.  x is complete when the grid
+// starts: the launch is ordered behind the call's permute kernel, which lets the next grid
+// start only once everything before it has completed (or behind a full completion).
+template <int QT, int XT>
+__device__ __forceinline__ void stage_x_static(const FfnParams &p, unsigned char *smem) {
+    const GvGeom G = p.geo;
+    const int Kr = G.nbr * 32, ks = blockIdx.x / (gridDim.x / p.KS);
+    unsigned char *slot0 = smem + GV_BARS + G.ring_bytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (ks >= p.KS) return;
+    for (int t = warp; t < p.T; t += GV_WARPS) stage_row<QT, XT, false>(p, t, ks * Kr, Kr, slot0, p.T, t, lane, [] {});
+}
+
 template <int QT, int XT, bool DOWN, int NTL>
 __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -823,7 +848,8 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
         for (int s = 0; s < GV_MAX_STAGES; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
-    pdl_wait();  // ranges, routing and activations come from earlier kernels
+    if (!DOWN) stage_x_static<QT, XT>(p, smem);
+    pdl_wait();  // ranges, routing (and h) come from earlier kernels
     pdl_trigger();
     ffn_body<QT, XT, DOWN, NTL, false>(p, smem, [] {});
 }
@@ -886,6 +912,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_fused_kernel(FfnParams p1, 
         }
         fence_mbar_init();
     }
+    stage_x_static<QT, XT>(p1, smem);
     pdl_wait();
     pdl_trigger();
     ffn_body<QT, XT, false, 2, false>(p1, smem, [] {});
@@ -937,7 +964,11 @@ __device__ __forceinline__ unsigned long long block_scan_excl(unsigned long long
 // pool, or the pinned host image for a fill, written through by the first group only), and
 // the unit ranges of the CTAs of both GEMV launches.  Every unit weighs the same (its bytes,
 // dequantisation and MMAs do not depend on its routes: the MMA computes every column of a
-// virtual expert), so CTA c of G takes units [floor(c U / G), floor((c+1) U / G)).
+// virtual expert), so CTA c of G takes units [floor(c U / G), floor((c+1) U / G)) of the down
+// launch.  The gate/up launch orders its pairs (K range, virtual expert) and gives each K
+// range G1 / KS1 CTAs (G1 is a multiple of KS1): CTA c takes, within K range k = c / (G1/KS1),
+// units k U' + [floor(c' U' / Gk), floor((c'+1) U' / Gk)) with U' the units of one K range,
+// Gk = G1 / KS1 and c' = c - k Gk.
 //
 // One CTA of 256 threads, everything in shared memory, no serial loop: a route's rank among
 // the earlier routes of its expert comes from a warp match (rank within the warp) plus the
@@ -949,7 +980,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
                                                       const int32_t *__restrict__ slot_table, int n_slots,
                                                       const uint8_t *pool, size_t slot_bytes,
                                                       const unsigned long long *__restrict__ fill_src,
-                                                      int G1, int per_v1, int G2, int per_v2,
+                                                      int G1, int per_v1, int KS1, int G2, int per_v2,
                                                       unsigned long long *__restrict__ first, int *status) {
     static_assert(GV_PERMUTE_MAX_R <= 256 && MOE_MAX_E <= 256, "one route and one expert per thread");
     constexpr int NW = 8;  // warps
@@ -1070,30 +1101,35 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
     }
     // ---- unit ranges of both launches
     {
-        const int G[2] = {G1, G2}, per_v[2] = {per_v1, per_v2};
-#pragma unroll
-        for (int l = 0; l < 2; ++l) {
-            int *rg = ints + ws_ranges_off(E, R, l);
-            const unsigned long long U = (unsigned long long)n_virt * per_v[l];
-            for (int c = tid; c <= G[l]; c += 256) {
-                const int u = (int)(U * (unsigned long long)c / (unsigned long long)G[l]);
-                s_rng[l][c] = u;
-                rg[c] = u;
-            }
+        int *rg1 = ints + ws_ranges_off(E, R, 0), *rg2 = ints + ws_ranges_off(E, R, 1);
+        const int Gk = G1 / KS1;
+        const unsigned long long Uk = (unsigned long long)n_virt * (per_v1 / KS1);
+        for (int c = tid; c <= G1; c += 256) {
+            const int k = c / Gk, cl = c - k * Gk;
+            const int u = (int)(k * Uk + Uk * (unsigned long long)cl / (unsigned long long)Gk);
+            s_rng[0][c] = u;
+            rg1[c] = u;
+        }
+        const unsigned long long U2 = (unsigned long long)n_virt * per_v2;
+        for (int c = tid; c <= G2; c += 256) {
+            const int u = (int)(U2 * (unsigned long long)c / (unsigned long long)G2);
+            s_rng[1][c] = u;
+            rg2[c] = u;
         }
     }
     __syncthreads();
     // ---- where each warp's first unit (unit ranges[c] + warp) is read from, so that a GEMV warp
-    // can issue its first copy with the range load (0: no such unit, a skip or a fill).  The 16
-    // units of a CTA row start at v0 = ranges[c] / per_v and cross into the next virtual
-    // expert at most per_v apart.
+    // can issue its first copy with the range load (0: no such unit, a skip or a fill).  A
+    // unit's pair is u / upp (upp units per pair); its virtual expert is the pair (down) or the
+    // pair modulo n_virt (gate/up: pairs ordered (K range, virtual expert)).
 #pragma unroll
     for (int l = 0; l < 2; ++l) {
-        const int G = l ? G2 : G1, pv = l ? per_v2 : per_v1;
+        const int G = l ? G2 : G1, upp = l ? per_v2 : per_v1 / KS1;
         unsigned long long *fo = first + (size_t)l * GV_MAX_GRID * GV_WARPS;
         for (int c = tid; c < G; c += 256) {
             const int u0 = s_rng[l][c], u1 = s_rng[l][c + 1];
-            int v = u0 / pv, r = u0 - v * pv;
+            const int pair = u0 / upp;
+            int v = l ? pair : (n_virt ? pair % n_virt : 0), r = u0 - pair * upp;
             for (int w = 0; w < GV_WARPS; ++w) {
                 unsigned long long d = 0ull;
                 if (u0 + w < u1) {
@@ -1105,9 +1141,9 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
                     }
                 }
                 fo[(size_t)c * GV_WARPS + w] = d;
-                if (++r == pv) {
+                if (++r == upp) {
                     r = 0;
-                    ++v;
+                    if (++v == n_virt && !l) v = 0;
                 }
             }
         }
@@ -1261,13 +1297,13 @@ std::atomic<int> g_coop_pdl{-1};
 // A launch whose CTAs wait on one another: cooperative (the driver refuses a grid that cannot
 // be resident at once), with the programmatic dependency on the previous kernel when the
 // driver takes both attributes together.
-static int launch_cooperative(const void *fn, dim3 grid, size_t smem, cudaStream_t s, void **args) {
+static int launch_cooperative(const void *fn, dim3 grid, size_t smem, cudaStream_t s, void **args, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     moe_pdl_config(&cfg, attr, grid, dim3(GV_THREADS), smem, s);
     attr[1].id = cudaLaunchAttributeCooperative;
     attr[1].val.cooperative = 1;
-    const int mode = g_coop_pdl.load();
+    const int mode = pdl ? g_coop_pdl.load() : 0;
     if (mode != 0) {
         cfg.numAttrs = 2;
         const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
@@ -1395,8 +1431,11 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
     int capf = 0;
     if ((rc = ring_grid_capacity(kf, smemf, &capf)) != MOE_OK) return rc;
     const int cap = std::min(std::min(cap1, cap2), capf);
-    const int G1 = (int)std::max(1L, std::min((long)cap, n_virt_max * std::max(per_v1, per_v2)));
+    // the gate/up launch gives each of its KS K ranges the same number of CTAs
+    const int G0 = (int)std::max(1L, std::min((long)cap, n_virt_max * std::max(per_v1, per_v2)));
+    const int G1 = std::max(pl.KS, G0 / pl.KS * pl.KS);
     const int G2 = G1;
+    if (G1 > cap) return MOE_ERR_UNSUPPORTED;
 
     FfnParams p;
     p.x = x;
@@ -1423,12 +1462,17 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
                                         (int32_t *)((char *)workspace + W.ints_off),
                                         (ActInfo *)((char *)workspace + W.info_off), d_slot_table, n_slots,
                                         (const uint8_t *)pool, slot_bytes,
-                                        (const unsigned long long *)d_fill_src, G1, per_v1, G2, per_v2,
+                                        (const unsigned long long *)d_fill_src, G1, per_v1, pl.KS, G2, per_v2,
                                         (unsigned long long *)((char *)workspace + W.first_off), p.status));
     }
     if (timing && timing->permute1) MOE_TRY_CUDA(cudaEventRecord(timing->permute1, s));
     }
     void *args[] = {&p};
+    // The gate/up kernel reads x before its dependency wait.  Launched right behind this call's
+    // permute kernel (which lets the next grid start only after its own wait, so everything
+    // before it has completed) it may start early; otherwise only if the caller says x was
+    // complete already, else behind a fully completed predecessor.
+    const bool early_x = (stages & (MOE_FFN_PERMUTE | MOE_FFN_X_READY)) != 0;
     constexpr int kGemvStages = MOE_FFN_GATEUP | MOE_FFN_REDUCE | MOE_FFN_DOWN;
     if (g_fused.load() && (stages & kGemvStages) == kGemvStages) {
         if (timing && timing->gateup0) MOE_TRY_CUDA(cudaEventRecord(timing->gateup0, s));
@@ -1441,7 +1485,7 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
         p2.first = p1.first + (size_t)GV_MAX_GRID * GV_WARPS;
         int *sync = (int *)((char *)workspace + W.ints_off) + GV_SYNC_OFF;
         void *fargs[] = {&p1, &p2, &sync};
-        if ((rc = launch_cooperative(kf, dim3(G1), smemf, s, fargs)) != MOE_OK) return rc;
+        if ((rc = launch_cooperative(kf, dim3(G1), smemf, s, fargs, early_x)) != MOE_OK) return rc;
         if (timing && timing->gateup1) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
         if (timing && timing->down0) MOE_TRY_CUDA(cudaEventRecord(timing->down0, s));
         if (timing && timing->down1) MOE_TRY_CUDA(cudaEventRecord(timing->down1, s));
@@ -1455,6 +1499,7 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         moe_pdl_config(&cfg, attr, dim3(G1), dim3(GV_THREADS), smem1, s);
+        if (!early_x) cfg.numAttrs = 0;  // start only behind a completed predecessor
         MOE_TRY_CUDA(cudaLaunchKernelExC(&cfg, k1, args));
         if (timing && timing->gateup1 && !(stages & MOE_FFN_REDUCE)) MOE_TRY_CUDA(cudaEventRecord(timing->gateup1, s));
     }

@@ -562,7 +562,8 @@ extern "C" int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, in
         rc = moe_router_topk(x_in, MOE_F32, T, d.H, st->w_router[l], st->bias[l], d.E, d.k, ids, w, nullptr, sv);
         if (rc == MOE_OK) rc = stage(l, MOE_FFN_PERMUTE);
     }
-    for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_GATEUP | MOE_FFN_REDUCE);  // warm-up
+    // x_in is complete long before: the gate/up rounds may start early
+    for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_GATEUP | MOE_FFN_REDUCE | MOE_FFN_X_READY);
     for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_DOWN);
     for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_ALL);
     if (rc == MOE_OK) {  // about 40 us of host time per launch to queue, at least 2 ms
@@ -572,7 +573,7 @@ extern "C" int moe_stack_gemv_timing(moe_stack *st, const float *x_in, int T, in
     }
     if (rc == MOE_OK && cudaEventRecord(ev[0], s) != cudaSuccess) rc = MOE_ERR_CUDA;
     for (int r = 0; r < reps && rc == MOE_OK; ++r)
-        for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_GATEUP);
+        for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_GATEUP | MOE_FFN_X_READY);
     if (rc == MOE_OK && cudaEventRecord(ev[1], s) != cudaSuccess) rc = MOE_ERR_CUDA;
     for (int r = 0; r < reps && rc == MOE_OK; ++r)
         for (int l = 0; l < L && rc == MOE_OK; ++l) rc = stage(l, MOE_FFN_REDUCE);

@@ -10,10 +10,12 @@
 //  * the routes of an expert are cut into groups of at most 4 ("virtual experts");
 //    a work unit is NTL 32-row tiles of one virtual expert over a K range: the gate and the
 //    up tile of the same rows (G1), or one or two neighbouring down tiles (G2);
-//  * persistent CTAs of 16 warps, one per SM, each over a contiguous, work-balanced range of
-//    units (precomputed by the permute kernel).  The warps of a CTA take its units in turn
-//    and are independent: each has its own ring of shared-memory stages, fed by its lane 0
-//    with bulk copies (TMA engine, cp.async.bulk) a few chunks ahead, and waits on its own
+//  * persistent CTAs of 16 warps, one per SM, each over a contiguous range of units of equal
+//    count (precomputed by the permute kernel; in the gate/up launch each CTA keeps to one K
+//    range, so it stages x before its dependency wait).  The warps of a CTA take its units in
+//    turn and are independent: each has its own ring of shared-memory stages, filled a few
+//    chunks ahead by bulk copies (TMA engine, cp.async.bulk, issued by lane 0) or, for a
+//    missed expert, by cp.async pieces from its pinned host image, and waits on its own
 //    mbarriers.  There is no block-wide barrier while weights stream;
 //  * a warp owns whole rows of its unit and needs no reduction with other warps: the codes
 //    of a 32-column block are turned into fp16 (exact small integers) in registers, laid
@@ -21,13 +23,14 @@
 //    tokens, fp32 accumulation), and the block's fp32 scale is applied to the block's
 //    partial sums in fp32, so the per-block arithmetic is exact except for the activations;
 //  * activations enter the tensor core as fp16 hi + lo parts of a per-token power-of-two
-//    scaled copy (about 22 significant bits), staged once per (virtual expert, K range) in
-//    shared memory for all warps of the CTA;
+//    scaled copy (about 22 significant bits), staged in shared memory for all warps of the
+//    CTA: once per CTA (x over its K range, G1) or per virtual expert (h rows, G2);
 //  * the warp's epilogue forms h = silu(gate) * up (G1, whole K) or stores the two partial
 //    sums (G1, K split; a small kernel between the GEMVs sums them in K order and forms h),
 //    or writes w[r] * (Wd h) for each route r (G2);
-//  * an expert that missed in a device-managed pool is read from its pinned host image and
-//    written through to its slot by the warps that use the bytes ("fill" units).
+//  * an expert that missed in a device-managed pool is read from its pinned host image over
+//    the CPU-GPU link into the ring and written through from there to its slot by the warps
+//    that use the bytes ("fill" chunks).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>

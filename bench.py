@@ -137,16 +137,32 @@ def _oracle_layer_time(cfg, layer, T, seed):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(cfg, T, budget_s=12.0):
+def cpu_baseline(cfg, T, budget_s=12.0, budget_1t_s=4.0):
+    """The fp64 C oracle on the host cores: a bounded sample of the layers of one batch-T
+    decode step with every thread (OpenMP over the expert rows), scaled to the step; then a
+    smaller sample with one thread."""
     import oracle
+    from oracle import build as obuild
     times, t_start, i = [], time.perf_counter(), 0
     while time.perf_counter() - t_start < budget_s and i < cfg.L:
         times.append(_oracle_layer_time(cfg, i, T, 5000 + i))
         i += 1
     step_s = float(np.mean(times)) * cfg.L
-    return {"value": T / step_s, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+    cores = oracle.num_threads()
+    t1, t_start = [], time.perf_counter()
+    oracle.set_num_threads(1)
+    try:
+        while (time.perf_counter() - t_start < budget_1t_s or not t1) and len(t1) < cfg.L:
+            t1.append(_oracle_layer_time(cfg, len(t1), T, 7000 + len(t1)))
+    finally:
+        oracle.set_num_threads(cores)
+    step1_s = float(np.mean(t1)) * cfg.L
+    return {"value": T / step_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{len(times)} layers of one batch-{T} decode step (fp64 C oracle, OpenMP over "
-                      f"rows), scaled by {cfg.L} layers"}
+                      f"rows), scaled by {cfg.L} layers",
+            "s_per_token": step_s / T, "one_thread": {"value": T / step1_s, "s_per_token": step1_s / T,
+                                                     "sample": f"{len(t1)} layers, scaled by {cfg.L}"},
+            "affinity_cpus": len(os.sched_getaffinity(0)), "compiler": "gcc " + " ".join(obuild.CFLAGS)}
 
 
 def run_reference(args, world, rank):

@@ -164,3 +164,10 @@ def test_overlap_and_serial_paths_agree():
     assert a.cache_stats() == b.cache_stats()
     a.close()
     b.close()
+
+
+def test_smoke_entry_point():
+    """The build entry point's smoke check (one stack layer of the tiny shape against the
+    oracle) passes through the same library the tests use."""
+    import __graft_entry__
+    __graft_entry__.smoke()

@@ -273,9 +273,12 @@ def gemv_roofline_block(gv, cfg, T, peaks):
 
 
 def max_over_ranks(v, world, torch):
+    """The largest of the ranks' values (the job's time is its slowest rank's): an all-reduce
+    on the process group, on the GPU under NCCL and on the host under gloo."""
     if world <= 1:
         return v
-    t = torch.tensor([v], device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 

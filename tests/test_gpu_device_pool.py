@@ -135,6 +135,44 @@ def test_fill_ffn_matches_oracle_and_fills_slots(qtype):
     L.moe_cache_destroy(fx.cache)
 
 
+@pytest.mark.parametrize("qtype,H,T,k,E", [
+    (0, 256, 8, 4, 6),    # about 5 routes per expert: two virtual experts per missed expert
+    (1, 512, 16, 6, 8),   # 4-bit, 12 routes per expert on average: three or four groups
+    (0, 1024, 1, 2, 12),  # one token: the gate/up K split reaches its maximum
+])
+def test_fill_ffn_with_several_groups_per_missed_expert(qtype, H, T, k, E):
+    """A missed expert routed by more than 4 routes is split into several virtual experts: all
+    read the pinned host image, the first writes it through to the slot."""
+    cfg = synth.small_config(qtype, H=H, F=96, E=E, k=k, seed_cfg=890 + qtype + H)
+    fx = DevicePool(cfg, 1, E)
+    rng = np.random.default_rng(H + T)
+    host = fx.host.numpy()
+    ids = np.stack([rng.choice(cfg.E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    w = rng.uniform(0.1, 1.0, size=(T, k)).astype(np.float32)
+    x = rng.standard_normal((T, cfg.H), dtype=np.float32)
+    ids_d = fx.plan(0, ids)
+    ws_bytes = L.moe_expert_ffn_workspace(T, cfg.H, cfg.F, qtype, 0, cfg.E, k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev())
+    partial = torch.full((T, k, cfg.H), float("nan"), dtype=torch.float32, device=dev())
+    L.moe_expert_ffn_fill(torch.from_numpy(x).to(dev()), 0, T, cfg.H, cfg.F, qtype, cfg.E, k, ids_d,
+                          torch.from_numpy(w).to(dev()), fx.table, E, fx.pool, fx.stride, fx.fill,
+                          partial, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert L.moe_device_status(clear=True) == 0
+    got = partial.cpu().numpy()
+    for t in range(T):
+        for j in range(k):
+            g, u, d = synth.expert_weights(cfg, 0, int(ids[t, j]))
+            ref = float(w[t, j]) * oracle.expert_ffn(qtype, cfg.H, cfg.F, g, u, d, x[t].astype(np.float64))
+            assert rel_err(got[t, j][None], ref[None])[0] <= TOL
+    pool, table = fx.pool.cpu().numpy(), fx.table.cpu().numpy()
+    for e in set(ids.reshape(-1).tolist()):
+        s = table[e]
+        assert np.array_equal(pool[s * fx.stride: s * fx.stride + fx.img_bytes],
+                              host[e * fx.stride: e * fx.stride + fx.img_bytes]), e
+    L.moe_cache_destroy(fx.cache)
+
+
 def _stack(*a, **kw):
     from routed_expert_ffn_gemv_gb300.workload import Stack
     return Stack(*a, **kw)

@@ -105,11 +105,14 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
                                                    int k, uint64_t image_bytes, int32_t *__restrict__ table_out,
                                                    uint64_t *__restrict__ src_out, int *status) {
     // Everything is read once into shared memory (one round of loads), the list is updated
-    // there by one thread, and the results are stored once.
+    // there in parallel (one short walk from the head by one thread) and stored once.
     extern __shared__ int32_t sm[];
     int32_t *owner = sm, *prev = sm + n_slots, *next = sm + 2 * n_slots, *slot_l = sm + 3 * n_slots;
     unsigned char *want = (unsigned char *)(slot_l + E), *miss = want + E;
-    __shared__ int abort_flag, route_hits, commit;
+    __shared__ int abort_flag, route_hits, commit, s_head, s_tail;
+    __shared__ int wsum[8];
+    __shared__ int32_t vict[MOE_MAX_E], app[MOE_MAX_E];
+    unsigned char *in_s = miss + E;  // hit slots (n_slots bytes)
     __shared__ int32_t s_ids[MOE_DECODE_MAX_T * MOE_MAX_K];
     __shared__ DevHeader s_hd;
     __shared__ uint64_t s_img[MOE_MAX_E];
@@ -120,6 +123,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     int32_t *g_next = (int32_t *)(state + L.next);
     const uint64_t *g_img = (const uint64_t *)(state + L.img);
     const int key0 = ll * E, n_ids = n_tokens * k;
+    const int n_keys = (int)((L.owner - L.slot_of) / 4);  // entries the slot_of region holds
     pdl_wait();  // ids and the pool state come from earlier kernels
     pdl_trigger();
     for (int i = threadIdx.x; i < n_slots; i += blockDim.x) {
@@ -153,71 +157,154 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0 && !abort_flag) {
-        int nd = 0;
-        for (int e = 0; e < E; ++e) nd += want[e];
-        if (nd > n_slots) {
+    // ---- the request: distinct experts, hits (resident) and misses, ranked by ascending id
+    const int e_t = threadIdx.x;  // one expert per thread (E <= MOE_MAX_E = blockDim.x)
+    const bool w_t = e_t < E && want[e_t];
+    const bool hit_t = w_t && slot_l[e_t] >= 0, miss_t = w_t && slot_l[e_t] < 0;
+    const int nd = __syncthreads_count(w_t);
+    int rh = 0, rm = 0, nh = 0, nm = 0;  // this expert's rank among the hits / misses; counts
+    {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        int x = (int)hit_t | ((int)miss_t << 16);
+        const int v = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        int before = 0, all = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+            before += w < warp ? wsum[w] : 0;
+            all += wsum[w];
+        }
+        const int ex = before + x - v;
+        rh = ex & 0xFFFF;
+        rm = ex >> 16;
+        nh = all & 0xFFFF;
+        nm = all >> 16;
+    }
+    if (threadIdx.x == 0 && !abort_flag && nd > n_slots) {
+        moe_set_status(status, MOE_ERR_CAPACITY);
+        abort_flag = 1;
+    }
+    if (threadIdx.x == 0) {
+        s_head = s_hd.head;
+        s_tail = s_hd.tail;
+        if (s_head < -1 || s_head >= n_slots || s_tail < -1 || s_tail >= n_slots || s_hd.n_filled < 0 ||
+            s_hd.n_filled > n_slots) {  // a corrupt header: record it, change nothing
             moe_set_status(status, MOE_ERR_CAPACITY);
             abort_flag = 1;
-        } else {
-            commit = 1;  // the list is updated (up to a capacity error) and its header stored
-            int head = s_hd.head, tail = s_hd.tail, filled = s_hd.n_filled;
-            auto unlink = [&](int s) {
-                const int p = prev[s], n = next[s];
-                if (p >= 0) next[p] = n; else head = n;
-                if (n >= 0) prev[n] = p; else tail = p;
-            };
-            auto append = [&](int s) {
-                prev[s] = tail;
-                next[s] = -1;
-                if (tail >= 0) next[tail] = s; else head = s;
-                tail = s;
-            };
-            int n_hit = 0, n_miss = 0, n_evict = 0;
-            for (int e = 0; e < E; ++e) {           // hits, ascending id: most recent
-                if (!want[e] || slot_l[e] < 0) continue;
-                unlink(slot_l[e]);
-                append(slot_l[e]);
-                ++n_hit;
-            }
-            for (int e = 0; e < E; ++e) {           // misses, ascending id
-                if (!want[e] || slot_l[e] >= 0) continue;
-                int s;
-                if (filled < n_slots) {
-                    s = filled++;
+        }
+    }
+    for (int i = threadIdx.x; i < n_slots; i += blockDim.x) in_s[i] = 0;
+    __syncthreads();
+    if (!abort_flag) {
+        // Same result as taking the hits one by one to the tail (ascending id), then for each
+        // miss (ascending id) the lowest free slot, else the first list entry not owned by the
+        // request, appended to the tail — done in parallel:
+        // (1) unlink every hit slot: the first slot of each run of hit slots in the list joins
+        //     the run's neighbours (runs touch disjoint links);
+        // (a slot or link outside the pool means the state is corrupt: record it, change nothing)
+        auto corrupt = [&]() {
+            moe_set_status(status, MOE_ERR_CAPACITY);
+            abort_flag = 1;
+        };
+        if (hit_t) {
+            if (slot_l[e_t] < n_slots) in_s[slot_l[e_t]] = 1;
+            else corrupt();
+        }
+        __syncthreads();
+        if (hit_t && !abort_flag) {
+            const int s = slot_l[e_t], pr = prev[s];
+            if (pr >= n_slots) {
+                corrupt();
+            } else if (pr < 0 || !in_s[pr]) {
+                int q = next[s], steps = 0;
+                while (q >= 0 && q < n_slots && in_s[q] && steps++ <= n_slots) q = next[q];
+                if (q >= n_slots || steps > n_slots) {
+                    corrupt();
                 } else {
-                    s = head;
-                    int steps = 0;  // the list holds at most n_slots entries: a longer walk is corruption
-                    while (s >= 0 && s < n_slots && steps++ <= n_slots) {
-                        const int o = owner[s];
-                        if (!(o >= key0 && o < key0 + E && want[o - key0])) break;
-                        s = next[s];
-                    }
-                    if (steps > n_slots + 1 || s >= n_slots) s = -1;
-                    if (s < 0) { moe_set_status(status, MOE_ERR_CAPACITY); abort_flag = 1; break; }
-                    unlink(s);
-                    const int o = owner[s];
-                    if (o >= key0 && o < key0 + E) slot_l[o - key0] = -1;
-                    else if (o >= 0) g_slot_of[o] = -1;
-                    ++n_evict;
+                    if (pr >= 0) next[pr] = q;
+                    else s_head = q;
+                    if (q >= 0) prev[q] = pr;
+                    else s_tail = pr;
                 }
-                append(s);
-                owner[s] = key0 + e;
-                slot_l[e] = s;
-                miss[e] = 1;
-                ++n_miss;
             }
-            s_hd.head = head;
-            s_hd.tail = tail;
-            s_hd.n_filled = filled;
-            const int b = n_tokens <= 8 ? 0 : 1;
-            s_hd.queries[b] += n_hit + n_miss;
-            s_hd.hits[b] += n_hit;
-            s_hd.misses[b] += n_miss;
-            s_hd.evictions += n_evict;
-            s_hd.h2d_bytes += (uint64_t)n_miss * image_bytes;
-            s_hd.route_queries += n_ids;
-            s_hd.ensure_calls += 1;
+        }
+        __syncthreads();
+        // (2) the victims: the first entries of what remains, from the head (one thread; the
+        //     capacity check leaves enough entries not owned by the request);
+        const int filled = s_hd.n_filled, n_free = n_slots - filled;
+        const int m_evict = max(0, nm - n_free);
+        if (threadIdx.x == 0 && m_evict > 0 && !abort_flag) {
+            int sv = s_head;
+            for (int i = 0; i < m_evict; ++i) {
+                if (sv < 0 || sv >= n_slots || in_s[sv]) {
+                    corrupt();
+                    break;
+                }
+                vict[i] = sv;
+                sv = next[sv];
+            }
+            if (sv >= n_slots) corrupt();
+            if (!abort_flag) {
+                s_head = sv;
+                if (sv >= 0) prev[sv] = -1;
+                else s_tail = -1;
+            }
+        }
+        __syncthreads();
+        if (!abort_flag) {
+            // (3) each miss's slot (a free one, else its victim; the victim's owner loses it),
+            //     and the order of the appended slots: hits then misses, ascending id;
+            int ms = -1;
+            if (miss_t) {
+                if (rm < n_free) {
+                    ms = filled + rm;
+                } else {
+                    ms = vict[rm - n_free];
+                    const int o = owner[ms];
+                    if (o >= key0 && o < key0 + E) slot_l[o - key0] = -1;  // not requested: no other writer
+                    else if (o >= 0 && o < n_keys) g_slot_of[o] = -1;
+                }
+                app[nh + rm] = ms;
+            }
+            if (hit_t) app[rh] = slot_l[e_t];
+            const int old_tail = s_tail;
+            __syncthreads();
+            // (4) append them at the tail
+            const int na = nh + nm;
+            for (int i = threadIdx.x; i < na; i += blockDim.x) {
+                const int sa = app[i];
+                prev[sa] = i == 0 ? old_tail : app[i - 1];
+                next[sa] = i + 1 < na ? app[i + 1] : -1;
+            }
+            if (miss_t) {
+                owner[ms] = key0 + e_t;
+                slot_l[e_t] = ms;
+                miss[e_t] = 1;
+            }
+            if (threadIdx.x == 0) {
+                if (na > 0) {
+                    if (old_tail >= 0) next[old_tail] = app[0];
+                    else s_head = app[0];
+                    s_tail = app[na - 1];
+                }
+                commit = 1;
+                s_hd.head = s_head;
+                s_hd.tail = s_tail;
+                s_hd.n_filled = min(n_slots, filled + nm);
+                const int b = n_tokens <= 8 ? 0 : 1;
+                s_hd.queries[b] += nh + nm;
+                s_hd.hits[b] += nh;
+                s_hd.misses[b] += nm;
+                s_hd.evictions += m_evict;
+                s_hd.h2d_bytes += (uint64_t)nm * image_bytes;
+                s_hd.route_queries += n_ids;
+                s_hd.ensure_calls += 1;
+            }
         }
     }
     __syncthreads();
@@ -230,16 +317,16 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
         __syncthreads();
         for (int i = threadIdx.x; i < (int)(sizeof(DevHeader) / 4); i += blockDim.x)
             ((int32_t *)hd)[i] = ((const int32_t *)&s_hd)[i];
-    }
-    for (int i = threadIdx.x; i < n_slots; i += blockDim.x) {
-        g_owner[i] = owner[i];
-        g_prev[i] = prev[i];
-        g_next[i] = next[i];
+        for (int i = threadIdx.x; i < n_slots; i += blockDim.x) {
+            g_owner[i] = owner[i];
+            g_prev[i] = prev[i];
+            g_next[i] = next[i];
+        }
     }
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        g_slot_of[key0 + e] = slot_l[e];
-        table_out[e] = abort_flag ? -1 : slot_l[e];
-        src_out[e] = (!abort_flag && miss[e]) ? s_img[e] : 0ull;
+        if (commit) g_slot_of[key0 + e] = slot_l[e];
+        table_out[e] = commit ? slot_l[e] : -1;
+        src_out[e] = (commit && miss[e]) ? s_img[e] : 0ull;
     }
 }
 
@@ -279,7 +366,8 @@ extern "C" int moe_cache_plan(moe_cache *c, int layer, const int32_t *d_ids, int
     const int ll = layer - d.first_layer;
     MOE_CHECK(ll >= 0 && ll < d.n_layers);
     const DevLayout L = dev_layout(d.n_layers, d.n_experts, d.n_slots);
-    const size_t smem = (size_t)3 * d.n_slots * 4 + (size_t)d.n_experts * 4 + 2 * (size_t)d.n_experts;
+    const size_t smem = (size_t)3 * d.n_slots * 4 + (size_t)d.n_experts * 4 + 2 * (size_t)d.n_experts +
+                        (size_t)d.n_slots;
     static bool attr_set = false;
     if (!attr_set) {
         MOE_TRY_CUDA(cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

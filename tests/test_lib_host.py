@@ -130,3 +130,44 @@ def test_workspace_sizes(lib):
         L.moe_expert_ffn_workspace(512, 2048, 768, 1, 0, 128, 8)
     assert n8 > n1 > 0 and n8 % 256 == 0
     assert L.moe_stack_workspace(1024, 512, 0, 32, 8, 8, 0) > n8 // 100
+
+
+def test_ctypes_structs_match_the_c_header(tmp_path):
+    """Every struct the binding mirrors has the C header's size and field offsets (compiled
+    with the host C compiler from include/moe.h)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    pairs = [(L.CacheDesc, "moe_cache_desc"), (L.CacheStats, "moe_cache_stats"),
+             (L.StackDesc, "moe_stack_desc"), (L.StackProfile, "moe_stack_profile"),
+             (L.GemvTiming, "moe_gemv_timing")]
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "moe.h"', "int main(void) {"]
+    for cls, cname in pairs:
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f in cls._fields_:
+            lines.append(f'printf("{cname} {f[0]} %zu\\n", offsetof({cname}, {f[0]}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    c = {" ".join(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for cls, cname in pairs:
+        assert c[f"{cname} size"] == ctypes.sizeof(cls), cname
+        for f in cls._fields_:
+            assert c[f"{cname} {f[0]}"] == getattr(cls, f[0]).offset, (cname, f[0])
+
+
+def test_decode_gemv_mode_switch(lib):
+    """The process-wide choice between the fused GEMV launch and the separate kernels."""
+    before = L.moe_get_decode_fused()
+    try:
+        L.moe_set_decode_fused(True)
+        assert L.moe_get_decode_fused() is True
+        L.moe_set_decode_fused(False)
+        assert L.moe_get_decode_fused() is False
+    finally:
+        L.moe_set_decode_fused(before)

@@ -366,12 +366,14 @@ extern "C" int moe_cache_plan(moe_cache *c, int layer, const int32_t *d_ids, int
     const int ll = layer - d.first_layer;
     MOE_CHECK(ll >= 0 && ll < d.n_layers);
     const DevLayout L = dev_layout(d.n_layers, d.n_experts, d.n_slots);
-    const size_t smem = (size_t)3 * d.n_slots * 4 + (size_t)d.n_experts * 4 + 2 * (size_t)d.n_experts +
-                        (size_t)d.n_slots;
+    // owner, prev, next (int32 per slot), the layer's slots (int32 per expert), want and miss
+    // (a byte per expert), the hit marks (a byte per slot)
+    auto plan_smem = [](int n_slots, int E) { return (size_t)n_slots * 13 + (size_t)E * 6; };
+    const size_t smem = plan_smem(d.n_slots, d.n_experts);
     static bool attr_set = false;
     if (!attr_set) {
         MOE_TRY_CUDA(cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          3 * MOE_PLAN_MAX_SLOTS * 4 + MOE_MAX_E * 6));
+                                          (int)plan_smem(MOE_PLAN_MAX_SLOTS, MOE_MAX_E)));
         attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};

@@ -66,7 +66,9 @@ class ClockSampler:
 
     def __init__(self, index: int):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # the raw samples (the JSON line carries their summary); BENCH_LOG_DIR moves them
+        log_dir = os.environ.get("BENCH_LOG_DIR", os.path.join(ROOT, "bench_logs"))
+        self.path = os.path.join(log_dir, f"clocks_bench_{os.getpid()}.csv")
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")

@@ -114,9 +114,14 @@ int moe_slot_image_bytes(int qtype, int H, int F, size_t *bytes_out);
  * moe_pack_expert — host: canonical expert tensors -> one slot image.
  * gate_aos, up_aos: host [F rows][H/32 blocks] canonical blocks; down_aos: [H][F/32].
  * slot_image_dst: host buffer of moe_slot_image_bytes() bytes (16-byte aligned);
- * pass NULL to query the size only.  The image regroups each matrix into tiles of
- * 32 rows so that one warp's 16-byte loads are contiguous, and keeps the block
- * scales in a separate region; no value is changed (the bytes are a permutation).
+ * pass NULL to query the size only.  Layout of the image: gate [F][H], up [F][H], down
+ * [H][F], each matrix a run of 32-row tiles, each tile a run of "tile blocks" (one per
+ * 32-column block along K): first the codes of the 32 rows (q8_0: two 512-byte pieces,
+ * row l's 16 codes of piece p at 512 p + 16 l, each stored as q + 128, offset binary;
+ * 4-bit: one 512-byte piece, row l's 16 canonical code bytes at 16 l), then the 32 rows'
+ * scale entries (fp16 d, or fp16 d and m), row l's entry at position 4 (l % 8) + l / 8.
+ * So any K range of a tile is one contiguous run of bytes.  The image has the canonical
+ * size and holds the same values; moe_unpack_expert inverts it exactly.
  */
 int moe_pack_expert(int qtype, int H, int F, const void *gate_aos, const void *up_aos,
                     const void *down_aos, void *slot_image_dst, size_t *slot_bytes_out);
@@ -296,7 +301,10 @@ int moe_expert_ffn_workspace(int T, int H, int F, int qtype, int xtype, int E, i
  * exits.  A request whose moe_expert_ffn_workspace() size exceeds it is rejected with
  * MOE_ERR_UNSUPPORTED before anything is enqueued.
  * Set-up: the first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream capture.
+ * device current) and caches it.  With lazy module loading (the CUDA default) that first
+ * call may also load the library's device code and back the array, a one-time cost; so
+ * make it during set-up, before any stream capture or latency-critical loop.  A call with
+ * T = 0 and valid sizes does only this set-up (x, ids, weights, pool, partial may be NULL).
  * Sharing: every call on a device uses the same array, which keeps the last call's
  * contents (nothing in it needs to start at zero).  Calls whose kernels can overlap on
  * the GPU — different streams, or different host threads — race on the array;
@@ -344,9 +352,14 @@ int moe_device_status(int *status_out, int clear);
 /* ------------------------------------------------------- decode-step runtime */
 
 /*
- * A stack of MoE layers with the residual h_{l+1} = h_l + MoE_l(h_l), driven
- * layer by layer on the host: router -> ids to host -> slot-pool ensure ->
- * FFN over hit experts while misses upload -> FFN over missed experts -> combine.
+ * A stack of MoE layers with a pre-norm residual, h_{l+1} = h_l + MoE_l(RMSNorm(h_l))
+ * (RMSNorm with unit weight, eps 1e-6; see moe_combine_rmsnorm).  Per layer, by pool kind:
+ *  - host-managed pools: router -> ids to the host (one host synchronisation) -> slot-pool
+ *    ensure -> FFN over hit experts while misses upload -> FFN over missed experts ->
+ *    combine;
+ *  - device-managed pools: router -> moe_cache_plan -> moe_expert_ffn_fill -> combine, all
+ *    stream-ordered on the GPU with no host round trip;
+ *  - every expert resident (n_groups == 0): router -> FFN -> combine, also host-free.
  */
 typedef struct {
     int qtype, H, F, E, k, n_layers, n_shared;
@@ -366,9 +379,10 @@ typedef struct {
     int device_managed;               /* 1: the caches are device-managed; each layer runs
                                          router -> moe_cache_plan -> moe_expert_ffn_fill ->
                                          combine on the stream, with no host round trip */
-    int use_graph;                    /* device_managed only: moe_stack_decode captures the
-                                         whole step once per batch size into a CUDA graph and
-                                         replays it (inputs/outputs copied in and out) */
+    int use_graph;                    /* device-managed or resident stacks: moe_stack_decode
+                                         captures the whole step once per batch size into a
+                                         CUDA graph and replays it (inputs/outputs copied in
+                                         and out) */
 } moe_stack_desc;
 
 typedef struct moe_stack moe_stack;
@@ -388,9 +402,12 @@ int moe_stack_workspace(int H, int F, int qtype, int E, int k, int max_T, int n_
 int moe_stack_create(const moe_stack_desc *desc, moe_stack **out);
 /*
  * moe_stack_decode — one decode step of T tokens through every layer.
- * x_in, y_out: device [T][H] fp32 (may alias).  Host-synchronising once per layer
- * (the routed ids are needed on the host by the slot pools); all kernels run on s.
- * ids_host_out / weights_host_out (optional, host [n_layers][T][k]) receive the routing.
+ * x_in, y_out: device [T][H] fp32 (may alias).  With host-managed pools the call
+ * synchronises the host once per layer (the slot pools need the routed ids on the host);
+ * with device-managed pools or a resident stack it only enqueues work on s (and with
+ * use_graph replays a captured step).  All kernels run on s.
+ * ids_host_out / weights_host_out (optional, host [n_layers][T][k]) receive the routing
+ * (valid once s has completed; such a call is never graph-replayed).
  */
 int moe_stack_decode(moe_stack *st, const float *x_in, float *y_out, int T,
                      int32_t *ids_host_out, float *weights_host_out, moe_stream_t s);

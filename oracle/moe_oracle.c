@@ -19,7 +19,7 @@
  *    q8_0 w = d*q, 4-bit scale+min w = d*q + m (page 5, section 1.2: quantised
  *    blocks used as-is by the GPU GEMV; block layouts as stated in synth.py).
  *  - Output: y = sum_j w_j * y_{e_j} (+ shared experts with weight 1), summed in
- *    the caller (oracle/oracle.py) in fp64.
+ *    the caller (the layer composition in oracle/__init__.py) in fp64.
  *
  * Everything is double precision.  fp16 / bf16 inputs are decoded exactly from
  * their bit patterns.  OpenMP (if enabled) only splits independent output rows;

@@ -11,6 +11,7 @@
 // cudaMemcpyAsync on the group's copy stream, issued after the event that marks the
 // slot's last reader (recorded by moe_cache_release on the compute stream).
 #include <algorithm>
+#include <mutex>
 #include <set>
 #include <utility>
 #include <vector>
@@ -370,11 +371,19 @@ extern "C" int moe_cache_plan(moe_cache *c, int layer, const int32_t *d_ids, int
     // (a byte per expert), the hit marks (a byte per slot)
     auto plan_smem = [](int n_slots, int E) { return (size_t)n_slots * 13 + (size_t)E * 6; };
     const size_t smem = plan_smem(d.n_slots, d.n_experts);
-    static bool attr_set = false;
-    if (!attr_set) {
-        MOE_TRY_CUDA(cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)plan_smem(MOE_PLAN_MAX_SLOTS, MOE_MAX_E)));
-        attr_set = true;
+    {
+        // the attribute belongs to the kernel on one device: set once per device
+        static std::mutex mu;
+        static bool attr_set[64] = {false};
+        int dev = -1;
+        MOE_TRY_CUDA(cudaGetDevice(&dev));
+        if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[dev]) {
+            MOE_TRY_CUDA(cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)plan_smem(MOE_PLAN_MAX_SLOTS, MOE_MAX_E)));
+            attr_set[dev] = true;
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];

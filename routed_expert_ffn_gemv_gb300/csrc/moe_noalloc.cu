@@ -31,7 +31,13 @@ int noalloc_scratch(void **out) {
     std::lock_guard<std::mutex> lock(mu);
     if (!addr[dev]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_moe_ffn_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_moe_ffn_scratch);
+        if (e != cudaSuccess) {
+            moe_note_cuda_error(e);   // reported by moe_last_cuda_error
+            (void)cudaGetLastError(); // not left behind for the next caller
+            return MOE_ERR_CUDA;
+        }
+        if (!p) return MOE_ERR_CUDA;
         addr[dev] = p;
     }
     *out = addr[dev];

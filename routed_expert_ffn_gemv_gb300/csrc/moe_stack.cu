@@ -1,10 +1,15 @@
-// Decode-step runtime: a stack of MoE layers with a residual, h_{l+1} = h_l + MoE_l(h_l).
+// Decode-step runtime: a stack of MoE layers with a pre-norm residual,
+// h_{l+1} = h_l + MoE_l(RMSNorm(h_l)).
 //
-// Per layer (page 4's cache flow, page 1 section 3): router -> routed ids to the host ->
-// slot-pool ensure (misses start uploading on the copy stream) -> FFN over the experts
-// that were already resident while the misses upload -> wait for the uploads -> FFN over
-// the missed experts -> release the slots -> combine with the residual (and the shared
-// experts, page 3: always-resident experts outside the pool).
+// Per layer with a host-managed pool (page 4's cache flow, page 1 section 3): router ->
+// routed ids to the host -> slot-pool ensure (misses start uploading on the copy stream) ->
+// FFN over the experts that were already resident while the misses upload -> wait for the
+// uploads -> FFN over the missed experts -> release the slots -> combine with the residual
+// (and the shared experts, page 3: always-resident experts outside the pool) and the next
+// layer's RMSNorm.  With a device-managed pool the LRU runs on the GPU (moe_cache_plan) and
+// the GEMVs fill the missed slots themselves; with every expert resident the FFN reads the
+// resident pool.  Neither of those needs the host during a step, so a whole step can be
+// captured once as a CUDA graph and replayed.
 #include <algorithm>
 #include <chrono>
 #include <vector>
@@ -461,7 +466,8 @@ extern "C" int moe_stack_decode(moe_stack *st, const float *x_in, float *y_out, 
     cudaStream_t cs = moe_cuda_stream(s);
     st->last_stream = cs;
     const moe_stack_desc &d = st->d;
-    const bool graphable = d.use_graph && d.device_managed && !d.profile && !ids_host_out && !weights_host_out;
+    const bool host_free = d.device_managed || d.n_groups == 0;  // no host round trip inside a step
+    const bool graphable = d.use_graph && host_free && !d.profile && !ids_host_out && !weights_host_out;
     if (graphable && st->eager_done[T]) {
         if (!st->graph[T]) {
             const int rc = capture_step(st, T);

@@ -347,3 +347,72 @@ def test_rmsnorm_closed_forms():
     # eps: a constant vector c gives c / sqrt(c^2 + eps)
     c = 0.01
     np.testing.assert_allclose(oracle.rmsnorm(np.full((1, 8), c), eps=1e-6), c / np.sqrt(c * c + 1e-6), rtol=1e-14)
+
+
+# ------------------------------------------------------------------------------------ comparison and inputs
+
+def test_relative_error_hand_worked_rows():
+    # row 0: |[1,-3] - [2,-4]| = [1, 1], max |ref| = 4 -> 1/4
+    # row 1: reference all zero -> the raw max difference (denominator 1)
+    # row 2: the largest difference sits on the smallest reference entry: 0.5 / 10
+    y = np.array([[1.0, -3.0], [0.5, -0.25], [10.0, 0.6]])
+    ref = np.array([[2.0, -4.0], [0.0, 0.0], [10.0, 0.1]])
+    got = oracle.relative_error(y, ref)
+    assert got.shape == (3,)
+    assert got.tolist() == [0.25, 0.5, 0.05]
+    # normwise per token: a row is not divided by its own element-wise magnitudes
+    assert oracle.relative_error(np.array([[1.0, 1e-9 + 1e-6]]), np.array([[1.0, 1e-9]]))[0] == pytest.approx(1e-6)
+    # the reduction runs over the hidden axis of [T][H], and y may come flattened
+    y3 = np.array([1.0, 2.0, 3.0, 4.0, 5.0, 6.0])
+    r3 = np.array([[1.0, 2.0, 4.0], [4.0, 5.0, 8.0]])
+    assert oracle.relative_error(y3, r3).tolist() == [1.0 / 4.0, 2.0 / 8.0]
+
+
+def test_x_to_double_bf16_and_fp32():
+    rng = np.random.default_rng(31)
+    bits = rng.integers(0, 65536, size=3000).astype(np.uint16)
+    bits = bits[((bits >> 7) & 0xFF) != 0xFF]  # drop inf / nan patterns
+    got = oracle.x_to_double(bits.reshape(-1, 1), 1).reshape(-1)
+    # against the oracle's own scalar decoder (pinned above against float32) ...
+    scalar = np.array([oracle.bf16_to_double(int(b)) for b in bits])
+    assert np.array_equal(got, scalar)
+    # ... and against numpy: a bf16 pattern is the upper half of a float32
+    via_np = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.array_equal(got, via_np)
+    # hand values: 0x3F80 = 1.0, 0xC000 = -2.0, 0x3E80 = 0.25, 0x0001 = 2^-133
+    hand = oracle.x_to_double(np.array([[0x3F80, 0xC000, 0x3E80, 0x0001]], dtype=np.uint16), 1)
+    assert hand.tolist() == [[1.0, -2.0, 0.25, 2.0 ** -133]]
+    # fp32 input: values unchanged, shape kept
+    xf = rng.standard_normal((4, 5)).astype(np.float32)
+    out = oracle.x_to_double(xf, 0)
+    assert out.dtype == np.float64 and out.shape == (4, 5)
+    assert np.array_equal(out, xf.astype(np.float64))
+
+
+def test_route_override_uses_the_given_ids_and_weights():
+    """moe_layer(route_override=(ids, w)) must weight the given experts by the given weights,
+    not by the oracle's own routing or softmax (near-tie tokens are checked this way)."""
+    cfg = synth.small_config(1, H=64, F=64, E=6, k=2, bias_a=1.0, n_shared=1)
+    x = np.random.default_rng(41).standard_normal((3, 64))
+    wr, b = synth.router_weights(cfg, 0), synth.router_bias(cfg, 0)
+    own = oracle.moe_layer(1, 64, 64, 2, x, wr, b, lambda e: synth.expert_weights(cfg, 0, e),
+                           shared=[synth.expert_weights(cfg, 0, 6)])
+    # a route the router did not take, in the reverse order, with weights unrelated to the logits
+    ids = np.array([[5, 0], [1, 4], [3, 2]], dtype=np.int32)
+    for t in range(3):
+        assert set(ids[t]) != set(own.ids[t]) or list(ids[t]) != list(own.ids[t])
+    w = np.array([[0.9, 0.1], [0.3, 0.7], [0.55, 0.45]])
+    res = oracle.moe_layer(1, 64, 64, 2, x, wr, b, lambda e: synth.expert_weights(cfg, 0, e),
+                           shared=[synth.expert_weights(cfg, 0, 6)], route_override=(ids, w))
+    ydense = _dense_layer_numpy(cfg, 0, x, wr, b, shared_ids=(6,))  # numpy, every expert
+    yref = np.stack([w[t, 0] * ydense[t, ids[t, 0]] + w[t, 1] * ydense[t, ids[t, 1]] + ydense[t, 6]
+                     for t in range(3)])
+    np.testing.assert_allclose(res.y, yref, rtol=1e-11, atol=1e-11)
+    assert res.ids.tolist() == ids.tolist()
+    assert np.array_equal(res.weights, w)
+    # the logits stay the router's own (the caller derives near-tie weights from them)
+    np.testing.assert_allclose(res.logits, own.logits, rtol=0, atol=0)
+    # the per-expert outputs follow the override's order
+    for t in range(3):
+        for j in range(2):
+            np.testing.assert_allclose(res.y_experts[t, j], ydense[t, ids[t, j]], rtol=1e-11, atol=1e-11)

@@ -127,16 +127,30 @@ def workload_config(cfg, T):
 # ----------------------------------------------------------------------------------- CPU oracle
 
 def _oracle_layer_time(cfg, layer, T, seed):
-    """Times one oracle layer on T tokens; the experts are generated before the clock starts."""
+    """Times one oracle layer on T tokens (routed and shared experts); the experts are
+    generated before the clock starts."""
     import oracle
     from routed_expert_ffn_gemv_gb300 import synth
     x = synth.tokens_x(cfg, seed, T).astype(np.float64)
     wr, b = synth.router_weights(cfg, layer), synth.router_bias(cfg, layer)
     ids, _, _ = oracle.topk_softmax(oracle.router_logits(x, wr, b), cfg.k)
     experts = {int(e): synth.expert_weights(cfg, layer, int(e)) for e in set(ids.reshape(-1).tolist())}
+    shared = [synth.expert_weights(cfg, layer, cfg.E + s) for s in range(cfg.n_shared)]
     t0 = time.perf_counter()
-    oracle.moe_layer(cfg.qtype, cfg.H, cfg.F, cfg.k, x, wr, b, experts.__getitem__)
+    oracle.moe_layer(cfg.qtype, cfg.H, cfg.F, cfg.k, x, wr, b, experts.__getitem__, shared=shared)
     return time.perf_counter() - t0
+
+
+def cpu_sample(cfg, T, budget_s):
+    """The fp64 oracle (every host thread) on a bounded sample of one batch-T decode step's
+    layers, scaled to the whole step."""
+    import oracle
+    times, t_start = [], time.perf_counter()
+    while (time.perf_counter() - t_start < budget_s or not times) and len(times) < cfg.L:
+        times.append(_oracle_layer_time(cfg, len(times), T, 6000 + len(times)))
+    step_s = float(np.mean(times)) * cfg.L
+    return {"value": T / step_s, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(times)} of {cfg.L} layers of one batch-{T} step, scaled to the step"}
 
 
 def cpu_baseline(cfg, T, budget_s=12.0, budget_1t_s=4.0):
@@ -221,6 +235,101 @@ def time_steps(stack, xs, T, steps, warmup, torch, stream):
     return ms, prof, d
 
 
+def time_window(stack, xs, T, total, warmup, torch, stream):
+    """From an empty pool: `warmup` untimed steps, then `total - warmup` steps bracketed by
+    events on the launching stream.  Returns (ms, statistics of the timed steps, statistics
+    of all `total` steps from the cold start)."""
+    y = torch.empty((T, stack.cfg.H), dtype=torch.float32, device=xs[0].device)
+    stack.reset_caches()
+    for i in range(warmup):
+        stack.decode(xs[i % len(xs)], y, stream=stream)
+    torch.cuda.synchronize()
+    stats0 = stack.cache_stats()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(warmup, total):
+        stack.decode(xs[i % len(xs)], y, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    stats1 = stack.cache_stats()
+    timed, cold = {}, {}
+    for k in (stats1[0] if stats1 else {}):
+        timed[k] = (sum(np.array(s1[k]) - np.array(s0[k]) for s0, s1 in zip(stats0, stats1))).tolist()
+        cold[k] = (sum(np.array(s1[k]) for s1 in stats1)).tolist()
+    return e0.elapsed_time(e1), timed, cold
+
+
+def hit_fields(st, prefix=""):
+    """Hit rates of a statistics dict: per distinct (layer, expert) query, per route, and by
+    ubatch bucket (<= 8 tokens, 9..32 tokens)."""
+    q, h = st["queries"], st["hits"]
+    out = {prefix + "hit_rate": sum(h) / sum(q) if sum(q) else None,
+           prefix + "route_hit_rate": st["route_hits"] / st["route_queries"] if st["route_queries"] else None}
+    for i, name in enumerate(("le8", "9to32")):
+        if q[i]:
+            out[prefix + f"hit_rate_{name}"] = h[i] / q[i]
+    return out
+
+
+def run_config(ci, Ts, torch, stream, peaks, link_gbs, warmup, total=256, stack=None, cpu_budget_s=4.0,
+               world=1, rank=0):
+    """One decode configuration at each batch size in Ts: the device-managed pool (the
+    configuration's slot counts, LRU on the GPU, misses read over the CPU-GPU link),
+    `total` steps from a cold pool of which the last total - warmup are timed, whole steps
+    replayed as CUDA graphs; then the same timed steps with every expert resident in HBM
+    (the HBM ceiling of the step); and the fp64 oracle on a bounded sample."""
+    from routed_expert_ffn_gemv_gb300 import synth
+    from routed_expert_ffn_gemv_gb300.workload import PinnedImages, Stack
+    cfg = synth.config(ci)
+    own = stack is None
+    if own:
+        images = PinnedImages(cfg, range(cfg.L), range(cfg.E))
+        stack = Stack(cfg, max_T=max(Ts), device_managed=True, use_graph=True, images=images)
+    images = stack.images
+    out = {}
+    xs = {T: [torch.from_numpy(synth.tokens_x(cfg, 3 + s, T)).cuda() for s in range(total)] for T in Ts}
+    shared_bytes = cfg.L * cfg.n_shared * cfg.expert_bytes
+    for T in Ts:
+        ms, st, cold = time_window(stack, xs[T], T, total, warmup, torch, stream)
+        ms = max_over_ranks(ms, world, torch)
+        steps = total - warmup
+        bytes_step = sum(st["queries"]) * cfg.expert_bytes / steps + shared_bytes
+        tps = T * steps / (ms / 1e3)
+        roof8 = T / (bytes_step / 8e12)
+        e = {"workload": f"{cfg.name} decode, batch {T}", "tokens_per_s": tps * world,
+             "ms_per_step": ms / steps, "steps_timed": steps, "steps_from_cold": total,
+             "pool": "+".join(str(g.n_slots) for g in cfg.groups) + " slots of "
+                     + "+".join(str(g.n_layers * cfg.E) for g in cfg.groups) + " experts",
+             "expert_bytes_per_step": bytes_step, "miss_bytes_per_step": st["h2d_bytes"] / steps,
+             "frac_of_8tbs_roofline": tps / roof8, "frac_of_measured_hbm_roofline":
+                 tps / (T / (bytes_step / (peaks["hbm_gbs"] * 1e9)))}
+        e.update(hit_fields(st))
+        e.update(hit_fields(cold, "from_cold_"))
+        miss_b = st["h2d_bytes"] / steps
+        t_att = miss_b / (link_gbs * 1e9) + (bytes_step - miss_b) / (peaks["hbm_gbs"] * 1e9)
+        e["frac_of_link_aware_attainable"] = tps / (T / t_att)
+        out[T] = e
+    stack.close()
+    # every expert resident in HBM, the same inputs (the same routing, so the same bytes)
+    res = Stack(cfg, max_T=max(Ts), resident=True, use_graph=True, images=images)
+    for T in Ts:
+        ms, _, _ = time_window(res, xs[T], T, total, warmup, torch, stream)
+        ms = max_over_ranks(ms, world, torch)
+        steps = total - warmup
+        tps = T * steps / (ms / 1e3)
+        b = out[T]["expert_bytes_per_step"]
+        out[T].update({"resident_tokens_per_s": tps * world, "resident_ms_per_step": ms / steps,
+                       "resident_frac_of_8tbs_roofline": tps / (T / (b / 8e12)),
+                       "resident_frac_of_measured_hbm_roofline": tps / (T / (b / (peaks["hbm_gbs"] * 1e9)))})
+    res.close()
+    del res, images
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and cpu_budget_s > 0:
+        for T in Ts:
+            out[T]["cpu_baseline"] = cpu_sample(cfg, T, cpu_budget_s)
+    return out
+
+
 def gemv_roofline(cfg, T, torch, stream, steps=40, warmup=5):
     """The decode GEMV kernels on HBM-resident weights: every layer's experts resident (24 x 32
     images, 1.28 GB, far above L2); every layer's router and permute run first, then rounds of
@@ -263,11 +372,12 @@ def gemv_roofline_block(gv, cfg, T, peaks):
             "achieved": gbs(gu_b, gu_ms), "peak": hbm, "unit": "GB/s", "frac": gbs(gu_b, gu_ms) / hbm,
             "peak_source": peaks["source"], "traffic": None if tr is None else tr["bytes_per_launch"],
             "algorithmic_bytes_per_launch": gu_b, "ms_per_launch": gu_ms, "launches": gv["launches"],
-            "down_kernel": {"achieved_gbs": gbs(dn_b, dn_ms), "frac": gbs(dn_b, dn_ms) / hbm,
-                            "ms_per_launch": dn_ms, "algorithmic_bytes_per_launch": dn_b},
+            "down_achieved_gbs": gbs(dn_b, dn_ms), "down_frac": gbs(dn_b, dn_ms) / hbm,
+            "down_ms_per_launch": dn_ms, "down_algorithmic_bytes_per_launch": dn_b,
             "ks_reduce_kernel_ms_per_launch": gv["reduce_ms_per_launch"],
-            "layer_chain": {"kernels": chain, "achieved_gbs": gbs(ch_b, ch_ms), "frac": gbs(ch_b, ch_ms) / hbm,
-                            "ms_per_layer": ch_ms, "algorithmic_bytes_per_layer": ch_b},
+            "layer_chain_kernels": chain, "layer_chain_achieved_gbs": gbs(ch_b, ch_ms),
+            "layer_chain_frac": gbs(ch_b, ch_ms) / hbm, "layer_chain_ms_per_layer": ch_ms,
+            "layer_chain_algorithmic_bytes_per_layer": ch_b,
             "measured_in": ("HBM-resident stack (all %d x %d expert images in HBM, above L2), batch %d; "
                             "each kernel (and each layer's chain) launched back to back over all layers in "
                             "rounds, CUDA events on the launching stream around the rounds (launch gaps "
@@ -375,6 +485,38 @@ def run_prefill(torch, peaks, steps=10, warmup=3):
     return out
 
 
+def flat_prefill(pf, peaks):
+    """The prefill results as flat scalars (t<T>_<field>)."""
+    out = {"peak_tflops": peaks["bf16_tflops"], "peak": "measured dense bf16 burst (fp16 tcgen05 runs at "
+           "the same rate)", "operands": "fp16 (bf16 x exact in fp16), fp32 accumulate"}
+    for T, r in pf.items():
+        for k, v in r.items():
+            if isinstance(v, (int, float)):
+                out[f"t{T}_{k}"] = v
+    return out
+
+
+def summary_lines(line):
+    """A compact human-readable table of the run (printed to stderr)."""
+    rows = [f"headline {line['config']['workload']}: {line['value']:.1f} tok/s "
+            f"({line['ms_per_step']:.3f} ms/step), e2e {line['e2e']['value']:.1f} tok/s"]
+    r = line["roofline"]
+    rows.append(f"gate/up GEMV {r['achieved']:.0f} GB/s = {r['frac']:.3f} of measured HBM; down "
+                f"{r['down_frac']:.3f}; layer chain {r['layer_chain_frac']:.3f}")
+    for name, e in line.get("configs", {}).items():
+        rows.append(f"{name}: {e['tokens_per_s']:.1f} tok/s ({e['frac_of_8tbs_roofline']:.3f} of 8 TB/s), "
+                    f"hit {e.get('hit_rate') or 0:.3f} (from cold {e.get('from_cold_hit_rate') or 0:.3f}); "
+                    f"resident {e['resident_tokens_per_s']:.1f} tok/s "
+                    f"({e['resident_frac_of_8tbs_roofline']:.3f} of 8 TB/s); "
+                    f"oracle {e.get('cpu_baseline', {}).get('value', float('nan')):.2f} tok/s")
+    pf = line.get("prefill", {})
+    for T in ("512", "4096"):
+        if f"t{T}_ffn_ms" in pf:
+            rows.append(f"prefill {T}: FFN {pf[f't{T}_ffn_ms']:.3f} ms, {pf[f't{T}_ffn_tflops']:.1f} TFLOP/s "
+                        f"= {pf[f't{T}_frac_of_dense_peak']:.3f} of dense peak")
+    return rows
+
+
 def run_gpu(args, world, rank, local):
     import torch
     torch.cuda.set_device(local)
@@ -386,40 +528,34 @@ def run_gpu(args, world, rank, local):
     L.load()
     cfg = synth.config(CONFIG_INDEX)
     peaks = load_peaks()
-    max_T = max(max(cfg.tokens), args.batch)
+    T = args.batch
+    max_T = max(max(cfg.tokens), T)
     link_gbs = h2d_bandwidth(torch)
     dev_stack = Stack(cfg, max_T=max_T, device_managed=True, use_graph=True)
     stream = torch.cuda.Stream()
-    batches = [args.batch] if args.lite else sorted(set(list(cfg.tokens) + [args.batch]))
-    inputs = {T: [torch.from_numpy(synth.tokens_x(cfg, 3 + s, T)).cuda() for s in range(64)] for T in batches}
+    inputs = [torch.from_numpy(synth.tokens_x(cfg, 3 + s, T)).cuda() for s in range(64)]
 
     clocks = ClockSampler(local)
-    results = {}
-    main = None
-    for T in batches:
-        steps = args.steps if T == args.batch else max(20, args.steps // 2)
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        ms, prof, st = time_steps(dev_stack, inputs[T], T, steps, args.warmup, torch, stream)
-        ms = max_over_ranks(ms, world, torch)
-        results[T] = batch_result(cfg, T, steps, ms, st, world, peaks, link_gbs)
-        results[T]["kernel_launches_per_step"] = prof["kernel_launches"] / steps
-        if T == args.batch:
-            main = (ms, prof, st, steps)
+    # the headline: W warm-up steps, then exactly K timed steps
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ms, prof, st = time_steps(dev_stack, inputs, T, args.steps, args.warmup, torch, stream)
+    ms = max_over_ranks(ms, world, torch)
+    r = batch_result(cfg, T, args.steps, ms, st, world, peaks, link_gbs)
+    r["kernel_launches_per_step"] = prof["kernel_launches"] / args.steps
     if args.lite:
         clocks.stop()
         if rank == 0:
-            print(json.dumps({"metric": METRIC, "value": results[args.batch]["tokens_per_s"], "unit": "tokens/s",
-                              "lite": True, "batch": args.batch, "result": results[args.batch]}), flush=True)
+            print(json.dumps({"metric": METRIC, "value": r["tokens_per_s"], "unit": "tokens/s",
+                              "lite": True, "batch": T, "result": r}), flush=True)
         dev_stack.close()
         return 0
 
     # per-kernel breakdown of the device-managed step (eager launches, events around every kernel)
-    T = args.batch
     dev_stack.set_profile(2)
     bsteps = max(20, args.steps // 4)
-    _, bprof, bst = time_steps(dev_stack, inputs[T], T, bsteps, 3, torch, stream)
+    _, bprof, bst = time_steps(dev_stack, inputs, T, bsteps, 3, torch, stream)
     breakdown = {k + "_per_step": bprof[k] / bsteps for k in
                  ("router_ms", "permute_ms", "gateup_ms", "down_ms", "combine_ms")}
     breakdown["steps"] = bsteps
@@ -429,11 +565,10 @@ def run_gpu(args, world, rank, local):
                             if L.moe_get_decode_fused() else ""))
     dev_stack.set_profile(0)
 
-    # host-managed pool (moe_cache_ensure + copy-engine uploads); its profiled loop times the
-    # gate/up GEMV on HBM-resident bytes only
-    host_stack = Stack(cfg, max_T=max_T, profile=1)
+    # host-managed pool (moe_cache_ensure + copy-engine uploads)
+    host_stack = Stack(cfg, max_T=max_T, profile=1, images=dev_stack.images)
     hsteps = max(20, args.steps // 2)
-    hms, hprof, hst = time_steps(host_stack, inputs[T], T, hsteps, args.warmup, torch, stream)
+    hms, hprof, hst = time_steps(host_stack, inputs, T, hsteps, args.warmup, torch, stream)
     hms = max_over_ranks(hms, world, torch)
     host_res = batch_result(cfg, T, hsteps, hms, hst, world, peaks, link_gbs)
     host_res["host_wait_ms_per_step"] = hprof["host_wait_ms"] / hsteps
@@ -462,35 +597,48 @@ def run_gpu(args, world, rank, local):
         stream.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, torch)
     e2e_tps = T * e2e_steps / (e2e_ms / 1e3) * world
-    dev_stack.close()
+
+    # every decode configuration at the metric's batch sizes (256 steps from a cold pool each)
+    configs = {}
+    cpu_budget = 0.0 if args.no_cpu else 4.0
+    for ci, Ts, stk in ((1, (1, 4, 8), dev_stack), (2, (1,), None), (3, (1, 32), None)):
+        if args.configs is not None and ci not in args.configs:
+            if stk is not None:
+                stk.close()
+            continue
+        res = run_config(ci, Ts, torch, stream, peaks, link_gbs, args.warmup, total=args.config_steps,
+                         stack=stk, cpu_budget_s=cpu_budget, world=world, rank=rank)
+        short = {1: "granite", 2: "qwen3", 3: "deepseek"}[ci]
+        for Tb, e in res.items():
+            configs[f"{short}_b{Tb}"] = e
 
     prefill = run_prefill(torch, peaks)
+    gv = gemv_roofline(cfg, T, torch, stream, steps=20, warmup=3)
     clk = clocks.stop()
 
-    ms, prof, st, steps = main
-    r = results[args.batch]
-    gv = gemv_roofline(cfg, T, torch, stream, steps=20, warmup=3)
     roofline = gemv_roofline_block(gv, cfg, T, peaks)
     if rank == 0:
-        cb = cpu_baseline(cfg, T) if world == 1 else None
+        cb = cpu_baseline(cfg, T) if world == 1 and not args.no_cpu else None
         line = {"metric": METRIC, "value": r["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
-                "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-                "data": "synthetic (seeded q8_0 experts, N(0,1) activations; no datasets or trained weights)",
+                "data": "synthetic (seeded q8_0 / 4-bit experts, N(0,1) activations; no datasets or trained weights)",
                 "config": workload_config(cfg, T), "impl": "gb300",
                 "mode": "device-managed pool, whole step replayed as a CUDA graph",
                 "hit_rate": r["hit_rate"], "frac_of_8tbs_roofline": r["frac_of_8tbs_roofline"],
                 "frac_of_measured_hbm_roofline": r["frac_of_measured_hbm_roofline"],
                 "h2d_link_gbs_measured": link_gbs,
                 "frac_of_link_aware_attainable": r["frac_of_link_aware_attainable"],
-                "batches": {str(b): results[b] for b in batches},
-                "host_managed": host_res, "breakdown": breakdown, "prefill": prefill,
-                "roofline": roofline, "cpu_baseline": cb,
+                "headline": r, "host_managed": host_res, "breakdown": breakdown,
+                "cpu_baseline": cb,
                 "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": T * cfg.H * 4,
                         "d2h_bytes_per_step": T * cfg.H * 4, "steps": e2e_steps},
                 "gpu_launches": int(prof["kernel_launches"]),
-                "clocks": clk}
+                "clocks": clk, "prefill": flat_prefill(prefill, peaks), "roofline": roofline,
+                "configs": configs}
         print(json.dumps(line), flush=True)
+        for row in summary_lines(line):
+            print(row, file=sys.stderr)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
@@ -505,6 +653,11 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--lite", action="store_true",
                     help="only the device-managed timed loop at --batch (the ncu target)")
+    ap.add_argument("--configs", type=lambda v: [int(c) for c in v.split(",")], default=None,
+                    help="decode configurations of the configs block (default 1,2,3)")
+    ap.add_argument("--config-steps", type=int, default=256,
+                    help="decode steps per configuration entry, from a cold pool (warm-up included)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU samples")
     ap.add_argument("--only", choices=["host", "gemv", "prefill"], default=None,
                     help="profiling targets: 'host' = host-managed pool loop at --batch, 'gemv' = the "
                          "decode GEMVs on an HBM-resident stack at --batch, 'prefill' = the prefill "

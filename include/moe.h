@@ -466,9 +466,14 @@ int moe_get_decode_fused(void);
 /* ------------------------------------------------------------------ test hooks */
 
 /*
- * moe_debug_inject_fault — host-side fault injection for tests: kind 1 makes the
- * n-th following miss upload (n = countdown, 0 = the next) fail as if the copy
- * could not be issued; kind 0 disarms.  Never touches the GPU.
+ * moe_debug_inject_fault — fault injection for tests, armed on the host; kind 0 disarms.
+ *  kind 1: the n-th following miss upload (n = countdown, 0 = the next) fails as if the
+ *          copy could not be issued.  Never touches the GPU.
+ *  kind 2: the n-th following fused decode GEMV launch (moe_set_decode_fused(1)) is given
+ *          a grid barrier that waits for one arrival more than it has CTAs, bounded at
+ *          20 ms: every CTA's wait runs out, MOE_ERR_TIMEOUT is recorded in the device status
+ *          word and the kernel goes on to its end (its outputs are then meaningless).  This
+ *          exercises the bounded-wait path without faulting or hanging the GPU.
  */
 int moe_debug_inject_fault(int kind, int countdown);
 

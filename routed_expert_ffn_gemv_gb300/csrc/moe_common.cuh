@@ -92,6 +92,9 @@ __device__ static inline void moe_set_status(int *status_word, int code) {
 
 // Host-side fault injection (tests): returns true if this miss upload must fail.
 bool moe_fault_take_upload();
+// Host-side fault injection (tests): returns true if this fused decode GEMV launch must be
+// given a grid barrier that waits for an arrival that never comes (bounded, short).
+bool moe_fault_take_grid_barrier();
 
 // ------------------------------------------------------------------ decode FFN internals
 

@@ -197,6 +197,9 @@ struct FfnParams {
     float *partial;
     const unsigned long long *first;  // [CTA][warp]: image of the warp's first unit, 0: none/skip/fill
     int *status;
+    int sync_extra;                     // fused launch: arrivals its grid barrier waits for beyond the
+                                        // grid (0; 1 only under test fault injection)
+    unsigned long long sync_wait_ns;    // fused launch: bound of each grid-barrier wait
     int x_vec;              // x is 16-byte aligned: vector loads
     GvGeom geo;             // this launch's geometry
 };
@@ -206,6 +209,15 @@ __device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// Wall time in nanoseconds (the global timer).
+__device__ __forceinline__ unsigned long long gv_globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bound of the drain after a timed-out wait (copies still landing in a warp's ring).
+#define GV_DRAIN_NS 4000000000ull
 
 // ------------------------------------------------------------------ fp16 fragments
 
@@ -824,9 +836,15 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
         a = e;
     }
     // Never leave with copies in flight: a wait that ran out left chunks J_done .. issued-1
-    // unconsumed; give each a second bounded wait.
-    if (lane == 0)
-        for (int j = J_done; j < J_issued; ++j) mbar_wait_bounded(&bars[j % S], (j / S) & 1, p.status);
+    // unconsumed.  Keep waiting for each (the status word already says MOE_ERR_TIMEOUT), up to
+    // GV_DRAIN_NS of wall time in all, so that the CTA exits only after its copies landed
+    // unless the copy engine itself stopped answering.
+    if (lane == 0 && J_done < J_issued) {
+        const unsigned long long t0 = gv_globaltimer();
+        for (int j = J_done; j < J_issued; ++j)
+            while (!mbar_try_wait(&bars[j % S], (j / S) & 1))
+                if (gv_globaltimer() - t0 > GV_DRAIN_NS) return;
+    }
 }
 
 // Gate/up launch: CTA c works on K range c / (G / KS) only, so it stages x (every token row
@@ -868,31 +886,29 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_warp_kernel(FfnParams p) {
 // Grid barrier: sync[0] counts the CTAs that arrived, sync[1] is the barrier's generation.
 // The last CTA to arrive resets the count and advances the generation, so the barrier can be
 // passed any number of times (sync[0] starts at 0: the permute kernel clears it).  The wait
-// is bounded: past GV_GRID_WAIT_NS the CTA sets MOE_ERR_TIMEOUT and goes on.
+// is bounded: past wait_ns (GV_GRID_WAIT_NS normally) the CTA sets MOE_ERR_TIMEOUT and goes
+// on.  `extra` raises the arrival count the barrier waits for above the grid size; it is 0
+// except under test fault injection, where 1 makes every CTA's wait run out.
 #define GV_GRID_WAIT_NS 500000000ull
-__device__ __forceinline__ unsigned long long gv_globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
+#define GV_GRID_WAIT_TEST_NS 20000000ull
 __device__ __forceinline__ int ld_acquire_gpu(const int *a) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
     return v;
 }
-__device__ void grid_sync(int *sync, int *status) {
+__device__ void grid_sync(int *sync, int *status, int extra, unsigned long long wait_ns) {
     __syncthreads();
     if (threadIdx.x == 0) {
         const int gen = ld_acquire_gpu(sync + 1);
         __threadfence();  // this CTA's writes before its arrival
-        if (atomicAdd(sync, 1) == (int)gridDim.x - 1) {
+        if (atomicAdd(sync, 1) == (int)gridDim.x + extra - 1) {
             atomicExch(sync, 0);
             __threadfence();
             atomicAdd(sync + 1, 1);
         } else {
             const unsigned long long t0 = gv_globaltimer();
             while (ld_acquire_gpu(sync + 1) == gen) {
-                if (gv_globaltimer() - t0 > GV_GRID_WAIT_NS) {
+                if (gv_globaltimer() - t0 > wait_ns) {
                     moe_set_status(status, MOE_ERR_TIMEOUT);
                     break;
                 }
@@ -921,7 +937,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_fused_kernel(FfnParams p1, 
     ffn_body<QT, XT, false, 2, false>(p1, smem, [] {});
     __syncthreads();  // the gate/up rings and slots are no longer read: the down rings reuse them
     ffn_body<QT, MOE_F32, true, NTL2, true>(p2, smem, [&] {
-        grid_sync(sync, p1.status);
+        grid_sync(sync, p1.status, p1.sync_extra, p1.sync_wait_ns);
         if (p1.KS > 1) {
             const size_t n = (size_t)p1.RT * p1.F, i0 = (size_t)blockIdx.x * GV_THREADS + threadIdx.x,
                          step = (size_t)gridDim.x * GV_THREADS;
@@ -931,7 +947,7 @@ __global__ void __launch_bounds__(GV_THREADS, 1) ffn_fused_kernel(FfnParams p1, 
                 case 8: ks_reduce_range<8>(p1.gu, p2.h, n, i0, step); break;
                 default: ks_reduce_range<16>(p1.gu, p2.h, n, i0, step); break;
             }
-            grid_sync(sync, p1.status);
+            grid_sync(sync, p1.status, p1.sync_extra, p1.sync_wait_ns);
         }
     });
 }
@@ -1454,6 +1470,8 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
     p.partial = partial;
     p.status = moe_status_word_device_ptr();
     p.x_vec = ((uintptr_t)x & 15) == 0;
+    p.sync_extra = 0;
+    p.sync_wait_ns = GV_GRID_WAIT_NS;
 
     if (stages & MOE_FFN_PERMUTE) {
     if (timing && timing->permute0) MOE_TRY_CUDA(cudaEventRecord(timing->permute0, s));
@@ -1480,6 +1498,10 @@ int moe_expert_ffn_stages(const void *x, int xtype, int T, int H, int F, int qty
     if (g_fused.load() && (stages & kGemvStages) == kGemvStages) {
         if (timing && timing->gateup0) MOE_TRY_CUDA(cudaEventRecord(timing->gateup0, s));
         FfnParams p1 = p, p2 = p;
+        if (moe_fault_take_grid_barrier()) {  // test fault injection: a barrier that times out
+            p1.sync_extra = 1;
+            p1.sync_wait_ns = GV_GRID_WAIT_TEST_NS;
+        }
         p1.geo = pl.g1;
         p1.ranges = p.ws_ints + ws_ranges_off(E, T * k, 0);
         p1.first = (const unsigned long long *)((char *)workspace + W.first_off);

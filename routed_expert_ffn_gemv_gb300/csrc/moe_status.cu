@@ -61,11 +61,21 @@ static std::atomic<int> g_fault_kind{0};
 static std::atomic<int> g_fault_countdown{0};
 
 extern "C" int moe_debug_inject_fault(int kind, int countdown) {
-    MOE_CHECK(kind == 0 || kind == 1);
+    MOE_CHECK(kind == 0 || kind == 1 || kind == 2);
     MOE_CHECK(countdown >= 0);
     g_fault_countdown.store(countdown);
     g_fault_kind.store(kind);
     return MOE_OK;
+}
+
+bool moe_fault_take_grid_barrier() {
+    if (g_fault_kind.load() != 2) return false;
+    int c = g_fault_countdown.fetch_sub(1);
+    if (c == 0) {
+        g_fault_kind.store(0);
+        return true;
+    }
+    return false;
 }
 
 bool moe_fault_take_upload() {

@@ -68,7 +68,8 @@ class Stack:
     def __init__(self, cfg: synth.MoEConfig, max_T: Optional[int] = None, overlap: bool = True,
                  profile: int = 0, pool_slots: Optional[Sequence[int]] = None,
                  n_layers: Optional[int] = None, random_scales: bool = False,
-                 resident: bool = False, device_managed: bool = False, use_graph: bool = False):
+                 resident: bool = False, device_managed: bool = False, use_graph: bool = False,
+                 images: Optional[PinnedImages] = None):
         self.cfg = cfg
         self.L = n_layers or cfg.L
         self.max_T = max_T or max(cfg.tokens)
@@ -83,8 +84,13 @@ class Stack:
         for l in range(self.L):
             b = synth.router_bias(cfg, l)
             self.bias.append(None if b is None else torch.from_numpy(b).to(self.dev))
-        # routed expert images
-        self.images = PinnedImages(cfg, range(self.L), range(E), random_scales)
+        # routed expert images (an existing set of the same config may be shared)
+        if images is not None:
+            assert images.cfg == cfg and images.layers[: self.L] == list(range(self.L))
+            assert images.experts == list(range(E)) and not random_scales
+            self.images = images
+        else:
+            self.images = PinnedImages(cfg, range(self.L), range(E), random_scales)
         self.caches: List[int] = []
         self.pools: List[torch.Tensor] = []
         self.states: List[torch.Tensor] = []
@@ -95,6 +101,7 @@ class Stack:
         if not groups:
             self.resident_pool = torch.empty(self.L * E * self.stride, dtype=torch.uint8, device=self.dev)
             self.resident_pool.copy_(self.images.buf[: self.L * E * self.stride])
+            torch.cuda.synchronize()
         else:
             for gi, grp in enumerate(groups):
                 n_layers_g = min(grp.n_layers, self.L - grp.first_layer)

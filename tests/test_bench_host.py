@@ -24,12 +24,13 @@ def test_roofline_block_is_the_gate_up_kernel_over_its_own_time():
     assert r["achieved"] == pytest.approx(30e6 / 10e-6 / 1e9)   # 3000 GB/s
     assert r["frac"] == pytest.approx(0.5)
     assert r["algorithmic_bytes_per_launch"] == 30e6 and r["ms_per_launch"] == 0.010
-    assert r["down_kernel"]["achieved_gbs"] == pytest.approx(15e6 / 8e-6 / 1e9)
-    chain = r["layer_chain"]
-    assert chain["algorithmic_bytes_per_layer"] == 45e6
-    assert chain["achieved_gbs"] == pytest.approx(45e6 / 25e-6 / 1e9)
-    assert "ks_reduce_kernel" in chain["kernels"]
-    assert "ffn_fused_kernel" in bench.gemv_roofline_block(_gv(True), cfg, 8, peaks)["layer_chain"]["kernels"]
+    assert r["down_achieved_gbs"] == pytest.approx(15e6 / 8e-6 / 1e9)
+    assert r["layer_chain_algorithmic_bytes_per_layer"] == 45e6
+    assert r["layer_chain_achieved_gbs"] == pytest.approx(45e6 / 25e-6 / 1e9)
+    assert "ks_reduce_kernel" in r["layer_chain_kernels"]
+    assert "ffn_fused_kernel" in bench.gemv_roofline_block(_gv(True), cfg, 8, peaks)["layer_chain_kernels"]
+    # the driver keeps only flat scalars inside the roofline object
+    assert all(not isinstance(v, (dict, list)) for v in r.values())
 
 
 def test_traffic_record_needs_the_current_kernel_source(tmp_path, monkeypatch):
@@ -79,3 +80,29 @@ def test_peaks_fall_back_when_no_measurement(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     p = bench.load_peaks()
     assert p["source"] == "fallback" and p["hbm_gbs"] == 6800.0 and p["bf16_tflops"] == 1900.0
+
+
+def test_hit_fields_by_query_route_and_bucket():
+    st = {"queries": [10, 30], "hits": [9, 15], "route_queries": 100, "route_hits": 80}
+    h = bench.hit_fields(st)
+    assert h["hit_rate"] == pytest.approx(24 / 40)
+    assert h["route_hit_rate"] == pytest.approx(0.8)
+    assert h["hit_rate_le8"] == pytest.approx(0.9) and h["hit_rate_9to32"] == pytest.approx(0.5)
+    h0 = bench.hit_fields({"queries": [4, 0], "hits": [1, 0], "route_queries": 0, "route_hits": 0}, "c_")
+    assert h0["c_hit_rate"] == 0.25 and h0["c_route_hit_rate"] is None and "c_hit_rate_9to32" not in h0
+
+
+def test_prefill_block_is_flat_and_summary_prints():
+    pf = bench.flat_prefill({"512": {"ffn_ms": 0.3, "ffn_tflops": 120.0, "frac_of_dense_peak": 0.06, "x": "s"},
+                             "4096": {"ffn_ms": 0.6, "ffn_tflops": 500.0, "frac_of_dense_peak": 0.27}},
+                            {"bf16_tflops": 1854.8})
+    assert pf["t512_ffn_ms"] == 0.3 and pf["t4096_frac_of_dense_peak"] == 0.27 and "t512_x" not in pf
+    assert all(not isinstance(v, (dict, list)) for v in pf.values())
+    line = {"config": {"workload": "w"}, "value": 1.0, "ms_per_step": 2.0, "e2e": {"value": 1.0},
+            "roofline": {"achieved": 1.0, "frac": 0.1, "down_frac": 0.2, "layer_chain_frac": 0.3},
+            "configs": {"qwen3_b1": {"tokens_per_s": 5.0, "frac_of_8tbs_roofline": 0.1, "hit_rate": 0.5,
+                                     "from_cold_hit_rate": 0.4, "resident_tokens_per_s": 9.0,
+                                     "resident_frac_of_8tbs_roofline": 0.2}},
+            "prefill": pf}
+    rows = bench.summary_lines(line)
+    assert len(rows) == 5 and rows[2].startswith("qwen3_b1")

@@ -1,54 +1,16 @@
-"""Full-size parity of the three large configurations, in the launch configuration the
-bench uses (the decode-step runtime over real-size slot pools), on sampled outputs:
-
-* Qwen3-30B-A3B-shaped stack (48 layers, 128 experts, top-8, 4-bit, two 24-layer groups of
-  1,834 slots): batch 1, every layer of several decode steps, teacher-forced;
-* DeepSeek-MoE-16B-shaped stack (28 layers, 64 routed + 2 shared, top-2, q8_0, 224 slots):
-  batch 1 and 32;
-* the Qwen-shaped prefill layer (bf16 x, all 128 experts resident): 512 tokens, sampled rows.
-
-Routing ids and slot assignments are compared bit-exact; outputs within 2e-3.
+"""Full-size parity of the Qwen-shaped prefill layer (bf16 x, all 128 experts resident,
+512 tokens) on sampled rows: routing ids bit-exact, outputs within 2e-3.  (The decode
+stacks at full size are covered over their whole 256-step length in test_gpu_long_runs.)
 """
 import numpy as np
 import pytest
 
 import oracle
 from tests.gpu_helpers import TOL, ids_match, rel_err
-from tests.test_gpu_stack import run_steps
 from routed_expert_ffn_gemv_gb300 import _lib as L, synth
 
 torch = pytest.importorskip("torch")
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
-
-
-def _stack(*a, **kw):
-    from routed_expert_ffn_gemv_gb300.workload import Stack
-    return Stack(*a, **kw)
-
-
-def test_qwen_stack_full_size_batch1():
-    cfg = synth.config(2)
-    st = _stack(cfg, max_T=1)
-    ck = run_steps(st, cfg, 1, 4, step0=0)
-    print(f"config2: worst rel err {ck.worst:.3e} over {ck.compared} token-layers, excluded {ck.excluded}")
-    s0, s1 = st.cache_stats()
-    assert s0["ensure_calls"] == 4 * 24 and s1["ensure_calls"] == 4 * 24
-    st.close()
-
-
-@pytest.fixture(scope="module")
-def deepseek_stack():
-    cfg = synth.config(3)
-    st = _stack(cfg, max_T=32)
-    yield cfg, st
-    st.close()
-
-
-@pytest.mark.parametrize("T", [1, 32])
-def test_deepseek_stack_full_size(deepseek_stack, T):
-    cfg, st = deepseek_stack
-    ck = run_steps(st, cfg, T, 2, step0=50 + T)
-    print(f"config3 T={T}: worst rel err {ck.worst:.3e}, excluded {ck.excluded}")
 
 
 def test_qwen_prefill_layer_512_tokens_sampled():

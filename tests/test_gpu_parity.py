@@ -377,3 +377,36 @@ def test_slot_pool_rejects_pageable_images():
     with pytest.raises(L.MoeError) as ei:
         L.moe_cache_create(desc)
     assert ei.value.status == L.MOE_ERR_INVALID
+
+
+# ------------------------------------------------------------------------------------ bounded waits
+
+@pytest.mark.parametrize("T", [8, 1])
+def test_grid_barrier_wait_runs_out_and_is_reported(T):
+    """A bounded device-side wait that runs out: the fused GEMV launch's grid barrier is made to
+    wait for one arrival more than the grid has (host-armed fault injection, 20 ms bound).  The
+    kernel records MOE_ERR_TIMEOUT and returns; the context stays usable and the next call
+    (disarmed) gives the same bits as the separate kernels."""
+    cfg = synth.small_config(0, H=1024, F=512, E=32, k=8, seed_cfg=960)
+    pool, stride = make_pool(cfg, 0, range(cfg.E), False)
+    rng = np.random.default_rng(61 + T)
+    x_d = to_dev(rng.standard_normal((T, cfg.H), dtype=np.float32))
+    ids, w = random_routes(rng, T, cfg.E, cfg.k)
+    before = L.moe_get_decode_fused()
+    status_clear()
+    try:
+        L.moe_set_decode_fused(True)
+        L.moe_debug_inject_fault(2, 0)
+        run_ffn(cfg, pool, stride, x_d, 0, ids, w)
+        torch.cuda.synchronize()
+        assert L.moe_device_status(clear=True) == L.MOE_ERR_TIMEOUT
+        assert L.moe_device_status(clear=False) == 0   # cleared
+        fused = run_ffn(cfg, pool, stride, x_d, 0, ids, w).cpu().numpy()   # disarmed again
+        status_clear()
+        L.moe_set_decode_fused(False)
+        sep = run_ffn(cfg, pool, stride, x_d, 0, ids, w).cpu().numpy()
+        status_clear()
+    finally:
+        L.moe_debug_inject_fault(0, 0)
+        L.moe_set_decode_fused(before)
+    assert np.array_equal(fused.view(np.uint32), sep.view(np.uint32))

@@ -15,7 +15,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.gpu_helpers import TOL, random_routes, rel_err
+from tests.gpu_helpers import TOL, ids_match, random_routes, rel_err
 from routed_expert_ffn_gemv_gb300 import _lib as L, synth
 
 torch = pytest.importorskip("torch")
@@ -152,26 +152,49 @@ def test_prefill_invalid_slot_reported_others_computed():
 
 
 def test_prefill_qwen_layer_4096_tokens_sampled():
+    """The Qwen-shaped prefill layer at 4096 tokens: ids bit-exact against the oracle's top-k
+    (near ties excluded) on every token, and sampled token outputs against the oracle's own
+    routing (route override only for near-tie tokens)."""
     cfg = synth.config(4)
-    T = 4096
+    T, H, F, E, k = 4096, cfg.H, cfg.F, cfg.E, cfg.k
     from routed_expert_ffn_gemv_gb300.workload import PinnedImages, slot_stride
-    imgs = PinnedImages(cfg, [0], range(cfg.E))
-    pool, stride = imgs.buf.cuda(), slot_stride(cfg)
-    xb = synth.tokens_x(cfg, 0, T)
+    imgs = PinnedImages(cfg, [0], range(E))
+    stride = slot_stride(cfg)
+    pool = imgs.buf.cuda()
+    xb = synth.tokens_x(cfg, 11, T)
     x_d = torch.from_numpy(xb.view(np.int16)).cuda()
     wr, b = synth.router_weights(cfg, 0), synth.router_bias(cfg, 0)
-    ids = torch.empty((T, cfg.k), dtype=torch.int32, device="cuda")
-    w = torch.empty((T, cfg.k), dtype=torch.float32, device="cuda")
-    L.moe_router_topk(x_d, 1, T, cfg.H, torch.from_numpy(wr.view(np.int16)).cuda(),
-                      torch.from_numpy(b).cuda(), cfg.E, cfg.k, ids, w)
-    ws_bytes = L.moe_expert_ffn_workspace(T, cfg.H, cfg.F, cfg.qtype, 1, cfg.E, cfg.k)
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    L.moe_router_topk(x_d, 1, T, H, torch.from_numpy(wr.view(np.int16)).cuda(), torch.from_numpy(b).cuda(),
+                      E, k, ids, w)
+    ws_bytes = L.moe_expert_ffn_workspace(T, H, F, cfg.qtype, 1, E, k)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    partial = torch.empty((T, cfg.k, cfg.H), dtype=torch.float32, device="cuda")
-    L.moe_expert_ffn(x_d, 1, T, cfg.H, cfg.F, cfg.qtype, cfg.E, cfg.k, ids, w, None, cfg.E, pool, stride,
-                     None, 0, partial, ws, ws_bytes)
+    partial = torch.empty((T, k, H), dtype=torch.float32, device="cuda")
+    L.moe_expert_ffn(x_d, 1, T, H, F, cfg.qtype, E, k, ids, w, None, E, pool, stride, None, 0, partial, ws,
+                     ws_bytes)
+    y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    L.moe_combine(partial, T, k, H, None, y)
     torch.cuda.synchronize()
     assert L.moe_device_status(clear=True) == 0
-    rng = np.random.default_rng(9)
-    sample = np.sort(rng.choice(T, size=12, replace=False))
     x64 = oracle.x_to_double(xb, 1)
-    _check(cfg, ids.cpu().numpy(), w.cpu().numpy(), x64, partial.cpu().numpy(), False, sample=sample)
+    logits = oracle.router_logits(x64, wr, b)
+    oids, ow, _ = oracle.topk_softmax(logits, k)
+    ids_h = ids.cpu().numpy()
+    m = ids_match(ids_h, logits, oids, k)
+    assert all(v is not False for v in m)
+    print(f"prefill 4096: {sum(v is None for v in m)} near-tie tokens excluded from the id check")
+    rng = np.random.default_rng(5)
+    sample = np.sort(rng.choice(T, size=24, replace=False))
+    need = sorted(set(oids[sample].reshape(-1).tolist()) | set(ids_h[sample].reshape(-1).tolist()))
+    ex = {e: synth.expert_weights(cfg, 0, e) for e in need}
+    ref = oracle.moe_layer(cfg.qtype, H, F, k, x64[sample], wr, b, ex.__getitem__).y
+    near = [i for i, t in enumerate(sample) if m[t] is None]
+    if near:
+        sel = np.take_along_axis(logits[sample[near]], ids_h[sample[near]].astype(np.int64), axis=1)
+        ww = np.exp(sel - sel.max(axis=1, keepdims=True))
+        ww /= ww.sum(axis=1, keepdims=True)
+        ref[near] = oracle.moe_layer(cfg.qtype, H, F, k, x64[sample[near]], wr, b, ex.__getitem__,
+                                     route_override=(ids_h[sample[near]], ww)).y
+    err = rel_err(y.cpu().numpy()[sample].astype(np.float64), ref)
+    assert err.max() <= TOL, err

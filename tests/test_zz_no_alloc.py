@@ -64,15 +64,15 @@ def _compare_calls(cfg, pool, stride, calls, seed):
     assert L.moe_device_status(clear=True) == 0
 
 
-@pytest.mark.parametrize("qtype,H,F,E,k", [(0, 1024, 512, 32, 8), (1, 2048, 768, 16, 8)])
-def test_noalloc_matches_workspace_entry_point_on_calls_in_a_row(qtype, H, F, E, k):
+@pytest.mark.parametrize("qtype,H,F,E,k,T0", [(0, 1024, 512, 32, 8, 24), (1, 2048, 768, 16, 8, 16)])
+def test_noalloc_matches_workspace_entry_point_on_calls_in_a_row(qtype, H, F, E, k, T0):
     cfg = synth.small_config(qtype, H=H, F=F, E=E, k=k, seed_cfg=990 + qtype)
     pool, stride = _pool(cfg)
     # set-up call (T = 0): resolves the array's address, computes nothing
     L.moe_expert_ffn_noalloc(None, 0, 0, H, F, qtype, E, k, None, None, None, E, None, stride, None, 0, None)
-    # a batch of 24 fp32 tokens, then 3 bf16 tokens, then 1 fp32 token: later calls need less
-    # scratch than the first and must not read what it left there
-    _compare_calls(cfg, pool, stride, [(24, 0), (3, 1), (1, 0)], seed=qtype + 7)
+    # a batch of T0 fp32 tokens (the largest that fits the array), then 3 bf16 tokens, then 1
+    # fp32 token: later calls need less scratch than the first and must not read what it left
+    _compare_calls(cfg, pool, stride, [(T0, 0), (3, 1), (1, 0)], seed=qtype + 7)
 
 
 def test_noalloc_prefill_path_then_decode():

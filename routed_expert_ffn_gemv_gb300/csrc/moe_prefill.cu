@@ -20,13 +20,19 @@
 //  * gather kernel: activations -> fp16 rows in position order (K permuted for 4-bit);
 //  * GEMM kernels: persistent, one CTA per SM over a strided list of work items, warp roles
 //    with mbarrier rings that run on across items:
-//      warp 0      per 64-column K stage: the chunk's token rows (2-D TMA boxes of 32 rows x
-//                  64 columns, 128-byte swizzle, straight into the UMMA layout) and the
-//                  slab's quantised tile blocks (4-D TMA box over the slot pool);
-//      warps 2-17  dequantise (row, 16 columns) each — integer codes to fp16 by exponent
-//                  tricks, then d*q [+ m] in one fp16 op (a single rounding) — and store
-//                  them into a 4-stage ring in TMEM (tcgen05.st, lane = weight row);
-//      warp 1      issues the MMAs into one of two 192-column TMEM accumulators;
+//      warp 0      per 64-column K stage the slab's quantised tile blocks (4-D TMA box over
+//                  the slot pool), and warp 22 the chunk's token rows (2-D TMA boxes of 64
+//                  rows x 64 columns, 128-byte swizzle, straight into the UMMA layout), both
+//                  completing the stage's one barrier;
+//      warps 2-17  four groups of four warps, group G taking the stages g = G mod 4: a thread
+//                  dequantises one weight row's 64 columns — integer codes to fp16 by
+//                  exponent tricks, then d*q [+ m] in one fp16 op (a single rounding) — and
+//                  stores them into its group's slot of a 4-stage ring in TMEM (tcgen05.st,
+//                  lane = weight row).  Every wait and hand-off costs a few hundred cycles
+//                  (measured), so each role keeps several stages in flight rather than
+//                  working through one stage at a time;
+//      warp 1      issues the MMAs into one of two 192-column TMEM accumulators once a
+//                  stage's weights are in TMEM (its group waited for the stage's copies);
 //      warps 18-21 the epilogue of the previous item from the other accumulator (lane =
 //                  weight row): GEMM 1 holds 64 gate rows in lanes 0-63 and the same 64 up
 //                  rows in 64-127; the up quarters pass their values through shared memory
@@ -54,12 +60,14 @@
 #define PF_NT 192          // most tokens of a chunk (MMA N)
 #define PF_WM 128          // weight rows of a work item (MMA M)
 #define PF_BK 64           // K columns per stage
-#define PF_BOX_ROWS 32     // token rows per TMA box
-#define PF_DQ_WARPS 16
+#define PF_BOX_ROWS 64     // token rows per TMA box
+#define PF_DQ_WARPS 16     // 4 groups of 4 (one warp per TMEM lane quarter)
 #define PF_EPI_WARPS 4
-#define PF_THREADS ((2 + PF_DQ_WARPS + PF_EPI_WARPS) * 32)
+#define PF_TOK_WARP (2 + PF_DQ_WARPS + PF_EPI_WARPS)  // the token producer
+#define PF_THREADS ((PF_TOK_WARP + 1) * 32)
 #define PF_S 6             // TMA ring stages (token rows + quantised weights)
-#define PF_AS 4            // TMEM ring stages of dequantised weights (32 columns each)
+#define PF_AS 4            // TMEM ring stages of dequantised weights (32 columns each), one per
+                           // dequant group
 #define PF_TMEM_COLS 512   // two accumulators of PF_NT columns, then the A ring
 #define PF_ACOL (2 * PF_NT)
 #define PF_CTRL 13312      // control block: barriers, epilogue exchange, route lists
@@ -130,6 +138,19 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+
+// Shared-memory counters with release / acquire semantics at CTA scope.
+__device__ __forceinline__ void red_release_add(unsigned *a, unsigned v) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(a)), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned *a) {
+    unsigned v;
+    asm volatile("ld.relaxed.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(a)) : "memory");
+    return v;
+}
+// With a relaxed load that observed a released value before it, makes the releasing thread's
+// earlier writes visible to this thread's later accesses.
+__device__ __forceinline__ void fence_acquire_cta() { asm volatile("fence.acq_rel.cta;" ::: "memory"); }
 
 // Named barrier over `count` threads.
 __device__ __forceinline__ void named_sync(int id, int count) {
@@ -387,10 +408,12 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 }
 
 // Wait for an mbarrier phase; gives up (returns false) when another role has aborted or,
-// after the spin limit, records MOE_ERR_TIMEOUT and aborts the CTA.
+// after the spin limit, records MOE_ERR_TIMEOUT and aborts the CTA.  It polls with the
+// non-blocking test (measured: a try_wait that suspends the thread adds hundreds of cycles
+// to every hand-off between the roles).
 __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int *status, volatile int *abort_flag) {
-    for (uint32_t i = 0; i < MOE_SPIN_LIMIT; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+    for (uint32_t i = 0; i < MOE_TEST_SPIN_LIMIT; ++i) {
+        if (mbar_test_wait(bar, parity)) return true;
         if (*abort_flag) return false;
     }
     moe_set_status(status, MOE_ERR_TIMEOUT);
@@ -424,13 +447,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
     uint8_t *smem = align1024(smem_raw);
     uint64_t *s_full = (uint64_t *)smem;
     uint64_t *s_empty = s_full + PF_S;
-    uint64_t *a_full = s_empty + PF_S;
-    uint64_t *a_empty = a_full + PF_AS;
+    uint64_t *a_empty = s_empty + PF_S;
     uint64_t *acc_full = a_empty + PF_AS;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *mma_done = acc_empty + 2;
     uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+    unsigned *a_cnt = (unsigned *)(smem + 512);  // per TMEM slot: dequant warps done (monotonic)
     float *xch = (float *)(smem + 1024);              // [2 pairs][2 slots][32 lanes][16] (GEMM 1)
     int *e_route = (int *)(smem + 1024 + 8192);       // [2 accumulators][PF_NT] (GEMM 2)
     float *e_w = (float *)(e_route + 2 * PF_NT);
@@ -440,12 +463,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
         for (int s = 0; s < PF_S; ++s) {
-            mbar_init(&s_full[s], 1);
+            mbar_init(&s_full[s], 2);  // the weight and the token producer
             mbar_init(&s_empty[s], 1);
         }
         for (int s = 0; s < PF_AS; ++s) {
-            mbar_init(&a_full[s], PF_DQ_WARPS);
             mbar_init(&a_empty[s], 1);
+            a_cnt[s] = 0;
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -464,10 +487,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ---------------- producer (lane 0): per K stage the chunk's token rows and the slab's
-        // quantised tile blocks
+    if (warp == 0 || warp == PF_TOK_WARP) {
+        // ---------------- producers (lane 0): per K stage the slab's quantised tile blocks
+        // (warp 0) or the chunk's token rows (the token warp)
         if (lane == 0) {
+            const bool tok = warp == PF_TOK_WARP;
             int g = 0;
             bool ok = true;
             for (int j = blockIdx.x; j < n_items && ok; j += gridDim.x) {
@@ -480,15 +504,19 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                     if (g >= PF_S && !(ok = pf_wait(&s_empty[s], ((g / PF_S) - 1) & 1, p.status, abort_flag)))
                         break;
                     uint8_t *st = ring + (size_t)s * PG::STAGE;
-                    mbar_arrive_expect_tx(&s_full[s], (uint32_t)(nbox * PF_BOX_ROWS * 128 + G::BYTES));
-                    for (int b = 0; b < nbox; ++b)
-                        tma_load_2d(st + b * PF_BOX_ROWS * 128, &p.tmap, kc * PF_BK, pos0 + PF_BOX_ROWS * b,
-                                    &s_full[s]);
-                    if (DOWN) {
-                        tma_load_4d(st + PG::TOKB, &p.wmap[2], 0, 2 * kc, 4 * m, slot, &s_full[s]);
+                    if (tok) {
+                        mbar_arrive_expect_tx(&s_full[s], (uint32_t)(nbox * PF_BOX_ROWS * 128));
+                        for (int b = 0; b < nbox; ++b)
+                            tma_load_2d(st + b * PF_BOX_ROWS * 128, &p.tmap, kc * PF_BK, pos0 + PF_BOX_ROWS * b,
+                                        &s_full[s]);
                     } else {
-                        tma_load_4d(st + PG::TOKB, &p.wmap[0], 0, 2 * kc, 2 * m, slot, &s_full[s]);
-                        tma_load_4d(st + PG::TOKB + 4 * G::TBB, &p.wmap[1], 0, 2 * kc, 2 * m, slot, &s_full[s]);
+                        mbar_arrive_expect_tx(&s_full[s], (uint32_t)G::BYTES);
+                        if (DOWN) {
+                            tma_load_4d(st + PG::TOKB, &p.wmap[2], 0, 2 * kc, 4 * m, slot, &s_full[s]);
+                        } else {
+                            tma_load_4d(st + PG::TOKB, &p.wmap[0], 0, 2 * kc, 2 * m, slot, &s_full[s]);
+                            tma_load_4d(st + PG::TOKB + 4 * G::TBB, &p.wmap[1], 0, 2 * kc, 2 * m, slot, &s_full[s]);
+                        }
                     }
                 }
             }
@@ -503,6 +531,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
         if (lane == 0) {
             int g = 0, jl = 0;
             bool ok = true;
+            unsigned seen = 0;  // the last value read of the next stage's dequant counter
             for (int j = blockIdx.x; j < n_items && ok; j += gridDim.x) {
                 const int c = j / MT;
                 if (p.c_slot[c] < 0) continue;
@@ -514,11 +543,32 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                 const uint32_t d = tmem + buf * PF_NT;
                 for (int kc = 0; kc < NK; ++kc, ++g) {
                     const int s = g % PF_S, sa = g % PF_AS;
-                    if (!(ok = pf_wait(&a_full[sa], (g / PF_AS) & 1, p.status, abort_flag))) break;
-                    if (!(ok = pf_wait(&s_full[s], (g / PF_S) & 1, p.status, abort_flag))) break;
+                    // the stage's weights are in TMEM once its dequant group's four warps counted
+                    // themselves in (release / acquire on a shared counter: an mbarrier wait costs
+                    // hundreds of cycles here, which would idle the tensor core); the group waited
+                    // for the stage's copies (tokens included) first, so they are visible too
+                    {
+                        const unsigned want = 4u * (unsigned)(g / PF_AS + 1);
+                        uint32_t i = 0;
+                        // `seen` was loaded (relaxed) before the previous stage's MMAs were issued,
+                        // so its latency is hidden behind them; reload only while it is short
+                        while (seen < want && (seen = ld_relaxed(&a_cnt[sa])) < want) {
+                            if (++i >= MOE_TEST_SPIN_LIMIT) {
+                                moe_set_status(p.status, MOE_ERR_TIMEOUT);
+                                *abort_flag = 1;
+                            }
+                            if (*abort_flag) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!ok) break;
+                    }
+                    fence_acquire_cta();  // the relaxed read saw the group's release
                     tc_fence_after();
                     const uint64_t b = umma_desc_sw128(smem_u32(ring + (size_t)s * PG::STAGE));
                     const uint32_t a = tmem + PF_ACOL + sa * 32;
+                    seen = ld_relaxed(&a_cnt[(g + 1) % PF_AS]);  // the next stage's count, early
 #pragma unroll
                     for (int kk = 0; kk < PF_BK / 16; ++kk)
                         umma_f16_tmem_a(d, a + 8 * kk, b + 2 * kk, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
@@ -533,31 +583,40 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
             mbar_wait_bounded(mma_done, 0, p.status);
         }
     } else if (warp < 2 + PF_DQ_WARPS) {
-        // ---------------- dequant: warp -> (TMEM lane quarter warp % 4 = raw row tile, 16-column
-        // quarter of the stage); thread -> one weight row
-        const int q = warp & 3, sub = (warp - 2) >> 2;
-        const int blk = sub >> 1, half = sub & 1;
-        const uint32_t a_lane = (uint32_t)(32 * q) << 16;
+        // ---------------- dequant: group dg = (warp - 2) / 4 takes the stages g = dg mod 4 and
+        // TMEM slot dg; warp -> TMEM lane quarter q = warp % 4 = raw row tile q; thread -> one
+        // weight row, all 64 columns of the stage
+        const int q = warp & 3, dg = (warp - 2) >> 2;
+        const uint32_t a_addr = tmem + ((uint32_t)(32 * q) << 16) + PF_ACOL + 32 * dg;
         int g = 0;
         bool ok = true;
         for (int j = blockIdx.x; j < n_items && ok; j += gridDim.x) {
             if (p.c_slot[j / MT] < 0) continue;
             for (int kc = 0; kc < NK; ++kc, ++g) {
-                const int s = g % PF_S, sa = g % PF_AS;
-                bool w = pf_wait(&s_full[s], (g / PF_S) & 1, p.status, abort_flag);
-                if (w && g >= PF_AS) w = pf_wait(&a_empty[sa], ((g / PF_AS) - 1) & 1, p.status, abort_flag);
-                if (!(ok = __all_sync(0xffffffffu, w))) break;  // the warp leaves together
+                if ((g & (PF_AS - 1)) != dg) continue;
+                const int s = g % PF_S;
+                bool w = true;
+                if (lane == 0) {
+                    w = pf_wait(&s_full[s], (g / PF_S) & 1, p.status, abort_flag);
+                    if (w && g >= PF_AS) w = pf_wait(&a_empty[dg], ((g / PF_AS) - 1) & 1, p.status, abort_flag);
+                }
+                w = __shfl_sync(0xffffffffu, w, 0);
+                __syncwarp();  // lane 0's acquire orders the other lanes' reads of the stage
+                if (!(ok = w)) break;  // the warp leaves together
                 tc_fence_after();
-                uint32_t o[8];
-                dequant16<QT>(ring + (size_t)s * PG::STAGE + PG::TOKB, q, blk, half, lane, o);
-                tmem_st8(tmem + a_lane + PF_ACOL + sa * 32 + 8 * sub, o);
+                uint32_t o[32];
+                const uint8_t *raw = ring + (size_t)s * PG::STAGE + PG::TOKB;
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                    dequant16<QT>(raw, q, h >> 1, h & 1, lane, *reinterpret_cast<uint32_t(*)[8]>(&o[8 * h]));
+                tmem_st32(a_addr, o);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[sa]);
+                if (lane == 0) red_release_add(&a_cnt[dg], 1);
             }
         }
-    } else {
+    } else if (warp < PF_TOK_WARP) {
         // ---------------- epilogue: TMEM lane quarter q = warp % 4, lane = weight row 32 q + lane
         const int q = warp & 3, ew = warp - 2 - PF_DQ_WARPS;
         int jl = 0, xs = 0;  // items done, exchange chunks done (slot parity)
@@ -573,9 +632,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                     e_route[buf * PF_NT + i] = r;
                     e_w[buf * PF_NT + i] = p.weights[r];
                 }
-            bool w = pf_wait(&acc_full[buf], (jl / 2) & 1, p.status, abort_flag);
-            w = __all_sync(0xffffffffu, w);
-            // the four epilogue warps agree (and the route lists are written) before going on
+            const bool w = ew == 0 && lane == 0 ? pf_wait(&acc_full[buf], (jl / 2) & 1, p.status, abort_flag) : true;
+            // one thread waited; the four epilogue warps agree (and the route lists are written)
+            // before going on
             if (!(ok = named_sync_and(1, 32 * PF_EPI_WARPS, w))) break;
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(32 * q) << 16) + buf * PF_NT;
@@ -585,34 +644,52 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                 tmem_ld_wait();
                 const int nn = min(16, n - c0);
                 if (!DOWN) {
-                    // up quarters (2, 3) hand their values to the gate quarters (0, 1)
-                    float *xb = xch + ((size_t)((q & 1) * 2 + (xs & 1)) * 32 + lane) * 16;
+                    // up quarters (2, 3) hand their values to the gate quarters (0, 1); column i of
+                    // lane l at xb[32 i + l] (no bank conflicts)
+                    float *xb = xch + (size_t)((q & 1) * 2 + (xs & 1)) * 512 + lane;
                     if (q >= 2)
 #pragma unroll
-                        for (int i = 0; i < 16; i += 4)
-                            *(float4 *)(xb + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                                              __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                        for (int i = 0; i < 16; ++i) xb[32 * i] = __uint_as_float(v[i]);
                     named_sync(2 + (q & 1), 64);
                     if (q < 2) {
                         const int f = 64 * m + 32 * q + lane;
                         const int fp = QT == MOE_Q4_SM ? (f & ~7) + (f & 3) * 2 + ((f >> 2) & 1) : f;
                         __half *dst = p.hg + (size_t)(pos0 + c0) * p.F + fp;
+                        // every shared-memory load first (one round trip), then all 16 values
+                        // computed side by side (no per-column branch: 16 independent chains), then
+                        // the stores
+                        __half hv[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            if (i < nn) {
-                                const float gv = __uint_as_float(v[i]), uv = xb[i];
-                                dst[(size_t)i * p.F] = __float2half_rn(gv / (1.0f + __expf(-gv)) * uv);
-                            }
+                            const float gv = __uint_as_float(v[i]);
+                            hv[i] = __float2half_rn(__fdividef(gv, 1.0f + __expf(-gv)) * xb[32 * i]);
+                        }
+                        if (nn == 16) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) dst[(size_t)i * p.F] = hv[i];
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (i < nn) dst[(size_t)i * p.F] = hv[i];
                         }
                     }
                 } else {
                     const int hr = PF_WM * m + 32 * q + lane;
+                    // every shared-memory load first (one round trip), then the stores
+                    int rt[16];
+                    float wt[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        if (i < nn) {
-                            const int t = buf * PF_NT + c0 + i;
-                            p.partial[(size_t)e_route[t] * p.H + hr] = e_w[t] * __uint_as_float(v[i]);
-                        }
+                        rt[i] = e_route[buf * PF_NT + c0 + i];
+                        wt[i] = e_w[buf * PF_NT + c0 + i];
+                    }
+                    if (nn == 16) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) p.partial[(size_t)rt[i] * p.H + hr] = wt[i] * __uint_as_float(v[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (i < nn) p.partial[(size_t)rt[i] * p.H + hr] = wt[i] * __uint_as_float(v[i]);
                     }
                 }
             }

@@ -101,6 +101,20 @@ int moe_router_topk(const void *x, int xtype, int T, int H, const uint16_t *w_ro
                     const float *bias, int E, int k, int32_t *ids, float *weights,
                     float *logits, moe_stream_t s);
 
+/*
+ * moe_router_topk_threshold — moe_router_topk with the load threshold of page 1 (section
+ * 4.3, --moe-expert-load-threshold 0.05: a selected expert whose gate score is below the
+ * threshold is not loaded).  Reading: a route (t, j) whose weight (the softmax over the k
+ * selected logits) is below min_weight is dropped: ids[t][j] = -1 and weights[t][j] = 0;
+ * the other routes keep their weights (no renormalisation), so the layer's output loses
+ * those terms (this variant changes the result).  Every other entry point treats id -1 as
+ * "no route": it is skipped, not an error; moe_expert_ffn leaves partial[t][j] of such a
+ * route untouched (the stack's combine skips it).  min_weight in [0, 1]; 0 drops nothing.
+ */
+int moe_router_topk_threshold(const void *x, int xtype, int T, int H, const uint16_t *w_router,
+                              const float *bias, int E, int k, float min_weight, int32_t *ids,
+                              float *weights, float *logits, moe_stream_t s);
+
 /* ------------------------------------------------------------------ slot images */
 
 /*
@@ -152,6 +166,20 @@ typedef struct {
     void *device_state;               /* device_managed: moe_cache_state_bytes() bytes of device
                                          memory, caller-owned, initialised by moe_cache_create */
     size_t device_state_bytes;
+    /* Policy variants (0 = off: plain LRU).
+     * admit_after: frequency admission (page 3, section "2.2 第二层专家缓存层": experts are
+     *   moved into VRAM once their access count passes a threshold).  Every request counts
+     *   one access per distinct (layer, expert); a miss whose count, this access included,
+     *   is below admit_after takes no slot and changes no LRU state ("bypassed": its slot
+     *   is reported as -1 and its weights are read from its pinned host image, see
+     *   moe_expert_ffn_fill); it still counts as a miss.  Values 0 and 1 mean plain LRU.
+     * lru_window: W tokens (page 1, section 4.3, --moe-lru-window: an expert not used within
+     *   the last W tokens is unloaded).  The pool's token clock advances by the ubatch's
+     *   token count at every request for the group's first layer; before each request every
+     *   slot whose last use is more than W tokens behind the clock is freed.  Host-managed
+     *   pools only (MOE_ERR_UNSUPPORTED at create for a device-managed pool). */
+    int admit_after;
+    int lru_window;
 } moe_cache_desc;
 
 typedef struct moe_cache moe_cache; /* opaque, library-owned host object */
@@ -165,6 +193,8 @@ typedef struct {
     uint64_t route_queries;   /* per-route (token, expert) lookups */
     uint64_t route_hits;
     uint64_t ensure_calls;
+    uint64_t bypassed;        /* misses served from host memory without a slot (admit_after) */
+    uint64_t window_evictions;/* slots freed by the LRU window */
 } moe_cache_stats;
 
 /*
@@ -181,10 +211,11 @@ int moe_cache_create(const moe_cache_desc *desc, moe_cache **out);
  * expert is not in this request (page 1 section 3.2; page 4).  Each miss is an
  * async cudaMemcpyAsync of the pinned image into its slot on desc.copy_stream,
  * issued after the slot's last reader (see moe_cache_release) has finished.
- * Outputs: slots_host_out [n_tokens*k] (the slot of each input id), *n_miss_out,
- * miss_mask_host_out (optional, [n_experts] bytes: 1 for experts uploaded by this
- * call, 0 otherwise), and the layer's device expert->slot table d_slot_table
- * [n_experts] (-1 for non-resident experts), written on stream s.
+ * Outputs: slots_host_out [n_tokens*k] (the slot of each input id; -1 for an expert the
+ * admission policy bypassed), *n_miss_out (uploads issued), miss_mask_host_out (optional,
+ * [n_experts] bytes: 1 for experts uploaded by this call, 0 otherwise), and the layer's
+ * device expert->slot table d_slot_table [n_experts] (-1 for non-resident experts),
+ * written on stream s.
  * Errors: MOE_ERR_CAPACITY when distinct ids > n_slots (nothing changes);
  * MOE_ERR_INVALID for a layer outside the group or an id outside [0, E);
  * MOE_ERR_CUDA if an upload could not be issued (the slot being filled is left
@@ -209,7 +240,8 @@ int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host, int n_tok
  *   d_fill_src_out [n_experts] for each expert that missed, the address of its pinned
  *                  host image (the slot it was given must be filled from there), else 0.
  * It moves no weight bytes: moe_expert_ffn_fill reads the missed experts from host memory
- * and writes them into their slots while computing.  Capacity overflow or an id out of
+ * and writes them into their slots while computing (an expert bypassed by the admission
+ * policy gets table -1 and its image address: read from host memory, written nowhere).  Capacity overflow or an id out of
  * range is recorded in the device status word (moe_device_status); the layer's table is
  * then all -1 and nothing is read.  Host-side ensure/wait/release are invalid on a
  * device-managed pool; moe_cache_stats_get, moe_cache_lookup and moe_cache_reset work on
@@ -277,8 +309,9 @@ int moe_expert_ffn(const void *x, int xtype, int T, int H, int F, int qtype, int
  * each expert e with d_fill_src[e] != 0 (set by moe_cache_plan for the experts that
  * missed) has its weights read from that pinned host image over the CPU-GPU link and
  * written into its slot (d_slot_table[e]) by the same kernels that compute with them,
- * so the upload and the compute overlap and no copy engine is involved; other experts
- * are read from their slots.  Decode path only (T <= MOE_DECODE_MAX_T or fp32 x);
+ * so the upload and the compute overlap and no copy engine is involved; with
+ * d_slot_table[e] == -1 the image is only read (an expert the admission policy bypassed);
+ * other experts are read from their slots.  Decode path only (T <= MOE_DECODE_MAX_T or fp32 x);
  * otherwise MOE_ERR_UNSUPPORTED.  The pool must be the one the plan was made for.
  */
 int moe_expert_ffn_fill(const void *x, int xtype, int T, int H, int F, int qtype, int E, int k,
@@ -383,6 +416,9 @@ typedef struct {
                                          captures the whole step once per batch size into a
                                          CUDA graph and replays it (inputs/outputs copied in
                                          and out) */
+    float load_threshold;             /* 0: off; else routes below it are dropped before the
+                                         pools see them (moe_router_topk_threshold; this
+                                         changes the layer's output) */
 } moe_stack_desc;
 
 typedef struct moe_stack moe_stack;

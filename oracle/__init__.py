@@ -173,17 +173,26 @@ class LayerResult:
 def moe_layer(qtype: int, H: int, F: int, k: int, x: np.ndarray, w_router_bits: np.ndarray,
               bias: Optional[np.ndarray], experts: ExpertFn,
               shared: Sequence[Tuple[np.ndarray, np.ndarray, np.ndarray]] = (),
-              route_override: Optional[Tuple[np.ndarray, np.ndarray]] = None) -> LayerResult:
+              route_override: Optional[Tuple[np.ndarray, np.ndarray]] = None,
+              load_threshold: float = 0.0) -> LayerResult:
     """One MoE FFN layer, in the method's order.
 
     x: [T][H] fp64 (exact input values).  ``experts(e)`` returns expert e's canonical
     (gate, up, down) blocks.  ``route_override`` = (ids, weights) replaces the oracle's
-    own routing (used to check outputs on near-tie tokens with a given route).
+    own routing (used to check outputs on near-tie tokens with a given route); an id of -1
+    there is a dropped route.  ``load_threshold`` (page 1, "MoE 模型卸载" blog, section 4.3:
+    experts whose gate score is below the threshold are not loaded): a selected route whose
+    softmax weight is below it is dropped — not computed, its term left out of the sum,
+    the other weights unchanged; its id becomes -1 and its weight 0 in the result.
     """
     xd = np.ascontiguousarray(x, dtype=np.float64)
     T = xd.shape[0]
     logits = router_logits(xd, w_router_bits, bias)
     ids, w, gap = topk_softmax(logits, k)
+    if load_threshold > 0.0:
+        drop = w < load_threshold
+        ids = np.where(drop, -1, ids).astype(np.int32)
+        w = np.where(drop, 0.0, w)
     if route_override is not None:
         ids = np.asarray(route_override[0], dtype=np.int32)
         w = np.asarray(route_override[1], dtype=np.float64)
@@ -193,12 +202,15 @@ def moe_layer(qtype: int, H: int, F: int, k: int, x: np.ndarray, w_router_bits: 
     for t in range(T):
         for j in range(k):
             e = int(ids[t, j])
+            if e < 0:
+                continue  # a dropped route
             if e not in cache:
                 cache[e] = experts(e)
             gt, ut, dt = cache[e]
             y_exp[t, j] = expert_ffn(qtype, H, F, gt, ut, dt, xd[t])
         for j in range(k):
-            y[t] += w[t, j] * y_exp[t, j]
+            if ids[t, j] >= 0:
+                y[t] += w[t, j] * y_exp[t, j]
         for (gs, us, ds) in shared:
             y[t] += expert_ffn(qtype, H, F, gs, us, ds, xd[t])
     return LayerResult(logits, ids, w, gap, y_exp, y)

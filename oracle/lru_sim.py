@@ -14,6 +14,19 @@ Rules, per ``ensure(layer, ids)`` on one group:
      slot with the smallest stamp whose owner is not in this request; the new
      owner is stamped with ++clock.
 One query is counted per distinct (layer, expert) per call.
+
+Policy variants (each off by default; with both off the rules above are unchanged):
+  * admit_after = theta (frequency admission; page 3, section "2.2 第二层专家缓存层": count
+    each expert's accesses and move it into VRAM once the count passes a threshold):
+    every request counts one access per distinct (layer, expert); a miss whose count,
+    this access included, is below theta is "bypassed" — served from host memory, no slot,
+    no LRU change — and still counted as a miss; from theta on it is admitted by rule 4.
+    theta = 1 is plain LRU.  The capacity check counts hits plus admitted misses only.
+  * window = W tokens (page 1, section "4.3 运行时配置bat脚本里的魔鬼参数": an expert not
+    used within the last W tokens is unloaded): the pool keeps a token clock, advanced by
+    the ubatch's token count at every request of the group's first layer; before a
+    request, every slot whose last use is more than W tokens behind the clock is freed
+    (its expert becomes non-resident), then rules 1-4 apply.
 """
 from __future__ import annotations
 
@@ -25,33 +38,66 @@ class CapacityError(Exception):
 
 
 class LRUSim:
-    def __init__(self, n_slots: int):
+    def __init__(self, n_slots: int, admit_after: int = 1, window: int = 0, first_layer: int = 0):
         if n_slots <= 0:
             raise ValueError("n_slots must be positive")
+        if admit_after < 1 or window < 0:
+            raise ValueError("admit_after >= 1 and window >= 0")
         self.n_slots = n_slots
+        self.admit_after = admit_after
+        self.window = window
+        self.first_layer = first_layer
         self.owner: List[Optional[Tuple[int, int]]] = [None] * n_slots
         self.stamp: List[int] = [0] * n_slots
+        self.last_tok: List[int] = [0] * n_slots
         self.where: Dict[Tuple[int, int], int] = {}
+        self.count: Dict[Tuple[int, int], int] = {}
         self.clock = 0
+        self.tok = 0
         self.hits = 0
         self.misses = 0
         self.evictions = 0
+        self.bypassed = 0
+        self.window_evictions = 0
 
-    def ensure(self, layer: int, ids: Iterable[int]) -> Tuple[Dict[int, int], List[int], List[int]]:
-        """Returns ({expert: slot}, hit ids, miss ids) for one request."""
+    def ensure(self, layer: int, ids: Iterable[int], n_tokens: int = 1
+               ) -> Tuple[Dict[int, int], List[int], List[int]]:
+        """Returns ({expert: slot, -1 if bypassed}, hit ids, miss ids) for one request."""
         req = sorted(set(int(e) for e in ids))
-        if len(req) > self.n_slots:
-            raise CapacityError(f"{len(req)} distinct experts > {self.n_slots} slots")
+        if layer == self.first_layer:
+            tok = self.tok + n_tokens
+        else:
+            tok = self.tok
         keys = {(layer, e) for e in req}
+        # the window: slots unused for more than W tokens are freed first
+        stale = []
+        if self.window > 0:
+            stale = [s for s in range(self.n_slots)
+                     if self.owner[s] is not None and tok - self.last_tok[s] > self.window]
+        resident = lambda e: (layer, e) in self.where and self.where[(layer, e)] not in stale
+        hit_ids = [e for e in req if resident(e)]
+        miss_ids = [e for e in req if not resident(e)]
+        counts = {e: self.count.get((layer, e), 0) + 1 for e in req}
+        admitted = [e for e in miss_ids if counts[e] >= self.admit_after]
+        bypass = [e for e in miss_ids if counts[e] < self.admit_after]
+        if len(hit_ids) + len(admitted) > self.n_slots:
+            raise CapacityError(f"{len(hit_ids) + len(admitted)} experts need slots > {self.n_slots} slots")
+        # commit
+        self.tok = tok
+        for s in stale:
+            del self.where[self.owner[s]]
+            self.owner[s] = None
+            self.window_evictions += 1
+        for e in req:
+            self.count[(layer, e)] = counts[e]
         result: Dict[int, int] = {}
-        hit_ids = [e for e in req if (layer, e) in self.where]
-        miss_ids = [e for e in req if (layer, e) not in self.where]
         for e in hit_ids:
             s = self.where[(layer, e)]
             self.clock += 1
             self.stamp[s] = self.clock
+            self.last_tok[s] = tok
             result[e] = s
-        for e in miss_ids:
+        for e in admitted:
             free = [s for s in range(self.n_slots) if self.owner[s] is None]
             if free:
                 s = free[0]
@@ -64,9 +110,13 @@ class LRUSim:
             self.where[(layer, e)] = s
             self.clock += 1
             self.stamp[s] = self.clock
+            self.last_tok[s] = tok
             result[e] = s
+        for e in bypass:
+            result[e] = -1
         self.hits += len(hit_ids)
         self.misses += len(miss_ids)
+        self.bypassed += len(bypass)
         return result, hit_ids, miss_ids
 
 

@@ -39,7 +39,7 @@ EXPORTED = [
     "moe_stack_destroy", "moe_debug_inject_fault", "moe_stack_set_profile", "moe_stack_gemv_timing",
     "moe_set_decode_fused", "moe_get_decode_fused",
     "moe_expert_ffn_noalloc", "moe_combine_rmsnorm", "moe_cache_state_bytes", "moe_cache_plan",
-    "moe_expert_ffn_fill", "moe_last_cuda_error",
+    "moe_expert_ffn_fill", "moe_last_cuda_error", "moe_router_topk_threshold",
 ]
 MOE_NOALLOC_SCRATCH_MAX = 8 << 20
 
@@ -60,20 +60,23 @@ class CacheDesc(ctypes.Structure):
     _fields_ = [("qtype", _i), ("H", _i), ("F", _i), ("n_layers", _i), ("n_experts", _i),
                 ("first_layer", _i), ("n_slots", _i), ("slot_bytes", _sz), ("device_pool", _vp),
                 ("host_images", ctypes.POINTER(_vp)), ("copy_stream", _vp), ("device_managed", _i),
-                ("device_state", _vp), ("device_state_bytes", _sz)]
+                ("device_state", _vp), ("device_state_bytes", _sz), ("admit_after", _i),
+                ("lru_window", _i)]
 
 
 class CacheStats(ctypes.Structure):
     _fields_ = [("queries", ctypes.c_uint64 * 2), ("hits", ctypes.c_uint64 * 2),
                 ("misses", ctypes.c_uint64 * 2), ("evictions", ctypes.c_uint64),
                 ("h2d_bytes", ctypes.c_uint64), ("route_queries", ctypes.c_uint64),
-                ("route_hits", ctypes.c_uint64), ("ensure_calls", ctypes.c_uint64)]
+                ("route_hits", ctypes.c_uint64), ("ensure_calls", ctypes.c_uint64),
+                ("bypassed", ctypes.c_uint64), ("window_evictions", ctypes.c_uint64)]
 
     def as_dict(self):
         return {"queries": list(self.queries), "hits": list(self.hits), "misses": list(self.misses),
                 "evictions": self.evictions, "h2d_bytes": self.h2d_bytes,
                 "route_queries": self.route_queries, "route_hits": self.route_hits,
-                "ensure_calls": self.ensure_calls}
+                "ensure_calls": self.ensure_calls, "bypassed": self.bypassed,
+                "window_evictions": self.window_evictions}
 
 
 class StackDesc(ctypes.Structure):
@@ -82,7 +85,7 @@ class StackDesc(ctypes.Structure):
                 ("n_groups", _i), ("caches", ctypes.POINTER(_vp)), ("resident_pool", _vp),
                 ("shared_pool", _vp), ("slot_bytes", _sz), ("max_T", _i), ("workspace", _vp),
                 ("ws_bytes", _sz), ("overlap", _i), ("profile", _i), ("device_managed", _i),
-                ("use_graph", _i)]
+                ("use_graph", _i), ("load_threshold", ctypes.c_float)]
 
 
 class StackProfile(ctypes.Structure):
@@ -126,6 +129,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_status_string": ([_i], ctypes.c_char_p),
         "moe_last_cuda_error": ([], ctypes.c_char_p),
         "moe_router_topk": ([_vp, _i, _i, _i, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp], _i),
+        "moe_router_topk_threshold": ([_vp, _i, _i, _i, _vp, _vp, _i, _i, ctypes.c_float, _vp, _vp, _vp, _vp], _i),
         "moe_slot_image_bytes": ([_i, _i, _i, P(_sz)], _i),
         "moe_pack_expert": ([_i, _i, _i, _vp, _vp, _vp, _vp, P(_sz)], _i),
         "moe_unpack_expert": ([_i, _i, _i, _vp, _vp, _vp, _vp], _i),
@@ -204,6 +208,13 @@ def moe_router_topk(x, xtype: int, T: int, H: int, w_router, bias, E: int, k: in
                     logits=None, stream=None) -> None:
     _ck("moe_router_topk", load().moe_router_topk(_ptr(x), xtype, T, H, _ptr(w_router), _ptr(bias), E, k,
                                                   _ptr(ids), _ptr(weights), _ptr(logits), _stream(stream)))
+
+
+def moe_router_topk_threshold(x, xtype: int, T: int, H: int, w_router, bias, E: int, k: int, min_weight: float,
+                              ids, weights, logits=None, stream=None) -> None:
+    _ck("moe_router_topk_threshold",
+        load().moe_router_topk_threshold(_ptr(x), xtype, T, H, _ptr(w_router), _ptr(bias), E, k, float(min_weight),
+                                         _ptr(ids), _ptr(weights), _ptr(logits), _stream(stream)))
 
 
 def moe_slot_image_bytes(qtype: int, H: int, F: int) -> int:

@@ -38,6 +38,9 @@ struct moe_cache {
     bool upload_pending = false;
     std::vector<int> last_slots;      // slots of the last ensure (for release)
     moe_cache_stats st{};
+    std::vector<uint32_t> count;      // [n_layers * E] accesses (admission policy)
+    std::vector<uint64_t> last_tok;   // [n_slots] token clock at the last use (window policy)
+    uint64_t tok = 0;                 // the pool's token clock
 };
 
 struct IntPayload {
@@ -66,6 +69,9 @@ void reset_state(moe_cache *c) {
     c->upload_pending = false;
     c->last_slots.clear();
     c->st = moe_cache_stats{};
+    std::fill(c->count.begin(), c->count.end(), 0u);
+    std::fill(c->last_tok.begin(), c->last_tok.end(), 0ull);
+    c->tok = 0;
 }
 
 // ------------------------------------------------------------------ device-managed state
@@ -80,10 +86,12 @@ void reset_state(moe_cache *c) {
 struct DevHeader {
     int32_t n_filled, head, tail, pad;
     uint64_t queries[2], hits[2], misses[2], evictions, h2d_bytes, route_queries, route_hits, ensure_calls;
+    uint64_t bypassed, window_evictions;
 };
+static_assert(sizeof(DevHeader) <= 256, "device header");
 
 struct DevLayout {
-    size_t slot_of, owner, prev, next, img, total;
+    size_t slot_of, owner, prev, next, img, count, total;
 };
 
 DevLayout dev_layout(int n_layers, int E, int n_slots) {
@@ -95,6 +103,7 @@ DevLayout dev_layout(int n_layers, int E, int n_slots) {
     L.prev = o;    o += ((size_t)n_slots * 4 + 15) / 16 * 16;
     L.next = o;    o += ((size_t)n_slots * 4 + 15) / 16 * 16;
     L.img = o;     o += nk * 8;
+    L.count = o;   o += (nk * 4 + 15) / 16 * 16;
     L.total = (o + 255) / 256 * 256;
     return L;
 }
@@ -103,13 +112,15 @@ DevLayout dev_layout(int n_layers, int E, int n_slots) {
 
 __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, DevLayout L, int ll, int E,
                                                    int n_slots, const int32_t *__restrict__ ids, int n_tokens,
-                                                   int k, uint64_t image_bytes, int32_t *__restrict__ table_out,
+                                                   int k, uint64_t image_bytes, int theta,
+                                                   int32_t *__restrict__ table_out,
                                                    uint64_t *__restrict__ src_out, int *status) {
     // Everything is read once into shared memory (one round of loads), the list is updated
     // there in parallel (one short walk from the head by one thread) and stored once.
     extern __shared__ int32_t sm[];
     int32_t *owner = sm, *prev = sm + n_slots, *next = sm + 2 * n_slots, *slot_l = sm + 3 * n_slots;
-    unsigned char *want = (unsigned char *)(slot_l + E), *miss = want + E;
+    uint32_t *cnt_l = (uint32_t *)(slot_l + E);  // accesses of the layer's experts (admission)
+    unsigned char *want = (unsigned char *)(cnt_l + E), *miss = want + E;
     __shared__ int abort_flag, route_hits, commit, s_head, s_tail;
     __shared__ int wsum[8];
     __shared__ int32_t vict[MOE_MAX_E], app[MOE_MAX_E];
@@ -123,6 +134,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     int32_t *g_prev = (int32_t *)(state + L.prev);
     int32_t *g_next = (int32_t *)(state + L.next);
     const uint64_t *g_img = (const uint64_t *)(state + L.img);
+    uint32_t *g_count = (uint32_t *)(state + L.count);
     const int key0 = ll * E, n_ids = n_tokens * k;
     const int n_keys = (int)((L.owner - L.slot_of) / 4);  // entries the slot_of region holds
     pdl_wait();  // ids and the pool state come from earlier kernels
@@ -135,6 +147,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         slot_l[e] = g_slot_of[key0 + e];
         s_img[e] = g_img[key0 + e];
+        cnt_l[e] = g_count[key0 + e];
         want[e] = 0;
         miss[e] = 0;
     }
@@ -150,6 +163,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     __syncthreads();
     for (int i = threadIdx.x; i < n_ids; i += blockDim.x) {
         const int e = s_ids[i];
+        if (e == -1) continue;  // a route dropped by the load threshold
         if (e < 0 || e >= E) {
             moe_set_status(status, MOE_ERR_INVALID);
             abort_flag = 1;
@@ -161,8 +175,16 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     // ---- the request: distinct experts, hits (resident) and misses, ranked by ascending id
     const int e_t = threadIdx.x;  // one expert per thread (E <= MOE_MAX_E = blockDim.x)
     const bool w_t = e_t < E && want[e_t];
-    const bool hit_t = w_t && slot_l[e_t] >= 0, miss_t = w_t && slot_l[e_t] < 0;
-    const int nd = __syncthreads_count(w_t);
+    const bool hit_t = w_t && slot_l[e_t] >= 0;
+    // a miss takes a slot once the expert's accesses (this one included) reach theta; before
+    // that it is bypassed: read from its host image, no slot, no LRU change
+    const uint32_t c_t = e_t < E ? cnt_l[e_t] + (w_t ? 1u : 0u) : 0u;
+    const bool miss_any = w_t && slot_l[e_t] < 0;
+    const bool miss_t = miss_any && c_t >= (uint32_t)theta, byp_t = miss_any && !miss_t;
+    const int nd = __syncthreads_count(hit_t || miss_t);  // experts that need a slot
+    int n_real = 0;  // routes that are not dropped
+    for (int i = 0; i < n_ids; ++i) n_real += s_ids[i] != -1;
+    const int nbyp = __syncthreads_count(byp_t);
     int rh = 0, rm = 0, nh = 0, nm = 0;  // this expert's rank among the hits / misses; counts
     {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -287,6 +309,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
                 slot_l[e_t] = ms;
                 miss[e_t] = 1;
             }
+            if (byp_t) miss[e_t] = 1;
             if (threadIdx.x == 0) {
                 if (na > 0) {
                     if (old_tail >= 0) next[old_tail] = app[0];
@@ -298,12 +321,13 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
                 s_hd.tail = s_tail;
                 s_hd.n_filled = min(n_slots, filled + nm);
                 const int b = n_tokens <= 8 ? 0 : 1;
-                s_hd.queries[b] += nh + nm;
+                s_hd.queries[b] += nh + nm + nbyp;
                 s_hd.hits[b] += nh;
-                s_hd.misses[b] += nm;
+                s_hd.misses[b] += nm + nbyp;
                 s_hd.evictions += m_evict;
-                s_hd.h2d_bytes += (uint64_t)nm * image_bytes;
-                s_hd.route_queries += n_ids;
+                s_hd.bypassed += nbyp;
+                s_hd.h2d_bytes += (uint64_t)(nm + nbyp) * image_bytes;  // read from host memory
+                s_hd.route_queries += n_real;
                 s_hd.ensure_calls += 1;
             }
         }
@@ -311,7 +335,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     __syncthreads();
     if (commit) {  // routes whose expert was resident before this call (every id is valid here)
         int h = 0;
-        for (int i = threadIdx.x; i < n_ids; i += blockDim.x) h += !miss[s_ids[i]];
+        for (int i = threadIdx.x; i < n_ids; i += blockDim.x) h += s_ids[i] >= 0 && !miss[s_ids[i]];
         if (h) atomicAdd(&route_hits, h);
         __syncthreads();
         if (threadIdx.x == 0) s_hd.route_hits += route_hits;
@@ -325,9 +349,12 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
         }
     }
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        if (commit) g_slot_of[key0 + e] = slot_l[e];
+        if (commit) {
+            g_slot_of[key0 + e] = slot_l[e];
+            if (want[e]) g_count[key0 + e] = cnt_l[e] + 1u;
+        }
         table_out[e] = commit ? slot_l[e] : -1;
-        src_out[e] = (commit && miss[e]) ? s_img[e] : 0ull;
+        src_out[e] = (commit && miss[e]) ? s_img[e] : 0ull;  // admitted misses and bypassed
     }
 }
 
@@ -369,7 +396,7 @@ extern "C" int moe_cache_plan(moe_cache *c, int layer, const int32_t *d_ids, int
     const DevLayout L = dev_layout(d.n_layers, d.n_experts, d.n_slots);
     // owner, prev, next (int32 per slot), the layer's slots (int32 per expert), want and miss
     // (a byte per expert), the hit marks (a byte per slot)
-    auto plan_smem = [](int n_slots, int E) { return (size_t)n_slots * 13 + (size_t)E * 6; };
+    auto plan_smem = [](int n_slots, int E) { return (size_t)n_slots * 13 + (size_t)E * 10; };
     const size_t smem = plan_smem(d.n_slots, d.n_experts);
     {
         // the attribute belongs to the kernel on one device: set once per device
@@ -389,8 +416,8 @@ extern "C" int moe_cache_plan(moe_cache *c, int layer, const int32_t *d_ids, int
     cudaLaunchAttribute attr[1];
     moe_pdl_config(&cfg, attr, dim3(1), dim3(256), smem, moe_cuda_stream(s));
     MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, plan_kernel, (uint8_t *)d.device_state, L, ll, d.n_experts, d.n_slots,
-                                    d_ids, n_tokens, k, c->image_bytes, d_table_out, d_fill_src_out,
-                                    moe_status_word_device_ptr()));
+                                    d_ids, n_tokens, k, c->image_bytes, std::max(1, d.admit_after), d_table_out,
+                                    d_fill_src_out, moe_status_word_device_ptr()));
     MOE_TRY_CUDA(cudaGetLastError());
     return MOE_OK;
 }
@@ -414,6 +441,8 @@ extern "C" int moe_cache_create(const moe_cache_desc *desc, moe_cache **out) {
     MOE_CHECK(d.H > 0 && d.F > 0 && d.H % 32 == 0 && d.F % 32 == 0);
     MOE_CHECK(d.n_layers >= 1 && d.n_experts >= 1 && d.n_experts <= MOE_MAX_E && d.first_layer >= 0);
     MOE_CHECK(d.n_slots >= 1);
+    MOE_CHECK(d.admit_after >= 0 && d.lru_window >= 0);
+    if (d.device_managed && d.lru_window > 0) return MOE_ERR_UNSUPPORTED;
     const size_t img = moe_expert_image_bytes(d.qtype, d.H, d.F);
     MOE_CHECK(d.slot_bytes >= img && d.slot_bytes % 256 == 0);
     MOE_CHECK(d.device_pool && ((uintptr_t)d.device_pool % 256) == 0);
@@ -450,6 +479,8 @@ extern "C" int moe_cache_create(const moe_cache_desc *desc, moe_cache **out) {
     c->owner.assign(d.n_slots, -1);
     c->stamp.assign(d.n_slots, 0);
     c->last_use.assign(d.n_slots, -1);
+    c->count.assign(n_img, 0u);
+    c->last_tok.assign(d.n_slots, 0ull);
     for (int i = 0; i < MOE_EVENT_RING; ++i) {
         if (cudaEventCreateWithFlags(&c->ring[i], cudaEventDisableTiming) != cudaSuccess) {
             moe_cache_destroy(c);
@@ -479,24 +510,53 @@ extern "C" int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host
     bool want[MOE_MAX_E] = {false};
     for (int i = 0; i < n_ids; ++i) {
         const int e = ids_host[i];
+        if (e == -1) continue;  // a route dropped by the load threshold
         MOE_CHECK(e >= 0 && e < E);
         want[e] = true;
     }
     int n_distinct = 0;
     for (int e = 0; e < E; ++e) n_distinct += want[e];
-    if (n_distinct > d.n_slots) return MOE_ERR_CAPACITY;
 
     const int64_t key0 = (int64_t)ll * E;
-    bool hit[MOE_MAX_E] = {false};
-    // 1. hits, ascending id: most recent
+    // the window: the token clock advances at the group's first layer; slots unused for more
+    // than lru_window tokens are freed before the request (their experts miss)
+    const uint64_t tok = c->tok + (layer == d.first_layer ? (uint64_t)n_tokens : 0ull);
+    std::vector<int> stale;
+    if (d.lru_window > 0)
+        for (int sl = 0; sl < d.n_slots; ++sl)
+            if (c->owner[sl] >= 0 && tok - c->last_tok[sl] > (uint64_t)d.lru_window) stale.push_back(sl);
+    auto is_stale = [&](int sl) { return std::binary_search(stale.begin(), stale.end(), sl); };
+    // admission: a miss takes a slot once its accesses (this one included) reach admit_after
+    const uint32_t theta = (uint32_t)std::max(1, d.admit_after);
+    bool hit[MOE_MAX_E] = {false}, bypass[MOE_MAX_E] = {false};
+    int n_need = 0, n_bypass = 0;
     for (int e = 0; e < E; ++e) {
         if (!want[e]) continue;
         const int sl = c->slot_of[key0 + e];
-        if (sl < 0) continue;
-        hit[e] = true;
+        hit[e] = sl >= 0 && !is_stale(sl);
+        bypass[e] = !hit[e] && c->count[key0 + e] + 1 < theta;
+        n_need += !bypass[e];
+        n_bypass += bypass[e];
+    }
+    if (n_need > d.n_slots) return MOE_ERR_CAPACITY;  // nothing has changed
+    c->tok = tok;
+    for (int sl : stale) {
+        c->lru.erase({c->stamp[sl], sl});
+        c->slot_of[c->owner[sl]] = -1;
+        c->owner[sl] = -1;
+        c->free_slots.insert(sl);
+        c->st.window_evictions++;
+    }
+    for (int e = 0; e < E; ++e)
+        if (want[e]) c->count[key0 + e]++;
+    // 1. hits, ascending id: most recent
+    for (int e = 0; e < E; ++e) {
+        if (!hit[e]) continue;
+        const int sl = c->slot_of[key0 + e];
         c->lru.erase({c->stamp[sl], sl});
         c->stamp[sl] = ++c->clock;
         c->lru.insert({c->stamp[sl], sl});
+        c->last_tok[sl] = tok;
     }
     // 2. misses, ascending id: lowest free slot, else LRU slot outside this request
     cudaStream_t cs = moe_cuda_stream(d.copy_stream);
@@ -505,7 +565,7 @@ extern "C" int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host
     int waited[MOE_EVENT_RING];
     int n_waited = 0;
     for (int e = 0; e < E; ++e) {
-        if (!want[e] || hit[e]) continue;
+        if (!want[e] || hit[e] || bypass[e]) continue;
         int sl;
         bool evicted = false;
         if (!c->free_slots.empty()) {
@@ -551,6 +611,7 @@ extern "C" int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host
         c->slot_of[key0 + e] = sl;
         c->stamp[sl] = ++c->clock;
         c->lru.insert({c->stamp[sl], sl});
+        c->last_tok[sl] = tok;
         c->last_use[sl] = -1;
         if (evicted) c->st.evictions++;
         ++n_miss;
@@ -569,19 +630,22 @@ extern "C" int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host
 
     c->last_slots.clear();
     for (int e = 0; e < E; ++e)
-        if (want[e]) c->last_slots.push_back(c->slot_of[key0 + e]);
-    int route_hits = 0;
+        if (want[e] && !bypass[e]) c->last_slots.push_back(c->slot_of[key0 + e]);
+    int route_hits = 0, n_real = 0;
     for (int i = 0; i < n_ids; ++i) {
-        slots_host_out[i] = c->slot_of[key0 + ids_host[i]];
-        route_hits += hit[ids_host[i]];
+        const int e = ids_host[i];
+        slots_host_out[i] = e < 0 ? -1 : c->slot_of[key0 + e];
+        route_hits += e >= 0 && hit[e];
+        n_real += e >= 0;
     }
     *n_miss_out = n_miss;
     const int bucket = n_tokens <= 8 ? 0 : 1;
     c->st.queries[bucket] += n_distinct;
-    c->st.hits[bucket] += n_distinct - n_miss;
-    c->st.misses[bucket] += n_miss;
-    c->st.h2d_bytes += bytes;
-    c->st.route_queries += n_ids;
+    c->st.hits[bucket] += n_distinct - n_miss - n_bypass;
+    c->st.misses[bucket] += n_miss + n_bypass;
+    c->st.bypassed += n_bypass;
+    c->st.h2d_bytes += bytes + (uint64_t)n_bypass * c->image_bytes;  // read from host memory
+    c->st.route_queries += n_real;
     c->st.route_hits += route_hits;
     c->st.ensure_calls++;
 
@@ -629,6 +693,8 @@ extern "C" int moe_cache_stats_get(const moe_cache *c, moe_cache_stats *out) {
         st.route_queries = h.route_queries;
         st.route_hits = h.route_hits;
         st.ensure_calls = h.ensure_calls;
+        st.bypassed = h.bypassed;
+        st.window_evictions = h.window_evictions;
         *out = st;
         return MOE_OK;
     }
@@ -656,6 +722,13 @@ extern "C" void moe_cache_destroy(moe_cache *c) {
         if (c->ring[i]) cudaEventDestroy(c->ring[i]);
     if (c->upload_done) cudaEventDestroy(c->upload_done);
     delete c;
+}
+
+const void *moe_cache_image(const moe_cache *c, int layer, int expert) {
+    if (!c) return nullptr;
+    const int ll = layer - c->d.first_layer;
+    if (ll < 0 || ll >= c->d.n_layers || expert < 0 || expert >= c->d.n_experts) return nullptr;
+    return c->images[(size_t)ll * c->d.n_experts + expert];
 }
 
 extern "C" int moe_cache_lookup(const moe_cache *c, int layer, int expert) {

@@ -159,12 +159,17 @@ static inline void moe_pdl_config(cudaLaunchConfig_t *cfg, cudaLaunchAttribute *
 // (values travel as kernel parameters, so no host staging buffer outlives the call).
 int moe_write_ints(int32_t *const dst[3], const int n[3], const int32_t *const src[3], cudaStream_t s);
 
+// Pinned host image of (layer, expert) of a cache (layer global; NULL outside the group).
+const void *moe_cache_image(const moe_cache *c, int layer, int expert);
 // Pool base and slot count of a cache; the layer range of its group.
 const void *moe_cache_pool(const moe_cache *c, int *n_slots);
 int moe_cache_layer_range(const moe_cache *c, int *first_layer, int *n_layers);
 bool moe_cache_is_device_managed(const moe_cache *c);
 
 size_t moe_decode_workspace_bytes(int T, int H, int F, int qtype, int E, int k);
+// moe_combine_rmsnorm skipping the routes whose id is -1 (ids [T][k] device, or NULL).
+int moe_combine_rmsnorm_routes(const float *partial, const int32_t *ids, int T, int k, int H, const float *extra,
+                               float *y, float *xn, float eps, cudaStream_t s);
 // Workspace of moe_expert_ffn for these sizes (decode GEMV or prefill grouped GEMM path).
 size_t moe_ffn_workspace_bytes(int T, int H, int F, int qtype, int xtype, int E, int k);
 

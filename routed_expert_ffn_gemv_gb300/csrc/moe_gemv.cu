@@ -1037,9 +1037,9 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
     }
     // ---- per warp: rank of each route among the warp's routes of its expert, and counts
     int e = -1;
-    if (tid < R) {
-        if (e_r < 0 || e_r >= E) moe_set_status(status, MOE_ERR_INVALID);
-        else if (insub[e_r]) e = e_r;
+    if (tid < R) {  // id -1: a route dropped by the load threshold (no route, not an error)
+        if (e_r < -1 || e_r >= E) moe_set_status(status, MOE_ERR_INVALID);
+        else if (e_r >= 0 && insub[e_r]) e = e_r;
     }
     const unsigned grp = __match_any_sync(0xffffffffu, e);
     const int wrank = __popc(grp & ((1u << lane) - 1u));
@@ -1099,19 +1099,22 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t *__restrict_
         ActInfo in;
         in.fill = in.wt = 0;
         in.src = in.dst = 0ull;
-        const bool bad = slot < 0 || slot >= n_slots;
+        // a fill source without a slot: read the host image only (an expert the pool's
+        // admission policy bypassed); a slot out of range otherwise is an error
+        const unsigned long long f = s_fill[ex_id];
+        const bool bypass = f != 0ull && slot < 0;
+        const bool bad = !bypass && (slot < 0 || slot >= n_slots);
         if (bad) {
             moe_set_status(status, MOE_ERR_INVALID);  // nothing of this expert is read
         } else {
-            in.dst = (unsigned long long)(pool + (size_t)slot * slot_bytes);
-            const unsigned long long f = s_fill[ex_id];
+            in.dst = bypass ? 0ull : (unsigned long long)(pool + (size_t)slot * slot_bytes);
             in.fill = f != 0ull;
             in.src = f ? f : in.dst;
         }
         for (int j = 0; j < vb[a + 1] - vb[a]; ++j) {
             in.pos0 = s_aoff[a] + GV_TOK * j;
             in.n_e = bad ? 0 : min(GV_TOK, n_e - GV_TOK * j);
-            in.wt = in.fill && j == 0;
+            in.wt = in.fill && !bypass && j == 0;
 #pragma unroll
             for (int t = 0; t < GV_TOK; ++t) in.rt[t] = t < in.n_e ? s_routes[in.pos0 + t] : 0;
             info[vb[a] + j] = in;
@@ -1189,7 +1192,7 @@ __global__ void combine_kernel(const float4 *__restrict__ partial, int T, int k,
 // order), then xn = y / sqrt(mean(y^2) + eps) with a fixed-order block reduction.
 __global__ void __launch_bounds__(256) combine_norm_kernel(const float4 *__restrict__ partial, int k, int H4,
                                                            const float4 *extra, float4 *y, float4 *xn,
-                                                           float eps) {
+                                                           float eps, const int32_t *__restrict__ ids) {
     __shared__ float red[8];
     constexpr int KEEP = 4;  // sums kept in registers for the scaling pass (H <= 4096 at 256 threads)
     const int t = blockIdx.x;
@@ -1201,6 +1204,7 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(const float4 *__restr
     for (int h = threadIdx.x; h < H4; h += blockDim.x, ++n) {
         float4 s = extra ? extra[(size_t)t * H4 + h] : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < k; ++j) {
+            if (ids && ids[(size_t)t * k + j] < 0) continue;  // a dropped route (load threshold)
             const float4 v = partial[((size_t)t * k + j) * H4 + h];
             s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
         }
@@ -1593,6 +1597,12 @@ extern "C" int moe_expert_ffn_workspace(int T, int H, int F, int qtype, int xtyp
 
 extern "C" int moe_combine_rmsnorm(const float *partial, int T, int k, int H, const float *extra, float *y,
                                    float *xn, float eps, moe_stream_t s) {
+    return moe_combine_rmsnorm_routes(partial, nullptr, T, k, H, extra, y, xn, eps, moe_cuda_stream(s));
+}
+
+// moe_combine_rmsnorm skipping the routes whose id is -1 (ids [T][k] device, or NULL).
+int moe_combine_rmsnorm_routes(const float *partial, const int32_t *ids, int T, int k, int H, const float *extra,
+                               float *y, float *xn, float eps, cudaStream_t s) {
     MOE_CHECK(T >= 0 && k >= 0 && k <= 64 && H > 0 && H % 4 == 0 && eps >= 0.f);
     if (T == 0) return MOE_OK;
     MOE_CHECK(k == 0 || partial);
@@ -1602,9 +1612,9 @@ extern "C" int moe_combine_rmsnorm(const float *partial, int T, int k, int H, co
     MOE_CHECK(!(xn && (xn == extra || xn == y)));
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    moe_pdl_config(&cfg, attr, dim3(T), dim3(256), 0, moe_cuda_stream(s));
+    moe_pdl_config(&cfg, attr, dim3(T), dim3(256), 0, s);
     MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, combine_norm_kernel, (const float4 *)partial, k, H / 4,
-                                    (const float4 *)extra, (float4 *)y, (float4 *)xn, eps));
+                                    (const float4 *)extra, (float4 *)y, (float4 *)xn, eps, ids));
     return MOE_OK;
 }
 

@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(1024) pf_route_kernel(const int32_t *__restric
         const int r = base + lane;
         if (r < r1) {
             const int v = ids[r];
-            if (v < 0 || v >= E) moe_set_status(status, MOE_ERR_INVALID);
+            if (v < -1 || v >= E) moe_set_status(status, MOE_ERR_INVALID);  // -1: a dropped route
         }
         const int e = expert_of(r);
         const unsigned grp = __match_any_sync(0xffffffffu, e);

@@ -61,7 +61,7 @@ __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
 // lanes 0..k-1 write ids/weights of row `row`.
 __device__ __forceinline__ void select_topk_softmax(const float (&v)[MOE_MAX_E / 32], int E, int k, int lane,
                                                     size_t row, int32_t *__restrict__ ids,
-                                                    float *__restrict__ weights) {
+                                                    float *__restrict__ weights, float min_w) {
     constexpr int NPL = MOE_MAX_E / 32;
     unsigned taken = 0;
     float sel_v[MOE_MAX_K];
@@ -100,8 +100,11 @@ __device__ __forceinline__ void select_topk_softmax(const float (&v)[MOE_MAX_E /
                 myv = sel_v[j];
                 myi = sel_i[j];
             }
-        ids[row * k + lane] = myi;
-        weights[row * k + lane] = expf(myv - sel_v[0]) / denom;
+        // a route whose weight is below the load threshold is dropped: id -1, weight 0
+        const float w = expf(myv - sel_v[0]) / denom;
+        const bool drop = w < min_w;
+        ids[row * k + lane] = drop ? -1 : myi;
+        weights[row * k + lane] = drop ? 0.f : w;
     }
 }
 
@@ -110,7 +113,7 @@ __global__ void __launch_bounds__(MOE_ROUTER_THREADS)
 router_topk_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__restrict__ w_router,
                    const float *__restrict__ bias, int E, int k, int32_t *__restrict__ ids,
                    float *__restrict__ weights, float *__restrict__ logits_out, int use_bulk,
-                   int *status) {
+                   int *status, float min_w) {
     extern __shared__ __align__(128) unsigned char smem[];
     const RouterSmem L = router_smem_layout(H, E);
     const uint16_t *w_s = (const uint16_t *)(smem + L.w);
@@ -216,7 +219,7 @@ router_topk_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__r
                     v[i] = (s != s) ? -INFINITY : s;  // NaN never wins
                 }
             }
-            select_topk_softmax(v, E, k, lane, (size_t)(t0 + t), ids, weights);
+            select_topk_softmax(v, E, k, lane, (size_t)(t0 + t), ids, weights, min_w);
         }
     }
     cluster_sync_all();  // rank 0 has finished reading the other CTAs' shared memory
@@ -248,7 +251,7 @@ template <int XT, int EPT>
 __global__ void __launch_bounds__(MOE_ROUTER_THREADS)
 router_tiled_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__restrict__ w_router,
                     const float *__restrict__ bias, int E, int k, int32_t *__restrict__ ids,
-                    float *__restrict__ weights, float *__restrict__ logits_out) {
+                    float *__restrict__ weights, float *__restrict__ logits_out, float min_w) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int EP = 32 * EPT;
     float2 *xs = (float2 *)smem;                                       // [2][KC][RT_XS]
@@ -394,7 +397,7 @@ router_tiled_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__
                 v[i] = (s != s) ? -INFINITY : s;  // NaN never wins
             }
         }
-        select_topk_softmax(v, E, k, lane, (size_t)(t0 + t), ids, weights);
+        select_topk_softmax(v, E, k, lane, (size_t)(t0 + t), ids, weights, min_w);
     }
     cluster_sync_all();  // the other ranks have finished reading this CTA's shared memory
 }
@@ -405,7 +408,7 @@ namespace {
 
 template <int XT, int EPT>
 int router_tiled_launch_t(const void *x, int T, int H, const uint16_t *w_router, const float *bias, int E,
-                          int k, int32_t *ids, float *weights, float *logits, cudaStream_t st) {
+                          int k, int32_t *ids, float *weights, float *logits, float min_w, cudaStream_t st) {
     const size_t smem = router_tiled_smem(32 * EPT);
     MOE_TRY_CUDA(cudaFuncSetAttribute(router_tiled_kernel<XT, EPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)smem));
@@ -425,17 +428,19 @@ int router_tiled_launch_t(const void *x, int T, int H, const uint16_t *w_router,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, router_tiled_kernel<XT, EPT>, x, T, H, w_router, bias, E, k, ids, weights,
-                                    logits));
+                                    logits, min_w));
     return MOE_OK;
 }
 
 int router_tiled_launch(const void *x, int xtype, int T, int H, const uint16_t *w_router, const float *bias,
-                        int E, int k, int32_t *ids, float *weights, float *logits, cudaStream_t st) {
+                        int E, int k, int32_t *ids, float *weights, float *logits, float min_w, cudaStream_t st) {
     if (E <= 128)
-        return xtype == MOE_F32 ? router_tiled_launch_t<MOE_F32, 4>(x, T, H, w_router, bias, E, k, ids, weights, logits, st)
-                                : router_tiled_launch_t<MOE_BF16, 4>(x, T, H, w_router, bias, E, k, ids, weights, logits, st);
-    return xtype == MOE_F32 ? router_tiled_launch_t<MOE_F32, 8>(x, T, H, w_router, bias, E, k, ids, weights, logits, st)
-                            : router_tiled_launch_t<MOE_BF16, 8>(x, T, H, w_router, bias, E, k, ids, weights, logits, st);
+        return xtype == MOE_F32
+                   ? router_tiled_launch_t<MOE_F32, 4>(x, T, H, w_router, bias, E, k, ids, weights, logits, min_w, st)
+                   : router_tiled_launch_t<MOE_BF16, 4>(x, T, H, w_router, bias, E, k, ids, weights, logits, min_w, st);
+    return xtype == MOE_F32
+               ? router_tiled_launch_t<MOE_F32, 8>(x, T, H, w_router, bias, E, k, ids, weights, logits, min_w, st)
+               : router_tiled_launch_t<MOE_BF16, 8>(x, T, H, w_router, bias, E, k, ids, weights, logits, min_w, st);
 }
 
 }  // namespace
@@ -443,14 +448,21 @@ int router_tiled_launch(const void *x, int xtype, int T, int H, const uint16_t *
 extern "C" int moe_router_topk(const void *x, int xtype, int T, int H, const uint16_t *w_router,
                                const float *bias, int E, int k, int32_t *ids, float *weights,
                                float *logits, moe_stream_t s) {
+    return moe_router_topk_threshold(x, xtype, T, H, w_router, bias, E, k, 0.0f, ids, weights, logits, s);
+}
+
+extern "C" int moe_router_topk_threshold(const void *x, int xtype, int T, int H, const uint16_t *w_router,
+                                         const float *bias, int E, int k, float min_weight, int32_t *ids,
+                                         float *weights, float *logits, moe_stream_t s) {
     MOE_CHECK(T >= 0);
+    MOE_CHECK(min_weight >= 0.0f && min_weight <= 1.0f);
     MOE_CHECK(xtype == MOE_F32 || xtype == MOE_BF16);
     MOE_CHECK(H > 0 && H % 32 == 0);
     MOE_CHECK(E >= 1 && E <= MOE_MAX_E && k >= 1 && k <= MOE_MAX_K && k <= E);
     if (T == 0) return MOE_OK;
     MOE_CHECK(x && w_router && ids && weights);
     if (T > MOE_DECODE_MAX_T && ((uintptr_t)x & 15) == 0 && ((uintptr_t)w_router & 15) == 0)
-        return router_tiled_launch(x, xtype, T, H, w_router, bias, E, k, ids, weights, logits,
+        return router_tiled_launch(x, xtype, T, H, w_router, bias, E, k, ids, weights, logits, min_weight,
                                    moe_cuda_stream(s));
     const RouterSmem L = router_smem_layout(H, E);
     if (L.total > 200 * 1024) return MOE_ERR_UNSUPPORTED;
@@ -478,12 +490,12 @@ extern "C" int moe_router_topk(const void *x, int xtype, int T, int H, const uin
         MOE_TRY_CUDA(cudaFuncSetAttribute(router_topk_kernel<MOE_F32>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total));
         MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, router_topk_kernel<MOE_F32>, x, T, H, w_router, bias, E,
-                                        k, ids, weights, logits, use_bulk, status));
+                                        k, ids, weights, logits, use_bulk, status, min_weight));
     } else {
         MOE_TRY_CUDA(cudaFuncSetAttribute(router_topk_kernel<MOE_BF16>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total));
         MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, router_topk_kernel<MOE_BF16>, x, T, H, w_router, bias,
-                                        E, k, ids, weights, logits, use_bulk, status));
+                                        E, k, ids, weights, logits, use_bulk, status, min_weight));
     }
     return MOE_OK;
 }

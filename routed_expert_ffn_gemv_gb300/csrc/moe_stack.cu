@@ -221,8 +221,8 @@ int layer_step(moe_stack *st, int layer, const float *h, float *y, int T, int32_
         st->prof.kernel_launches += 1;
     }
     if ((rc = begin_timed(st, s, &ep))) return rc;
-    if ((rc = moe_router_topk(x, MOE_F32, T, d.H, st->w_router[layer], st->bias[layer], d.E, d.k,
-                              ids_d, w_d, nullptr, (moe_stream_t)s)))
+    if ((rc = moe_router_topk_threshold(x, MOE_F32, T, d.H, st->w_router[layer], st->bias[layer], d.E, d.k,
+                                        d.load_threshold, ids_d, w_d, nullptr, (moe_stream_t)s)))
         return rc;
     st->prof.kernel_launches += 1;
     if ((rc = end_timed(st, s, K_ROUTER, ep))) return rc;
@@ -253,14 +253,33 @@ int layer_step(moe_stack *st, int layer, const float *h, float *y, int T, int32_
                                    nullptr, (moe_stream_t)s)))
             return rc;
         bool want[MOE_MAX_E] = {false};
-        for (int i = 0; i < T * d.k; ++i) want[st->ids_h[i]] = true;
+        for (int i = 0; i < T * d.k; ++i)
+            if (st->ids_h[i] >= 0) want[st->ids_h[i]] = true;  // -1: a dropped route
         int32_t hits[MOE_MAX_E], misses[MOE_MAX_E], tbl[MOE_MAX_E];
+        uint64_t fsrc[MOE_MAX_E];
         int nh = 0, nm = 0;
+        bool any_bypass = false;
         for (int e = 0; e < d.E; ++e) {
             tbl[e] = moe_cache_lookup(c, layer, e);
+            fsrc[e] = 0ull;
             if (!want[e]) continue;
-            if (miss_mask[e]) misses[nm++] = e;
-            else hits[nh++] = e;
+            if (miss_mask[e]) {
+                misses[nm++] = e;
+            } else {
+                hits[nh++] = e;  // resident, or bypassed by the admission policy (no slot):
+                if (tbl[e] < 0) {  // then read from its pinned host image
+                    fsrc[e] = (uint64_t)(uintptr_t)moe_cache_image(c, layer, e);
+                    any_bypass = true;
+                }
+            }
+        }
+        uint64_t *fill = any_bypass ? (uint64_t *)(st->ws + L.fill) : nullptr;
+        if (fill) {  // the u64 table as two runs of 32-bit words
+            int32_t *dst[3] = {(int32_t *)fill, (int32_t *)fill + d.E, nullptr};
+            const int n[3] = {d.E, d.E, 0};
+            const int32_t *src[3] = {(const int32_t *)fsrc, (const int32_t *)fsrc + d.E, nullptr};
+            if ((rc = moe_write_ints(dst, n, src, s))) return rc;
+            st->prof.kernel_launches += 1;
         }
         const bool two_phase = d.overlap && nh > 0 && nm > 0;
         {
@@ -275,7 +294,8 @@ int layer_step(moe_stack *st, int layer, const float *h, float *y, int T, int32_
             int ns = 0;
             const void *pool = moe_cache_pool(c, &ns);
             if (two_phase) {
-                if ((rc = ffn_call(st, x, T, d.E, d.k, ids_d, w_d, table, ns, pool, hit_d, nh, partial, nh, s)))
+                if ((rc = ffn_call(st, x, T, d.E, d.k, ids_d, w_d, table, ns, pool, hit_d, nh, partial, nh, s,
+                                   fill)))
                     return rc;
                 if ((rc = moe_cache_wait_uploads(c, (moe_stream_t)s))) return rc;
                 if ((rc = ffn_call(st, x, T, d.E, d.k, ids_d, w_d, table, ns, pool, miss_d, nm, partial, nm, s)))
@@ -283,7 +303,7 @@ int layer_step(moe_stack *st, int layer, const float *h, float *y, int T, int32_
             } else {
                 if ((rc = moe_cache_wait_uploads(c, (moe_stream_t)s))) return rc;
                 if ((rc = ffn_call(st, x, T, d.E, d.k, ids_d, w_d, table, ns, pool, nullptr, 0, partial,
-                                   nh + nm, s)))
+                                   nh + nm, s, fill)))
                     return rc;
             }
         }
@@ -311,8 +331,8 @@ int layer_step(moe_stack *st, int layer, const float *h, float *y, int T, int32_
         extra = tmp;
     }
     if ((rc = begin_timed(st, s, &ep))) return rc;
-    if ((rc = moe_combine_rmsnorm(partial, T, d.k, d.H, extra, y, norm_out ? x : nullptr, MOE_STACK_EPS,
-                                  (moe_stream_t)s)))
+    if ((rc = moe_combine_rmsnorm_routes(partial, d.load_threshold > 0.f ? ids_d : nullptr, T, d.k, d.H, extra, y,
+                                         norm_out ? x : nullptr, MOE_STACK_EPS, s)))
         return rc;
     st->prof.kernel_launches += 1;
     if ((rc = end_timed(st, s, K_COMBINE, ep))) return rc;

@@ -62,14 +62,16 @@ class Stack:
     """A full decode stack of one configuration on the current CUDA device.
 
     pool_slots: override the per-group slot counts (None: the configuration's); a config
-    with no groups keeps every expert resident in one device pool.
+    with no groups keeps every expert resident in one device pool.  admit_after / lru_window:
+    the pools' policy variants (0: plain LRU; see moe_cache_desc).
     """
 
     def __init__(self, cfg: synth.MoEConfig, max_T: Optional[int] = None, overlap: bool = True,
                  profile: int = 0, pool_slots: Optional[Sequence[int]] = None,
                  n_layers: Optional[int] = None, random_scales: bool = False,
                  resident: bool = False, device_managed: bool = False, use_graph: bool = False,
-                 images: Optional[PinnedImages] = None):
+                 images: Optional[PinnedImages] = None, admit_after: int = 0, lru_window: int = 0,
+                 load_threshold: float = 0.0):
         self.cfg = cfg
         self.L = n_layers or cfg.L
         self.max_T = max_T or max(cfg.tokens)
@@ -123,7 +125,8 @@ class Stack:
                                    copy_stream=self.copy_stream.cuda_stream,
                                    device_managed=int(device_managed),
                                    device_state=None if state is None else state.data_ptr(),
-                                   device_state_bytes=state_bytes)
+                                   device_state_bytes=state_bytes, admit_after=admit_after,
+                                   lru_window=lru_window)
                 self.caches.append(L.moe_cache_create(desc))
                 self.pools.append(pool)
         # shared experts (always resident)
@@ -148,7 +151,7 @@ class Stack:
                            slot_bytes=self.stride, max_T=self.max_T, workspace=self.workspace.data_ptr(),
                            ws_bytes=ws, overlap=int(overlap), profile=int(profile),
                            device_managed=int(device_managed and bool(self.caches)),
-                           use_graph=int(use_graph))
+                           use_graph=int(use_graph), load_threshold=float(load_threshold))
         torch.cuda.synchronize()
         self.handle = L.moe_stack_create(desc)
 

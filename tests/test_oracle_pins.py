@@ -416,3 +416,69 @@ def test_route_override_uses_the_given_ids_and_weights():
     for t in range(3):
         for j in range(2):
             np.testing.assert_allclose(res.y_experts[t, j], ydense[t, ids[t, j]], rtol=1e-11, atol=1e-11)
+
+
+def test_lru_policy_golden_traces():
+    """Frequency admission and the LRU window against hand-derived traces."""
+    for tr in _golden("lru_traces.json")["policy_traces"]:
+        sim = LRUSim(tr["n_slots"], admit_after=tr["admit_after"], window=tr["window"],
+                     first_layer=tr["first_layer"])
+        for (layer, ids, nt), slots, h, m in zip(tr["requests"], tr["slots"], tr["hits"], tr["misses"]):
+            res, hit_ids, miss_ids = sim.ensure(layer, ids, n_tokens=nt)
+            assert {str(e): s for e, s in res.items()} == slots, tr["name"]
+            assert (len(hit_ids), len(miss_ids)) == (h, m), tr["name"]
+        assert sim.evictions == tr["evictions"], tr["name"]
+        assert sim.bypassed == tr["bypassed"], tr["name"]
+        assert sim.window_evictions == tr["window_evictions"], tr["name"]
+
+
+def test_lru_policies_reduce_to_plain_lru_and_keep_invariants():
+    rng = np.random.default_rng(17)
+    plain, same = LRUSim(6), LRUSim(6, admit_after=1, window=0)
+    adm, win = LRUSim(6, admit_after=3), LRUSim(6, window=4, first_layer=0)
+    for step in range(500):
+        layer = int(rng.integers(0, 3))
+        ids = rng.integers(0, 10, size=int(rng.integers(1, 5)))
+        r0 = plain.ensure(layer, ids, n_tokens=2)
+        assert same.ensure(layer, ids, n_tokens=2) == r0     # the defaults are plain LRU
+        for sim in (adm, win):
+            res, hit, miss = sim.ensure(layer, ids, n_tokens=2)
+            slots = [s for s in res.values() if s >= 0]
+            assert len(set(slots)) == len(slots)              # distinct slots
+            for e, s in res.items():
+                if s >= 0:
+                    assert sim.owner[s] == (layer, e)
+            assert set(hit) | set(miss) == set(int(e) for e in ids)
+    # admission: an expert is never resident before its third access
+    assert all(adm.count[key] >= 3 for key in adm.where)
+    # window: nothing resident is more than 4 tokens stale after the last request
+    assert all(win.tok - win.last_tok[s] <= 4 + 2 for s in range(6) if win.owner[s] is not None)
+    assert adm.bypassed > 0 and win.window_evictions > 0
+
+
+def test_load_threshold_drops_light_routes_without_renormalising():
+    """moe_layer(load_threshold=th) against a numpy dense computation that keeps only the
+    selected routes whose softmax weight is at least th (page 1, section 4.3)."""
+    cfg = synth.small_config(0, H=64, F=64, E=8, k=4, bias_a=1.0)
+    x = np.random.default_rng(23).standard_normal((5, 64)) * 3.0   # spread out the weights
+    wr, b = synth.router_weights(cfg, 0), synth.router_bias(cfg, 0)
+    ex = lambda e: synth.expert_weights(cfg, 0, e)
+    full = oracle.moe_layer(0, 64, 64, 4, x, wr, b, ex)
+    th = float(np.median(full.weights))         # some routes on each side
+    res = oracle.moe_layer(0, 64, 64, 4, x, wr, b, ex, load_threshold=th)
+    ydense = _dense_layer_numpy(cfg, 0, x, wr, b)
+    expect = np.zeros((5, 64))
+    n_drop = 0
+    for t in range(5):
+        for j in range(4):
+            if full.weights[t, j] >= th:
+                expect[t] += full.weights[t, j] * ydense[t, full.ids[t, j]]
+                assert res.ids[t, j] == full.ids[t, j] and res.weights[t, j] == full.weights[t, j]
+            else:
+                n_drop += 1
+                assert res.ids[t, j] == -1 and res.weights[t, j] == 0.0
+    assert 0 < n_drop < 20
+    np.testing.assert_allclose(res.y, expect, rtol=1e-11, atol=1e-11)
+    # threshold 0 changes nothing; above every weight only shared experts would remain
+    np.testing.assert_allclose(oracle.moe_layer(0, 64, 64, 4, x, wr, b, ex, load_threshold=0.0).y, full.y, rtol=0, atol=0)
+    assert np.all(oracle.moe_layer(0, 64, 64, 4, x, wr, b, ex, load_threshold=1.01).y == 0.0)

@@ -539,6 +539,8 @@ extern "C" int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host
         n_bypass += bypass[e];
     }
     if (n_need > d.n_slots) return MOE_ERR_CAPACITY;  // nothing has changed
+    if (miss_mask_host_out)  // 1 only for the experts this call uploads
+        for (int e = 0; e < E; ++e) miss_mask_host_out[e] = 0;
     c->tok = tok;
     for (int sl : stale) {
         c->lru.erase({c->stamp[sl], sl});
@@ -624,9 +626,6 @@ extern "C" int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host
     } else {
         c->upload_pending = false;
     }
-    if (miss_mask_host_out)
-        for (int e = 0; e < E; ++e)
-            if (!(want[e] && !hit[e])) miss_mask_host_out[e] = 0;
 
     c->last_slots.clear();
     for (int e = 0; e < E; ++e)

@@ -70,10 +70,11 @@ def _requests(rng, E, n_layers, steps):
             yield step, layer, np.stack([rng.choice(E, size=2, replace=False, p=p) for _ in range(T)]).astype(np.int32)
 
 
-@pytest.mark.parametrize("admit_after,lru_window", [(3, 0), (1, 6), (2, 5)])
-def test_host_pool_policies_match_simulator(admit_after, lru_window):
+# (slot counts chosen with the simulator so that each trace also has LRU evictions)
+@pytest.mark.parametrize("admit_after,lru_window,n_slots", [(3, 0, 12), (1, 4, 20), (2, 3, 16)])
+def test_host_pool_policies_match_simulator(admit_after, lru_window, n_slots):
     cfg = synth.small_config(0, H=64, F=64, E=16, k=2, seed_cfg=840)
-    n_layers, n_slots = 3, 12
+    n_layers = 3
     fx = Pool(cfg, n_layers, n_slots, False, admit_after, lru_window)
     sim = LRUSim(n_slots, admit_after=max(1, admit_after), window=lru_window, first_layer=0)
     host_view = fx.host.numpy()
@@ -106,6 +107,7 @@ def test_host_pool_policies_match_simulator(admit_after, lru_window):
     assert st["window_evictions"] == sim.window_evictions
     assert st["h2d_bytes"] == sim.misses * fx.img_bytes
     assert (sim.bypassed > 0) == (admit_after > 1) and (sim.window_evictions > 0) == (lru_window > 0)
+    assert sim.evictions > 0
     L.moe_cache_destroy(fx.cache)
 
 

@@ -272,7 +272,7 @@ def hit_fields(st, prefix=""):
 
 
 def run_config(ci, Ts, torch, stream, peaks, link_gbs, warmup, total=256, stack=None, cpu_budget_s=4.0,
-               world=1, rank=0):
+               world=1, rank=0, resident=True):
     """One decode configuration at each batch size in Ts: the device-managed pool (the
     configuration's slot counts, LRU on the GPU, misses read over the CPU-GPU link),
     `total` steps from a cold pool of which the last total - warmup are timed, whole steps
@@ -310,6 +310,10 @@ def run_config(ci, Ts, torch, stream, peaks, link_gbs, warmup, total=256, stack=
         e["frac_of_link_aware_attainable"] = tps / (T / t_att)
         out[T] = e
     stack.close()
+    if not resident:
+        del images
+        torch.cuda.empty_cache()
+        return out
     # every expert resident in HBM, the same inputs (the same routing, so the same bytes)
     res = Stack(cfg, max_T=max(Ts), resident=True, use_graph=True, images=images)
     for T in Ts:
@@ -327,6 +331,47 @@ def run_config(ci, Ts, torch, stream, peaks, link_gbs, warmup, total=256, stack=
     if rank == 0 and world == 1 and cpu_budget_s > 0:
         for T in Ts:
             out[T]["cpu_baseline"] = cpu_sample(cfg, T, cpu_budget_s)
+    return out
+
+
+POLICIES = (
+    # name, pool mode, Stack options (page 3 section 2.2: frequency admission; page 1 section 4.3:
+    # --moe-lru-window 15 and --moe-expert-load-threshold 0.05)
+    ("lru_device", dict(device_managed=True, use_graph=True)),
+    ("admit2_device", dict(device_managed=True, use_graph=True, admit_after=2)),
+    ("admit4_device", dict(device_managed=True, use_graph=True, admit_after=4)),
+    ("load_threshold_0.05_device", dict(device_managed=True, use_graph=True, load_threshold=0.05)),
+    ("lru_host", dict()),
+    ("window15_host", dict(lru_window=15)),
+)
+
+
+def run_policies(torch, stream, peaks, link_gbs, warmup, total=128, T=8):
+    """The Granite-shaped stack at batch 8 (where plain LRU hits nothing: the 24 layers' ~720
+    distinct experts per step cycle through 384 slots) under each pool policy: tokens/s, hit
+    rates, bypassed misses and window evictions over `total - warmup` timed steps from a cold
+    pool.  The load threshold changes the routing (fewer routes, a different result); the
+    other policies only change where the weights are read from."""
+    from routed_expert_ffn_gemv_gb300 import synth
+    from routed_expert_ffn_gemv_gb300.workload import PinnedImages, Stack
+    cfg = synth.config(1)
+    images = PinnedImages(cfg, range(cfg.L), range(cfg.E))
+    xs = [torch.from_numpy(synth.tokens_x(cfg, 3 + s, T)).cuda() for s in range(total)]
+    out = {}
+    for name, kw in POLICIES:
+        st = Stack(cfg, max_T=T, images=images, **kw)
+        ms, tst, cold = time_window(st, xs, T, total, warmup, torch, stream)
+        steps = total - warmup
+        e = {"tokens_per_s": T * steps / (ms / 1e3), "ms_per_step": ms / steps,
+             "miss_bytes_per_step": tst["h2d_bytes"] / steps,
+             "routes_per_step": tst["route_queries"] / steps,
+             "bypassed_per_step": tst["bypassed"] / steps,
+             "window_evictions_per_step": tst["window_evictions"] / steps}
+        e.update(hit_fields(tst))
+        out[name] = e
+        st.close()
+    del images
+    torch.cuda.empty_cache()
     return out
 
 
@@ -509,6 +554,11 @@ def summary_lines(line):
                     f"resident {e['resident_tokens_per_s']:.1f} tok/s "
                     f"({e['resident_frac_of_8tbs_roofline']:.3f} of 8 TB/s); "
                     f"oracle {e.get('cpu_baseline', {}).get('value', float('nan')):.2f} tok/s")
+    for name, e in line.get("policies_granite_b8", {}).items():
+        rows.append(f"policy {name}: {e['tokens_per_s']:.1f} tok/s, hit {e.get('hit_rate') or 0:.3f}, "
+                    f"{e['routes_per_step']:.0f} routes/step, {e['miss_bytes_per_step'] / 1e6:.0f} MB from host/step")
+    for name, e in line.get("batch_growth_qwen3", {}).items():
+        rows.append(f"qwen3 batch {name[1:]}: {e['tokens_per_s']:.1f} tok/s, hit {e.get('hit_rate') or 0:.3f}")
     pf = line.get("prefill", {})
     for T in ("512", "4096"):
         if f"t{T}_ffn_ms" in pf:
@@ -612,6 +662,17 @@ def run_gpu(args, world, rank, local):
         for Tb, e in res.items():
             configs[f"{short}_b{Tb}"] = e
 
+    # pool policy variants, and batch growth on the Qwen-shaped stack (the pages' model)
+    policies = run_policies(torch, stream, peaks, link_gbs, args.warmup) if not args.lite else {}
+    growth = {}
+    if args.configs is None or 2 in args.configs:
+        g = run_config(2, (2, 4, 8, 16, 32), torch, stream, peaks, link_gbs, args.warmup, total=64,
+                       cpu_budget_s=0.0, world=world, rank=rank, resident=False)
+        growth = {f"t{Tb}": {k: v for k, v in e.items() if k in (
+            "tokens_per_s", "ms_per_step", "hit_rate", "route_hit_rate", "hit_rate_le8", "hit_rate_9to32",
+            "miss_bytes_per_step", "expert_bytes_per_step", "frac_of_8tbs_roofline")} for Tb, e in g.items()}
+        if "qwen3_b1" in configs:
+            growth["t1"] = {k: configs["qwen3_b1"][k] for k in growth["t2"] if k in configs["qwen3_b1"]}
     prefill = run_prefill(torch, peaks)
     gv = gemv_roofline(cfg, T, torch, stream, steps=20, warmup=3)
     clk = clocks.stop()
@@ -635,6 +696,7 @@ def run_gpu(args, world, rank, local):
                         "d2h_bytes_per_step": T * cfg.H * 4, "steps": e2e_steps},
                 "gpu_launches": int(prof["kernel_launches"]),
                 "clocks": clk, "prefill": flat_prefill(prefill, peaks), "roofline": roofline,
+                "policies_granite_b8": policies, "batch_growth_qwen3": growth,
                 "configs": configs}
         print(json.dumps(line), flush=True)
         for row in summary_lines(line):

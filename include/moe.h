@@ -195,6 +195,10 @@ typedef struct {
     uint64_t ensure_calls;
     uint64_t bypassed;        /* misses served from host memory without a slot (admit_after) */
     uint64_t window_evictions;/* slots freed by the LRU window */
+    uint64_t prefetch_queries;/* speculative requests (moe_cache_prefetch_plan): distinct experts */
+    uint64_t prefetch_hits;   /*   already resident */
+    uint64_t prefetch_fills;  /*   given a slot and copied by moe_cache_prefetch_fill */
+    uint64_t prefetch_aborts; /*   requests abandoned (they would evict a slot in use) */
 } moe_cache_stats;
 
 /*
@@ -250,6 +254,27 @@ int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host, int n_tok
 int moe_cache_state_bytes(int n_layers, int n_experts, int n_slots, size_t *bytes);
 int moe_cache_plan(moe_cache *c, int layer, const int32_t *d_ids, int n_tokens, int k,
                    int32_t *d_table_out, uint64_t *d_fill_src_out, moe_stream_t s);
+
+/*
+ * Cross-layer speculative prefetch for device-managed pools (page 3, tiered MoE scheduling
+ * note, section "2.3 第三层传输与计算重叠层": a background stream prefetches the experts
+ * the next one or two layers will use while the GPU computes the current layer; section
+ * 4.3: prefetch depth 2).
+ * moe_cache_prefetch_plan — a speculative request: the same LRU rules as moe_cache_plan for
+ *   the predicted ids d_ids [n_tokens][k] of `layer` (hits stamped most recent, misses given
+ *   a slot), so the real request later finds them resident; its lookups are counted in the
+ *   prefetch statistics, not the hit rate.  It is abandoned (nothing changes, the table is
+ *   all -1 and the fill sources 0) if it would need a slot of the last real request of the
+ *   pool (that layer's kernels may still be using it) or more slots than the pool has.
+ *   Outputs as moe_cache_plan (d_fill_src_out: the image of each expert given a slot).
+ * moe_cache_prefetch_fill — copies every expert with d_fill_src[e] != 0 from its pinned host
+ *   image into slot d_table[e] (stream-ordered on s; typically a side stream forked after
+ *   the plan and joined before the predicted layer's FFN).  The experts' slots must not be
+ *   read before the copy completes.
+ */
+int moe_cache_prefetch_plan(moe_cache *c, int layer, const int32_t *d_ids, int n_tokens, int k,
+                            int32_t *d_table_out, uint64_t *d_fill_src_out, moe_stream_t s);
+int moe_cache_prefetch_fill(moe_cache *c, const int32_t *d_table, const uint64_t *d_fill_src, moe_stream_t s);
 
 /* moe_cache_wait_uploads — stream s waits for the uploads issued by the last ensure. */
 int moe_cache_wait_uploads(moe_cache *c, moe_stream_t s);
@@ -419,6 +444,14 @@ typedef struct {
     float load_threshold;             /* 0: off; else routes below it are dropped before the
                                          pools see them (moe_router_topk_threshold; this
                                          changes the layer's output) */
+    int prefetch_depth;               /* device-managed pools: 0 off, 1 or 2 = cross-layer
+                                         speculative prefetch (page 3, sections 2.3 and 4.3):
+                                         after layer l's plan, layers l+1 .. l+depth are routed
+                                         on layer l's input, planned speculatively
+                                         (moe_cache_prefetch_plan) and their predicted misses
+                                         copied into their slots on a side stream while layer l
+                                         computes; joined before layer l+1's plan (the plans)
+                                         and FFN (the copies).  Values are unchanged. */
 } moe_stack_desc;
 
 typedef struct moe_stack moe_stack;

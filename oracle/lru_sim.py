@@ -27,6 +27,14 @@ Policy variants (each off by default; with both off the rules above are unchange
     the ubatch's token count at every request of the group's first layer; before a
     request, every slot whose last use is more than W tokens behind the clock is freed
     (its expert becomes non-resident), then rules 1-4 apply.
+
+Speculative requests (cross-layer prefetch; page 3, section "2.3 第三层传输与计算重叠层":
+the experts the next one or two layers will use are prefetched while the current layer
+computes): ``prefetch(layer, ids)`` applies rules 1-4 to the predicted ids like a request
+(hits stamped, misses given slots — under admission the misses the real access would
+admit — without counting an access), with its own statistics, and is abandoned — nothing
+changes — when it needs more slots than the pool has or would evict a slot of the last
+real request (that layer's work may still be using it).
 """
 from __future__ import annotations
 
@@ -59,6 +67,11 @@ class LRUSim:
         self.evictions = 0
         self.bypassed = 0
         self.window_evictions = 0
+        self.last_real_slots: set = set()
+        self.pf_queries = 0
+        self.pf_hits = 0
+        self.pf_fills = 0
+        self.pf_aborts = 0
 
     def ensure(self, layer: int, ids: Iterable[int], n_tokens: int = 1
                ) -> Tuple[Dict[int, int], List[int], List[int]]:
@@ -117,7 +130,53 @@ class LRUSim:
         self.hits += len(hit_ids)
         self.misses += len(miss_ids)
         self.bypassed += len(bypass)
+        self.last_real_slots = {s for s in result.values() if s >= 0}
         return result, hit_ids, miss_ids
+
+    def prefetch(self, layer: int, ids: Iterable[int]) -> Dict[int, int]:
+        """A speculative request; returns {expert: slot, -1 if not resident} ({} if abandoned)."""
+        req = sorted(set(int(e) for e in ids))
+        keys = {(layer, e) for e in req}
+        hit_ids = [e for e in req if (layer, e) in self.where]
+        miss_ids = [e for e in req if (layer, e) not in self.where]
+        # what the real access would admit (count + 1 >= theta), without counting the access
+        admitted = [e for e in miss_ids if self.count.get((layer, e), 0) + 1 >= self.admit_after]
+        if len(hit_ids) + len(admitted) > self.n_slots:
+            self.pf_aborts += 1
+            return {}
+        # the victims the misses would take (after the free slots), oldest first
+        n_free = sum(1 for s in range(self.n_slots) if self.owner[s] is None)
+        n_evict = max(0, len(admitted) - n_free)
+        cands = sorted((s for s in range(self.n_slots) if self.owner[s] not in keys and self.owner[s] is not None),
+                       key=lambda i: self.stamp[i])
+        if any(s in self.last_real_slots for s in cands[:n_evict]):
+            self.pf_aborts += 1
+            return {}
+        result: Dict[int, int] = {}
+        for e in hit_ids:
+            s = self.where[(layer, e)]
+            self.clock += 1
+            self.stamp[s] = self.clock
+            result[e] = s
+        for e in admitted:
+            free = [s for s in range(self.n_slots) if self.owner[s] is None]
+            if free:
+                s = free[0]
+            else:
+                s = min((s for s in range(self.n_slots) if self.owner[s] not in keys), key=lambda i: self.stamp[i])
+                del self.where[self.owner[s]]
+                self.evictions += 1
+            self.owner[s] = (layer, e)
+            self.where[(layer, e)] = s
+            self.clock += 1
+            self.stamp[s] = self.clock
+            result[e] = s
+        for e in miss_ids:
+            result.setdefault(e, -1)
+        self.pf_queries += len(req)
+        self.pf_hits += len(hit_ids)
+        self.pf_fills += len(admitted)
+        return result
 
 
 def slots_for_budget(budget_bytes: int, per_expert_bytes: Iterable[int], k: int) -> List[int]:

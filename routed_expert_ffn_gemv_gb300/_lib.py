@@ -40,6 +40,7 @@ EXPORTED = [
     "moe_set_decode_fused", "moe_get_decode_fused",
     "moe_expert_ffn_noalloc", "moe_combine_rmsnorm", "moe_cache_state_bytes", "moe_cache_plan",
     "moe_expert_ffn_fill", "moe_last_cuda_error", "moe_router_topk_threshold",
+    "moe_cache_prefetch_plan", "moe_cache_prefetch_fill",
 ]
 MOE_NOALLOC_SCRATCH_MAX = 8 << 20
 
@@ -69,14 +70,18 @@ class CacheStats(ctypes.Structure):
                 ("misses", ctypes.c_uint64 * 2), ("evictions", ctypes.c_uint64),
                 ("h2d_bytes", ctypes.c_uint64), ("route_queries", ctypes.c_uint64),
                 ("route_hits", ctypes.c_uint64), ("ensure_calls", ctypes.c_uint64),
-                ("bypassed", ctypes.c_uint64), ("window_evictions", ctypes.c_uint64)]
+                ("bypassed", ctypes.c_uint64), ("window_evictions", ctypes.c_uint64),
+                ("prefetch_queries", ctypes.c_uint64), ("prefetch_hits", ctypes.c_uint64),
+                ("prefetch_fills", ctypes.c_uint64), ("prefetch_aborts", ctypes.c_uint64)]
 
     def as_dict(self):
         return {"queries": list(self.queries), "hits": list(self.hits), "misses": list(self.misses),
                 "evictions": self.evictions, "h2d_bytes": self.h2d_bytes,
                 "route_queries": self.route_queries, "route_hits": self.route_hits,
                 "ensure_calls": self.ensure_calls, "bypassed": self.bypassed,
-                "window_evictions": self.window_evictions}
+                "window_evictions": self.window_evictions, "prefetch_queries": self.prefetch_queries,
+                "prefetch_hits": self.prefetch_hits, "prefetch_fills": self.prefetch_fills,
+                "prefetch_aborts": self.prefetch_aborts}
 
 
 class StackDesc(ctypes.Structure):
@@ -85,7 +90,7 @@ class StackDesc(ctypes.Structure):
                 ("n_groups", _i), ("caches", ctypes.POINTER(_vp)), ("resident_pool", _vp),
                 ("shared_pool", _vp), ("slot_bytes", _sz), ("max_T", _i), ("workspace", _vp),
                 ("ws_bytes", _sz), ("overlap", _i), ("profile", _i), ("device_managed", _i),
-                ("use_graph", _i), ("load_threshold", ctypes.c_float)]
+                ("use_graph", _i), ("load_threshold", ctypes.c_float), ("prefetch_depth", _i)]
 
 
 class StackProfile(ctypes.Structure):
@@ -151,6 +156,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_combine_rmsnorm": ([_vp, _i, _i, _i, _vp, _vp, _vp, ctypes.c_float, _vp], _i),
         "moe_cache_state_bytes": ([_i, _i, _i, P(_sz)], _i),
         "moe_cache_plan": ([_vp, _i, _vp, _i, _i, _vp, _vp, _vp], _i),
+        "moe_cache_prefetch_plan": ([_vp, _i, _vp, _i, _i, _vp, _vp, _vp], _i),
+        "moe_cache_prefetch_fill": ([_vp, _vp, _vp, _vp], _i),
         "moe_expert_ffn_fill": ([_vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _sz, _vp, _vp, _vp,
                                  _sz, _vp], _i),
         "moe_device_status": ([P(_i), _i], _i),
@@ -269,6 +276,17 @@ def moe_cache_plan(cache: int, layer: int, d_ids, n_tokens: int, k: int, d_table
                    stream=None) -> None:
     _ck("moe_cache_plan", load().moe_cache_plan(cache, layer, _ptr(d_ids), n_tokens, k, _ptr(d_table),
                                                 _ptr(d_fill_src), _stream(stream)))
+
+
+def moe_cache_prefetch_plan(cache: int, layer: int, d_ids, n_tokens: int, k: int, d_table, d_fill_src,
+                            stream=None) -> None:
+    _ck("moe_cache_prefetch_plan", load().moe_cache_prefetch_plan(cache, layer, _ptr(d_ids), n_tokens, k,
+                                                                  _ptr(d_table), _ptr(d_fill_src), _stream(stream)))
+
+
+def moe_cache_prefetch_fill(cache: int, d_table, d_fill_src, stream=None) -> None:
+    _ck("moe_cache_prefetch_fill", load().moe_cache_prefetch_fill(cache, _ptr(d_table), _ptr(d_fill_src),
+                                                                  _stream(stream)))
 
 
 def moe_expert_ffn_fill(x, xtype: int, T: int, H: int, F: int, qtype: int, E: int, k: int, ids, weights,

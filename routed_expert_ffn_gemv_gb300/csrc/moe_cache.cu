@@ -87,11 +87,13 @@ struct DevHeader {
     int32_t n_filled, head, tail, pad;
     uint64_t queries[2], hits[2], misses[2], evictions, h2d_bytes, route_queries, route_hits, ensure_calls;
     uint64_t bypassed, window_evictions;
+    uint64_t pf_queries, pf_hits, pf_fills, pf_aborts;  // speculative (prefetch) requests
+    uint32_t epoch, pad2;                                // real requests so far
 };
 static_assert(sizeof(DevHeader) <= 256, "device header");
 
 struct DevLayout {
-    size_t slot_of, owner, prev, next, img, count, total;
+    size_t slot_of, owner, prev, next, img, count, recent, total;
 };
 
 DevLayout dev_layout(int n_layers, int E, int n_slots) {
@@ -104,6 +106,7 @@ DevLayout dev_layout(int n_layers, int E, int n_slots) {
     L.next = o;    o += ((size_t)n_slots * 4 + 15) / 16 * 16;
     L.img = o;     o += nk * 8;
     L.count = o;   o += (nk * 4 + 15) / 16 * 16;
+    L.recent = o;  o += ((size_t)n_slots * 4 + 15) / 16 * 16;  // epoch of the last real request using a slot
     L.total = (o + 255) / 256 * 256;
     return L;
 }
@@ -112,7 +115,7 @@ DevLayout dev_layout(int n_layers, int E, int n_slots) {
 
 __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, DevLayout L, int ll, int E,
                                                    int n_slots, const int32_t *__restrict__ ids, int n_tokens,
-                                                   int k, uint64_t image_bytes, int theta,
+                                                   int k, uint64_t image_bytes, int theta, int speculative,
                                                    int32_t *__restrict__ table_out,
                                                    uint64_t *__restrict__ src_out, int *status) {
     // Everything is read once into shared memory (one round of loads), the list is updated
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     int32_t *owner = sm, *prev = sm + n_slots, *next = sm + 2 * n_slots, *slot_l = sm + 3 * n_slots;
     uint32_t *cnt_l = (uint32_t *)(slot_l + E);  // accesses of the layer's experts (admission)
     unsigned char *want = (unsigned char *)(cnt_l + E), *miss = want + E;
-    __shared__ int abort_flag, route_hits, commit, s_head, s_tail;
+    __shared__ int abort_flag, abort_invalid, route_hits, commit, s_head, s_tail;
     __shared__ int wsum[8];
     __shared__ int32_t vict[MOE_MAX_E], app[MOE_MAX_E];
     unsigned char *in_s = miss + E;  // hit slots (n_slots bytes)
@@ -135,6 +138,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     int32_t *g_next = (int32_t *)(state + L.next);
     const uint64_t *g_img = (const uint64_t *)(state + L.img);
     uint32_t *g_count = (uint32_t *)(state + L.count);
+    uint32_t *g_recent = (uint32_t *)(state + L.recent);
     const int key0 = ll * E, n_ids = n_tokens * k;
     const int n_keys = (int)((L.owner - L.slot_of) / 4);  // entries the slot_of region holds
     pdl_wait();  // ids and the pool state come from earlier kernels
@@ -157,6 +161,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
         ((int32_t *)&s_hd)[i] = ((const int32_t *)hd)[i];
     if (threadIdx.x == 0) {
         abort_flag = 0;
+        abort_invalid = 0;
         route_hits = 0;
         commit = 0;
     }
@@ -167,6 +172,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
         if (e < 0 || e >= E) {
             moe_set_status(status, MOE_ERR_INVALID);
             abort_flag = 1;
+            abort_invalid = 1;
         } else {
             want[e] = 1;
         }
@@ -178,6 +184,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     const bool hit_t = w_t && slot_l[e_t] >= 0;
     // a miss takes a slot once the expert's accesses (this one included) reach theta; before
     // that it is bypassed: read from its host image, no slot, no LRU change
+    // (a speculative request admits what the real access would, but stores no access count)
     const uint32_t c_t = e_t < E ? cnt_l[e_t] + (w_t ? 1u : 0u) : 0u;
     const bool miss_any = w_t && slot_l[e_t] < 0;
     const bool miss_t = miss_any && c_t >= (uint32_t)theta, byp_t = miss_any && !miss_t;
@@ -209,7 +216,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
         nm = all >> 16;
     }
     if (threadIdx.x == 0 && !abort_flag && nd > n_slots) {
-        moe_set_status(status, MOE_ERR_CAPACITY);
+        if (!speculative) moe_set_status(status, MOE_ERR_CAPACITY);  // a prefetch just gives up
         abort_flag = 1;
     }
     if (threadIdx.x == 0) {
@@ -268,6 +275,12 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
                     corrupt();
                     break;
                 }
+                // a prefetch never takes a slot of the last real request: that layer's kernels
+                // may still be reading it (or writing it through) while the prefetch copies
+                if (speculative && g_recent[sv] == s_hd.epoch && s_hd.epoch != 0u) {
+                    abort_flag = 1;
+                    break;
+                }
                 vict[i] = sv;
                 sv = next[sv];
             }
@@ -296,6 +309,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
             }
             if (hit_t) app[rh] = slot_l[e_t];
             const int old_tail = s_tail;
+            const uint32_t ep_new = s_hd.epoch + 1u;  // read before thread 0 advances it below
             __syncthreads();
             // (4) append them at the tail
             const int na = nh + nm;
@@ -310,6 +324,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
                 miss[e_t] = 1;
             }
             if (byp_t) miss[e_t] = 1;
+            if (!speculative && (hit_t || miss_t)) g_recent[slot_l[e_t]] = ep_new;  // the slots of this request
             if (threadIdx.x == 0) {
                 if (na > 0) {
                     if (old_tail >= 0) next[old_tail] = app[0];
@@ -320,26 +335,38 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
                 s_hd.head = s_head;
                 s_hd.tail = s_tail;
                 s_hd.n_filled = min(n_slots, filled + nm);
-                const int b = n_tokens <= 8 ? 0 : 1;
-                s_hd.queries[b] += nh + nm + nbyp;
-                s_hd.hits[b] += nh;
-                s_hd.misses[b] += nm + nbyp;
-                s_hd.evictions += m_evict;
-                s_hd.bypassed += nbyp;
-                s_hd.h2d_bytes += (uint64_t)(nm + nbyp) * image_bytes;  // read from host memory
-                s_hd.route_queries += n_real;
-                s_hd.ensure_calls += 1;
+                if (speculative) {  // a prefetch: the same LRU rules, its own counters
+                    s_hd.pf_queries += nh + nm + nbyp;
+                    s_hd.pf_hits += nh;
+                    s_hd.pf_fills += nm;
+                    s_hd.evictions += m_evict;
+                    s_hd.h2d_bytes += (uint64_t)nm * image_bytes;  // copied by the prefetch
+                } else {
+                    const int b = n_tokens <= 8 ? 0 : 1;
+                    s_hd.queries[b] += nh + nm + nbyp;
+                    s_hd.hits[b] += nh;
+                    s_hd.misses[b] += nm + nbyp;
+                    s_hd.evictions += m_evict;
+                    s_hd.bypassed += nbyp;
+                    s_hd.h2d_bytes += (uint64_t)(nm + nbyp) * image_bytes;  // read from host memory
+                    s_hd.route_queries += n_real;
+                    s_hd.ensure_calls += 1;
+                    s_hd.epoch += 1;
+                }
             }
         }
     }
     __syncthreads();
-    if (commit) {  // routes whose expert was resident before this call (every id is valid here)
+    if (threadIdx.x == 0 && speculative && !commit && !abort_invalid) ((DevHeader *)state)->pf_aborts += 1;
+    if (commit && !speculative) {  // routes whose expert was resident before this call (ids valid here)
         int h = 0;
         for (int i = threadIdx.x; i < n_ids; i += blockDim.x) h += s_ids[i] >= 0 && !miss[s_ids[i]];
         if (h) atomicAdd(&route_hits, h);
         __syncthreads();
         if (threadIdx.x == 0) s_hd.route_hits += route_hits;
-        __syncthreads();
+    }
+    __syncthreads();
+    if (commit) {
         for (int i = threadIdx.x; i < (int)(sizeof(DevHeader) / 4); i += blockDim.x)
             ((int32_t *)hd)[i] = ((const int32_t *)&s_hd)[i];
         for (int i = threadIdx.x; i < n_slots; i += blockDim.x) {
@@ -351,7 +378,7 @@ __global__ void __launch_bounds__(256) plan_kernel(uint8_t *__restrict__ state, 
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         if (commit) {
             g_slot_of[key0 + e] = slot_l[e];
-            if (want[e]) g_count[key0 + e] = cnt_l[e] + 1u;
+            if (want[e] && !speculative) g_count[key0 + e] = cnt_l[e] + 1u;
         }
         table_out[e] = commit ? slot_l[e] : -1;
         src_out[e] = (commit && miss[e]) ? s_img[e] : 0ull;  // admitted misses and bypassed
@@ -386,8 +413,8 @@ extern "C" int moe_cache_state_bytes(int n_layers, int n_experts, int n_slots, s
     return MOE_OK;
 }
 
-extern "C" int moe_cache_plan(moe_cache *c, int layer, const int32_t *d_ids, int n_tokens, int k,
-                              int32_t *d_table_out, uint64_t *d_fill_src_out, moe_stream_t s) {
+static int plan_launch(moe_cache *c, int layer, const int32_t *d_ids, int n_tokens, int k, int32_t *d_table_out,
+                       uint64_t *d_fill_src_out, moe_stream_t s, int speculative) {
     MOE_CHECK(c && c->d.device_managed && d_ids && d_table_out && d_fill_src_out);
     MOE_CHECK(n_tokens >= 1 && n_tokens <= MOE_DECODE_MAX_T && k >= 1 && k <= MOE_MAX_K);
     const moe_cache_desc &d = c->d;
@@ -416,8 +443,57 @@ extern "C" int moe_cache_plan(moe_cache *c, int layer, const int32_t *d_ids, int
     cudaLaunchAttribute attr[1];
     moe_pdl_config(&cfg, attr, dim3(1), dim3(256), smem, moe_cuda_stream(s));
     MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, plan_kernel, (uint8_t *)d.device_state, L, ll, d.n_experts, d.n_slots,
-                                    d_ids, n_tokens, k, c->image_bytes, std::max(1, d.admit_after), d_table_out,
-                                    d_fill_src_out, moe_status_word_device_ptr()));
+                                    d_ids, n_tokens, k, c->image_bytes, std::max(1, d.admit_after), speculative,
+                                    d_table_out, d_fill_src_out, moe_status_word_device_ptr()));
+    MOE_TRY_CUDA(cudaGetLastError());
+    return MOE_OK;
+}
+
+extern "C" int moe_cache_plan(moe_cache *c, int layer, const int32_t *d_ids, int n_tokens, int k,
+                              int32_t *d_table_out, uint64_t *d_fill_src_out, moe_stream_t s) {
+    return plan_launch(c, layer, d_ids, n_tokens, k, d_table_out, d_fill_src_out, s, 0);
+}
+
+extern "C" int moe_cache_prefetch_plan(moe_cache *c, int layer, const int32_t *d_ids, int n_tokens, int k,
+                                       int32_t *d_table_out, uint64_t *d_fill_src_out, moe_stream_t s) {
+    return plan_launch(c, layer, d_ids, n_tokens, k, d_table_out, d_fill_src_out, s, 1);
+}
+
+namespace {
+// Copies each expert's pinned host image (src[e] != 0) into its slot (table[e] >= 0): the CTAs
+// split the experts' images into 16-byte pieces, eight in flight per thread.
+__global__ void __launch_bounds__(256) prefetch_fill_kernel(const int32_t *__restrict__ table,
+                                                            const uint64_t *__restrict__ src, int E,
+                                                            uint8_t *__restrict__ pool, size_t slot_bytes,
+                                                            size_t image_bytes, int n_slots) {
+    const size_t n16 = image_bytes / 16;
+    for (int e = 0; e < E; ++e) {
+        const uint64_t sp = src[e];
+        const int sl = table[e];
+        if (sp == 0ull || sl < 0 || sl >= n_slots) continue;
+        const uint4 *from = (const uint4 *)(uintptr_t)sp;
+        uint4 *to = (uint4 *)(pool + (size_t)sl * slot_bytes);
+        const size_t stride = (size_t)gridDim.x * blockDim.x;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += 8 * stride) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i + u * stride < n16) v[u] = __ldcs(from + i + u * stride);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i + u * stride < n16) __stcg(to + i + u * stride, v[u]);
+        }
+    }
+}
+}  // namespace
+
+extern "C" int moe_cache_prefetch_fill(moe_cache *c, const int32_t *d_table, const uint64_t *d_fill_src,
+                                       moe_stream_t s) {
+    MOE_CHECK(c && c->d.device_managed && d_table && d_fill_src);
+    MOE_CHECK((c->image_bytes % 16) == 0);
+    prefetch_fill_kernel<<<64, 256, 0, moe_cuda_stream(s)>>>(d_table, d_fill_src, c->d.n_experts,
+                                                            (uint8_t *)c->d.device_pool, c->d.slot_bytes,
+                                                            c->image_bytes, c->d.n_slots);
     MOE_TRY_CUDA(cudaGetLastError());
     return MOE_OK;
 }
@@ -694,6 +770,10 @@ extern "C" int moe_cache_stats_get(const moe_cache *c, moe_cache_stats *out) {
         st.ensure_calls = h.ensure_calls;
         st.bypassed = h.bypassed;
         st.window_evictions = h.window_evictions;
+        st.prefetch_queries = h.pf_queries;
+        st.prefetch_hits = h.pf_hits;
+        st.prefetch_fills = h.pf_fills;
+        st.prefetch_aborts = h.pf_aborts;
         *out = st;
         return MOE_OK;
     }

@@ -21,8 +21,8 @@ namespace {
 inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct StackWs {
-    size_t ids, w, partial, table, hit, miss, hA, hB, xn, ids_s, w_s, partial_s, tmp, fill, gin, gout, nact, ffn,
-        total;
+    size_t ids, w, partial, table, hit, miss, hA, hB, xn, ids_s, w_s, partial_s, tmp, fill, gin, gout, nact,
+        pf_ids, pf_w, pf_table, pf_fill, ffn, total;
     size_t ffn_bytes;
 };
 
@@ -47,6 +47,10 @@ StackWs stack_ws(int H, int F, int qtype, int E, int k, int T, int n_shared) {
     L.gin = off;       off = align256(off + (size_t)T * H * 4);
     L.gout = off;      off = align256(off + (size_t)T * H * 4);
     L.nact = off;      off = align256(off + 8);
+    L.pf_ids = off;    off = align256(off + 2 * (size_t)T * k * 4);   // predicted ids, depth 1 and 2
+    L.pf_w = off;      off = align256(off + 2 * (size_t)T * k * 4);
+    L.pf_table = off;  off = align256(off + 2 * (size_t)E * 4);
+    L.pf_fill = off;   off = align256(off + 2 * (size_t)E * 8);
     size_t f = moe_decode_workspace_bytes(T, H, F, qtype, E, k);
     if (ns > 0) {
         const size_t f2 = moe_decode_workspace_bytes(T, H, F, qtype, ns, ns);
@@ -89,6 +93,10 @@ struct moe_stack {
     uint64_t graph_launches[MOE_DECODE_MAX_T + 1] = {};  // kernels per captured step
     bool eager_done[MOE_DECODE_MAX_T + 1] = {};
     uint64_t nact_pending = 0;  // routed FFN calls counted on the device since the last harvest
+    // cross-layer prefetch: side stream and the events ordering it against the layer's stream
+    cudaStream_t pf_stream = nullptr;
+    cudaEvent_t pf_fork = nullptr, pf_rdone = nullptr, pf_pdone = nullptr, pf_fdone = nullptr;
+    bool pf_pending = false;  // side work forked by the previous layer not yet joined
 };
 
 namespace {
@@ -199,6 +207,58 @@ int ffn_call(moe_stack *st, const float *x, int T, int E, int k, const int32_t *
 // RMSNorm epsilon of the stack's pre-norm
 #define MOE_STACK_EPS 1e-6f
 
+// Cross-layer speculative prefetch (page 3, tiered MoE scheduling note, section 2.3: while the
+// GPU computes the current layer a second stream prefetches the experts the next one or two
+// layers will use; section 4.3: depth 2).  After layer `layer`'s plan: the routers of the next
+// `prefetch_depth` layers are applied to this layer's input x (their prediction), their pools
+// plan the predicted ids speculatively, and the predicted misses are copied into their slots —
+// all on the side stream, ordered by events: the main stream waits for the routers before x
+// is overwritten (the combine), for the plans before the next plan, for the copies before the
+// next FFN.
+int prefetch_fork(moe_stack *st, int layer, const float *x, int T, cudaStream_t s) {
+    const moe_stack_desc &d = st->d;
+    const StackWs &L = st->L;
+    int targets[2], n = 0;
+    for (int dd = 1; dd <= d.prefetch_depth && dd <= 2; ++dd) {
+        const int l2 = layer + dd;
+        if (l2 < d.n_layers && st->group_of_layer[l2] >= 0) targets[n++] = l2;
+    }
+    if (n == 0) return MOE_OK;
+    if (!st->pf_stream) {
+        MOE_TRY_CUDA(cudaStreamCreateWithFlags(&st->pf_stream, cudaStreamNonBlocking));
+        for (cudaEvent_t *e : {&st->pf_fork, &st->pf_rdone, &st->pf_pdone, &st->pf_fdone})
+            MOE_TRY_CUDA(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+    }
+    cudaStream_t ps = st->pf_stream;
+    const size_t R = (size_t)T * d.k;
+    int32_t *pids = (int32_t *)(st->ws + L.pf_ids);
+    float *pw = (float *)(st->ws + L.pf_w);
+    int32_t *ptab = (int32_t *)(st->ws + L.pf_table);
+    uint64_t *pfill = (uint64_t *)(st->ws + L.pf_fill);
+    MOE_TRY_CUDA(cudaEventRecord(st->pf_fork, s));
+    MOE_TRY_CUDA(cudaStreamWaitEvent(ps, st->pf_fork, 0));
+    int rc;
+    for (int i = 0; i < n; ++i)
+        if ((rc = moe_router_topk_threshold(x, MOE_F32, T, d.H, st->w_router[targets[i]], st->bias[targets[i]], d.E,
+                                            d.k, d.load_threshold, pids + i * R, pw + i * R, nullptr,
+                                            (moe_stream_t)ps)))
+            return rc;
+    MOE_TRY_CUDA(cudaEventRecord(st->pf_rdone, ps));
+    for (int i = 0; i < n; ++i)
+        if ((rc = moe_cache_prefetch_plan(st->caches[st->group_of_layer[targets[i]]], targets[i], pids + i * R, T,
+                                          d.k, ptab + i * d.E, pfill + i * d.E, (moe_stream_t)ps)))
+            return rc;
+    MOE_TRY_CUDA(cudaEventRecord(st->pf_pdone, ps));
+    for (int i = 0; i < n; ++i)
+        if ((rc = moe_cache_prefetch_fill(st->caches[st->group_of_layer[targets[i]]], ptab + i * d.E,
+                                          pfill + i * d.E, (moe_stream_t)ps)))
+            return rc;
+    MOE_TRY_CUDA(cudaEventRecord(st->pf_fdone, ps));
+    st->prof.kernel_launches += 3 * n;
+    st->pf_pending = true;
+    return MOE_OK;
+}
+
 // One layer: y = h + MoE(RMSNorm(h)).  norm_in: compute RMSNorm(h) here (else the previous
 // layer's combine left it in the xn buffer); norm_out: leave RMSNorm(y) in xn for the next.
 int layer_step(moe_stack *st, int layer, const float *h, float *y, int T, int32_t *ids_out,
@@ -228,12 +288,23 @@ int layer_step(moe_stack *st, int layer, const float *h, float *y, int T, int32_
     if ((rc = end_timed(st, s, K_ROUTER, ep))) return rc;
 
     const int g = st->group_of_layer[layer];
+    bool forked = false;
     if (g >= 0 && d.device_managed) {
         // the pool's bookkeeping on the GPU, then the FFN filling the missed experts' slots
         moe_cache *c = st->caches[g];
         uint64_t *fill = (uint64_t *)(st->ws + L.fill);
+        // the previous layer's speculative plans come before this plan
+        if (st->pf_pending) MOE_TRY_CUDA(cudaStreamWaitEvent(s, st->pf_pdone, 0));
         if ((rc = moe_cache_plan(c, layer, ids_d, T, d.k, table, fill, (moe_stream_t)s))) return rc;
         st->prof.kernel_launches += 1;
+        if (st->pf_pending) {  // and its copies land before this FFN reads the slots
+            MOE_TRY_CUDA(cudaStreamWaitEvent(s, st->pf_fdone, 0));
+            st->pf_pending = false;
+        }
+        if (d.prefetch_depth > 0) {
+            if ((rc = prefetch_fork(st, layer, x, T, s))) return rc;
+            forked = st->pf_pending;
+        }
         int ns = 0;
         const void *pool = moe_cache_pool(c, &ns);
         if ((rc = ffn_call(st, x, T, d.E, d.k, ids_d, w_d, table, ns, pool, nullptr, 0, partial, -1, s, fill)))
@@ -330,6 +401,7 @@ int layer_step(moe_stack *st, int layer, const float *h, float *y, int T, int32_
         if ((rc = end_timed(st, s, K_COMBINE, ep))) return rc;
         extra = tmp;
     }
+    if (forked) MOE_TRY_CUDA(cudaStreamWaitEvent(s, st->pf_rdone, 0));  // the predictions read x
     if ((rc = begin_timed(st, s, &ep))) return rc;
     if ((rc = moe_combine_rmsnorm_routes(partial, d.load_threshold > 0.f ? ids_d : nullptr, T, d.k, d.H, extra, y,
                                          norm_out ? x : nullptr, MOE_STACK_EPS, s)))
@@ -369,6 +441,9 @@ extern "C" int moe_stack_create(const moe_stack_desc *desc, moe_stack **out) {
     if (d.n_groups == 0) MOE_CHECK(d.resident_pool != nullptr);
     else MOE_CHECK(d.caches != nullptr);
     if (d.n_shared > 0) MOE_CHECK(d.shared_pool != nullptr);
+    MOE_CHECK(d.prefetch_depth >= 0 && d.prefetch_depth <= 2);
+    MOE_CHECK(d.load_threshold >= 0.f && d.load_threshold <= 1.f);
+    if (d.prefetch_depth > 0 && !(d.device_managed && d.n_groups > 0)) return MOE_ERR_UNSUPPORTED;
 
     moe_stack *st = new moe_stack();
     st->d = d;
@@ -428,7 +503,12 @@ extern "C" int moe_stack_layer(moe_stack *st, int layer, const float *x_in, floa
     MOE_CHECK(T >= 1 && T <= st->d.max_T);
     cudaStream_t cs = moe_cuda_stream(s);
     st->last_stream = cs;
-    return layer_step(st, layer, x_in, y_out, T, ids_host_out, weights_host_out, cs, true, false);
+    const int rc = layer_step(st, layer, x_in, y_out, T, ids_host_out, weights_host_out, cs, true, false);
+    if (rc == MOE_OK && st->pf_pending) {  // a single layer leaves no work behind on the side stream
+        MOE_TRY_CUDA(cudaStreamWaitEvent(cs, st->pf_fdone, 0));
+        st->pf_pending = false;
+    }
+    return rc;
 }
 
 namespace {
@@ -446,6 +526,10 @@ int run_step(moe_stack *st, const float *x_in, float *y_out, int T, int32_t *ids
                                   l + 1 < L);
         if (rc) return rc;
         cur = out;
+    }
+    if (st->pf_pending) {  // every side-stream copy joins the step
+        MOE_TRY_CUDA(cudaStreamWaitEvent(cs, st->pf_fdone, 0));
+        st->pf_pending = false;
     }
     return MOE_OK;
 }
@@ -648,6 +732,10 @@ extern "C" void moe_stack_destroy(moe_stack *st) {
     for (int t = 0; t <= MOE_DECODE_MAX_T; ++t)
         if (st->graph[t]) cudaGraphExecDestroy(st->graph[t]);
     if (st->cap_stream) cudaStreamDestroy(st->cap_stream);
+    if (st->pf_stream) cudaStreamSynchronize(st->pf_stream);
+    for (cudaEvent_t e : {st->pf_fork, st->pf_rdone, st->pf_pdone, st->pf_fdone})
+        if (e) cudaEventDestroy(e);
+    if (st->pf_stream) cudaStreamDestroy(st->pf_stream);
     if (st->ids_ready) cudaEventDestroy(st->ids_ready);
     if (st->ids_h) cudaFreeHost(st->ids_h);
     if (st->slots_h) cudaFreeHost(st->slots_h);

@@ -71,7 +71,7 @@ class Stack:
                  n_layers: Optional[int] = None, random_scales: bool = False,
                  resident: bool = False, device_managed: bool = False, use_graph: bool = False,
                  images: Optional[PinnedImages] = None, admit_after: int = 0, lru_window: int = 0,
-                 load_threshold: float = 0.0):
+                 load_threshold: float = 0.0, prefetch_depth: int = 0):
         self.cfg = cfg
         self.L = n_layers or cfg.L
         self.max_T = max_T or max(cfg.tokens)
@@ -151,7 +151,8 @@ class Stack:
                            slot_bytes=self.stride, max_T=self.max_T, workspace=self.workspace.data_ptr(),
                            ws_bytes=ws, overlap=int(overlap), profile=int(profile),
                            device_managed=int(device_managed and bool(self.caches)),
-                           use_graph=int(use_graph), load_threshold=float(load_threshold))
+                           use_graph=int(use_graph), load_threshold=float(load_threshold),
+                           prefetch_depth=int(prefetch_depth))
         torch.cuda.synchronize()
         self.handle = L.moe_stack_create(desc)
 

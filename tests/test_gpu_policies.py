@@ -252,3 +252,66 @@ def test_load_threshold_stack_layers_match_oracle():
     assert stt["route_queries"] == kept
     print(f"load threshold {th}: {dropped} of {dropped + kept} routes dropped")
     st.close()
+
+
+def test_cross_layer_prefetch_follows_simulator_and_keeps_values():
+    """Cross-layer speculative prefetch (page 3, sections 2.3 and 4.3, depth 2) on the
+    Granite-shaped stack, device-managed pool, batch 8, layer by layer for 3 steps: outputs
+    bit-identical to the plain device-managed stack; the pool bit-exact against the simulator
+    fed each layer's real ids and the predicted ids of the next two layers (the next layers'
+    routers on this layer's normalised input, recomputed here with the same kernels); then
+    the same steps as graph-replayed decode steps from an empty pool end in the same state."""
+    cfg = synth.config(1)
+    T = 8
+    plain = _stack(cfg, max_T=T, device_managed=True)
+    pf = _stack(cfg, max_T=T, device_managed=True, images=plain.images, prefetch_depth=2)
+    sim = LRUSim(cfg.groups[0].n_slots)
+    xn = torch.empty((T, cfg.H), dtype=torch.float32, device=dev())
+    pid = torch.empty((T, cfg.k), dtype=torch.int32, device=dev())
+    pw = torch.empty((T, cfg.k), dtype=torch.float32, device=dev())
+    finals = []
+    for step in range(3):
+        h = torch.from_numpy(synth.tokens_x(cfg, 800 + step, T)).to(dev())
+        for layer in range(cfg.L):
+            ya, yb = torch.empty_like(h), torch.empty_like(h)
+            ids = np.empty((T, cfg.k), dtype=np.int32)
+            plain.layer(layer, h, ya)
+            pf.layer(layer, h, yb, ids)
+            torch.cuda.synchronize()
+            assert torch.equal(ya, yb), (step, layer)
+            sim.ensure(layer, ids.reshape(-1), n_tokens=T)
+            L.moe_combine_rmsnorm(None, T, 0, cfg.H, h, None, xn)   # the stack's pre-norm of h
+            for dd in (1, 2):
+                l2 = layer + dd
+                if l2 >= cfg.L:
+                    break
+                L.moe_router_topk(xn, 0, T, cfg.H, pf.w_router[l2], pf.bias[l2], cfg.E, cfg.k, pid, pw)
+                torch.cuda.synchronize()
+                sim.prefetch(l2, pid.cpu().numpy().reshape(-1))
+            c = pf.caches[0]
+            for e in set(ids.reshape(-1).tolist()):
+                assert L.moe_cache_lookup(c, layer, e) == sim.where.get((layer, e), -1), (step, layer, e)
+            h = yb
+        finals.append(h.clone())
+    assert L.moe_device_status(clear=True) == 0
+    st = pf.cache_stats()[0]
+    assert sum(st["hits"]) == sim.hits and sum(st["misses"]) == sim.misses and st["evictions"] == sim.evictions
+    assert (st["prefetch_queries"], st["prefetch_hits"], st["prefetch_fills"], st["prefetch_aborts"]) == \
+        (sim.pf_queries, sim.pf_hits, sim.pf_fills, sim.pf_aborts)
+    assert sim.pf_fills > 0
+    for layer in range(cfg.L):
+        for e in range(cfg.E):
+            assert L.moe_cache_lookup(pf.caches[0], layer, e) == sim.where.get((layer, e), -1)
+    print(f"prefetch: {sim.pf_queries} predicted, {sim.pf_hits} already resident, {sim.pf_fills} copied, "
+          f"{sim.pf_aborts} abandoned; real hits {sim.hits} of {sim.hits + sim.misses}")
+    # the same steps as decode steps (eager first, then graph replay) from an empty pool
+    g = _stack(cfg, max_T=T, device_managed=True, use_graph=True, images=plain.images, prefetch_depth=2)
+    y = torch.empty((T, cfg.H), dtype=torch.float32, device=dev())
+    for step in range(3):
+        g.decode(torch.from_numpy(synth.tokens_x(cfg, 800 + step, T)).to(dev()), y)
+        torch.cuda.synchronize()
+        assert torch.equal(y, finals[step]), step
+    assert g.cache_stats() == pf.cache_stats()
+    assert L.moe_device_status(clear=True) == 0
+    for s_ in (g, pf, plain):
+        s_.close()

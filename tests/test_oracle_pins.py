@@ -482,3 +482,39 @@ def test_load_threshold_drops_light_routes_without_renormalising():
     # threshold 0 changes nothing; above every weight only shared experts would remain
     np.testing.assert_allclose(oracle.moe_layer(0, 64, 64, 4, x, wr, b, ex, load_threshold=0.0).y, full.y, rtol=0, atol=0)
     assert np.all(oracle.moe_layer(0, 64, 64, 4, x, wr, b, ex, load_threshold=1.01).y == 0.0)
+
+
+def test_lru_prefetch_hand_trace():
+    """Speculative requests (page 3, section 2.3, cross-layer prefetch): the same LRU rules,
+    their own statistics, abandoned when a victim would be a slot of the last real request.
+    Derived by hand (stamps in brackets):
+      1 real (0,[0])      -> 0:s0 [1]                        last real {s0}
+      2 pf   (1,[5])      -> 5:s1 [2] (free slot)
+      3 real (0,[1])      -> 1:s2 [3]                        last real {s2}
+      4 pf   (1,[5,6])    -> 5 hit s1 [4]; 6 evicts s0 (oldest, not s2) [5]
+      5 real (1,[6])      -> hit s0 [6]                      last real {s0}
+      6 pf   (2,[7])      -> evicts s2 [3] -> 7:s2 [7]
+      7 real (0,[0,1])    -> 0 evicts s1 [4] -> s1 [8]; 1 evicts s0 [6] -> s0 [9]; last real {s1, s0}
+      8 pf   (1,[5,6])    -> would evict s2 then s1: s1 is the last real request's -> abandoned"""
+    sim = LRUSim(3)
+    assert sim.ensure(0, [0])[0] == {0: 0}
+    assert sim.prefetch(1, [5]) == {5: 1}
+    assert sim.ensure(0, [1])[0] == {1: 2}
+    assert sim.prefetch(1, [5, 6]) == {5: 1, 6: 0}
+    res, hit, miss = sim.ensure(1, [6])
+    assert res == {6: 0} and hit == [6]
+    assert sim.prefetch(2, [7]) == {7: 2}
+    assert sim.ensure(0, [0, 1])[0] == {0: 1, 1: 0}
+    before = (list(sim.owner), list(sim.stamp), sim.clock)
+    assert sim.prefetch(1, [5, 6]) == {}
+    assert (list(sim.owner), list(sim.stamp), sim.clock) == before
+    assert (sim.pf_queries, sim.pf_hits, sim.pf_fills, sim.pf_aborts) == (4, 1, 3, 1)
+    assert (sim.hits, sim.misses, sim.evictions) == (1, 4, 4)
+    # admission: a prediction admits what the real access would (count + 1 >= theta) but
+    # stores no access
+    adm = LRUSim(4, admit_after=2)
+    assert adm.ensure(0, [3])[0] == {3: -1}              # count 1: bypassed
+    assert adm.prefetch(0, [3]) == {3: 0} and adm.count[(0, 3)] == 1 and adm.pf_fills == 1
+    res, hit, _ = adm.ensure(0, [3])                     # count 2, prefetched: a hit
+    assert res == {3: 0} and hit == [3]
+    assert adm.prefetch(0, [7]) == {7: -1} and adm.pf_fills == 1   # never seen: 0 + 1 < 2

@@ -341,6 +341,9 @@ POLICIES = (
     ("admit2_device", dict(device_managed=True, use_graph=True, admit_after=2)),
     ("admit4_device", dict(device_managed=True, use_graph=True, admit_after=4)),
     ("load_threshold_0.05_device", dict(device_managed=True, use_graph=True, load_threshold=0.05)),
+    # page 3 sections 2.3 / 4.3: cross-layer speculative prefetch, depth 1 and 2
+    ("prefetch1_device", dict(device_managed=True, use_graph=True, prefetch_depth=1)),
+    ("prefetch2_device", dict(device_managed=True, use_graph=True, prefetch_depth=2)),
     ("lru_host", dict()),
     ("window15_host", dict(lru_window=15)),
 )
@@ -366,7 +369,9 @@ def run_policies(torch, stream, peaks, link_gbs, warmup, total=128, T=8):
              "miss_bytes_per_step": tst["h2d_bytes"] / steps,
              "routes_per_step": tst["route_queries"] / steps,
              "bypassed_per_step": tst["bypassed"] / steps,
-             "window_evictions_per_step": tst["window_evictions"] / steps}
+             "window_evictions_per_step": tst["window_evictions"] / steps,
+             "prefetch_fills_per_step": tst["prefetch_fills"] / steps,
+             "prefetch_hits_per_step": tst["prefetch_hits"] / steps}
         e.update(hit_fields(tst))
         out[name] = e
         st.close()

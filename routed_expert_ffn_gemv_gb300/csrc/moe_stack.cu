@@ -51,10 +51,12 @@ StackWs stack_ws(int H, int F, int qtype, int E, int k, int T, int n_shared) {
     L.pf_w = off;      off = align256(off + 2 * (size_t)T * k * 4);
     L.pf_table = off;  off = align256(off + 2 * (size_t)E * 4);
     L.pf_fill = off;   off = align256(off + 2 * (size_t)E * 8);
-    size_t f = moe_decode_workspace_bytes(T, H, F, qtype, E, k);
-    if (ns > 0) {
-        const size_t f2 = moe_decode_workspace_bytes(T, H, F, qtype, ns, ns);
-        if (f2 > f) f = f2;
+    // the FFN workspace of a call depends on its token count (the gate/up K split is chosen per
+    // count), and not monotonically: size it for every batch up to T
+    size_t f = 0;
+    for (int t = 1; t <= T; ++t) {
+        f = std::max(f, moe_decode_workspace_bytes(t, H, F, qtype, E, k));
+        if (ns > 0) f = std::max(f, moe_decode_workspace_bytes(t, H, F, qtype, ns, ns));
     }
     L.ffn = off;       off = align256(off + f);
     L.ffn_bytes = f;

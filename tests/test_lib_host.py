@@ -171,3 +171,14 @@ def test_decode_gemv_mode_switch(lib):
         assert L.moe_get_decode_fused() is False
     finally:
         L.moe_set_decode_fused(before)
+
+
+def test_stack_workspace_covers_every_batch_up_to_max_T():
+    """The decode FFN workspace is not monotonic in the token count (the K split of the gate/up
+    GEMV is chosen per count): a stack sized for max_T must hold the FFN workspace of every
+    smaller batch (the Qwen-shaped layer needs more at 27 tokens than at 32)."""
+    for (q, H, F, E, k, ns) in [(1, 2048, 768, 128, 8, 0), (0, 1024, 512, 32, 8, 0), (0, 2048, 1408, 64, 2, 2)]:
+        for max_T in (1, 8, 32):
+            stack = L.moe_stack_workspace(H, F, q, E, k, max_T, ns)
+            need = max(L.moe_expert_ffn_workspace(t, H, F, q, 0, E, k) for t in range(1, max_T + 1))
+            assert stack > need, (q, H, F, E, k, max_T)

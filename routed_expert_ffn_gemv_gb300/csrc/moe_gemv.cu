@@ -118,6 +118,9 @@ inline bool gv_plan(int T, int H, int F, int qtype, int n_act_max, GvPlan *pl) {
     int ks = 1;
     while (ks < GV_KS_MAX && (long)n_act_max * RTF * ks < GV_UNITS_TARGET && NB % (2 * ks) == 0) ks *= 2;
     while (gv_slot_bytes(qtype, NB / ks, T) > GV_SLOT_MAX && NB % (2 * ks) == 0 && ks < 16) ks *= 2;
+    // and until the staged activations fit beside the smallest ring (4-bit blocks leave less
+    // room: at hidden 2048 and 32 tokens the slot of a 2-way split does not fit)
+    while (!gv_geom(qtype, 2, NB / ks, T, &pl->g1) && NB % (2 * ks) == 0 && ks < 16) ks *= 2;
     pl->KS = ks;
     pl->TPU = RTH % 2 == 0 && (long)n_act_max * (RTH / 2) >= GV_UNITS_TARGET ? 2 : 1;
     return gv_geom(qtype, 2, NB / ks, T, &pl->g1) && gv_geom(qtype, pl->TPU, F / 32, GV_TOK, &pl->g2);

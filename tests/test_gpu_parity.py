@@ -115,6 +115,8 @@ FFN_CASES = [
     (1, 64, 96, 4, 2, 3, True, 0),
     (0, 1024, 512, 32, 8, 8, False, 0),   # Granite-shaped, K split in 2
     (1, 2048, 768, 16, 8, 4, True, 0),    # Qwen-shaped, 4-bit
+    (1, 2048, 768, 32, 8, 32, False, 0),  # Qwen-shaped at batch 32: the K split grows until the
+                                          # staged activations fit beside the ring
     (0, 2048, 1408, 8, 2, 32, False, 0),  # DeepSeek-shaped at batch 32: >8 tokens per expert
     (1, 256, 160, 6, 3, 13, True, 0),     # 5 row tiles, 13 tokens
     (0, 128, 64, 4, 4, 9, True, 1),       # bf16 activations, k = E

@@ -20,19 +20,22 @@
 //  * gather kernel: activations -> fp16 rows in position order (K permuted for 4-bit);
 //  * GEMM kernels: persistent, one CTA per SM over a strided list of work items, warp roles
 //    with mbarrier rings that run on across items:
-//      warp 0      per 64-column K stage the slab's quantised tile blocks (4-D TMA box over
-//                  the slot pool), and warp 22 the chunk's token rows (2-D TMA boxes of 64
-//                  rows x 64 columns, 128-byte swizzle, straight into the UMMA layout), both
-//                  completing the stage's one barrier;
+//      warps 0, 22 per 64-column K stage (warp 0 the even stages, warp 22 the odd ones) the
+//                  slab's quantised tile blocks (4-D TMA boxes over the slot pool) and the
+//                  chunk's token rows (2-D TMA boxes of 64 columns x 64 rows, or one box of
+//                  192 rows for a chunk of more than 128, 128-byte swizzle, straight into the
+//                  UMMA layout), completing the stage's one barrier;
 //      warps 2-17  four groups of four warps, group G taking the stages g = G mod 4: a thread
 //                  dequantises one weight row's 64 columns — integer codes to fp16 by
 //                  exponent tricks, then d*q [+ m] in one fp16 op (a single rounding) — and
 //                  stores them into its group's slot of a 4-stage ring in TMEM (tcgen05.st,
-//                  lane = weight row).  Every wait and hand-off costs a few hundred cycles
-//                  (measured), so each role keeps several stages in flight rather than
-//                  working through one stage at a time;
+//                  lane = weight row); a slot is rewritten once the MMAs of its previous
+//                  stage have completed (that stage's ring release).  Every wait and hand-off
+//                  costs a few hundred cycles (measured), so each role keeps several stages
+//                  in flight rather than working through one stage at a time;
 //      warp 1      issues the MMAs into one of two 192-column TMEM accumulators once a
-//                  stage's weights are in TMEM (its group waited for the stage's copies);
+//                  stage's weights are in TMEM (its group waited for the stage's copies),
+//                  and one commit per stage that releases both the ring stage and the slot;
 //      warps 18-21 the epilogue of the previous item from the other accumulator (lane =
 //                  weight row): GEMM 1 holds 64 gate rows in lanes 0-63 and the same 64 up
 //                  rows in 64-127; the up quarters pass their values through shared memory
@@ -63,8 +66,8 @@
 #define PF_BOX_ROWS 64     // token rows per TMA box
 #define PF_DQ_WARPS 16     // 4 groups of 4 (one warp per TMEM lane quarter)
 #define PF_EPI_WARPS 4
-#define PF_TOK_WARP (2 + PF_DQ_WARPS + PF_EPI_WARPS)  // the token producer
-#define PF_THREADS ((PF_TOK_WARP + 1) * 32)
+#define PF_PROD2_WARP (2 + PF_DQ_WARPS + PF_EPI_WARPS)  // the producer of the odd stages
+#define PF_THREADS ((PF_PROD2_WARP + 1) * 32)
 #define PF_S 6             // TMA ring stages (token rows + quantised weights)
 #define PF_AS 4            // TMEM ring stages of dequantised weights (32 columns each), one per
                            // dequant group
@@ -72,6 +75,7 @@
 #define PF_ACOL (2 * PF_NT)
 #define PF_CTRL 13312      // control block: barriers, epilogue exchange, route lists
 static_assert(PF_ACOL + PF_AS * 32 <= PF_TMEM_COLS, "TMEM budget");
+static_assert(PF_S % 2 == 0, "each ring stage keeps one producer");
 static_assert(PF_NT % 16 == 0 && PF_NT <= 256, "MMA N");
 
 namespace {
@@ -105,7 +109,8 @@ inline PfLayout pf_layout(int T, int H, int F, int E, int k) {
 
 struct PfParams {
     CUtensorMap wmap[3];  // quantised tile blocks of gate, up, down over the pool (4-D)
-    CUtensorMap tmap;     // token rows: xg (GEMM 1) or hg (GEMM 2), 2-D [R][K] fp16
+    CUtensorMap tmap;     // token rows: xg (GEMM 1) or hg (GEMM 2), 2-D [R][K] fp16, 64-row boxes
+    CUtensorMap tmap_nt;  // the same rows in PF_NT-row boxes (one copy for a chunk of > 128 rows)
     int T, H, F, k, E;
     const float *weights;
     const int32_t *ints;
@@ -143,14 +148,11 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
 __device__ __forceinline__ void red_release_add(unsigned *a, unsigned v) {
     asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(a)), "r"(v) : "memory");
 }
-__device__ __forceinline__ unsigned ld_relaxed(const unsigned *a) {
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *a) {
     unsigned v;
-    asm volatile("ld.relaxed.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(a)) : "memory");
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(a)) : "memory");
     return v;
 }
-// With a relaxed load that observed a released value before it, makes the releasing thread's
-// earlier writes visible to this thread's later accesses.
-__device__ __forceinline__ void fence_acquire_cta() { asm volatile("fence.acq_rel.cta;" ::: "memory"); }
 
 // Named barrier over `count` threads.
 __device__ __forceinline__ void named_sync(int id, int count) {
@@ -447,8 +449,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
     uint8_t *smem = align1024(smem_raw);
     uint64_t *s_full = (uint64_t *)smem;
     uint64_t *s_empty = s_full + PF_S;
-    uint64_t *a_empty = s_empty + PF_S;
-    uint64_t *acc_full = a_empty + PF_AS;
+    uint64_t *acc_full = s_empty + PF_S;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *mma_done = acc_empty + 2;
     uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
@@ -463,13 +464,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
         for (int s = 0; s < PF_S; ++s) {
-            mbar_init(&s_full[s], 2);  // the weight and the token producer
+            mbar_init(&s_full[s], 1);  // the stage's producer
             mbar_init(&s_empty[s], 1);
         }
-        for (int s = 0; s < PF_AS; ++s) {
-            mbar_init(&a_empty[s], 1);
-            a_cnt[s] = 0;
-        }
+        for (int s = 0; s < PF_AS; ++s) a_cnt[s] = 0;
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], PF_EPI_WARPS);
@@ -487,30 +485,41 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 || warp == PF_TOK_WARP) {
-        // ---------------- producers (lane 0): per K stage the slab's quantised tile blocks
-        // (warp 0) or the chunk's token rows (the token warp)
+    if (warp == 0 || warp == PF_PROD2_WARP) {
+        // ---------------- producers (lane 0): warp 0 the even K stages, the last warp the odd
+        // ones (PF_S is even, so each ring stage always has the same producer); per stage the
+        // chunk's token rows and the slab's quantised tile blocks.  A one-thread loop is bound
+        // by its own instruction latency (measured: a few hundred cycles per wait or copy
+        // issue), so two of them share the stages; each keeps its stage index and phase in
+        // registers (no division per stage).
         if (lane == 0) {
-            const bool tok = warp == PF_TOK_WARP;
+            const uint32_t mine = warp == 0 ? 0u : 1u;
             int g = 0;
+            uint32_t s = 0, ph = 0;  // ring stage of stage g, and the parity of its last release
             bool ok = true;
             for (int j = blockIdx.x; j < n_items && ok; j += gridDim.x) {
                 const int c = j / MT, m = j % MT;
                 const int slot = p.c_slot[c];
                 if (slot < 0) continue;
-                const int pos0 = p.c_pos[c], nbox = (p.c_n[c] + PF_BOX_ROWS - 1) / PF_BOX_ROWS;
+                const int pos0 = p.c_pos[c], n = p.c_n[c];
+                // a chunk of more than 128 rows comes in one PF_NT-row box, a smaller one in
+                // 64-row boxes (rows past the chunk belong to the next one or read 0: unused)
+                const bool big = n > 2 * PF_BOX_ROWS;
+                const int nbox = big ? 1 : (n + PF_BOX_ROWS - 1) / PF_BOX_ROWS;
+                const uint32_t bytes =
+                    (big ? (uint32_t)PF_NT * 128u : (uint32_t)(nbox * PF_BOX_ROWS * 128)) + (uint32_t)G::BYTES;
+                uint8_t *st = ring + (size_t)s * PG::STAGE;
                 for (int kc = 0; kc < NK; ++kc, ++g) {
-                    const int s = g % PF_S;
-                    if (g >= PF_S && !(ok = pf_wait(&s_empty[s], ((g / PF_S) - 1) & 1, p.status, abort_flag)))
-                        break;
-                    uint8_t *st = ring + (size_t)s * PG::STAGE;
-                    if (tok) {
-                        mbar_arrive_expect_tx(&s_full[s], (uint32_t)(nbox * PF_BOX_ROWS * 128));
-                        for (int b = 0; b < nbox; ++b)
-                            tma_load_2d(st + b * PF_BOX_ROWS * 128, &p.tmap, kc * PF_BK, pos0 + PF_BOX_ROWS * b,
-                                        &s_full[s]);
-                    } else {
-                        mbar_arrive_expect_tx(&s_full[s], (uint32_t)G::BYTES);
+                    if ((s & 1u) == mine) {
+                        if (g >= PF_S && !(ok = pf_wait(&s_empty[s], ph ^ 1u, p.status, abort_flag))) break;
+                        mbar_arrive_expect_tx(&s_full[s], bytes);
+                        if (big) {
+                            tma_load_2d(st, &p.tmap_nt, kc * PF_BK, pos0, &s_full[s]);
+                        } else {
+                            for (int b = 0; b < nbox; ++b)
+                                tma_load_2d(st + b * PF_BOX_ROWS * 128, &p.tmap, kc * PF_BK, pos0 + PF_BOX_ROWS * b,
+                                            &s_full[s]);
+                        }
                         if (DOWN) {
                             tma_load_4d(st + PG::TOKB, &p.wmap[2], 0, 2 * kc, 4 * m, slot, &s_full[s]);
                         } else {
@@ -518,20 +527,36 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                             tma_load_4d(st + PG::TOKB + 4 * G::TBB, &p.wmap[1], 0, 2 * kc, 2 * m, slot, &s_full[s]);
                         }
                     }
+                    if (++s == PF_S) {
+                        s = 0;
+                        ph ^= 1u;
+                        st = ring;
+                    } else {
+                        st += PG::STAGE;
+                    }
                 }
             }
-            // never leave with copies in flight: wait for the last phase issued on each stage
-            for (int s = 0; s < PF_S && s < g; ++s) {
-                const int last = s + ((g - 1 - s) / PF_S) * PF_S;
-                mbar_wait_bounded(&s_full[s], (last / PF_S) & 1, p.status);
+            // never leave with copies in flight: wait for the last phase issued on each of this
+            // producer's stages
+            for (int q = (int)mine; q < PF_S && q < g; q += 2) {
+                const int last = q + ((g - 1 - q) / PF_S) * PF_S;
+                mbar_wait_bounded(&s_full[q], (last / PF_S) & 1, p.status);
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer (lane 0).  Its loop is the kernel's critical path: a chain
+        // of dependent instructions per stage (measured ~45 clocks per tcgen05.mma issued and
+        // ~5 per dependent ALU instruction), so the stage and slot indexes, the descriptors and
+        // the dequant count a slot needs are carried in registers, and a stage costs one
+        // acquire load, one fence, four MMAs and one commit.
         if (lane == 0) {
-            int g = 0, jl = 0;
+            int jl = 0;
             bool ok = true;
-            unsigned seen = 0;  // the last value read of the next stage's dequant counter
+            uint32_t s = 0, sph = 0;  // ring stage and the parity of its current fill
+            uint32_t sa = 0, want = 4;  // TMEM slot, and the dequant count its next use needs
+            const uint64_t b_first = umma_desc_sw128(smem_u32(ring));
+            uint64_t b = b_first;
+            uint32_t a = tmem + PF_ACOL;
             for (int j = blockIdx.x; j < n_items && ok; j += gridDim.x) {
                 const int c = j / MT;
                 if (p.c_slot[c] < 0) continue;
@@ -541,18 +566,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                 if (jl >= 2 && !(ok = pf_wait(&acc_empty[buf], ((jl / 2) - 1) & 1, p.status, abort_flag))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * PF_NT;
-                for (int kc = 0; kc < NK; ++kc, ++g) {
-                    const int s = g % PF_S, sa = g % PF_AS;
+                for (int kc = 0; kc < NK; ++kc) {
                     // the stage's weights are in TMEM once its dequant group's four warps counted
-                    // themselves in (release / acquire on a shared counter: an mbarrier wait costs
-                    // hundreds of cycles here, which would idle the tensor core); the group waited
-                    // for the stage's copies (tokens included) first, so they are visible too
-                    {
-                        const unsigned want = 4u * (unsigned)(g / PF_AS + 1);
+                    // themselves in (release / acquire on a shared counter); the group waited for
+                    // the stage's copies (tokens included) first, so they are visible too
+                    if (ld_acquire(&a_cnt[sa]) < want) {
                         uint32_t i = 0;
-                        // `seen` was loaded (relaxed) before the previous stage's MMAs were issued,
-                        // so its latency is hidden behind them; reload only while it is short
-                        while (seen < want && (seen = ld_relaxed(&a_cnt[sa])) < want) {
+                        while (ld_acquire(&a_cnt[sa]) < want) {
                             if (++i >= MOE_TEST_SPIN_LIMIT) {
                                 moe_set_status(p.status, MOE_ERR_TIMEOUT);
                                 *abort_flag = 1;
@@ -564,16 +584,31 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                         }
                         if (!ok) break;
                     }
-                    fence_acquire_cta();  // the relaxed read saw the group's release
+                    // the tokens the MMAs read were landed by TMA: observe the stage's fill here too
+                    // (it completed before the dequant group counted in, so this test passes at once)
+                    if (!mbar_test_wait(&s_full[s], sph) && !(ok = pf_wait(&s_full[s], sph, p.status, abort_flag)))
+                        break;
                     tc_fence_after();
-                    const uint64_t b = umma_desc_sw128(smem_u32(ring + (size_t)s * PG::STAGE));
-                    const uint32_t a = tmem + PF_ACOL + sa * 32;
-                    seen = ld_relaxed(&a_cnt[(g + 1) % PF_AS]);  // the next stage's count, early
 #pragma unroll
                     for (int kk = 0; kk < PF_BK / 16; ++kk)
                         umma_f16_tmem_a(d, a + 8 * kk, b + 2 * kk, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(&a_empty[sa]);
+                    // one commit frees the ring stage (producers) and the TMEM slot (the dequant
+                    // group that next writes it waits for this stage's release)
                     umma_commit(&s_empty[s]);
+                    if (++s == PF_S) {
+                        s = 0;
+                        sph ^= 1u;
+                        b = b_first;
+                    } else {
+                        b += PG::STAGE >> 4;
+                    }
+                    if (++sa == PF_AS) {
+                        sa = 0;
+                        want += 4;
+                        a = tmem + PF_ACOL;
+                    } else {
+                        a += 32;
+                    }
                 }
                 if (ok) umma_commit(&acc_full[buf]);
                 ++jl;
@@ -598,11 +633,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                 bool w = true;
                 if (lane == 0) {
                     w = pf_wait(&s_full[s], (g / PF_S) & 1, p.status, abort_flag);
-                    if (w && g >= PF_AS) w = pf_wait(&a_empty[dg], ((g / PF_AS) - 1) & 1, p.status, abort_flag);
+                    // the TMEM slot is free once the MMAs of stage g - PF_AS (its previous use) have
+                    // completed: that stage's ring release
+                    if (w && g >= PF_AS)
+                        w = pf_wait(&s_empty[(g - PF_AS) % PF_S], ((g - PF_AS) / PF_S) & 1, p.status, abort_flag);
                 }
                 w = __shfl_sync(0xffffffffu, w, 0);
-                __syncwarp();  // lane 0's acquire orders the other lanes' reads of the stage
                 if (!(ok = w)) break;  // the warp leaves together
+                // every lane observes both completed phases itself (one test each), so that each
+                // lane's reads of the stage and writes of the slot are ordered after them
+                mbar_test_wait(&s_full[s], (g / PF_S) & 1);
+                if (g >= PF_AS) mbar_test_wait(&s_empty[(g - PF_AS) % PF_S], ((g - PF_AS) / PF_S) & 1);
                 tc_fence_after();
                 uint32_t o[32];
                 const uint8_t *raw = ring + (size_t)s * PG::STAGE + PG::TOKB;
@@ -616,7 +657,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                 if (lane == 0) red_release_add(&a_cnt[dg], 1);
             }
         }
-    } else if (warp < PF_TOK_WARP) {
+    } else if (warp < PF_PROD2_WARP) {
         // ---------------- epilogue: TMEM lane quarter q = warp % 4, lane = weight row 32 q + lane
         const int q = warp & 3, ew = warp - 2 - PF_DQ_WARPS;
         int jl = 0, xs = 0;  // items done, exchange chunks done (slot parity)
@@ -745,14 +786,14 @@ int encode_matrix_map(const uint8_t *pool, int n_slots, size_t slot_bytes, int H
     return MOE_OK;
 }
 
-// Map of fp16 token rows [rows][K] (row stride K): boxes of 64 columns x 32 rows with the
+// Map of fp16 token rows [rows][K] (row stride K): boxes of 64 columns x box_rows rows with the
 // 128-byte swizzle, which lands them in the UMMA K-major layout; rows past the end read 0.
-int encode_rows_map(const __half *base, int rows, int K, CUtensorMap *map) {
+int encode_rows_map(const __half *base, int rows, int K, int box_rows, CUtensorMap *map) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return MOE_ERR_UNSUPPORTED;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {PF_BK, PF_BOX_ROWS};
+    const cuuint32_t box[2] = {PF_BK, (cuuint32_t)box_rows};
     const cuuint32_t es[2] = {1, 1};
     if (enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (void *)base, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -850,9 +891,11 @@ int moe_prefill_ffn(const void *x, int xtype, int T, int H, int F, int qtype, in
         if (rc != MOE_OK) return rc;
     }
     PfParams p2 = p;
-    int rc = encode_rows_map(xg, R, H, &p.tmap);
+    int rc = encode_rows_map(xg, R, H, PF_BOX_ROWS, &p.tmap);
+    if (rc == MOE_OK) rc = encode_rows_map(xg, R, H, PF_NT, &p.tmap_nt);
+    if (rc == MOE_OK) rc = encode_rows_map(p.hg, R, F, PF_BOX_ROWS, &p2.tmap);
+    if (rc == MOE_OK) rc = encode_rows_map(p.hg, R, F, PF_NT, &p2.tmap_nt);
     if (rc != MOE_OK) return rc;
-    if ((rc = encode_rows_map(p.hg, R, F, &p2.tmap)) != MOE_OK) return rc;
 
     if (timing && timing->permute0) MOE_TRY_CUDA(cudaEventRecord(timing->permute0, s));
     pf_route_kernel<<<1, 1024, 0, s>>>(ids, R, E, expert_subset, n_subset, d_slot_table, n_slots, ints, L.o_rows,

@@ -75,7 +75,8 @@
 #define PF_ACOL (2 * PF_NT)
 #define PF_CTRL 13312      // control block: barriers, epilogue exchange, route lists
 static_assert(PF_ACOL + PF_AS * 32 <= PF_TMEM_COLS, "TMEM budget");
-static_assert(PF_S % 2 == 0, "each ring stage keeps one producer");
+static_assert(PF_S % 2 == 0, "each ring stage keeps one producer; stage pairs never wrap");
+static_assert(PF_AS % 2 == 0 && PF_BK == 64, "TMEM slot pairs");
 static_assert(PF_NT % 16 == 0 && PF_NT <= 256, "MMA N");
 
 namespace {
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
     uint64_t *mma_done = acc_empty + 2;
     uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
-    unsigned *a_cnt = (unsigned *)(smem + 512);  // per TMEM slot: dequant warps done (monotonic)
+    unsigned *a_cnt = (unsigned *)(smem + 512);  // per TMEM slot pair: dequant warps done (monotonic)
     float *xch = (float *)(smem + 1024);              // [2 pairs][2 slots][32 lanes][16] (GEMM 1)
     int *e_route = (int *)(smem + 1024 + 8192);       // [2 accumulators][PF_NT] (GEMM 2)
     float *e_w = (float *)(e_route + 2 * PF_NT);
@@ -545,15 +546,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer (lane 0).  Its loop is the kernel's critical path: a chain
-        // of dependent instructions per stage (measured ~45 clocks per tcgen05.mma issued and
-        // ~5 per dependent ALU instruction), so the stage and slot indexes, the descriptors and
-        // the dequant count a slot needs are carried in registers, and a stage costs one
-        // acquire load, one fence, four MMAs and one commit.
+        // of dependent instructions (measured: ~45 clocks per tcgen05 instruction issued and ~5
+        // per dependent ALU instruction), so it takes the K stages two at a time (one acquire
+        // and one fence per pair, eight MMAs), and carries the stage and slot indexes, the
+        // descriptors and the dequant count a slot pair needs in registers.  NK is even (the
+        // host requires H and F to be multiples of 128), so a pair never straddles two items,
+        // and g is even at every pair: the pair's slots are {0, 1} or {2, 3}, its ring stages
+        // s and s + 1 (PF_S is even).
         if (lane == 0) {
             int jl = 0;
             bool ok = true;
-            uint32_t s = 0, sph = 0;  // ring stage and the parity of its current fill
-            uint32_t sa = 0, want = 4;  // TMEM slot, and the dequant count its next use needs
+            uint32_t s = 0, sph = 0;    // ring stage of the pair's first stage, parity of its fill
+            uint32_t pc = 0, want = 8;  // slot pair, and the dequant count its next use needs
             const uint64_t b_first = umma_desc_sw128(smem_u32(ring));
             uint64_t b = b_first;
             uint32_t a = tmem + PF_ACOL;
@@ -566,13 +570,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                 if (jl >= 2 && !(ok = pf_wait(&acc_empty[buf], ((jl / 2) - 1) & 1, p.status, abort_flag))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * PF_NT;
-                for (int kc = 0; kc < NK; ++kc) {
-                    // the stage's weights are in TMEM once its dequant group's four warps counted
-                    // themselves in (release / acquire on a shared counter); the group waited for
-                    // the stage's copies (tokens included) first, so they are visible too
-                    if (ld_acquire(&a_cnt[sa]) < want) {
+                for (int kc = 0; kc < NK; kc += 2) {
+                    // both stages' weights are in TMEM once their two dequant groups' eight warps
+                    // counted themselves in (release / acquire on the pair's shared counter)
+                    if (ld_acquire(&a_cnt[pc]) < want) {
                         uint32_t i = 0;
-                        while (ld_acquire(&a_cnt[sa]) < want) {
+                        while (ld_acquire(&a_cnt[pc]) < want) {
                             if (++i >= MOE_TEST_SPIN_LIMIT) {
                                 moe_set_status(p.status, MOE_ERR_TIMEOUT);
                                 *abort_flag = 1;
@@ -584,30 +587,38 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                         }
                         if (!ok) break;
                     }
-                    // the tokens the MMAs read were landed by TMA: observe the stage's fill here too
-                    // (it completed before the dequant group counted in, so this test passes at once)
+                    // the tokens the MMAs read were landed by TMA: observe both fills here too (they
+                    // completed before the dequant groups counted in, so the tests pass at once)
                     if (!mbar_test_wait(&s_full[s], sph) && !(ok = pf_wait(&s_full[s], sph, p.status, abort_flag)))
+                        break;
+                    if (!mbar_test_wait(&s_full[s + 1], sph) &&
+                        !(ok = pf_wait(&s_full[s + 1], sph, p.status, abort_flag)))
                         break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < PF_BK / 16; ++kk)
                         umma_f16_tmem_a(d, a + 8 * kk, b + 2 * kk, idesc, (kc > 0 || kk > 0) ? 1u : 0u);
-                    // one commit frees the ring stage (producers) and the TMEM slot (the dequant
-                    // group that next writes it waits for this stage's release)
+                    // one commit per stage frees the ring stage (producers) and its TMEM slot (the
+                    // dequant group that next writes the slot waits for this stage's release)
                     umma_commit(&s_empty[s]);
-                    if (++s == PF_S) {
+                    const uint64_t b2 = b + (PG::STAGE >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < PF_BK / 16; ++kk)
+                        umma_f16_tmem_a(d, a + 32 + 8 * kk, b2 + 2 * kk, idesc, 1u);
+                    umma_commit(&s_empty[s + 1]);
+                    if ((s += 2) == PF_S) {
                         s = 0;
                         sph ^= 1u;
                         b = b_first;
                     } else {
-                        b += PG::STAGE >> 4;
+                        b = b2 + (PG::STAGE >> 4);
                     }
-                    if (++sa == PF_AS) {
-                        sa = 0;
-                        want += 4;
+                    if (++pc == PF_AS / 2) {
+                        pc = 0;
+                        want += 8;
                         a = tmem + PF_ACOL;
                     } else {
-                        a += 32;
+                        a += 64;
                     }
                 }
                 if (ok) umma_commit(&acc_full[buf]);
@@ -654,7 +665,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) red_release_add(&a_cnt[dg], 1);
+                if (lane == 0) red_release_add(&a_cnt[dg >> 1], 1);  // the slot pair's counter
             }
         }
     } else if (warp < PF_PROD2_WARP) {
@@ -854,7 +865,7 @@ int launch_gemms(PfParams &p1, PfParams &p2, int max_chunks, cudaStream_t s, con
 }  // namespace
 
 bool moe_prefill_eligible(int T, int H, int F, int qtype, int xtype) {
-    return T > MOE_DECODE_MAX_T && xtype == MOE_BF16 && H % PF_WM == 0 && F % 64 == 0 &&
+    return T > MOE_DECODE_MAX_T && xtype == MOE_BF16 && H % 128 == 0 && F % 128 == 0 &&
            (qtype == MOE_Q8_0 || qtype == MOE_Q4_SM);
 }
 

@@ -66,6 +66,7 @@ def _check(cfg, ids, w, x64, partial, rs, subset=None, sample=None):
     T, k = ids.shape
     cache = {}
     worst_tok, worst_route = 0.0, 0.0
+    bad = []  # (token, route, expert, error, 128-row blocks where the route's error is largest)
     for t in (range(T) if sample is None else sample):
         y_gpu = np.zeros(cfg.H)
         y_ref = np.zeros(cfg.H)
@@ -78,12 +79,16 @@ def _check(cfg, ids, w, x64, partial, rs, subset=None, sample=None):
                 cache[e] = synth.expert_weights(cfg, 0, e, rs)
             g, u, d = cache[e]
             ref = float(w[t, j]) * oracle.expert_ffn(cfg.qtype, cfg.H, cfg.F, g, u, d, x64[t])
-            worst_route = max(worst_route, rel_err(partial[t, j][None], ref[None])[0])
+            err = rel_err(partial[t, j][None], ref[None])[0]
+            worst_route = max(worst_route, err)
+            if not err <= ROUTE_TOL:
+                dev = np.abs(partial[t, j] - ref) > ROUTE_TOL * np.abs(ref).max()
+                bad.append((t, j, e, float(err), sorted(set((np.nonzero(dev)[0] // 128).tolist()))))
             y_gpu += partial[t, j]
             y_ref += ref
         worst_tok = max(worst_tok, rel_err(y_gpu[None], y_ref[None])[0])
-    assert worst_tok <= TOL, worst_tok
-    assert worst_route <= ROUTE_TOL, worst_route
+    assert worst_tok <= TOL, (worst_tok, bad[:8])
+    assert worst_route <= ROUTE_TOL, (worst_route, bad[:8])
     return worst_tok, worst_route
 
 

@@ -406,6 +406,227 @@ router_tiled_kernel(const void *__restrict__ x, int T, int H, const uint16_t *__
 
 namespace {
 
+// ------------------------------------------------------------------ bf16 prefill on tensor cores
+//
+// With bf16 activations (the prefill path) the product runs on the tensor cores: bf16 values
+// in the normal fp16 range are exact in fp16 (8 significant bits of 11), W_r is fp16, so every
+// product of an m16n8k16 MMA (fp16 operands, fp32 accumulation) is exact and only the sums
+// round.  A cluster of C CTAs owns 32 tokens and every expert (E a multiple of 32, at most
+// 128), each CTA a share of H (C is chosen so that the grid covers the SMs twice); in a CTA
+// warp w takes tokens 16 (w % 2).. and experts E/4 (w / 2)..; H is walked in chunks of 64
+// rows, x (converted to fp16) and W_r double-buffered in shared memory, operand fragments
+// loaded with ldmatrix.  Each chunk's products are summed on their own (four K = 16 MMAs)
+// and then added to the total, as in the fp32 kernel; the CTAs' partial logits are summed in
+// rank order over distributed shared memory, and each rank adds the bias and runs the warp
+// selection for its share of the tokens.
+
+#define RM_TT 32
+#define RM_KC 64
+#define RM_XS (RM_KC + 8)  // fp16 row stride of the x chunk (ldmatrix rows on distinct banks)
+
+__host__ __device__ inline size_t router_mma_smem(int E) {
+    const size_t xs = 2 * (size_t)RM_TT * RM_XS * 2;
+    const size_t ws = 2 * (size_t)RM_KC * (E + 8) * 2;
+    const size_t lg = (size_t)RM_TT * (E + 1) * 4;
+    return xs + (ws > lg ? ws : lg);
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t &r0, uint32_t &r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// NTW = n-tiles (8 experts) per warp = E / 32.
+template <int NTW>
+__global__ void __launch_bounds__(MOE_ROUTER_THREADS)
+router_mma_kernel(const __nv_bfloat16 *__restrict__ x, int T, int H, const uint16_t *__restrict__ w_router,
+                  const float *__restrict__ bias, int E, int k, int32_t *__restrict__ ids,
+                  float *__restrict__ weights, float *__restrict__ logits_out, float min_w) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int WS = E + 8;  // fp16 row stride of the W_r chunk
+    __half *xs = (__half *)smem;                                        // [2][RM_TT][RM_XS]
+    __half *ws = (__half *)(smem + 2 * (size_t)RM_TT * RM_XS * 2);      // [2][RM_KC][WS]
+    float *lg = (float *)ws;                                            // [RM_TT][E + 1] after the loop
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int C = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
+    const int t0 = (blockIdx.x / C) * RM_TT;
+    const int tg = warp & 1, n_base = (warp >> 1) * (E / 4);
+    const int NC = H / RM_KC;
+    const int c_lo = rank * NC / C, c_hi = (rank + 1) * NC / C;
+    const int wv = RM_KC * E / 8;  // 16-byte vectors of a W_r chunk
+    constexpr int WPT = (RM_KC * 128 / 8 + MOE_ROUTER_THREADS - 1) / MOE_ROUTER_THREADS;
+
+    uint4 xr, wr[WPT];
+    const int xt = tid / 8, xc = (tid % 8) * 8;  // token and first column of this thread's x piece
+    auto load = [&](int c) {
+        const int h0 = c * RM_KC;
+        xr = make_uint4(0u, 0u, 0u, 0u);
+        if (t0 + xt < T) xr = *(const uint4 *)(x + (size_t)(t0 + xt) * H + h0 + xc);
+        const uint4 *src = (const uint4 *)(w_router + (size_t)h0 * E);
+#pragma unroll
+        for (int q = 0; q < WPT; ++q) {
+            const int v = tid + q * MOE_ROUTER_THREADS;
+            if (v < wv) wr[q] = src[v];
+        }
+    };
+    auto store = [&](int buf) {
+        // bf16 -> fp16 (exact in the normal fp16 range)
+        const uint32_t in[4] = {xr.x, xr.y, xr.z, xr.w};
+        uint32_t outv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(*(const __nv_bfloat162 *)&in[i]);
+            const __half2 h = __floats2half2_rn(f.x, f.y);
+            outv[i] = *(const uint32_t *)&h;
+        }
+        *(uint4 *)(xs + ((size_t)buf * RM_TT + xt) * RM_XS + xc) = make_uint4(outv[0], outv[1], outv[2], outv[3]);
+        const int vpr = E / 8;  // vectors per W_r row
+#pragma unroll
+        for (int q = 0; q < WPT; ++q) {
+            const int v = tid + q * MOE_ROUTER_THREADS;
+            if (v < wv) *(uint4 *)(ws + ((size_t)buf * RM_KC + v / vpr) * WS + (v % vpr) * 8) = wr[q];
+        }
+    };
+
+    float tot[NTW][4], part[NTW][4];
+#pragma unroll
+    for (int j = 0; j < NTW; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tot[j][i] = 0.f;
+
+    // ldmatrix lane addresses: A (x, 16 x 16) as four 8 x 8 matrices rows 0-7 / 8-15 x
+    // columns 0-7 / 8-15; B (W_r, 16 x 8 per n-tile) as two transposed 8 x 8 matrices
+    const int am = lane >> 3, ar = lane & 7;
+    const int a_row = 16 * tg + (am & 1) * 8 + ar, a_col = (am >> 1) * 8;
+    const int b_row = ((lane >> 3) & 1) * 8 + ar;
+    const uint32_t xs_base = smem_u32(xs), ws_base = smem_u32(ws);
+
+    if (c_lo < c_hi) {
+        load(c_lo);
+        store(c_lo & 1);
+    }
+    __syncthreads();
+    for (int c = c_lo; c < c_hi; ++c) {
+        if (c + 1 < c_hi) load(c + 1);
+        const int buf = c & 1;
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) part[j][i] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < RM_KC / 16; ++ks) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(xs_base + (uint32_t)((((size_t)buf * RM_TT + a_row) * RM_XS + 16 * ks + a_col) * 2), a0, a1, a2,
+                    a3);
+#pragma unroll
+            for (int j = 0; j < NTW; ++j) {
+                uint32_t b0, b1;
+                ldsm_x2_trans(ws_base + (uint32_t)((((size_t)buf * RM_KC + 16 * ks + b_row) * WS + n_base + 8 * j) * 2),
+                              b0, b1);
+                mma_f16_16816(part[j], a0, a1, a2, a3, b0, b1);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tot[j][i] += part[j][i];
+        if (c + 1 < c_hi) store((c + 1) & 1);
+        __syncthreads();
+    }
+    // logits -> shared memory (the W_r buffers are free after the last barrier): accumulator
+    // element (row g, columns 2t, 2t+1) and (row g + 8, ...) of each n-tile
+    const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int j = 0; j < NTW; ++j) {
+        const int e = n_base + 8 * j + 2 * t4;
+        const int r = 16 * tg + g;
+        lg[(size_t)r * (E + 1) + e] = tot[j][0];
+        lg[(size_t)r * (E + 1) + e + 1] = tot[j][1];
+        lg[(size_t)(r + 8) * (E + 1) + e] = tot[j][2];
+        lg[(size_t)(r + 8) * (E + 1) + e + 1] = tot[j][3];
+    }
+    cluster_sync_all();  // every rank's partial logits are complete and visible
+    for (int t = rank + C * warp; t < RM_TT && t0 + t < T; t += C * (MOE_ROUTER_THREADS / 32)) {
+        float v[MOE_MAX_E / 32];
+#pragma unroll
+        for (int i = 0; i < MOE_MAX_E / 32; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = -INFINITY;
+            if (e < E) {
+                float sv = 0.f;
+                for (int r = 0; r < C; ++r) sv += ld_cluster_f32(cluster_map(&lg[(size_t)t * (E + 1) + e], r));
+                if (bias) sv += bias[e];
+                if (logits_out) logits_out[(size_t)(t0 + t) * E + e] = sv;
+                v[i] = (sv != sv) ? -INFINITY : sv;  // NaN never wins
+            }
+        }
+        select_topk_softmax(v, E, k, lane, (size_t)(t0 + t), ids, weights, min_w);
+    }
+    cluster_sync_all();  // the other ranks have finished reading this CTA's shared memory
+}
+
+// SMs of the current device (queried at every call: a process may drive several devices).
+int router_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0)
+        return 1;
+    return n;
+}
+
+template <int NTW>
+int router_mma_launch_t(const void *x, int T, int H, const uint16_t *w_router, const float *bias, int E, int k,
+                        int32_t *ids, float *weights, float *logits, float min_w, cudaStream_t st) {
+    const size_t smem = router_mma_smem(E);
+    MOE_TRY_CUDA(cudaFuncSetAttribute(router_mma_kernel<NTW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    const int tiles = (T + RM_TT - 1) / RM_TT, NC = H / RM_KC;
+    int C = 1;  // CTAs per cluster splitting H: until the grid covers the SMs twice
+    while (2 * C <= MOE_ROUTER_CLUSTER && 2 * C <= NC && tiles * C < 2 * router_sm_count()) C *= 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C * tiles, 1, 1);
+    cfg.blockDim = dim3(MOE_ROUTER_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    MOE_TRY_CUDA(cudaLaunchKernelEx(&cfg, router_mma_kernel<NTW>, (const __nv_bfloat16 *)x, T, H, w_router, bias, E,
+                                    k, ids, weights, logits, min_w));
+    return MOE_OK;
+}
+
+// The tensor-core router takes bf16 tokens with E a multiple of 32 up to 128 and H a multiple
+// of 64 (16-byte aligned rows); anything else keeps the fp32 kernel.
+bool router_mma_eligible(int xtype, int H, int E) {
+    return xtype == MOE_BF16 && E % 32 == 0 && E <= 128 && H % RM_KC == 0;
+}
+
+int router_mma_launch(const void *x, int T, int H, const uint16_t *w_router, const float *bias, int E, int k,
+                      int32_t *ids, float *weights, float *logits, float min_w, cudaStream_t st) {
+    switch (E / 32) {
+        case 1: return router_mma_launch_t<1>(x, T, H, w_router, bias, E, k, ids, weights, logits, min_w, st);
+        case 2: return router_mma_launch_t<2>(x, T, H, w_router, bias, E, k, ids, weights, logits, min_w, st);
+        case 3: return router_mma_launch_t<3>(x, T, H, w_router, bias, E, k, ids, weights, logits, min_w, st);
+        default: return router_mma_launch_t<4>(x, T, H, w_router, bias, E, k, ids, weights, logits, min_w, st);
+    }
+}
+
 template <int XT, int EPT>
 int router_tiled_launch_t(const void *x, int T, int H, const uint16_t *w_router, const float *bias, int E,
                           int k, int32_t *ids, float *weights, float *logits, float min_w, cudaStream_t st) {
@@ -461,9 +682,13 @@ extern "C" int moe_router_topk_threshold(const void *x, int xtype, int T, int H,
     MOE_CHECK(E >= 1 && E <= MOE_MAX_E && k >= 1 && k <= MOE_MAX_K && k <= E);
     if (T == 0) return MOE_OK;
     MOE_CHECK(x && w_router && ids && weights);
-    if (T > MOE_DECODE_MAX_T && ((uintptr_t)x & 15) == 0 && ((uintptr_t)w_router & 15) == 0)
+    if (T > MOE_DECODE_MAX_T && ((uintptr_t)x & 15) == 0 && ((uintptr_t)w_router & 15) == 0) {
+        if (router_mma_eligible(xtype, H, E))
+            return router_mma_launch(x, T, H, w_router, bias, E, k, ids, weights, logits, min_weight,
+                                     moe_cuda_stream(s));
         return router_tiled_launch(x, xtype, T, H, w_router, bias, E, k, ids, weights, logits, min_weight,
                                    moe_cuda_stream(s));
+    }
     const RouterSmem L = router_smem_layout(H, E);
     if (L.total > 200 * 1024) return MOE_ERR_UNSUPPORTED;
     const int HS = H / MOE_ROUTER_CLUSTER;

@@ -41,6 +41,10 @@ ROUTER_CASES = [
     (2048, 256, 8, 64, 1, 1.0),    # E = 256: 8 experts per thread
     (64, 200, 6, 45, 0, 0.5),      # E = 200, 2 chunks
     (2048, 128, 8, 300, 0, 1.1),   # Qwen-shaped, fp32 tokens, ragged last tile
+    # bf16 tokens above 32 with E a multiple of 32 (at most 128): the tensor-core router
+    (1024, 64, 6, 77, 1, 1.0),     # 2 n-tiles per warp, ragged last tile
+    (512, 96, 4, 40, 1, 0.8),      # 3 n-tiles per warp
+    (2048, 32, 2, 520, 1, 1.2),    # 1 n-tile per warp, many tiles
 ]
 
 

@@ -77,7 +77,13 @@ __host__ __device__ inline int gv_sb(int qtype) { return 32 * moe_scale_entry_by
 
 // Row stride of the staged fp16 activations (bytes): 2 Kr + 32 keeps 16-byte alignment
 // and spreads the 8 rows of a B-fragment load over the banks.
-__host__ __device__ inline int gv_row_stride(int Kr) { return 2 * Kr + 32; }
+// Row stride of a staged activation row (fp16, Kr columns): a multiple of 128 bytes, so that
+// every hi row starts on bank 0, with room for a lo row to start 64 bytes (16 banks) into its
+// row.  The eight lanes of one phase of a 16-byte shared-memory load read one route's hi and
+// lo rows (B columns 2 s and 2 s + 1, below), which therefore fall on opposite halves of the
+// banks whatever the route's token is: no bank conflicts.
+#define GV_LO_SHIFT 64
+__host__ __device__ inline int gv_row_stride(int Kr) { return (2 * Kr + GV_LO_SHIFT + 127) / 128 * 128; }
 
 // One pair's slot: 2*NTS fp16 rows (hi, lo per token row), up to 32 inverse token scales,
 // the header (SlotHdr, 128 bytes), and for the 4-bit format the per-block activation sums
@@ -273,16 +279,16 @@ __device__ __forceinline__ uint32_t q4_odd(uint32_t w) {
 // and (2,6), (3,7) of the 8, which is why the staged 4-bit activations are permuted the
 // same way within each group of 8).  The B fragment of a lane is then the 16 bytes of fp16
 // activations at columns 8c .. 8c+7 of its B row, one shared-memory load per block.
-// B rows: column n is route n % 4 of the virtual expert, its hi part (n < 4) or lo part.
+// B rows: column n is route slot n / 2 of the virtual expert, its hi part (n even) or lo
+// part (n odd).
 
-// acc[i][hr][j]: tile i, row 16 hr + r (+ 8 for j >= 2), column 2c + (j & 1).
-// brow: this lane's B row at the chunk's first column (plus 16 c bytes); as0 / as1: the
-// 4-bit block sums of the lane's two columns at the chunk's first block (stride NTS per
-// block), or null for lo columns (no minimum term).
+// acc[i][hr][j]: tile i, row 16 hr + r (+ 8 for j >= 2), column 2c + (j & 1): route slot c,
+// hi part (j even) or lo part.  brow: this lane's B row at the chunk's first column (plus
+// 16 c bytes); as: the 4-bit block sums of route slot c's token at the chunk's first block
+// (stride NTS per block), added with the block minimum to the hi columns.
 template <int QT, int NTL>
 __device__ __forceinline__ void chunk_dot(const unsigned char *st, int tb, int cb, const unsigned char *brow,
-                                          const float *as0, const float *as1, int NTS, int lane,
-                                          float (&acc)[NTL][2][4]) {
+                                          const float *as_, int NTS, int lane, float (&acc)[NTL][2][4]) {
     constexpr int TBB = QT == MOE_Q8_0 ? 1088 : 640;  // tile block: codes, then 32 scale entries
     constexpr int SC = QT == MOE_Q8_0 ? 1024 : 512;   // offset of the scales in a tile block
     const int r = lane >> 2, c = lane & 3;
@@ -290,10 +296,8 @@ __device__ __forceinline__ void chunk_dot(const unsigned char *st, int tb, int c
 #pragma unroll 1
     for (int b = 0; b < cb; ++b) {
         const uint4 bf = *(const uint4 *)(brow + 64 * b);
-        float2 as = make_float2(0.f, 0.f);
-        if constexpr (QT == MOE_Q4_SM) {
-            if (as0) as = make_float2(as0[b * NTS], as1[b * NTS]);
-        }
+        float as = 0.f;
+        if constexpr (QT == MOE_Q4_SM) as = as_[b * NTS];
 #pragma unroll
         for (int i = 0; i < NTL; ++i) {
             const unsigned char *blk = st + (size_t)i * tb + (size_t)b * TBB;
@@ -342,31 +346,27 @@ __device__ __forceinline__ void chunk_dot(const unsigned char *st, int tb, int c
                 a[1] = fmaf(d0, C[1], a[1]);
                 a[2] = fmaf(d1, C[2], a[2]);
                 a[3] = fmaf(d1, C[3], a[3]);
-                if (QT == MOE_Q4_SM) {  // the block minimum times the hi columns' sums
-                    a[0] = fmaf(m0, as.x, a[0]);
-                    a[1] = fmaf(m0, as.y, a[1]);
-                    a[2] = fmaf(m1, as.x, a[2]);
-                    a[3] = fmaf(m1, as.y, a[3]);
+                if (QT == MOE_Q4_SM) {  // the block minimum times the hi column's sum
+                    a[0] = fmaf(m0, as, a[0]);
+                    a[2] = fmaf(m1, as, a[2]);
                 }
             }
         }
     }
 }
 
-// Hi and lo parts of this lane's columns added (lane c + 2 holds the lo part of lane c's
-// columns) and the route scales (i0, i1 for its two columns) removed, into acc[i][hr][j]
-// for column 2c + (j & 1) (valid on lanes c < 2).
+// Hi and lo parts of this lane's route slot added (columns 2c and 2c + 1: j = 0, 1 for row r,
+// j = 2, 3 for row r + 8) and the route's token scale removed, into acc[i][hr][0] (row r) and
+// acc[i][hr][2] (row r + 8).
 template <int NTL>
-__device__ __forceinline__ void finish_acc(float (&acc)[NTL][2][4], float i0, float i1) {
+__device__ __forceinline__ void finish_acc(float (&acc)[NTL][2][4], float inv) {
 #pragma unroll
     for (int i = 0; i < NTL; ++i)
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float v = acc[i][hr][j] + __shfl_xor_sync(0xffffffffu, acc[i][hr][j], 2);
-                acc[i][hr][j] = v * ((j & 1) ? i1 : i0);
-            }
+        for (int hr = 0; hr < 2; ++hr) {
+            acc[i][hr][0] = (acc[i][hr][0] + acc[i][hr][1]) * inv;
+            acc[i][hr][2] = (acc[i][hr][2] + acc[i][hr][3]) * inv;
+        }
 }
 
 // ------------------------------------------------------------------ staging the activations
@@ -449,7 +449,7 @@ __device__ void stage_row(const FfnParams &p, int row, int c0, int Kr, unsigned 
     float *asum = (float *)(slot + GV_ASUM_OFF(NTS, RS));
     if (lane == 0) inv[t] = __int_as_float((127 - 14 + ex) << 23);
     __half *hi = (__half *)(slot + (size_t)(2 * t) * RS);
-    __half *lo = (__half *)(slot + (size_t)(2 * t + 1) * RS);
+    __half *lo = (__half *)(slot + (size_t)(2 * t + 1) * RS + GV_LO_SHIFT);
     // one step of 8 columns per lane; every lane calls it (the 4-bit block sums shuffle)
     auto emit = [&](int col, const float (&v)[8]) {
         float bs = 0.f;
@@ -772,12 +772,11 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
             // route's token; down: q); slots past n_e read row 0 (their columns are not used).
             auto trow = [&](int q) { return q >= n_e ? 0 : (DOWN ? q : hdr->in.rt[q] / p.k); };
             const int r_ = lane >> 2, c_ = lane & 3;
-            // B row of column r_: route slot r_ % 4, hi (r_ < 4) or lo
-            const unsigned char *brow = slot + (size_t)(2 * trow(r_ & 3) + (r_ >> 2)) * RS + 16 * c_;
-            // the lane's two accumulator columns 2c, 2c+1: route slots, hi on lanes c < 2
-            const int q0 = (2 * c_) & 3, q1 = q0 + 1;
-            const bool hi_cols = c_ < 2;
-            const int tr0 = trow(q0), tr1 = trow(q1);
+            // B row of column r_: route slot r_ / 2, hi (r_ even) or lo (64 bytes into its row)
+            const unsigned char *brow =
+                slot + (size_t)(2 * trow(r_ >> 1) + (r_ & 1)) * RS + (r_ & 1) * GV_LO_SHIFT + 16 * c_;
+            // the lane's two accumulator columns 2c, 2c+1: route slot c, hi and lo
+            const int trc = trow(c_);
             const float *asb = (const float *)(slot + GV_ASUM_OFF(NTS, RS));
             float acc[NTL][2][4];
 #pragma unroll
@@ -799,9 +798,8 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
                     const int cb = min(CB, nbr - ch * CB);
                     if (fill && hdr->in.wt)  // the first group of a missed expert fills its slot
                         write_through<QT>(hdr->in, p.H, p.F, DOWN, NTL, g, ks * nbr + ch * CB, cb, st, tb, lane);
-                    const float *a0 = hi_cols ? asb + (size_t)ch * CB * NTS + tr0 : nullptr;
-                    const float *a1 = hi_cols ? asb + (size_t)ch * CB * NTS + tr1 : nullptr;
-                    chunk_dot<QT, NTL>(st, tb, cb, brow + (size_t)64 * ch * CB, a0, a1, NTS, lane, acc);
+                    chunk_dot<QT, NTL>(st, tb, cb, brow + (size_t)64 * ch * CB, asb + (size_t)ch * CB * NTS + trc, NTS,
+                                       lane, acc);
                     // the stage was written through the generic proxy (cp.async); a later bulk
                     // copy (async proxy) overwrites it
                     if (fill) fence_proxy_async_smem();
@@ -811,11 +809,11 @@ __device__ __forceinline__ void ffn_body(const FfnParams &p, unsigned char *smem
             }
             if (dead || n_e == 0) continue;
             const float *inv = (const float *)(slot + GV_INV_OFF(NTS, RS));
-            finish_acc<NTL>(acc, inv[tr0], inv[tr1]);
+            finish_acc<NTL>(acc, inv[trc]);
             const int r = lane >> 2, c = lane & 3, pos0 = hdr->in.pos0;
+            const int t = c;  // this lane's route slot
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int t = 2 * c + (j & 1);
+            for (int j = 0; j < 4; j += 2) {
                 if (t >= n_e) continue;
                 const int pos = pos0 + t;
 #pragma unroll

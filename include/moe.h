@@ -131,7 +131,8 @@ int moe_slot_image_bytes(int qtype, int H, int F, size_t *bytes_out);
  * pass NULL to query the size only.  Layout of the image: gate [F][H], up [F][H], down
  * [H][F], each matrix a run of 32-row tiles, each tile a run of "tile blocks" (one per
  * 32-column block along K): first the codes of the 32 rows (q8_0: two 512-byte pieces,
- * row l's 16 codes of piece p at 512 p + 16 l, each stored as q + 128, offset binary;
+ * row l's 16 codes of piece p at 512 p + 16 ((l + 4 p) mod 32), each stored as q + 128,
+ * offset binary;
  * 4-bit: one 512-byte piece, row l's 16 canonical code bytes at 16 l), then the 32 rows'
  * scale entries (fp16 d, or fp16 d and m), row l's entry at position 4 (l % 8) + l / 8.
  * So any K range of a tile is one contiguous run of bytes.  The image has the canonical

@@ -33,7 +33,10 @@ static inline cudaStream_t moe_cuda_stream(moe_stream_t s) { return (cudaStream_
 // along K, so that any K range of a tile is one contiguous run of bytes.  A tile block is
 //   codes:  PPB pieces of 512 bytes (q8_0: 2, 4-bit: 1); piece p holds, for lane 0..31,
 //           16 bytes of codes: q8_0 columns 16p .. 16p+15 of the block, one byte each, stored
-//           as q + 128 (offset binary); 4-bit the block's 16 code bytes in canonical order;
+//           as q + 128 (offset binary); 4-bit the block's 16 code bytes in canonical order.
+//           Lane l's 16 bytes sit at 512 p + 16 ((l + 4 p) mod 32): the second q8_0 piece is
+//           rotated by four rows, so that the decode GEMV's 8-byte loads of rows r..r+3 from
+//           both pieces (one half-warp) fall on opposite halves of the shared-memory banks;
 //   scales: 32 entries, fp16 d (q8_0) or fp16 d, fp16 m (4-bit), the entry of row (lane) l
 //           at position moe_scale_pos(l) = 4 (l % 8) + l / 8, so that rows l, l+8, l+16,
 //           l+24 are adjacent.
@@ -65,7 +68,7 @@ __host__ __device__ static inline size_t moe_tile_block_offset(int qtype, int K,
     return ((size_t)g * (K / 32) + b) * moe_tile_block_bytes(qtype);
 }
 // within a tile block: the code bytes of lane l in piece p, and the scale entry of lane l
-__host__ __device__ static inline int moe_piece_in_block(int p, int lane) { return p * 512 + lane * 16; }
+__host__ __device__ static inline int moe_piece_in_block(int p, int lane) { return p * 512 + ((lane + 4 * p) & 31) * 16; }
 __host__ __device__ static inline int moe_scale_in_block(int qtype, int lane) {
     return MOE_TILE_ROWS * (qtype == MOE_Q8_0 ? 32 : 16) + moe_scale_pos(lane) * moe_scale_entry_bytes(qtype);
 }

@@ -322,9 +322,11 @@ __device__ __forceinline__ void chunk_dot(const unsigned char *st, int tb, int c
                 const int R0 = 16 * hr + r;
                 uint32_t A0[4], A1[4];
                 if constexpr (QT == MOE_Q8_0) {  // offset-binary codes: no sign flip needed
-                    const unsigned char *cp = blk + (c >> 1) * 512 + (c & 1) * 8;
-                    const uint2 w0 = *(const uint2 *)(cp + R0 * 16);
-                    const uint2 w1 = *(const uint2 *)(cp + (R0 + 8) * 16);
+                    // piece c / 2 (its rows rotated by 4 c / 2: see moe_piece_in_block)
+                    const int pc = c >> 1;
+                    const unsigned char *cp = blk + pc * 512 + (c & 1) * 8;
+                    const uint2 w0 = *(const uint2 *)(cp + ((R0 + 4 * pc) & 31) * 16);
+                    const uint2 w1 = *(const uint2 *)(cp + ((R0 + 8 + 4 * pc) & 31) * 16);
                     A0[0] = q8_pair(w0.x, 0x4140); A0[1] = q8_pair(w1.x, 0x4140);
                     A0[2] = q8_pair(w0.x, 0x4342); A0[3] = q8_pair(w1.x, 0x4342);
                     A1[0] = q8_pair(w0.y, 0x4140); A1[1] = q8_pair(w1.y, 0x4140);

@@ -60,7 +60,7 @@ def test_pack_unpack_round_trip_and_layout(lib, qtype):
     L.moe_unpack_expert(qtype, 64, 96, view.ctypes.data, g2.ctypes.data, u2.ctypes.data, d2.ctypes.data)
     assert np.array_equal(g, g2) and np.array_equal(u, u2) and np.array_equal(d, d2)
     # documented layout: gate row r, block b -> tile g = r // 32, lane = r % 32, tile block
-    # (g, b) at (g * nb + b) * TBB: codes (piece p of lane l at 512 p + 16 l), then the scale
+    # (g, b) at (g * nb + b) * TBB: codes (piece p of lane l at 512 p + 16 ((l + 4 p) % 32)), then the scale
     # entries with lane l at position 4 (l % 8) + l // 8
     nb = 2
     r, b = 37, 1
@@ -69,7 +69,7 @@ def test_pack_unpack_round_trip_and_layout(lib, qtype):
     pos = 4 * (lane % 8) + lane // 8
     if qtype == 0:
         tb = (tile * nb + b) * 1088
-        q_off = tb + 512 + lane * 16  # second piece of the block: codes 16..31
+        q_off = tb + 512 + ((lane + 4) % 32) * 16  # second piece of the block: codes 16..31
         assert np.array_equal(view[q_off:q_off + 16], blk[2 + 16:2 + 32] ^ 0x80)
         s_off = tb + 1024 + pos * 2
         assert np.array_equal(view[s_off:s_off + 2], blk[0:2])

@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE decode tokens/s at batch 1/8/32 (1 GB300); % HBM roofline; cache hit %"
 CONFIG_INDEX = 1
+HEADLINE_PREFETCH = 1  # cross-layer speculative prefetch depth of the headline stack
 
 
 def load_peaks():
@@ -586,7 +587,10 @@ def run_gpu(args, world, rank, local):
     T = args.batch
     max_T = max(max(cfg.tokens), T)
     link_gbs = h2d_bandwidth(torch)
-    dev_stack = Stack(cfg, max_T=max_T, device_managed=True, use_graph=True)
+    # the headline stack: device-managed pool, graph replay, cross-layer prefetch of depth 1
+    # (outputs identical to the plain pool; the fills of the next layer's misses start while
+    # this layer computes)
+    dev_stack = Stack(cfg, max_T=max_T, device_managed=True, use_graph=True, prefetch_depth=HEADLINE_PREFETCH)
     stream = torch.cuda.Stream()
     inputs = [torch.from_numpy(synth.tokens_x(cfg, 3 + s, T)).cuda() for s in range(64)]
 
@@ -656,7 +660,10 @@ def run_gpu(args, world, rank, local):
     # every decode configuration at the metric's batch sizes (256 steps from a cold pool each)
     configs = {}
     cpu_budget = 0.0 if args.no_cpu else 4.0
-    for ci, Ts, stk in ((1, (1, 4, 8), dev_stack), (2, (1,), None), (3, (1, 32), None)):
+    # (the plain LRU pool, as on the pages; the headline's images are shared)
+    plain = Stack(cfg, max_T=max_T, device_managed=True, use_graph=True, images=dev_stack.images)
+    dev_stack.close()
+    for ci, Ts, stk in ((1, (1, 4, 8), plain), (2, (1,), None), (3, (1, 32), None)):
         if args.configs is not None and ci not in args.configs:
             if stk is not None:
                 stk.close()
@@ -690,7 +697,9 @@ def run_gpu(args, world, rank, local):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic (seeded q8_0 / 4-bit experts, N(0,1) activations; no datasets or trained weights)",
                 "config": workload_config(cfg, T), "impl": "gb300",
-                "mode": "device-managed pool, whole step replayed as a CUDA graph",
+                "mode": "device-managed pool, whole step replayed as a CUDA graph, cross-layer speculative "
+                        "prefetch of depth %d (the real plans' hits include prefetched experts; the plain "
+                        "LRU pool is policies_granite_b8.lru_device and configs.granite_b8)" % HEADLINE_PREFETCH,
                 "hit_rate": r["hit_rate"], "frac_of_8tbs_roofline": r["frac_of_8tbs_roofline"],
                 "frac_of_measured_hbm_roofline": r["frac_of_measured_hbm_roofline"],
                 "h2d_link_gbs_measured": link_gbs,

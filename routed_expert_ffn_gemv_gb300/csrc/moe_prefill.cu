@@ -14,9 +14,10 @@
 // chunks); a work item is (chunk, 128-row weight slab).  The dequantised operand never
 // passes through shared memory, and a batch with few tokens per expert runs MMAs only as
 // wide as its tokens.
-//  * route kernel: a stable counting sort of the routes by expert (positions), the chunks of
-//    every expert, experts with the most tokens first (each expert's chunks consecutive, so
-//    that the items reading one expert's weights run together and share them in L2);
+//  * route kernels (count, chunk, place): the routes sorted by expert into positions, the
+//    chunks of every expert, experts with the most tokens first (each expert's chunks
+//    consecutive, so that the items reading one expert's weights run together and share them
+//    in L2);
 //  * gather kernel: activations -> fp16 rows in position order (K permuted for 4-bit);
 //  * GEMM kernels: persistent, one CTA per SM over a strided list of work items, warp roles
 //    with mbarrier rings that run on across items:
@@ -85,12 +86,13 @@ namespace {
 
 struct PfLayout {
     int max_chunks;
-    size_t o_rows, o_cexp, o_cslot, o_cpos, o_cn;  // int offsets (in ints)
+    size_t o_rows, o_cexp, o_cslot, o_cpos, o_cn, o_cnt, o_cur;  // int offsets (in ints)
     size_t ints_bytes, xg, hg, total;
 };
 
 // ints[0] = chunks, ints[1] = positions placed; rows [R]: position -> route; per chunk its
-// expert, slot, first position and token count.
+// expert, slot, first position and token count; per expert its route count and placement
+// cursor.
 inline PfLayout pf_layout(int T, int H, int F, int E, int k) {
     PfLayout L;
     const long R = (long)T * k;
@@ -101,6 +103,8 @@ inline PfLayout pf_layout(int T, int H, int F, int E, int k) {
     L.o_cslot = o; o += L.max_chunks;
     L.o_cpos = o;  o += L.max_chunks;
     L.o_cn = o;    o += L.max_chunks;
+    L.o_cnt = o;   o += MOE_MAX_E;
+    L.o_cur = o;   o += MOE_MAX_E;
     L.ints_bytes = (o * 4 + 1023) / 1024 * 1024;
     L.xg = L.ints_bytes;
     L.hg = L.xg + ((size_t)R * H * 2 + 1023) / 1024 * 1024;
@@ -175,71 +179,74 @@ __device__ __forceinline__ bool named_sync_and(int id, int count, bool v) {
 
 // ------------------------------------------------------------------ route + gather
 
-// Stable counting sort of the routes by expert (restricted to a subset) into positions, and
-// the chunks: an expert with c routes gets ceil(c / PF_NT) chunks of near-equal size (the
-// first c % n one larger), chunk j starting at its expert's offset + j (c / n) + min(j, c % n).
-// Chunks are listed expert by expert, the experts with the most routes first (ties: lower
-// id).  An expert whose slot is out of range is reported and its chunks get slot -1 (skipped
-// by the GEMMs).  One CTA of 1024 threads (32 warps): warp w sorts a contiguous range of
-// routes in rounds of 32; a route's rank among the round's routes of its expert comes from a
-// warp match, and the earlier rounds and warps from per-warp counters.
-__global__ void __launch_bounds__(1024) pf_route_kernel(const int32_t *__restrict__ ids, int R, int E,
-                                                        const int32_t *__restrict__ subset, int n_subset,
-                                                        const int32_t *__restrict__ slot_table, int n_slots,
-                                                        int32_t *__restrict__ ints, size_t o_rows, size_t o_cexp,
-                                                        size_t o_cslot, size_t o_cpos, size_t o_cn, int *status) {
-    constexpr int NW = 32;
-    __shared__ int cntw[NW][MOE_MAX_E];
-    __shared__ int tot[MOE_MAX_E], offs[MOE_MAX_E + 1], order[MOE_MAX_E];
-    __shared__ int wsum[NW];
-    __shared__ unsigned char insub[MOE_MAX_E];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < NW * MOE_MAX_E; i += blockDim.x) (&cntw[0][0])[i] = 0;
-    if (tid < MOE_MAX_E) insub[tid] = subset ? 0 : 1;
-    __syncthreads();
+// Routes sorted by expert (restricted to a subset) into positions, in three launches over the
+// whole grid: (1) per-expert route counts (shared-memory histograms, one global add per block
+// and expert; ids outside [-1, E) are reported), (2) one CTA: expert offsets, the experts
+// ordered by count and their chunks (below), (3) positions: each warp groups its routes by
+// expert (warp match), the group's leader reserves a run of positions with one global add.
+// Within an expert the order of the routes is not fixed (a route's result does not depend on
+// where it sits in its chunk).
+#define PF_RB 256  // threads (routes) per block of the count and place kernels
+
+__device__ __forceinline__ int pf_expert_of(const int32_t *ids, int r, int R, int E, const int32_t *subset,
+                                            int n_subset) {
+    if (r >= R) return -1;
+    const int v = ids[r];
+    if (v < 0 || v >= E) return -1;
     if (subset) {
-        for (int i = tid; i < n_subset; i += blockDim.x) {
-            const int e = subset[i];
-            if (e >= 0 && e < E) insub[e] = 1;
-            else moe_set_status(status, MOE_ERR_INVALID);
-        }
-        __syncthreads();
+        bool in = false;
+        for (int i = 0; i < n_subset; ++i) in |= subset[i] == v;
+        if (!in) return -1;
     }
-    const int per = ((R + NW - 1) / NW + 31) / 32 * 32;
-    const int r0 = warp * per, r1 = min(R, r0 + per);
-    auto expert_of = [&](int r) {
-        int e = -1;
-        if (r < r1) {
-            const int v = ids[r];
-            if (v >= 0 && v < E) {
-                if (insub[v]) e = v;
-            }
-        }
-        return e;
-    };
-    // pass 1: per-warp counts
-    for (int base = r0; base < r1; base += 32) {
-        const int r = base + lane;
-        if (r < r1) {
-            const int v = ids[r];
-            if (v < -1 || v >= E) moe_set_status(status, MOE_ERR_INVALID);  // -1: a dropped route
-        }
-        const int e = expert_of(r);
-        const unsigned grp = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && lane == __ffs(grp) - 1) cntw[warp][e] += __popc(grp);
-        __syncwarp();
-    }
+    return v;
+}
+
+__global__ void __launch_bounds__(PF_RB) pf_count_kernel(const int32_t *__restrict__ ids, int R, int E,
+                                                         const int32_t *__restrict__ subset, int n_subset,
+                                                         int32_t *__restrict__ cnt, int *status) {
+    __shared__ int hist[MOE_MAX_E];
+    for (int e = threadIdx.x; e < E; e += PF_RB) hist[e] = 0;
     __syncthreads();
-    // per expert: earlier warps' counts, total; then the offsets (scan over experts)
-    int cnt = 0;
-    if (tid < E) {
-        for (int w = 0; w < NW; ++w) {
-            const int c = cntw[w][tid];
-            cntw[w][tid] = cnt;
-            cnt += c;
-        }
-        tot[tid] = cnt;
-    }
+    const int r = blockIdx.x * PF_RB + threadIdx.x;
+    if (r < R && (ids[r] < -1 || ids[r] >= E)) moe_set_status(status, MOE_ERR_INVALID);  // -1: a dropped route
+    if (subset && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_subset; i += PF_RB)
+            if (subset[i] < 0 || subset[i] >= E) moe_set_status(status, MOE_ERR_INVALID);
+    const int e = pf_expert_of(ids, r, R, E, subset, n_subset);
+    if (e >= 0) atomicAdd(&hist[e], 1);
+    __syncthreads();
+    for (int x = threadIdx.x; x < E; x += PF_RB)
+        if (hist[x]) atomicAdd(&cnt[x], hist[x]);
+}
+
+__global__ void __launch_bounds__(PF_RB) pf_place_kernel(const int32_t *__restrict__ ids, int R, int E,
+                                                         const int32_t *__restrict__ subset, int n_subset,
+                                                         int32_t *__restrict__ cur, int32_t *__restrict__ rows) {
+    const int r = blockIdx.x * PF_RB + threadIdx.x, lane = threadIdx.x & 31;
+    const int e = pf_expert_of(ids, r, R, E, subset, n_subset);
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    const int leader = __ffs(grp) - 1;
+    int base = 0;
+    if (e >= 0 && lane == leader) base = atomicAdd(&cur[e], __popc(grp));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (e >= 0) rows[base + __popc(grp & ((1u << lane) - 1u))] = r;
+}
+
+// (2) One CTA: from the counts, the expert offsets (in id order) and placement cursors, the
+// experts ordered by descending count (ties: lower id) and the chunks: an expert with c routes
+// gets ceil(c / PF_NT) chunks of near-equal size (the first c % n one larger), chunk j starting
+// at its expert's offset + j (c / n) + min(j, c % n), listed expert by expert in that order.
+// An expert whose slot is out of range is reported and its chunks get slot -1 (skipped by the
+// GEMMs).
+__global__ void __launch_bounds__(1024) pf_chunk_kernel(int E, const int32_t *__restrict__ slot_table, int n_slots,
+                                                        int32_t *__restrict__ ints, size_t o_cexp, size_t o_cslot,
+                                                        size_t o_cpos, size_t o_cn, size_t o_cnt, size_t o_cur,
+                                                        int *status) {
+    __shared__ int tot[MOE_MAX_E], offs[MOE_MAX_E + 1], order[MOE_MAX_E];
+    __shared__ int wsum[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cnt = tid < E ? ints[o_cnt + tid] : 0;
+    if (tid < E) tot[tid] = cnt;
     {
         int x = cnt;
 #pragma unroll
@@ -251,63 +258,49 @@ __global__ void __launch_bounds__(1024) pf_route_kernel(const int32_t *__restric
         __syncthreads();
         int before = 0;
         for (int w = 0; w < warp; ++w) before += wsum[w];
-        if (tid < E) offs[tid] = before + x - cnt;
+        if (tid < E) {
+            offs[tid] = before + x - cnt;
+            ints[o_cur + tid] = before + x - cnt;
+        }
         if (tid == E - 1) offs[E] = before + x;
     }
     __syncthreads();
-    if (tid < E)
-        for (int w = 0; w < NW; ++w) cntw[w][tid] += offs[tid];
-    // experts by descending count (ties: lower id first)
     if (tid < E) {
         int rank = 0;
         for (int e = 0; e < E; ++e) rank += (tot[e] > cnt) || (tot[e] == cnt && e < tid);
         order[rank] = tid;
     }
     __syncthreads();
-    // pass 2: positions
-    int32_t *rows = ints + o_rows;
-    for (int base = r0; base < r1; base += 32) {
-        const int r = base + lane;
-        const int e = expert_of(r);
-        const unsigned grp = __match_any_sync(0xffffffffu, e);
-        if (e >= 0) rows[cntw[warp][e] + __popc(grp & ((1u << lane) - 1u))] = r;
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(grp) - 1) cntw[warp][e] += __popc(grp);
-        __syncwarp();
-    }
-    // chunks: scan of the chunk counts in expert order
-    {
-        const int e = tid < E ? order[tid] : -1;
-        const int nch = e >= 0 ? (tot[e] + PF_NT - 1) / PF_NT : 0;
-        int x = nch;
+    const int e = tid < E ? order[tid] : -1;
+    const int nch = e >= 0 ? (tot[e] + PF_NT - 1) / PF_NT : 0;
+    int x = nch;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    __syncthreads();  // wsum reuse
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += wsum[w];
+    if (tid == E - 1) {
+        ints[0] = before + x;
+        ints[1] = offs[E];
+    }
+    if (nch > 0) {
+        int slot = slot_table ? slot_table[e] : e;
+        if (slot < 0 || slot >= n_slots) {
+            moe_set_status(status, MOE_ERR_INVALID);
+            slot = -1;
         }
-        __syncthreads();  // wsum reuse
-        if (lane == 31) wsum[warp] = x;
-        __syncthreads();
-        int before = 0;
-        for (int w = 0; w < warp; ++w) before += wsum[w];
-        if (tid == E - 1) {
-            ints[0] = before + x;
-            ints[1] = offs[E];
-        }
-        if (nch > 0) {
-            int slot = slot_table ? slot_table[e] : e;
-            if (slot < 0 || slot >= n_slots) {
-                moe_set_status(status, MOE_ERR_INVALID);
-                slot = -1;
-            }
-            const int c = tot[e], q = c / nch, rem = c % nch;
-            const int b0 = before + x - nch;
-            for (int j = 0; j < nch; ++j) {
-                ints[o_cexp + b0 + j] = e;
-                ints[o_cslot + b0 + j] = slot;
-                ints[o_cpos + b0 + j] = offs[e] + j * q + min(j, rem);
-                ints[o_cn + b0 + j] = q + (j < rem ? 1 : 0);
-            }
+        const int c = tot[e], q = c / nch, rem = c % nch;
+        const int b0 = before + x - nch;
+        for (int j = 0; j < nch; ++j) {
+            ints[o_cexp + b0 + j] = e;
+            ints[o_cslot + b0 + j] = slot;
+            ints[o_cpos + b0 + j] = offs[e] + j * q + min(j, rem);
+            ints[o_cn + b0 + j] = q + (j < rem ? 1 : 0);
         }
     }
 }
@@ -909,8 +902,14 @@ int moe_prefill_ffn(const void *x, int xtype, int T, int H, int F, int qtype, in
     if (rc != MOE_OK) return rc;
 
     if (timing && timing->permute0) MOE_TRY_CUDA(cudaEventRecord(timing->permute0, s));
-    pf_route_kernel<<<1, 1024, 0, s>>>(ids, R, E, expert_subset, n_subset, d_slot_table, n_slots, ints, L.o_rows,
-                                       L.o_cexp, L.o_cslot, L.o_cpos, L.o_cn, p.status);
+    const int rblocks = (R + PF_RB - 1) / PF_RB;
+    MOE_TRY_CUDA(cudaMemsetAsync(ints + L.o_cnt, 0, MOE_MAX_E * sizeof(int32_t), s));
+    pf_count_kernel<<<rblocks, PF_RB, 0, s>>>(ids, R, E, expert_subset, n_subset, ints + L.o_cnt, p.status);
+    MOE_TRY_CUDA(cudaGetLastError());
+    pf_chunk_kernel<<<1, 1024, 0, s>>>(E, d_slot_table, n_slots, ints, L.o_cexp, L.o_cslot, L.o_cpos, L.o_cn, L.o_cnt,
+                                       L.o_cur, p.status);
+    MOE_TRY_CUDA(cudaGetLastError());
+    pf_place_kernel<<<rblocks, PF_RB, 0, s>>>(ids, R, E, expert_subset, n_subset, ints + L.o_cur, ints + L.o_rows);
     MOE_TRY_CUDA(cudaGetLastError());
     const int gblocks = (R + 7) / 8;
     const bool q4 = !q8;

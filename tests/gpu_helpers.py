@@ -4,7 +4,7 @@ import numpy as np
 import oracle
 from routed_expert_ffn_gemv_gb300 import synth
 
-# Spec tolerances: per-token max relative error (normwise, l-infinity) of layer
+# Output tolerances: per-token max relative error (normwise, l-infinity) of layer
 # outputs against the fp64 oracle; routes whose top-k margin is below GAP are excluded
 # from the bit-exact id comparison.
 TOL = 2e-3

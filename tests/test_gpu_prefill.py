@@ -3,7 +3,7 @@ operands) against the fp64 oracle.
 
 Shapes span several 128-row weight tiles, several token tiles per expert with ragged
 tails, both token-tile widths (64 and 128 rows), q8_0 and 4-bit weights, expert subsets
-and a slot table.  The spec check is on the MoE output per token (the routes
+and a slot table.  The 2e-3 check is on the MoE output per token (the routes
 combined): max relative error <= 2e-3.  Each route's partial output is also checked, against
 a bound derived from fp16 arithmetic: weights and the SwiGLU output are each rounded once
 to fp16 (unit roundoff 2^-11); with 4-bit blocks whose per-block minimum is drawn at random,

@@ -121,6 +121,49 @@ def test_prefill_subset_and_slot_table():
     _check(cfg, ids, w, x64, partial, True, subset=subset)
 
 
+def test_prefill_subset_many_routes_and_dropped_routes():
+    """Routing over several blocks of the count / place kernels with an expert subset and a
+    slot table, and routes with id -1 (dropped): excluded and dropped routes are not written,
+    every other route matches the oracle."""
+    cfg = synth.small_config(1, H=256, F=128, E=16, k=4, seed_cfg=862)
+    subset = [0, 3, 4, 7, 9, 10, 12, 15]
+    H, F, E, k, T = cfg.H, cfg.F, cfg.E, cfg.k, 400
+    order = list(range(E))[::-1]
+    pool, stride = _pool(cfg, order, True)
+    table = torch.tensor([E - 1 - e for e in range(E)], dtype=torch.int32, device="cuda")
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((T, H), dtype=np.float32)
+    xb = synth.f32_to_bf16_bits(x)
+    ids, w = random_routes(rng, T, E, k)
+    ids[rng.random((T, k)) < 0.1] = -1  # about a tenth of the routes dropped
+    ws_bytes = L.moe_expert_ffn_workspace(T, H, F, cfg.qtype, 1, E, k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    partial = torch.full((T, k, H), float("nan"), dtype=torch.float32, device="cuda")
+    sub = torch.tensor(subset, dtype=torch.int32, device="cuda")
+    L.moe_expert_ffn(torch.from_numpy(xb.view(np.int16)).cuda(), 1, T, H, F, cfg.qtype, E, k,
+                     torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), table, E, pool, stride,
+                     sub, len(subset), partial, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert L.moe_device_status(clear=True) == 0
+    p = partial.cpu().numpy()
+    x64 = oracle.x_to_double(xb, 1)
+    cache = {}
+    checked = 0
+    for t in range(0, T, 7):
+        for j in range(k):
+            e = int(ids[t, j])
+            if e < 0 or e not in subset:
+                assert np.all(np.isnan(p[t, j])), (t, j, e)
+                continue
+            if e not in cache:
+                cache[e] = synth.expert_weights(cfg, 0, e, True)
+            g, u, d = cache[e]
+            ref = float(w[t, j]) * oracle.expert_ffn(cfg.qtype, H, F, g, u, d, x64[t])
+            assert rel_err(p[t, j][None], ref[None])[0] <= ROUTE_TOL, (t, j, e)
+            checked += 1
+    assert checked > 50
+
+
 def test_prefill_invalid_slot_reported_others_computed():
     """An expert whose slot is out of range is reported (MOE_ERR_INVALID) and skipped; the
     other experts' routes are still computed."""

@@ -96,6 +96,10 @@ enum moe_xtype { MOE_F32 = 0, MOE_BF16 = 1 };
  * ids      device [T][k] int32 out;  weights device [T][k] fp32 out.
  * logits   device [T][E] fp32 out, or NULL.
  * Limits: 1 <= k <= min(E, MOE_MAX_K), E <= MOE_MAX_E, H % 32 == 0, T >= 0 (T == 0: no-op).
+ * Path: T <= MOE_DECODE_MAX_T one 8-CTA cluster per 32 tokens (fp32 FMAs); larger T with bf16
+ * x, E a multiple of 32 up to 128 and H a multiple of 64 on tensor cores (bf16 values in the
+ * normal fp16 range are exact in fp16, W_r is fp16: exact products, fp32 sums per 64 rows of
+ * H); otherwise a tiled fp32 kernel.
  */
 int moe_router_topk(const void *x, int xtype, int T, int H, const uint16_t *w_router,
                     const float *bias, int E, int k, int32_t *ids, float *weights,

@@ -254,8 +254,10 @@ def test_load_threshold_stack_layers_match_oracle():
     st.close()
 
 
-def test_cross_layer_prefetch_follows_simulator_and_keeps_values():
-    """Cross-layer speculative prefetch (page 3, sections 2.3 and 4.3, depth 2) on the
+@pytest.mark.parametrize("depth,admit", [(2, 1), (1, 1), (1, 2)])
+def test_cross_layer_prefetch_follows_simulator_and_keeps_values(depth, admit):
+    """Cross-layer speculative prefetch (page 3, sections 2.3 and 4.3, depth 1 or 2, with plain
+    LRU or frequency admission) on the
     Granite-shaped stack, device-managed pool, batch 8, layer by layer for 3 steps: outputs
     bit-identical to the plain device-managed stack; the pool bit-exact against the simulator
     fed each layer's real ids and the predicted ids of the next two layers (the next layers'
@@ -264,8 +266,8 @@ def test_cross_layer_prefetch_follows_simulator_and_keeps_values():
     cfg = synth.config(1)
     T = 8
     plain = _stack(cfg, max_T=T, device_managed=True)
-    pf = _stack(cfg, max_T=T, device_managed=True, images=plain.images, prefetch_depth=2)
-    sim = LRUSim(cfg.groups[0].n_slots)
+    pf = _stack(cfg, max_T=T, device_managed=True, images=plain.images, prefetch_depth=depth, admit_after=admit)
+    sim = LRUSim(cfg.groups[0].n_slots, admit_after=admit)
     xn = torch.empty((T, cfg.H), dtype=torch.float32, device=dev())
     pid = torch.empty((T, cfg.k), dtype=torch.int32, device=dev())
     pw = torch.empty((T, cfg.k), dtype=torch.float32, device=dev())
@@ -281,7 +283,7 @@ def test_cross_layer_prefetch_follows_simulator_and_keeps_values():
             assert torch.equal(ya, yb), (step, layer)
             sim.ensure(layer, ids.reshape(-1), n_tokens=T)
             L.moe_combine_rmsnorm(None, T, 0, cfg.H, h, None, xn)   # the stack's pre-norm of h
-            for dd in (1, 2):
+            for dd in range(1, depth + 1):
                 l2 = layer + dd
                 if l2 >= cfg.L:
                     break
@@ -305,7 +307,8 @@ def test_cross_layer_prefetch_follows_simulator_and_keeps_values():
     print(f"prefetch: {sim.pf_queries} predicted, {sim.pf_hits} already resident, {sim.pf_fills} copied, "
           f"{sim.pf_aborts} abandoned; real hits {sim.hits} of {sim.hits + sim.misses}")
     # the same steps as decode steps (eager first, then graph replay) from an empty pool
-    g = _stack(cfg, max_T=T, device_managed=True, use_graph=True, images=plain.images, prefetch_depth=2)
+    g = _stack(cfg, max_T=T, device_managed=True, use_graph=True, images=plain.images, prefetch_depth=depth,
+               admit_after=admit)
     y = torch.empty((T, cfg.H), dtype=torch.float32, device=dev())
     for step in range(3):
         g.decode(torch.from_numpy(synth.tokens_x(cfg, 800 + step, T)).to(dev()), y)

@@ -1183,10 +1183,16 @@ __global__ void combine_kernel(const float4 *__restrict__ partial, int T, int k,
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const size_t t = i / H4, h = i % H4;
         float4 s = extra ? extra[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            const float4 v = partial[(t * k + j) * H4 + h];
-            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
-        }
+        // every route's load issued first, then the sum in route order
+        float4 v[MOE_MAX_K];
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j)
+            if (j < k) v[j] = partial[(t * k + j) * H4 + h];
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j)
+            if (j < k) {
+                s.x += v[j].x; s.y += v[j].y; s.z += v[j].z; s.w += v[j].w;
+            }
         y[i] = s;
     }
 }
@@ -1206,11 +1212,20 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(const float4 *__restr
     int n = 0;
     for (int h = threadIdx.x; h < H4; h += blockDim.x, ++n) {
         float4 s = extra ? extra[(size_t)t * H4 + h] : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            if (ids && ids[(size_t)t * k + j] < 0) continue;  // a dropped route (load threshold)
-            const float4 v = partial[((size_t)t * k + j) * H4 + h];
-            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+        // every route's load issued first, then the sum in route order (a dropped route, id -1
+        // under a load threshold, is skipped)
+        float4 v[MOE_MAX_K];
+        bool use[MOE_MAX_K];
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j) {
+            use[j] = j < k && !(ids && ids[(size_t)t * k + j] < 0);
+            if (use[j]) v[j] = partial[((size_t)t * k + j) * H4 + h];
         }
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_K; ++j)
+            if (use[j]) {
+                s.x += v[j].x; s.y += v[j].y; s.z += v[j].z; s.w += v[j].w;
+            }
         if (y) y[(size_t)t * H4 + h] = s;
         ss += s.x * s.x + s.y * s.y + s.z * s.z + s.w * s.w;
 #pragma unroll

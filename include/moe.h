@@ -203,7 +203,8 @@ typedef struct {
     uint64_t prefetch_queries;/* speculative requests (moe_cache_prefetch_plan): distinct experts */
     uint64_t prefetch_hits;   /*   already resident */
     uint64_t prefetch_fills;  /*   given a slot and copied by moe_cache_prefetch_fill */
-    uint64_t prefetch_aborts; /*   requests abandoned (they would evict a slot in use) */
+    uint64_t prefetch_aborts; /*   requests abandoned (more slots than the pool has, or a victim
+                                    that the last real request uses) */
 } moe_cache_stats;
 
 /*
@@ -250,8 +251,9 @@ int moe_cache_ensure(moe_cache *c, int layer, const int32_t *ids_host, int n_tok
  *                  host image (the slot it was given must be filled from there), else 0.
  * It moves no weight bytes: moe_expert_ffn_fill reads the missed experts from host memory
  * and writes them into their slots while computing (an expert bypassed by the admission
- * policy gets table -1 and its image address: read from host memory, written nowhere).  Capacity overflow or an id out of
- * range is recorded in the device status word (moe_device_status); the layer's table is
+ * policy gets table -1 and its image address: read from host memory, written nowhere).
+ * Capacity overflow or an id out of range is recorded in the device status word
+ * (moe_device_status); the layer's table is
  * then all -1 and nothing is read.  Host-side ensure/wait/release are invalid on a
  * device-managed pool; moe_cache_stats_get, moe_cache_lookup and moe_cache_reset work on
  * both kinds (synchronously for this one).

@@ -78,6 +78,7 @@
 static_assert(PF_ACOL + PF_AS * 32 <= PF_TMEM_COLS, "TMEM budget");
 static_assert(PF_S % 2 == 0, "each ring stage keeps one producer; stage pairs never wrap");
 static_assert(PF_AS % 2 == 0 && PF_BK == 64, "TMEM slot pairs");
+static_assert(PF_S > PF_AS, "a slot's release follows the previous fill of the stage that reuses it");
 static_assert(PF_NT % 16 == 0 && PF_NT <= 256, "MMA N");
 
 namespace {
@@ -636,18 +637,23 @@ __global__ void __launch_bounds__(PF_THREADS, 1) pf_gemm_kernel(const __grid_con
                 const int s = g % PF_S;
                 bool w = true;
                 if (lane == 0) {
-                    w = pf_wait(&s_full[s], (g / PF_S) & 1, p.status, abort_flag);
-                    // the TMEM slot is free once the MMAs of stage g - PF_AS (its previous use) have
-                    // completed: that stage's ring release
-                    if (w && g >= PF_AS)
+                    // The TMEM slot is free once the MMAs of stage g - PF_AS (its previous use) have
+                    // completed: that stage's ring release.  It is waited for first: a group sees
+                    // only every other fill of a ring stage (stage g - PF_S belongs to another
+                    // group), and a parity test cannot tell the fill of stage g from that earlier
+                    // one while the earlier one is still landing.  The release of g - PF_AS comes
+                    // after the MMA issuer saw the fill of g - PF_S, so after it the parity of
+                    // s_full[s] can only mean stage g.
+                    if (g >= PF_AS)
                         w = pf_wait(&s_empty[(g - PF_AS) % PF_S], ((g - PF_AS) / PF_S) & 1, p.status, abort_flag);
+                    if (w) w = pf_wait(&s_full[s], (g / PF_S) & 1, p.status, abort_flag);
                 }
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (!(ok = w)) break;  // the warp leaves together
                 // every lane observes both completed phases itself (one test each), so that each
                 // lane's reads of the stage and writes of the slot are ordered after them
-                mbar_test_wait(&s_full[s], (g / PF_S) & 1);
                 if (g >= PF_AS) mbar_test_wait(&s_empty[(g - PF_AS) % PF_S], ((g - PF_AS) / PF_S) & 1);
+                mbar_test_wait(&s_full[s], (g / PF_S) & 1);
                 tc_fence_after();
                 uint32_t o[32];
                 const uint8_t *raw = ring + (size_t)s * PG::STAGE + PG::TOKB;

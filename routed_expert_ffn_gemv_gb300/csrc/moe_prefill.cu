@@ -812,15 +812,19 @@ int encode_rows_map(const __half *base, int rows, int K, int box_rows, CUtensorM
     return MOE_OK;
 }
 
+// SM count of the current device, looked up once per device.
 int sm_count_cached() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 1;
+    static std::mutex mu;
+    static int n[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!n[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+        n[dev] = v;
     }
-    return n;
+    return n[dev];
 }
 
 // The GEMMs' dynamic shared-memory limit, raised once per device.
